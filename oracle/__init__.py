@@ -1,0 +1,179 @@
+"""fp64 CPU oracle for Kimi Delta Attention (KDA) — TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never does, and the two
+share no code; the only thing both sides take is the seeded input generator
+``kda_synth``.
+
+The arithmetic lives in ``kda_oracle.c`` (plain C99, fp64, one thread per
+(sequence, head) chain), compiled with gcc into ``_oracle.so`` next to it:
+
+* :func:`kda_tokenloop` — the recurrence one token at a time, the definition of
+  the result ("Kimi-K3 深度解析", section 三, "KDA 的关键改进").
+* :func:`kda_chunked` — the same result chunk by chunk (the ``chunk_kda`` form named
+  in "Kimi K3 架构全景", section 02), checked against the token loop.
+* :func:`shortconv_silu_l2norm` — ShortConv(kernel 4) + SiLU on q, k, v and the L2
+  norm of q and k ("深入 Kimi-K3: Hugging Face 仓库分析", paragraph on KDA).
+* :func:`output_gate` — o * sigmoid(gate), the full-rank output gate (same paragraph).
+* :func:`recurrent_step` — one decode step: the front end on one token per
+  sequence followed by one step of the token loop (``fused_recurrent_kda``).
+
+All arrays are fp64 numpy arrays in the layouts of ``kda_oracle.c``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kda_oracle.c")
+_LIB = os.path.join(_HERE, "_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (portable C99, -O2, no fast-math)."""
+    with _lock:
+        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+            tmp = _LIB + f".{os.getpid()}.tmp"
+            subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-pthread",
+                                   "-ffp-contract=off", "-o", tmp, _SRC, "-lm"])
+            os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P, I, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_double
+        lib.oracle_kda_tokenloop.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, D, P, P, ctypes.c_int]
+        lib.oracle_kda_chunked.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, D, I, P, P, ctypes.c_int]
+        lib.oracle_shortconv_silu_l2norm.argtypes = [P, P, P, I, P, P, I, I, I, I, P, D, P, P, P, P,
+                                                     ctypes.c_int]
+        for f in (lib.oracle_kda_tokenloop, lib.oracle_kda_chunked, lib.oracle_shortconv_silu_l2norm):
+            f.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def threads() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def _f64(a):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    return a
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _cu(cu_seqlens, T):
+    if cu_seqlens is None:
+        return None, 1
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int64)
+    assert cu[0] == 0 and cu[-1] == T
+    return cu, len(cu) - 1
+
+
+def _kda(fn, q, k, v, g, beta, init_state, cu_seqlens, scale, chunk, nthreads):
+    q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    assert k.shape == (T, H, dk) and g.shape == (T, H, dk) and v.shape == (T, H, dv)
+    assert beta.shape == (T, H)
+    cu, N = _cu(cu_seqlens, T)
+    s0 = _f64(init_state)
+    if s0 is not None:
+        assert s0.shape == (N, H, dv, dk)
+    o = np.empty((T, H, dv), np.float64)
+    fs = np.empty((N, H, dv, dk), np.float64)
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(s0), _ptr(cu), N, T, H, dk, dv, float(scale)]
+    if chunk is not None:
+        args.append(int(chunk))
+    args += [_ptr(o), _ptr(fs), nthreads or threads()]
+    if fn(*args) != 0:
+        raise ValueError("oracle rejected its arguments")
+    return o, fs
+
+
+def kda_tokenloop(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale=1.0, nthreads=None):
+    """(o [T,H,dv], final_state [N,H,dv,dk]) by the per-token recurrence."""
+    return _kda(_load().oracle_kda_tokenloop, q, k, v, g, beta, init_state, cu_seqlens, scale, None, nthreads)
+
+
+def kda_chunked(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale=1.0, chunk=64, nthreads=None):
+    """The same pair computed chunk by chunk (unit-triangular solve per chunk)."""
+    return _kda(_load().oracle_kda_chunked, q, k, v, g, beta, init_state, cu_seqlens, scale, chunk, nthreads)
+
+
+def shortconv_silu_l2norm(xq, xk, xv, conv_w, H, d, cu_seqlens=None, conv_state_in=None, eps=1e-6,
+                          want_state=True, nthreads=None):
+    """Front end.  x*: [T, >=H*d] raw rows; conv_w: [3*H*d, 4] (q|k|v channel blocks,
+    taps oldest..current); conv_state_in: [N, 3, 3*H*d] or None (zeros).
+    Returns q, k, v [T, H, d] and the carried state [N, 3, 3*H*d] (or None)."""
+    xq, xk, xv, w = (_f64(x) for x in (xq, xk, xv, conv_w))
+    T, ld = xq.shape
+    assert xk.shape == (T, ld) and xv.shape == (T, ld) and w.shape == (3 * H * d, 4)
+    cu, N = _cu(cu_seqlens, T)
+    cs = _f64(conv_state_in)
+    if cs is not None:
+        assert cs.shape == (N, 3, 3 * H * d)
+    q = np.empty((T, H, d)); k = np.empty((T, H, d)); v = np.empty((T, H, d))
+    cs_out = np.empty((N, 3, 3 * H * d)) if want_state else None
+    rc = _load().oracle_shortconv_silu_l2norm(_ptr(xq), _ptr(xk), _ptr(xv), ld, _ptr(w), _ptr(cu), N, T, H, d,
+                                              _ptr(cs), float(eps), _ptr(q), _ptr(k), _ptr(v), _ptr(cs_out),
+                                              nthreads or threads())
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return q, k, v, cs_out
+
+
+def output_gate(o, gate):
+    """o * sigmoid(gate); o [T, H, dv], gate [T, H*dv]."""
+    o = np.asarray(o, np.float64)
+    gt = np.asarray(gate, np.float64).reshape(o.shape)
+    return o * (1.0 / (1.0 + np.exp(-gt)))
+
+
+def recurrent_step(xq, xk, xv, conv_w, g, beta, state, conv_state, H, d, scale=1.0, eps=1e-6, nthreads=None):
+    """One decode step for N sequences of one token each.
+
+    x*: [N, H*d] raw; g: [N, H, d]; beta: [N, H]; state [N, H, d, d]; conv_state [N, 3, 3*H*d].
+    Returns (o [N, H, d], new state, new conv_state)."""
+    N = np.asarray(xq).shape[0]
+    cu = np.arange(N + 1, dtype=np.int64)
+    q, k, v, cs = shortconv_silu_l2norm(xq, xk, xv, conv_w, H, d, cu, conv_state, eps, True, nthreads)
+    o, s = kda_tokenloop(q, k, v, g, beta, state, cu, scale, nthreads)
+    return o, s, cs
+
+
+def state_numel(layers: int, H: int, dk: int, dv: int) -> int:
+    """Values of recurrent state one sequence holds across ``layers`` KDA layers."""
+    return int(layers) * int(H) * int(dv) * int(dk)
+
+
+def rel_l2(x, ref) -> float:
+    """||x - ref||_2 / ||ref||_2 over the whole tensor, accumulated in fp64."""
+    x = np.asarray(x, np.float64).ravel(); ref = np.asarray(ref, np.float64).ravel()
+    den = float(np.sqrt(np.dot(ref, ref)))
+    num = float(np.sqrt(np.dot(x - ref, x - ref)))
+    return num / den if den > 0 else num
+
+
+def max_abs(x, ref) -> float:
+    x = np.asarray(x, np.float64); ref = np.asarray(ref, np.float64)
+    return float(np.max(np.abs(x - ref))) if x.size else 0.0

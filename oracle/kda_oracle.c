@@ -1,0 +1,352 @@
+/*
+ * fp64 CPU oracle for Kimi Delta Attention (KDA).
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's CPU
+ * baseline use this file; the CUDA library never links, loads or calls it, and
+ * it shares no code with it.  It is plain, slow and meant to be read against
+ * the pages:
+ *
+ *  - "Kimi-K3 深度解析: 2.8T 开源 MoE 模型的架构创新与设计哲学", section 三
+ *    (Kimi Delta Attention), subsection "KDA 的关键改进": the decayed state
+ *    S~_t = S_{t-1} Diag(alpha_t) and the corrected update S_t = S~_t + e_t k_t^T
+ *    with e_t = beta_t (v_t - v^_t), v^_t predicted from the current state.
+ *  - "Kimi K3 架构全景", section 02 (KDA column): ShortConv kernel 4, gate with
+ *    lower bound -5.0, operators chunk_kda / fused_recurrent_kda, 96 heads x 128.
+ *  - "深入 Kimi-K3: Hugging Face 仓库分析", paragraph on KDA: q, k, v each pass a
+ *    short convolution with SiLU; q and k are L2-normalised inside the kernel;
+ *    the per-channel decay has a lower bound of -5; the output gate is full rank.
+ *
+ * Readings where the pages leave a step open (each is listed with its reason in
+ * the design notes): alpha_t = exp(g_t) per key channel; beta_t a scalar per
+ * token and head; v^_t = S~_t k_t (prediction from the decayed state); the
+ * output o_t = scale * S_t q_t reads the state after the update; S is dv x dk,
+ * stored row-major; ShortConv is depthwise, causal, without bias, tap 3 is the
+ * current token and positions before a sequence start read the carried
+ * convolution state (or zero); L2 norm is x / sqrt(sum x^2 + eps).
+ *
+ * Layouts: q, k, g [T_total, H, dk]; v, o [T_total, H, dv]; beta [T_total, H];
+ * states [N, H, dv, dk]; cu_seqlens [N + 1] (NULL = one sequence of T_total).
+ * Every function returns 0, or -1 for an argument it cannot accept.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------------------------------- */
+/* a tiny work queue over independent (sequence, head) chains                               */
+/* ---------------------------------------------------------------------------------------- */
+
+typedef void (*chain_fn)(void* ctx, int64_t item, double* scratch);
+
+typedef struct {
+    chain_fn fn;
+    void* ctx;
+    int64_t n_items;
+    size_t scratch_doubles;
+    int64_t next;
+    int failed;
+    pthread_mutex_t mu;
+} queue_t;
+
+static void* queue_worker(void* arg) {
+    queue_t* qu = (queue_t*)arg;
+    double* scratch = (double*)malloc(qu->scratch_doubles * sizeof(double) + 64);
+    if (!scratch) {
+        pthread_mutex_lock(&qu->mu);
+        qu->failed = 1;
+        pthread_mutex_unlock(&qu->mu);
+        return NULL;
+    }
+    for (;;) {
+        pthread_mutex_lock(&qu->mu);
+        int64_t it = qu->next++;
+        pthread_mutex_unlock(&qu->mu);
+        if (it >= qu->n_items) break;
+        qu->fn(qu->ctx, it, scratch);
+    }
+    free(scratch);
+    return NULL;
+}
+
+static int run_queue(chain_fn fn, void* ctx, int64_t n_items, size_t scratch_doubles, int nthreads) {
+    queue_t qu;
+    qu.fn = fn;
+    qu.ctx = ctx;
+    qu.n_items = n_items;
+    qu.scratch_doubles = scratch_doubles;
+    qu.next = 0;
+    qu.failed = 0;
+    pthread_mutex_init(&qu.mu, NULL);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 512) nthreads = 512;
+    if ((int64_t)nthreads > n_items) nthreads = n_items > 0 ? (int)n_items : 1;
+    pthread_t th[512];
+    int ok[512];
+    for (int t = 0; t < nthreads; ++t) ok[t] = pthread_create(&th[t], NULL, queue_worker, &qu) == 0;
+    int any = 0;
+    for (int t = 0; t < nthreads; ++t) any |= ok[t];
+    if (!any) queue_worker(&qu);
+    for (int t = 0; t < nthreads; ++t)
+        if (ok[t]) pthread_join(th[t], NULL);
+    pthread_mutex_destroy(&qu.mu);
+    return qu.failed ? -1 : 0;
+}
+
+static int check_seqlens(const int64_t* cu, int64_t N, int64_t T_total) {
+    if (N < 1) return -1;
+    if (!cu) return N == 1 ? 0 : -1;
+    if (cu[0] != 0 || cu[N] != T_total) return -1;
+    for (int64_t n = 0; n < N; ++n)
+        if (cu[n + 1] < cu[n]) return -1;
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------------------- */
+/* O1: the recurrence, one token at a time                                                  */
+/* ---------------------------------------------------------------------------------------- */
+
+typedef struct {
+    const double *q, *k, *v, *g, *beta, *init_state;
+    const int64_t* cu;
+    int64_t N, T, H, dk, dv, chunk;
+    double scale;
+    double *o, *final_state;
+} kda_ctx;
+
+static void seq_range(const kda_ctx* c, int64_t n, int64_t* bos, int64_t* eos) {
+    *bos = c->cu ? c->cu[n] : 0;
+    *eos = c->cu ? c->cu[n + 1] : c->T;
+}
+
+/*
+ * Per token t of sequence n, head h (section 三, "KDA 的关键改进"):
+ *   alpha      = exp(g_t)                      per key channel j
+ *   S~[i][j]   = S[i][j] * alpha[j]            S~ = S Diag(alpha)
+ *   p[i]       = sum_j S~[i][j] k_t[j]         v^_t = S~ k_t
+ *   e[i]       = beta_t (v_t[i] - p[i])
+ *   S[i][j]    = S~[i][j] + e[i] k_t[j]        S = S~ + e k_t^T
+ *   o_t[i]     = scale * sum_j S[i][j] q_t[j]  o_t = scale S_t q_t
+ */
+static void tokenloop_chain(void* vctx, int64_t item, double* S) {
+    const kda_ctx* c = (const kda_ctx*)vctx;
+    const int64_t n = item / c->H, h = item % c->H, dk = c->dk, dv = c->dv, H = c->H;
+    double* alpha = S + dv * dk;
+    double* e = alpha + dk;
+    int64_t bos, eos;
+    seq_range(c, n, &bos, &eos);
+    if (c->init_state) memcpy(S, c->init_state + (n * H + h) * dv * dk, sizeof(double) * dv * dk);
+    else memset(S, 0, sizeof(double) * dv * dk);
+    for (int64_t t = bos; t < eos; ++t) {
+        const double* kt = c->k + (t * H + h) * dk;
+        const double* qt = c->q + (t * H + h) * dk;
+        const double* vt = c->v + (t * H + h) * dv;
+        const double* gt = c->g + (t * H + h) * dk;
+        const double bt = c->beta[t * H + h];
+        for (int64_t j = 0; j < dk; ++j) alpha[j] = exp(gt[j]);
+        for (int64_t i = 0; i < dv; ++i)
+            for (int64_t j = 0; j < dk; ++j) S[i * dk + j] *= alpha[j];
+        for (int64_t i = 0; i < dv; ++i) {
+            double p = 0.0;
+            for (int64_t j = 0; j < dk; ++j) p += S[i * dk + j] * kt[j];
+            e[i] = bt * (vt[i] - p);
+        }
+        for (int64_t i = 0; i < dv; ++i)
+            for (int64_t j = 0; j < dk; ++j) S[i * dk + j] += e[i] * kt[j];
+        double* ot = c->o + (t * H + h) * dv;
+        for (int64_t i = 0; i < dv; ++i) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < dk; ++j) acc += S[i * dk + j] * qt[j];
+            ot[i] = c->scale * acc;
+        }
+    }
+    if (c->final_state) memcpy(c->final_state + (n * H + h) * dv * dk, S, sizeof(double) * dv * dk);
+}
+
+int oracle_kda_tokenloop(const double* q, const double* k, const double* v, const double* g,
+                         const double* beta, const double* init_state, const int64_t* cu_seqlens,
+                         int64_t N, int64_t T_total, int64_t H, int64_t dk, int64_t dv, double scale,
+                         double* o, double* final_state, int nthreads) {
+    if (!q || !k || !v || !g || !beta || !o || H < 1 || dk < 1 || dv < 1 || T_total < 0) return -1;
+    if (check_seqlens(cu_seqlens, N, T_total)) return -1;
+    kda_ctx c = {q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, dk, dv, 0, scale, o, final_state};
+    return run_queue(tokenloop_chain, &c, N * H, (size_t)(dv * dk + dk + dv), nthreads);
+}
+
+/* ---------------------------------------------------------------------------------------- */
+/* O2: the same result, chunk by chunk (the chunk_kda form), as a check of the algebra       */
+/* ---------------------------------------------------------------------------------------- */
+
+/*
+ * Unrolling the recurrence inside a chunk that starts from state S0, with
+ * G_t = sum_{tau <= t} g_tau (cumulated inside the chunk, per key channel):
+ *   S_t = S0 Diag(e^{G_t}) + sum_{j <= t} u_j (k_j . e^{G_t - G_j})^T
+ * where the corrections u_j = beta_j (v_j - S~_j k_j) satisfy
+ *   u_i + beta_i sum_{j < i} A[i][j] u_j = beta_i (v_i - S0 (k_i . e^{G_i})),
+ *   A[i][j] = sum_c k_ic k_jc e^{G_ic - G_jc},
+ * a unit lower-triangular system solved here by forward substitution, and
+ *   o_i   = scale (S0 (q_i . e^{G_i}) + sum_{j <= i} B[i][j] u_j),
+ *   B[i][j] = sum_c q_ic k_jc e^{G_ic - G_jc},
+ *   S_end = S0 Diag(e^{G_L}) + sum_j u_j (k_j . e^{G_L - G_j})^T.
+ * In fp64 every exponent here is <= 0, so no reference point is needed.
+ */
+static void chunked_chain(void* vctx, int64_t item, double* S) {
+    const kda_ctx* c = (const kda_ctx*)vctx;
+    const int64_t n = item / c->H, h = item % c->H, dk = c->dk, dv = c->dv, H = c->H, C = c->chunk;
+    double* G = S + dv * dk;      /* [C][dk] */
+    double* U = G + C * dk;       /* [C][dv] */
+    double* x = U + C * dv;       /* [dk]    */
+    double* Snew = x + dk;        /* [dv][dk] */
+    int64_t bos, eos;
+    seq_range(c, n, &bos, &eos);
+    if (c->init_state) memcpy(S, c->init_state + (n * H + h) * dv * dk, sizeof(double) * dv * dk);
+    else memset(S, 0, sizeof(double) * dv * dk);
+    for (int64_t c0 = bos; c0 < eos; c0 += C) {
+        const int64_t L = (eos - c0) < C ? (eos - c0) : C;
+#define KP(t) (c->k + ((c0 + (t)) * H + h) * dk)
+#define QP(t) (c->q + ((c0 + (t)) * H + h) * dk)
+#define VP(t) (c->v + ((c0 + (t)) * H + h) * dv)
+#define GP(t) (c->g + ((c0 + (t)) * H + h) * dk)
+        for (int64_t t = 0; t < L; ++t)
+            for (int64_t j = 0; j < dk; ++j) G[t * dk + j] = GP(t)[j] + (t ? G[(t - 1) * dk + j] : 0.0);
+        for (int64_t i = 0; i < L; ++i) {
+            const double bi = c->beta[(c0 + i) * H + h];
+            for (int64_t j = 0; j < dk; ++j) x[j] = KP(i)[j] * exp(G[i * dk + j]);
+            for (int64_t r = 0; r < dv; ++r) {
+                double s = 0.0;
+                for (int64_t j = 0; j < dk; ++j) s += S[r * dk + j] * x[j];
+                U[i * dv + r] = bi * (VP(i)[r] - s);
+            }
+            for (int64_t j = 0; j < i; ++j) {
+                double a = 0.0;
+                for (int64_t cc = 0; cc < dk; ++cc)
+                    a += KP(i)[cc] * KP(j)[cc] * exp(G[i * dk + cc] - G[j * dk + cc]);
+                for (int64_t r = 0; r < dv; ++r) U[i * dv + r] -= bi * a * U[j * dv + r];
+            }
+        }
+        for (int64_t i = 0; i < L; ++i) {
+            double* oi = c->o + ((c0 + i) * H + h) * dv;
+            for (int64_t j = 0; j < dk; ++j) x[j] = QP(i)[j] * exp(G[i * dk + j]);
+            for (int64_t r = 0; r < dv; ++r) {
+                double s = 0.0;
+                for (int64_t j = 0; j < dk; ++j) s += S[r * dk + j] * x[j];
+                oi[r] = s;
+            }
+            for (int64_t j = 0; j <= i; ++j) {
+                double b = 0.0;
+                for (int64_t cc = 0; cc < dk; ++cc)
+                    b += QP(i)[cc] * KP(j)[cc] * exp(G[i * dk + cc] - G[j * dk + cc]);
+                for (int64_t r = 0; r < dv; ++r) oi[r] += b * U[j * dv + r];
+            }
+            for (int64_t r = 0; r < dv; ++r) oi[r] *= c->scale;
+        }
+        const double* GL = G + (L - 1) * dk;
+        for (int64_t r = 0; r < dv; ++r)
+            for (int64_t j = 0; j < dk; ++j) Snew[r * dk + j] = S[r * dk + j] * exp(GL[j]);
+        for (int64_t t = 0; t < L; ++t) {
+            for (int64_t j = 0; j < dk; ++j) x[j] = KP(t)[j] * exp(GL[j] - G[t * dk + j]);
+            for (int64_t r = 0; r < dv; ++r)
+                for (int64_t j = 0; j < dk; ++j) Snew[r * dk + j] += U[t * dv + r] * x[j];
+        }
+        memcpy(S, Snew, sizeof(double) * dv * dk);
+#undef KP
+#undef QP
+#undef VP
+#undef GP
+    }
+    if (c->final_state) memcpy(c->final_state + (n * H + h) * dv * dk, S, sizeof(double) * dv * dk);
+}
+
+int oracle_kda_chunked(const double* q, const double* k, const double* v, const double* g,
+                       const double* beta, const double* init_state, const int64_t* cu_seqlens,
+                       int64_t N, int64_t T_total, int64_t H, int64_t dk, int64_t dv, double scale,
+                       int64_t chunk, double* o, double* final_state, int nthreads) {
+    if (!q || !k || !v || !g || !beta || !o || H < 1 || dk < 1 || dv < 1 || T_total < 0 || chunk < 1)
+        return -1;
+    if (check_seqlens(cu_seqlens, N, T_total)) return -1;
+    kda_ctx c = {q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, dk, dv, chunk, scale, o, final_state};
+    size_t scratch = (size_t)(2 * dv * dk + chunk * dk + chunk * dv + dk);
+    return run_queue(chunked_chain, &c, N * H, scratch, nthreads);
+}
+
+/* ---------------------------------------------------------------------------------------- */
+/* F: ShortConv(4) + SiLU on q, k, v; L2 norm of q and k per head                           */
+/* ---------------------------------------------------------------------------------------- */
+
+typedef struct {
+    const double *xq, *xk, *xv, *w, *cs_in;
+    int64_t x_ld;
+    const int64_t* cu;
+    int64_t N, T, H, d;
+    double eps;
+    double *q, *k, *v, *cs_out;
+} fe_ctx;
+
+/*
+ * Raw input of part p (0 = q, 1 = k, 2 = v), channel ch (0 <= ch < H*d), at
+ * absolute position s of sequence n: positions before the sequence start come
+ * from the carried convolution state (oldest row first), or are zero.
+ */
+static double fe_raw(const fe_ctx* c, int p, int64_t n, int64_t bos, int64_t s, int64_t ch) {
+    const int64_t C = c->H * c->d;
+    if (s >= bos) {
+        const double* x = p == 0 ? c->xq : (p == 1 ? c->xk : c->xv);
+        return x[s * c->x_ld + ch];
+    }
+    int64_t back = bos - s; /* 1, 2 or 3 positions before the start */
+    if (!c->cs_in || back > 3) return 0.0;
+    return c->cs_in[(n * 3 + (3 - back)) * 3 * C + p * C + ch];
+}
+
+/*
+ * One (sequence, head): for each position, part and channel
+ *   y = sum_{i=0..3} w[ch][i] x_{t-3+i}   (tap 3 = current token)
+ *   a = y / (1 + e^{-y})                   (SiLU)
+ * then q and k are divided by sqrt(sum over the head's d channels of a^2 + eps).
+ */
+static void frontend_chain(void* vctx, int64_t item, double* a) {
+    const fe_ctx* c = (const fe_ctx*)vctx;
+    const int64_t n = item / c->H, h = item % c->H, d = c->d, H = c->H, C = H * d;
+    int64_t bos = c->cu ? c->cu[n] : 0, eos = c->cu ? c->cu[n + 1] : c->T;
+    for (int64_t t = bos; t < eos; ++t) {
+        for (int p = 0; p < 3; ++p) {
+            double ss = 0.0;
+            for (int64_t j = 0; j < d; ++j) {
+                const int64_t ch = h * d + j;
+                const double* wr = c->w + (p * C + ch) * 4;
+                double y = 0.0;
+                for (int i = 0; i < 4; ++i) y += wr[i] * fe_raw(c, p, n, bos, t - 3 + i, ch);
+                a[j] = y / (1.0 + exp(-y));
+                ss += a[j] * a[j];
+            }
+            double* out = p == 0 ? c->q : (p == 1 ? c->k : c->v);
+            double inv = p == 2 ? 1.0 : 1.0 / sqrt(ss + c->eps);
+            for (int64_t j = 0; j < d; ++j) out[(t * H + h) * d + j] = a[j] * inv;
+        }
+    }
+    if (c->cs_out) {
+        /* the last three raw inputs of the sequence, oldest first */
+        for (int r = 0; r < 3; ++r)
+            for (int p = 0; p < 3; ++p)
+                for (int64_t j = 0; j < d; ++j) {
+                    const int64_t ch = h * d + j;
+                    a[(r * 3 + p) * d + j] = fe_raw(c, p, n, bos, eos - 3 + r, ch);
+                }
+        for (int r = 0; r < 3; ++r)
+            for (int p = 0; p < 3; ++p)
+                for (int64_t j = 0; j < d; ++j)
+                    c->cs_out[(n * 3 + r) * 3 * C + p * C + h * d + j] = a[(r * 3 + p) * d + j];
+    }
+}
+
+int oracle_shortconv_silu_l2norm(const double* xq, const double* xk, const double* xv, int64_t x_ld,
+                                 const double* w, const int64_t* cu_seqlens, int64_t N, int64_t T_total,
+                                 int64_t H, int64_t d, const double* conv_state_in, double eps,
+                                 double* q, double* k, double* v, double* conv_state_out, int nthreads) {
+    if (!xq || !xk || !xv || !w || !q || !k || !v || H < 1 || d < 1 || T_total < 0 || x_ld < H * d) return -1;
+    if (check_seqlens(cu_seqlens, N, T_total)) return -1;
+    if (conv_state_out && conv_state_out == conv_state_in) return -1; /* the oracle wants separate buffers */
+    fe_ctx c = {xq, xk, xv, w, conv_state_in, x_ld, cu_seqlens, N, T_total, H, d, eps, q, k, v, conv_state_out};
+    return run_queue(frontend_chain, &c, N * H, (size_t)(9 * d), nthreads);
+}
