@@ -1,0 +1,423 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA hot path on GB300.
+
+One step = one chunkwise prefill (kda_chunk_fwd) of the 8K-token workload:
+1 sequence x 8192 tokens x 96 heads x d 128, bf16 q/k/v (q, k L2-normalised),
+fp32 g = -5 sigmoid(z) and beta = sigmoid(z), zero initial state; output o
+(bf16) and the final fp32 state.  ``value`` is prefill tokens/s (whole job:
+sum over ranks).  The same JSON line carries the decode half of the metric:
+one fused kda_recurrent_step of 64 sequences x 96 heads, in place on the
+403 MB fp32 state, as state GB/s.
+
+Inputs are synthetic (seeded counter-based generator, kda_synth) and larger
+than the 129 MB L2 (1.2 GB per prefill step, 0.84 GB per decode step), so L2 is
+not flushed between iterations.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica (the path shards by
+sequence and head with no exchange); rank 0 prints one JSON line.
+``--impl reference`` times the fp64 CPU oracle on a bounded sample of the same
+workload on this host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s (H=96,d=128) + decode state GB/s, % of roofline"
+
+# prefill: algorithmic bytes per token-head = q, k, v bf16 (3 x 256) + g fp32 (512) + beta (4) + o bf16 (256)
+PREFILL_BYTES_PER_TOKEN_HEAD = 3 * 256 + 512 + 4 + 256
+# algorithmic flops per token-head at chunk 64: 3 state products (6 d^2) + triangular intra-chunk
+# products (~5 C d) + UT solve (~C^2 / 3)
+PREFILL_FLOPS_PER_TOKEN_HEAD = 6 * 128 * 128 + 5 * 64 * 128 + (64 * 64) // 3
+
+
+def prefill_bytes(T, H, N, d=128, init_state=False):
+    b = T * H * PREFILL_BYTES_PER_TOKEN_HEAD + N * H * d * d * 4   # + final state out
+    if init_state:
+        b += N * H * d * d * 4
+    return b
+
+
+def decode_bytes(N, H, d=128):
+    C = H * d
+    state = 2 * N * H * d * d * 4              # fp32 state read + written
+    conv_state = 2 * N * 3 * 3 * C * 2         # bf16 conv state read + written
+    x = 3 * N * C * 2                          # raw q, k, v
+    g = N * H * d * 4
+    o = N * H * d * 2
+    w = 3 * C * 4 * 2
+    beta = N * H * 4
+    return state + conv_state + x + g + o + w + beta
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def smi_index(local_rank: int) -> str:
+    """nvidia-smi's name for this process's GPU (CUDA_VISIBLE_DEVICES entries are indices or UUIDs)."""
+    cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "").strip()
+    if cvd:
+        entries = [e.strip() for e in cvd.split(",") if e.strip()]
+        if local_rank < len(entries):
+            return entries[local_rank]
+    return str(local_rank)
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(self.gpu_index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------------
+# our arm
+# ------------------------------------------------------------------------------------------------
+
+def make_prefill_inputs(w, device):
+    import kda_synth as ks
+    from kda_synth.device import fill_device
+    T, H, d = w.T, w.H, w.d
+    q = fill_device(w.seed, ks.TID_Q, ks.UNIT_GROUPS, (T, H, d), "bf16", 0.0, float(d), device=device)
+    k = fill_device(w.seed, ks.TID_K, ks.UNIT_GROUPS, (T, H, d), "bf16", 0.0, float(d), device=device)
+    v = fill_device(w.seed, ks.TID_V, ks.NORMAL, (T, H, d), "bf16", device=device)
+    g = fill_device(w.seed, ks.TID_G, w.g_kind, (T, H, d), "f32", device=device)
+    b = fill_device(w.seed, ks.TID_BETA, ks.SIGMOID, (T, H), "f32", device=device)
+    return q, k, v, g, b
+
+
+def make_decode_inputs(w, device):
+    import kda_synth as ks
+    from kda_synth.device import fill_device
+    N, H, d = w.N, w.H, w.d
+    C = H * d
+    xs = [fill_device(w.seed, t, ks.NORMAL, (N, C), "bf16", device=device) for t in (ks.TID_Q, ks.TID_K, ks.TID_V)]
+    cw = fill_device(w.seed, ks.TID_CONV_W, ks.NORMAL, (3 * C, 4), "bf16", 0.0, w.conv_w_std, device=device)
+    g = fill_device(w.seed, ks.TID_G, w.g_kind, (N, H, d), "f32", device=device)
+    b = fill_device(w.seed, ks.TID_BETA, ks.SIGMOID, (N, H), "f32", device=device)
+    st = fill_device(w.seed, ks.TID_STATE, ks.NORMAL, (N, H, d, d), "f32", 0.0, w.init_state_std, device=device)
+    cs = fill_device(w.seed, ks.TID_CONV_STATE, ks.NORMAL, (N, 3, 3 * C), "bf16", device=device)
+    return xs, cw, g, b, st, cs
+
+
+def timed(fn, steps, warmup, stream, dist=None):
+    """Warm-up, then `steps` calls between two barriers + synchronizes, timed with CUDA events
+    on `stream`; returns (ms per step over the whole region, mean ms per call, max over ranks)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for i in range(steps):
+            fn()
+            evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+    total_ms = evs[0].elapsed_time(evs[-1])
+    if dist is not None:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        if dist is not None:
+            dist.barrier()
+    return total_ms / steps, statistics.mean(per), wall
+
+
+def run_ours(args):
+    import torch
+
+    import gated_delta_rule_53_gb300 as kda
+    import kda_synth as ks
+    from gated_delta_rule_53_gb300 import build as kbuild
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl")
+        dist = tdist
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", torch.cuda.current_device())
+    if rank == 0:
+        kbuild.build()
+    if dist is not None:
+        dist.barrier()
+    kda.library()
+    hbm_peak, tc_peak, peak_src = load_peaks()
+    stream = torch.cuda.Stream(device)
+
+    # ---------------- prefill (the step) ----------------
+    w = ks.workload(args.workload)
+    q, k, v, g, b = make_prefill_inputs(w, device)
+    o = torch.empty((w.T, w.H, w.d), dtype=torch.bfloat16, device=device)
+    fs = torch.empty((w.N, w.H, w.d, w.d), dtype=torch.float32, device=device)
+    step = lambda: kda.kda_chunk_fwd(q, k, v, g, b, o=o, final_state=fs, stream=stream)
+    clocks = ClockSampler(smi_index(local))
+    clocks.start()
+    ms_step, ms_launch, _ = timed(step, args.steps, args.warmup, stream, dist)
+    clk = clocks.stop()
+    tokens = w.T * world
+    value = tokens / (ms_step * 1e-3)
+    pbytes = prefill_bytes(w.T, w.H, w.N)
+    achieved_gbs = pbytes / (ms_launch * 1e-3) / 1e9
+    pflops = w.T * w.H * PREFILL_FLOPS_PER_TOKEN_HEAD
+    achieved_tflops = pflops / (ms_launch * 1e-3) / 1e12
+
+    # ---------------- end to end through the API with host buffers ----------------
+    host_in = [t.to("cpu").pin_memory() for t in (q, k, v, g, b)]
+    host_o = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    host_fs = torch.empty(fs.shape, dtype=fs.dtype, pin_memory=True)
+    dev_in = [torch.empty_like(t) for t in (q, k, v, g, b)]
+
+    def e2e_step():
+        for dst, src in zip(dev_in, host_in):
+            dst.copy_(src, non_blocking=True)
+        kda.kda_chunk_fwd(*dev_in, o=o, final_state=fs, stream=stream)
+        host_o.copy_(o, non_blocking=True)
+        host_fs.copy_(fs, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 20))
+    ms_e2e, _, _ = timed(e2e_step, e2e_steps, 2, stream, dist)
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_o.numel() * host_o.element_size() + host_fs.numel() * host_fs.element_size()
+    del host_in, dev_in
+
+    # ---------------- decode (second half of the metric) ----------------
+    wd = ks.workload("decode_64")
+    xs, cw, gd, bd, st, cs = make_decode_inputs(wd, device)
+    od = torch.empty((wd.N, wd.H, wd.d), dtype=torch.bfloat16, device=device)
+    dstep = lambda: kda.kda_recurrent_step(*xs, cw, gd, bd, st, cs, o=od, stream=stream)
+    dclocks = ClockSampler(smi_index(local))
+    dclocks.start()
+    dsteps = max(args.steps, 50)
+    ms_dec, ms_dec_launch, _ = timed(dstep, dsteps, args.warmup, stream, dist)
+    dclk = dclocks.stop()
+    dbytes = decode_bytes(wd.N, wd.H)
+    dec_gbs = dbytes / (ms_dec_launch * 1e-3) / 1e9
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generator; no dataset or weights involved)",
+        "config": {"workload": f"{w.name}: prefill N={w.N} T={w.T} H={w.H} dk=dv={w.d} chunk={w.chunk}, "
+                               "bf16 q,k,v (q,k L2-normalised), fp32 g=-5*sigmoid(z), beta=sigmoid(z), S0=0",
+                   "global_batch": w.N * world, "seq_len": w.T, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (1.2 GB per step), no flush"},
+        "clocks": clk,
+        "e2e": {"value": w.T * world / (ms_e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps + dsteps,
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved_gbs / hbm_peak, "traffic": None, "peak_source": peak_src,
+                     "kernel": "kda_chunk_fwd (bf16)", "algorithmic_bytes_per_launch": pbytes,
+                     "tensor": {"achieved_tflops": achieved_tflops, "peak_tflops": tc_peak,
+                                "frac": achieved_tflops / tc_peak,
+                                "algorithmic_flops_per_launch": pflops}},
+        "decode": {"workload": "decode_64: 64 sequences x 1 token, H=96, d=128, fused ShortConv+SiLU+L2norm, "
+                               "in-place fp32 state N(0,0.02)",
+                   "value": dec_gbs, "unit": "GB/s", "ms_per_step": ms_dec, "steps": dsteps,
+                   "algorithmic_bytes_per_launch": dbytes, "clocks": dclk,
+                   "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
+                                "frac": dec_gbs / hbm_peak, "traffic": None, "peak_source": peak_src}},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------------------
+# the oracle on host cores (cpu_baseline leg and --impl reference)
+# ------------------------------------------------------------------------------------------------
+
+def oracle_sample(w, heads, t_len):
+    import numpy as np
+
+    import kda_synth as ks
+    d = w.d
+    Hs = len(heads)
+    q = np.empty((t_len, Hs, d)); k = np.empty((t_len, Hs, d)); v = np.empty((t_len, Hs, d))
+    g = np.empty((t_len, Hs, d)); b = np.empty((t_len, Hs))
+    for i, h in enumerate(heads):
+        q[:, i] = ks.to_f64(w.head_rows(ks.TID_Q, ks.UNIT_GROUPS, h, w.dtype, p1=float(d), t1=t_len))
+        k[:, i] = ks.to_f64(w.head_rows(ks.TID_K, ks.UNIT_GROUPS, h, w.dtype, p1=float(d), t1=t_len))
+        v[:, i] = ks.to_f64(w.head_rows(ks.TID_V, ks.NORMAL, h, w.dtype, t1=t_len))
+        g[:, i] = w.head_rows(ks.TID_G, w.g_kind, h, "f32", t1=t_len)
+        b[:, i] = w.head_beta(h, 0, t_len)
+    return q, k, v, g, b
+
+
+def cpu_baseline(w, budget_s=20.0):
+    """The oracle as it stands on this host's cores, on a bounded sample of the workload:
+    whole sequences of the first heads, as many heads as fit about half of ``budget_s``."""
+    import oracle
+    oracle.build()
+    cores = oracle.threads()
+    heads = min(w.H, max(1, cores))
+    t_len = w.T
+    while True:
+        sample = oracle_sample(w, list(range(heads)), t_len)
+        t0 = time.perf_counter()
+        oracle.kda_tokenloop(*sample)
+        dt = time.perf_counter() - t0
+        if heads >= w.H or dt >= 0.25 * budget_s:
+            break
+        heads = min(w.H, max(heads + 1, int(heads * 0.5 * budget_s / max(dt, 1e-3))))
+    token_heads = t_len * heads
+    return {"value": token_heads / w.H / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{w.name}: heads 0..{heads - 1} of {w.H}, all {t_len} tokens "
+                      f"(fp64 per-token loop, {token_heads} token-heads, {dt:.1f} s); "
+                      f"tokens/s = token-heads / {w.H} / seconds"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import kda_synth as ks
+    import oracle
+    oracle.build()
+    w = ks.workload(args.workload)
+    cores = oracle.threads()
+    heads = list(range(min(w.H, cores)))
+    t_len = min(w.T, 256)
+    sample = oracle_sample(w, heads, t_len)
+    for _ in range(args.warmup):
+        oracle.kda_tokenloop(*sample)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.kda_tokenloop(*sample)
+        times.append(time.perf_counter() - t0)
+    sec = statistics.mean(times)
+    value = t_len * len(heads) / w.H / sec
+    desc = (f"{w.name}: heads 0..{len(heads) - 1} of {w.H}, tokens 0..{t_len - 1} per step "
+            f"(fp64 per-token loop); tokens/s = token-heads / {w.H} / seconds")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: prefill N={w.N} T={w.T} H={w.H} dk=dv={w.d} (bounded sample per step)",
+                   "global_batch": w.N, "seq_len": w.T, "parallelism": "host threads"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="prefill_8k", choices=["prefill_8k"])
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

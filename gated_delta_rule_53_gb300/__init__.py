@@ -1,0 +1,174 @@
+"""Kimi Delta Attention (KDA) on one GB300: thin Python binding of ``libkda.so``.
+
+Every function here marshals torch tensors into the C ABI declared in
+``include/kda.h`` (device pointers, sizes, the current CUDA stream) and calls
+it; all arithmetic runs in the library's CUDA kernels.  PyTorch provides device
+memory and streams only.  There is no CPU fallback: if ``libkda.so`` has not
+been built (``python -m gated_delta_rule_53_gb300.build``), or no CUDA device is
+present, the calls raise.
+
+Entry points (same names as the C ABI):
+
+* :func:`kda_shortconv_l2norm` — ShortConv(4) + SiLU on q, k, v; L2 norm of q, k.
+* :func:`kda_chunk_fwd` — chunkwise prefill (``chunk_kda``), optional output gate.
+* :func:`kda_recurrent_step` — fused single-token decode (``fused_recurrent_kda``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = ["kda_shortconv_l2norm", "kda_chunk_fwd", "kda_recurrent_step", "library", "KDAError",
+           "device_error", "LIB_PATH"]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkda.so")
+KDA_DTYPE_F32, KDA_DTYPE_BF16 = 0, 1
+_lib = None
+
+
+class KDAError(RuntimeError):
+    pass
+
+
+def library() -> ctypes.CDLL:
+    """The loaded ``libkda.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise KDAError(f"{LIB_PATH} is missing: build it with `python -m gated_delta_rule_53_gb300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I32, I64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+        lib.kda_shortconv_l2norm.argtypes = [P, P, P, I64, P, P, I32, I64, I32, I32, P, P, F, I32, P, P, P, P]
+        lib.kda_chunk_fwd.argtypes = [P, P, P, P, P, P, P, I32, I64, I32, I32, I32, F, I32, I32, P, P, P, P]
+        lib.kda_recurrent_step.argtypes = [P, P, P, I64, P, P, P, P, P, I32, I32, I32, I32, F, F, P, P]
+        for f in (lib.kda_shortconv_l2norm, lib.kda_chunk_fwd, lib.kda_recurrent_step, lib.kda_device_error):
+            f.restype = ctypes.c_int
+        lib.kda_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_status_string.argtypes = [ctypes.c_int]
+        lib.kda_last_error.restype = ctypes.c_char_p
+        lib.kda_version.restype = ctypes.c_char_p
+        _lib = lib
+    return _lib
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        lib = library()
+        raise KDAError(f"{what}: {lib.kda_status_string(rc).decode()} — {lib.kda_last_error().decode()}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t, name, dtype=None, shape=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise KDAError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise KDAError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise KDAError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise KDAError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def device_error() -> int:
+    """Read and clear the library's device error word (synchronises the device)."""
+    code = ctypes.c_uint(0)
+    _check(library().kda_device_error(ctypes.byref(code)), "kda_device_error")
+    return int(code.value)
+
+
+def kda_shortconv_l2norm(xq, xk, xv, conv_w, H: int, cu_seqlens=None, conv_state_in=None, conv_state_out=None,
+                         eps: float = 1e-6, out_dtype=torch.bfloat16, q=None, k=None, v=None, stream=None):
+    """ShortConv(4) + SiLU on raw bf16 rows x* [T, >=H*128] (row stride = x.stride(0));
+    returns (q, k, v) [T, H, 128] with q, k L2-normalised per head."""
+    d = 128
+    T = xq.shape[0]
+    for name, x in (("xq", xq), ("xk", xk), ("xv", xv)):
+        if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1:
+            raise KDAError(f"{name} must be a CUDA bf16 [T, width] tensor with unit inner stride")
+        if x.shape[0] != T or x.stride(0) != xq.stride(0):
+            raise KDAError("xq, xk, xv must share shape and row stride")
+    _dev(conv_w, "conv_w", torch.bfloat16, (3 * H * d, 4))
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    _dev(cu_seqlens, "cu_seqlens", torch.int32)
+    _dev(conv_state_in, "conv_state_in", torch.bfloat16, (N, 3, 3 * H * d))
+    _dev(conv_state_out, "conv_state_out", torch.bfloat16, (N, 3, 3 * H * d))
+    outs = []
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t is None:
+            t = torch.empty((T, H, d), dtype=out_dtype, device=xq.device)
+        outs.append(_dev(t, name, out_dtype, (T, H, d)))
+    dt = KDA_DTYPE_BF16 if out_dtype == torch.bfloat16 else KDA_DTYPE_F32
+    rc = library().kda_shortconv_l2norm(_ptr(xq), _ptr(xk), _ptr(xv), xq.stride(0), _ptr(conv_w), _ptr(cu_seqlens),
+                                        N, T, H, d, _ptr(conv_state_in), _ptr(conv_state_out), float(eps), dt,
+                                        _ptr(outs[0]), _ptr(outs[1]), _ptr(outs[2]), _stream(stream))
+    _check(rc, "kda_shortconv_l2norm")
+    return tuple(outs)
+
+
+def kda_chunk_fwd(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale: float = 1.0, chunk_size: int = 64,
+                  out_gate=None, o=None, final_state=None, output_final_state: bool = True, stream=None):
+    """Chunkwise KDA prefill.  q, k, v [T, H, 128] (bf16 or fp32, q and k L2-normalised),
+    g fp32 [T, H, 128] in [-5, 0], beta fp32 [T, H], init_state fp32 [N, H, 128, 128] or None,
+    cu_seqlens int32 [N+1] or None, out_gate bf16 [T, H*128] or None.
+    Returns (o [T, H, 128], final_state [N, H, 128, 128] or None)."""
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    dtype = q.dtype
+    if dtype not in (torch.bfloat16, torch.float32):
+        raise KDAError("q, k, v must be bf16 or fp32")
+    _dev(q, "q", dtype); _dev(k, "k", dtype, (T, H, dk)); _dev(v, "v", dtype, (T, H, dv))
+    _dev(g, "g", torch.float32, (T, H, dk)); _dev(beta, "beta", torch.float32, (T, H))
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    _dev(cu_seqlens, "cu_seqlens", torch.int32)
+    _dev(init_state, "init_state", torch.float32, (N, H, dv, dk))
+    _dev(out_gate, "out_gate", torch.bfloat16, (T, H * dv))
+    if o is None:
+        o = torch.empty((T, H, dv), dtype=dtype, device=q.device)
+    _dev(o, "o", dtype, (T, H, dv))
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, dv, dk), dtype=torch.float32, device=q.device)
+    _dev(final_state, "final_state", torch.float32, (N, H, dv, dk))
+    dt = KDA_DTYPE_BF16 if dtype == torch.bfloat16 else KDA_DTYPE_F32
+    rc = library().kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state), _ptr(cu_seqlens),
+                                 N, T, H, dk, dv, float(scale), int(chunk_size), dt, _ptr(out_gate), _ptr(o),
+                                 _ptr(final_state), _stream(stream))
+    _check(rc, "kda_chunk_fwd")
+    return o, final_state
+
+
+def kda_recurrent_step(xq, xk, xv, conv_w, g, beta, state, conv_state, scale: float = 1.0, eps: float = 1e-6,
+                       o=None, stream=None):
+    """One fused decode step, in place on ``state`` (fp32 [N, H, 128, 128]) and
+    ``conv_state`` (bf16 [N, 3, 3*H*128]).  x* raw bf16 [N, >=H*128]; g fp32 [N, H, 128];
+    beta fp32 [N, H].  Returns o bf16 [N, H, 128]."""
+    N, H, dv, dk = state.shape
+    for name, x in (("xq", xq), ("xk", xk), ("xv", xv)):
+        if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1 or x.shape[0] != N:
+            raise KDAError(f"{name} must be a CUDA bf16 [N, width] tensor with unit inner stride")
+        if x.stride(0) != xq.stride(0):
+            raise KDAError("xq, xk, xv must share their row stride")
+    _dev(conv_w, "conv_w", torch.bfloat16, (3 * H * dk, 4))
+    _dev(g, "g", torch.float32, (N, H, dk)); _dev(beta, "beta", torch.float32, (N, H))
+    _dev(state, "state", torch.float32); _dev(conv_state, "conv_state", torch.bfloat16, (N, 3, 3 * H * dk))
+    if o is None:
+        o = torch.empty((N, H, dv), dtype=torch.bfloat16, device=state.device)
+    _dev(o, "o", torch.bfloat16, (N, H, dv))
+    rc = library().kda_recurrent_step(_ptr(xq), _ptr(xk), _ptr(xv), xq.stride(0), _ptr(conv_w), _ptr(g), _ptr(beta),
+                                      _ptr(state), _ptr(conv_state), N, H, dk, dv, float(scale), float(eps), _ptr(o),
+                                      _stream(stream))
+    _check(rc, "kda_recurrent_step")
+    return o

@@ -1,0 +1,159 @@
+// The C ABI of libkda.so (declared in include/kda.h): argument checks, error
+// reporting and dispatch to the kernel launchers.  Nothing here allocates.
+#include <cstdarg>
+#include <cstdio>
+#include <cmath>
+
+#include "kda_common.cuh"
+
+namespace kda {
+namespace {
+
+thread_local char t_last_error[512] = "";
+
+}  // namespace
+
+kda_status set_error(kda_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+}  // namespace kda
+
+__device__ unsigned int g_kda_device_error = 0;
+
+using kda::set_error;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kda_status ok() {
+    kda::t_last_error[0] = '\0';
+    return KDA_OK;
+}
+
+kda_status from_cuda(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return ok();
+    return set_error(KDA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define REQUIRE(cond, ...)                                        \
+    do {                                                          \
+        if (!(cond)) return set_error(KDA_ERR_INVALID_ARG, __VA_ARGS__); \
+    } while (0)
+
+#define REQUIRE_PTR(p)                                                          \
+    do {                                                                        \
+        REQUIRE((p) != nullptr, "%s must not be NULL", #p);                     \
+        REQUIRE(aligned16(p), "%s must be 16-byte aligned", #p);                \
+    } while (0)
+
+#define OPTIONAL_PTR(p)                                                         \
+    do {                                                                        \
+        REQUIRE((p) == nullptr || aligned16(p), "%s must be 16-byte aligned", #p); \
+    } while (0)
+
+kda_status check_batch(const int32_t* cu, int N, int64_t T_total, int H) {
+    REQUIRE(N >= 1, "N must be >= 1 (got %d)", N);
+    REQUIRE(H >= 1 && H <= 65535, "H must be in [1, 65535] (got %d)", H);
+    REQUIRE(T_total >= 0, "T_total must be >= 0");
+    REQUIRE(cu != nullptr || N == 1, "cu_seqlens may be NULL only for N == 1 (got N = %d)", N);
+    REQUIRE((int64_t)N * H <= 0x7FFFFFFF, "N * H too large");
+    REQUIRE(T_total <= ((int64_t)1 << 40), "T_total too large");
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kda_status_string(kda_status s) {
+    switch (s) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: unsupported shape or option";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime error";
+    case KDA_ERR_DEVICE: return "KDA_ERR_DEVICE: a kernel reported a fault";
+    }
+    return "unknown kda_status";
+}
+
+const char* kda_last_error(void) { return kda::t_last_error; }
+
+const char* kda_version(void) { return "0.1.0"; }
+
+kda_status kda_device_error(unsigned int* code) {
+    REQUIRE(code != nullptr, "code must not be NULL");
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_kda_device_error, sizeof(v));
+    if (e != cudaSuccess) return from_cuda(e, "reading the device error word");
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_kda_device_error, &zero, sizeof(zero));
+    if (e != cudaSuccess) return from_cuda(e, "clearing the device error word");
+    *code = v;
+    return ok();
+}
+
+kda_status kda_shortconv_l2norm(const void* xq, const void* xk, const void* xv, int64_t x_row_stride,
+                                const void* conv_w, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
+                                int d, const void* conv_state_in, void* conv_state_out, float eps,
+                                kda_dtype out_dtype, void* q_out, void* k_out, void* v_out, void* stream) {
+    REQUIRE_PTR(xq); REQUIRE_PTR(xk); REQUIRE_PTR(xv); REQUIRE_PTR(conv_w);
+    REQUIRE_PTR(q_out); REQUIRE_PTR(k_out); REQUIRE_PTR(v_out);
+    OPTIONAL_PTR(conv_state_in); OPTIONAL_PTR(conv_state_out);
+    kda_status s = check_batch(cu_seqlens, N, T_total, H);
+    if (s != KDA_OK) return s;
+    if (d != kda::kHeadDim) return set_error(KDA_ERR_UNSUPPORTED, "only d = 128 is supported (got %d)", d);
+    REQUIRE(x_row_stride >= (int64_t)H * d && x_row_stride % 8 == 0,
+            "x_row_stride must be >= H*d and a multiple of 8 (got %lld)", (long long)x_row_stride);
+    REQUIRE(out_dtype == KDA_DTYPE_F32 || out_dtype == KDA_DTYPE_BF16, "bad out_dtype");
+    REQUIRE(std::isfinite(eps) && eps >= 0.f, "eps must be finite and >= 0");
+    REQUIRE((T_total + 63) / 64 <= 0x7FFFFFFF, "T_total too large");
+    return from_cuda(kda::launch_shortconv_l2norm(xq, xk, xv, x_row_stride, conv_w, cu_seqlens, N, T_total, H,
+                                                  conv_state_in, conv_state_out, eps, out_dtype, q_out, k_out,
+                                                  v_out, static_cast<cudaStream_t>(stream)),
+                     "kda_shortconv_l2norm launch");
+}
+
+kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
+                         int dk, int dv, float scale, int chunk_size, kda_dtype dtype, const void* out_gate,
+                         void* o, float* final_state, void* stream) {
+    REQUIRE_PTR(q); REQUIRE_PTR(k); REQUIRE_PTR(v); REQUIRE_PTR(g); REQUIRE_PTR(beta); REQUIRE_PTR(o);
+    OPTIONAL_PTR(init_state); OPTIONAL_PTR(final_state); OPTIONAL_PTR(out_gate);
+    kda_status s = check_batch(cu_seqlens, N, T_total, H);
+    if (s != KDA_OK) return s;
+    if (dk != kda::kHeadDim || dv != kda::kHeadDim)
+        return set_error(KDA_ERR_UNSUPPORTED, "only dk = dv = 128 is supported (got %d, %d)", dk, dv);
+    if (chunk_size != kda::kChunk)
+        return set_error(KDA_ERR_UNSUPPORTED, "only chunk_size = 64 is supported (got %d)", chunk_size);
+    REQUIRE(dtype == KDA_DTYPE_F32 || dtype == KDA_DTYPE_BF16, "bad dtype");
+    REQUIRE(std::isfinite(scale), "scale must be finite");
+    return from_cuda(kda::launch_chunk_simt(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, scale, dtype,
+                                            out_gate, o, final_state, static_cast<cudaStream_t>(stream)),
+                     "kda_chunk_fwd launch");
+}
+
+kda_status kda_recurrent_step(const void* xq, const void* xk, const void* xv, int64_t x_row_stride,
+                              const void* conv_w, const float* g, const float* beta, float* state,
+                              void* conv_state, int N, int H, int dk, int dv, float scale, float eps, void* o,
+                              void* stream) {
+    REQUIRE_PTR(xq); REQUIRE_PTR(xk); REQUIRE_PTR(xv); REQUIRE_PTR(conv_w); REQUIRE_PTR(g);
+    REQUIRE_PTR(beta); REQUIRE_PTR(state); REQUIRE_PTR(conv_state); REQUIRE_PTR(o);
+    REQUIRE(N >= 1, "N must be >= 1 (got %d)", N);
+    REQUIRE(H >= 1 && (int64_t)N * H <= 0x7FFFFFFF, "bad H");
+    if (dk != kda::kHeadDim || dv != kda::kHeadDim)
+        return set_error(KDA_ERR_UNSUPPORTED, "only dk = dv = 128 is supported (got %d, %d)", dk, dv);
+    REQUIRE(x_row_stride >= (int64_t)H * dk && x_row_stride % 8 == 0,
+            "x_row_stride must be >= H*d and a multiple of 8 (got %lld)", (long long)x_row_stride);
+    REQUIRE(std::isfinite(scale) && std::isfinite(eps) && eps >= 0.f, "scale and eps must be finite, eps >= 0");
+    return from_cuda(kda::launch_recurrent_step(xq, xk, xv, x_row_stride, conv_w, g, beta, state, conv_state, N,
+                                                H, scale, eps, o, static_cast<cudaStream_t>(stream)),
+                     "kda_recurrent_step launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,90 @@
+// Shared device helpers of libkda.so (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+constexpr int kHeadDim = 128;  // d = dk = dv supported by every kernel
+constexpr int kChunk = 64;     // chunk length of the prefill
+
+// Kernels that wait on a barrier get a pointer to the library's device error
+// word (kda_api.cu); a wait that runs out sets it instead of spinning forever,
+// and the host reads it through kda_device_error().
+enum DeviceError : unsigned int {
+    kErrNone = 0,
+    kErrMbarTimeout = 1,
+};
+
+__device__ __forceinline__ void raise_device_error(unsigned int* err, unsigned int code) {
+    if (err) atomicCAS(err, 0u, code);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t packed) { return __uint_as_float(packed & 0xFFFF0000u); }
+
+// Round-to-nearest-even fp32 -> bf16 of two values, packed low | high << 16.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <typename T>
+__device__ __forceinline__ float load_as_float(const T* p);
+template <>
+__device__ __forceinline__ float load_as_float<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float load_as_float<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+
+template <typename T>
+__device__ __forceinline__ void store_from_float(T* p, float x);
+template <>
+__device__ __forceinline__ void store_from_float<float>(float* p, float x) { *p = x; }
+template <>
+__device__ __forceinline__ void store_from_float<__nv_bfloat16>(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+    return x;
+}
+
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
+
+// Sequence bounds of chain n (cu_seqlens may be null: one sequence).
+__device__ __forceinline__ void seq_bounds(const int32_t* cu, int n, int64_t T_total, int64_t& bos, int64_t& eos) {
+    if (cu) {
+        bos = cu[n];
+        eos = cu[n + 1];
+    } else {
+        bos = 0;
+        eos = T_total;
+    }
+}
+
+}  // namespace kda
+
+// Kernel launchers (one per kernel file), called by the entry points in kda_api.cu
+// after the arguments have been checked.  They return the launch's error.
+namespace kda {
+
+cudaError_t launch_recurrent_step(const void* xq, const void* xk, const void* xv, int64_t x_stride,
+                                  const void* conv_w, const float* g, const float* beta, float* state,
+                                  void* conv_state, int N, int H, float scale, float eps, void* o,
+                                  cudaStream_t stream);
+
+cudaError_t launch_shortconv_l2norm(const void* xq, const void* xk, const void* xv, int64_t x_stride,
+                                    const void* conv_w, const int32_t* cu_seqlens, int N, int64_t T_total,
+                                    int H, const void* conv_state_in, void* conv_state_out, float eps,
+                                    kda_dtype out_dtype, void* q, void* k, void* v, cudaStream_t stream);
+
+cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                              const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total,
+                              int H, float scale, kda_dtype dtype, const void* out_gate, void* o,
+                              float* final_state, cudaStream_t stream);
+
+}  // namespace kda

@@ -1,0 +1,186 @@
+// kda_shortconv_l2norm: the prefill front end.  ShortConv(kernel 4) + SiLU on
+// each of q, k, v and the L2 norm of q and k over each head ("深入 Kimi-K3:
+// Hugging Face 仓库分析", paragraph on KDA; kernel size 4 from "Kimi K3 架构全景",
+// section 02).
+//
+// Memory-bound elementwise work: every raw element is read once and every
+// output written once.  One warp owns one (part, head) and a run of 16 tokens;
+// each lane owns 4 adjacent channels, so a token row of the head is one 256-byte
+// coalesced load.  The warp loads its 16 rows up front, keeps the last three raw
+// inputs of every channel in registers as it walks the run, and reduces the
+// squared norm of q / k with shuffles.  A second small kernel writes the carried
+// convolution state (last three raw inputs per sequence) after the first has
+// finished reading the incoming one, so the two buffers may alias.
+#include "kda_common.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kRun = 16;          // tokens per warp
+constexpr int kWarps = 4;         // warps per CTA (64 tokens of one part and head)
+
+__device__ __forceinline__ float4 bf16x4(uint2 u) {
+    return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+}
+
+// Largest n with cu[n] <= t < cu[n + 1] (skips empty sequences).
+__device__ __forceinline__ int find_seq(const int32_t* cu, int N, int64_t t) {
+    int lo = 0, hi = N;  // invariant: cu[lo] <= t, answer in [lo, hi)
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if ((int64_t)cu[mid] <= t) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+template <typename OutT>
+__device__ __forceinline__ void store4(OutT* p, float a, float b, float c, float d);
+template <>
+__device__ __forceinline__ void store4<float>(float* p, float a, float b, float c, float d) {
+    *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float a, float b, float c, float d) {
+    *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(a, b), pack_bf16x2(c, d));
+}
+
+template <typename OutT>
+__global__ void __launch_bounds__(kWarps * 32)
+shortconv_kernel(const __nv_bfloat16* __restrict__ xq, const __nv_bfloat16* __restrict__ xk,
+                 const __nv_bfloat16* __restrict__ xv, int64_t x_stride,
+                 const __nv_bfloat16* __restrict__ conv_w, const int32_t* __restrict__ cu, int N,
+                 int64_t T_total, int H, const __nv_bfloat16* __restrict__ cs_in, float eps,
+                 OutT* __restrict__ q_out, OutT* __restrict__ k_out, OutT* __restrict__ v_out) {
+    const int p = blockIdx.z, h = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t t0 = ((int64_t)blockIdx.x * kWarps + warp) * kRun;
+    if (t0 >= T_total) return;
+    const int64_t t_end = min(t0 + kRun, T_total);
+    const int64_t C = (int64_t)H * kHeadDim;
+    const int64_t ch = (int64_t)h * kHeadDim + 4 * lane;
+    const int64_t gc = p * C + ch;
+    const __nv_bfloat16* x = p == 0 ? xq : (p == 1 ? xk : xv);
+    OutT* out = p == 0 ? q_out : (p == 1 ? k_out : v_out);
+
+    // the run's raw rows, loaded before any arithmetic
+    uint2 xr[kRun];
+#pragma unroll
+    for (int i = 0; i < kRun; ++i)
+        xr[i] = (t0 + i < t_end) ? *reinterpret_cast<const uint2*>(x + (t0 + i) * x_stride + ch) : make_uint2(0, 0);
+
+    // taps of the lane's 4 channels: w[e][0..3], oldest .. current
+    const uint4 w01 = *reinterpret_cast<const uint4*>(conv_w + gc * 4);
+    const uint4 w23 = *reinterpret_cast<const uint4*>(conv_w + gc * 4 + 8);
+    const uint32_t wr[8] = {w01.x, w01.y, w01.z, w01.w, w23.x, w23.y, w23.z, w23.w};
+    float w[4][4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        w[e][0] = bf16_lo(wr[2 * e]); w[e][1] = bf16_hi(wr[2 * e]);
+        w[e][2] = bf16_lo(wr[2 * e + 1]); w[e][3] = bf16_hi(wr[2 * e + 1]);
+    }
+
+    int n = cu ? find_seq(cu, N, t0) : 0;
+    int64_t bos = cu ? cu[n] : 0, eos = cu ? cu[n + 1] : T_total;
+    // raw input at absolute position s < t (before the run, or before the sequence)
+    auto history = [&](int64_t s) -> float4 {
+        if (s >= bos) return bf16x4(*reinterpret_cast<const uint2*>(x + s * x_stride + ch));
+        const int64_t back = bos - s;
+        if (!cs_in || back > 3) return make_float4(0.f, 0.f, 0.f, 0.f);
+        return bf16x4(*reinterpret_cast<const uint2*>(cs_in + ((int64_t)n * 3 + (3 - back)) * 3 * C + gc));
+    };
+    float4 h1 = history(t0 - 3), h2 = history(t0 - 2), h3 = history(t0 - 1);
+
+#pragma unroll
+    for (int i = 0; i < kRun; ++i) {
+        const int64_t t = t0 + i;
+        if (t >= t_end) break;
+        if (t >= eos) {  // a new sequence starts at t: its history is the carried state
+            while ((int64_t)cu[n + 1] <= t) ++n;
+            bos = cu[n];
+            eos = cu[n + 1];
+            h1 = history(t - 3); h2 = history(t - 2); h3 = history(t - 1);
+        }
+        const float4 xt = bf16x4(xr[i]);
+        const float a0[4] = {h1.x, h1.y, h1.z, h1.w}, a1[4] = {h2.x, h2.y, h2.z, h2.w};
+        const float a2[4] = {h3.x, h3.y, h3.z, h3.w}, a3[4] = {xt.x, xt.y, xt.z, xt.w};
+        float y[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float acc = w[e][0] * a0[e];
+            acc = fmaf(w[e][1], a1[e], acc);
+            acc = fmaf(w[e][2], a2[e], acc);
+            acc = fmaf(w[e][3], a3[e], acc);
+            y[e] = acc / (1.0f + expf(-acc));
+        }
+        float inv = 1.0f;
+        if (p < 2) inv = 1.0f / sqrtf(warp_sum(y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3]) + eps);
+        store4<OutT>(out + (t * H + h) * kHeadDim + 4 * lane, y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv);
+        h1 = h2; h2 = h3; h3 = xt;
+    }
+}
+
+// conv_state_out[n][r][gc] = raw input at position eos - 3 + r of sequence n.
+__global__ void conv_state_out_kernel(const __nv_bfloat16* __restrict__ xq, const __nv_bfloat16* __restrict__ xk,
+                                      const __nv_bfloat16* __restrict__ xv, int64_t x_stride,
+                                      const int32_t* __restrict__ cu, int64_t T_total, int H,
+                                      const __nv_bfloat16* cs_in, __nv_bfloat16* cs_out) {
+    const int n = blockIdx.y;
+    const int64_t C = (int64_t)H * kHeadDim;
+    const int64_t gc = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (gc >= 3 * C) return;
+    const int p = (int)(gc / C);
+    const int64_t ch = gc - p * C;
+    const __nv_bfloat16* x = p == 0 ? xq : (p == 1 ? xk : xv);
+    int64_t bos, eos;
+    seq_bounds(cu, n, T_total, bos, eos);
+    __nv_bfloat16 val[3];
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+        const int64_t s = eos - 3 + r;
+        if (s >= bos) {
+            val[r] = x[s * x_stride + ch];
+        } else {
+            const int64_t back = bos - s;
+            val[r] = (cs_in && back <= 3) ? cs_in[((int64_t)n * 3 + (3 - back)) * 3 * C + gc] : __float2bfloat16_rn(0.f);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 3; ++r) cs_out[((int64_t)n * 3 + r) * 3 * C + gc] = val[r];
+}
+
+}  // namespace
+
+cudaError_t launch_shortconv_l2norm(const void* xq, const void* xk, const void* xv, int64_t x_stride,
+                                    const void* conv_w, const int32_t* cu_seqlens, int N, int64_t T_total,
+                                    int H, const void* conv_state_in, void* conv_state_out, float eps,
+                                    kda_dtype out_dtype, void* q, void* k, void* v, cudaStream_t stream) {
+    const auto* bq = static_cast<const __nv_bfloat16*>(xq);
+    const auto* bk = static_cast<const __nv_bfloat16*>(xk);
+    const auto* bv = static_cast<const __nv_bfloat16*>(xv);
+    const auto* w = static_cast<const __nv_bfloat16*>(conv_w);
+    const auto* cs_in = static_cast<const __nv_bfloat16*>(conv_state_in);
+    if (T_total > 0) {
+        const int64_t per_cta = (int64_t)kWarps * kRun;
+        dim3 grid((unsigned)((T_total + per_cta - 1) / per_cta), (unsigned)H, 3);
+        if (out_dtype == KDA_DTYPE_BF16)
+            shortconv_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, stream>>>(
+                bq, bk, bv, x_stride, w, cu_seqlens, N, T_total, H, cs_in, eps, static_cast<__nv_bfloat16*>(q),
+                static_cast<__nv_bfloat16*>(k), static_cast<__nv_bfloat16*>(v));
+        else
+            shortconv_kernel<float><<<grid, kWarps * 32, 0, stream>>>(
+                bq, bk, bv, x_stride, w, cu_seqlens, N, T_total, H, cs_in, eps, static_cast<float*>(q),
+                static_cast<float*>(k), static_cast<float*>(v));
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (conv_state_out) {
+        const int64_t C3 = 3 * (int64_t)H * kHeadDim;
+        dim3 grid((unsigned)((C3 + 255) / 256), (unsigned)N);
+        conv_state_out_kernel<<<grid, 256, 0, stream>>>(bq, bk, bv, x_stride, cu_seqlens, T_total, H, cs_in,
+                                                        static_cast<__nv_bfloat16*>(conv_state_out));
+        return cudaGetLastError();
+    }
+    return cudaSuccess;
+}
+
+}  // namespace kda

@@ -1,0 +1,172 @@
+/*
+ * kda.h — C ABI of libkda.so: Kimi Delta Attention (KDA) on one GB300 (sm_103a).
+ *
+ * KDA is the gated delta-rule linear attention of the Kimi K3 model.  Per head
+ * it carries a state S of dv x dk values.  For each token, with q, k, v after
+ * ShortConv(kernel 4) + SiLU and q, k L2-normalised, alpha = exp(g) a
+ * per-key-channel decay (g >= -5) and beta a scalar in [0, 1]:
+ *
+ *     S~  = S Diag(alpha)                 (decay, one factor per key channel)
+ *     S   = S~ + beta (v - S~ k) k^T      (delta-rule correction)
+ *     o   = scale * S q
+ *
+ * Sources: "Kimi-K3 深度解析: 2.8T 开源 MoE 模型的架构创新与设计哲学", section 三,
+ * subsection "KDA 的关键改进" (the two update equations); "Kimi K3 架构全景",
+ * section 02, KDA column (96 heads x 128, ShortConv kernel 4, gate lower bound
+ * -5.0, operators chunk_kda / fused_recurrent_kda, recurrent state instead of a
+ * KV cache); "深入 Kimi-K3: Hugging Face 仓库分析", paragraph on KDA (short
+ * convolution with SiLU on q, k, v; L2 norm of q and k inside the kernel;
+ * per-channel decay bounded below by -5; full-rank output gate).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor pointer is CALLER-OWNED DEVICE memory on the current CUDA
+ *    device.  The library allocates nothing, frees nothing and keeps no state
+ *    between calls (apart from one device error word, see kda_device_error).
+ *  - Calls are asynchronous: they check their arguments on the host, enqueue
+ *    kernels on `stream` (a cudaStream_t; NULL = legacy default stream) and
+ *    return.  An argument error returns before anything is enqueued.  A launch
+ *    failure returns KDA_ERR_CUDA.  kda_last_error() gives a message.
+ *  - Layouts are row-major, innermost index last:
+ *      q, k, g            [T_total, H, dk]
+ *      v, o               [T_total, H, dv]
+ *      beta               [T_total, H]
+ *      states             [N, H, dv, dk]   fp32 (S is dv x dk)
+ *      raw front-end rows [T_total, x_row_stride], the first H*d used
+ *      conv_w             [3*H*d, 4] bf16: rows are q channels, then k, then v;
+ *                          taps oldest .. current token
+ *      conv_state         [N, 3, 3*H*d] bf16: the last three raw inputs of each
+ *                          sequence, oldest row first, same channel order
+ *      cu_seqlens         [N + 1] int32 on the device, non-decreasing, first 0,
+ *                          last T_total (NULL = one sequence of T_total tokens)
+ *  - Every device pointer must be 16-byte aligned.  Only d = dk = dv = 128 is
+ *    supported (KDA_ERR_UNSUPPORTED otherwise); chunk_size must be 64.
+ *  - Preconditions the kernels rely on: g in [-5, 0], beta in [0, 1], finite
+ *    inputs.  They are not clamped.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* a null, misaligned or inconsistent argument          */
+    KDA_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. d != 128)            */
+    KDA_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed                 */
+    KDA_ERR_DEVICE = 4       /* a kernel reported a fault through the error word     */
+} kda_status;
+
+typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
+
+/*
+ * Front end of a prefill: ShortConv(kernel 4) + SiLU on each of q, k, v, then
+ * L2 normalisation of q and k over each head's d channels ("深入 Kimi-K3: Hugging
+ * Face 仓库分析", paragraph on KDA; kernel size from "Kimi K3 架构全景", section 02).
+ *
+ * For part p in {q, k, v}, channel c, token t of sequence n:
+ *   y = sum_{i=0..3} conv_w[p*H*d + c][i] * x_p[t - 3 + i][c]
+ *   a = y / (1 + exp(-y))
+ *   q_out, k_out = a / sqrt(sum over the head's channels of a^2 + eps); v_out = a
+ * Positions before a sequence's first token read conv_state_in[n] (row 3 - j
+ * for j positions back), or zero when conv_state_in is NULL.  The convolution
+ * has no bias and restarts at every cu_seqlens boundary.
+ *
+ *  xq, xk, xv      raw bf16 rows [T_total, x_row_stride] (x_row_stride >= H*d,
+ *                  a multiple of 8 elements)
+ *  conv_w          bf16 [3*H*d, 4]
+ *  cu_seqlens, N   see conventions
+ *  conv_state_in   bf16 [N, 3, 3*H*d] or NULL
+ *  conv_state_out  bf16 [N, 3, 3*H*d] or NULL: receives the last three raw
+ *                  inputs of each sequence (reading conv_state_in for sequences
+ *                  shorter than 3).  May be the same buffer as conv_state_in.
+ *  out_dtype       storage type of q_out, k_out, v_out ([T_total, H, d])
+ */
+KDA_API kda_status kda_shortconv_l2norm(const void* xq, const void* xk, const void* xv, int64_t x_row_stride,
+                                const void* conv_w, const int32_t* cu_seqlens, int N, int64_t T_total,
+                                int H, int d, const void* conv_state_in, void* conv_state_out, float eps,
+                                kda_dtype out_dtype, void* q_out, void* k_out, void* v_out, void* stream);
+
+/*
+ * Chunkwise prefill (the chunk_kda operator of "Kimi K3 架构全景", section 02):
+ * runs the recurrence above over every sequence of a packed batch and returns
+ * every token's output and each sequence's final state.  The result equals the
+ * token-by-token recurrence; the chunk form only reorders the arithmetic.
+ *
+ *  q, k            [T_total, H, dk], storage `dtype`; L2-normalised by the caller
+ *  v               [T_total, H, dv], storage `dtype`
+ *  g               fp32 [T_total, H, dk], log-decay in [-5, 0]
+ *  beta            fp32 [T_total, H], in [0, 1]
+ *  init_state      fp32 [N, H, dv, dk] or NULL (= zeros)
+ *  cu_seqlens, N   see conventions; sequences may be empty (final = initial)
+ *  scale           multiplies every output
+ *  chunk_size      64
+ *  dtype           KDA_DTYPE_F32: fp32 inputs and output, computed in fp32 with
+ *                  explicit position-pair decays (no use of the -5 bound).
+ *                  KDA_DTYPE_BF16: bf16 inputs and output, intra-chunk products
+ *                  on bf16 tensor cores with fp32 accumulation, fp32 state.
+ *  out_gate        bf16 [T_total, H*dv] or NULL: if given, o *= sigmoid(out_gate)
+ *                  (the full-rank output gate, "深入 Kimi-K3: Hugging Face 仓库分析")
+ *  o               [T_total, H, dv], storage `dtype`
+ *  final_state     fp32 [N, H, dv, dk] or NULL.  May be the same buffer as
+ *                  init_state (each sequence's state is read before it is written).
+ */
+KDA_API kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
+                         int dk, int dv, float scale, int chunk_size, kda_dtype dtype, const void* out_gate,
+                         void* o, float* final_state, void* stream);
+
+/*
+ * One decode step (the fused_recurrent_kda operator of "Kimi K3 架构全景",
+ * section 02) for N sequences of one new token each, fused end to end: the
+ * ShortConv(4) + SiLU + L2 norm front end on the token's raw q, k, v (shifting
+ * conv_state in place), then the recurrence on the fp32 state (in place), and
+ * the output.
+ *
+ *  xq, xk, xv      raw bf16 rows [N, x_row_stride] (x_row_stride >= H*d, a
+ *                  multiple of 8 elements)
+ *  conv_w          bf16 [3*H*d, 4]
+ *  g               fp32 [N, H, dk] log-decay in [-5, 0];  beta fp32 [N, H]
+ *  state           fp32 [N, H, dv, dk], read and overwritten
+ *  conv_state      bf16 [N, 3, 3*H*d], read and overwritten (rows shift up by
+ *                  one, the raw token enters as row 2)
+ *  o               bf16 [N, H, dv]
+ */
+KDA_API kda_status kda_recurrent_step(const void* xq, const void* xk, const void* xv, int64_t x_row_stride,
+                              const void* conv_w, const float* g, const float* beta, float* state,
+                              void* conv_state, int N, int H, int dk, int dv, float scale, float eps, void* o,
+                              void* stream);
+
+/* Static description of a status code. */
+KDA_API const char* kda_status_string(kda_status s);
+
+/* Message of the last failing call on this host thread ("" if none). */
+KDA_API const char* kda_last_error(void);
+
+/*
+ * Reads and clears the device error word of the current device (synchronous:
+ * waits for all work on the device).  0 = no fault.  A kernel sets it instead
+ * of hanging when one of its bounded waits runs out.  Returns KDA_ERR_CUDA if
+ * the read itself fails.
+ */
+KDA_API kda_status kda_device_error(unsigned int* code);
+
+/* Library version, e.g. "0.1.0". */
+KDA_API const char* kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

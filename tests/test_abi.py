@@ -1,0 +1,94 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry point and
+rejects bad arguments on the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gated_delta_rule_53_gb300 import build
+    build.build()
+    import gated_delta_rule_53_gb300 as kda
+    return kda.library()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"KDA_API\s+[\w\s\*]+?\b(kda_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_three_operations():
+    syms = declared_symbols()
+    for name in ("kda_shortconv_l2norm", "kda_chunk_fwd", "kda_recurrent_step"):
+        assert name in syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), f"{name} declared in kda.h but not exported"
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert lib.kda_status_string(code).startswith(b"KDA_")
+    assert lib.kda_version().decode().count(".") == 2
+
+
+P = ctypes.c_void_p
+
+
+def _chunk(lib, **over):
+    a = dict(q=P(4096), k=P(4096), v=P(4096), g=P(4096), beta=P(4096), init=None, cu=None, N=1, T=64, H=2,
+             dk=128, dv=128, scale=1.0, chunk=64, dtype=1, gate=None, o=P(4096), fs=None, stream=None)
+    a.update(over)
+    return lib.kda_chunk_fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["init"], a["cu"], a["N"], a["T"], a["H"],
+                             a["dk"], a["dv"], a["scale"], a["chunk"], a["dtype"], a["gate"], a["o"], a["fs"],
+                             a["stream"])
+
+
+def test_chunk_fwd_rejects_bad_arguments(lib):
+    INVALID, UNSUPPORTED = 1, 2
+    assert _chunk(lib, q=None) == INVALID
+    assert _chunk(lib, o=P(4100)) == INVALID                 # misaligned
+    assert _chunk(lib, dk=64) == UNSUPPORTED
+    assert _chunk(lib, chunk=32) == UNSUPPORTED
+    assert _chunk(lib, N=2) == INVALID                       # several sequences need cu_seqlens
+    assert _chunk(lib, N=0) == INVALID
+    assert _chunk(lib, T=-1) == INVALID
+    assert _chunk(lib, dtype=7) == INVALID
+    assert _chunk(lib, scale=float("nan")) == INVALID
+    assert b"must" in lib.kda_last_error()
+
+
+def test_shortconv_rejects_bad_arguments(lib):
+    def call(**over):
+        a = dict(x=P(4096), stride=256, w=P(4096), cu=None, N=1, T=5, H=2, d=128, cs_in=None, cs_out=None, eps=1e-6,
+                 dt=1, out=P(4096))
+        a.update(over)
+        return lib.kda_shortconv_l2norm(a["x"], a["x"], a["x"], a["stride"], a["w"], a["cu"], a["N"], a["T"],
+                                        a["H"], a["d"], a["cs_in"], a["cs_out"], a["eps"], a["dt"], a["out"],
+                                        a["out"], a["out"], None)
+    assert call(x=None) == 1
+    assert call(stride=200) == 1          # < H*d
+    assert call(stride=260) == 1          # not a multiple of 8
+    assert call(d=64) == 2
+    assert call(eps=-1.0) == 1
+    assert call(cs_in=P(4097)) == 1
+
+
+def test_recurrent_step_rejects_bad_arguments(lib):
+    def call(**over):
+        a = dict(x=P(4096), stride=256, p=P(4096), N=4, H=2, dk=128, dv=128)
+        a.update(over)
+        return lib.kda_recurrent_step(a["x"], a["x"], a["x"], a["stride"], a["p"], a["p"], a["p"], a["p"], a["p"],
+                                      a["N"], a["H"], a["dk"], a["dv"], 1.0, 1e-6, a["p"], None)
+    assert call(p=None) == 1
+    assert call(N=0) == 1
+    assert call(dv=96) == 2
+    assert call(stride=8) == 1

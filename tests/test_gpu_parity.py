@@ -1,0 +1,306 @@
+"""GPU parity: the CUDA library (through its C ABI) against the fp64 oracle on the same
+seeded inputs.
+
+Tolerances (element by element over whole tensors unless noted):
+  * bf16 prefill and decode: o rel-L2 <= 5e-3 and max-abs <= 2e-2, state rel-L2 <= 5e-3.
+  * fp32 prefill: rel-L2 <= 1e-4 on o and on the final state.
+  * conv_state: bit-exact (it is a copy of raw inputs).
+  * front end: fp32 outputs rel-L2 <= 1e-5 (fp32 arithmetic on bf16 inputs, a handful
+    of roundings per element); bf16 outputs rel-L2 <= 5e-3 and max relative error per
+    element <= 2^-8 + 1e-5 (one bf16 rounding, 2^-9, plus fp32 noise).
+The oracle consumes exactly the bits the GPU receives, widened to fp64.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import kda_synth as ks
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+BF16_O_REL, BF16_O_ABS, BF16_S_REL = 5e-3, 2e-2, 5e-3
+F32_REL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def kda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_delta_rule_53_gb300 import build
+    build.build()
+    import gated_delta_rule_53_gb300 as m
+    return m
+
+
+@pytest.fixture(scope="module")
+def orc():
+    import oracle
+    oracle.build()
+    return oracle
+
+
+def dev(a):
+    from kda_synth.device import to_device
+    return to_device(a)
+
+
+def host(t):
+    from kda_synth.device import to_host_f64
+    return to_host_f64(t)
+
+
+def small_prefill(seed, lengths, H, dtype, init_std=0.0, g_kind=ks.NEG5_SIGMOID):
+    w = ks.Workload("small", "prefill", seed, H=H, lengths=list(lengths), dtype=dtype, g_kind=g_kind,
+                    init_state_std=init_std)
+    q, k, v, g, b = w.qkv("q"), w.qkv("k"), w.qkv("v"), w.g(), w.beta()
+    s0 = w.init_state()
+    return w, q, k, v, g, b, s0
+
+
+def run_chunk(kda, w, q, k, v, g, b, s0, scale=1.0, gate=None):
+    cu = dev(w.cu_seqlens()) if w.N > 1 else None
+    o, fs = kda.kda_chunk_fwd(dev(q), dev(k), dev(v), dev(g), dev(b), None if s0 is None else dev(s0), cu,
+                              scale=scale, out_gate=None if gate is None else dev(gate))
+    torch.cuda.synchronize()
+    return o, fs
+
+
+def oracle_chunk(orc, w, q, k, v, g, b, s0, scale=1.0, gate=None):
+    cu = w.cu_seqlens() if w.N > 1 else None
+    o, fs = orc.kda_tokenloop(ks.to_f64(q), ks.to_f64(k), ks.to_f64(v), g, b, s0, cu, scale)
+    if gate is not None:
+        o = orc.output_gate(o, ks.to_f64(gate))
+    return o, fs
+
+
+# ------------------------------------------------------------------------------------------
+# kda_chunk_fwd
+# ------------------------------------------------------------------------------------------
+
+def test_chunk_fp32_tiny_workload(kda, orc):
+    """The tiny fp32 workload: H=4, T=256, chunk 64, zero initial state."""
+    w = ks.workload("tiny_fp32")
+    q, k, v, g, b = w.qkv("q"), w.qkv("k"), w.qkv("v"), w.g(), w.beta()
+    o, fs = run_chunk(kda, w, q, k, v, g, b, None)
+    o_ref, fs_ref = oracle_chunk(orc, w, q, k, v, g, b, None)
+    assert orc.rel_l2(host(o), o_ref) <= F32_REL
+    assert orc.rel_l2(host(fs), fs_ref) <= F32_REL
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_chunk_ragged_varlen_with_state_and_scale(kda, orc, dtype):
+    lengths = [1, 63, 64, 65, 130, 0, 7]
+    w, q, k, v, g, b, s0 = small_prefill(101, lengths, 3, dtype, init_std=0.02)
+    scale = 1.0 / math.sqrt(128)
+    o, fs = run_chunk(kda, w, q, k, v, g, b, s0, scale=scale)
+    o_ref, fs_ref = oracle_chunk(orc, w, q, k, v, g, b, s0, scale=scale)
+    if dtype == "f32":
+        assert orc.rel_l2(host(o), o_ref) <= F32_REL and orc.rel_l2(host(fs), fs_ref) <= F32_REL
+    else:
+        assert orc.rel_l2(host(o), o_ref) <= BF16_O_REL and orc.max_abs(host(o), o_ref) <= BF16_O_ABS
+        assert orc.rel_l2(host(fs), fs_ref) <= BF16_S_REL
+    # the empty sequence keeps its initial state exactly
+    assert torch.equal(fs[5], dev(s0)[5])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_chunk_output_gate(kda, orc, dtype):
+    w, q, k, v, g, b, s0 = small_prefill(102, [200], 2, dtype, g_kind=ks.NEG_SOFTPLUS5)
+    gate = ks.fill(102, ks.TID_GATE, ks.NORMAL, (w.T, w.H * w.d), "bf16")
+    o, fs = run_chunk(kda, w, q, k, v, g, b, None, gate=gate)
+    o_ref, fs_ref = oracle_chunk(orc, w, q, k, v, g, b, None, gate=gate)
+    tol = F32_REL if dtype == "f32" else BF16_O_REL
+    assert orc.rel_l2(host(o), o_ref) <= tol and orc.rel_l2(host(fs), fs_ref) <= tol
+
+
+def test_chunk_final_state_may_alias_initial(kda, orc):
+    w, q, k, v, g, b, s0 = small_prefill(103, [70, 5], 2, "f32", init_std=0.02)
+    s = dev(s0)
+    o, fs = kda.kda_chunk_fwd(dev(q), dev(k), dev(v), dev(g), dev(b), s, dev(w.cu_seqlens()), final_state=s)
+    torch.cuda.synchronize()
+    o_ref, fs_ref = oracle_chunk(orc, w, q, k, v, g, b, s0)
+    assert orc.rel_l2(host(s), fs_ref) <= F32_REL
+
+
+def test_chunk_every_output_written_and_deterministic(kda):
+    w, q, k, v, g, b, s0 = small_prefill(104, [129, 3], 2, "bf16", init_std=0.02)
+    args = [dev(x) for x in (q, k, v, g, b, s0)]
+    o1 = torch.full((w.T, w.H, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    f1 = torch.full((2, w.H, 128, 128), float("nan"), device="cuda")
+    kda.kda_chunk_fwd(*args, dev(w.cu_seqlens()), o=o1, final_state=f1)
+    o2, f2 = kda.kda_chunk_fwd(*args, dev(w.cu_seqlens()))
+    torch.cuda.synchronize()
+    assert not torch.isnan(o1).any() and not torch.isnan(f1).any()
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
+
+
+def test_chunk_causality(kda):
+    w, q, k, v, g, b, s0 = small_prefill(105, [150], 2, "bf16")
+    o1, _ = run_chunk(kda, w, q, k, v, g, b, None)
+    v2 = v.copy()
+    v2[90:] = ks.f32_to_bf16(ks.bf16_to_f32(v2[90:]) + 1.0)
+    o2, _ = run_chunk(kda, w, q, k, v2, g, b, None)
+    assert torch.equal(o1[:90], o2[:90]) and not torch.equal(o1[90:], o2[90:])
+
+
+def test_chunk_packed_equals_separate(kda):
+    lengths = [33, 64, 100]
+    w, q, k, v, g, b, s0 = small_prefill(106, lengths, 2, "bf16", init_std=0.02)
+    o, fs = run_chunk(kda, w, q, k, v, g, b, s0)
+    cu = w.cu_seqlens()
+    for n in range(len(lengths)):
+        sl = slice(cu[n], cu[n + 1])
+        o1, f1 = kda.kda_chunk_fwd(dev(q[sl]), dev(k[sl]), dev(v[sl]), dev(g[sl]), dev(b[sl]), dev(s0[n:n + 1]))
+        assert torch.equal(o1, o[sl]) and torch.equal(f1[0], fs[n])
+
+
+# ------------------------------------------------------------------------------------------
+# kda_shortconv_l2norm
+# ------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+def test_shortconv_varlen_with_state(kda, orc, out_dtype):
+    H, d = 3, 128
+    C = H * d
+    lengths = [1, 2, 17, 0, 40]
+    T, N = sum(lengths), len(lengths)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    width = C + 8   # a row stride larger than H*d
+    xs = [ks.fill(201, tid, ks.NORMAL, (T, width), "bf16") for tid in (1, 2, 3)]
+    w = ks.fill(201, ks.TID_CONV_W, ks.NORMAL, (3 * C, 4), "bf16", 0.0, 0.25)
+    cs = ks.fill(201, ks.TID_CONV_STATE, ks.NORMAL, (N, 3, 3 * C), "bf16")
+    tdt = torch.float32 if out_dtype == "f32" else torch.bfloat16
+    cs_out = torch.empty((N, 3, 3 * C), dtype=torch.bfloat16, device="cuda")
+    q, k, v = kda.kda_shortconv_l2norm(*(dev(x) for x in xs), dev(w), H, dev(cu), dev(cs), cs_out, out_dtype=tdt)
+    torch.cuda.synchronize()
+    rq, rk, rv, rcs = orc.shortconv_silu_l2norm(*(ks.to_f64(x)[:, :C] for x in xs), ks.to_f64(w), H, d, cu,
+                                                ks.to_f64(cs))
+    for got, ref in ((q, rq), (k, rk), (v, rv)):
+        g64 = host(got)
+        if out_dtype == "f32":
+            assert orc.rel_l2(g64, ref) <= 1e-5
+        else:
+            assert orc.rel_l2(g64, ref) <= 5e-3
+            assert np.max(np.abs(g64 - ref) / np.maximum(np.abs(ref), 1e-30)) <= 2.0 ** -8 + 1e-5
+    assert np.array_equal(cs_out.view(torch.int16).cpu().numpy().view(np.uint16), ks.f32_to_bf16(rcs))
+
+
+def test_shortconv_state_in_place(kda, orc):
+    H, d, C = 2, 128, 256
+    lengths = [5, 1]
+    T, N = 6, 2
+    cu = np.array([0, 5, 6], np.int32)
+    xs = [ks.fill(202, tid, ks.NORMAL, (T, C), "bf16") for tid in (1, 2, 3)]
+    w = ks.fill(202, ks.TID_CONV_W, ks.NORMAL, (3 * C, 4), "bf16", 0.0, 0.25)
+    cs = ks.fill(202, ks.TID_CONV_STATE, ks.NORMAL, (N, 3, 3 * C), "bf16")
+    cs_dev = dev(cs)
+    kda.kda_shortconv_l2norm(*(dev(x) for x in xs), dev(w), H, dev(cu), cs_dev, cs_dev)
+    torch.cuda.synchronize()
+    _, _, _, rcs = orc.shortconv_silu_l2norm(*(ks.to_f64(x) for x in xs), ks.to_f64(w), H, d, cu, ks.to_f64(cs))
+    assert np.array_equal(cs_dev.view(torch.int16).cpu().numpy().view(np.uint16), ks.f32_to_bf16(rcs))
+
+
+# ------------------------------------------------------------------------------------------
+# kda_recurrent_step
+# ------------------------------------------------------------------------------------------
+
+def decode_inputs(w):
+    xs = [ks.fill(w.seed, tid, ks.NORMAL, (w.N, w.H * w.d), "bf16") for tid in (1, 2, 3)]
+    g = ks.fill(w.seed, ks.TID_G, w.g_kind, (w.N, w.H, w.d), "f32")
+    b = ks.fill(w.seed, ks.TID_BETA, ks.SIGMOID, (w.N, w.H), "f32")
+    return xs, w.conv_w(), g, b, w.init_state(), w.conv_state()
+
+
+def check_decode(kda, orc, w, scale=1.0, steps=1):
+    xs, cw, g, b, s0, cs = decode_inputs(w)
+    s_dev, cs_dev = dev(s0), dev(cs)
+    s_ref, cs_ref = s0.astype(np.float64), ks.to_f64(cs)
+    for step in range(steps):
+        if step:  # fresh tokens for later steps
+            xs = [ks.fill(w.seed + 1000 * step, tid, ks.NORMAL, (w.N, w.H * w.d), "bf16") for tid in (1, 2, 3)]
+        o = kda.kda_recurrent_step(*(dev(x) for x in xs), dev(cw), dev(g), dev(b), s_dev, cs_dev, scale=scale)
+        torch.cuda.synchronize()
+        o_ref, s_ref, cs_ref = orc.recurrent_step(*(ks.to_f64(x) for x in xs), ks.to_f64(cw), g, b, s_ref, cs_ref,
+                                                  w.H, w.d, scale)
+        assert orc.rel_l2(host(o), o_ref) <= BF16_O_REL and orc.max_abs(host(o), o_ref) <= BF16_O_ABS
+        assert orc.rel_l2(host(s_dev), s_ref) <= BF16_S_REL
+        assert np.array_equal(host(cs_dev), cs_ref)   # bf16 widened exactly: bit-exact
+
+
+def test_decode_small(kda, orc):
+    w = ks.Workload("d", "decode", 301, H=3, lengths=[1] * 5, init_state_std=0.02)
+    check_decode(kda, orc, w, scale=0.5, steps=8)
+
+
+def test_decode_full_workload(kda, orc):
+    """64 sequences x 96 heads, fp32 state N(0, 0.02), the whole step checked."""
+    check_decode(kda, orc, ks.workload("decode_64"))
+
+
+def test_prefill_equals_repeated_decode(kda):
+    """Front end + chunkwise prefill over T tokens == T fused decode steps (bf16 bounds)."""
+    H, C, T = 2, 256, 70
+    xs = [ks.fill(302, tid, ks.NORMAL, (T, C), "bf16") for tid in (1, 2, 3)]
+    cw = ks.fill(302, ks.TID_CONV_W, ks.NORMAL, (3 * C, 4), "bf16", 0.0, 0.25)
+    cs0 = ks.fill(302, ks.TID_CONV_STATE, ks.NORMAL, (1, 3, 3 * C), "bf16")
+    g = ks.fill(302, ks.TID_G, ks.NEG5_SIGMOID, (T, H, 128), "f32")
+    b = ks.fill(302, ks.TID_BETA, ks.SIGMOID, (T, H), "f32")
+    s0 = ks.fill(302, ks.TID_STATE, ks.NORMAL, (1, H, 128, 128), "f32", 0.0, 0.02)
+    xd = [dev(x) for x in xs]
+    cs_pre = dev(cs0)
+    q, k, v = kda.kda_shortconv_l2norm(*xd, dev(cw), H, None, cs_pre, cs_pre)
+    o_pre, fs = kda.kda_chunk_fwd(q, k, v, dev(g), dev(b), dev(s0))
+    s, cs = dev(s0), dev(cs0)
+    outs = []
+    for t in range(T):
+        outs.append(kda.kda_recurrent_step(*(x[t:t + 1] for x in xd), dev(cw), dev(g[t:t + 1]), dev(b[t:t + 1]),
+                                           s, cs))
+    torch.cuda.synchronize()
+    o_dec = torch.cat(outs).float()
+    rel = (o_dec - o_pre.float()).norm() / o_dec.norm()
+    assert rel <= BF16_O_REL
+    assert ((s - fs).norm() / s.norm()) <= BF16_S_REL
+    assert torch.equal(cs, cs_pre)
+
+
+# ------------------------------------------------------------------------------------------
+# full-size workloads, checked on sampled heads / chains
+# ------------------------------------------------------------------------------------------
+
+def fill_dev(w, tid, kind, shape, dtype, p0=0.0, p1=1.0):
+    from kda_synth.device import fill_device
+    return fill_device(w.seed, tid, kind, shape, dtype, p0, p1)
+
+
+def head_inputs(w, h, t0, t1):
+    """Oracle inputs of head h, tokens [t0, t1): regenerated from the counter-based streams."""
+    d, H = w.d, w.H
+    q = w.head_rows(ks.TID_Q, ks.UNIT_GROUPS, h, w.dtype, p1=float(d), t0=t0, t1=t1)
+    k = w.head_rows(ks.TID_K, ks.UNIT_GROUPS, h, w.dtype, p1=float(d), t0=t0, t1=t1)
+    v = w.head_rows(ks.TID_V, ks.NORMAL, h, w.dtype, t0=t0, t1=t1)
+    g = w.head_rows(ks.TID_G, w.g_kind, h, "f32", t0=t0, t1=t1)
+    b = w.head_beta(h, t0, t1)
+    ex = lambda a: ks.to_f64(a)[:, None, :]
+    return ex(q), ex(k), ex(v), g.astype(np.float64)[:, None, :], b.astype(np.float64)[:, None]
+
+
+def test_prefill_8k_sampled_heads(kda, orc):
+    """H=96, T=8192 bf16 prefill as the benchmark launches it; heads 0, 37, 95 checked in full."""
+    w = ks.workload("prefill_8k")
+    T, H, d = w.T, w.H, w.d
+    q = fill_dev(w, ks.TID_Q, ks.UNIT_GROUPS, (T, H, d), "bf16", 0.0, float(d))
+    k = fill_dev(w, ks.TID_K, ks.UNIT_GROUPS, (T, H, d), "bf16", 0.0, float(d))
+    v = fill_dev(w, ks.TID_V, ks.NORMAL, (T, H, d), "bf16")
+    g = fill_dev(w, ks.TID_G, w.g_kind, (T, H, d), "f32")
+    b = fill_dev(w, ks.TID_BETA, ks.SIGMOID, (T, H), "f32")
+    o, fs = kda.kda_chunk_fwd(q, k, v, g, b)
+    torch.cuda.synchronize()
+    assert not torch.isnan(o).any()
+    for h in (0, 37, 95):
+        qh, kh, vh, gh, bh = head_inputs(w, h, 0, T)
+        o_ref, fs_ref = orc.kda_tokenloop(qh, kh, vh, gh, bh)
+        o_h = host(o[:, h:h + 1, :])
+        assert orc.rel_l2(o_h, o_ref) <= BF16_O_REL and orc.max_abs(o_h, o_ref) <= BF16_O_ABS
+        assert orc.rel_l2(host(fs[:, h:h + 1]), fs_ref) <= BF16_S_REL
