@@ -1,0 +1,69 @@
+"""Profiling harness: runs one entry point of the library on a named synthetic case a
+few times, so that a profiler can capture a handful of launches of one kernel.
+
+  python -m gated_delta_rule_53_gb300.profile {prefill_8k,prefill_2k,decode_64,decode_16,frontend_8k} [--iters N]
+
+Cases (all inputs larger than the 129 MB L2, a few GB on the device at most):
+  prefill_8k   kda_chunk_fwd, 1 x 8192 tokens x 96 heads, bf16
+  prefill_2k   kda_chunk_fwd, 1 x 2048 tokens x 96 heads, bf16
+  decode_64    kda_recurrent_step, 64 sequences x 96 heads
+  decode_16    kda_recurrent_step, 16 sequences x 96 heads
+  frontend_8k  kda_shortconv_l2norm, 8192 tokens x 96 heads, bf16 out
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def main():
+    import torch
+
+    import gated_delta_rule_53_gb300 as kda
+    import kda_synth as ks
+    from kda_synth.device import fill_device
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=["prefill_8k", "prefill_2k", "decode_64", "decode_16", "frontend_8k"])
+    ap.add_argument("--iters", type=int, default=3)
+    args = ap.parse_args()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    if args.case.startswith("prefill"):
+        T = 8192 if args.case == "prefill_8k" else 2048
+        w = ks.Workload(args.case, "prefill", 53002, H=96, lengths=[T])
+        q = fill_device(w.seed, ks.TID_Q, ks.UNIT_GROUPS, (T, 96, 128), "bf16", 0.0, 128.0, device=dev)
+        k = fill_device(w.seed, ks.TID_K, ks.UNIT_GROUPS, (T, 96, 128), "bf16", 0.0, 128.0, device=dev)
+        v = fill_device(w.seed, ks.TID_V, ks.NORMAL, (T, 96, 128), "bf16", device=dev)
+        g = fill_device(w.seed, ks.TID_G, w.g_kind, (T, 96, 128), "f32", device=dev)
+        b = fill_device(w.seed, ks.TID_BETA, ks.SIGMOID, (T, 96), "f32", device=dev)
+        fn = lambda: kda.kda_chunk_fwd(q, k, v, g, b)
+    elif args.case.startswith("decode"):
+        N = 64 if args.case == "decode_64" else 16
+        w = ks.Workload(args.case, "decode", 53003, H=96, lengths=[1] * N, init_state_std=0.02)
+        C = 96 * 128
+        xs = [fill_device(w.seed, t, ks.NORMAL, (N, C), "bf16", device=dev) for t in (1, 2, 3)]
+        cw = fill_device(w.seed, ks.TID_CONV_W, ks.NORMAL, (3 * C, 4), "bf16", 0.0, 0.25, device=dev)
+        g = fill_device(w.seed, ks.TID_G, w.g_kind, (N, 96, 128), "f32", device=dev)
+        b = fill_device(w.seed, ks.TID_BETA, ks.SIGMOID, (N, 96), "f32", device=dev)
+        st = fill_device(w.seed, ks.TID_STATE, ks.NORMAL, (N, 96, 128, 128), "f32", 0.0, 0.02, device=dev)
+        cs = fill_device(w.seed, ks.TID_CONV_STATE, ks.NORMAL, (N, 3, 3 * C), "bf16", device=dev)
+        fn = lambda: kda.kda_recurrent_step(*xs, cw, g, b, st, cs)
+    else:
+        T, C = 8192, 96 * 128
+        xs = [fill_device(53005, t, ks.NORMAL, (T, C), "bf16", device=dev) for t in (1, 2, 3)]
+        cw = fill_device(53005, ks.TID_CONV_W, ks.NORMAL, (3 * C, 4), "bf16", 0.0, 0.25, device=dev)
+        fn = lambda: kda.kda_shortconv_l2norm(*xs, cw, 96)
+    for _ in range(args.iters):
+        fn()
+    torch.cuda.synchronize()
+    print(f"{args.case}: {args.iters} iterations ok")
+
+
+if __name__ == "__main__":
+    main()
