@@ -84,7 +84,7 @@ def smi_index(local_rank: int) -> str:
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms during the timed region."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -99,7 +99,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200", "-i", str(self.gpu_index)], stdout=subprocess.PIPE,
+                                          "-lms", "50", "-i", str(self.gpu_index)], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -270,8 +270,10 @@ def run_ours(args):
     dstep = lambda: kda.kda_recurrent_step(*xs, cw, gd, bd, st, cs, o=od, stream=stream)
     dclocks = ClockSampler(smi_index(local))
     dclocks.start()
-    dsteps = max(args.steps, 50)
-    ms_dec, ms_dec_launch, _ = timed(dstep, dsteps, args.warmup, stream, dist)
+    # the decode step is ~0.1 ms: time enough of them for the clock sampler to see the region
+    _, probe_ms, _ = timed(dstep, 20, args.warmup, stream, dist)
+    dsteps = max(args.steps, int(1.0 / max(probe_ms * 1e-3, 1e-6)))
+    ms_dec, ms_dec_launch, _ = timed(dstep, dsteps, 0, stream, dist)
     dclk = dclocks.stop()
     dbytes = decode_bytes(wd.N, wd.H)
     dec_gbs = dbytes / (ms_dec_launch * 1e-3) / 1e9
@@ -404,7 +406,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="prefill_8k", choices=["prefill_8k"])

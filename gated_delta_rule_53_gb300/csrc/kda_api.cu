@@ -3,6 +3,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cmath>
+#include <mutex>
 
 #include "kda_common.cuh"
 
@@ -24,6 +25,24 @@ kda_status set_error(kda_status s, const char* fmt, ...) {
 }  // namespace kda
 
 __device__ unsigned int g_kda_device_error = 0;
+
+namespace kda {
+
+unsigned int* device_error_word() {
+    static std::mutex mu;
+    static unsigned int* cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_kda_device_error) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<unsigned int*>(p);
+    }
+    return cache[dev];
+}
+
+}  // namespace kda
 
 using kda::set_error;
 
@@ -133,8 +152,12 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const floa
         return set_error(KDA_ERR_UNSUPPORTED, "only chunk_size = 64 is supported (got %d)", chunk_size);
     REQUIRE(dtype == KDA_DTYPE_F32 || dtype == KDA_DTYPE_BF16, "bad dtype");
     REQUIRE(std::isfinite(scale), "scale must be finite");
-    return from_cuda(kda::launch_chunk_simt(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, scale, dtype,
-                                            out_gate, o, final_state, static_cast<cudaStream_t>(stream)),
+    if (dtype == KDA_DTYPE_F32)
+        return from_cuda(kda::launch_chunk_simt(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, scale, dtype,
+                                                out_gate, o, final_state, static_cast<cudaStream_t>(stream)),
+                         "kda_chunk_fwd launch");
+    return from_cuda(kda::launch_chunk_tc(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, scale, out_gate, o,
+                                          final_state, kda::device_error_word(), static_cast<cudaStream_t>(stream)),
                      "kda_chunk_fwd launch");
 }
 

@@ -87,4 +87,12 @@ cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, const
                               int H, float scale, kda_dtype dtype, const void* out_gate, void* o,
                               float* final_state, cudaStream_t stream);
 
+cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                            const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
+                            float scale, const void* out_gate, void* o, float* final_state, unsigned int* err,
+                            cudaStream_t stream);
+
+// Device address of the library's error word on the current device (nullptr if unavailable).
+unsigned int* device_error_word();
+
 }  // namespace kda
