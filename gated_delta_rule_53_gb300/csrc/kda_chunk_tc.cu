@@ -11,26 +11,33 @@
 //   S    = S0 Diag(e^{G_C}) + V'^T (K . e^{G_C - G})
 //
 // Dense intra-chunk blocks.  The position-pair factor e^{G_ic - G_jc} is split
-// as e^{G_ic - R_c} e^{R_c - G_jc} around a reference R, which turns each block
-// into a plain matrix product.  With the log-decay bounded below by -5 ("Kimi K3
+// around a reference as e^{G_ic - R_c} e^{R_c - G_jc}, which turns each block of
+// A into a plain matrix product.  With the log-decay bounded below by -5 ("Kimi K3
 // 架构全景", section 02: gate lower_bound -5.0; "月之暗面发布Kimi K3开源大模型技术
 // 报告", 架构: the bound lets the diagonal blocks run as dense tensor-core
-// products), 16 tokens span at most 5 * 15 = 75 in the exponent, and e^75 fits
-// fp32 / bf16 (max ~ e^88.7).  Column block J (16 tokens) uses R = G at its last
-// token: the column factor e^{R - G_j} is in [e^-75, 1], the row factor of a row
-// in block J is in [1, e^75], and rows of later blocks get factors <= 1 whose
-// underflow only drops terms that are below e^-87 in truth.  So A_kk and A_qk
-// are four M=128 (64 k-rows + 64 q-rows) x N=16 x K=128 MMAs, one per column block.
+// products), a 16-token block spans at most 5 * 15 = 75 in the exponent and e^75
+// fits fp32 and bf16 (max ~ e^88.7).  Row block I (tokens 16I .. 16I+15) takes
+// R = E_I, the value of G at its last token:
+//   row operand     x_i e^{G_i - E_I(i)}     in [1, e^75] x |x|   (one operand for all I)
+//   column operand  k_j e^{E_I - G_j}        <= |k|, for j <= 16I + 15
+// so row block I of A_kk and A_qk is one MMA of M = 128 (64 k-rows on top of 64
+// q-rows) x N = 16(I+1) x K = 128, and the four are issued together.  A column
+// factor that underflows fp32 (below e^-87.3) drops a term smaller than e^-12.3
+// |x k| against a row factor of at most e^75: at most 4.5e-6 per entry of A, far
+// under the bf16 rounding of the operands.  The column operand of block 3 is
+// K e^{G_C - G}, the same tile the state update uses.
 //
 // State path.  S0 (fp32) lives in registers: thread (r, half) of the 256 holds
 // row r, key channels [64 half, 64 half + 64); a bf16 copy in shared memory is
 // the A operand of the S0 products, so every product has M = 128 = dv and maps
-// row r to TMEM lane r.  The UT solve (I + A_kk)^-1 runs in fp32 on the CUDA
-// cores.  All tensor-core products take bf16 operands and accumulate in fp32.
+// row r to TMEM lane r.  All tensor-core products take bf16 operands and
+// accumulate in fp32 in TMEM.  T = (I + A_kk)^-1 is computed in fp32 on the CUDA
+// cores by 16 x 16 blocks: the four diagonal blocks by forward substitution, then
+// the blocks below them level by level, T_IJ = -T_II sum_{M=J..I-1} A_IM T_MJ.
 //
-// This first tensor-core version runs the phases of a chunk one after another
-// in one CTA per (sequence, head); operands are written to shared memory by the
-// threads (all of them are decay-scaled), so no operand comes raw from memory.
+// One CTA per (sequence, head) walks the chunks in order.  The next chunk's
+// inputs are copied into shared memory with cp.async while the current chunk
+// computes (k, q, g once the operands are built, v once Z is built).
 #include "kda_common.cuh"
 #include "kda_tc.cuh"
 
@@ -42,34 +49,47 @@ using namespace tc;
 constexpr int kThreads = 256;
 constexpr int kC = kChunk;    // 64
 constexpr int kD = kHeadDim;  // 128
-constexpr int kAStride = 65;  // fp32 row stride of A_kk / T work arrays
+constexpr int kAS = 68;       // fp32 row stride of the A_kk / T work arrays (float4 rows on distinct banks)
 constexpr uint32_t kWaitLimit = 1u << 22;
 
-// shared-memory map (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_STK = 0;          // k staging bf16 [64][128]   | later Z^T / V'^T operand [128][64]
-constexpr uint32_t OFF_STQ = 16384;      // q staging bf16 [64][128]   | later T operand [64][64] and A_qk [64][64]
-constexpr uint32_t OFF_STV = 32768;      // v staging bf16 [64][128]
-constexpr uint32_t OFF_STG = 49152;      // g -> G fp32 [64][128]      | later T fp32 work [64][65]
-constexpr uint32_t OFF_KT = 81920;       // K~ operand [64][128]  (2 regions of 8 KB)
-constexpr uint32_t OFF_B1 = 98304;       // [beta K e^G ; Q e^G] operand [128][128] (2 regions of 16 KB)
-constexpr uint32_t OFF_KP = 131072;      // K e^{G_C - G} operand [64 tokens][128] (MN-major B)
-constexpr uint32_t OFF_R = 147456;       // row operand of column block J [128][128] | later A_kk fp32 [64][65]
-constexpr uint32_t OFF_S = 180224;       // bf16 S0 operand [128][128]
-constexpr uint32_t OFF_BETA = 212992;    // fp32 [64]
-constexpr uint32_t OFF_GEND = OFF_BETA + 256;     // fp32 [4][128] G at the end of each 16-token block
-constexpr uint32_t OFF_EGL = OFF_GEND + 2048;     // fp32 [128] e^{G_C}
-constexpr uint32_t OFF_BAR = OFF_EGL + 512;       // mbarrier
-constexpr uint32_t OFF_MISC = OFF_BAR + 16;       // TMEM base, abort flag
+// shared-memory map (bytes from a 1024-aligned base); "|" = reuse later in the chunk
+constexpr uint32_t OFF_STK = 0;        // k staging bf16 [64][128]
+constexpr uint32_t OFF_STQ = 16384;    // q staging bf16 [64][128]
+constexpr uint32_t OFF_STV = 32768;    // v staging bf16 [64][128]
+constexpr uint32_t OFF_STG = 49152;    // g -> G fp32 [64][128]
+constexpr uint32_t OFF_B1 = 81920;     // [beta K e^G ; Q e^G] [128][128] | A_qk bf16 [64][64], T fp32, level scratch
+constexpr uint32_t OFF_KP = 114688;    // K e^{G_C - G} [64][128]: column operand of row block 3, B of dS
+constexpr uint32_t OFF_RR = 131072;    // row operand [K e^{G-E} ; Q e^{G-E}] [128][128] | A_kk fp32 | O fp32 [64][128]
+constexpr uint32_t OFF_CC = 163840;    // column operands of row blocks 0..2 (16, 32, 48 rows) | Z^T / V'^T, T bf16
+constexpr uint32_t OFF_S = 188416;     // bf16 S0 [128][128]
+constexpr uint32_t OFF_SMALL = 221184;
+constexpr uint32_t OFF_BETA = OFF_SMALL;             // fp32 [2][64] (double-buffered)
+constexpr uint32_t OFF_E = OFF_BETA + 512;           // fp32 [4][128] E_I = G at the last token of block I
+constexpr uint32_t OFF_DT = OFF_E + 2048;            // fp32 [6][128] e^{E_J - E_I}, J > I
+constexpr uint32_t OFF_EGL = OFF_DT + 3072;          // fp32 [128] e^{G_C}
+constexpr uint32_t OFF_BAR = OFF_EGL + 512;          // mbarrier
+constexpr uint32_t OFF_MISC = OFF_BAR + 16;          // TMEM base, abort flag
 constexpr uint32_t kSmemUsed = OFF_MISC + 64;
-constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // slack for aligning the base
+
+constexpr uint32_t OFF_AQ = OFF_B1;                  // A_qk operand [64][64]     (8 KB)
+constexpr uint32_t OFF_TF = OFF_B1 + 8192;           // T fp32 [64][kAS]           (17 KB)
+constexpr uint32_t OFF_YS = OFF_B1 + 8192 + 64 * kAS * 4;  // level scratch fp32 [3][16][16]
+constexpr uint32_t OFF_Z = OFF_CC;                   // Z^T, then V'^T [128][64]   (16 KB)
+constexpr uint32_t OFF_TB = OFF_CC + 16384;          // T operand [64][64]         (8 KB)
+// column operand of row block I < 3: 16(I+1) rows, two regions of 16(I+1) * 128 bytes
+__host__ __device__ constexpr uint32_t cc_off(int I) { return I == 0 ? 0u : (I == 1 ? 4096u : 12288u); }
 
 // TMEM columns
-constexpr uint32_t TM_A = 0;     // [A_kk raw ; A_qk raw] 64 columns
-constexpr uint32_t TM_V = 64;    // V'^T 64 columns
-constexpr uint32_t TM_Y = 128;   // Y^T = S0 (beta K e^G)^T 64 columns, then O^T 64 columns
-constexpr uint32_t TM_O = 192;
-constexpr uint32_t TM_DS = 256;  // delta S 128 columns
+constexpr uint32_t TM_A0 = 0, TM_A1 = 32, TM_A2 = 64, TM_A3 = 128;  // row blocks of A: 16, 32, 48, 64 columns
+constexpr uint32_t TM_V = 192;    // V'^T
+constexpr uint32_t TM_Y = 256;    // Y^T = S0 (beta K e^G)^T, then O^T at TM_O
+constexpr uint32_t TM_O = 320;
+constexpr uint32_t TM_DS = 384;   // delta S
 constexpr uint32_t kTmemCols = 512;
+
+static_assert(OFF_YS + 3 * 256 * 4 <= OFF_KP, "T work overflows its region");
+static_assert(kSmemBytes <= 232448, "shared memory");
 
 __device__ __forceinline__ void unpack8(uint4 u, float (&f)[8]) {
     f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x); f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
@@ -80,24 +100,58 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
     return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
 }
 
-// MMA with a K = 128 (two-region) A operand of 128 rows and a K-major B operand.
+// D (+)= A B^T with a K = 128 (two-region) A of 128 rows and a K-major two-region B.
 __device__ __forceinline__ void mma_k128(uint32_t d, uint32_t a_base, uint32_t a_region, uint32_t b_base,
-                                         uint32_t b_region, uint32_t idesc, bool accumulate_first) {
+                                         uint32_t b_region, uint32_t idesc) {
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
         const uint32_t reg = ks >> 2, off = (ks & 3) * 32;
         mma_bf16(d, sdesc_sw128(a_base + reg * a_region + off, 16, 1024), sdesc_sw128(b_base + reg * b_region + off, 16, 1024),
-                 idesc, (ks > 0 || accumulate_first) ? 1u : 0u);
+                 idesc, ks > 0 ? 1u : 0u);
     }
 }
 
-// MMA with a K = 64 (one-region) A operand and a K-major one-region B operand.
+// D (+)= A B^T with a K = 64 (one-region) A and a K-major one-region B.
 __device__ __forceinline__ void mma_k64(uint32_t d, uint32_t a_base, uint32_t b_base, uint32_t idesc,
                                         bool accumulate_first) {
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
         mma_bf16(d, sdesc_sw128(a_base + ks * 32, 16, 1024), sdesc_sw128(b_base + ks * 32, 16, 1024), idesc,
                  (ks > 0 || accumulate_first) ? 1u : 0u);
+}
+
+// cp.async of chunk [c0, c0 + L) of one head: k, q, g (and beta into beta_dst), or v.
+__device__ __forceinline__ void prefetch_kqg(uint8_t* sm, float* beta_dst, const __nv_bfloat16* k,
+                                             const __nv_bfloat16* q, const float* g, const float* beta, int64_t c0,
+                                             int L, int H, int h, int tid) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const int id = tid + kThreads * m, i = id >> 4, cc = id & 15;
+        const bool ok = i < L;
+        const int64_t at = ok ? ((c0 + i) * H + h) * kD + cc * 8 : 0;
+        cp_async16(sm + OFF_STK + i * 256 + cc * 16, k + at, ok ? 16u : 0u);
+        cp_async16(sm + OFF_STQ + i * 256 + cc * 16, q + at, ok ? 16u : 0u);
+    }
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const int id = tid + kThreads * m, i = id >> 5, cc = id & 31;
+        const bool ok = i < L;
+        cp_async16(sm + OFF_STG + i * 512 + cc * 16, g + (ok ? ((c0 + i) * H + h) * kD + cc * 4 : 0), ok ? 16u : 0u);
+    }
+    if (tid < kC) {
+        const bool ok = tid < L;
+        cp_async4(beta_dst + tid, beta + (ok ? (c0 + tid) * H + h : 0), ok ? 4u : 0u);
+    }
+}
+
+__device__ __forceinline__ void prefetch_v(uint8_t* sm, const __nv_bfloat16* v, int64_t c0, int L, int H, int h,
+                                           int tid) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const int id = tid + kThreads * m, i = id >> 4, cc = id & 15;
+        const bool ok = i < L;
+        cp_async16(sm + OFF_STV + i * 256 + cc * 16, v + (ok ? ((c0 + i) * H + h) * kD + cc * 8 : 0), ok ? 16u : 0u);
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -109,15 +163,18 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
-    float* sBeta = reinterpret_cast<float*>(sm + OFF_BETA);
-    float* sGend = reinterpret_cast<float*>(sm + OFF_GEND);
+    float* sBetaBuf = reinterpret_cast<float*>(sm + OFF_BETA);
+    float* sE = reinterpret_cast<float*>(sm + OFF_E);
+    float* sDt = reinterpret_cast<float*>(sm + OFF_DT);
     float* sEGl = reinterpret_cast<float*>(sm + OFF_EGL);
     uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
     volatile int* sAbort = reinterpret_cast<volatile int*>(sm + OFF_MISC + 4);
     float* sG = reinterpret_cast<float*>(sm + OFF_STG);
-    float* sAkk = reinterpret_cast<float*>(sm + OFF_R);
-    float* sTf = reinterpret_cast<float*>(sm + OFF_STG);
+    float* sAkk = reinterpret_cast<float*>(sm + OFF_RR);
+    float* sTf = reinterpret_cast<float*>(sm + OFF_TF);
+    float* sYs = reinterpret_cast<float*>(sm + OFF_YS);
+    float* sO = reinterpret_cast<float*>(sm + OFF_RR);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int chain = blockIdx.x, n = chain / H, h = chain % H;
@@ -133,6 +190,12 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         *sAbort = 0;
     }
     if (warp == 0) tmem_alloc(sTmem, kTmemCols);
+    if (bos < eos) {  // the first chunk's inputs
+        const int L0 = (eos - bos) < kC ? (int)(eos - bos) : kC;
+        prefetch_kqg(sm, sBetaBuf, k, q, g, beta, bos, L0, H, h, tid);
+        prefetch_v(sm, v, bos, L0, H, h, tid);
+        cp_async_commit();
+    }
 
     // state rows in registers, bf16 copy as the S0 operand
     float s[64];
@@ -166,253 +229,343 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         tc_fence_after();
     };
 
-    const uint32_t id_a = idesc_bf16_f32(128, 16, false, false);
     const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
     const uint32_t id_64 = idesc_bf16_f32(128, 64, false, false);
     const uint32_t id_ds = idesc_bf16_f32(128, 128, false, true);
 
-    for (int64_t c0 = bos; c0 < eos; c0 += kC) {
+    int buf = 0;
+    for (int64_t c0 = bos; c0 < eos; c0 += kC, buf ^= 1) {
         const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
-        // ---- (1) staging loads (rows past L are zero)
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int id = tid + kThreads * m, i = id >> 4, cc = id & 15;
-            uint4 uk = make_uint4(0, 0, 0, 0), uq = uk, uv = uk;
-            if (i < L) {
-                const int64_t at = ((c0 + i) * H + h) * kD + cc * 8;
-                uk = *reinterpret_cast<const uint4*>(k + at);
-                uq = *reinterpret_cast<const uint4*>(q + at);
-                uv = *reinterpret_cast<const uint4*>(v + at);
-            }
-            *reinterpret_cast<uint4*>(sm + OFF_STK + i * 256 + cc * 16) = uk;
-            *reinterpret_cast<uint4*>(sm + OFF_STQ + i * 256 + cc * 16) = uq;
-            *reinterpret_cast<uint4*>(sm + OFF_STV + i * 256 + cc * 16) = uv;
-        }
-#pragma unroll
-        for (int m = 0; m < 8; ++m) {
-            const int id = tid + kThreads * m, i = id >> 5, cc = id & 31;
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (i < L) x = *reinterpret_cast<const float4*>(g + ((c0 + i) * H + h) * kD + cc * 4);
-            *reinterpret_cast<float4*>(sm + OFF_STG + i * 512 + cc * 16) = x;
-        }
-        if (tid < kC) sBeta[tid] = tid < L ? beta[(c0 + tid) * H + h] : 0.f;
+        const int64_t c1 = c0 + kC;
+        const int L1 = c1 < eos ? ((eos - c1) < kC ? (int)(eos - c1) : kC) : 0;
+        const float* sBeta = sBetaBuf + 64 * buf;
+        cp_async_wait_all();
         __syncthreads();
-        // ---- (2) running sum of g per key channel; block-end references
-        if (tid < kD) {
+        // ---- (1) running sum of g per key channel (two halves of 32 tokens), block references
+        {
+            const int c = tid & 127, i0 = 32 * half;
             float acc = 0.f;
-#pragma unroll 16
-            for (int i = 0; i < kC; ++i) {
-                acc += sG[i * kD + tid];
-                sG[i * kD + tid] = acc;
-                if ((i & 15) == 15) sGend[(i >> 4) * kD + tid] = acc;
+#pragma unroll 8
+            for (int i = i0; i < i0 + 32; ++i) {
+                acc += sG[i * kD + c];
+                sG[i * kD + c] = acc;
             }
-            sEGl[tid] = expf(acc);
+            __syncthreads();
+            if (half == 1) {
+                const float base = sG[31 * kD + c];
+#pragma unroll 8
+                for (int i = 32; i < 64; ++i) sG[i * kD + c] += base;
+            }
+            __syncthreads();
+            if (half == 0) {
+                float e[4];
+#pragma unroll
+                for (int I = 0; I < 4; ++I) { e[I] = sG[(16 * I + 15) * kD + c]; sE[I * kD + c] = e[I]; }
+                sEGl[c] = expf(e[3]);
+                // e^{E_J - E_I}, J > I: (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
+                sDt[0 * kD + c] = __expf(e[1] - e[0]);
+                sDt[1 * kD + c] = __expf(e[2] - e[0]);
+                sDt[2 * kD + c] = __expf(e[3] - e[0]);
+                sDt[3 * kD + c] = __expf(e[2] - e[1]);
+                sDt[4 * kD + c] = __expf(e[3] - e[1]);
+                sDt[5 * kD + c] = __expf(e[3] - e[2]);
+            }
+            __syncthreads();
         }
-        __syncthreads();
-        // ---- (3) operands that do not depend on the column block, and the row operand of block 0
+        // ---- (2) operands: row operand RR, column operands CC / KP, B1 = [beta K e^G ; Q e^G]
 #pragma unroll 1
         for (int m = 0; m < 4; ++m) {
-            const int id = tid + kThreads * m, i = id >> 4, cc = id & 15, c = cc * 8;
+            const int id = tid + kThreads * m, i = id >> 4, cc = id & 15, c = cc * 8, I = i >> 4;
             const uint32_t reg = cc >> 3, ch = cc & 7;
-            float kv[8], qv[8], Gv[8];
+            float kv[8], qv[8], Gv[8], Ev[8];
             unpack8(*reinterpret_cast<const uint4*>(sm + OFF_STK + i * 256 + cc * 16), kv);
             unpack8(*reinterpret_cast<const uint4*>(sm + OFF_STQ + i * 256 + cc * 16), qv);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) Gv[e] = sG[i * kD + c + e];
+            *reinterpret_cast<float4*>(Gv) = *reinterpret_cast<const float4*>(sG + i * kD + c);
+            *reinterpret_cast<float4*>(Gv + 4) = *reinterpret_cast<const float4*>(sG + i * kD + c + 4);
+            *reinterpret_cast<float4*>(Ev) = *reinterpret_cast<const float4*>(sE + I * kD + c);
+            *reinterpret_cast<float4*>(Ev + 4) = *reinterpret_cast<const float4*>(sE + I * kD + c + 4);
             const float b = sBeta[i];
-            const float* gb = sGend + (i >> 4) * kD + c;
-            const float* gl = sGend + 3 * kD + c;
-            const float* g0 = sGend + c;
-            float f0[8], f1[8], f2[8], f3[8], f4[8], f5[8];
+            float rk[8], rq[8], bk[8], eq[8], kr[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const float eg = __expf(Gv[e]);
-                f0[e] = kv[e] * __expf(gb[e] - Gv[e]);    // K~
-                f1[e] = b * kv[e] * eg;                   // beta K e^G
-                f2[e] = qv[e] * eg;                       // Q e^G
-                f3[e] = kv[e] * __expf(gl[e] - Gv[e]);    // K e^{G_C - G}
-                const float r0 = __expf(Gv[e] - g0[e]);   // row factor of column block 0
-                f4[e] = kv[e] * r0;
-                f5[e] = qv[e] * r0;
+                const float f = __expf(Gv[e] - Ev[e]);   // >= 1
+                const float r = __expf(Ev[e] - Gv[e]);   // <= 1
+                const float eg = __expf(Gv[e]);          // <= 1
+                rk[e] = kv[e] * f;
+                rq[e] = qv[e] * f;
+                bk[e] = b * kv[e] * eg;
+                eq[e] = qv[e] * eg;
+                kr[e] = kv[e] * r;
             }
-            *reinterpret_cast<uint4*>(sm + OFF_KT + reg * 8192 + sw128(i, ch)) = pack8(f0);
-            *reinterpret_cast<uint4*>(sm + OFF_B1 + reg * 16384 + sw128(i, ch)) = pack8(f1);
-            *reinterpret_cast<uint4*>(sm + OFF_B1 + reg * 16384 + sw128(64 + i, ch)) = pack8(f2);
-            *reinterpret_cast<uint4*>(sm + OFF_KP + reg * 8192 + sw128(i, ch)) = pack8(f3);
-            *reinterpret_cast<uint4*>(sm + OFF_R + reg * 16384 + sw128(i, ch)) = pack8(f4);
-            *reinterpret_cast<uint4*>(sm + OFF_R + reg * 16384 + sw128(64 + i, ch)) = pack8(f5);
+            *reinterpret_cast<uint4*>(sm + OFF_RR + reg * 16384 + sw128(i, ch)) = pack8(rk);
+            *reinterpret_cast<uint4*>(sm + OFF_RR + reg * 16384 + sw128(64 + i, ch)) = pack8(rq);
+            *reinterpret_cast<uint4*>(sm + OFF_B1 + reg * 16384 + sw128(i, ch)) = pack8(bk);
+            *reinterpret_cast<uint4*>(sm + OFF_B1 + reg * 16384 + sw128(64 + i, ch)) = pack8(eq);
+            // column operands of row blocks J >= I: k_j e^{E_J - G_j} = kr * e^{E_J - E_I}
+#pragma unroll
+            for (int J = 0; J < 4; ++J) {
+                if (J < I) continue;
+                float cv[8];
+                if (J == I) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) cv[e] = kr[e];
+                } else {
+                    const int pair = I == 0 ? J - 1 : (I == 1 ? J + 1 : 5);
+                    const float* dt = sDt + pair * kD + c;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) cv[e] = kr[e] * dt[e];
+                }
+                if (J == 3)
+                    *reinterpret_cast<uint4*>(sm + OFF_KP + reg * 8192 + sw128(i, ch)) = pack8(cv);
+                else
+                    *reinterpret_cast<uint4*>(sm + OFF_CC + cc_off(J) + reg * (16u * (J + 1) * 128u) + sw128(i, ch)) =
+                        pack8(cv);
+            }
         }
         fence_proxy_async();
         __syncthreads();
-        // ---- (4) A block 0 and the S0 products
+        // k, q, g of the next chunk may now land in the staging buffers
+        if (L1 > 0) prefetch_kqg(sm, sBetaBuf + 64 * (buf ^ 1), k, q, g, beta, c1, L1, H, h, tid);
+        cp_async_commit();
+        // ---- (3) the S0 products and the four row blocks of A, one commit
         if (tid == 0) {
             tc_fence_after();
-            mma_k128(tbase + TM_A, sbase + OFF_R, 16384, sbase + OFF_KT, 8192, id_a, false);
-            mma_k128(tbase + TM_Y, sbase + OFF_S, 16384, sbase + OFF_B1, 16384, id_s, false);
+            mma_k128(tbase + TM_Y, sbase + OFF_S, 16384, sbase + OFF_B1, 16384, id_s);
+            mma_k128(tbase + TM_A0, sbase + OFF_RR, 16384, sbase + OFF_CC + cc_off(0), 2048,
+                     idesc_bf16_f32(128, 16, false, false));
+            mma_k128(tbase + TM_A1, sbase + OFF_RR, 16384, sbase + OFF_CC + cc_off(1), 4096,
+                     idesc_bf16_f32(128, 32, false, false));
+            mma_k128(tbase + TM_A2, sbase + OFF_RR, 16384, sbase + OFF_CC + cc_off(2), 6144,
+                     idesc_bf16_f32(128, 48, false, false));
+            mma_k128(tbase + TM_A3, sbase + OFF_RR, 16384, sbase + OFF_KP, 8192, idesc_bf16_f32(128, 64, false, false));
             mma_commit(bar);
         }
         wait_mma();
-        for (int J = 1; J < 4; ++J) {
-            const int rows = kC - 16 * J;  // rows of blocks >= J, for the k half and the q half
-#pragma unroll 1
-            for (int id = tid; id < rows * 16; id += kThreads) {
-                const int i = 16 * J + (id >> 4), cc = id & 15, c = cc * 8;
-                const uint32_t reg = cc >> 3, ch = cc & 7;
-                float kv[8], qv[8], f4[8], f5[8];
-                unpack8(*reinterpret_cast<const uint4*>(sm + OFF_STK + i * 256 + cc * 16), kv);
-                unpack8(*reinterpret_cast<const uint4*>(sm + OFF_STQ + i * 256 + cc * 16), qv);
-                const float* gj = sGend + J * kD + c;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float r = __expf(sG[i * kD + c + e] - gj[e]);
-                    f4[e] = kv[e] * r;
-                    f5[e] = qv[e] * r;
-                }
-                *reinterpret_cast<uint4*>(sm + OFF_R + reg * 16384 + sw128(i, ch)) = pack8(f4);
-                *reinterpret_cast<uint4*>(sm + OFF_R + reg * 16384 + sw128(64 + i, ch)) = pack8(f5);
-            }
-            fence_proxy_async();
-            __syncthreads();
-            if (tid == 0) {
-                tc_fence_after();
-                // B = rows [16J, 16J + 16) of K~: 16 rows = two 8-row groups, so the sub-tile starts 2048 J bytes in
-                mma_k128(tbase + TM_A + 16 * J, sbase + OFF_R, 16384, sbase + OFF_KT + 2048 * J, 8192, id_a, false);
-                mma_commit(bar);
-            }
-            wait_mma();
-        }
-        // ---- (5) A_kk (fp32 work array), A_qk (bf16 operand) and Z^T (bf16 operand)
+        // ---- (4) A_kk (fp32 work), A_qk (bf16 operand), Z^T (bf16 operand)
         {
-            float a[32];
-            tmem_ld32(tbase + lane_base + TM_A + 32 * half, a);
-            if (row < kC) {
-                const int i = row;
-                const float b = sBeta[i];
+            // lane quarter q holds rows 32q .. 32q+31 of [k-rows ; q-rows]: lanes 0-15 belong to row block
+            // 2(q%2) and lanes 16-31 to 2(q%2)+1; warp half 0 reads the first block's columns, half 1 the second's.
+            const int qtr = warp & 3, Ib = 2 * (qtr & 1) + half;  // row block whose columns this warp reads
+            const bool mine = ((lane >> 4) == half);              // lanes whose row lies in block Ib
+            const int r = 32 * qtr + lane;                        // TMEM lane
+            const int i = r & 63;                                 // token row in the chunk
+            const bool is_k = r < 64;
+            uint32_t a[64];
+            {
+                uint32_t t0[32], t1[32];
+                if (Ib == 0) {
+                    uint32_t x[16];
+                    tmem_ld16_async(tbase + lane_base + TM_A0, x);
+                    tmem_wait_ld(); reg_fence(x);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int j = 32 * half + e;
-                    sAkk[i * kAStride + j] = j < i ? b * a[e] : 0.f;
-                }
-            } else {
-                const int i = row - kC;
+                    for (int e = 0; e < 16; ++e) a[e] = x[e];
+                } else if (Ib == 1) {
+                    tmem_ld32_async(tbase + lane_base + TM_A1, t0);
+                    tmem_wait_ld(); reg_fence(t0);
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    float f[8];
+                    for (int e = 0; e < 32; ++e) a[e] = t0[e];
+                } else if (Ib == 2) {
+                    uint32_t x[16];
+                    tmem_ld32_async(tbase + lane_base + TM_A2, t0);
+                    tmem_ld16_async(tbase + lane_base + TM_A2 + 32, x);
+                    tmem_wait_ld(); reg_fence(t0); reg_fence(x);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int j = 32 * half + 8 * c4 + e;
-                        f[e] = j <= i ? a[8 * c4 + e] : 0.f;
-                    }
-                    *reinterpret_cast<uint4*>(sm + OFF_STQ + 8192 + sw128(i, 4 * half + c4)) = pack8(f);
+                    for (int e = 0; e < 32; ++e) a[e] = t0[e];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) a[32 + e] = x[e];
+                } else {
+                    tmem_ld32_async(tbase + lane_base + TM_A3, t0);
+                    tmem_ld32_async(tbase + lane_base + TM_A3 + 32, t1);
+                    tmem_wait_ld(); reg_fence(t0); reg_fence(t1);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) { a[e] = t0[e]; a[32 + e] = t1[e]; }
                 }
             }
-            float y[32];
-            tmem_ld32(tbase + lane_base + TM_Y + 32 * half, y);
+            const int ncols = 16 * (Ib + 1);
+            if (mine) {
+                if (is_k) {
+                    const float b = sBeta[i];
+#pragma unroll
+                    for (int j4 = 0; j4 < 16; ++j4) {
+                        float4 w;
+                        float* wp = reinterpret_cast<float*>(&w);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = 4 * j4 + e;
+                            wp[e] = (j < i && j < ncols) ? b * __uint_as_float(a[j]) : 0.f;
+                        }
+                        *reinterpret_cast<float4*>(sAkk + i * kAS + 4 * j4) = w;
+                    }
+                } else {
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch) {
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int j = 8 * ch + e;
+                            f[e] = (j <= i && j < ncols) ? __uint_as_float(a[j]) : 0.f;
+                        }
+                        *reinterpret_cast<uint4*>(sm + OFF_AQ + sw128(i, ch)) = pack8(f);
+                    }
+                }
+            }
+            uint32_t y[32];
+            tmem_ld32_async(tbase + lane_base + TM_Y + 32 * half, y);
+            tmem_wait_ld(); reg_fence(y);
+            const __nv_bfloat16* sv = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STV);
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
                 float f[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int j = 32 * half + 8 * c4 + e;
-                    const float vj = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STV)[j * kD + row]);
-                    f[e] = sBeta[j] * vj - y[8 * c4 + e];
+                    f[e] = sBeta[j] * __bfloat162float(sv[j * kD + row]) - __uint_as_float(y[8 * c4 + e]);
                 }
-                *reinterpret_cast<uint4*>(sm + OFF_STK + sw128(row, 4 * half + c4)) = pack8(f);
+                *reinterpret_cast<uint4*>(sm + OFF_Z + sw128(row, 4 * half + c4)) = pack8(f);
             }
         }
         __syncthreads();
-        // ---- (6) T = (I + A_kk)^-1 by forward substitution (fp32); warp w owns columns 8w .. 8w+7
-        {
-            const int col = 8 * warp + (lane & 7), grp = lane >> 3;
-            for (int i = 0; i < kC; ++i) {
-                float p0 = 0.f, p1 = 0.f;
-                int j = grp;
-                for (; j + 4 < i; j += 8) {
-                    p0 = fmaf(sAkk[i * kAStride + j], sTf[j * kAStride + col], p0);
-                    p1 = fmaf(sAkk[i * kAStride + j + 4], sTf[(j + 4) * kAStride + col], p1);
-                }
-                if (j < i) p0 = fmaf(sAkk[i * kAStride + j], sTf[j * kAStride + col], p0);
-                float part = p0 + p1;
-                part += __shfl_xor_sync(0xFFFFFFFFu, part, 8);
-                part += __shfl_xor_sync(0xFFFFFFFFu, part, 16);
-                if (grp == 0) sTf[i * kAStride + col] = col < i ? -part : (col == i ? 1.f : 0.f);
-                __syncwarp();
+        // v of the next chunk may now land
+        if (L1 > 0) prefetch_v(sm, v, c1, L1, H, h, tid);
+        cp_async_commit();
+        // ---- (5) T = (I + A_kk)^-1 by 16 x 16 blocks (fp32)
+        if (lane < 16 && warp < 4) {  // diagonal block `warp`, column `lane`
+            const int I = warp, c = lane;
+            const float* A = sAkk + 16 * I * kAS + 16 * I;
+            float x[16];
+#pragma unroll
+            for (int r2 = 0; r2 < 16; ++r2) {
+                float acc = (r2 == c) ? 1.f : 0.f;
+#pragma unroll
+                for (int m2 = 0; m2 < r2; ++m2) acc = fmaf(-A[r2 * kAS + m2], x[m2], acc);
+                x[r2] = acc;
             }
+#pragma unroll
+            for (int r2 = 0; r2 < 16; ++r2) sTf[(16 * I + r2) * kAS + 16 * I + c] = x[r2];
         }
         __syncthreads();
-        for (int id = tid; id < kC * 8; id += kThreads) {
+#pragma unroll 1
+        for (int d = 1; d < 4; ++d) {  // blocks (I, J = I - d), all I together
+            const int nb = 4 - d;
+            const int task = tid, bI = task >> 6;  // 64 tasks per block: (r, c4)
+            const bool act = bI < nb;
+            const int I = d + bI, J = I - d, r2 = (task & 63) >> 2, c4 = task & 3;
+            float4 y4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (act) {
+                const float* Ar = sAkk + (16 * I + r2) * kAS + 16 * J;
+                const float* Tc = sTf + (16 * J) * kAS + 16 * J + 4 * c4;
+                for (int m2 = 0; m2 < 16 * d; ++m2) {
+                    const float a2 = Ar[m2];
+                    const float4 t4 = *reinterpret_cast<const float4*>(Tc + m2 * kAS);
+                    y4.x = fmaf(a2, t4.x, y4.x); y4.y = fmaf(a2, t4.y, y4.y);
+                    y4.z = fmaf(a2, t4.z, y4.z); y4.w = fmaf(a2, t4.w, y4.w);
+                }
+                *reinterpret_cast<float4*>(sYs + (bI * 16 + r2) * 16 + 4 * c4) = y4;
+            }
+            __syncthreads();
+            if (act) {
+                const float* Tr = sTf + (16 * I + r2) * kAS + 16 * I;
+                float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int m2 = 0; m2 < 16; ++m2) {
+                    const float a2 = Tr[m2];
+                    const float4 yv = *reinterpret_cast<const float4*>(sYs + (bI * 16 + m2) * 16 + 4 * c4);
+                    t4.x = fmaf(a2, yv.x, t4.x); t4.y = fmaf(a2, yv.y, t4.y);
+                    t4.z = fmaf(a2, yv.z, t4.z); t4.w = fmaf(a2, yv.w, t4.w);
+                }
+                *reinterpret_cast<float4*>(sTf + (16 * I + r2) * kAS + 16 * J + 4 * c4) =
+                    make_float4(-t4.x, -t4.y, -t4.z, -t4.w);
+            }
+            __syncthreads();
+        }
+        for (int id = tid; id < kC * 8; id += kThreads) {  // T as a bf16 operand, zero above the diagonal blocks
             const int i = id >> 3, ch = id & 7;
             float f[8];
+            if ((ch >> 1) > (i >> 4)) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = sTf[i * kAStride + 8 * ch + e];
-            *reinterpret_cast<uint4*>(sm + OFF_STQ + sw128(i, ch)) = pack8(f);
+                for (int e = 0; e < 8; ++e) f[e] = 0.f;
+            } else {
+                *reinterpret_cast<float4*>(f) = *reinterpret_cast<const float4*>(sTf + i * kAS + 8 * ch);
+                *reinterpret_cast<float4*>(f + 4) = *reinterpret_cast<const float4*>(sTf + i * kAS + 8 * ch + 4);
+            }
+            *reinterpret_cast<uint4*>(sm + OFF_TB + sw128(i, ch)) = pack8(f);
         }
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
         if (*sAbort) break;
-        // ---- (7) V'^T = Z^T T^T
+        // ---- (6) V'^T = Z^T T^T
         if (tid == 0) {
             tc_fence_after();
-            mma_k64(tbase + TM_V, sbase + OFF_STK, sbase + OFF_STQ, id_64, false);
+            mma_k64(tbase + TM_V, sbase + OFF_Z, sbase + OFF_TB, id_64, false);
             mma_commit(bar);
         }
         wait_mma();
         {
-            float x[32];
-            tmem_ld32(tbase + lane_base + TM_V + 32 * half, x);
+            uint32_t x[32];
+            tmem_ld32_async(tbase + lane_base + TM_V + 32 * half, x);
+            tmem_wait_ld(); reg_fence(x);
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
                 float f[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = x[8 * c4 + e];
-                *reinterpret_cast<uint4*>(sm + OFF_STK + sw128(row, 4 * half + c4)) = pack8(f);
+                for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(x[8 * c4 + e]);
+                *reinterpret_cast<uint4*>(sm + OFF_Z + sw128(row, 4 * half + c4)) = pack8(f);
             }
         }
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
-        // ---- (8) O^T += V'^T A_qk^T;  dS = V'^T (K e^{G_C - G})
+        // ---- (7) O^T += V'^T A_qk^T;  dS = V'^T (K e^{G_C - G})
         if (tid == 0) {
             tc_fence_after();
-            mma_k64(tbase + TM_O, sbase + OFF_STK, sbase + OFF_STQ + 8192, id_64, true);
+            mma_k64(tbase + TM_O, sbase + OFF_Z, sbase + OFF_AQ, id_64, true);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tbase + TM_DS, sdesc_sw128(sbase + OFF_STK + ks * 32, 16, 1024),
+                mma_bf16(tbase + TM_DS, sdesc_sw128(sbase + OFF_Z + ks * 32, 16, 1024),
                          sdesc_sw128(sbase + OFF_KP + ks * 2048, 8192, 1024), id_ds, ks > 0 ? 1u : 0u);
             mma_commit(bar);
         }
         wait_mma();
-        // ---- (9) outputs and the state update
+        // ---- (8) outputs (fp32 staging, then coalesced) and the state update
         {
-            float x[32];
-            tmem_ld32(tbase + lane_base + TM_O + 32 * half, x);
+            uint32_t xo[32], d0[32], d1[32];
+            tmem_ld32_async(tbase + lane_base + TM_O + 32 * half, xo);
+            tmem_ld32_async(tbase + lane_base + TM_DS + 64 * half, d0);
+            tmem_ld32_async(tbase + lane_base + TM_DS + 64 * half + 32, d1);
+            tmem_wait_ld(); reg_fence(xo); reg_fence(d0); reg_fence(d1);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sO[(32 * half + e) * kD + row] = scale * __uint_as_float(xo[e]);
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-                const int j = 32 * half + e;
-                if (j < L) {
-                    const int64_t at = ((c0 + j) * H + h) * kD + row;
-                    float val = scale * x[e];
-                    if (gate) val *= 1.0f / (1.0f + __expf(-__bfloat162float(gate[at])));
-                    o[at] = __float2bfloat16_rn(val);
-                }
-            }
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-                tmem_ld32(tbase + lane_base + TM_DS + 64 * half + 32 * part, x);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int jj = 32 * part + e;
-                    s[jj] = fmaf(s[jj], sEGl[64 * half + jj], x[e]);
-                }
+                s[e] = fmaf(s[e], sEGl[64 * half + e], __uint_as_float(d0[e]));
+                s[32 + e] = fmaf(s[32 + e], sEGl[64 * half + 32 + e], __uint_as_float(d1[e]));
             }
         }
         write_state_operand();
         tc_fence_before();
         __syncthreads();
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int id = tid + kThreads * m, j = id >> 4, c16 = id & 15;
+            if (j < L) {
+                float f[8];
+                *reinterpret_cast<float4*>(f) = *reinterpret_cast<const float4*>(sO + j * kD + 8 * c16);
+                *reinterpret_cast<float4*>(f + 4) = *reinterpret_cast<const float4*>(sO + j * kD + 8 * c16 + 4);
+                const int64_t at = ((c0 + j) * H + h) * kD + 8 * c16;
+                if (gate) {
+                    float gv[8];
+                    unpack8(*reinterpret_cast<const uint4*>(gate + at), gv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] *= 1.0f / (1.0f + __expf(-gv[e]));
+                }
+                *reinterpret_cast<uint4*>(o + at) = pack8(f);
+            }
+        }
         if (*sAbort) break;
     }
 
+    cp_async_wait_all();
     if (final_state && !*sAbort) {
 #pragma unroll
         for (int j = 0; j < 64; j += 4)
