@@ -67,16 +67,17 @@ constexpr uint32_t OFF_BETA = OFF_SMALL;             // fp32 [2][64] (double-buf
 constexpr uint32_t OFF_E = OFF_BETA + 512;           // fp32 [4][128] E_I = G at the last token of block I
 constexpr uint32_t OFF_DT = OFF_E + 2048;            // fp32 [6][128] e^{E_J - E_I}, J > I
 constexpr uint32_t OFF_EGL = OFF_DT + 3072;          // fp32 [128] e^{G_C}
-constexpr uint32_t OFF_BAR = OFF_EGL + 512;          // mbarrier
+constexpr uint32_t OFF_BAR = OFF_EGL + 512;          // two mbarriers: A products, state products
 constexpr uint32_t OFF_MISC = OFF_BAR + 16;          // TMEM base, abort flag
 constexpr uint32_t kSmemUsed = OFF_MISC + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // slack for aligning the base
 
-constexpr uint32_t OFF_AQ = OFF_B1;                  // A_qk operand [64][64]     (8 KB)
-constexpr uint32_t OFF_TF = OFF_B1 + 8192;           // T fp32 [64][kAS]           (17 KB)
-constexpr uint32_t OFF_YS = OFF_B1 + 8192 + 64 * kAS * 4;  // level scratch fp32 [3][16][16]
-constexpr uint32_t OFF_Z = OFF_CC;                   // Z^T, then V'^T [128][64]   (16 KB)
-constexpr uint32_t OFF_TB = OFF_CC + 16384;          // T operand [64][64]         (8 KB)
+// After the A products complete (the S0 products may still be running and read B1):
+constexpr uint32_t OFF_AQ = OFF_RR + 64 * kAS * 4;   // A_qk operand [64][64] (8 KB), after A_kk fp32 [64][kAS]
+constexpr uint32_t OFF_YS = OFF_AQ + 8192;           // level scratch fp32 [3][16][16]
+constexpr uint32_t OFF_TF = OFF_CC;                  // T fp32 [64][kAS] (17 KB)
+constexpr uint32_t OFF_TB = OFF_CC + 16384;          // T operand [64][64] (8 KB), written once T is in registers
+constexpr uint32_t OFF_Z = OFF_CC;                   // Z^T, then V'^T [128][64] (16 KB), after T is consumed
 // column operand of row block I < 3: 16(I+1) rows, two regions of 16(I+1) * 128 bytes
 __host__ __device__ constexpr uint32_t cc_off(int I) { return I == 0 ? 0u : (I == 1 ? 4096u : 12288u); }
 
@@ -88,7 +89,8 @@ constexpr uint32_t TM_O = 320;
 constexpr uint32_t TM_DS = 384;   // delta S
 constexpr uint32_t kTmemCols = 512;
 
-static_assert(OFF_YS + 3 * 256 * 4 <= OFF_KP, "T work overflows its region");
+static_assert(OFF_AQ % 1024 == 0 && OFF_YS + 3 * 256 * 4 <= OFF_CC, "T work overflows its region");
+static_assert(OFF_TF + 64 * kAS * 4 <= OFF_S && OFF_TB + 8192 <= OFF_S, "T operand overflows its region");
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 __device__ __forceinline__ void unpack8(uint4 u, float (&f)[8]) {
@@ -154,6 +156,56 @@ __device__ __forceinline__ void prefetch_v(uint8_t* sm, const __nv_bfloat16* v, 
     }
 }
 
+// One level of the blocked inverse: every block (I, J = I - D) of T below the diagonal,
+// T_IJ = -T_II Y with Y = sum_{m = 16J}^{16I - 1} A[16I + r][m] T[m][16J + ...].  A task computes
+// four columns of one row of one block; P = 4 / (4 - D) threads share a task and split its sums.
+template <int D>
+__device__ __forceinline__ void t_level(const float* sAkk, float* sTf, float* sYs, int tid) {
+    constexpr int NB = 4 - D, P = 4 / NB, TERMS = 16 * D / P, TERMS2 = 16 / P;
+    const int task = tid / P, part = tid % P, bI = task >> 6;
+    const bool act = bI < NB;
+    const int I = D + (act ? bI : 0), J = I - D, r2 = (task & 63) >> 2, c4 = task & 3;
+    float4 y4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (act) {
+        const float* Ar = sAkk + (16 * I + r2) * kAS + 16 * J + part * TERMS;
+        const float* Tc = sTf + (16 * J + part * TERMS) * kAS + 16 * J + 4 * c4;
+#pragma unroll
+        for (int m = 0; m < TERMS; ++m) {
+            const float a = Ar[m];
+            const float4 t4 = *reinterpret_cast<const float4*>(Tc + m * kAS);
+            y4.x = fmaf(a, t4.x, y4.x); y4.y = fmaf(a, t4.y, y4.y);
+            y4.z = fmaf(a, t4.z, y4.z); y4.w = fmaf(a, t4.w, y4.w);
+        }
+    }
+#pragma unroll
+    for (int o = 1; o < P; o <<= 1) {
+        y4.x += __shfl_xor_sync(0xFFFFFFFFu, y4.x, o); y4.y += __shfl_xor_sync(0xFFFFFFFFu, y4.y, o);
+        y4.z += __shfl_xor_sync(0xFFFFFFFFu, y4.z, o); y4.w += __shfl_xor_sync(0xFFFFFFFFu, y4.w, o);
+    }
+    if (act && part == 0) *reinterpret_cast<float4*>(sYs + (bI * 16 + r2) * 16 + 4 * c4) = y4;
+    __syncthreads();
+    float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (act) {
+        const float* Tr = sTf + (16 * I + r2) * kAS + 16 * I + part * TERMS2;
+        const float* Yc = sYs + (bI * 16 + part * TERMS2) * 16 + 4 * c4;
+#pragma unroll
+        for (int m = 0; m < TERMS2; ++m) {
+            const float a = Tr[m];
+            const float4 yv = *reinterpret_cast<const float4*>(Yc + m * 16);
+            t4.x = fmaf(a, yv.x, t4.x); t4.y = fmaf(a, yv.y, t4.y);
+            t4.z = fmaf(a, yv.z, t4.z); t4.w = fmaf(a, yv.w, t4.w);
+        }
+    }
+#pragma unroll
+    for (int o = 1; o < P; o <<= 1) {
+        t4.x += __shfl_xor_sync(0xFFFFFFFFu, t4.x, o); t4.y += __shfl_xor_sync(0xFFFFFFFFu, t4.y, o);
+        t4.z += __shfl_xor_sync(0xFFFFFFFFu, t4.z, o); t4.w += __shfl_xor_sync(0xFFFFFFFFu, t4.w, o);
+    }
+    if (act && part == 0)
+        *reinterpret_cast<float4*>(sTf + (16 * I + r2) * kAS + 16 * J + 4 * c4) = make_float4(-t4.x, -t4.y, -t4.z, -t4.w);
+    __syncthreads();
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                 const __nv_bfloat16* __restrict__ v, const float* __restrict__ g, const float* __restrict__ beta,
@@ -167,7 +219,8 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     float* sE = reinterpret_cast<float*>(sm + OFF_E);
     float* sDt = reinterpret_cast<float*>(sm + OFF_DT);
     float* sEGl = reinterpret_cast<float*>(sm + OFF_EGL);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    uint64_t* barA = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+    uint64_t* barS = barA + 1;
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
     volatile int* sAbort = reinterpret_cast<volatile int*>(sm + OFF_MISC + 4);
     float* sG = reinterpret_cast<float*>(sm + OFF_STG);
@@ -185,7 +238,8 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     const int64_t state_off = (int64_t)chain * kD * kD + (int64_t)row * kD + 64 * half;
 
     if (tid == 0) {
-        mbar_init(bar, 1);
+        mbar_init(barA, 1);
+        mbar_init(barS, 1);
         fence_mbar_init();
         *sAbort = 0;
     }
@@ -218,16 +272,17 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *sTmem;
-    uint32_t phase = 0;
+    uint32_t phaseA = 0, phaseS = 0;
 
-    auto wait_mma = [&]() {
-        if (!mbar_wait(bar, phase, kWaitLimit)) {
+    auto wait_bar = [&](uint64_t* b, uint32_t& ph) {
+        if (!mbar_wait(b, ph, kWaitLimit)) {
             *sAbort = 1;
             raise_device_error(err, kErrMbarTimeout);
         }
-        phase ^= 1u;
+        ph ^= 1u;
         tc_fence_after();
     };
+    auto wait_mma = [&]() { wait_bar(barS, phaseS); };
 
     const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
     const uint32_t id_64 = idesc_bf16_f32(128, 64, false, false);
@@ -327,10 +382,9 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         // k, q, g of the next chunk may now land in the staging buffers
         if (L1 > 0) prefetch_kqg(sm, sBetaBuf + 64 * (buf ^ 1), k, q, g, beta, c1, L1, H, h, tid);
         cp_async_commit();
-        // ---- (3) the S0 products and the four row blocks of A, one commit
+        // ---- (3) the four row blocks of A (barrier A), then the S0 products (barrier S)
         if (tid == 0) {
             tc_fence_after();
-            mma_k128(tbase + TM_Y, sbase + OFF_S, 16384, sbase + OFF_B1, 16384, id_s);
             mma_k128(tbase + TM_A0, sbase + OFF_RR, 16384, sbase + OFF_CC + cc_off(0), 2048,
                      idesc_bf16_f32(128, 16, false, false));
             mma_k128(tbase + TM_A1, sbase + OFF_RR, 16384, sbase + OFF_CC + cc_off(1), 4096,
@@ -338,10 +392,12 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
             mma_k128(tbase + TM_A2, sbase + OFF_RR, 16384, sbase + OFF_CC + cc_off(2), 6144,
                      idesc_bf16_f32(128, 48, false, false));
             mma_k128(tbase + TM_A3, sbase + OFF_RR, 16384, sbase + OFF_KP, 8192, idesc_bf16_f32(128, 64, false, false));
-            mma_commit(bar);
+            mma_commit(barA);
+            mma_k128(tbase + TM_Y, sbase + OFF_S, 16384, sbase + OFF_B1, 16384, id_s);
+            mma_commit(barS);
         }
-        wait_mma();
-        // ---- (4) A_kk (fp32 work), A_qk (bf16 operand), Z^T (bf16 operand)
+        wait_bar(barA, phaseA);
+        // ---- (4) A_kk (fp32 work array) and A_qk (bf16 operand)
         {
             // lane quarter q holds rows 32q .. 32q+31 of [k-rows ; q-rows]: lanes 0-15 belong to row block
             // 2(q%2) and lanes 16-31 to 2(q%2)+1; warp half 0 reads the first block's columns, half 1 the second's.
@@ -409,25 +465,8 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
                     }
                 }
             }
-            uint32_t y[32];
-            tmem_ld32_async(tbase + lane_base + TM_Y + 32 * half, y);
-            tmem_wait_ld(); reg_fence(y);
-            const __nv_bfloat16* sv = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STV);
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                float f[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int j = 32 * half + 8 * c4 + e;
-                    f[e] = sBeta[j] * __bfloat162float(sv[j * kD + row]) - __uint_as_float(y[8 * c4 + e]);
-                }
-                *reinterpret_cast<uint4*>(sm + OFF_Z + sw128(row, 4 * half + c4)) = pack8(f);
-            }
         }
         __syncthreads();
-        // v of the next chunk may now land
-        if (L1 > 0) prefetch_v(sm, v, c1, L1, H, h, tid);
-        cp_async_commit();
         // ---- (5) T = (I + A_kk)^-1 by 16 x 16 blocks (fp32)
         if (lane < 16 && warp < 4) {  // diagonal block `warp`, column `lane`
             const int I = warp, c = lane;
@@ -444,61 +483,59 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
             for (int r2 = 0; r2 < 16; ++r2) sTf[(16 * I + r2) * kAS + 16 * I + c] = x[r2];
         }
         __syncthreads();
-#pragma unroll 1
-        for (int d = 1; d < 4; ++d) {  // blocks (I, J = I - d), all I together
-            const int nb = 4 - d;
-            const int task = tid, bI = task >> 6;  // 64 tasks per block: (r, c4)
-            const bool act = bI < nb;
-            const int I = d + bI, J = I - d, r2 = (task & 63) >> 2, c4 = task & 3;
-            float4 y4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (act) {
-                const float* Ar = sAkk + (16 * I + r2) * kAS + 16 * J;
-                const float* Tc = sTf + (16 * J) * kAS + 16 * J + 4 * c4;
-                for (int m2 = 0; m2 < 16 * d; ++m2) {
-                    const float a2 = Ar[m2];
-                    const float4 t4 = *reinterpret_cast<const float4*>(Tc + m2 * kAS);
-                    y4.x = fmaf(a2, t4.x, y4.x); y4.y = fmaf(a2, t4.y, y4.y);
-                    y4.z = fmaf(a2, t4.z, y4.z); y4.w = fmaf(a2, t4.w, y4.w);
-                }
-                *reinterpret_cast<float4*>(sYs + (bI * 16 + r2) * 16 + 4 * c4) = y4;
-            }
-            __syncthreads();
-            if (act) {
-                const float* Tr = sTf + (16 * I + r2) * kAS + 16 * I;
-                float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        t_level<1>(sAkk, sTf, sYs, tid);
+        t_level<2>(sAkk, sTf, sYs, tid);
+        t_level<3>(sAkk, sTf, sYs, tid);
+        {   // T as a bf16 operand (zero above the diagonal blocks); read all of T before writing over its tail
+            float f[2][8];
 #pragma unroll
-                for (int m2 = 0; m2 < 16; ++m2) {
-                    const float a2 = Tr[m2];
-                    const float4 yv = *reinterpret_cast<const float4*>(sYs + (bI * 16 + m2) * 16 + 4 * c4);
-                    t4.x = fmaf(a2, yv.x, t4.x); t4.y = fmaf(a2, yv.y, t4.y);
-                    t4.z = fmaf(a2, yv.z, t4.z); t4.w = fmaf(a2, yv.w, t4.w);
+            for (int u = 0; u < 2; ++u) {
+                const int id = tid + kThreads * u, i = id >> 3, ch = id & 7;
+                if ((ch >> 1) > (i >> 4)) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[u][e] = 0.f;
+                } else {
+                    *reinterpret_cast<float4*>(f[u]) = *reinterpret_cast<const float4*>(sTf + i * kAS + 8 * ch);
+                    *reinterpret_cast<float4*>(f[u] + 4) = *reinterpret_cast<const float4*>(sTf + i * kAS + 8 * ch + 4);
                 }
-                *reinterpret_cast<float4*>(sTf + (16 * I + r2) * kAS + 16 * J + 4 * c4) =
-                    make_float4(-t4.x, -t4.y, -t4.z, -t4.w);
             }
             __syncthreads();
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int id = tid + kThreads * u, i = id >> 3, ch = id & 7;
+                *reinterpret_cast<uint4*>(sm + OFF_TB + sw128(i, ch)) = pack8(f[u]);
+            }
         }
-        for (int id = tid; id < kC * 8; id += kThreads) {  // T as a bf16 operand, zero above the diagonal blocks
-            const int i = id >> 3, ch = id & 7;
-            float f[8];
-            if ((ch >> 1) > (i >> 4)) {
+        // ---- Z^T = (beta V)^T - Y^T once the S0 products are done
+        wait_bar(barS, phaseS);
+        {
+            uint32_t y[32];
+            tmem_ld32_async(tbase + lane_base + TM_Y + 32 * half, y);
+            tmem_wait_ld(); reg_fence(y);
+            const __nv_bfloat16* sv = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STV);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = 0.f;
-            } else {
-                *reinterpret_cast<float4*>(f) = *reinterpret_cast<const float4*>(sTf + i * kAS + 8 * ch);
-                *reinterpret_cast<float4*>(f + 4) = *reinterpret_cast<const float4*>(sTf + i * kAS + 8 * ch + 4);
+            for (int c4 = 0; c4 < 4; ++c4) {
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int j = 32 * half + 8 * c4 + e;
+                    f[e] = sBeta[j] * __bfloat162float(sv[j * kD + row]) - __uint_as_float(y[8 * c4 + e]);
+                }
+                *reinterpret_cast<uint4*>(sm + OFF_Z + sw128(row, 4 * half + c4)) = pack8(f);
             }
-            *reinterpret_cast<uint4*>(sm + OFF_TB + sw128(i, ch)) = pack8(f);
         }
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
+        // v of the next chunk may now land
+        if (L1 > 0) prefetch_v(sm, v, c1, L1, H, h, tid);
+        cp_async_commit();
         if (*sAbort) break;
         // ---- (6) V'^T = Z^T T^T
         if (tid == 0) {
             tc_fence_after();
             mma_k64(tbase + TM_V, sbase + OFF_Z, sbase + OFF_TB, id_64, false);
-            mma_commit(bar);
+            mma_commit(barS);
         }
         wait_mma();
         {
@@ -524,7 +561,7 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
             for (int ks = 0; ks < 4; ++ks)
                 mma_bf16(tbase + TM_DS, sdesc_sw128(sbase + OFF_Z + ks * 32, 16, 1024),
                          sdesc_sw128(sbase + OFF_KP + ks * 2048, 8192, 1024), id_ds, ks > 0 ? 1u : 0u);
-            mma_commit(bar);
+            mma_commit(barS);
         }
         wait_mma();
         // ---- (8) outputs (fp32 staging, then coalesced) and the state update

@@ -304,3 +304,71 @@ def test_prefill_8k_sampled_heads(kda, orc):
         o_h = host(o[:, h:h + 1, :])
         assert orc.rel_l2(o_h, o_ref) <= BF16_O_REL and orc.max_abs(o_h, o_ref) <= BF16_O_ABS
         assert orc.rel_l2(host(fs[:, h:h + 1]), fs_ref) <= BF16_S_REL
+
+
+def test_varlen_32_sampled_chains(kda, orc):
+    """32 packed sequences (1K..32K tokens), H=96, initial states N(0, 0.02); the shortest,
+    a middle and the longest sequence checked in full on heads 0 and 95."""
+    w = ks.workload("varlen_32")
+    T, H, d, N = w.T, w.H, w.d, w.N
+    q = fill_dev(w, ks.TID_Q, ks.UNIT_GROUPS, (T, H, d), "bf16", 0.0, float(d))
+    k = fill_dev(w, ks.TID_K, ks.UNIT_GROUPS, (T, H, d), "bf16", 0.0, float(d))
+    v = fill_dev(w, ks.TID_V, ks.NORMAL, (T, H, d), "bf16")
+    g = fill_dev(w, ks.TID_G, w.g_kind, (T, H, d), "f32")
+    b = fill_dev(w, ks.TID_BETA, ks.SIGMOID, (T, H), "f32")
+    s0 = fill_dev(w, ks.TID_STATE, ks.NORMAL, (N, H, d, d), "f32", 0.0, w.init_state_std)
+    cu = w.cu_seqlens()
+    o, fs = kda.kda_chunk_fwd(q, k, v, g, b, s0, dev(cu))
+    torch.cuda.synchronize()
+    order = np.argsort(w.lengths)
+    for n in (int(order[0]), int(order[N // 2]), int(order[-1])):
+        t0, t1 = int(cu[n]), int(cu[n + 1])
+        for h in (0, 95):
+            qh, kh, vh, gh, bh = head_inputs(w, h, t0, t1)
+            sh = w.head_state(n, h).astype(np.float64)[None, None]
+            o_ref, fs_ref = orc.kda_tokenloop(qh, kh, vh, gh, bh, sh)
+            o_h = host(o[t0:t1, h:h + 1, :])
+            assert orc.rel_l2(o_h, o_ref) <= BF16_O_REL and orc.max_abs(o_h, o_ref) <= BF16_O_ABS
+            assert orc.rel_l2(host(fs[n:n + 1, h:h + 1]), fs_ref) <= BF16_S_REL
+
+
+def test_long_256k_frontend_gate_sampled_heads(kda, orc):
+    """T = 262,144: raw q, k, v -> kda_shortconv_l2norm -> kda_chunk_fwd with the sigmoid
+    output gate, as one pass; heads 0 and 61 checked in full against front end + token loop."""
+    w = ks.workload("long_256k")
+    T, H, d = w.T, w.H, w.d
+    C = H * d
+    xq = fill_dev(w, ks.TID_Q, ks.NORMAL, (T, C), "bf16")
+    xk = fill_dev(w, ks.TID_K, ks.NORMAL, (T, C), "bf16")
+    xv = fill_dev(w, ks.TID_V, ks.NORMAL, (T, C), "bf16")
+    cw = fill_dev(w, ks.TID_CONV_W, ks.NORMAL, (3 * C, 4), "bf16", 0.0, w.conv_w_std)
+    g = fill_dev(w, ks.TID_G, w.g_kind, (T, H, d), "f32")
+    b = fill_dev(w, ks.TID_BETA, ks.SIGMOID, (T, H), "f32")
+    gate = fill_dev(w, ks.TID_GATE, ks.NORMAL, (T, C), "bf16")
+    q, k, v = kda.kda_shortconv_l2norm(xq, xk, xv, cw, H)
+    del xq, xk, xv
+    o, fs = kda.kda_chunk_fwd(q, k, v, g, b, out_gate=gate)
+    torch.cuda.synchronize()
+    del q, k, v, g
+    cw_h = ks.to_f64(w.conv_w())
+    heads = (0, 61)
+    fe = []
+    for h in heads:
+        raw = [ks.to_f64(w.head_rows(tid, ks.NORMAL, h, "bf16")) for tid in (ks.TID_Q, ks.TID_K, ks.TID_V)]
+        wh = np.concatenate([cw_h[p * C + h * d: p * C + (h + 1) * d] for p in range(3)])
+        fe.append(orc.shortconv_silu_l2norm(*raw, wh, 1, d, want_state=False)[:3])
+    qh, kh, vh = (np.concatenate([f[i] for f in fe], axis=1) for i in range(3))   # [T, 2, d]
+    gh = np.stack([w.head_rows(ks.TID_G, w.g_kind, h, "f32") for h in heads], axis=1).astype(np.float64)
+    bh = np.stack([w.head_beta(h) for h in heads], axis=1).astype(np.float64)
+    gt = np.concatenate([ks.to_f64(w.head_rows(ks.TID_GATE, ks.NORMAL, h, "bf16")) for h in heads], axis=1)
+    o_h = np.concatenate([host(o[:, h:h + 1, :]) for h in heads], axis=1)
+    fs_h = np.concatenate([host(fs[:, h:h + 1]) for h in heads], axis=1)
+    # the chunk kernel stores q, k, v in bf16: the oracle rounds its own front-end output the same way
+    rq, rk, rv = (ks.bf16_to_f64(ks.f32_to_bf16(x.astype(np.float32))) for x in (qh, kh, vh))
+    o_ref, fs_ref = orc.kda_tokenloop(rq, rk, rv, gh, bh)
+    o_ref = orc.output_gate(o_ref, gt)
+    assert orc.rel_l2(o_h, o_ref) <= BF16_O_REL and orc.max_abs(o_h, o_ref) <= BF16_O_ABS
+    assert orc.rel_l2(fs_h, fs_ref) <= BF16_S_REL
+    # and against the unrounded fp64 front end
+    o_ref2, _ = orc.kda_tokenloop(qh, kh, vh, gh, bh)
+    assert orc.rel_l2(o_h, orc.output_gate(o_ref2, gt)) <= BF16_O_REL
