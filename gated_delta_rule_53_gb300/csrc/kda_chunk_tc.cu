@@ -33,11 +33,13 @@
 // row r to TMEM lane r.  All tensor-core products take bf16 operands and
 // accumulate in fp32 in TMEM.  T = (I + A_kk)^-1 is computed in fp32 on the CUDA
 // cores by 16 x 16 blocks: the four diagonal blocks by forward substitution, then
-// the blocks below them level by level, T_IJ = -T_II sum_{M=J..I-1} A_IM T_MJ.
+// the blocks below them, T_IJ = -T_II sum_{M=J..I-1} A_IM T_MJ, one block column per
+// warp pair.
 //
-// One CTA per (sequence, head) walks the chunks in order.  The next chunk's
-// inputs are copied into shared memory with cp.async while the current chunk
-// computes (k, q, g once the operands are built, v once Z is built).
+// One CTA of 16 warps per (sequence, head) walks the chunks in order; thread
+// (r, quarter) holds state row r, key channels [32 quarter, 32 quarter + 32).  The
+// next chunk's inputs are copied into shared memory with cp.async while the
+// current chunk computes (k, q, g once the operands are built, v once Z is built).
 #include "kda_common.cuh"
 #include "kda_tc.cuh"
 
@@ -46,35 +48,36 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kC = kChunk;    // 64
 constexpr int kD = kHeadDim;  // 128
 constexpr int kAS = 68;       // fp32 row stride of the A_kk / T work arrays (float4 rows on distinct banks)
 constexpr uint32_t kWaitLimit = 1u << 22;
 
-// shared-memory map (bytes from a 1024-aligned base); "|" = reuse later in the chunk
+// shared-memory map (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_STK = 0;        // k staging bf16 [64][128]
 constexpr uint32_t OFF_STQ = 16384;    // q staging bf16 [64][128]
 constexpr uint32_t OFF_STV = 32768;    // v staging bf16 [64][128]
 constexpr uint32_t OFF_STG = 49152;    // g -> G fp32 [64][128]
-constexpr uint32_t OFF_B1 = 81920;     // [beta K e^G ; Q e^G] [128][128] | A_qk bf16 [64][64], T fp32, level scratch
+constexpr uint32_t OFF_B1 = 81920;     // [beta K e^G ; Q e^G] [128][128] (B of the S0 products)
 constexpr uint32_t OFF_KP = 114688;    // K e^{G_C - G} [64][128]: column operand of row block 3, B of dS
-constexpr uint32_t OFF_RR = 131072;    // row operand [K e^{G-E} ; Q e^{G-E}] [128][128] | A_kk fp32 | O fp32 [64][128]
-constexpr uint32_t OFF_CC = 163840;    // column operands of row blocks 0..2 (16, 32, 48 rows) | Z^T / V'^T, T bf16
+constexpr uint32_t OFF_RR = 131072;    // row operand [K e^{G-E} ; Q e^{G-E}] [128][128] | A_kk, A_qk, scratch | O fp32
+constexpr uint32_t OFF_CC = 163840;    // column operands of row blocks 0..2 (16, 32, 48 rows) | T fp32, T bf16 | Z^T
 constexpr uint32_t OFF_S = 188416;     // bf16 S0 [128][128]
 constexpr uint32_t OFF_SMALL = 221184;
 constexpr uint32_t OFF_BETA = OFF_SMALL;             // fp32 [2][64] (double-buffered)
 constexpr uint32_t OFF_E = OFF_BETA + 512;           // fp32 [4][128] E_I = G at the last token of block I
 constexpr uint32_t OFF_DT = OFF_E + 2048;            // fp32 [6][128] e^{E_J - E_I}, J > I
 constexpr uint32_t OFF_EGL = OFF_DT + 3072;          // fp32 [128] e^{G_C}
-constexpr uint32_t OFF_BAR = OFF_EGL + 512;          // two mbarriers: A products, state products
+constexpr uint32_t OFF_TOT = OFF_EGL + 512;          // fp32 [4][128] per-block sums of g
+constexpr uint32_t OFF_BAR = OFF_TOT + 2048;         // two mbarriers: A products, state products
 constexpr uint32_t OFF_MISC = OFF_BAR + 16;          // TMEM base, abort flag
 constexpr uint32_t kSmemUsed = OFF_MISC + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // slack for aligning the base
 
 // After the A products complete (the S0 products may still be running and read B1):
 constexpr uint32_t OFF_AQ = OFF_RR + 64 * kAS * 4;   // A_qk operand [64][64] (8 KB), after A_kk fp32 [64][kAS]
-constexpr uint32_t OFF_YS = OFF_AQ + 8192;           // level scratch fp32 [3][16][16]
+constexpr uint32_t OFF_YS = OFF_AQ + 8192;           // per-warp scratch fp32 [6][16][8]
 constexpr uint32_t OFF_TF = OFF_CC;                  // T fp32 [64][kAS] (17 KB)
 constexpr uint32_t OFF_TB = OFF_CC + 16384;          // T operand [64][64] (8 KB), written once T is in registers
 constexpr uint32_t OFF_Z = OFF_CC;                   // Z^T, then V'^T [128][64] (16 KB), after T is consumed
@@ -89,7 +92,7 @@ constexpr uint32_t TM_O = 320;
 constexpr uint32_t TM_DS = 384;   // delta S
 constexpr uint32_t kTmemCols = 512;
 
-static_assert(OFF_AQ % 1024 == 0 && OFF_YS + 3 * 256 * 4 <= OFF_CC, "T work overflows its region");
+static_assert(OFF_AQ % 1024 == 0 && OFF_YS + 6 * 128 * 4 <= OFF_CC, "T work overflows its region");
 static_assert(OFF_TF + 64 * kAS * 4 <= OFF_S && OFF_TB + 8192 <= OFF_S, "T operand overflows its region");
 static_assert(kSmemBytes <= 232448, "shared memory");
 
@@ -127,7 +130,7 @@ __device__ __forceinline__ void prefetch_kqg(uint8_t* sm, float* beta_dst, const
                                              const __nv_bfloat16* q, const float* g, const float* beta, int64_t c0,
                                              int L, int H, int h, int tid) {
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
+    for (int m = 0; m < 2; ++m) {
         const int id = tid + kThreads * m, i = id >> 4, cc = id & 15;
         const bool ok = i < L;
         const int64_t at = ok ? ((c0 + i) * H + h) * kD + cc * 8 : 0;
@@ -135,7 +138,7 @@ __device__ __forceinline__ void prefetch_kqg(uint8_t* sm, float* beta_dst, const
         cp_async16(sm + OFF_STQ + i * 256 + cc * 16, q + at, ok ? 16u : 0u);
     }
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
+    for (int m = 0; m < 4; ++m) {
         const int id = tid + kThreads * m, i = id >> 5, cc = id & 31;
         const bool ok = i < L;
         cp_async16(sm + OFF_STG + i * 512 + cc * 16, g + (ok ? ((c0 + i) * H + h) * kD + cc * 4 : 0), ok ? 16u : 0u);
@@ -149,61 +152,48 @@ __device__ __forceinline__ void prefetch_kqg(uint8_t* sm, float* beta_dst, const
 __device__ __forceinline__ void prefetch_v(uint8_t* sm, const __nv_bfloat16* v, int64_t c0, int L, int H, int h,
                                            int tid) {
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
+    for (int m = 0; m < 2; ++m) {
         const int id = tid + kThreads * m, i = id >> 4, cc = id & 15;
         const bool ok = i < L;
         cp_async16(sm + OFF_STV + i * 256 + cc * 16, v + (ok ? ((c0 + i) * H + h) * kD + cc * 8 : 0), ok ? 16u : 0u);
     }
 }
 
-// One level of the blocked inverse: every block (I, J = I - D) of T below the diagonal,
-// T_IJ = -T_II Y with Y = sum_{m = 16J}^{16I - 1} A[16I + r][m] T[m][16J + ...].  A task computes
-// four columns of one row of one block; P = 4 / (4 - D) threads share a task and split its sums.
-template <int D>
-__device__ __forceinline__ void t_level(const float* sAkk, float* sTf, float* sYs, int tid) {
-    constexpr int NB = 4 - D, P = 4 / NB, TERMS = 16 * D / P, TERMS2 = 16 / P;
-    const int task = tid / P, part = tid % P, bI = task >> 6;
-    const bool act = bI < NB;
-    const int I = D + (act ? bI : 0), J = I - D, r2 = (task & 63) >> 2, c4 = task & 3;
-    float4 y4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (act) {
-        const float* Ar = sAkk + (16 * I + r2) * kAS + 16 * J + part * TERMS;
-        const float* Tc = sTf + (16 * J + part * TERMS) * kAS + 16 * J + 4 * c4;
-#pragma unroll
-        for (int m = 0; m < TERMS; ++m) {
+// Blocks of T below the diagonal, one block column per warp pair: warp `w` (0..7) owns block
+// column J = w / 2, columns 8 (w % 2) .. 8 (w % 2) + 7 of it, and walks down it:
+//   T_IJ = -T_II Y,  Y = sum_{M = J}^{I-1} A_IM T_MJ,  I = J+1 .. 3
+// Everything a warp reads is either a diagonal block (written before the block barrier that
+// precedes this call) or an earlier block of its own columns, so warps only sync with themselves.
+// Lane l holds rows l / 2 and four columns 4 (l % 2) .. +3 of the warp's eight; Y goes through
+// the warp's own 16 x 8 scratch tile.
+__device__ __forceinline__ void t_column(const float* sAkk, float* sTf, float* sYw, int warp, int lane) {
+    const int J = warp >> 1, c0 = 16 * J + 8 * (warp & 1) + 4 * (lane & 1), r = lane >> 1;
+    for (int I = J + 1; I < 4; ++I) {
+        const float* Ar = sAkk + (16 * I + r) * kAS + 16 * J;
+        const float* Tc = sTf + 16 * J * kAS + c0;
+        float4 y4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int terms = 16 * (I - J);
+#pragma unroll 8
+        for (int m = 0; m < terms; ++m) {
             const float a = Ar[m];
             const float4 t4 = *reinterpret_cast<const float4*>(Tc + m * kAS);
             y4.x = fmaf(a, t4.x, y4.x); y4.y = fmaf(a, t4.y, y4.y);
             y4.z = fmaf(a, t4.z, y4.z); y4.w = fmaf(a, t4.w, y4.w);
         }
-    }
+        *reinterpret_cast<float4*>(sYw + r * 8 + 4 * (lane & 1)) = y4;
+        __syncwarp();
+        const float* Tr = sTf + (16 * I + r) * kAS + 16 * I;
+        float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int o = 1; o < P; o <<= 1) {
-        y4.x += __shfl_xor_sync(0xFFFFFFFFu, y4.x, o); y4.y += __shfl_xor_sync(0xFFFFFFFFu, y4.y, o);
-        y4.z += __shfl_xor_sync(0xFFFFFFFFu, y4.z, o); y4.w += __shfl_xor_sync(0xFFFFFFFFu, y4.w, o);
-    }
-    if (act && part == 0) *reinterpret_cast<float4*>(sYs + (bI * 16 + r2) * 16 + 4 * c4) = y4;
-    __syncthreads();
-    float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (act) {
-        const float* Tr = sTf + (16 * I + r2) * kAS + 16 * I + part * TERMS2;
-        const float* Yc = sYs + (bI * 16 + part * TERMS2) * 16 + 4 * c4;
-#pragma unroll
-        for (int m = 0; m < TERMS2; ++m) {
+        for (int m = 0; m < 16; ++m) {
             const float a = Tr[m];
-            const float4 yv = *reinterpret_cast<const float4*>(Yc + m * 16);
+            const float4 yv = *reinterpret_cast<const float4*>(sYw + m * 8 + 4 * (lane & 1));
             t4.x = fmaf(a, yv.x, t4.x); t4.y = fmaf(a, yv.y, t4.y);
             t4.z = fmaf(a, yv.z, t4.z); t4.w = fmaf(a, yv.w, t4.w);
         }
+        *reinterpret_cast<float4*>(sTf + (16 * I + r) * kAS + c0) = make_float4(-t4.x, -t4.y, -t4.z, -t4.w);
+        __syncwarp();
     }
-#pragma unroll
-    for (int o = 1; o < P; o <<= 1) {
-        t4.x += __shfl_xor_sync(0xFFFFFFFFu, t4.x, o); t4.y += __shfl_xor_sync(0xFFFFFFFFu, t4.y, o);
-        t4.z += __shfl_xor_sync(0xFFFFFFFFu, t4.z, o); t4.w += __shfl_xor_sync(0xFFFFFFFFu, t4.w, o);
-    }
-    if (act && part == 0)
-        *reinterpret_cast<float4*>(sTf + (16 * I + r2) * kAS + 16 * J + 4 * c4) = make_float4(-t4.x, -t4.y, -t4.z, -t4.w);
-    __syncthreads();
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -219,6 +209,7 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     float* sE = reinterpret_cast<float*>(sm + OFF_E);
     float* sDt = reinterpret_cast<float*>(sm + OFF_DT);
     float* sEGl = reinterpret_cast<float*>(sm + OFF_EGL);
+    float* sTot = reinterpret_cast<float*>(sm + OFF_TOT);
     uint64_t* barA = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     uint64_t* barS = barA + 1;
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
@@ -231,11 +222,11 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int chain = blockIdx.x, n = chain / H, h = chain % H;
-    const int row = tid & 127, half = tid >> 7;  // state row / TMEM lane, key-channel half
+    const int row = tid & 127, qq = tid >> 7;  // state row / TMEM lane; quarter of the key channels / tokens
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     int64_t bos, eos;
     seq_bounds(cu, n, T_total, bos, eos);
-    const int64_t state_off = (int64_t)chain * kD * kD + (int64_t)row * kD + 64 * half;
+    const int64_t state_off = (int64_t)chain * kD * kD + (int64_t)row * kD + 32 * qq;
 
     if (tid == 0) {
         mbar_init(barA, 1);
@@ -251,20 +242,20 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         cp_async_commit();
     }
 
-    // state rows in registers, bf16 copy as the S0 operand
-    float s[64];
+    // state: row `row`, key channels [32 qq, 32 qq + 32) in registers; bf16 copy as the S0 operand
+    float s[32];
 #pragma unroll
-    for (int j = 0; j < 64; j += 4) {
+    for (int j = 0; j < 32; j += 4) {
         float4 x = init_state ? *reinterpret_cast<const float4*>(init_state + state_off + j) : make_float4(0.f, 0.f, 0.f, 0.f);
         s[j] = x.x; s[j + 1] = x.y; s[j + 2] = x.z; s[j + 3] = x.w;
     }
     auto write_state_operand = [&]() {
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
+        for (int c = 0; c < 4; ++c) {
             float f[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = s[8 * ch + e];
-            *reinterpret_cast<uint4*>(sm + OFF_S + half * 16384 + sw128(row, ch)) = pack8(f);
+            for (int e = 0; e < 8; ++e) f[e] = s[8 * c + e];
+            *reinterpret_cast<uint4*>(sm + OFF_S + (qq >> 1) * 16384 + sw128(row, 4 * (qq & 1) + c)) = pack8(f);
         }
     };
     write_state_operand();
@@ -296,40 +287,46 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         const float* sBeta = sBetaBuf + 64 * buf;
         cp_async_wait_all();
         __syncthreads();
-        // ---- (1) running sum of g per key channel (two halves of 32 tokens), block references
+        // ---- (1) running sum of g per key channel: thread (c, qq) sums the 16 tokens of block qq
         {
-            const int c = tid & 127, i0 = 32 * half;
+            const int c = row;
             float acc = 0.f;
-#pragma unroll 8
-            for (int i = i0; i < i0 + 32; ++i) {
+#pragma unroll
+            for (int i = 16 * qq; i < 16 * qq + 16; ++i) {
                 acc += sG[i * kD + c];
                 sG[i * kD + c] = acc;
             }
+            sTot[qq * kD + c] = acc;
             __syncthreads();
-            if (half == 1) {
-                const float base = sG[31 * kD + c];
-#pragma unroll 8
-                for (int i = 32; i < 64; ++i) sG[i * kD + c] += base;
+            float base = 0.f;
+#pragma unroll
+            for (int p2 = 0; p2 < 3; ++p2)
+                if (p2 < qq) base += sTot[p2 * kD + c];
+            if (qq > 0) {
+#pragma unroll
+                for (int i = 16 * qq; i < 16 * qq + 16; ++i) sG[i * kD + c] += base;
             }
+            sE[qq * kD + c] = base + acc;  // G at the last token of block qq
             __syncthreads();
-            if (half == 0) {
+            if (qq == 0) {
                 float e[4];
 #pragma unroll
-                for (int I = 0; I < 4; ++I) { e[I] = sG[(16 * I + 15) * kD + c]; sE[I * kD + c] = e[I]; }
+                for (int I = 0; I < 4; ++I) e[I] = sE[I * kD + c];
                 sEGl[c] = expf(e[3]);
-                // e^{E_J - E_I}, J > I: (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
                 sDt[0 * kD + c] = __expf(e[1] - e[0]);
                 sDt[1 * kD + c] = __expf(e[2] - e[0]);
                 sDt[2 * kD + c] = __expf(e[3] - e[0]);
-                sDt[3 * kD + c] = __expf(e[2] - e[1]);
-                sDt[4 * kD + c] = __expf(e[3] - e[1]);
-                sDt[5 * kD + c] = __expf(e[3] - e[2]);
+            } else if (qq == 1) {
+                const float e1 = sE[1 * kD + c], e2 = sE[2 * kD + c], e3 = sE[3 * kD + c];
+                sDt[3 * kD + c] = __expf(e2 - e1);
+                sDt[4 * kD + c] = __expf(e3 - e1);
+                sDt[5 * kD + c] = __expf(e3 - e2);
             }
             __syncthreads();
         }
         // ---- (2) operands: row operand RR, column operands CC / KP, B1 = [beta K e^G ; Q e^G]
-#pragma unroll 1
-        for (int m = 0; m < 4; ++m) {
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
             const int id = tid + kThreads * m, i = id >> 4, cc = id & 15, c = cc * 8, I = i >> 4;
             const uint32_t reg = cc >> 3, ch = cc & 7;
             float kv[8], qv[8], Gv[8], Ev[8];
@@ -397,45 +394,25 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
             mma_commit(barS);
         }
         wait_bar(barA, phaseA);
-        // ---- (4) A_kk (fp32 work array) and A_qk (bf16 operand)
-        {
-            // lane quarter q holds rows 32q .. 32q+31 of [k-rows ; q-rows]: lanes 0-15 belong to row block
-            // 2(q%2) and lanes 16-31 to 2(q%2)+1; warp half 0 reads the first block's columns, half 1 the second's.
-            const int qtr = warp & 3, Ib = 2 * (qtr & 1) + half;  // row block whose columns this warp reads
-            const bool mine = ((lane >> 4) == half);              // lanes whose row lies in block Ib
-            const int r = 32 * qtr + lane;                        // TMEM lane
-            const int i = r & 63;                                 // token row in the chunk
+        // ---- (4) A_kk (fp32 work array) and A_qk (bf16 operand); warps of key quarters 0, 1
+        if (qq < 2) {
+            // lane quarter qt holds rows 32qt .. 32qt+31 of [k-rows ; q-rows]: lanes 0-15 belong to row block
+            // 2(qt%2) and lanes 16-31 to 2(qt%2)+1; warps with qq = 0 read the first block's columns, qq = 1 the second's.
+            const int qt = warp & 3, Ib = 2 * (qt & 1) + qq;
+            const bool mine = ((lane >> 4) == qq);
+            const int r = 32 * qt + lane;
+            const int i = r & 63;
             const bool is_k = r < 64;
+            // 64 columns from the block's first column; those past its 16(Ib+1) are masked below
+            const uint32_t col0 = Ib == 0 ? TM_A0 : (Ib == 1 ? TM_A1 : (Ib == 2 ? TM_A2 : TM_A3));
             uint32_t a[64];
             {
                 uint32_t t0[32], t1[32];
-                if (Ib == 0) {
-                    uint32_t x[16];
-                    tmem_ld16_async(tbase + lane_base + TM_A0, x);
-                    tmem_wait_ld(); reg_fence(x);
+                tmem_ld32_async(tbase + lane_base + col0, t0);
+                tmem_ld32_async(tbase + lane_base + col0 + 32, t1);
+                tmem_wait_ld(); reg_fence(t0); reg_fence(t1);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) a[e] = x[e];
-                } else if (Ib == 1) {
-                    tmem_ld32_async(tbase + lane_base + TM_A1, t0);
-                    tmem_wait_ld(); reg_fence(t0);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) a[e] = t0[e];
-                } else if (Ib == 2) {
-                    uint32_t x[16];
-                    tmem_ld32_async(tbase + lane_base + TM_A2, t0);
-                    tmem_ld16_async(tbase + lane_base + TM_A2 + 32, x);
-                    tmem_wait_ld(); reg_fence(t0); reg_fence(x);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) a[e] = t0[e];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) a[32 + e] = x[e];
-                } else {
-                    tmem_ld32_async(tbase + lane_base + TM_A3, t0);
-                    tmem_ld32_async(tbase + lane_base + TM_A3 + 32, t1);
-                    tmem_wait_ld(); reg_fence(t0); reg_fence(t1);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) { a[e] = t0[e]; a[32 + e] = t1[e]; }
-                }
+                for (int e = 0; e < 32; ++e) { a[e] = t0[e]; a[32 + e] = t1[e]; }
             }
             const int ncols = 16 * (Ib + 1);
             if (mine) {
@@ -468,60 +445,51 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         }
         __syncthreads();
         // ---- (5) T = (I + A_kk)^-1 by 16 x 16 blocks (fp32)
-        if (lane < 16 && warp < 4) {  // diagonal block `warp`, column `lane`
+        if (lane < 16 && warp < 4) {  // diagonal block `warp`, column `lane`, right-looking (independent updates)
             const int I = warp, c = lane;
             const float* A = sAkk + 16 * I * kAS + 16 * I;
             float x[16];
 #pragma unroll
-            for (int r2 = 0; r2 < 16; ++r2) {
-                float acc = (r2 == c) ? 1.f : 0.f;
+            for (int r2 = 0; r2 < 16; ++r2) x[r2] = (r2 == c) ? 1.f : 0.f;
 #pragma unroll
-                for (int m2 = 0; m2 < r2; ++m2) acc = fmaf(-A[r2 * kAS + m2], x[m2], acc);
-                x[r2] = acc;
-            }
+            for (int r2 = 0; r2 < 16; ++r2)
+#pragma unroll
+                for (int r3 = r2 + 1; r3 < 16; ++r3) x[r3] = fmaf(-A[r3 * kAS + r2], x[r2], x[r3]);
 #pragma unroll
             for (int r2 = 0; r2 < 16; ++r2) sTf[(16 * I + r2) * kAS + 16 * I + c] = x[r2];
         }
         __syncthreads();
-        t_level<1>(sAkk, sTf, sYs, tid);
-        t_level<2>(sAkk, sTf, sYs, tid);
-        t_level<3>(sAkk, sTf, sYs, tid);
+        if (warp < 6) t_column(sAkk, sTf, sYs + warp * 128, warp, lane);  // block column 3 has nothing below
+        __syncthreads();
         {   // T as a bf16 operand (zero above the diagonal blocks); read all of T before writing over its tail
-            float f[2][8];
+            const int i = tid >> 3, ch = tid & 7;
+            float f[8];
+            if ((ch >> 1) > (i >> 4)) {
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int id = tid + kThreads * u, i = id >> 3, ch = id & 7;
-                if ((ch >> 1) > (i >> 4)) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) f[u][e] = 0.f;
-                } else {
-                    *reinterpret_cast<float4*>(f[u]) = *reinterpret_cast<const float4*>(sTf + i * kAS + 8 * ch);
-                    *reinterpret_cast<float4*>(f[u] + 4) = *reinterpret_cast<const float4*>(sTf + i * kAS + 8 * ch + 4);
-                }
+                for (int e = 0; e < 8; ++e) f[e] = 0.f;
+            } else {
+                *reinterpret_cast<float4*>(f) = *reinterpret_cast<const float4*>(sTf + i * kAS + 8 * ch);
+                *reinterpret_cast<float4*>(f + 4) = *reinterpret_cast<const float4*>(sTf + i * kAS + 8 * ch + 4);
             }
             __syncthreads();
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int id = tid + kThreads * u, i = id >> 3, ch = id & 7;
-                *reinterpret_cast<uint4*>(sm + OFF_TB + sw128(i, ch)) = pack8(f[u]);
-            }
+            *reinterpret_cast<uint4*>(sm + OFF_TB + sw128(i, ch)) = pack8(f);
         }
-        // ---- Z^T = (beta V)^T - Y^T once the S0 products are done
+        // ---- Z^T = (beta V)^T - Y^T once the S0 products are done; thread (row, qq) owns tokens 16qq .. 16qq+15
         wait_bar(barS, phaseS);
         {
-            uint32_t y[32];
-            tmem_ld32_async(tbase + lane_base + TM_Y + 32 * half, y);
+            uint32_t y[16];
+            tmem_ld16_async(tbase + lane_base + TM_Y + 16 * qq, y);
             tmem_wait_ld(); reg_fence(y);
             const __nv_bfloat16* sv = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STV);
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
+            for (int c2 = 0; c2 < 2; ++c2) {
                 float f[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const int j = 32 * half + 8 * c4 + e;
-                    f[e] = sBeta[j] * __bfloat162float(sv[j * kD + row]) - __uint_as_float(y[8 * c4 + e]);
+                    const int j = 16 * qq + 8 * c2 + e;
+                    f[e] = sBeta[j] * __bfloat162float(sv[j * kD + row]) - __uint_as_float(y[8 * c2 + e]);
                 }
-                *reinterpret_cast<uint4*>(sm + OFF_Z + sw128(row, 4 * half + c4)) = pack8(f);
+                *reinterpret_cast<uint4*>(sm + OFF_Z + sw128(row, 2 * qq + c2)) = pack8(f);
             }
         }
         fence_proxy_async();
@@ -539,15 +507,15 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         }
         wait_mma();
         {
-            uint32_t x[32];
-            tmem_ld32_async(tbase + lane_base + TM_V + 32 * half, x);
+            uint32_t x[16];
+            tmem_ld16_async(tbase + lane_base + TM_V + 16 * qq, x);
             tmem_wait_ld(); reg_fence(x);
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
+            for (int c2 = 0; c2 < 2; ++c2) {
                 float f[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(x[8 * c4 + e]);
-                *reinterpret_cast<uint4*>(sm + OFF_Z + sw128(row, 4 * half + c4)) = pack8(f);
+                for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(x[8 * c2 + e]);
+                *reinterpret_cast<uint4*>(sm + OFF_Z + sw128(row, 2 * qq + c2)) = pack8(f);
             }
         }
         fence_proxy_async();
@@ -566,24 +534,20 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         wait_mma();
         // ---- (8) outputs (fp32 staging, then coalesced) and the state update
         {
-            uint32_t xo[32], d0[32], d1[32];
-            tmem_ld32_async(tbase + lane_base + TM_O + 32 * half, xo);
-            tmem_ld32_async(tbase + lane_base + TM_DS + 64 * half, d0);
-            tmem_ld32_async(tbase + lane_base + TM_DS + 64 * half + 32, d1);
-            tmem_wait_ld(); reg_fence(xo); reg_fence(d0); reg_fence(d1);
+            uint32_t xo[16], d0[32];
+            tmem_ld16_async(tbase + lane_base + TM_O + 16 * qq, xo);
+            tmem_ld32_async(tbase + lane_base + TM_DS + 32 * qq, d0);
+            tmem_wait_ld(); reg_fence(xo); reg_fence(d0);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) sO[(32 * half + e) * kD + row] = scale * __uint_as_float(xo[e]);
+            for (int e = 0; e < 16; ++e) sO[(16 * qq + e) * kD + row] = scale * __uint_as_float(xo[e]);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                s[e] = fmaf(s[e], sEGl[64 * half + e], __uint_as_float(d0[e]));
-                s[32 + e] = fmaf(s[32 + e], sEGl[64 * half + 32 + e], __uint_as_float(d1[e]));
-            }
+            for (int e = 0; e < 32; ++e) s[e] = fmaf(s[e], sEGl[32 * qq + e], __uint_as_float(d0[e]));
         }
         write_state_operand();
         tc_fence_before();
         __syncthreads();
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
+        for (int m = 0; m < 2; ++m) {
             const int id = tid + kThreads * m, j = id >> 4, c16 = id & 15;
             if (j < L) {
                 float f[8];
@@ -605,7 +569,7 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     cp_async_wait_all();
     if (final_state && !*sAbort) {
 #pragma unroll
-        for (int j = 0; j < 64; j += 4)
+        for (int j = 0; j < 32; j += 4)
             *reinterpret_cast<float4*>(final_state + state_off + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
     }
     tc_fence_before();
