@@ -32,9 +32,8 @@
 // the A operand of the S0 products, so every product has M = 128 = dv and maps
 // row r to TMEM lane r.  All tensor-core products take bf16 operands and
 // accumulate in fp32 in TMEM.  T = (I + A_kk)^-1 is computed in fp32 on the CUDA
-// cores by 16 x 16 blocks: the four diagonal blocks by forward substitution, then
-// the blocks below them, T_IJ = -T_II sum_{M=J..I-1} A_IM T_MJ, one block column per
-// warp pair.
+// cores by 16 x 16 blocks: the four diagonal blocks D by forward substitution, then
+// the blocks below them as (I - N + N^2 - N^3) D with N = D A_below (N^4 = 0).
 //
 // One CTA of 16 warps per (sequence, head) walks the chunks in order; thread
 // (r, quarter) holds state row r, key channels [32 quarter, 32 quarter + 32).  The
@@ -53,6 +52,14 @@ constexpr int kC = kChunk;    // 64
 constexpr int kD = kHeadDim;  // 128
 constexpr int kAS = 68;       // fp32 row stride of the A_kk / T work arrays (float4 rows on distinct banks)
 constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^x by the hardware approximation (relative error about 2^-22; results below 2^-126 flush to 0)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // shared-memory map (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_STK = 0;        // k staging bf16 [64][128]
@@ -77,7 +84,6 @@ constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // slack for aligning the b
 
 // After the A products complete (the S0 products may still be running and read B1):
 constexpr uint32_t OFF_AQ = OFF_RR + 64 * kAS * 4;   // A_qk operand [64][64] (8 KB), after A_kk fp32 [64][kAS]
-constexpr uint32_t OFF_YS = OFF_AQ + 8192;           // per-warp scratch fp32 [6][16][8]
 constexpr uint32_t OFF_TF = OFF_CC;                  // T fp32 [64][kAS] (17 KB)
 constexpr uint32_t OFF_TB = OFF_CC + 16384;          // T operand [64][64] (8 KB), written once T is in registers
 constexpr uint32_t OFF_Z = OFF_CC;                   // Z^T, then V'^T [128][64] (16 KB), after T is consumed
@@ -92,7 +98,7 @@ constexpr uint32_t TM_O = 320;
 constexpr uint32_t TM_DS = 384;   // delta S
 constexpr uint32_t kTmemCols = 512;
 
-static_assert(OFF_AQ % 1024 == 0 && OFF_YS + 6 * 128 * 4 <= OFF_CC, "T work overflows its region");
+static_assert(OFF_AQ % 1024 == 0 && OFF_AQ + 8192 <= OFF_CC, "T work overflows its region");
 static_assert(OFF_TF + 64 * kAS * 4 <= OFF_S && OFF_TB + 8192 <= OFF_S, "T operand overflows its region");
 static_assert(kSmemBytes <= 232448, "shared memory");
 
@@ -105,25 +111,28 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
     return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
 }
 
-// D (+)= A B^T with a K = 128 (two-region) A of 128 rows and a K-major two-region B.
-__device__ __forceinline__ void mma_k128(uint32_t d, uint32_t a_base, uint32_t a_region, uint32_t b_base,
+// D (+)= A B^T with a K = 128 (two-region) A of 128 rows and a K-major two-region B.  The
+// descriptors of the operands' first bytes are passed in; moving the start address by `off`
+// bytes adds off / 16 to the descriptor (shared addresses stay below 2^18, so no carry).
+__device__ __forceinline__ void mma_k128(uint32_t d, uint64_t a_desc, uint32_t a_region, uint64_t b_desc,
                                          uint32_t b_region, uint32_t idesc) {
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
         const uint32_t reg = ks >> 2, off = (ks & 3) * 32;
-        mma_bf16(d, sdesc_sw128(a_base + reg * a_region + off, 16, 1024), sdesc_sw128(b_base + reg * b_region + off, 16, 1024),
-                 idesc, ks > 0 ? 1u : 0u);
+        mma_bf16(d, a_desc + ((reg * a_region + off) >> 4), b_desc + ((reg * b_region + off) >> 4), idesc,
+                 ks > 0 ? 1u : 0u);
     }
 }
 
 // D (+)= A B^T with a K = 64 (one-region) A and a K-major one-region B.
-__device__ __forceinline__ void mma_k64(uint32_t d, uint32_t a_base, uint32_t b_base, uint32_t idesc,
+__device__ __forceinline__ void mma_k64(uint32_t d, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                         bool accumulate_first) {
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(d, sdesc_sw128(a_base + ks * 32, 16, 1024), sdesc_sw128(b_base + ks * 32, 16, 1024), idesc,
-                 (ks > 0 || accumulate_first) ? 1u : 0u);
+        mma_bf16(d, a_desc + ks * 2, b_desc + ks * 2, idesc, (ks > 0 || accumulate_first) ? 1u : 0u);
 }
+
+__device__ __forceinline__ uint64_t kdesc(uint32_t saddr) { return sdesc_sw128(saddr, 16, 1024); }
 
 // cp.async of chunk [c0, c0 + L) of one head: k, q, g (and beta into beta_dst), or v.
 __device__ __forceinline__ void prefetch_kqg(uint8_t* sm, float* beta_dst, const __nv_bfloat16* k,
@@ -159,41 +168,87 @@ __device__ __forceinline__ void prefetch_v(uint8_t* sm, const __nv_bfloat16* v, 
     }
 }
 
-// Blocks of T below the diagonal, one block column per warp pair: warp `w` (0..7) owns block
-// column J = w / 2, columns 8 (w % 2) .. 8 (w % 2) + 7 of it, and walks down it:
-//   T_IJ = -T_II Y,  Y = sum_{M = J}^{I-1} A_IM T_MJ,  I = J+1 .. 3
-// Everything a warp reads is either a diagonal block (written before the block barrier that
-// precedes this call) or an earlier block of its own columns, so warps only sync with themselves.
-// Lane l holds rows l / 2 and four columns 4 (l % 2) .. +3 of the warp's eight; Y goes through
-// the warp's own 16 x 8 scratch tile.
-__device__ __forceinline__ void t_column(const float* sAkk, float* sTf, float* sYw, int warp, int lane) {
-    const int J = warp >> 1, c0 = 16 * J + 8 * (warp & 1) + 4 * (lane & 1), r = lane >> 1;
-    for (int I = J + 1; I < 4; ++I) {
-        const float* Ar = sAkk + (16 * I + r) * kAS + 16 * J;
-        const float* Tc = sTf + 16 * J * kAS + c0;
-        float4 y4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        const int terms = 16 * (I - J);
-#pragma unroll 8
-        for (int m = 0; m < terms; ++m) {
-            const float a = Ar[m];
-            const float4 t4 = *reinterpret_cast<const float4*>(Tc + m * kAS);
-            y4.x = fmaf(a, t4.x, y4.x); y4.y = fmaf(a, t4.y, y4.y);
-            y4.z = fmaf(a, t4.z, y4.z); y4.w = fmaf(a, t4.w, y4.w);
+// One 16 x 16 fp32 block product for 64 threads (t = 0..63 owns row t / 4, columns 4 (t % 4) .. +3):
+//   out = sign * (A0 + w1 A1 + w2 A2) B  [+ A3 B3]
+// NA = number of A blocks combined on the fly (an entry of P = -N + N^2 - N^3); SECOND adds A3 B3.
+struct Blk {
+    const float* p;
+    int ld;
+};
+template <int NA, bool SECOND>
+__device__ __forceinline__ void blk_mma(float* out, int ldo, float sign, Blk a0, Blk a1, float w1, Blk a2, float w2,
+                                        Blk b, Blk a3, Blk b3, int t) {
+    const int r = t >> 2, c = 4 * (t & 3);
+    float av[16];
+#pragma unroll
+    for (int m = 0; m < 16; m += 4) {
+        float4 x = *reinterpret_cast<const float4*>(a0.p + r * a0.ld + m);
+        if (NA > 1) {
+            const float4 y = *reinterpret_cast<const float4*>(a1.p + r * a1.ld + m);
+            x.x = fmaf(w1, y.x, x.x); x.y = fmaf(w1, y.y, x.y); x.z = fmaf(w1, y.z, x.z); x.w = fmaf(w1, y.w, x.w);
         }
-        *reinterpret_cast<float4*>(sYw + r * 8 + 4 * (lane & 1)) = y4;
-        __syncwarp();
-        const float* Tr = sTf + (16 * I + r) * kAS + 16 * I;
-        float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (NA > 2) {
+            const float4 y = *reinterpret_cast<const float4*>(a2.p + r * a2.ld + m);
+            x.x = fmaf(w2, y.x, x.x); x.y = fmaf(w2, y.y, x.y); x.z = fmaf(w2, y.z, x.z); x.w = fmaf(w2, y.w, x.w);
+        }
+        av[m] = x.x; av[m + 1] = x.y; av[m + 2] = x.z; av[m + 3] = x.w;
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), acc2 = acc;
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        const float4 bv = *reinterpret_cast<const float4*>(b.p + m * b.ld + c);
+        float4& ac = (m & 1) ? acc2 : acc;
+        ac.x = fmaf(av[m], bv.x, ac.x); ac.y = fmaf(av[m], bv.y, ac.y);
+        ac.z = fmaf(av[m], bv.z, ac.z); ac.w = fmaf(av[m], bv.w, ac.w);
+    }
+    if (SECOND) {
+#pragma unroll
+        for (int m = 0; m < 16; m += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(a3.p + r * a3.ld + m);
+            av[m] = x.x; av[m + 1] = x.y; av[m + 2] = x.z; av[m + 3] = x.w;
+        }
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
-            const float a = Tr[m];
-            const float4 yv = *reinterpret_cast<const float4*>(sYw + m * 8 + 4 * (lane & 1));
-            t4.x = fmaf(a, yv.x, t4.x); t4.y = fmaf(a, yv.y, t4.y);
-            t4.z = fmaf(a, yv.z, t4.z); t4.w = fmaf(a, yv.w, t4.w);
+            const float4 bv = *reinterpret_cast<const float4*>(b3.p + m * b3.ld + c);
+            float4& ac = (m & 1) ? acc2 : acc;
+            ac.x = fmaf(av[m], bv.x, ac.x); ac.y = fmaf(av[m], bv.y, ac.y);
+            ac.z = fmaf(av[m], bv.z, ac.z); ac.w = fmaf(av[m], bv.w, ac.w);
         }
-        *reinterpret_cast<float4*>(sTf + (16 * I + r) * kAS + c0) = make_float4(-t4.x, -t4.y, -t4.z, -t4.w);
-        __syncwarp();
     }
+    *reinterpret_cast<float4*>(out + r * ldo + c) = make_float4(sign * (acc.x + acc2.x), sign * (acc.y + acc2.y),
+                                                                  sign * (acc.z + acc2.z), sign * (acc.w + acc2.w));
+}
+
+// Blocks of T below the diagonal.  With D = diag(T_00 .. T_33) (inverses of the diagonal blocks of
+// I + A_kk) and N = D A_off (A_off: the blocks of A_kk below the diagonal; N is strictly block-lower,
+// so N^4 = 0):  (I + A_kk)^-1 = (I + N)^-1 D = (I - N + N^2 - N^3) D.
+// Four levels, each a set of independent 16 x 16 products spread over the CTA's warps.
+constexpr int kNB = 20;  // row stride of the N blocks (float4 rows, eight rows on distinct banks)
+__device__ __forceinline__ void t_offdiag(const float* A, float* T, float* nb, int tid) {
+    const int u = tid >> 6, t = tid & 63;
+    auto Ablk = [&](int I, int J) { return Blk{A + 16 * I * kAS + 16 * J, kAS}; };
+    auto Tblk = [&](int I, int J) { return Blk{T + 16 * I * kAS + 16 * J, kAS}; };
+    // N_IJ at nb[slot]: (1,0) 0, (2,0) 1, (3,0) 2, (2,1) 3, (3,1) 4, (3,2) 5; N^2: (2,0) 6, (3,1) 7, (3,0) 8; N^3 (3,0) 9
+    auto Nb = [&](int slot) { return Blk{nb + slot * 16 * kNB, kNB}; };
+    const Blk none{nullptr, 0};
+    if (u < 6) {  // slots 0..5: (1,0) (2,0) (3,0) (2,1) (3,1) (3,2)
+        const int I = u < 3 ? u + 1 : (u < 5 ? u - 1 : 3), J = u < 3 ? 0 : (u < 5 ? 1 : 2);
+        blk_mma<1, false>(nb + u * 16 * kNB, kNB, 1.f, Tblk(I, I), none, 0.f, none, 0.f, Ablk(I, J), none, none, t);
+    }
+    __syncthreads();
+    if (u == 0) blk_mma<1, false>(nb + 6 * 16 * kNB, kNB, 1.f, Nb(3), none, 0.f, none, 0.f, Nb(0), none, none, t);   // N21 N10
+    if (u == 1) blk_mma<1, false>(nb + 7 * 16 * kNB, kNB, 1.f, Nb(5), none, 0.f, none, 0.f, Nb(3), none, none, t);   // N32 N21
+    if (u == 2) blk_mma<1, true>(nb + 8 * 16 * kNB, kNB, 1.f, Nb(4), none, 0.f, none, 0.f, Nb(0), Nb(5), Nb(1), t);  // N31 N10 + N32 N20
+    if (u == 3) blk_mma<1, false>(T + 16 * kAS * 1 + 0, kAS, -1.f, Nb(0), none, 0.f, none, 0.f, Tblk(0, 0), none, none, t);   // T10
+    if (u == 4) blk_mma<1, false>(T + 16 * kAS * 2 + 16, kAS, -1.f, Nb(3), none, 0.f, none, 0.f, Tblk(1, 1), none, none, t);  // T21
+    if (u == 5) blk_mma<1, false>(T + 16 * kAS * 3 + 32, kAS, -1.f, Nb(5), none, 0.f, none, 0.f, Tblk(2, 2), none, none, t);  // T32
+    __syncthreads();
+    if (u == 0) blk_mma<1, false>(nb + 9 * 16 * kNB, kNB, 1.f, Nb(5), none, 0.f, none, 0.f, Nb(6), none, none, t);   // N32 N^2_20
+    if (u == 1) blk_mma<2, false>(T + 16 * kAS * 2 + 0, kAS, 1.f, Nb(6), Nb(1), -1.f, none, 0.f, Tblk(0, 0), none, none, t);  // T20
+    if (u == 2) blk_mma<2, false>(T + 16 * kAS * 3 + 16, kAS, 1.f, Nb(7), Nb(4), -1.f, none, 0.f, Tblk(1, 1), none, none, t); // T31
+    __syncthreads();
+    if (u == 0) blk_mma<3, false>(T + 16 * kAS * 3 + 0, kAS, 1.f, Nb(8), Nb(2), -1.f, Nb(9), -1.f, Tblk(0, 0), none, none, t); // T30
+    __syncthreads();
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -217,7 +272,6 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     float* sG = reinterpret_cast<float*>(sm + OFF_STG);
     float* sAkk = reinterpret_cast<float*>(sm + OFF_RR);
     float* sTf = reinterpret_cast<float*>(sm + OFF_TF);
-    float* sYs = reinterpret_cast<float*>(sm + OFF_YS);
     float* sO = reinterpret_cast<float*>(sm + OFF_RR);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -292,8 +346,8 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
             const int c = row;
             float acc = 0.f;
 #pragma unroll
-            for (int i = 16 * qq; i < 16 * qq + 16; ++i) {
-                acc += sG[i * kD + c];
+            for (int i = 16 * qq; i < 16 * qq + 16; ++i) {  // in log2 units: every use is a power of e
+                acc = fmaf(sG[i * kD + c], kLog2e, acc);
                 sG[i * kD + c] = acc;
             }
             sTot[qq * kD + c] = acc;
@@ -312,15 +366,15 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
                 float e[4];
 #pragma unroll
                 for (int I = 0; I < 4; ++I) e[I] = sE[I * kD + c];
-                sEGl[c] = expf(e[3]);
-                sDt[0 * kD + c] = __expf(e[1] - e[0]);
-                sDt[1 * kD + c] = __expf(e[2] - e[0]);
-                sDt[2 * kD + c] = __expf(e[3] - e[0]);
+                sEGl[c] = exp2f(e[3]);
+                sDt[0 * kD + c] = ex2(e[1] - e[0]);
+                sDt[1 * kD + c] = ex2(e[2] - e[0]);
+                sDt[2 * kD + c] = ex2(e[3] - e[0]);
             } else if (qq == 1) {
                 const float e1 = sE[1 * kD + c], e2 = sE[2 * kD + c], e3 = sE[3 * kD + c];
-                sDt[3 * kD + c] = __expf(e2 - e1);
-                sDt[4 * kD + c] = __expf(e3 - e1);
-                sDt[5 * kD + c] = __expf(e3 - e2);
+                sDt[3 * kD + c] = ex2(e2 - e1);
+                sDt[4 * kD + c] = ex2(e3 - e1);
+                sDt[5 * kD + c] = ex2(e3 - e2);
             }
             __syncthreads();
         }
@@ -340,9 +394,9 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
             float rk[8], rq[8], bk[8], eq[8], kr[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const float f = __expf(Gv[e] - Ev[e]);   // >= 1
-                const float r = __expf(Ev[e] - Gv[e]);   // <= 1
-                const float eg = __expf(Gv[e]);          // <= 1
+                const float f = ex2(Gv[e] - Ev[e]);   // >= 1
+                const float r = ex2(Ev[e] - Gv[e]);   // <= 1
+                const float eg = ex2(Gv[e]);          // <= 1
                 rk[e] = kv[e] * f;
                 rq[e] = qv[e] * f;
                 bk[e] = b * kv[e] * eg;
@@ -382,15 +436,13 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         // ---- (3) the four row blocks of A (barrier A), then the S0 products (barrier S)
         if (tid == 0) {
             tc_fence_after();
-            mma_k128(tbase + TM_A0, sbase + OFF_RR, 16384, sbase + OFF_CC + cc_off(0), 2048,
-                     idesc_bf16_f32(128, 16, false, false));
-            mma_k128(tbase + TM_A1, sbase + OFF_RR, 16384, sbase + OFF_CC + cc_off(1), 4096,
-                     idesc_bf16_f32(128, 32, false, false));
-            mma_k128(tbase + TM_A2, sbase + OFF_RR, 16384, sbase + OFF_CC + cc_off(2), 6144,
-                     idesc_bf16_f32(128, 48, false, false));
-            mma_k128(tbase + TM_A3, sbase + OFF_RR, 16384, sbase + OFF_KP, 8192, idesc_bf16_f32(128, 64, false, false));
+            const uint64_t rr = kdesc(sbase + OFF_RR);
+            mma_k128(tbase + TM_A0, rr, 16384, kdesc(sbase + OFF_CC + cc_off(0)), 2048, idesc_bf16_f32(128, 16, false, false));
+            mma_k128(tbase + TM_A1, rr, 16384, kdesc(sbase + OFF_CC + cc_off(1)), 4096, idesc_bf16_f32(128, 32, false, false));
+            mma_k128(tbase + TM_A2, rr, 16384, kdesc(sbase + OFF_CC + cc_off(2)), 6144, idesc_bf16_f32(128, 48, false, false));
+            mma_k128(tbase + TM_A3, rr, 16384, kdesc(sbase + OFF_KP), 8192, idesc_bf16_f32(128, 64, false, false));
             mma_commit(barA);
-            mma_k128(tbase + TM_Y, sbase + OFF_S, 16384, sbase + OFF_B1, 16384, id_s);
+            mma_k128(tbase + TM_Y, kdesc(sbase + OFF_S), 16384, kdesc(sbase + OFF_B1), 16384, id_s);
             mma_commit(barS);
         }
         wait_bar(barA, phaseA);
@@ -459,8 +511,8 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
             for (int r2 = 0; r2 < 16; ++r2) sTf[(16 * I + r2) * kAS + 16 * I + c] = x[r2];
         }
         __syncthreads();
-        if (warp < 6) t_column(sAkk, sTf, sYs + warp * 128, warp, lane);  // block column 3 has nothing below
-        __syncthreads();
+        wait_bar(barS, phaseS);  // the S0 products are done: B1 becomes scratch for the N blocks
+        t_offdiag(sAkk, sTf, reinterpret_cast<float*>(sm + OFF_B1), tid);
         {   // T as a bf16 operand (zero above the diagonal blocks); read all of T before writing over its tail
             const int i = tid >> 3, ch = tid & 7;
             float f[8];
@@ -474,8 +526,7 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
             __syncthreads();
             *reinterpret_cast<uint4*>(sm + OFF_TB + sw128(i, ch)) = pack8(f);
         }
-        // ---- Z^T = (beta V)^T - Y^T once the S0 products are done; thread (row, qq) owns tokens 16qq .. 16qq+15
-        wait_bar(barS, phaseS);
+        // ---- Z^T = (beta V)^T - Y^T; thread (row, qq) owns tokens 16qq .. 16qq+15
         {
             uint32_t y[16];
             tmem_ld16_async(tbase + lane_base + TM_Y + 16 * qq, y);
@@ -502,7 +553,7 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         // ---- (6) V'^T = Z^T T^T
         if (tid == 0) {
             tc_fence_after();
-            mma_k64(tbase + TM_V, sbase + OFF_Z, sbase + OFF_TB, id_64, false);
+            mma_k64(tbase + TM_V, kdesc(sbase + OFF_Z), kdesc(sbase + OFF_TB), id_64, false);
             mma_commit(barS);
         }
         wait_mma();
@@ -524,11 +575,11 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         // ---- (7) O^T += V'^T A_qk^T;  dS = V'^T (K e^{G_C - G})
         if (tid == 0) {
             tc_fence_after();
-            mma_k64(tbase + TM_O, sbase + OFF_Z, sbase + OFF_AQ, id_64, true);
+            mma_k64(tbase + TM_O, kdesc(sbase + OFF_Z), kdesc(sbase + OFF_AQ), id_64, true);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tbase + TM_DS, sdesc_sw128(sbase + OFF_Z + ks * 32, 16, 1024),
-                         sdesc_sw128(sbase + OFF_KP + ks * 2048, 8192, 1024), id_ds, ks > 0 ? 1u : 0u);
+                mma_bf16(tbase + TM_DS, kdesc(sbase + OFF_Z) + ks * 2, sdesc_sw128(sbase + OFF_KP, 8192, 1024) + ks * 128,
+                         id_ds, ks > 0 ? 1u : 0u);
             mma_commit(barS);
         }
         wait_mma();
