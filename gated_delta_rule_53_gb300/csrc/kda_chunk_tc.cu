@@ -39,6 +39,11 @@
 // (r, quarter) holds state row r, key channels [32 quarter, 32 quarter + 32).  The
 // next chunk's inputs are copied into shared memory with cp.async while the
 // current chunk computes (k, q, g once the operands are built, v once Z is built).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "kda_common.cuh"
 #include "kda_tc.cuh"
 
@@ -77,8 +82,8 @@ constexpr uint32_t OFF_E = OFF_BETA + 512;           // fp32 [4][128] E_I = G at
 constexpr uint32_t OFF_DT = OFF_E + 2048;            // fp32 [6][128] e^{E_J - E_I}, J > I
 constexpr uint32_t OFF_EGL = OFF_DT + 3072;          // fp32 [128] e^{G_C}
 constexpr uint32_t OFF_TOT = OFF_EGL + 512;          // fp32 [4][128] per-block sums of g
-constexpr uint32_t OFF_BAR = OFF_TOT + 2048;         // two mbarriers: A products, state products
-constexpr uint32_t OFF_MISC = OFF_BAR + 16;          // TMEM base, abort flag
+constexpr uint32_t OFF_BAR = OFF_TOT + 2048;         // mbarriers: A products, state products, k/q/g tiles, v tile
+constexpr uint32_t OFF_MISC = OFF_BAR + 32;          // TMEM base, abort flag
 constexpr uint32_t kSmemUsed = OFF_MISC + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // slack for aligning the base
 
@@ -134,23 +139,23 @@ __device__ __forceinline__ void mma_k64(uint32_t d, uint64_t a_desc, uint64_t b_
 
 __device__ __forceinline__ uint64_t kdesc(uint32_t saddr) { return sdesc_sw128(saddr, 16, 1024); }
 
-// cp.async of chunk [c0, c0 + L) of one head: k, q, g (and beta into beta_dst), or v.
-__device__ __forceinline__ void prefetch_kqg(uint8_t* sm, float* beta_dst, const __nv_bfloat16* k,
-                                             const __nv_bfloat16* q, const float* g, const float* beta, int64_t c0,
-                                             int L, int H, int h, int tid) {
-#pragma unroll
-    for (int m = 0; m < 2; ++m) {
-        const int id = tid + kThreads * m, i = id >> 4, cc = id & 15;
-        const bool ok = i < L;
-        const int64_t at = ok ? ((c0 + i) * H + h) * kD + cc * 8 : 0;
-        cp_async16(sm + OFF_STK + i * 256 + cc * 16, k + at, ok ? 16u : 0u);
-        cp_async16(sm + OFF_STQ + i * 256 + cc * 16, q + at, ok ? 16u : 0u);
-    }
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        const int id = tid + kThreads * m, i = id >> 5, cc = id & 31;
-        const bool ok = i < L;
-        cp_async16(sm + OFF_STG + i * 512 + cc * 16, g + (ok ? ((c0 + i) * H + h) * kD + cc * 4 : 0), ok ? 16u : 0u);
+// Loads of the chunk starting at token c0 of head h.  Thread 0 issues one TMA box per tensor
+// ([64 tokens][1 head][128 channels]; rows past the end of the tensor read as zero) and arms the
+// stage's mbarrier with the byte count; beta (64 strided words) comes by cp.async, zero past the
+// chunk's L tokens.  Rows past L that belong to the next packed sequence are harmless in k, q
+// and v (their beta is zero) and g is masked where it is summed.
+constexpr uint32_t kKQGBytes = 2 * 16384 + 32768;
+constexpr uint32_t kVBytes = 16384;
+
+__device__ __forceinline__ void prefetch_kqg(uint8_t* sm, uint64_t* bar, float* beta_dst, const CUtensorMap* tm_k,
+                                             const CUtensorMap* tm_q, const CUtensorMap* tm_g, const float* beta,
+                                             int64_t c0, int L, int H, int h, int tid) {
+    if (tid == 0) {
+        fence_proxy_async();
+        mbar_arrive_expect_tx(bar, kKQGBytes);
+        tma_load_3d(sm + OFF_STK, tm_k, 0, h, (int)c0, bar);
+        tma_load_3d(sm + OFF_STQ, tm_q, 0, h, (int)c0, bar);
+        tma_load_3d(sm + OFF_STG, tm_g, 0, h, (int)c0, bar);
     }
     if (tid < kC) {
         const bool ok = tid < L;
@@ -158,13 +163,12 @@ __device__ __forceinline__ void prefetch_kqg(uint8_t* sm, float* beta_dst, const
     }
 }
 
-__device__ __forceinline__ void prefetch_v(uint8_t* sm, const __nv_bfloat16* v, int64_t c0, int L, int H, int h,
+__device__ __forceinline__ void prefetch_v(uint8_t* sm, uint64_t* bar, const CUtensorMap* tm_v, int64_t c0, int h,
                                            int tid) {
-#pragma unroll
-    for (int m = 0; m < 2; ++m) {
-        const int id = tid + kThreads * m, i = id >> 4, cc = id & 15;
-        const bool ok = i < L;
-        cp_async16(sm + OFF_STV + i * 256 + cc * 16, v + (ok ? ((c0 + i) * H + h) * kD + cc * 8 : 0), ok ? 16u : 0u);
+    if (tid == 0) {
+        fence_proxy_async();
+        mbar_arrive_expect_tx(bar, kVBytes);
+        tma_load_3d(sm + OFF_STV, tm_v, 0, h, (int)c0, bar);
     }
 }
 
@@ -252,8 +256,9 @@ __device__ __forceinline__ void t_offdiag(const float* A, float* T, float* nb, i
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                const __nv_bfloat16* __restrict__ v, const float* __restrict__ g, const float* __restrict__ beta,
+chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                const float* __restrict__ beta,
                 const float* init_state, const int32_t* __restrict__ cu, int64_t T_total, int H, float scale,
                 const __nv_bfloat16* __restrict__ gate, __nv_bfloat16* __restrict__ o, float* final_state,
                 unsigned int* err) {
@@ -267,6 +272,8 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     float* sTot = reinterpret_cast<float*>(sm + OFF_TOT);
     uint64_t* barA = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
     uint64_t* barS = barA + 1;
+    uint64_t* barL = barA + 2;  // k, q, g tiles
+    uint64_t* barV = barA + 3;  // v tile
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
     volatile int* sAbort = reinterpret_cast<volatile int*>(sm + OFF_MISC + 4);
     float* sG = reinterpret_cast<float*>(sm + OFF_STG);
@@ -285,14 +292,17 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     if (tid == 0) {
         mbar_init(barA, 1);
         mbar_init(barS, 1);
+        mbar_init(barL, 1);
+        mbar_init(barV, 1);
         fence_mbar_init();
         *sAbort = 0;
     }
     if (warp == 0) tmem_alloc(sTmem, kTmemCols);
+    __syncthreads();  // barriers initialised before the first copy lands on them
     if (bos < eos) {  // the first chunk's inputs
         const int L0 = (eos - bos) < kC ? (int)(eos - bos) : kC;
-        prefetch_kqg(sm, sBetaBuf, k, q, g, beta, bos, L0, H, h, tid);
-        prefetch_v(sm, v, bos, L0, H, h, tid);
+        prefetch_kqg(sm, barL, sBetaBuf, &tm_k, &tm_q, &tm_g, beta, bos, L0, H, h, tid);
+        prefetch_v(sm, barV, &tm_v, bos, h, tid);
         cp_async_commit();
     }
 
@@ -317,7 +327,7 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *sTmem;
-    uint32_t phaseA = 0, phaseS = 0;
+    uint32_t phaseA = 0, phaseS = 0, phaseL = 0, phaseV = 0;
 
     auto wait_bar = [&](uint64_t* b, uint32_t& ph) {
         if (!mbar_wait(b, ph, kWaitLimit)) {
@@ -340,6 +350,8 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         const int L1 = c1 < eos ? ((eos - c1) < kC ? (int)(eos - c1) : kC) : 0;
         const float* sBeta = sBetaBuf + 64 * buf;
         cp_async_wait_all();
+        wait_bar(barL, phaseL);
+        wait_bar(barV, phaseV);
         __syncthreads();
         // ---- (1) running sum of g per key channel: thread (c, qq) sums the 16 tokens of block qq
         {
@@ -347,7 +359,7 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
             float acc = 0.f;
 #pragma unroll
             for (int i = 16 * qq; i < 16 * qq + 16; ++i) {  // in log2 units: every use is a power of e
-                acc = fmaf(sG[i * kD + c], kLog2e, acc);
+                acc = fmaf(i < L ? sG[i * kD + c] : 0.f, kLog2e, acc);
                 sG[i * kD + c] = acc;
             }
             sTot[qq * kD + c] = acc;
@@ -431,7 +443,7 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         fence_proxy_async();
         __syncthreads();
         // k, q, g of the next chunk may now land in the staging buffers
-        if (L1 > 0) prefetch_kqg(sm, sBetaBuf + 64 * (buf ^ 1), k, q, g, beta, c1, L1, H, h, tid);
+        if (L1 > 0) prefetch_kqg(sm, barL, sBetaBuf + 64 * (buf ^ 1), &tm_k, &tm_q, &tm_g, beta, c1, L1, H, h, tid);
         cp_async_commit();
         // ---- (3) the four row blocks of A (barrier A), then the S0 products (barrier S)
         if (tid == 0) {
@@ -547,7 +559,7 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
         tc_fence_before();
         __syncthreads();
         // v of the next chunk may now land
-        if (L1 > 0) prefetch_v(sm, v, c1, L1, H, h, tid);
+        if (L1 > 0) prefetch_v(sm, barV, &tm_v, c1, h, tid);
         cp_async_commit();
         if (*sAbort) break;
         // ---- (6) V'^T = Z^T T^T
@@ -618,6 +630,10 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
     }
 
     cp_async_wait_all();
+    if (*sAbort) {  // a chunk issued its successor's loads and then stopped: let them land (bounded)
+        mbar_wait(barL, phaseL, kWaitLimit);
+        mbar_wait(barV, phaseV, kWaitLimit);
+    }
     if (final_state && !*sAbort) {
 #pragma unroll
         for (int j = 0; j < 32; j += 4)
@@ -630,15 +646,50 @@ chunk_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __rest
 
 }  // namespace
 
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// [T, H, 128] tensor of `elem` bytes per value, boxes of [64 tokens][1 head][128 channels], no swizzle.
+bool encode_chunk_map(CUtensorMap* m, const void* base, CUtensorMapDataType type, int elem, int64_t T, int H) {
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
+    const cuuint64_t strides[2] = {(cuuint64_t)128 * elem, (cuuint64_t)H * 128 * elem};
+    const cuuint32_t box[3] = {128, 1, 64};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, type, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
                             const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
                             float scale, const void* out_gate, void* o, float* final_state, unsigned int* err,
                             cudaStream_t stream) {
+    CUtensorMap tq, tk, tv, tg;
+    if (!encode_chunk_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T_total, H) ||
+        !encode_chunk_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T_total, H) ||
+        !encode_chunk_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T_total, H) ||
+        !encode_chunk_map(&tg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, T_total, H))
+        return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     chunk_tc_kernel<<<(unsigned)((int64_t)N * H), kThreads, kSmemBytes, stream>>>(
-        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), g,
-        beta, init_state, cu_seqlens, T_total, H, scale, static_cast<const __nv_bfloat16*>(out_gate),
+        tq, tk, tv, tg, beta, init_state, cu_seqlens, T_total, H, scale, static_cast<const __nv_bfloat16*>(out_gate),
         static_cast<__nv_bfloat16*>(o), final_state, err);
     return cudaGetLastError();
 }
