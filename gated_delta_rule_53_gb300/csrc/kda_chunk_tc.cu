@@ -30,8 +30,9 @@
 // State path.  S0 (fp32) lives in registers: thread (r, half) of the 256 holds
 // row r, key channels [64 half, 64 half + 64); a bf16 copy in shared memory is
 // the A operand of the S0 products, so every product has M = 128 = dv and maps
-// row r to TMEM lane r.  All tensor-core products take bf16 operands and
-// accumulate in fp32 in TMEM.  T = (I + A_kk)^-1 is computed in fp32 on the CUDA
+// row r to TMEM lane r.  Products accumulate in fp32 in TMEM; their operands are
+// bf16, except Z T^T and the output's A_qk V' term, which run on kind::tf32 (tf32
+// operands): that halves the bf16 rounding in the output.  T = (I + A_kk)^-1 is computed in fp32 on the CUDA
 // cores by 16 x 16 blocks: the four diagonal blocks D by forward substitution, then
 // the blocks below them as (I - N + N^2 - N^3) D with N = D A_below (N^4 = 0).
 //
@@ -87,11 +88,16 @@ constexpr uint32_t OFF_MISC = OFF_BAR + 32;          // TMEM base, abort flag
 constexpr uint32_t kSmemUsed = OFF_MISC + 64;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // slack for aligning the base
 
-// After the A products complete (the S0 products may still be running and read B1):
-constexpr uint32_t OFF_AQ = OFF_RR + 64 * kAS * 4;   // A_qk operand [64][64] (8 KB), after A_kk fp32 [64][kAS]
-constexpr uint32_t OFF_TF = OFF_CC;                  // T fp32 [64][kAS] (17 KB)
-constexpr uint32_t OFF_TB = OFF_CC + 16384;          // T operand [64][64] (8 KB), written once T is in registers
-constexpr uint32_t OFF_Z = OFF_CC;                   // Z^T, then V'^T [128][64] (16 KB), after T is consumed
+// After the A products complete (RR and CC are free; the S0 products may still read B1):
+constexpr uint32_t OFF_AKK = OFF_CC;                 // A_kk fp32 [64][kAS] (17 KB)
+constexpr uint32_t OFF_AQ = OFF_RR;                  // A_qk tf32 operand [64][64] (2 regions of 8 KB)
+// After the S0 products complete (B1 is free):
+constexpr uint32_t OFF_TF = OFF_B1;                  // T fp32 [64][kAS] (17 KB)
+constexpr uint32_t OFF_NB = OFF_B1 + 64 * kAS * 4;   // N blocks of the solve, 9 x [16][20] fp32
+// Once T is in registers:
+constexpr uint32_t OFF_TT = OFF_CC;                  // T tf32 operand [64][64] (2 regions of 8 KB)
+constexpr uint32_t OFF_ZT = OFF_B1;                  // Z^T, then V'^T, tf32 operand [128][64] (2 regions of 16 KB)
+constexpr uint32_t OFF_VB = OFF_CC;                  // V'^T bf16 operand [128][64] (16 KB), once T is consumed
 // column operand of row block I < 3: 16(I+1) rows, two regions of 16(I+1) * 128 bytes
 __host__ __device__ constexpr uint32_t cc_off(int I) { return I == 0 ? 0u : (I == 1 ? 4096u : 12288u); }
 
@@ -103,8 +109,8 @@ constexpr uint32_t TM_O = 320;
 constexpr uint32_t TM_DS = 384;   // delta S
 constexpr uint32_t kTmemCols = 512;
 
-static_assert(OFF_AQ % 1024 == 0 && OFF_AQ + 8192 <= OFF_CC, "T work overflows its region");
-static_assert(OFF_TF + 64 * kAS * 4 <= OFF_S && OFF_TB + 8192 <= OFF_S, "T operand overflows its region");
+static_assert(OFF_AKK + 64 * kAS * 4 <= OFF_S && OFF_AQ + 16384 <= OFF_CC, "A work overflows its region");
+static_assert(OFF_NB + 9 * 16 * 20 * 4 <= OFF_KP, "T work overflows its region");
 static_assert(kSmemBytes <= 232448, "shared memory");
 
 __device__ __forceinline__ void unpack8(uint4 u, float (&f)[8]) {
@@ -127,14 +133,6 @@ __device__ __forceinline__ void mma_k128(uint32_t d, uint64_t a_desc, uint32_t a
         mma_bf16(d, a_desc + ((reg * a_region + off) >> 4), b_desc + ((reg * b_region + off) >> 4), idesc,
                  ks > 0 ? 1u : 0u);
     }
-}
-
-// D (+)= A B^T with a K = 64 (one-region) A and a K-major one-region B.
-__device__ __forceinline__ void mma_k64(uint32_t d, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                        bool accumulate_first) {
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(d, a_desc + ks * 2, b_desc + ks * 2, idesc, (ks > 0 || accumulate_first) ? 1u : 0u);
 }
 
 __device__ __forceinline__ uint64_t kdesc(uint32_t saddr) { return sdesc_sw128(saddr, 16, 1024); }
@@ -226,13 +224,13 @@ __device__ __forceinline__ void blk_mma(float* out, int ldo, float sign, Blk a0,
 // Blocks of T below the diagonal.  With D = diag(T_00 .. T_33) (inverses of the diagonal blocks of
 // I + A_kk) and N = D A_off (A_off: the blocks of A_kk below the diagonal; N is strictly block-lower,
 // so N^4 = 0):  (I + A_kk)^-1 = (I + N)^-1 D = (I - N + N^2 - N^3) D.
-// Four levels, each a set of independent 16 x 16 products spread over the CTA's warps.
+// Three levels, each a set of independent 16 x 16 products spread over the CTA's warps.
 constexpr int kNB = 20;  // row stride of the N blocks (float4 rows, eight rows on distinct banks)
 __device__ __forceinline__ void t_offdiag(const float* A, float* T, float* nb, int tid) {
     const int u = tid >> 6, t = tid & 63;
     auto Ablk = [&](int I, int J) { return Blk{A + 16 * I * kAS + 16 * J, kAS}; };
     auto Tblk = [&](int I, int J) { return Blk{T + 16 * I * kAS + 16 * J, kAS}; };
-    // N_IJ at nb[slot]: (1,0) 0, (2,0) 1, (3,0) 2, (2,1) 3, (3,1) 4, (3,2) 5; N^2: (2,0) 6, (3,1) 7, (3,0) 8; N^3 (3,0) 9
+    // N_IJ at nb[slot]: (1,0) 0, (2,0) 1, (3,0) 2, (2,1) 3, (3,1) 4, (3,2) 5; N^2: (2,0) 6, (3,1) 7, (3,0) 8
     auto Nb = [&](int slot) { return Blk{nb + slot * 16 * kNB, kNB}; };
     const Blk none{nullptr, 0};
     if (u < 6) {  // slots 0..5: (1,0) (2,0) (3,0) (2,1) (3,1) (3,2)
@@ -247,11 +245,10 @@ __device__ __forceinline__ void t_offdiag(const float* A, float* T, float* nb, i
     if (u == 4) blk_mma<1, false>(T + 16 * kAS * 2 + 16, kAS, -1.f, Nb(3), none, 0.f, none, 0.f, Tblk(1, 1), none, none, t);  // T21
     if (u == 5) blk_mma<1, false>(T + 16 * kAS * 3 + 32, kAS, -1.f, Nb(5), none, 0.f, none, 0.f, Tblk(2, 2), none, none, t);  // T32
     __syncthreads();
-    if (u == 0) blk_mma<1, false>(nb + 9 * 16 * kNB, kNB, 1.f, Nb(5), none, 0.f, none, 0.f, Nb(6), none, none, t);   // N32 N^2_20
+    // T_30 = (N^2_30 - N_30 - N^3_30) D_0 with N^3_30 D_0 = N^2_31 N_10 D_0 = -N^2_31 T_10
+    if (u == 0) blk_mma<2, true>(T + 16 * kAS * 3 + 0, kAS, 1.f, Nb(8), Nb(2), -1.f, none, 0.f, Tblk(0, 0), Nb(7), Tblk(1, 0), t);
     if (u == 1) blk_mma<2, false>(T + 16 * kAS * 2 + 0, kAS, 1.f, Nb(6), Nb(1), -1.f, none, 0.f, Tblk(0, 0), none, none, t);  // T20
     if (u == 2) blk_mma<2, false>(T + 16 * kAS * 3 + 16, kAS, 1.f, Nb(7), Nb(4), -1.f, none, 0.f, Tblk(1, 1), none, none, t); // T31
-    __syncthreads();
-    if (u == 0) blk_mma<3, false>(T + 16 * kAS * 3 + 0, kAS, 1.f, Nb(8), Nb(2), -1.f, Nb(9), -1.f, Tblk(0, 0), none, none, t); // T30
     __syncthreads();
 }
 
@@ -277,7 +274,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
     volatile int* sAbort = reinterpret_cast<volatile int*>(sm + OFF_MISC + 4);
     float* sG = reinterpret_cast<float*>(sm + OFF_STG);
-    float* sAkk = reinterpret_cast<float*>(sm + OFF_RR);
+    float* sAkk = reinterpret_cast<float*>(sm + OFF_AKK);
     float* sTf = reinterpret_cast<float*>(sm + OFF_TF);
     float* sO = reinterpret_cast<float*>(sm + OFF_RR);
 
@@ -340,7 +337,7 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     auto wait_mma = [&]() { wait_bar(barS, phaseS); };
 
     const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
-    const uint32_t id_64 = idesc_bf16_f32(128, 64, false, false);
+    const uint32_t id_t64 = idesc_tf32_f32(128, 64);
     const uint32_t id_ds = idesc_bf16_f32(128, 128, false, true);
 
     int buf = 0;
@@ -495,18 +492,20 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     }
                 } else {
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
-                        float f[8];
+                    for (int c4 = 0; c4 < 16; ++c4) {  // tf32: 32 columns per 128-byte region row
+                        float f[4];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int j = 8 * ch + e;
-                            f[e] = (j <= i && j < ncols) ? __uint_as_float(a[j]) : 0.f;
+                        for (int e = 0; e < 4; ++e) {
+                            const int j = 4 * c4 + e;
+                            f[e] = (j <= i && j < ncols) ? to_tf32(__uint_as_float(a[j])) : 0.f;
                         }
-                        *reinterpret_cast<uint4*>(sm + OFF_AQ + sw128(i, ch)) = pack8(f);
+                        *reinterpret_cast<float4*>(sm + OFF_AQ + (c4 >> 3) * 8192 + sw128(i, c4 & 7)) =
+                            make_float4(f[0], f[1], f[2], f[3]);
                     }
                 }
             }
         }
+        wait_bar(barS, phaseS);  // the S0 products are done: B1 becomes the solve's work space
         __syncthreads();
         // ---- (5) T = (I + A_kk)^-1 by 16 x 16 blocks (fp32)
         if (lane < 16 && warp < 4) {  // diagonal block `warp`, column `lane`, right-looking (independent updates)
@@ -523,20 +522,25 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int r2 = 0; r2 < 16; ++r2) sTf[(16 * I + r2) * kAS + 16 * I + c] = x[r2];
         }
         __syncthreads();
-        wait_bar(barS, phaseS);  // the S0 products are done: B1 becomes scratch for the N blocks
-        t_offdiag(sAkk, sTf, reinterpret_cast<float*>(sm + OFF_B1), tid);
-        {   // T as a bf16 operand (zero above the diagonal blocks); read all of T before writing over its tail
-            const int i = tid >> 3, ch = tid & 7;
-            float f[8];
-            if ((ch >> 1) > (i >> 4)) {
+        t_offdiag(sAkk, sTf, reinterpret_cast<float*>(sm + OFF_NB), tid);
+        {   // T as a tf32 operand (zero above the diagonal blocks); all of T is read before B1 / CC are reused
+            float4 f[2];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = 0.f;
-            } else {
-                *reinterpret_cast<float4*>(f) = *reinterpret_cast<const float4*>(sTf + i * kAS + 8 * ch);
-                *reinterpret_cast<float4*>(f + 4) = *reinterpret_cast<const float4*>(sTf + i * kAS + 8 * ch + 4);
+            for (int u = 0; u < 2; ++u) {
+                const int id = tid + kThreads * u, i = id >> 4, c4 = id & 15;
+                if ((c4 >> 2) > (i >> 4)) {
+                    f[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                } else {
+                    const float4 x = *reinterpret_cast<const float4*>(sTf + i * kAS + 4 * c4);
+                    f[u] = make_float4(to_tf32(x.x), to_tf32(x.y), to_tf32(x.z), to_tf32(x.w));
+                }
             }
             __syncthreads();
-            *reinterpret_cast<uint4*>(sm + OFF_TB + sw128(i, ch)) = pack8(f);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int id = tid + kThreads * u, i = id >> 4, c4 = id & 15;
+                *reinterpret_cast<float4*>(sm + OFF_TT + (c4 >> 3) * 8192 + sw128(i, c4 & 7)) = f[u];
+            }
         }
         // ---- Z^T = (beta V)^T - Y^T; thread (row, qq) owns tokens 16qq .. 16qq+15
         {
@@ -544,15 +548,17 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tmem_ld16_async(tbase + lane_base + TM_Y + 16 * qq, y);
             tmem_wait_ld(); reg_fence(y);
             const __nv_bfloat16* sv = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STV);
+            // tf32 row `row` of Z^T: tokens 16qq .. 16qq+15 are 4 chunks of region qq >> 1
 #pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-                float f[8];
+            for (int c4 = 0; c4 < 4; ++c4) {
+                float f[4];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int j = 16 * qq + 8 * c2 + e;
-                    f[e] = sBeta[j] * __bfloat162float(sv[j * kD + row]) - __uint_as_float(y[8 * c2 + e]);
+                for (int e = 0; e < 4; ++e) {
+                    const int j = 16 * qq + 4 * c4 + e;
+                    f[e] = to_tf32(sBeta[j] * __bfloat162float(sv[j * kD + row]) - __uint_as_float(y[4 * c4 + e]));
                 }
-                *reinterpret_cast<uint4*>(sm + OFF_Z + sw128(row, 2 * qq + c2)) = pack8(f);
+                *reinterpret_cast<float4*>(sm + OFF_ZT + (qq >> 1) * 16384 + sw128(row, 4 * (qq & 1) + c4)) =
+                    make_float4(f[0], f[1], f[2], f[3]);
             }
         }
         fence_proxy_async();
@@ -565,7 +571,13 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // ---- (6) V'^T = Z^T T^T
         if (tid == 0) {
             tc_fence_after();
-            mma_k64(tbase + TM_V, kdesc(sbase + OFF_Z), kdesc(sbase + OFF_TB), id_64, false);
+            const uint64_t za = kdesc(sbase + OFF_ZT), tb = kdesc(sbase + OFF_TT);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {  // K = 64 tokens, 8 per tf32 instruction
+                const uint32_t reg = ks >> 2, off = (ks & 3) * 32;
+                mma_tf32(tbase + TM_V, za + ((reg * 16384 + off) >> 4), tb + ((reg * 8192 + off) >> 4), id_t64,
+                         ks > 0 ? 1u : 0u);
+            }
             mma_commit(barS);
         }
         wait_mma();
@@ -574,11 +586,16 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tmem_ld16_async(tbase + lane_base + TM_V + 16 * qq, x);
             tmem_wait_ld(); reg_fence(x);
 #pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
+            for (int c4 = 0; c4 < 4; ++c4)  // tf32 copy for the output product
+                *reinterpret_cast<float4*>(sm + OFF_ZT + (qq >> 1) * 16384 + sw128(row, 4 * (qq & 1) + c4)) =
+                    make_float4(to_tf32(__uint_as_float(x[4 * c4])), to_tf32(__uint_as_float(x[4 * c4 + 1])),
+                                to_tf32(__uint_as_float(x[4 * c4 + 2])), to_tf32(__uint_as_float(x[4 * c4 + 3])));
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {  // bf16 copy for the state update
                 float f[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(x[8 * c2 + e]);
-                *reinterpret_cast<uint4*>(sm + OFF_Z + sw128(row, 2 * qq + c2)) = pack8(f);
+                *reinterpret_cast<uint4*>(sm + OFF_VB + sw128(row, 2 * qq + c2)) = pack8(f);
             }
         }
         fence_proxy_async();
@@ -587,10 +604,15 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // ---- (7) O^T += V'^T A_qk^T;  dS = V'^T (K e^{G_C - G})
         if (tid == 0) {
             tc_fence_after();
-            mma_k64(tbase + TM_O, kdesc(sbase + OFF_Z), kdesc(sbase + OFF_AQ), id_64, true);
+            const uint64_t va = kdesc(sbase + OFF_ZT), aq = kdesc(sbase + OFF_AQ);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t reg = ks >> 2, off = (ks & 3) * 32;
+                mma_tf32(tbase + TM_O, va + ((reg * 16384 + off) >> 4), aq + ((reg * 8192 + off) >> 4), id_t64, 1u);
+            }
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tbase + TM_DS, kdesc(sbase + OFF_Z) + ks * 2, sdesc_sw128(sbase + OFF_KP, 8192, 1024) + ks * 128,
+                mma_bf16(tbase + TM_DS, kdesc(sbase + OFF_VB) + ks * 2, sdesc_sw128(sbase + OFF_KP, 8192, 1024) + ks * 128,
                          id_ds, ks > 0 ? 1u : 0u);
             mma_commit(barS);
         }
