@@ -73,6 +73,37 @@ def load_peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+def kernel_source_hash(filename: str) -> str:
+    import hashlib
+    path = os.path.join(ROOT, "gated_delta_rule_53_gb300", "csrc", filename)
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, source: str, workload: str):
+    """DRAM bytes per launch (read + write) from the committed ncu capture of `kernel` on `workload`,
+    or None when there is none or the kernel's source has changed since it was taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[kernel]
+    except Exception:
+        return None
+    if rec.get("workload") != workload or rec.get("source_sha256_16") != kernel_source_hash(source):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def reduce_max(value: float, dist) -> float:
+    """Max of a per-rank number over all ranks (identity without a process group)."""
+    if dist is None:
+        return value
+    import torch
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def smi_index(local_rank: int) -> str:
     """nvidia-smi's name for this process's GPU (CUDA_VISIBLE_DEVICES entries are indices or UUIDs)."""
     cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "").strip()
@@ -190,13 +221,9 @@ def timed(fn, steps, warmup, stream, dist=None):
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     per = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
-    total_ms = evs[0].elapsed_time(evs[-1])
+    total_ms = reduce_max(evs[0].elapsed_time(evs[-1]), dist)
     if dist is not None:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-        if dist is not None:
-            dist.barrier()
+        dist.barrier()
     return total_ms / steps, statistics.mean(per), wall
 
 
@@ -278,6 +305,22 @@ def run_ours(args):
     dbytes = decode_bytes(wd.N, wd.H)
     dec_gbs = dbytes / (ms_dec_launch * 1e-3) / 1e9
 
+    del xs, cw, gd, bd, st, cs, od
+
+    # ---------------- prefill front end (kda_shortconv_l2norm), a memory-bound pass ----------------
+    wf = ks.Workload("frontend_32k", "frontend", 53005, H=96, lengths=[32768])
+    Cw = wf.H * wf.d
+    from kda_synth.device import fill_device
+    xf = [fill_device(wf.seed, t, ks.NORMAL, (wf.T, Cw), "bf16", device=device) for t in (ks.TID_Q, ks.TID_K, ks.TID_V)]
+    cwf = fill_device(wf.seed, ks.TID_CONV_W, ks.NORMAL, (3 * Cw, 4), "bf16", 0.0, wf.conv_w_std, device=device)
+    outs = [torch.empty((wf.T, wf.H, wf.d), dtype=torch.bfloat16, device=device) for _ in range(3)]
+    fstep = lambda: kda.kda_shortconv_l2norm(*xf, cwf, wf.H, q=outs[0], k=outs[1], v=outs[2], stream=stream)
+    fsteps = max(20, args.steps // 4)
+    ms_fe, ms_fe_launch, _ = timed(fstep, fsteps, args.warmup, stream, dist)
+    fe_bytes = 2 * 3 * wf.T * Cw * 2 + 3 * Cw * 4 * 2   # raw in + normalised out (bf16) + weights
+    fe_gbs = fe_bytes / (ms_fe_launch * 1e-3) / 1e9
+    del xf, outs
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -305,7 +348,9 @@ def run_ours(args):
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved_gbs / hbm_peak, "traffic": None, "peak_source": peak_src,
+                     "frac": achieved_gbs / hbm_peak,
+                     "traffic": measured_traffic("chunk_tc_kernel", "kda_chunk_tc.cu", w.name),
+                     "peak_source": peak_src,
                      "kernel": "kda_chunk_fwd (bf16)", "algorithmic_bytes_per_launch": pbytes,
                      "tensor": {"achieved_tflops": achieved_tflops, "peak_tflops": tc_peak,
                                 "frac": achieved_tflops / tc_peak,
@@ -315,7 +360,15 @@ def run_ours(args):
                    "value": dec_gbs, "unit": "GB/s", "ms_per_step": ms_dec, "steps": dsteps, "gpu_launches": dsteps,
                    "algorithmic_bytes_per_launch": dbytes, "clocks": dclk,
                    "roofline": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm_peak, "unit": "GB/s",
-                                "frac": dec_gbs / hbm_peak, "traffic": None, "peak_source": peak_src}},
+                                "frac": dec_gbs / hbm_peak,
+                                "traffic": measured_traffic("recurrent_step_kernel", "kda_recurrent.cu", wd.name),
+                                "peak_source": peak_src}},
+        "frontend": {"workload": "frontend_32k: raw q, k, v bf16 [32768, 12288] -> ShortConv(4)+SiLU+L2norm -> "
+                                 "bf16 [32768, 96, 128] x 3",
+                     "value": fe_gbs, "unit": "GB/s", "ms_per_step": ms_fe, "steps": fsteps, "gpu_launches": fsteps,
+                     "algorithmic_bytes_per_launch": fe_bytes,
+                     "roofline": {"bound": "hbm", "achieved": fe_gbs, "peak": hbm_peak, "unit": "GB/s",
+                                  "frac": fe_gbs / hbm_peak, "traffic": None, "peak_source": peak_src}},
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)

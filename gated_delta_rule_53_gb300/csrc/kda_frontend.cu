@@ -4,11 +4,12 @@
 // section 02).
 //
 // Memory-bound elementwise work: every raw element is read once and every
-// output written once.  One warp owns one (part, head) and a run of 16 tokens;
+// output written once.  One warp owns one (part, head) and a run of 8 tokens;
 // each lane owns 4 adjacent channels, so a token row of the head is one 256-byte
-// coalesced load.  The warp loads its 16 rows up front, keeps the last three raw
-// inputs of every channel in registers as it walks the run, and reduces the
-// squared norm of q / k with shuffles.  A second small kernel writes the carried
+// coalesced load.  The warp loads its 8 rows and their 3-token history up front,
+// computes every token's convolution and SiLU, then reduces all the run's squared
+// norms of q / k together (the shuffles of different tokens overlap).  A run that
+// crosses a sequence start takes a general path that reads the carried state.  A second small kernel writes the carried
 // convolution state (last three raw inputs per sequence) after the first has
 // finished reading the incoming one, so the two buffers may alias.
 #include "kda_common.cuh"
@@ -16,8 +17,8 @@
 namespace kda {
 namespace {
 
-constexpr int kRun = 16;          // tokens per warp
-constexpr int kWarps = 4;         // warps per CTA (64 tokens of one part and head)
+constexpr int kRun = 8;           // tokens per warp
+constexpr int kWarps = 8;         // warps per CTA (64 tokens of one part and head)
 
 __device__ __forceinline__ float4 bf16x4(uint2 u) {
     return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
@@ -55,19 +56,19 @@ shortconv_kernel(const __nv_bfloat16* __restrict__ xq, const __nv_bfloat16* __re
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t0 = ((int64_t)blockIdx.x * kWarps + warp) * kRun;
     if (t0 >= T_total) return;
-    const int64_t t_end = min(t0 + kRun, T_total);
     const int64_t C = (int64_t)H * kHeadDim;
     const int64_t ch = (int64_t)h * kHeadDim + 4 * lane;
     const int64_t gc = p * C + ch;
     const __nv_bfloat16* x = p == 0 ? xq : (p == 1 ? xk : xv);
     OutT* out = p == 0 ? q_out : (p == 1 ? k_out : v_out);
 
-    // the run's raw rows, loaded before any arithmetic
-    uint2 xr[kRun];
+    // raw rows t0 - 3 .. t0 + kRun - 1 (zero outside the tensor), loaded before any arithmetic
+    uint2 xr[kRun + 3];
 #pragma unroll
-    for (int i = 0; i < kRun; ++i)
-        xr[i] = (t0 + i < t_end) ? *reinterpret_cast<const uint2*>(x + (t0 + i) * x_stride + ch) : make_uint2(0, 0);
-
+    for (int i = 0; i < kRun + 3; ++i) {
+        const int64_t s = t0 - 3 + i;
+        xr[i] = (s >= 0 && s < T_total) ? *reinterpret_cast<const uint2*>(x + s * x_stride + ch) : make_uint2(0, 0);
+    }
     // taps of the lane's 4 channels: w[e][0..3], oldest .. current
     const uint4 w01 = *reinterpret_cast<const uint4*>(conv_w + gc * 4);
     const uint4 w23 = *reinterpret_cast<const uint4*>(conv_w + gc * 4 + 8);
@@ -79,43 +80,61 @@ shortconv_kernel(const __nv_bfloat16* __restrict__ xq, const __nv_bfloat16* __re
         w[e][2] = bf16_lo(wr[2 * e + 1]); w[e][3] = bf16_hi(wr[2 * e + 1]);
     }
 
+    // Sequence bounds.  Fast path: the run and its 3-token history lie inside one sequence.
     int n = cu ? find_seq(cu, N, t0) : 0;
     int64_t bos = cu ? cu[n] : 0, eos = cu ? cu[n + 1] : T_total;
-    // raw input at absolute position s < t (before the run, or before the sequence)
-    auto history = [&](int64_t s) -> float4 {
-        if (s >= bos) return bf16x4(*reinterpret_cast<const uint2*>(x + s * x_stride + ch));
-        const int64_t back = bos - s;
-        if (!cs_in || back > 3) return make_float4(0.f, 0.f, 0.f, 0.f);
-        return bf16x4(*reinterpret_cast<const uint2*>(cs_in + ((int64_t)n * 3 + (3 - back)) * 3 * C + gc));
-    };
-    float4 h1 = history(t0 - 3), h2 = history(t0 - 2), h3 = history(t0 - 1);
+    const int64_t t_last = (t0 + kRun < T_total ? t0 + kRun : T_total);  // one past the run's last real token
+    const bool simple = (t0 - 3 >= bos) && (t_last <= eos);
 
+    float y[kRun][4];
+    float ss[kRun];
 #pragma unroll
     for (int i = 0; i < kRun; ++i) {
         const int64_t t = t0 + i;
-        if (t >= t_end) break;
-        if (t >= eos) {  // a new sequence starts at t: its history is the carried state
+        if (!simple && t < T_total && cu) {
             while ((int64_t)cu[n + 1] <= t) ++n;
             bos = cu[n];
-            eos = cu[n + 1];
-            h1 = history(t - 3); h2 = history(t - 2); h3 = history(t - 1);
         }
-        const float4 xt = bf16x4(xr[i]);
-        const float a0[4] = {h1.x, h1.y, h1.z, h1.w}, a1[4] = {h2.x, h2.y, h2.z, h2.w};
-        const float a2[4] = {h3.x, h3.y, h3.z, h3.w}, a3[4] = {xt.x, xt.y, xt.z, xt.w};
-        float y[4];
+        float hist[4][4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {  // position t - 3 + j
+            float4 a = bf16x4(xr[i + j]);
+            if (!simple) {  // a sequence starts inside the window: read the carried state (or zero)
+                const int64_t s2 = t - 3 + j;
+                if (s2 < bos) {
+                    const int64_t back = bos - s2;
+                    a = (cs_in && back <= 3)
+                            ? bf16x4(*reinterpret_cast<const uint2*>(cs_in + ((int64_t)n * 3 + (3 - back)) * 3 * C + gc))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+            hist[j][0] = a.x; hist[j][1] = a.y; hist[j][2] = a.z; hist[j][3] = a.w;
+        }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            float acc = w[e][0] * a0[e];
-            acc = fmaf(w[e][1], a1[e], acc);
-            acc = fmaf(w[e][2], a2[e], acc);
-            acc = fmaf(w[e][3], a3[e], acc);
-            y[e] = acc / (1.0f + expf(-acc));
+            float acc = w[e][0] * hist[0][e];
+            acc = fmaf(w[e][1], hist[1][e], acc);
+            acc = fmaf(w[e][2], hist[2][e], acc);
+            acc = fmaf(w[e][3], hist[3][e], acc);
+            y[i][e] = __fdividef(acc, 1.0f + __expf(-acc));  // SiLU
         }
-        float inv = 1.0f;
-        if (p < 2) inv = 1.0f / sqrtf(warp_sum(y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3]) + eps);
-        store4<OutT>(out + (t * H + h) * kHeadDim + 4 * lane, y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv);
-        h1 = h2; h2 = h3; h3 = xt;
+        ss[i] = y[i][0] * y[i][0] + y[i][1] * y[i][1] + y[i][2] * y[i][2] + y[i][3] * y[i][3];
+    }
+    // L2 norms of q and k: all the run's reductions interleaved
+    if (p < 2) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int i = 0; i < kRun; ++i) ss[i] += __shfl_xor_sync(0xFFFFFFFFu, ss[i], o);
+    }
+#pragma unroll
+    for (int i = 0; i < kRun; ++i) {
+        const int64_t t = t0 + i;
+        if (t < T_total) {
+            const float inv = p < 2 ? rsqrtf(ss[i] + eps) : 1.0f;
+            store4<OutT>(out + (t * H + h) * kHeadDim + 4 * lane, y[i][0] * inv, y[i][1] * inv, y[i][2] * inv,
+                         y[i][3] * inv);
+        }
     }
 }
 

@@ -1,0 +1,67 @@
+"""Host-side logic of bench.py without a GPU: the max-over-ranks reduction with two gloo
+ranks (the replica timing of a multi-GPU run), and the traffic lookup that must go null
+once the kernel source no longer matches its ncu capture."""
+import json
+import os
+import socket
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, out_dir):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    got = bench.reduce_max(10.0 + 5.0 * rank, dist)
+    dist.barrier()
+    with open(os.path.join(out_dir, f"r{rank}.json"), "w") as f:
+        json.dump({"max": got}, f)
+    dist.destroy_process_group()
+
+
+def test_reduce_max_over_two_gloo_ranks(tmp_path):
+    mp = pytest.importorskip("torch.multiprocessing")
+    port = _free_port()
+    mp.spawn(_rank_main, args=(2, port, str(tmp_path)), nprocs=2, join=True)
+    for r in range(2):
+        assert json.load(open(tmp_path / f"r{r}.json"))["max"] == 15.0
+
+
+def test_reduce_max_single_process():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.reduce_max(3.5, None) == 3.5
+
+
+def test_traffic_lookup_follows_the_kernel_source(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    h = bench.kernel_source_hash("kda_recurrent.cu")
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "traffic.json").write_text(json.dumps({"recurrent_step_kernel": {
+        "workload": "decode_64", "source_sha256_16": h, "dram_bytes_per_launch": 123}}))
+    real_root = bench.ROOT
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    csrc = tmp_path / "gated_delta_rule_53_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    src = open(os.path.join(real_root, "gated_delta_rule_53_gb300", "csrc", "kda_recurrent.cu"), "rb").read()
+    (csrc / "kda_recurrent.cu").write_bytes(src)
+    assert bench.measured_traffic("recurrent_step_kernel", "kda_recurrent.cu", "decode_64") == 123
+    assert bench.measured_traffic("recurrent_step_kernel", "kda_recurrent.cu", "other") is None
+    (csrc / "kda_recurrent.cu").write_bytes(src + b"\n// changed\n")
+    assert bench.measured_traffic("recurrent_step_kernel", "kda_recurrent.cu", "decode_64") is None

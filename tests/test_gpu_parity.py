@@ -160,11 +160,11 @@ def test_chunk_packed_equals_separate(kda):
 # kda_shortconv_l2norm
 # ------------------------------------------------------------------------------------------
 
-@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
-def test_shortconv_varlen_with_state(kda, orc, out_dtype):
+@pytest.mark.parametrize("out_dtype,lengths", [("f32", [1, 2, 17, 0, 40]), ("bf16", [1, 2, 17, 0, 40]),
+                                               ("f32", [130, 1, 37, 200, 8, 3])])
+def test_shortconv_varlen_with_state(kda, orc, out_dtype, lengths):
     H, d = 3, 128
     C = H * d
-    lengths = [1, 2, 17, 0, 40]
     T, N = sum(lengths), len(lengths)
     cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
     width = C + 8   # a row stride larger than H*d
