@@ -18,7 +18,7 @@ namespace kda {
 namespace {
 
 constexpr int kRun = 8;           // tokens per warp
-constexpr int kWarps = 8;         // warps per CTA (64 tokens of one part and head)
+constexpr int kWarps = 8;         // warps per CTA (64 tokens of one part and head); 4 CTAs per SM
 
 __device__ __forceinline__ float4 bf16x4(uint2 u) {
     return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
@@ -46,7 +46,7 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float a,
 }
 
 template <typename OutT>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, 4)
 shortconv_kernel(const __nv_bfloat16* __restrict__ xq, const __nv_bfloat16* __restrict__ xk,
                  const __nv_bfloat16* __restrict__ xv, int64_t x_stride,
                  const __nv_bfloat16* __restrict__ conv_w, const int32_t* __restrict__ cu, int N,
@@ -88,37 +88,56 @@ shortconv_kernel(const __nv_bfloat16* __restrict__ xq, const __nv_bfloat16* __re
 
     float y[kRun][4];
     float ss[kRun];
+    if (simple) {
 #pragma unroll
-    for (int i = 0; i < kRun; ++i) {
-        const int64_t t = t0 + i;
-        if (!simple && t < T_total && cu) {
-            while ((int64_t)cu[n + 1] <= t) ++n;
-            bos = cu[n];
+        for (int i = 0; i < kRun; ++i) {
+            const float4 a0 = bf16x4(xr[i]), a1 = bf16x4(xr[i + 1]), a2 = bf16x4(xr[i + 2]), a3 = bf16x4(xr[i + 3]);
+            const float h0[4] = {a0.x, a0.y, a0.z, a0.w}, h1[4] = {a1.x, a1.y, a1.z, a1.w};
+            const float h2[4] = {a2.x, a2.y, a2.z, a2.w}, h3[4] = {a3.x, a3.y, a3.z, a3.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float acc = w[e][0] * h0[e];
+                acc = fmaf(w[e][1], h1[e], acc);
+                acc = fmaf(w[e][2], h2[e], acc);
+                acc = fmaf(w[e][3], h3[e], acc);
+                y[i][e] = __fdividef(acc, 1.0f + __expf(-acc));  // SiLU
+            }
+            ss[i] = y[i][0] * y[i][0] + y[i][1] * y[i][1] + y[i][2] * y[i][2] + y[i][3] * y[i][3];
         }
-        float hist[4][4];
+    } else {
+        // general path: a sequence starts inside the window; earlier positions read the carried state (or zero)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {  // position t - 3 + j
-            float4 a = bf16x4(xr[i + j]);
-            if (!simple) {  // a sequence starts inside the window: read the carried state (or zero)
+        for (int i = 0; i < kRun; ++i) {
+            const int64_t t = t0 + i;
+            if (t < T_total && cu) {
+                while ((int64_t)cu[n + 1] <= t) ++n;
+                bos = cu[n];
+            }
+            float hist[4][4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {  // position t - 3 + j
                 const int64_t s2 = t - 3 + j;
-                if (s2 < bos) {
+                float4 a;
+                if (s2 >= bos) {
+                    a = bf16x4(xr[i + j]);
+                } else {
                     const int64_t back = bos - s2;
                     a = (cs_in && back <= 3)
                             ? bf16x4(*reinterpret_cast<const uint2*>(cs_in + ((int64_t)n * 3 + (3 - back)) * 3 * C + gc))
                             : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
+                hist[j][0] = a.x; hist[j][1] = a.y; hist[j][2] = a.z; hist[j][3] = a.w;
             }
-            hist[j][0] = a.x; hist[j][1] = a.y; hist[j][2] = a.z; hist[j][3] = a.w;
-        }
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float acc = w[e][0] * hist[0][e];
-            acc = fmaf(w[e][1], hist[1][e], acc);
-            acc = fmaf(w[e][2], hist[2][e], acc);
-            acc = fmaf(w[e][3], hist[3][e], acc);
-            y[i][e] = __fdividef(acc, 1.0f + __expf(-acc));  // SiLU
+            for (int e = 0; e < 4; ++e) {
+                float acc = w[e][0] * hist[0][e];
+                acc = fmaf(w[e][1], hist[1][e], acc);
+                acc = fmaf(w[e][2], hist[2][e], acc);
+                acc = fmaf(w[e][3], hist[3][e], acc);
+                y[i][e] = __fdividef(acc, 1.0f + __expf(-acc));
+            }
+            ss[i] = y[i][0] * y[i][0] + y[i][1] * y[i][1] + y[i][2] * y[i][2] + y[i][3] * y[i][3];
         }
-        ss[i] = y[i][0] * y[i][0] + y[i][1] * y[i][1] + y[i][2] * y[i][2] + y[i][3] * y[i][3];
     }
     // L2 norms of q and k: all the run's reductions interleaved
     if (p < 2) {
