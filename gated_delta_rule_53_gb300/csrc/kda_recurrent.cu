@@ -1,11 +1,11 @@
 // kda_recurrent_step: one fused decode step (the fused_recurrent_kda operator of
 // "Kimi K3 架构全景", section 02) for N sequences of one token each.
 //
-// One CTA per (sequence, head), 8 warps.  Warps 0-2 run the front end for q, k
+// One CTA per (sequence, head), 16 warps (two CTAs per SM).  Warps 0-2 run the front end for q, k
 // and v of the head (ShortConv(4) + SiLU, L2 norm of q and k by warp shuffles,
 // "深入 Kimi-K3: Hugging Face 仓库分析", paragraph on KDA) and shift the
 // convolution state; warp 3 turns g into alpha = exp(g).  Meanwhile every warp
-// has already issued the 128-bit loads of its 16 state rows, so the 64 KB of
+// has already issued the 128-bit loads of its 8 state rows, so the 64 KB of
 // state per head is in flight while the front end runs.  Then each row r of
 // S (dv x dk) is updated on its own ("Kimi-K3 深度解析", section 三,
 // "KDA 的关键改进"):
@@ -17,7 +17,7 @@
 namespace kda {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kRowsPerWarp = kHeadDim / (kThreads / 32);  // 16
 
 __device__ __forceinline__ float4 bf16x4_to_f4(uint2 u) {
