@@ -85,7 +85,7 @@ def measured_traffic(kernel: str, source: str, workload: str):
     or None when there is none or the kernel's source has changed since it was taken."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            rec = json.load(f)[kernel]
+            rec = json.load(f)[f"{kernel}@{workload}"]
     except Exception:
         return None
     if rec.get("workload") != workload or rec.get("source_sha256_16") != kernel_source_hash(source):
@@ -368,7 +368,9 @@ def run_ours(args):
                      "value": fe_gbs, "unit": "GB/s", "ms_per_step": ms_fe, "steps": fsteps, "gpu_launches": fsteps,
                      "algorithmic_bytes_per_launch": fe_bytes,
                      "roofline": {"bound": "hbm", "achieved": fe_gbs, "peak": hbm_peak, "unit": "GB/s",
-                                  "frac": fe_gbs / hbm_peak, "traffic": None, "peak_source": peak_src}},
+                                  "frac": fe_gbs / hbm_peak,
+                                  "traffic": measured_traffic("shortconv_kernel", "kda_frontend.cu", wf.name),
+                                  "peak_source": peak_src}},
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)

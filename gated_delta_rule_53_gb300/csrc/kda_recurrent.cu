@@ -18,7 +18,7 @@ namespace kda {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kRowsPerWarp = kHeadDim / (kThreads / 32);  // 16
+constexpr int kRowsPerWarp = kHeadDim / (kThreads / 32);  // 8
 
 __device__ __forceinline__ float4 bf16x4_to_f4(uint2 u) {
     return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));

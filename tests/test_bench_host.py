@@ -53,7 +53,7 @@ def test_traffic_lookup_follows_the_kernel_source(tmp_path, monkeypatch):
     h = bench.kernel_source_hash("kda_recurrent.cu")
     prof = tmp_path / "profiles"
     prof.mkdir()
-    (prof / "traffic.json").write_text(json.dumps({"recurrent_step_kernel": {
+    (prof / "traffic.json").write_text(json.dumps({"recurrent_step_kernel@decode_64": {
         "workload": "decode_64", "source_sha256_16": h, "dram_bytes_per_launch": 123}}))
     real_root = bench.ROOT
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
