@@ -46,6 +46,8 @@ def library() -> ctypes.CDLL:
         for f in (lib.kda_shortconv_l2norm, lib.kda_chunk_fwd, lib.kda_recurrent_step, lib.kda_device_error):
             f.restype = ctypes.c_int
         lib.kda_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        lib.kda_selftest_bounded_wait.argtypes = [ctypes.c_uint, ctypes.c_void_p]
+        lib.kda_selftest_bounded_wait.restype = ctypes.c_int
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_status_string.argtypes = [ctypes.c_int]
         lib.kda_last_error.restype = ctypes.c_char_p
@@ -88,6 +90,11 @@ def device_error() -> int:
     code = ctypes.c_uint(0)
     _check(library().kda_device_error(ctypes.byref(code)), "kda_device_error")
     return int(code.value)
+
+
+def selftest_bounded_wait(poll_limit: int = 1000, stream=None) -> None:
+    """Launch the diagnostic kernel whose barrier wait always runs out (see include/kda.h)."""
+    _check(library().kda_selftest_bounded_wait(int(poll_limit), _stream(stream)), "kda_selftest_bounded_wait")
 
 
 def kda_shortconv_l2norm(xq, xk, xv, conv_w, H: int, cu_seqlens=None, conv_state_in=None, conv_state_out=None,

@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "kda_common.cuh"
+#include "kda_tc.cuh"
 
 namespace kda {
 namespace {
@@ -45,6 +46,18 @@ unsigned int* device_error_word() {
 }  // namespace kda
 
 using kda::set_error;
+
+namespace {
+
+// One thread waits on a barrier no one arrives at; the bounded wait gives up and reports.
+__global__ void selftest_wait_kernel(unsigned int limit, unsigned int* err) {
+    __shared__ uint64_t bar;
+    kda::tc::mbar_init(&bar, 1);
+    kda::tc::fence_mbar_init();
+    if (!kda::tc::mbar_wait(&bar, 0, limit)) kda::raise_device_error(err, kda::kErrMbarTimeout);
+}
+
+}  // namespace
 
 namespace {
 
@@ -115,6 +128,14 @@ kda_status kda_device_error(unsigned int* code) {
     if (e != cudaSuccess) return from_cuda(e, "clearing the device error word");
     *code = v;
     return ok();
+}
+
+kda_status kda_selftest_bounded_wait(unsigned int poll_limit, void* stream) {
+    REQUIRE(poll_limit >= 1 && poll_limit <= (1u << 24), "poll_limit must be in [1, 2^24]");
+    unsigned int* err = kda::device_error_word();
+    if (!err) return set_error(KDA_ERR_CUDA, "device error word unavailable");
+    selftest_wait_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(poll_limit, err);
+    return from_cuda(cudaGetLastError(), "kda_selftest_bounded_wait launch");
 }
 
 kda_status kda_shortconv_l2norm(const void* xq, const void* xk, const void* xv, int64_t x_row_stride,

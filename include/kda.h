@@ -162,6 +162,17 @@ KDA_API const char* kda_last_error(void);
  */
 KDA_API kda_status kda_device_error(unsigned int* code);
 
+/*
+ * Diagnostic (no counterpart in the sources): launches one CTA whose thread waits on an
+ * mbarrier that nothing ever arrives at, polling at most `poll_limit` times (1 .. 2^24),
+ * exactly as the library's kernels wait on their tensor-core and copy barriers.  The
+ * wait runs out, the kernel records KDA_DEVICE_ERR_WAIT_TIMEOUT in the device error word
+ * and returns; kda_device_error() then reports it.  It exercises the path a kernel takes
+ * instead of hanging, without faulting the GPU.  Asynchronous on `stream`.
+ */
+#define KDA_DEVICE_ERR_WAIT_TIMEOUT 1u
+KDA_API kda_status kda_selftest_bounded_wait(unsigned int poll_limit, void* stream);
+
 /* Library version, e.g. "0.1.0". */
 KDA_API const char* kda_version(void);
 
