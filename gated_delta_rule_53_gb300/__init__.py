@@ -20,8 +20,8 @@ import os
 
 import torch
 
-__all__ = ["kda_shortconv_l2norm", "kda_chunk_fwd", "kda_recurrent_step", "library", "KDAError",
-           "device_error", "LIB_PATH"]
+__all__ = ["kda_shortconv_l2norm", "kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurrent_step", "library",
+           "KDAError", "device_error", "LIB_PATH"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkda.so")
 KDA_DTYPE_F32, KDA_DTYPE_BF16 = 0, 1
@@ -41,9 +41,13 @@ def library() -> ctypes.CDLL:
         lib = ctypes.CDLL(LIB_PATH)
         P, I32, I64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
         lib.kda_shortconv_l2norm.argtypes = [P, P, P, I64, P, P, I32, I64, I32, I32, P, P, F, I32, P, P, P, P]
-        lib.kda_chunk_fwd.argtypes = [P, P, P, P, P, P, P, I32, I64, I32, I32, I32, F, I32, I32, P, P, P, P]
+        SZ = ctypes.c_size_t
+        lib.kda_chunk_fwd.argtypes = [P, P, P, P, P, P, P, I32, I64, I32, I32, I32, F, I32, I32, P, P, P, P, SZ, P]
+        lib.kda_chunk_fwd_workspace_size.argtypes = [I32, I64, I32, I32, I32, I32, I32, I32, ctypes.POINTER(SZ),
+                                                     ctypes.POINTER(SZ)]
         lib.kda_recurrent_step.argtypes = [P, P, P, I64, P, P, P, P, P, I32, I32, I32, I32, F, F, P, P]
-        for f in (lib.kda_shortconv_l2norm, lib.kda_chunk_fwd, lib.kda_recurrent_step, lib.kda_device_error):
+        for f in (lib.kda_shortconv_l2norm, lib.kda_chunk_fwd, lib.kda_recurrent_step, lib.kda_device_error,
+                  lib.kda_chunk_fwd_workspace_size):
             f.restype = ctypes.c_int
         lib.kda_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         lib.kda_selftest_bounded_wait.argtypes = [ctypes.c_uint, ctypes.c_void_p]
@@ -126,12 +130,28 @@ def kda_shortconv_l2norm(xq, xk, xv, conv_w, H: int, cu_seqlens=None, conv_state
     return tuple(outs)
 
 
+WORKSPACE_LIMIT = 8 << 30  # default cap of the prefill workspace (bytes); larger problems run in ranges
+
+
+def kda_chunk_fwd_workspace_size(N: int, T: int, H: int, dtype=torch.bfloat16, have_cu_seqlens: bool = True,
+                                 dk: int = 128, dv: int = 128, chunk_size: int = 64):
+    """(full_bytes, min_bytes) of the prefill workspace for these sizes (0, 0 for fp32)."""
+    full, least = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    dt = KDA_DTYPE_BF16 if dtype == torch.bfloat16 else KDA_DTYPE_F32
+    _check(library().kda_chunk_fwd_workspace_size(N, T, H, dk, dv, chunk_size, dt, 1 if have_cu_seqlens else 0,
+                                                  ctypes.byref(full), ctypes.byref(least)),
+           "kda_chunk_fwd_workspace_size")
+    return int(full.value), int(least.value)
+
+
 def kda_chunk_fwd(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale: float = 1.0, chunk_size: int = 64,
-                  out_gate=None, o=None, final_state=None, output_final_state: bool = True, stream=None):
+                  out_gate=None, o=None, final_state=None, output_final_state: bool = True, workspace=None,
+                  workspace_limit: int = WORKSPACE_LIMIT, stream=None):
     """Chunkwise KDA prefill.  q, k, v [T, H, 128] (bf16 or fp32, q and k L2-normalised),
     g fp32 [T, H, 128] in [-5, 0], beta fp32 [T, H], init_state fp32 [N, H, 128, 128] or None,
-    cu_seqlens int32 [N+1] or None, out_gate bf16 [T, H*128] or None.
-    Returns (o [T, H, 128], final_state [N, H, 128, 128] or None)."""
+    cu_seqlens int32 [N+1] or None, out_gate bf16 [T, H*128] or None.  workspace: a uint8 CUDA
+    tensor, or None to take one of min(full, workspace_limit) bytes (at least the minimum) from
+    PyTorch's allocator.  Returns (o [T, H, 128], final_state [N, H, 128, 128] or None)."""
     T, H, dk = q.shape
     dv = v.shape[-1]
     dtype = q.dtype
@@ -150,9 +170,15 @@ def kda_chunk_fwd(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale: flo
         final_state = torch.empty((N, H, dv, dk), dtype=torch.float32, device=q.device)
     _dev(final_state, "final_state", torch.float32, (N, H, dv, dk))
     dt = KDA_DTYPE_BF16 if dtype == torch.bfloat16 else KDA_DTYPE_F32
+    if workspace is None and dt == KDA_DTYPE_BF16:
+        full, least = kda_chunk_fwd_workspace_size(N, T, H, dtype, cu_seqlens is not None, dk, dv, chunk_size)
+        workspace = torch.empty(max(least, min(full, int(workspace_limit))), dtype=torch.uint8, device=q.device)
+    if workspace is not None:
+        _dev(workspace, "workspace", torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel()
     rc = library().kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state), _ptr(cu_seqlens),
                                  N, T, H, dk, dv, float(scale), int(chunk_size), dt, _ptr(out_gate), _ptr(o),
-                                 _ptr(final_state), _stream(stream))
+                                 _ptr(final_state), _ptr(workspace), ws_bytes, _stream(stream))
     _check(rc, "kda_chunk_fwd")
     return o, final_state
 

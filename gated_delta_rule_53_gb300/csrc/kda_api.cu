@@ -162,7 +162,7 @@ kda_status kda_shortconv_l2norm(const void* xq, const void* xk, const void* xv, 
 kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                          const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
                          int dk, int dv, float scale, int chunk_size, kda_dtype dtype, const void* out_gate,
-                         void* o, float* final_state, void* stream) {
+                         void* o, float* final_state, void* workspace, size_t workspace_bytes, void* stream) {
     REQUIRE_PTR(q); REQUIRE_PTR(k); REQUIRE_PTR(v); REQUIRE_PTR(g); REQUIRE_PTR(beta); REQUIRE_PTR(o);
     OPTIONAL_PTR(init_state); OPTIONAL_PTR(final_state); OPTIONAL_PTR(out_gate);
     kda_status s = check_batch(cu_seqlens, N, T_total, H);
@@ -177,9 +177,37 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const floa
         return from_cuda(kda::launch_chunk_simt(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, scale, dtype,
                                                 out_gate, o, final_state, static_cast<cudaStream_t>(stream)),
                          "kda_chunk_fwd launch");
+    REQUIRE(T_total < ((int64_t)1 << 31), "T_total must be below 2^31 for the bf16 path (tensor-map coordinates)");
+    REQUIRE(T_total / 64 + N <= 0x7FFFFFFF, "too many chunks");
+    size_t need = 0;
+    kda::chunk_tc_workspace(N, T_total, H, cu_seqlens != nullptr, nullptr, &need);
+    REQUIRE(workspace != nullptr && workspace_bytes >= need,
+            "workspace must hold at least %zu bytes for these sizes (got %zu)", need, workspace_bytes);
+    OPTIONAL_PTR(workspace);
+    unsigned int* err = kda::device_error_word();
+    if (!err) return set_error(KDA_ERR_CUDA, "device error word unavailable");
     return from_cuda(kda::launch_chunk_tc(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, scale, out_gate, o,
-                                          final_state, kda::device_error_word(), static_cast<cudaStream_t>(stream)),
+                                          final_state, workspace, workspace_bytes, err,
+                                          static_cast<cudaStream_t>(stream)),
                      "kda_chunk_fwd launch");
+}
+
+kda_status kda_chunk_fwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv, int chunk_size,
+                                        kda_dtype dtype, int have_cu_seqlens, size_t* full_bytes,
+                                        size_t* min_bytes) {
+    REQUIRE(N >= 1 && H >= 1 && T_total >= 0 && (int64_t)N * H <= 0x7FFFFFFF, "bad N, H or T_total");
+    REQUIRE(have_cu_seqlens || N == 1, "several sequences need cu_seqlens");
+    if (dk != kda::kHeadDim || dv != kda::kHeadDim)
+        return set_error(KDA_ERR_UNSUPPORTED, "only dk = dv = 128 is supported (got %d, %d)", dk, dv);
+    if (chunk_size != kda::kChunk)
+        return set_error(KDA_ERR_UNSUPPORTED, "only chunk_size = 64 is supported (got %d)", chunk_size);
+    REQUIRE(dtype == KDA_DTYPE_F32 || dtype == KDA_DTYPE_BF16, "bad dtype");
+    REQUIRE(T_total / 64 + N <= 0x7FFFFFFF, "T_total too large");
+    size_t full = 0, least = 0;
+    if (dtype == KDA_DTYPE_BF16) kda::chunk_tc_workspace(N, T_total, H, have_cu_seqlens != 0, &full, &least);
+    if (full_bytes) *full_bytes = full;
+    if (min_bytes) *min_bytes = least;
+    return ok();
 }
 
 kda_status kda_recurrent_step(const void* xq, const void* xk, const void* xv, int64_t x_row_stride,

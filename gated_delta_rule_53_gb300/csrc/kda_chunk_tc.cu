@@ -1,4 +1,4 @@
-// kda_chunk_fwd, bf16 path: chunkwise prefill on the tcgen05 tensor cores.
+// kda_chunk_fwd, bf16 path: chunkwise prefill on the tcgen05 tensor cores, as two kernels.
 //
 // Math (chunk of C = 64 tokens, state S0 entering it; "Kimi-K3 深度解析",
 // section 三, "KDA 的关键改进", unrolled over the chunk as in the chunk_kda
@@ -27,19 +27,33 @@
 // under the bf16 rounding of the operands.  The column operand of block 3 is
 // K e^{G_C - G}, the same tile the state update uses.
 //
-// State path.  S0 (fp32) lives in registers: thread (r, half) of the 256 holds
-// row r, key channels [64 half, 64 half + 64); a bf16 copy in shared memory is
-// the A operand of the S0 products, so every product has M = 128 = dv and maps
-// row r to TMEM lane r.  Products accumulate in fp32 in TMEM; their operands are
-// bf16, except Z T^T and the output's A_qk V' term, which run on kind::tf32 (tf32
-// operands): that halves the bf16 rounding in the output.  T = (I + A_kk)^-1 is computed in fp32 on the CUDA
-// cores by 16 x 16 blocks: the four diagonal blocks D by forward substitution, then
-// the blocks below them as (I - N + N^2 - N^3) D with N = D A_below (N^4 = 0).
+// Two kernels.  Everything except the state path is independent of S0: the running sum,
+// the operand tiles, A_kk, A_qk, T, and with them the two products
+//   W = T Diag(beta) (K . e^G)     U = T Diag(beta) V           (so that V'^T = U^T - S0 W^T).
+// chunk_prep_kernel computes them for every (chunk, head) at once (256-thread CTAs, two per
+// SM) and stores each chunk's state-path operands in the workspace, laid out exactly as the
+// state path reads them (128-byte-swizzled tiles), so that one bulk copy brings each in:
+//   B1    [W ; Q e^G]       bf16 [128][128]   B of the S0 products
+//   U     fp32 [64][128]                      V' = U - Y
+//   A_qk  (tf32 words)           [64][64]     B of O^T += V'^T A_qk^T
+//   KP    K e^{G_C - G}     bf16 [64][128]    B (MN-major) of dS = V'^T KP
+//   e^{G_C}                 fp32 [128]
+// chunk_state_kernel then walks each (sequence, head) chain in order, one CTA of 16 warps
+// per chain, with S0 (fp32) in registers: thread (r, quarter) holds row r, key channels
+// [32 quarter, 32 quarter + 32); a bf16 copy in shared memory is the A operand of the S0
+// products, so every product has M = 128 = dv and maps row r to TMEM lane r.  Per chunk the
+// serial path is one product (S0 B1^T), V' = U - Y, one product (dS) and the state update;
+// the output product and its store overlap the next chunk's first product.
 //
-// One CTA of 16 warps per (sequence, head) walks the chunks in order; thread
-// (r, quarter) holds state row r, key channels [32 quarter, 32 quarter + 32).  The
-// next chunk's inputs are copied into shared memory with cp.async while the
-// current chunk computes (k, q, g once the operands are built, v once Z is built).
+// Precision.  Products accumulate in fp32 in TMEM.  W and U come from T Diag(beta) split as
+// hi + lo in bf16 (two bf16 products each, T kept to about 16 bits); A_qk V' runs on
+// kind::tf32; the other operands are bf16.  T = (I + A_kk)^-1 is computed in fp32 on the CUDA
+// cores by 16 x 16 blocks: the four diagonal blocks D by forward substitution, then the blocks
+// below them as (I - N + N^2 - N^3) D with N = D A_below (N^4 = 0).
+//
+// Packed sequences are numbered chunk by chunk (sequence-major); the workspace holds the
+// operands of a range of chunk rows (all heads) at a time, and a chain that crosses the end
+// of a range hands its fp32 state to the next range through the workspace.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -53,7 +67,6 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 512;
 constexpr int kC = kChunk;    // 64
 constexpr int kD = kHeadDim;  // 128
 constexpr int kAS = 68;       // fp32 row stride of the A_kk / T work arrays (float4 rows on distinct banks)
@@ -67,51 +80,18 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// shared-memory map (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_STK = 0;        // k staging bf16 [64][128]
-constexpr uint32_t OFF_STQ = 16384;    // q staging bf16 [64][128]
-constexpr uint32_t OFF_STV = 32768;    // v staging bf16 [64][128]
-constexpr uint32_t OFF_STG = 49152;    // g -> G fp32 [64][128]
-constexpr uint32_t OFF_B1 = 81920;     // [beta K e^G ; Q e^G] [128][128] (B of the S0 products)
-constexpr uint32_t OFF_KP = 114688;    // K e^{G_C - G} [64][128]: column operand of row block 3, B of dS
-constexpr uint32_t OFF_RR = 131072;    // row operand [K e^{G-E} ; Q e^{G-E}] [128][128] | A_kk, A_qk, scratch | O fp32
-constexpr uint32_t OFF_CC = 163840;    // column operands of row blocks 0..2 (16, 32, 48 rows) | T fp32, T bf16 | Z^T
-constexpr uint32_t OFF_S = 188416;     // bf16 S0 [128][128]
-constexpr uint32_t OFF_SMALL = 221184;
-constexpr uint32_t OFF_BETA = OFF_SMALL;             // fp32 [2][64] (double-buffered)
-constexpr uint32_t OFF_E = OFF_BETA + 512;           // fp32 [4][128] E_I = G at the last token of block I
-constexpr uint32_t OFF_DT = OFF_E + 2048;            // fp32 [6][128] e^{E_J - E_I}, J > I
-constexpr uint32_t OFF_EGL = OFF_DT + 3072;          // fp32 [128] e^{G_C}
-constexpr uint32_t OFF_TOT = OFF_EGL + 512;          // fp32 [4][128] per-block sums of g
-constexpr uint32_t OFF_BAR = OFF_TOT + 2048;         // mbarriers: A products, state products, k/q/g tiles, v tile
-constexpr uint32_t OFF_MISC = OFF_BAR + 32;          // TMEM base, abort flag
-constexpr uint32_t kSmemUsed = OFF_MISC + 64;
-constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // slack for aligning the base
+// Operands of one (chunk, head) in the workspace, byte offsets (each tile in the layout its
+// reader uses; the last three are contiguous so that one copy brings them in).
+constexpr uint32_t BLOB_B1 = 0;        // [W ; Q e^G] bf16, two regions of [128][64] (128-byte swizzle)
+constexpr uint32_t BLOB_U = 32768;     // U fp32 [64][128], row-major
+constexpr uint32_t BLOB_AQ = 65536;    // A_qk tf32, two regions of [64][32]
+constexpr uint32_t BLOB_KP = 81920;    // K e^{G_C - G} bf16, two regions of [64][64]
+constexpr uint32_t BLOB_EGL = 98304;   // e^{G_C} fp32 [128]
+constexpr uint32_t kBlobBytes = 98816;
+constexpr uint32_t kStateBytes = kD * kD * 4;
 
-// After the A products complete (RR and CC are free; the S0 products may still read B1):
-constexpr uint32_t OFF_AKK = OFF_CC;                 // A_kk fp32 [64][kAS] (17 KB)
-constexpr uint32_t OFF_AQ = OFF_RR;                  // A_qk tf32 operand [64][64] (2 regions of 8 KB)
-// After the S0 products complete (B1 is free):
-constexpr uint32_t OFF_TF = OFF_B1;                  // T fp32 [64][kAS] (17 KB)
-constexpr uint32_t OFF_NB = OFF_B1 + 64 * kAS * 4;   // N blocks of the solve, 9 x [16][20] fp32
-// Once T is in registers:
-constexpr uint32_t OFF_TT = OFF_CC;                  // T tf32 operand [64][64] (2 regions of 8 KB)
-constexpr uint32_t OFF_ZT = OFF_B1;                  // Z^T, then V'^T, tf32 operand [128][64] (2 regions of 16 KB)
-constexpr uint32_t OFF_VB = OFF_CC;                  // V'^T bf16 operand [128][64] (16 KB), once T is consumed
 // column operand of row block I < 3: 16(I+1) rows, two regions of 16(I+1) * 128 bytes
 __host__ __device__ constexpr uint32_t cc_off(int I) { return I == 0 ? 0u : (I == 1 ? 4096u : 12288u); }
-
-// TMEM columns
-constexpr uint32_t TM_A0 = 0, TM_A1 = 32, TM_A2 = 64, TM_A3 = 128;  // row blocks of A: 16, 32, 48, 64 columns
-constexpr uint32_t TM_V = 192;    // V'^T
-constexpr uint32_t TM_Y = 256;    // Y^T = S0 (beta K e^G)^T, then O^T at TM_O
-constexpr uint32_t TM_O = 320;
-constexpr uint32_t TM_DS = 384;   // delta S
-constexpr uint32_t kTmemCols = 512;
-
-static_assert(OFF_AKK + 64 * kAS * 4 <= OFF_S && OFF_AQ + 16384 <= OFF_CC, "A work overflows its region");
-static_assert(OFF_NB + 9 * 16 * 20 * 4 <= OFF_KP, "T work overflows its region");
-static_assert(kSmemBytes <= 232448, "shared memory");
 
 __device__ __forceinline__ void unpack8(uint4 u, float (&f)[8]) {
     f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x); f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
@@ -137,50 +117,18 @@ __device__ __forceinline__ void mma_k128(uint32_t d, uint64_t a_desc, uint32_t a
 
 __device__ __forceinline__ uint64_t kdesc(uint32_t saddr) { return sdesc_sw128(saddr, 16, 1024); }
 
-// Loads of the chunk starting at token c0 of head h.  Thread 0 issues one TMA box per tensor
-// ([64 tokens][1 head][128 channels]; rows past the end of the tensor read as zero) and arms the
-// stage's mbarrier with the byte count; beta (64 strided words) comes by cp.async, zero past the
-// chunk's L tokens.  Rows past L that belong to the next packed sequence are harmless in k, q
-// and v (their beta is zero) and g is masked where it is summed.
-constexpr uint32_t kKQGBytes = 2 * 16384 + 32768;
-constexpr uint32_t kVBytes = 16384;
-
-__device__ __forceinline__ void prefetch_kqg(uint8_t* sm, uint64_t* bar, float* beta_dst, const CUtensorMap* tm_k,
-                                             const CUtensorMap* tm_q, const CUtensorMap* tm_g, const float* beta,
-                                             int64_t c0, int L, int H, int h, int tid) {
-    if (tid == 0) {
-        fence_proxy_async();
-        mbar_arrive_expect_tx(bar, kKQGBytes);
-        tma_load_3d(sm + OFF_STK, tm_k, 0, h, (int)c0, bar);
-        tma_load_3d(sm + OFF_STQ, tm_q, 0, h, (int)c0, bar);
-        tma_load_3d(sm + OFF_STG, tm_g, 0, h, (int)c0, bar);
-    }
-    if (tid < kC) {
-        const bool ok = tid < L;
-        cp_async4(beta_dst + tid, beta + (ok ? (c0 + tid) * H + h : 0), ok ? 4u : 0u);
-    }
-}
-
-__device__ __forceinline__ void prefetch_v(uint8_t* sm, uint64_t* bar, const CUtensorMap* tm_v, int64_t c0, int h,
-                                           int tid) {
-    if (tid == 0) {
-        fence_proxy_async();
-        mbar_arrive_expect_tx(bar, kVBytes);
-        tma_load_3d(sm + OFF_STV, tm_v, 0, h, (int)c0, bar);
-    }
-}
-
-// One 16 x 16 fp32 block product for 64 threads (t = 0..63 owns row t / 4, columns 4 (t % 4) .. +3):
-//   out = sign * (A0 + w1 A1 + w2 A2) B  [+ A3 B3]
+// One 16 x 16 fp32 block product for 16 * 16 / CW threads; thread t owns row t / (16 / CW) and the
+// CW columns from CW (t % (16 / CW)):   out = sign * (A0 + w1 A1 + w2 A2) B  [+ A3 B3]
 // NA = number of A blocks combined on the fly (an entry of P = -N + N^2 - N^3); SECOND adds A3 B3.
 struct Blk {
     const float* p;
     int ld;
 };
-template <int NA, bool SECOND>
+template <int NA, bool SECOND, int CW>
 __device__ __forceinline__ void blk_mma(float* out, int ldo, float sign, Blk a0, Blk a1, float w1, Blk a2, float w2,
                                         Blk b, Blk a3, Blk b3, int t) {
-    const int r = t >> 2, c = 4 * (t & 3);
+    constexpr int TPR = 16 / CW;  // threads per row
+    const int r = t / TPR, c = CW * (t % TPR);
     float av[16];
 #pragma unroll
     for (int m = 0; m < 16; m += 4) {
@@ -195,13 +143,18 @@ __device__ __forceinline__ void blk_mma(float* out, int ldo, float sign, Blk a0,
         }
         av[m] = x.x; av[m + 1] = x.y; av[m + 2] = x.z; av[m + 3] = x.w;
     }
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), acc2 = acc;
+    float acc[CW], acc2[CW];
+#pragma unroll
+    for (int e = 0; e < CW; ++e) acc[e] = acc2[e] = 0.f;
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
-        const float4 bv = *reinterpret_cast<const float4*>(b.p + m * b.ld + c);
-        float4& ac = (m & 1) ? acc2 : acc;
-        ac.x = fmaf(av[m], bv.x, ac.x); ac.y = fmaf(av[m], bv.y, ac.y);
-        ac.z = fmaf(av[m], bv.z, ac.z); ac.w = fmaf(av[m], bv.w, ac.w);
+#pragma unroll
+        for (int e4 = 0; e4 < CW; e4 += 4) {
+            const float4 bv = *reinterpret_cast<const float4*>(b.p + m * b.ld + c + e4);
+            float* ac = (m & 1) ? acc2 : acc;
+            ac[e4] = fmaf(av[m], bv.x, ac[e4]); ac[e4 + 1] = fmaf(av[m], bv.y, ac[e4 + 1]);
+            ac[e4 + 2] = fmaf(av[m], bv.z, ac[e4 + 2]); ac[e4 + 3] = fmaf(av[m], bv.w, ac[e4 + 3]);
+        }
     }
     if (SECOND) {
 #pragma unroll
@@ -211,260 +164,341 @@ __device__ __forceinline__ void blk_mma(float* out, int ldo, float sign, Blk a0,
         }
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
-            const float4 bv = *reinterpret_cast<const float4*>(b3.p + m * b3.ld + c);
-            float4& ac = (m & 1) ? acc2 : acc;
-            ac.x = fmaf(av[m], bv.x, ac.x); ac.y = fmaf(av[m], bv.y, ac.y);
-            ac.z = fmaf(av[m], bv.z, ac.z); ac.w = fmaf(av[m], bv.w, ac.w);
+#pragma unroll
+            for (int e4 = 0; e4 < CW; e4 += 4) {
+                const float4 bv = *reinterpret_cast<const float4*>(b3.p + m * b3.ld + c + e4);
+                float* ac = (m & 1) ? acc2 : acc;
+                ac[e4] = fmaf(av[m], bv.x, ac[e4]); ac[e4 + 1] = fmaf(av[m], bv.y, ac[e4 + 1]);
+                ac[e4 + 2] = fmaf(av[m], bv.z, ac[e4 + 2]); ac[e4 + 3] = fmaf(av[m], bv.w, ac[e4 + 3]);
+            }
         }
     }
-    *reinterpret_cast<float4*>(out + r * ldo + c) = make_float4(sign * (acc.x + acc2.x), sign * (acc.y + acc2.y),
-                                                                  sign * (acc.z + acc2.z), sign * (acc.w + acc2.w));
+#pragma unroll
+    for (int e4 = 0; e4 < CW; e4 += 4)
+        *reinterpret_cast<float4*>(out + r * ldo + c + e4) =
+            make_float4(sign * (acc[e4] + acc2[e4]), sign * (acc[e4 + 1] + acc2[e4 + 1]),
+                        sign * (acc[e4 + 2] + acc2[e4 + 2]), sign * (acc[e4 + 3] + acc2[e4 + 3]));
 }
 
 // Blocks of T below the diagonal.  With D = diag(T_00 .. T_33) (inverses of the diagonal blocks of
 // I + A_kk) and N = D A_off (A_off: the blocks of A_kk below the diagonal; N is strictly block-lower,
 // so N^4 = 0):  (I + A_kk)^-1 = (I + N)^-1 D = (I - N + N^2 - N^3) D.
-// Three levels, each a set of independent 16 x 16 products spread over the CTA's warps.
+// Three rounds of independent 16 x 16 products on the first 192 threads (32 or 64 per product).
 constexpr int kNB = 20;  // row stride of the N blocks (float4 rows, eight rows on distinct banks)
 __device__ __forceinline__ void t_offdiag(const float* A, float* T, float* nb, int tid) {
-    const int u = tid >> 6, t = tid & 63;
     auto Ablk = [&](int I, int J) { return Blk{A + 16 * I * kAS + 16 * J, kAS}; };
     auto Tblk = [&](int I, int J) { return Blk{T + 16 * I * kAS + 16 * J, kAS}; };
     // N_IJ at nb[slot]: (1,0) 0, (2,0) 1, (3,0) 2, (2,1) 3, (3,1) 4, (3,2) 5; N^2: (2,0) 6, (3,1) 7, (3,0) 8
     auto Nb = [&](int slot) { return Blk{nb + slot * 16 * kNB, kNB}; };
     const Blk none{nullptr, 0};
-    if (u < 6) {  // slots 0..5: (1,0) (2,0) (3,0) (2,1) (3,1) (3,2)
+    const int u = tid >> 5, t = tid & 31;
+    if (u < 6) {  // N blocks: (1,0) (2,0) (3,0) (2,1) (3,1) (3,2)
         const int I = u < 3 ? u + 1 : (u < 5 ? u - 1 : 3), J = u < 3 ? 0 : (u < 5 ? 1 : 2);
-        blk_mma<1, false>(nb + u * 16 * kNB, kNB, 1.f, Tblk(I, I), none, 0.f, none, 0.f, Ablk(I, J), none, none, t);
+        blk_mma<1, false, 8>(nb + u * 16 * kNB, kNB, 1.f, Tblk(I, I), none, 0.f, none, 0.f, Ablk(I, J), none, none, t);
     }
     __syncthreads();
-    if (u == 0) blk_mma<1, false>(nb + 6 * 16 * kNB, kNB, 1.f, Nb(3), none, 0.f, none, 0.f, Nb(0), none, none, t);   // N21 N10
-    if (u == 1) blk_mma<1, false>(nb + 7 * 16 * kNB, kNB, 1.f, Nb(5), none, 0.f, none, 0.f, Nb(3), none, none, t);   // N32 N21
-    if (u == 2) blk_mma<1, true>(nb + 8 * 16 * kNB, kNB, 1.f, Nb(4), none, 0.f, none, 0.f, Nb(0), Nb(5), Nb(1), t);  // N31 N10 + N32 N20
-    if (u == 3) blk_mma<1, false>(T + 16 * kAS * 1 + 0, kAS, -1.f, Nb(0), none, 0.f, none, 0.f, Tblk(0, 0), none, none, t);   // T10
-    if (u == 4) blk_mma<1, false>(T + 16 * kAS * 2 + 16, kAS, -1.f, Nb(3), none, 0.f, none, 0.f, Tblk(1, 1), none, none, t);  // T21
-    if (u == 5) blk_mma<1, false>(T + 16 * kAS * 3 + 32, kAS, -1.f, Nb(5), none, 0.f, none, 0.f, Tblk(2, 2), none, none, t);  // T32
+    switch (u) {
+        case 0: blk_mma<1, false, 8>(nb + 6 * 16 * kNB, kNB, 1.f, Nb(3), none, 0.f, none, 0.f, Nb(0), none, none, t); break;  // N21 N10
+        case 1: blk_mma<1, false, 8>(nb + 7 * 16 * kNB, kNB, 1.f, Nb(5), none, 0.f, none, 0.f, Nb(3), none, none, t); break;  // N32 N21
+        case 2: blk_mma<1, true, 8>(nb + 8 * 16 * kNB, kNB, 1.f, Nb(4), none, 0.f, none, 0.f, Nb(0), Nb(5), Nb(1), t); break; // N31 N10 + N32 N20
+        case 3: blk_mma<1, false, 8>(T + 16 * kAS * 1 + 0, kAS, -1.f, Nb(0), none, 0.f, none, 0.f, Tblk(0, 0), none, none, t); break;   // T10
+        case 4: blk_mma<1, false, 8>(T + 16 * kAS * 2 + 16, kAS, -1.f, Nb(3), none, 0.f, none, 0.f, Tblk(1, 1), none, none, t); break;  // T21
+        case 5: blk_mma<1, false, 8>(T + 16 * kAS * 3 + 32, kAS, -1.f, Nb(5), none, 0.f, none, 0.f, Tblk(2, 2), none, none, t); break;  // T32
+        default: break;
+    }
     __syncthreads();
     // T_30 = (N^2_30 - N_30 - N^3_30) D_0 with N^3_30 D_0 = N^2_31 N_10 D_0 = -N^2_31 T_10
-    if (u == 0) blk_mma<2, true>(T + 16 * kAS * 3 + 0, kAS, 1.f, Nb(8), Nb(2), -1.f, none, 0.f, Tblk(0, 0), Nb(7), Tblk(1, 0), t);
-    if (u == 1) blk_mma<2, false>(T + 16 * kAS * 2 + 0, kAS, 1.f, Nb(6), Nb(1), -1.f, none, 0.f, Tblk(0, 0), none, none, t);  // T20
-    if (u == 2) blk_mma<2, false>(T + 16 * kAS * 3 + 16, kAS, 1.f, Nb(7), Nb(4), -1.f, none, 0.f, Tblk(1, 1), none, none, t); // T31
+    const int u3 = tid >> 6, t3 = tid & 63;
+    switch (u3) {
+        case 0: blk_mma<2, true, 4>(T + 16 * kAS * 3 + 0, kAS, 1.f, Nb(8), Nb(2), -1.f, none, 0.f, Tblk(0, 0), Nb(7), Tblk(1, 0), t3); break;
+        case 1: blk_mma<2, false, 4>(T + 16 * kAS * 2 + 0, kAS, 1.f, Nb(6), Nb(1), -1.f, none, 0.f, Tblk(0, 0), none, none, t3); break;  // T20
+        case 2: blk_mma<2, false, 4>(T + 16 * kAS * 3 + 16, kAS, 1.f, Nb(7), Nb(4), -1.f, none, 0.f, Tblk(1, 1), none, none, t3); break; // T31
+        default: break;
+    }
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-                const float* __restrict__ beta,
-                const float* init_state, const int32_t* __restrict__ cu, int64_t T_total, int H, float scale,
-                const __nv_bfloat16* __restrict__ gate, __nv_bfloat16* __restrict__ o, float* final_state,
-                unsigned int* err) {
+// One thread waits (bounded) for phase `ph` of an mbarrier; a wait that runs out marks the CTA aborted
+// and reports.  The other warps meet that thread at a CTA barrier afterwards, blocked in bar.sync
+// rather than polling the mbarrier (polling by every warp takes issue slots from the ones working).
+__device__ __forceinline__ void solo_wait(uint64_t* b, uint32_t ph, volatile int* abort_flag, unsigned int* err) {
+    if (!mbar_wait(b, ph, kWaitLimit)) {
+        *abort_flag = 1;
+        raise_device_error(err, kErrMbarTimeout);
+    }
+}
+
+// All threads meet; TMEM accesses after it are ordered after the tcgen05 operations before it.
+__device__ __forceinline__ void cta_sync_tc() {
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+}
+
+// Chunk offsets of the packed sequences: off[n] = sum over n' < n of ceil(L_n' / 64), off[N] = all.
+__global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* __restrict__ cu, int N, int64_t T_total,
+                                                             int32_t* __restrict__ off) {
+    __shared__ int32_t warp_tot[32];
+    __shared__ int32_t carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) carry = 0;
+    __syncthreads();
+    for (int base = 0; base < N; base += 1024) {
+        const int n = base + tid;
+        int cnt = 0;
+        if (n < N) {
+            int64_t bos, eos;
+            seq_bounds(cu, n, T_total, bos, eos);
+            cnt = eos > bos ? (int)((eos - bos + kC - 1) / kC) : 0;
+        }
+        int incl = cnt;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+            if (lane >= d) incl += y;
+        }
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int w = warp_tot[lane];
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, w, d);
+                if (lane >= d) w += y;
+            }
+            warp_tot[lane] = w;  // inclusive over warps
+        }
+        __syncthreads();
+        const int before = carry + (warp > 0 ? warp_tot[warp - 1] : 0) + incl - cnt;
+        if (n < N) off[n] = before;
+        __syncthreads();
+        if (tid == 0) carry += warp_tot[31];
+        __syncthreads();
+    }
+    if (tid == 0) off[N] = carry;
+}
+
+// =============================================================================================
+// chunk_prep_kernel: the S0-independent part of one (chunk, head)
+// =============================================================================================
+constexpr int kPrepThreads = 256;
+constexpr uint32_t P_RR = 0;          // k (rows 0-63) and q (rows 64-127) land here by TMA in the layout of the row
+                                      // operand, two regions of 16 KB, and are scaled in place
+constexpr uint32_t P_KP = 32768;      // K e^{G_C - G} (two regions of [64][64])
+constexpr uint32_t P_G = 49152;       // g fp32, four TMA boxes of [64][32]
+constexpr uint32_t P_KG = 49152;      // then: K e^G (two regions of [64][64]), B (MN-major) of the W products
+constexpr uint32_t P_V = 65536;       // then: V by TMA (two regions of [64][64]), B (MN-major) of the U products
+constexpr uint32_t P_CC = 81920;      // column operands of row blocks 0..2 (24 KB)
+constexpr uint32_t P_BETA = P_CC + 24576;  // fp32 [64]
+constexpr uint32_t P_BAR = P_BETA + 256;   // mbarriers: k/q/g, v, A products, W/U products
+constexpr uint32_t P_MISC = P_BAR + 32;    // TMEM base, abort flag
+constexpr uint32_t kPrepSmem = P_MISC + 16 + 1024;
+// After the A products complete (row and column operands free):
+constexpr uint32_t P_AKK = 0;                    // A_kk fp32 [64][kAS]
+constexpr uint32_t P_TF = 17408;                 // T fp32 [64][kAS]
+constexpr uint32_t P_NB = 34816;                 // N blocks of the solve, 9 x [16][20] fp32
+// Once T is in registers: T Diag(beta) as bf16 hi and lo, A operands of 128 rows (the first 64 used)
+constexpr uint32_t P_TH = 0, P_TL = 16384;
+constexpr uint32_t kPrepTmemCols = 256;
+constexpr uint32_t TM_A0 = 0, TM_A1 = 32, TM_A2 = 64, TM_A3 = 128;  // row blocks of A: 16, 32, 48, 64 columns
+constexpr uint32_t TM_W = 0, TM_U = 128;                            // then W and U (rows in lanes 0-63)
+constexpr uint32_t kKQGBytes = 4 * 8192 + 4 * 8192;
+
+static_assert(P_NB + 9 * 16 * kNB * 4 <= P_G, "solve work overflows its region");
+static_assert(P_CC + cc_off(2) + 2 * 48 * 128 <= P_BETA, "column operands overflow");
+static_assert(2 * (kPrepSmem + 1024) <= 233472, "two prep CTAs per SM");
+
+__global__ void __launch_bounds__(kPrepThreads, 2)
+chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                  const float* __restrict__ beta, const int32_t* __restrict__ cu, const int32_t* __restrict__ off,
+                  int N, int64_t T_total, int H, int m0, uint8_t* __restrict__ blobs, unsigned int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
-    float* sBetaBuf = reinterpret_cast<float*>(sm + OFF_BETA);
-    float* sE = reinterpret_cast<float*>(sm + OFF_E);
-    float* sDt = reinterpret_cast<float*>(sm + OFF_DT);
-    float* sEGl = reinterpret_cast<float*>(sm + OFF_EGL);
-    float* sTot = reinterpret_cast<float*>(sm + OFF_TOT);
-    uint64_t* barA = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-    uint64_t* barS = barA + 1;
-    uint64_t* barL = barA + 2;  // k, q, g tiles
-    uint64_t* barV = barA + 3;  // v tile
-    uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
-    volatile int* sAbort = reinterpret_cast<volatile int*>(sm + OFF_MISC + 4);
-    float* sG = reinterpret_cast<float*>(sm + OFF_STG);
-    float* sAkk = reinterpret_cast<float*>(sm + OFF_AKK);
-    float* sTf = reinterpret_cast<float*>(sm + OFF_TF);
-    float* sO = reinterpret_cast<float*>(sm + OFF_RR);
-
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int chain = blockIdx.x, n = chain / H, h = chain % H;
-    const int row = tid & 127, qq = tid >> 7;  // state row / TMEM lane; quarter of the key channels / tokens
-    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const int h = blockIdx.x % H;
+    const int m = m0 + blockIdx.x / H;
+    if (m >= off[N]) return;  // past the last chunk (the grid covers an upper bound of the chunk count)
+    int lo = 0, hi = N;       // off[lo] <= m < off[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (off[mid] <= m) lo = mid; else hi = mid;
+    }
     int64_t bos, eos;
-    seq_bounds(cu, n, T_total, bos, eos);
-    const int64_t state_off = (int64_t)chain * kD * kD + (int64_t)row * kD + 32 * qq;
+    seq_bounds(cu, lo, T_total, bos, eos);
+    const int64_t c0 = bos + (int64_t)kC * (m - off[lo]);
+    const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
+    uint8_t* blob = blobs + ((int64_t)(m - m0) * H + h) * kBlobBytes;
+
+    float* sBeta = reinterpret_cast<float*>(sm + P_BETA);
+    uint64_t* barL = reinterpret_cast<uint64_t*>(sm + P_BAR);
+    uint64_t* barV = barL + 1;
+    uint64_t* barA = barL + 2;
+    uint64_t* barW = barL + 3;
+    uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + P_MISC);
+    volatile int* sAbort = reinterpret_cast<volatile int*>(sm + P_MISC + 4);
 
     if (tid == 0) {
-        mbar_init(barA, 1);
-        mbar_init(barS, 1);
         mbar_init(barL, 1);
         mbar_init(barV, 1);
+        mbar_init(barA, 1);
+        mbar_init(barW, 1);
         fence_mbar_init();
         *sAbort = 0;
-    }
-    if (warp == 0) tmem_alloc(sTmem, kTmemCols);
-    __syncthreads();  // barriers initialised before the first copy lands on them
-    if (bos < eos) {  // the first chunk's inputs
-        const int L0 = (eos - bos) < kC ? (int)(eos - bos) : kC;
-        prefetch_kqg(sm, barL, sBetaBuf, &tm_k, &tm_q, &tm_g, beta, bos, L0, H, h, tid);
-        prefetch_v(sm, barV, &tm_v, bos, h, tid);
-        cp_async_commit();
-    }
-
-    // state: row `row`, key channels [32 qq, 32 qq + 32) in registers; bf16 copy as the S0 operand
-    float s[32];
+        mbar_arrive_expect_tx(barL, kKQGBytes);
+        tma_load_3d(sm + P_RR, &tm_k, 0, h, (int)c0, barL);             // k, channels 0-63  -> region 0 rows 0-63
+        tma_load_3d(sm + P_RR + 8192, &tm_q, 0, h, (int)c0, barL);      // q, channels 0-63  -> region 0 rows 64-127
+        tma_load_3d(sm + P_RR + 16384, &tm_k, 64, h, (int)c0, barL);    // k, channels 64-127 -> region 1
+        tma_load_3d(sm + P_RR + 24576, &tm_q, 64, h, (int)c0, barL);
 #pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-        float4 x = init_state ? *reinterpret_cast<const float4*>(init_state + state_off + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-        s[j] = x.x; s[j + 1] = x.y; s[j + 2] = x.z; s[j + 3] = x.w;
+        for (int b4 = 0; b4 < 4; ++b4) tma_load_3d(sm + P_G + b4 * 8192, &tm_g, 32 * b4, h, (int)c0, barL);
     }
-    auto write_state_operand = [&]() {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = s[8 * c + e];
-            *reinterpret_cast<uint4*>(sm + OFF_S + (qq >> 1) * 16384 + sw128(row, 4 * (qq & 1) + c)) = pack8(f);
-        }
-    };
-    write_state_operand();
+    if (tid < kC) {
+        const bool ok = tid < L;
+        cp_async4(sBeta + tid, beta + (ok ? (c0 + tid) * H + h : 0), ok ? 4u : 0u);
+    }
+    cp_async_commit();
+    if (warp == 0) tmem_alloc(sTmem, kPrepTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = *sTmem;
-    uint32_t phaseA = 0, phaseS = 0, phaseL = 0, phaseV = 0;
-
-    auto wait_bar = [&](uint64_t* b, uint32_t& ph) {
-        if (!mbar_wait(b, ph, kWaitLimit)) {
-            *sAbort = 1;
-            raise_device_error(err, kErrMbarTimeout);
+    uint32_t issued = 1u;  // thread 0: which barriers have work in flight (1 = loads, 2 = v, 4 = A, 8 = W/U)
+    if (tid == 0) solo_wait(barL, 0, sAbort, err);
+    cp_async_wait_all();
+    __syncthreads();
+    do {
+        if (*sAbort) break;
+        // ---- running sum of g (log2 units).  Thread (cc, r4) owns channels 8cc .. 8cc+7 of rows r4 + 16 I
+        // (I = 0..3); the 16 lanes of a half-warp hold the 16 rows of a block, summed by shuffles.
+        const int cc = 2 * warp + (lane >> 4), r4 = lane & 15, c = 8 * cc;
+        const uint32_t reg = cc >> 3, ch = cc & 7;
+        float G[4][8], E[4][8];
+#pragma unroll
+        for (int I = 0; I < 4; ++I) {
+            const int i = r4 + 16 * I;
+            const uint8_t* gp = sm + P_G + (cc >> 2) * 8192;
+            const float4 x0 = *reinterpret_cast<const float4*>(gp + sw128(i, 2 * (cc & 3)));
+            const float4 x1 = *reinterpret_cast<const float4*>(gp + sw128(i, 2 * (cc & 3) + 1));
+            const float s = i < L ? kLog2e : 0.f;
+            G[I][0] = x0.x * s; G[I][1] = x0.y * s; G[I][2] = x0.z * s; G[I][3] = x0.w * s;
+            G[I][4] = x1.x * s; G[I][5] = x1.y * s; G[I][6] = x1.z * s; G[I][7] = x1.w * s;
         }
-        ph ^= 1u;
-        tc_fence_after();
-    };
-    auto wait_mma = [&]() { wait_bar(barS, phaseS); };
-
-    const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
-    const uint32_t id_t64 = idesc_tf32_f32(128, 64);
-    const uint32_t id_ds = idesc_bf16_f32(128, 128, false, true);
-
-    int buf = 0;
-    for (int64_t c0 = bos; c0 < eos; c0 += kC, buf ^= 1) {
-        const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
-        const int64_t c1 = c0 + kC;
-        const int L1 = c1 < eos ? ((eos - c1) < kC ? (int)(eos - c1) : kC) : 0;
-        const float* sBeta = sBetaBuf + 64 * buf;
-        cp_async_wait_all();
-        wait_bar(barL, phaseL);
-        wait_bar(barV, phaseV);
-        __syncthreads();
-        // ---- (1) running sum of g per key channel: thread (c, qq) sums the 16 tokens of block qq
+#pragma unroll
+        for (int d = 1; d < 16; d <<= 1) {
+#pragma unroll
+            for (int I = 0; I < 4; ++I)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float y = __shfl_up_sync(0xFFFFFFFFu, G[I][e], d, 16);
+                    if (r4 >= d) G[I][e] += y;
+                }
+        }
         {
-            const int c = row;
-            float acc = 0.f;
+            float base[8];
 #pragma unroll
-            for (int i = 16 * qq; i < 16 * qq + 16; ++i) {  // in log2 units: every use is a power of e
-                acc = fmaf(i < L ? sG[i * kD + c] : 0.f, kLog2e, acc);
-                sG[i * kD + c] = acc;
-            }
-            sTot[qq * kD + c] = acc;
-            __syncthreads();
-            float base = 0.f;
+            for (int e = 0; e < 8; ++e) base[e] = 0.f;
 #pragma unroll
-            for (int p2 = 0; p2 < 3; ++p2)
-                if (p2 < qq) base += sTot[p2 * kD + c];
-            if (qq > 0) {
+            for (int I = 0; I < 4; ++I)
 #pragma unroll
-                for (int i = 16 * qq; i < 16 * qq + 16; ++i) sG[i * kD + c] += base;
-            }
-            sE[qq * kD + c] = base + acc;  // G at the last token of block qq
-            __syncthreads();
-            if (qq == 0) {
-                float e[4];
-#pragma unroll
-                for (int I = 0; I < 4; ++I) e[I] = sE[I * kD + c];
-                sEGl[c] = exp2f(e[3]);
-                sDt[0 * kD + c] = ex2(e[1] - e[0]);
-                sDt[1 * kD + c] = ex2(e[2] - e[0]);
-                sDt[2 * kD + c] = ex2(e[3] - e[0]);
-            } else if (qq == 1) {
-                const float e1 = sE[1 * kD + c], e2 = sE[2 * kD + c], e3 = sE[3 * kD + c];
-                sDt[3 * kD + c] = ex2(e2 - e1);
-                sDt[4 * kD + c] = ex2(e3 - e1);
-                sDt[5 * kD + c] = ex2(e3 - e2);
-            }
-            __syncthreads();
+                for (int e = 0; e < 8; ++e) {
+                    const float tot = __shfl_sync(0xFFFFFFFFu, G[I][e], 15, 16);
+                    G[I][e] += base[e];
+                    base[e] += tot;
+                    E[I][e] = base[e];  // G at the last token of block I
+                }
         }
-        // ---- (2) operands: row operand RR, column operands CC / KP, B1 = [beta K e^G ; Q e^G]
+        if (r4 == 0) {
+            float4* eg = reinterpret_cast<float4*>(blob + BLOB_EGL + 4 * c);
+            eg[0] = make_float4(exp2f(E[3][0]), exp2f(E[3][1]), exp2f(E[3][2]), exp2f(E[3][3]));
+            eg[1] = make_float4(exp2f(E[3][4]), exp2f(E[3][5]), exp2f(E[3][6]), exp2f(E[3][7]));
+        }
+        float dn[3][8];  // e^{E_{J+1} - E_J}
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            const int id = tid + kThreads * m, i = id >> 4, cc = id & 15, c = cc * 8, I = i >> 4;
-            const uint32_t reg = cc >> 3, ch = cc & 7;
-            float kv[8], qv[8], Gv[8], Ev[8];
-            unpack8(*reinterpret_cast<const uint4*>(sm + OFF_STK + i * 256 + cc * 16), kv);
-            unpack8(*reinterpret_cast<const uint4*>(sm + OFF_STQ + i * 256 + cc * 16), qv);
-            *reinterpret_cast<float4*>(Gv) = *reinterpret_cast<const float4*>(sG + i * kD + c);
-            *reinterpret_cast<float4*>(Gv + 4) = *reinterpret_cast<const float4*>(sG + i * kD + c + 4);
-            *reinterpret_cast<float4*>(Ev) = *reinterpret_cast<const float4*>(sE + I * kD + c);
-            *reinterpret_cast<float4*>(Ev + 4) = *reinterpret_cast<const float4*>(sE + I * kD + c + 4);
-            const float b = sBeta[i];
-            float rk[8], rq[8], bk[8], eq[8], kr[8];
+        for (int J = 0; J < 3; ++J)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dn[J][e] = ex2(E[J + 1][e] - E[J][e]);
+        __syncthreads();  // every thread holds its g: the g boxes become K e^G and V
+        if (tid == 0) {
+            fence_proxy_async();
+            mbar_arrive_expect_tx(barV, 16384);
+            tma_load_3d(sm + P_V, &tm_v, 0, h, (int)c0, barV);
+            tma_load_3d(sm + P_V + 8192, &tm_v, 64, h, (int)c0, barV);
+            issued |= 2u;
+        }
+        // ---- operands.  Row i = r4 + 16 I, channels 8cc ..:  row operand in place; K e^G (for W);
+        // Q e^G (workspace); column operands of blocks J >= I (KP also to the workspace).
+#pragma unroll
+        for (int I = 0; I < 4; ++I) {
+            const int i = r4 + 16 * I;
+            uint4* kp = reinterpret_cast<uint4*>(sm + P_RR + reg * 16384 + sw128(i, ch));
+            uint4* qp = reinterpret_cast<uint4*>(sm + P_RR + reg * 16384 + sw128(64 + i, ch));
+            float kv[8], qv[8];
+            unpack8(*kp, kv);
+            unpack8(*qp, qv);
+            float rk[8], rq[8], kg[8], qg[8], kr[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const float f = ex2(Gv[e] - Ev[e]);   // >= 1
-                const float r = ex2(Ev[e] - Gv[e]);   // <= 1
-                const float eg = ex2(Gv[e]);          // <= 1
+                const float f = ex2(G[I][e] - E[I][e]);   // >= 1
+                const float r = ex2(E[I][e] - G[I][e]);   // <= 1
+                const float eg = ex2(G[I][e]);            // <= 1
                 rk[e] = kv[e] * f;
                 rq[e] = qv[e] * f;
-                bk[e] = b * kv[e] * eg;
-                eq[e] = qv[e] * eg;
+                kg[e] = kv[e] * eg;
+                qg[e] = qv[e] * eg;
                 kr[e] = kv[e] * r;
             }
-            *reinterpret_cast<uint4*>(sm + OFF_RR + reg * 16384 + sw128(i, ch)) = pack8(rk);
-            *reinterpret_cast<uint4*>(sm + OFF_RR + reg * 16384 + sw128(64 + i, ch)) = pack8(rq);
-            *reinterpret_cast<uint4*>(sm + OFF_B1 + reg * 16384 + sw128(i, ch)) = pack8(bk);
-            *reinterpret_cast<uint4*>(sm + OFF_B1 + reg * 16384 + sw128(64 + i, ch)) = pack8(eq);
+            *kp = pack8(rk);
+            *qp = pack8(rq);
+            *reinterpret_cast<uint4*>(sm + P_KG + reg * 8192 + sw128(i, ch)) = pack8(kg);
+            *reinterpret_cast<uint4*>(blob + BLOB_B1 + reg * 16384 + sw128(64 + i, ch)) = pack8(qg);
             // column operands of row blocks J >= I: k_j e^{E_J - G_j} = kr * e^{E_J - E_I}
 #pragma unroll
             for (int J = 0; J < 4; ++J) {
                 if (J < I) continue;
-                float cv[8];
-                if (J == I) {
+                if (J > I) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) cv[e] = kr[e];
-                } else {
-                    const int pair = I == 0 ? J - 1 : (I == 1 ? J + 1 : 5);
-                    const float* dt = sDt + pair * kD + c;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) cv[e] = kr[e] * dt[e];
+                    for (int e = 0; e < 8; ++e) kr[e] *= dn[J - 1][e];
                 }
-                if (J == 3)
-                    *reinterpret_cast<uint4*>(sm + OFF_KP + reg * 8192 + sw128(i, ch)) = pack8(cv);
-                else
-                    *reinterpret_cast<uint4*>(sm + OFF_CC + cc_off(J) + reg * (16u * (J + 1) * 128u) + sw128(i, ch)) =
-                        pack8(cv);
+                const uint4 u = pack8(kr);
+                if (J == 3) {
+                    *reinterpret_cast<uint4*>(sm + P_KP + reg * 8192 + sw128(i, ch)) = u;
+                    *reinterpret_cast<uint4*>(blob + BLOB_KP + reg * 8192 + sw128(i, ch)) = u;
+                } else {
+                    *reinterpret_cast<uint4*>(sm + P_CC + cc_off(J) + reg * (16u * (J + 1) * 128u) + sw128(i, ch)) = u;
+                }
             }
         }
         fence_proxy_async();
+        tc_fence_before();
         __syncthreads();
-        // k, q, g of the next chunk may now land in the staging buffers
-        if (L1 > 0) prefetch_kqg(sm, barL, sBetaBuf + 64 * (buf ^ 1), &tm_k, &tm_q, &tm_g, beta, c1, L1, H, h, tid);
-        cp_async_commit();
-        // ---- (3) the four row blocks of A (barrier A), then the S0 products (barrier S)
+        // ---- the four row blocks of A
         if (tid == 0) {
             tc_fence_after();
-            const uint64_t rr = kdesc(sbase + OFF_RR);
-            mma_k128(tbase + TM_A0, rr, 16384, kdesc(sbase + OFF_CC + cc_off(0)), 2048, idesc_bf16_f32(128, 16, false, false));
-            mma_k128(tbase + TM_A1, rr, 16384, kdesc(sbase + OFF_CC + cc_off(1)), 4096, idesc_bf16_f32(128, 32, false, false));
-            mma_k128(tbase + TM_A2, rr, 16384, kdesc(sbase + OFF_CC + cc_off(2)), 6144, idesc_bf16_f32(128, 48, false, false));
-            mma_k128(tbase + TM_A3, rr, 16384, kdesc(sbase + OFF_KP), 8192, idesc_bf16_f32(128, 64, false, false));
+            const uint64_t rr = kdesc(sbase + P_RR);
+            mma_k128(tbase + TM_A0, rr, 16384, kdesc(sbase + P_CC + cc_off(0)), 2048, idesc_bf16_f32(128, 16, false, false));
+            mma_k128(tbase + TM_A1, rr, 16384, kdesc(sbase + P_CC + cc_off(1)), 4096, idesc_bf16_f32(128, 32, false, false));
+            mma_k128(tbase + TM_A2, rr, 16384, kdesc(sbase + P_CC + cc_off(2)), 6144, idesc_bf16_f32(128, 48, false, false));
+            mma_k128(tbase + TM_A3, rr, 16384, kdesc(sbase + P_KP), 8192, idesc_bf16_f32(128, 64, false, false));
             mma_commit(barA);
-            mma_k128(tbase + TM_Y, kdesc(sbase + OFF_S), 16384, kdesc(sbase + OFF_B1), 16384, id_s);
-            mma_commit(barS);
+            issued |= 4u;
+            solo_wait(barA, 0, sAbort, err);
         }
-        wait_bar(barA, phaseA);
-        // ---- (4) A_kk (fp32 work array) and A_qk (bf16 operand); warps of key quarters 0, 1
-        if (qq < 2) {
+        cta_sync_tc();
+        if (*sAbort) break;
+        float* sAkk = reinterpret_cast<float*>(sm + P_AKK);
+        float* sTf = reinterpret_cast<float*>(sm + P_TF);
+        // ---- A_kk (fp32 work array) and A_qk (tf32 operand, to the workspace)
+        {
             // lane quarter qt holds rows 32qt .. 32qt+31 of [k-rows ; q-rows]: lanes 0-15 belong to row block
-            // 2(qt%2) and lanes 16-31 to 2(qt%2)+1; warps with qq = 0 read the first block's columns, qq = 1 the second's.
-            const int qt = warp & 3, Ib = 2 * (qt & 1) + qq;
-            const bool mine = ((lane >> 4) == qq);
+            // 2(qt%2) and lanes 16-31 to 2(qt%2)+1; warps 0-3 read the first block's columns, warps 4-7 the second's.
+            const int qt = warp & 3, hq = warp >> 2, Ib = 2 * (qt & 1) + hq;
+            const bool mine = ((lane >> 4) == hq);
             const int r = 32 * qt + lane;
             const int i = r & 63;
             const bool is_k = r < 64;
-            // 64 columns from the block's first column; those past its 16(Ib+1) are masked below
+            const uint32_t lane_base = (uint32_t)(32 * qt) << 16;
             const uint32_t col0 = Ib == 0 ? TM_A0 : (Ib == 1 ? TM_A1 : (Ib == 2 ? TM_A2 : TM_A3));
             uint32_t a[64];
             {
@@ -499,167 +533,391 @@ chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             const int j = 4 * c4 + e;
                             f[e] = (j <= i && j < ncols) ? to_tf32(__uint_as_float(a[j])) : 0.f;
                         }
-                        *reinterpret_cast<float4*>(sm + OFF_AQ + (c4 >> 3) * 8192 + sw128(i, c4 & 7)) =
+                        *reinterpret_cast<float4*>(blob + BLOB_AQ + (c4 >> 3) * 8192 + sw128(i, c4 & 7)) =
                             make_float4(f[0], f[1], f[2], f[3]);
                     }
                 }
             }
         }
-        wait_bar(barS, phaseS);  // the S0 products are done: B1 becomes the solve's work space
         __syncthreads();
-        // ---- (5) T = (I + A_kk)^-1 by 16 x 16 blocks (fp32)
+        // ---- T = (I + A_kk)^-1 by 16 x 16 blocks (fp32)
         if (lane < 16 && warp < 4) {  // diagonal block `warp`, column `lane`, right-looking (independent updates)
-            const int I = warp, c = lane;
+            const int I = warp, cl = lane;
             const float* A = sAkk + 16 * I * kAS + 16 * I;
             float x[16];
 #pragma unroll
-            for (int r2 = 0; r2 < 16; ++r2) x[r2] = (r2 == c) ? 1.f : 0.f;
+            for (int r2 = 0; r2 < 16; ++r2) x[r2] = (r2 == cl) ? 1.f : 0.f;
 #pragma unroll
             for (int r2 = 0; r2 < 16; ++r2)
 #pragma unroll
                 for (int r3 = r2 + 1; r3 < 16; ++r3) x[r3] = fmaf(-A[r3 * kAS + r2], x[r2], x[r3]);
 #pragma unroll
-            for (int r2 = 0; r2 < 16; ++r2) sTf[(16 * I + r2) * kAS + 16 * I + c] = x[r2];
+            for (int r2 = 0; r2 < 16; ++r2) sTf[(16 * I + r2) * kAS + 16 * I + cl] = x[r2];
         }
         __syncthreads();
-        t_offdiag(sAkk, sTf, reinterpret_cast<float*>(sm + OFF_NB), tid);
-        {   // T as a tf32 operand (zero above the diagonal blocks); all of T is read before B1 / CC are reused
-            float4 f[2];
+        t_offdiag(sAkk, sTf, reinterpret_cast<float*>(sm + P_NB), tid);
+        // ---- T Diag(beta) = hi + lo (bf16 each): thread owns row tid / 4, columns 16 (tid % 4) ..
+        {
+            const int i = tid >> 2, j0 = 16 * (tid & 3);
+            float tv[16];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int id = tid + kThreads * u, i = id >> 4, c4 = id & 15;
-                if ((c4 >> 2) > (i >> 4)) {
-                    f[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int j4 = 0; j4 < 16; j4 += 4) {
+                const float4 x = *reinterpret_cast<const float4*>(sTf + i * kAS + j0 + j4);
+                const float4 bb = *reinterpret_cast<const float4*>(sBeta + j0 + j4);
+                const bool zero = (j0 >> 4) > (i >> 4);   // above the diagonal blocks
+                tv[j4] = zero ? 0.f : x.x * bb.x; tv[j4 + 1] = zero ? 0.f : x.y * bb.y;
+                tv[j4 + 2] = zero ? 0.f : x.z * bb.z; tv[j4 + 3] = zero ? 0.f : x.w * bb.w;
+            }
+            float hiv[16], lov[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                hiv[e] = __bfloat162float(__float2bfloat16_rn(tv[e]));
+                lov[e] = tv[e] - hiv[e];
+            }
+            __syncthreads();  // every read of T is done: its space takes the two operands
+#pragma unroll
+            for (int h8 = 0; h8 < 2; ++h8) {
+                float a8[8], b8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) { a8[e] = hiv[8 * h8 + e]; b8[e] = lov[8 * h8 + e]; }
+                const uint32_t at = sw128(i, (j0 >> 3) + h8);
+                *reinterpret_cast<uint4*>(sm + P_TH + at) = pack8(a8);
+                *reinterpret_cast<uint4*>(sm + P_TL + at) = pack8(b8);
+            }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        // ---- W = T Diag(beta) K e^G and U = T Diag(beta) V (rows of D in TMEM lanes 0-63)
+        if (tid == 0) {
+            solo_wait(barV, 0, sAbort, err);
+            tc_fence_after();
+            const uint32_t id_w = idesc_bf16_f32(128, 128, false, true);
+            const uint64_t th = kdesc(sbase + P_TH), tl = kdesc(sbase + P_TL);
+            const uint64_t kgd = sdesc_sw128(sbase + P_KG, 8192, 1024), vd = sdesc_sw128(sbase + P_V, 8192, 1024);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) mma_bf16(tbase + TM_W, th + ks * 2, kgd + ks * 128, id_w, ks > 0 ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) mma_bf16(tbase + TM_W, tl + ks * 2, kgd + ks * 128, id_w, 1u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) mma_bf16(tbase + TM_U, th + ks * 2, vd + ks * 128, id_w, ks > 0 ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) mma_bf16(tbase + TM_U, tl + ks * 2, vd + ks * 128, id_w, 1u);
+            mma_commit(barW);
+            issued |= 8u;
+            solo_wait(barW, 0, sAbort, err);
+        }
+        cta_sync_tc();
+        if (*sAbort) break;
+        // W (bf16, rows 0-63 of B1) by warps 0, 1; U (fp32 rows) by warps 4, 5
+        if ((warp & 2) == 0) {
+            const int i = 32 * (warp & 1) + lane;
+            const uint32_t lane_base = (uint32_t)(32 * (warp & 1)) << 16;
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                uint32_t x[32];
+                tmem_ld32_async(tbase + lane_base + (warp < 4 ? TM_W : TM_U) + 32 * p, x);
+                tmem_wait_ld(); reg_fence(x);
+                if (warp < 4) {
+#pragma unroll
+                    for (int q8 = 0; q8 < 4; ++q8) {
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(x[8 * q8 + e]);
+                        const int cch = 4 * p + q8;  // 16-byte chunk of the row: channels 8 cch ..
+                        *reinterpret_cast<uint4*>(blob + BLOB_B1 + (cch >> 3) * 16384 + sw128(i, cch & 7)) = pack8(f);
+                    }
                 } else {
-                    const float4 x = *reinterpret_cast<const float4*>(sTf + i * kAS + 4 * c4);
-                    f[u] = make_float4(to_tf32(x.x), to_tf32(x.y), to_tf32(x.z), to_tf32(x.w));
+                    float4* up = reinterpret_cast<float4*>(blob + BLOB_U + i * 512 + 128 * p);
+#pragma unroll
+                    for (int q4 = 0; q4 < 8; ++q4)
+                        up[q4] = make_float4(__uint_as_float(x[4 * q4]), __uint_as_float(x[4 * q4 + 1]),
+                                             __uint_as_float(x[4 * q4 + 2]), __uint_as_float(x[4 * q4 + 3]));
                 }
             }
-            __syncthreads();
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int id = tid + kThreads * u, i = id >> 4, c4 = id & 15;
-                *reinterpret_cast<float4*>(sm + OFF_TT + (c4 >> 3) * 8192 + sw128(i, c4 & 7)) = f[u];
-            }
         }
-        // ---- Z^T = (beta V)^T - Y^T; thread (row, qq) owns tokens 16qq .. 16qq+15
-        {
-            uint32_t y[16];
-            tmem_ld16_async(tbase + lane_base + TM_Y + 16 * qq, y);
-            tmem_wait_ld(); reg_fence(y);
-            const __nv_bfloat16* sv = reinterpret_cast<const __nv_bfloat16*>(sm + OFF_STV);
-            // tf32 row `row` of Z^T: tokens 16qq .. 16qq+15 are 4 chunks of region qq >> 1
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                float f[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int j = 16 * qq + 4 * c4 + e;
-                    f[e] = to_tf32(sBeta[j] * __bfloat162float(sv[j * kD + row]) - __uint_as_float(y[4 * c4 + e]));
-                }
-                *reinterpret_cast<float4*>(sm + OFF_ZT + (qq >> 1) * 16384 + sw128(row, 4 * (qq & 1) + c4)) =
-                    make_float4(f[0], f[1], f[2], f[3]);
-            }
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-        // v of the next chunk may now land
-        if (L1 > 0) prefetch_v(sm, barV, &tm_v, c1, h, tid);
-        cp_async_commit();
-        if (*sAbort) break;
-        // ---- (6) V'^T = Z^T T^T
+    } while (0);
+    if (*sAbort && tid == 0) {  // copies or products still in flight end before the CTA does (bounded)
+        if (issued & 1u) mbar_wait(barL, 0, kWaitLimit);
+        if (issued & 2u) mbar_wait(barV, 0, kWaitLimit);
+        if (issued & 4u) mbar_wait(barA, 0, kWaitLimit);
+        if (issued & 8u) mbar_wait(barW, 0, kWaitLimit);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, kPrepTmemCols);
+}
+
+// =============================================================================================
+// chunk_state_kernel: one (sequence, head) chain through a range of its chunks
+// =============================================================================================
+constexpr int kThreads = 512;
+constexpr uint32_t S_S = 0;             // bf16 S0 [128][128], A operand of the S0 products
+constexpr uint32_t S_B1 = 32768;        // [W ; Q e^G] of two chunks, 32 KB each
+constexpr uint32_t S_U = 98304;         // U fp32 [64][128]
+constexpr uint32_t S_AQ = 131072;       // A_qk tf32          } one copy
+constexpr uint32_t S_KP = 147456;       // K e^{G_C - G} bf16 }
+constexpr uint32_t S_EGL = 163840;      // e^{G_C} fp32 [128] }
+constexpr uint32_t S_ZT = 164864;       // V'^T tf32 [128][64] (two regions of 16 KB), A of the output product
+constexpr uint32_t S_VB = 197632;       // V'^T bf16 [128][64], A of the state product
+constexpr uint32_t S_BAR = 214016;      // mbarriers: B1 x2, U, A_qk/KP/e^{G_C}, S0 products, dS, output product
+constexpr uint32_t S_MISC = S_BAR + 64; // TMEM base, abort flag
+constexpr uint32_t kStateSmem = S_MISC + 64 + 1024;
+constexpr uint32_t kAQKBytes = BLOB_EGL + 512 - BLOB_AQ;
+// TMEM columns: S0 products of chunk parity p at 128 p (Y^T in 64 columns, then O^T in 64); dS at 256
+constexpr uint32_t TM_DS = 256;
+constexpr uint32_t kTmemCols = 512;
+
+static_assert(S_KP - S_AQ == BLOB_KP - BLOB_AQ && S_EGL - S_AQ == BLOB_EGL - BLOB_AQ, "copy layout");
+static_assert(S_EGL + 512 <= S_ZT && S_ZT % 1024 == 0 && S_VB % 1024 == 0, "alignment");
+static_assert(kStateSmem <= 232448, "shared memory");
+
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, const int32_t* __restrict__ off,
+                   int64_t T_total, int H, float scale, const __nv_bfloat16* __restrict__ gate,
+                   __nv_bfloat16* __restrict__ o, float* final_state, const float* carry_in, float* carry_out,
+                   int first_range, int m0, int m1, const uint8_t* __restrict__ blobs, unsigned int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int chain = blockIdx.x, n = chain / H, h = chain % H;
+    const int on = off[n], on1 = off[n + 1];
+    int lo = on > m0 ? on : m0, hi = on1 < m1 ? on1 : m1;
+    const bool empty_seq = on == on1;
+    if (empty_seq) {
+        if (!first_range) return;  // an empty sequence passes its initial state through once
+        lo = hi = 0;
+    } else if (lo >= hi) {
+        return;                    // no chunk of this chain in the range
+    }
+    const bool starts = empty_seq || lo == on;   // the chain begins here: initial state
+    const bool ends = empty_seq || hi == on1;    // the chain ends here: final state
+    const int row = tid & 127, qq = tid >> 7;    // state row / TMEM lane; quarter of the key channels / tokens
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const int64_t in_off = (starts ? (int64_t)chain : (int64_t)h) * kD * kD + (int64_t)row * kD + 32 * qq;
+    const int64_t out_off = (ends ? (int64_t)chain : (int64_t)h) * kD * kD + (int64_t)row * kD + 32 * qq;
+    const float* s_in = starts ? init_state : carry_in;
+    float* s_out = ends ? final_state : carry_out;
+    int64_t bos, eos;
+    seq_bounds(cu, n, T_total, bos, eos);
+
+    const float* sU = reinterpret_cast<const float*>(sm + S_U);
+    const float* sEGl = reinterpret_cast<const float*>(sm + S_EGL);
+    uint64_t* barB = reinterpret_cast<uint64_t*>(sm + S_BAR);  // [2]
+    uint64_t* barU = barB + 2;
+    uint64_t* barK = barB + 3;
+    uint64_t* barM = barB + 4;
+    uint64_t* barD = barB + 5;
+    uint64_t* barO = barB + 6;
+    uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + S_MISC);
+    volatile int* sAbort = reinterpret_cast<volatile int*>(sm + S_MISC + 4);
+
+    auto blob_of = [&](int mm) { return blobs + ((int64_t)(mm - m0) * H + h) * kBlobBytes; };
+    auto chunk_start = [&](int mm) { return bos + (int64_t)kC * (mm - on); };
+    // loads (thread 0 issues; the previous readers of each buffer are ordered before by a barrier or a
+    // completed product)
+    uint32_t pend = 0;  // copies in flight (thread 0): bit b = B1 buffer b, 4 = U, 8 = A_qk/KP/e^{G_C}
+    auto load_b1 = [&](int mm, int b) {
         if (tid == 0) {
-            tc_fence_after();
-            const uint64_t za = kdesc(sbase + OFF_ZT), tb = kdesc(sbase + OFF_TT);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {  // K = 64 tokens, 8 per tf32 instruction
-                const uint32_t reg = ks >> 2, off = (ks & 3) * 32;
-                mma_tf32(tbase + TM_V, za + ((reg * 16384 + off) >> 4), tb + ((reg * 8192 + off) >> 4), id_t64,
-                         ks > 0 ? 1u : 0u);
-            }
-            mma_commit(barS);
+            fence_proxy_async();
+            mbar_arrive_expect_tx(barB + b, 32768);
+            bulk_load(sm + S_B1 + b * 32768, blob_of(mm) + BLOB_B1, 32768, barB + b);
+            pend |= 1u << b;
         }
-        wait_mma();
-        {
-            uint32_t x[16];
-            tmem_ld16_async(tbase + lane_base + TM_V + 16 * qq, x);
-            tmem_wait_ld(); reg_fence(x);
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)  // tf32 copy for the output product
-                *reinterpret_cast<float4*>(sm + OFF_ZT + (qq >> 1) * 16384 + sw128(row, 4 * (qq & 1) + c4)) =
-                    make_float4(to_tf32(__uint_as_float(x[4 * c4])), to_tf32(__uint_as_float(x[4 * c4 + 1])),
-                                to_tf32(__uint_as_float(x[4 * c4 + 2])), to_tf32(__uint_as_float(x[4 * c4 + 3])));
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {  // bf16 copy for the state update
-                float f[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(x[8 * c2 + e]);
-                *reinterpret_cast<uint4*>(sm + OFF_VB + sw128(row, 2 * qq + c2)) = pack8(f);
-            }
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-        // ---- (7) O^T += V'^T A_qk^T;  dS = V'^T (K e^{G_C - G})
+    };
+    auto load_u = [&](int mm) {
         if (tid == 0) {
-            tc_fence_after();
-            const uint64_t va = kdesc(sbase + OFF_ZT), aq = kdesc(sbase + OFF_AQ);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t reg = ks >> 2, off = (ks & 3) * 32;
-                mma_tf32(tbase + TM_O, va + ((reg * 16384 + off) >> 4), aq + ((reg * 8192 + off) >> 4), id_t64, 1u);
-            }
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tbase + TM_DS, kdesc(sbase + OFF_VB) + ks * 2, sdesc_sw128(sbase + OFF_KP, 8192, 1024) + ks * 128,
-                         id_ds, ks > 0 ? 1u : 0u);
-            mma_commit(barS);
+            fence_proxy_async();
+            mbar_arrive_expect_tx(barU, 32768);
+            bulk_load(sm + S_U, blob_of(mm) + BLOB_U, 32768, barU);
+            pend |= 4u;
         }
-        wait_mma();
-        // ---- (8) outputs (fp32 staging, then coalesced) and the state update
-        {
-            uint32_t xo[16], d0[32];
-            tmem_ld16_async(tbase + lane_base + TM_O + 16 * qq, xo);
-            tmem_ld32_async(tbase + lane_base + TM_DS + 32 * qq, d0);
-            tmem_wait_ld(); reg_fence(xo); reg_fence(d0);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) sO[(16 * qq + e) * kD + row] = scale * __uint_as_float(xo[e]);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) s[e] = fmaf(s[e], sEGl[32 * qq + e], __uint_as_float(d0[e]));
+    };
+    auto load_aqk = [&](int mm) {
+        if (tid == 0) {
+            fence_proxy_async();
+            mbar_arrive_expect_tx(barK, kAQKBytes);
+            bulk_load(sm + S_AQ, blob_of(mm) + BLOB_AQ, kAQKBytes, barK);
+            pend |= 8u;
         }
-        write_state_operand();
-        tc_fence_before();
-        __syncthreads();
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            const int id = tid + kThreads * m, j = id >> 4, c16 = id & 15;
-            if (j < L) {
-                float f[8];
-                *reinterpret_cast<float4*>(f) = *reinterpret_cast<const float4*>(sO + j * kD + 8 * c16);
-                *reinterpret_cast<float4*>(f + 4) = *reinterpret_cast<const float4*>(sO + j * kD + 8 * c16 + 4);
-                const int64_t at = ((c0 + j) * H + h) * kD + 8 * c16;
-                if (gate) {
-                    float gv[8];
-                    unpack8(*reinterpret_cast<const uint4*>(gate + at), gv);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] *= 1.0f / (1.0f + __expf(-gv[e]));
-                }
-                *reinterpret_cast<uint4*>(o + at) = pack8(f);
-            }
-        }
-        if (*sAbort) break;
+    };
+
+    if (tid == 0) {
+        for (int i = 0; i < 7; ++i) mbar_init(barB + i, 1);
+        fence_mbar_init();
+        *sAbort = 0;
+    }
+    if (warp == 0) tmem_alloc(sTmem, kTmemCols);
+    __syncthreads();  // barriers initialised before the first copy lands on them
+    if (lo < hi) {
+        load_b1(lo, 0);
+        if (lo + 1 < hi) load_b1(lo + 1, 1);
+        load_u(lo);
+        load_aqk(lo);
     }
 
-    cp_async_wait_all();
-    if (*sAbort) {  // a chunk issued its successor's loads and then stopped: let them land (bounded)
-        mbar_wait(barL, phaseL, kWaitLimit);
-        mbar_wait(barV, phaseV, kWaitLimit);
+    // state: row `row`, key channels [32 qq, 32 qq + 32) in registers; bf16 copy as the S0 operand
+    float s[32];
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+        float4 x = s_in ? *reinterpret_cast<const float4*>(s_in + in_off + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        s[j] = x.x; s[j + 1] = x.y; s[j + 2] = x.z; s[j + 3] = x.w;
     }
-    if (final_state && !*sAbort) {
+    auto write_state_operand = [&]() {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = s[8 * c + e];
+            *reinterpret_cast<uint4*>(sm + S_S + (qq >> 1) * 16384 + sw128(row, 4 * (qq & 1) + c)) = pack8(f);
+        }
+        fence_proxy_async();  // the products read it through the async proxy
+    };
+    write_state_operand();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *sTmem;
+    uint32_t phB = 0, phU = 0, phK = 0, phM = 0, phD = 0, phO = 0;  // phB: bit b = phase of B1 buffer b
+
+    const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
+    const uint32_t id_t64 = idesc_tf32_f32(128, 64);
+    const uint32_t id_ds = idesc_bf16_f32(128, 128, false, true);
+
+    // outputs of chunk mm (its product complete, in TMEM columns 128 p + 64): thread (row, qq) stores
+    // tokens 16qq .. 16qq+15 of value row `row`; a warp writes 64 contiguous bytes per token
+    auto emit_o = [&](int mm, int p) {
+        const int64_t c0 = chunk_start(mm);
+        const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
+        tc_fence_after();
+        uint32_t xo[16];
+        tmem_ld16_async(tbase + lane_base + 128 * p + 64 + 16 * qq, xo);
+        tmem_wait_ld(); reg_fence(xo);
+        const int64_t stride = (int64_t)H * kD;
+        const int64_t at0 = ((c0 + 16 * qq) * H + h) * kD + row;
+        __nv_bfloat16* op = o + at0;
+        if (gate) {
+            const __nv_bfloat16* gp = gate + at0;
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                if (16 * qq + e < L) {
+                    const float gv = __bfloat162float(gp[e * stride]);
+                    op[e * stride] = __float2bfloat16_rn(scale * __uint_as_float(xo[e]) / (1.0f + __expf(-gv)));
+                }
+        } else if (L == kC) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) op[e * stride] = __float2bfloat16_rn(scale * __uint_as_float(xo[e]));
+        } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                if (16 * qq + e < L) op[e * stride] = __float2bfloat16_rn(scale * __uint_as_float(xo[e]));
+        }
+    };
+
+    int b = 0;
+    for (int mm = lo; mm < hi; ++mm, b ^= 1) {
+        // ---- (1) [Y^T | O^T] = S0 [W ; Q e^G]^T into the columns of parity b
+        if (tid == 0) {
+            solo_wait(barB + b, (phB >> b) & 1u, sAbort, err);
+            pend &= ~(1u << b);
+            tc_fence_after();
+            mma_k128(tbase + 128 * b, kdesc(sbase + S_S), 16384, kdesc(sbase + S_B1 + b * 32768), 16384, id_s);
+            mma_commit(barM);
+        }
+        phB ^= 1u << b;
+        // ---- (2) the previous chunk's outputs while these products run
+        if (mm > lo) emit_o(mm - 1, b ^ 1);
+        if (tid == 0) {
+            solo_wait(barM, phM, sAbort, err);
+            solo_wait(barU, phU, sAbort, err);
+            pend &= ~4u;
+            if (mm + 2 < hi) load_b1(mm + 2, b);
+        }
+        phM ^= 1u;
+        phU ^= 1u;
+        cta_sync_tc();
+        // ---- (3) V'^T = U^T - Y^T; thread (row, qq) owns tokens 16qq .. 16qq+15
+        {
+            uint32_t y[16];
+            tmem_ld16_async(tbase + lane_base + 128 * b + 16 * qq, y);
+            tmem_wait_ld(); reg_fence(y);
+            float x[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x[e] = sU[(16 * qq + e) * kD + row] - __uint_as_float(y[e]);
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4)  // tf32 copy for the output product
+                *reinterpret_cast<float4*>(sm + S_ZT + (qq >> 1) * 16384 + sw128(row, 4 * (qq & 1) + c4)) =
+                    make_float4(to_tf32(x[4 * c4]), to_tf32(x[4 * c4 + 1]), to_tf32(x[4 * c4 + 2]),
+                                to_tf32(x[4 * c4 + 3]));
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {  // bf16 copy for the state product
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = x[8 * c2 + e];
+                *reinterpret_cast<uint4*>(sm + S_VB + sw128(row, 2 * qq + c2)) = pack8(f);
+            }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        if (*sAbort) break;
+        // ---- (4) dS = V'^T (K e^{G_C - G}) first (the state waits for it), then O^T += V'^T A_qk^T
+        if (tid == 0) {
+            if (mm + 1 < hi) load_u(mm + 1);  // every thread has read U
+            solo_wait(barK, phK, sAbort, err);
+            pend &= ~8u;
+            tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16(tbase + TM_DS, kdesc(sbase + S_VB) + ks * 2, sdesc_sw128(sbase + S_KP, 8192, 1024) + ks * 128,
+                         id_ds, ks > 0 ? 1u : 0u);
+            mma_commit(barD);
+            const uint64_t va = kdesc(sbase + S_ZT), aq = kdesc(sbase + S_AQ);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t reg = ks >> 2, off2 = (ks & 3) * 32;
+                mma_tf32(tbase + 128 * b + 64, va + ((reg * 16384 + off2) >> 4), aq + ((reg * 8192 + off2) >> 4),
+                         id_t64, 1u);
+            }
+            mma_commit(barO);
+            solo_wait(barD, phD, sAbort, err);
+        }
+        phK ^= 1u;
+        phD ^= 1u;
+        cta_sync_tc();
+        // ---- (5) the state update
+        {
+            uint32_t d0[32];
+            tmem_ld32_async(tbase + lane_base + TM_DS + 32 * qq, d0);
+            float eg[32];
+#pragma unroll
+            for (int e4 = 0; e4 < 32; e4 += 4) *reinterpret_cast<float4*>(eg + e4) = *reinterpret_cast<const float4*>(sEGl + 32 * qq + e4);
+            tmem_wait_ld(); reg_fence(d0);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) s[e] = fmaf(s[e], eg[e], __uint_as_float(d0[e]));
+        }
+        write_state_operand();
+        if (tid == 0) solo_wait(barO, phO, sAbort, err);  // the output product is done: outputs ready, A_qk/KP free
+        phO ^= 1u;
+        tc_fence_before();
+        __syncthreads();
+        if (mm + 1 < hi) load_aqk(mm + 1);
+        if (*sAbort) break;
+    }
+    if (lo < hi && !*sAbort) emit_o(hi - 1, (hi - 1 - lo) & 1);
+
+    if (*sAbort && tid == 0) {  // let copies still in flight land (bounded) before the CTA exits
+        if (pend & 1u) mbar_wait(barB, phB & 1u, kWaitLimit);
+        if (pend & 2u) mbar_wait(barB + 1, (phB >> 1) & 1u, kWaitLimit);
+        if (pend & 4u) mbar_wait(barU, phU, kWaitLimit);
+        if (pend & 8u) mbar_wait(barK, phK, kWaitLimit);
+    }
+    __syncthreads();
+    if (s_out && !*sAbort) {
 #pragma unroll
         for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<float4*>(final_state + state_off + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
+            *reinterpret_cast<float4*>(s_out + out_off + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
     }
     tc_fence_before();
     __syncthreads();
@@ -683,36 +941,81 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// [T, H, 128] tensor of `elem` bytes per value, boxes of [64 tokens][1 head][128 channels], no swizzle.
-bool encode_chunk_map(CUtensorMap* m, const void* base, CUtensorMapDataType type, int elem, int64_t T, int H) {
+// [T, H, 128] tensor of `elem` bytes per value, boxes of [64 tokens][1 head][inner channels], with the
+// 128-byte swizzle (inner * elem = 128 bytes, the operand-tile layout).
+bool encode_chunk_map(CUtensorMap* m, const void* base, CUtensorMapDataType type, int elem, int inner, int64_t T,
+                      int H) {
     auto fn = tensor_map_encoder();
     if (!fn) return false;
     const cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
     const cuuint64_t strides[2] = {(cuuint64_t)128 * elem, (cuuint64_t)H * 128 * elem};
-    const cuuint32_t box[3] = {128, 1, 64};
+    const cuuint32_t box[3] = {(cuuint32_t)inner, 1, 64};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, type, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
 
+// Workspace: [carried states, 2 x H x 128 x 128 fp32][chunk offsets, int32 N + 1][operands of
+// `rows` chunk rows x H heads, kBlobBytes each].
+static size_t ws_header_bytes(int N, int H) {
+    return (size_t)2 * H * kStateBytes + (((size_t)(N + 1) * 4 + 1023) / 1024) * 1024;
+}
+
+// Upper bound of the number of chunks over all sequences (exact for one sequence without offsets).
+static int64_t max_chunk_rows(int N, int64_t T_total, bool have_cu) {
+    return have_cu ? T_total / kC + N : (T_total + kC - 1) / kC;
+}
+
+void chunk_tc_workspace(int N, int64_t T_total, int H, bool have_cu, size_t* full_bytes, size_t* min_bytes) {
+    const size_t row = (size_t)H * kBlobBytes, hdr = ws_header_bytes(N, H);
+    const int64_t rows = max_chunk_rows(N, T_total, have_cu);
+    if (full_bytes) *full_bytes = hdr + row * (size_t)(rows > 0 ? rows : 1);
+    if (min_bytes) *min_bytes = hdr + row;
+}
+
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
                             const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
-                            float scale, const void* out_gate, void* o, float* final_state, unsigned int* err,
-                            cudaStream_t stream) {
+                            float scale, const void* out_gate, void* o, float* final_state, void* workspace,
+                            size_t workspace_bytes, unsigned int* err, cudaStream_t stream) {
     CUtensorMap tq, tk, tv, tg;
-    if (!encode_chunk_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T_total, H) ||
-        !encode_chunk_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T_total, H) ||
-        !encode_chunk_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T_total, H) ||
-        !encode_chunk_map(&tg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, T_total, H))
+    if (!encode_chunk_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, T_total, H) ||
+        !encode_chunk_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, T_total, H) ||
+        !encode_chunk_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, T_total, H) ||
+        !encode_chunk_map(&tg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32, T_total, H))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* carry = reinterpret_cast<float*>(ws);
+    int32_t* off = reinterpret_cast<int32_t*>(ws + (size_t)2 * H * kStateBytes);
+    uint8_t* blobs = ws + ws_header_bytes(N, H);
+    const int64_t rows_max = max_chunk_rows(N, T_total, cu_seqlens != nullptr);
+    int64_t rows = (int64_t)((workspace_bytes - ws_header_bytes(N, H)) / ((size_t)H * kBlobBytes));
+    if (rows < 1) return cudaErrorInvalidValue;
+    if (rows > rows_max) rows = rows_max > 0 ? rows_max : 1;
+    if (rows * H > 0x7FFFFFFF) rows = 0x7FFFFFFF / H;  // grid size of the prep kernel
+
+    cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStateSmem);
     if (e != cudaSuccess) return e;
-    chunk_tc_kernel<<<(unsigned)((int64_t)N * H), kThreads, kSmemBytes, stream>>>(
-        tq, tk, tv, tg, beta, init_state, cu_seqlens, T_total, H, scale, static_cast<const __nv_bfloat16*>(out_gate),
-        static_cast<__nv_bfloat16*>(o), final_state, err);
+    chunk_offsets_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, T_total, off);
+    int range = 0;
+    for (int64_t r0 = 0; range == 0 || r0 < rows_max; r0 += rows, ++range) {
+        const int64_t r1 = r0 + rows < rows_max ? r0 + rows : rows_max;
+        if (r1 > r0)
+            chunk_prep_kernel<<<(unsigned)((r1 - r0) * H), kPrepThreads, kPrepSmem, stream>>>(
+                tq, tk, tv, tg, beta, cu_seqlens, off, N, T_total, H, (int)r0, blobs, err);
+        float* c_out = carry + (size_t)(range & 1) * H * kD * kD;
+        const float* c_in = carry + (size_t)((range + 1) & 1) * H * kD * kD;
+        chunk_state_kernel<<<(unsigned)((int64_t)N * H), kThreads, kStateSmem, stream>>>(
+            init_state, cu_seqlens, off, T_total, H, scale, static_cast<const __nv_bfloat16*>(out_gate),
+            static_cast<__nv_bfloat16*>(o), final_state, c_in, c_out, range == 0 ? 1 : 0, (int)r0, (int)r1, blobs,
+            err);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     return cudaGetLastError();
 }
 

@@ -89,8 +89,11 @@ cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, const
 
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
                             const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
-                            float scale, const void* out_gate, void* o, float* final_state, unsigned int* err,
-                            cudaStream_t stream);
+                            float scale, const void* out_gate, void* o, float* final_state, void* workspace,
+                            size_t workspace_bytes, unsigned int* err, cudaStream_t stream);
+
+// Workspace of launch_chunk_tc: all chunks in one range / the least accepted.
+void chunk_tc_workspace(int N, int64_t T_total, int H, bool have_cu, size_t* full_bytes, size_t* min_bytes);
 
 // Device address of the library's error word on the current device (nullptr if unavailable).
 unsigned int* device_error_word();

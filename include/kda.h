@@ -20,9 +20,10 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *  - Every tensor pointer is CALLER-OWNED DEVICE memory on the current CUDA
- *    device.  The library allocates nothing, frees nothing and keeps no state
- *    between calls (apart from one device error word, see kda_device_error).
+ *  - Every tensor pointer (and the prefill's workspace) is CALLER-OWNED DEVICE
+ *    memory on the current CUDA device.  The library allocates nothing, frees
+ *    nothing and keeps no state between calls (apart from one device error
+ *    word, see kda_device_error).
  *  - Calls are asynchronous: they check their arguments on the host, enqueue
  *    kernels on `stream` (a cudaStream_t; NULL = legacy default stream) and
  *    return.  An argument error returns before anything is enqueued.  A launch
@@ -121,11 +122,32 @@ KDA_API kda_status kda_shortconv_l2norm(const void* xq, const void* xk, const vo
  *  o               [T_total, H, dv], storage `dtype`
  *  final_state     fp32 [N, H, dv, dk] or NULL.  May be the same buffer as
  *                  init_state (each sequence's state is read before it is written).
+ *  workspace       device scratch of workspace_bytes bytes, 16-byte aligned, used
+ *                  only during the call (stream-ordered).  KDA_DTYPE_BF16 needs at
+ *                  least the `min_bytes` of kda_chunk_fwd_workspace_size and runs
+ *                  fastest with `full_bytes`; with less, the chunks are processed in
+ *                  several ranges.  KDA_DTYPE_F32 ignores it (may be NULL, 0).
+ *
+ * The bf16 path runs two kernels per range of chunks: the first computes, for every
+ * (chunk, head) at once, everything that does not depend on the carried state (the
+ * in-chunk decays, the A_kk / A_qk blocks, T = (I + A_kk)^-1, W = T diag(beta) K e^G and
+ * U = T diag(beta) V) and stores the chunk's operands in the workspace (98,816 bytes per
+ * chunk and head); the second walks each sequence's chunks in order with the state.
  */
 KDA_API kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                          const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
                          int dk, int dv, float scale, int chunk_size, kda_dtype dtype, const void* out_gate,
-                         void* o, float* final_state, void* stream);
+                         void* o, float* final_state, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace of kda_chunk_fwd for these sizes (no device access): *full_bytes runs every
+ * chunk in one range, *min_bytes is the least accepted (one chunk row of all heads).
+ * Both are 0 for KDA_DTYPE_F32.  have_cu_seqlens: whether cu_seqlens will be given.
+ * Either output pointer may be NULL.
+ */
+KDA_API kda_status kda_chunk_fwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv, int chunk_size,
+                                        kda_dtype dtype, int have_cu_seqlens, size_t* full_bytes,
+                                        size_t* min_bytes);
 
 /*
  * One decode step (the fused_recurrent_kda operator of "Kimi K3 架构全景",

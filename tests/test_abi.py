@@ -45,11 +45,32 @@ P = ctypes.c_void_p
 
 def _chunk(lib, **over):
     a = dict(q=P(4096), k=P(4096), v=P(4096), g=P(4096), beta=P(4096), init=None, cu=None, N=1, T=64, H=2,
-             dk=128, dv=128, scale=1.0, chunk=64, dtype=1, gate=None, o=P(4096), fs=None, stream=None)
+             dk=128, dv=128, scale=1.0, chunk=64, dtype=1, gate=None, o=P(4096), fs=None, ws=P(4096),
+             wsb=1 << 30, stream=None)
     a.update(over)
     return lib.kda_chunk_fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["init"], a["cu"], a["N"], a["T"], a["H"],
                              a["dk"], a["dv"], a["scale"], a["chunk"], a["dtype"], a["gate"], a["o"], a["fs"],
-                             a["stream"])
+                             a["ws"], a["wsb"], a["stream"])
+
+
+def _ws(lib, N, T, H, dtype=1, cu=1):
+    full, least = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    rc = lib.kda_chunk_fwd_workspace_size(N, T, H, 128, 128, 64, dtype, cu, ctypes.byref(full), ctypes.byref(least))
+    return rc, full.value, least.value
+
+
+def test_workspace_size(lib):
+    # carried states 2 x H x 64 KiB, chunk offsets rounded to 1 KiB, 82,432 bytes per chunk and head
+    hdr = 2 * 96 * 65536 + 1024
+    assert _ws(lib, 1, 8192, 96, cu=0) == (0, hdr + 128 * 96 * 98816, hdr + 96 * 98816)
+    assert _ws(lib, 1, 8193, 96, cu=0) == (0, hdr + 129 * 96 * 98816, hdr + 96 * 98816)
+    # with cu_seqlens the chunk count is bounded by T / 64 + N
+    assert _ws(lib, 32, 520949, 96)[1] == hdr + (520949 // 64 + 32) * 96 * 98816
+    assert _ws(lib, 300, 1000, 4)[2] == 2 * 4 * 65536 + 2048 + 4 * 98816
+    assert _ws(lib, 1, 0, 96, cu=0)[1] == hdr + 96 * 98816
+    assert _ws(lib, 1, 256, 4, dtype=0) == (0, 0, 0)      # the fp32 path needs none
+    assert _ws(lib, 2, 256, 4, cu=0)[0] == 1               # several sequences need cu_seqlens
+    assert _ws(lib, 1, 256, 4, cu=0)[0] == 0
 
 
 def test_chunk_fwd_rejects_bad_arguments(lib):
@@ -64,6 +85,11 @@ def test_chunk_fwd_rejects_bad_arguments(lib):
     assert _chunk(lib, dtype=7) == INVALID
     assert _chunk(lib, scale=float("nan")) == INVALID
     assert b"must" in lib.kda_last_error()
+    least = _ws(lib, 1, 64, 2, cu=0)[2]
+    assert _chunk(lib, ws=None) == INVALID                   # the bf16 path needs a workspace
+    assert _chunk(lib, wsb=least - 1) == INVALID
+    assert _chunk(lib, ws=P(4104), wsb=least) == INVALID     # misaligned workspace
+    assert _chunk(lib, T=1 << 31) == INVALID                 # tensor-map coordinates are 32-bit
 
 
 def test_shortconv_rejects_bad_arguments(lib):

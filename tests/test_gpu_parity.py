@@ -156,6 +156,28 @@ def test_chunk_packed_equals_separate(kda):
         assert torch.equal(o1, o[sl]) and torch.equal(f1[0], fs[n])
 
 
+@pytest.mark.parametrize("rows", [1, 3])
+def test_chunk_workspace_ranges(kda, orc, rows):
+    """A workspace of `rows` chunk rows runs the chunks in ranges; chains that cross a range carry
+    their fp32 state through the workspace.  The result is bit-identical to one range and matches
+    the oracle."""
+    lengths = [130, 1, 0, 257, 64, 5, 0, 70]
+    w, q, k, v, g, b, s0 = small_prefill(107, lengths, 3, "bf16", init_std=0.02)
+    args = [dev(x) for x in (q, k, v, g, b, s0)] + [dev(w.cu_seqlens())]
+    o_full, f_full = kda.kda_chunk_fwd(*args)
+    full, least = kda.kda_chunk_fwd_workspace_size(w.N, w.T, w.H)
+    per_row = (full - least) // (w.T // 64 + w.N - 1)
+    ws = torch.empty(least + (rows - 1) * per_row, dtype=torch.uint8, device="cuda")
+    o_r, f_r = kda.kda_chunk_fwd(*args, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o_r, o_full) and torch.equal(f_r, f_full)
+    o_ref, fs_ref = oracle_chunk(orc, w, q, k, v, g, b, s0)
+    assert orc.rel_l2(host(o_r), o_ref) <= BF16_O_REL and orc.max_abs(host(o_r), o_ref) <= BF16_O_ABS
+    assert orc.rel_l2(host(f_r), fs_ref) <= BF16_S_REL
+    assert torch.equal(f_r[2], dev(s0)[2]) and torch.equal(f_r[6], dev(s0)[6])
+    assert kda.device_error() == 0
+
+
 # ------------------------------------------------------------------------------------------
 # kda_shortconv_l2norm
 # ------------------------------------------------------------------------------------------
