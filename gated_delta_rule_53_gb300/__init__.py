@@ -20,7 +20,8 @@ import os
 
 import torch
 
-__all__ = ["kda_shortconv_l2norm", "kda_chunk_fwd", "kda_chunk_fwd_workspace_size", "kda_recurrent_step", "library",
+__all__ = ["kda_shortconv_l2norm", "kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_chunk_fwd_workspace_size",
+           "kda_recurrent_step", "library",
            "KDAError", "device_error", "LIB_PATH"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkda.so")
@@ -43,11 +44,12 @@ def library() -> ctypes.CDLL:
         lib.kda_shortconv_l2norm.argtypes = [P, P, P, I64, P, P, I32, I64, I32, I32, P, P, F, I32, P, P, P, P]
         SZ = ctypes.c_size_t
         lib.kda_chunk_fwd.argtypes = [P, P, P, P, P, P, P, I32, I64, I32, I32, I32, F, I32, I32, P, P, P, P, SZ, P]
+        lib.kda_chunk_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, I32, I64, I32, I32, I32, F, I32, I32, P, P, P, P]
         lib.kda_chunk_fwd_workspace_size.argtypes = [I32, I64, I32, I32, I32, I32, I32, I32, ctypes.POINTER(SZ),
                                                      ctypes.POINTER(SZ)]
         lib.kda_recurrent_step.argtypes = [P, P, P, I64, P, P, P, P, P, I32, I32, I32, I32, F, F, P, P]
         for f in (lib.kda_shortconv_l2norm, lib.kda_chunk_fwd, lib.kda_recurrent_step, lib.kda_device_error,
-                  lib.kda_chunk_fwd_workspace_size):
+                  lib.kda_chunk_fwd_workspace_size, lib.kda_chunk_fwd_noalloc):
             f.restype = ctypes.c_int
         lib.kda_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         lib.kda_selftest_bounded_wait.argtypes = [ctypes.c_uint, ctypes.c_void_p]
@@ -180,6 +182,36 @@ def kda_chunk_fwd(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale: flo
                                  N, T, H, dk, dv, float(scale), int(chunk_size), dt, _ptr(out_gate), _ptr(o),
                                  _ptr(final_state), _ptr(workspace), ws_bytes, _stream(stream))
     _check(rc, "kda_chunk_fwd")
+    return o, final_state
+
+
+def kda_chunk_fwd_noalloc(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale: float = 1.0,
+                          chunk_size: int = 64, out_gate=None, o=None, final_state=None,
+                          output_final_state: bool = True, stream=None):
+    """kda_chunk_fwd on the library's static 64 MiB scratch instead of a workspace (no allocation
+    for it); raises KDAError when the sizes need more than that.  Calls must not overlap."""
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    dtype = q.dtype
+    if dtype not in (torch.bfloat16, torch.float32):
+        raise KDAError("q, k, v must be bf16 or fp32")
+    _dev(q, "q", dtype); _dev(k, "k", dtype, (T, H, dk)); _dev(v, "v", dtype, (T, H, dv))
+    _dev(g, "g", torch.float32, (T, H, dk)); _dev(beta, "beta", torch.float32, (T, H))
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    _dev(cu_seqlens, "cu_seqlens", torch.int32)
+    _dev(init_state, "init_state", torch.float32, (N, H, dv, dk))
+    _dev(out_gate, "out_gate", torch.bfloat16, (T, H * dv))
+    if o is None:
+        o = torch.empty((T, H, dv), dtype=dtype, device=q.device)
+    _dev(o, "o", dtype, (T, H, dv))
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, dv, dk), dtype=torch.float32, device=q.device)
+    _dev(final_state, "final_state", torch.float32, (N, H, dv, dk))
+    dt = KDA_DTYPE_BF16 if dtype == torch.bfloat16 else KDA_DTYPE_F32
+    rc = library().kda_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state),
+                                         _ptr(cu_seqlens), N, T, H, dk, dv, float(scale), int(chunk_size), dt,
+                                         _ptr(out_gate), _ptr(o), _ptr(final_state), _stream(stream))
+    _check(rc, "kda_chunk_fwd_noalloc")
     return o, final_state
 
 

@@ -49,6 +49,15 @@ using kda::set_error;
 
 namespace {
 
+// Scratch of kda_chunk_fwd_noalloc: part of the library's device image, so that entry point needs
+// no allocation by anyone.  Calls that use it must not overlap (one stream, or ordered streams).
+constexpr size_t kStaticScratchBytes = size_t(64) << 20;
+static __device__ __align__(256) uint8_t g_chunk_scratch[kStaticScratchBytes];
+
+}  // namespace
+
+namespace {
+
 // One thread waits on a barrier no one arrives at; the bounded wait gives up and reports.
 __global__ void selftest_wait_kernel(unsigned int limit, unsigned int* err) {
     __shared__ uint64_t bar;
@@ -190,6 +199,30 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const floa
                                           final_state, workspace, workspace_bytes, err,
                                           static_cast<cudaStream_t>(stream)),
                      "kda_chunk_fwd launch");
+}
+
+kda_status kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                 const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
+                                 int dk, int dv, float scale, int chunk_size, kda_dtype dtype, const void* out_gate,
+                                 void* o, float* final_state, void* stream) {
+    if (dtype == KDA_DTYPE_F32)  // the fp32 path needs no workspace
+        return kda_chunk_fwd(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, dk, dv, scale, chunk_size,
+                             dtype, out_gate, o, final_state, nullptr, 0, stream);
+    REQUIRE_PTR(q); REQUIRE_PTR(k); REQUIRE_PTR(v); REQUIRE_PTR(g); REQUIRE_PTR(beta); REQUIRE_PTR(o);
+    kda_status s = check_batch(cu_seqlens, N, T_total, H);
+    if (s != KDA_OK) return s;
+    REQUIRE(dtype == KDA_DTYPE_BF16, "bad dtype");
+    REQUIRE(T_total / 64 + N <= 0x7FFFFFFF, "too many chunks");
+    size_t need = 0;
+    kda::chunk_tc_workspace(N, T_total, H, cu_seqlens != nullptr, nullptr, &need);
+    if (need > kStaticScratchBytes)
+        return set_error(KDA_ERR_UNSUPPORTED, "the static scratch holds %zu bytes; these sizes need at least %zu",
+                         kStaticScratchBytes, need);
+    void* scratch = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&scratch, g_chunk_scratch);
+    if (e != cudaSuccess) return from_cuda(e, "kda_chunk_fwd_noalloc scratch");
+    return kda_chunk_fwd(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, dk, dv, scale, chunk_size, dtype,
+                         out_gate, o, final_state, scratch, kStaticScratchBytes, stream);
 }
 
 kda_status kda_chunk_fwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv, int chunk_size,

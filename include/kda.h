@@ -140,6 +140,21 @@ KDA_API kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, co
                          void* o, float* final_state, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * kda_chunk_fwd without a caller workspace (no counterpart in the sources; an interface
+ * convenience).  The bf16 path uses a 64 MiB scratch array that is part of the library's
+ * device image (so nothing is allocated), processing as many chunk rows per range as fit.
+ * Returns KDA_ERR_UNSUPPORTED, before enqueueing anything, when even one chunk row of all
+ * heads does not fit (the `min_bytes` of kda_chunk_fwd_workspace_size exceeds 64 MiB: H above
+ * about 290).  Calls share the scratch: they must not run concurrently on one device.
+ * Arguments and layouts as kda_chunk_fwd.
+ */
+KDA_API kda_status kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g,
+                                 const float* beta, const float* init_state, const int32_t* cu_seqlens, int N,
+                                 int64_t T_total, int H, int dk, int dv, float scale, int chunk_size,
+                                 kda_dtype dtype, const void* out_gate, void* o, float* final_state,
+                                 void* stream);
+
+/*
  * Workspace of kda_chunk_fwd for these sizes (no device access): *full_bytes runs every
  * chunk in one range, *min_bytes is the least accepted (one chunk row of all heads).
  * Both are 0 for KDA_DTYPE_F32.  have_cu_seqlens: whether cu_seqlens will be given.
