@@ -90,8 +90,6 @@ constexpr uint32_t BLOB_EGL = 98304;   // e^{G_C} fp32 [128]
 constexpr uint32_t kBlobBytes = 98816;
 constexpr uint32_t kStateBytes = kD * kD * 4;
 
-// column operand of row block I < 3: 16(I+1) rows, two regions of 16(I+1) * 128 bytes
-__host__ __device__ constexpr uint32_t cc_off(int I) { return I == 0 ? 0u : (I == 1 ? 4096u : 12288u); }
 
 __device__ __forceinline__ void unpack8(uint4 u, float (&f)[8]) {
     f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x); f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
@@ -117,73 +115,63 @@ __device__ __forceinline__ void mma_k128(uint32_t d, uint64_t a_desc, uint32_t a
 
 __device__ __forceinline__ uint64_t kdesc(uint32_t saddr) { return sdesc_sw128(saddr, 16, 1024); }
 
-// One 16 x 16 fp32 block product for 16 * 16 / CW threads; thread t owns row t / (16 / CW) and the
-// CW columns from CW (t % (16 / CW)):   out = sign * (A0 + w1 A1 + w2 A2) B  [+ A3 B3]
+// One 16 x 16 fp32 block product for 32 threads; thread t owns rows 2 (t / 4) and 2 (t / 4) + 1, columns
+// 4 (t % 4) .. +3:   out = sign * (A0 + w1 A1 + w2 A2) B  [+ A3 B3]
 // NA = number of A blocks combined on the fly (an entry of P = -N + N^2 - N^3); SECOND adds A3 B3.
 struct Blk {
     const float* p;
     int ld;
 };
-template <int NA, bool SECOND, int CW>
-__device__ __forceinline__ void blk_mma(float* out, int ldo, float sign, Blk a0, Blk a1, float w1, Blk a2, float w2,
-                                        Blk b, Blk a3, Blk b3, int t) {
-    constexpr int TPR = 16 / CW;  // threads per row
-    const int r = t / TPR, c = CW * (t % TPR);
-    float av[16];
+template <int NA>
+__device__ __forceinline__ void load_rows(float (&av)[2][16], Blk a0, Blk a1, float w1, Blk a2, float w2, int r0) {
 #pragma unroll
-    for (int m = 0; m < 16; m += 4) {
-        float4 x = *reinterpret_cast<const float4*>(a0.p + r * a0.ld + m);
-        if (NA > 1) {
-            const float4 y = *reinterpret_cast<const float4*>(a1.p + r * a1.ld + m);
-            x.x = fmaf(w1, y.x, x.x); x.y = fmaf(w1, y.y, x.y); x.z = fmaf(w1, y.z, x.z); x.w = fmaf(w1, y.w, x.w);
-        }
-        if (NA > 2) {
-            const float4 y = *reinterpret_cast<const float4*>(a2.p + r * a2.ld + m);
-            x.x = fmaf(w2, y.x, x.x); x.y = fmaf(w2, y.y, x.y); x.z = fmaf(w2, y.z, x.z); x.w = fmaf(w2, y.w, x.w);
-        }
-        av[m] = x.x; av[m + 1] = x.y; av[m + 2] = x.z; av[m + 3] = x.w;
-    }
-    float acc[CW], acc2[CW];
-#pragma unroll
-    for (int e = 0; e < CW; ++e) acc[e] = acc2[e] = 0.f;
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-#pragma unroll
-        for (int e4 = 0; e4 < CW; e4 += 4) {
-            const float4 bv = *reinterpret_cast<const float4*>(b.p + m * b.ld + c + e4);
-            float* ac = (m & 1) ? acc2 : acc;
-            ac[e4] = fmaf(av[m], bv.x, ac[e4]); ac[e4 + 1] = fmaf(av[m], bv.y, ac[e4 + 1]);
-            ac[e4 + 2] = fmaf(av[m], bv.z, ac[e4 + 2]); ac[e4 + 3] = fmaf(av[m], bv.w, ac[e4 + 3]);
-        }
-    }
-    if (SECOND) {
+    for (int rr = 0; rr < 2; ++rr)
 #pragma unroll
         for (int m = 0; m < 16; m += 4) {
-            const float4 x = *reinterpret_cast<const float4*>(a3.p + r * a3.ld + m);
-            av[m] = x.x; av[m + 1] = x.y; av[m + 2] = x.z; av[m + 3] = x.w;
-        }
-#pragma unroll
-        for (int m = 0; m < 16; ++m) {
-#pragma unroll
-            for (int e4 = 0; e4 < CW; e4 += 4) {
-                const float4 bv = *reinterpret_cast<const float4*>(b3.p + m * b3.ld + c + e4);
-                float* ac = (m & 1) ? acc2 : acc;
-                ac[e4] = fmaf(av[m], bv.x, ac[e4]); ac[e4 + 1] = fmaf(av[m], bv.y, ac[e4 + 1]);
-                ac[e4 + 2] = fmaf(av[m], bv.z, ac[e4 + 2]); ac[e4 + 3] = fmaf(av[m], bv.w, ac[e4 + 3]);
+            float4 x = *reinterpret_cast<const float4*>(a0.p + (r0 + rr) * a0.ld + m);
+            if (NA > 1) {
+                const float4 y = *reinterpret_cast<const float4*>(a1.p + (r0 + rr) * a1.ld + m);
+                x.x = fmaf(w1, y.x, x.x); x.y = fmaf(w1, y.y, x.y); x.z = fmaf(w1, y.z, x.z); x.w = fmaf(w1, y.w, x.w);
             }
+            if (NA > 2) {
+                const float4 y = *reinterpret_cast<const float4*>(a2.p + (r0 + rr) * a2.ld + m);
+                x.x = fmaf(w2, y.x, x.x); x.y = fmaf(w2, y.y, x.y); x.z = fmaf(w2, y.z, x.z); x.w = fmaf(w2, y.w, x.w);
+            }
+            av[rr][m] = x.x; av[rr][m + 1] = x.y; av[rr][m + 2] = x.z; av[rr][m + 3] = x.w;
+        }
+}
+__device__ __forceinline__ void acc_rows(float (&acc)[2][4], const float (&av)[2][16], Blk b, int c) {
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        const float4 bv = *reinterpret_cast<const float4*>(b.p + m * b.ld + c);
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            acc[rr][0] = fmaf(av[rr][m], bv.x, acc[rr][0]); acc[rr][1] = fmaf(av[rr][m], bv.y, acc[rr][1]);
+            acc[rr][2] = fmaf(av[rr][m], bv.z, acc[rr][2]); acc[rr][3] = fmaf(av[rr][m], bv.w, acc[rr][3]);
         }
     }
+}
+template <int NA, bool SECOND>
+__device__ __forceinline__ void blk_mma(float* out, int ldo, float sign, Blk a0, Blk a1, float w1, Blk a2, float w2,
+                                        Blk b, Blk a3, Blk b3, int t) {
+    const int r0 = 2 * (t >> 2), c = 4 * (t & 3);
+    float av[2][16], acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    load_rows<NA>(av, a0, a1, w1, a2, w2, r0);
+    acc_rows(acc, av, b, c);
+    if (SECOND) {
+        load_rows<1>(av, a3, a3, 0.f, a3, 0.f, r0);
+        acc_rows(acc, av, b3, c);
+    }
 #pragma unroll
-    for (int e4 = 0; e4 < CW; e4 += 4)
-        *reinterpret_cast<float4*>(out + r * ldo + c + e4) =
-            make_float4(sign * (acc[e4] + acc2[e4]), sign * (acc[e4 + 1] + acc2[e4 + 1]),
-                        sign * (acc[e4 + 2] + acc2[e4 + 2]), sign * (acc[e4 + 3] + acc2[e4 + 3]));
+    for (int rr = 0; rr < 2; ++rr)
+        *reinterpret_cast<float4*>(out + (r0 + rr) * ldo + c) =
+            make_float4(sign * acc[rr][0], sign * acc[rr][1], sign * acc[rr][2], sign * acc[rr][3]);
 }
 
 // Blocks of T below the diagonal.  With D = diag(T_00 .. T_33) (inverses of the diagonal blocks of
 // I + A_kk) and N = D A_off (A_off: the blocks of A_kk below the diagonal; N is strictly block-lower,
 // so N^4 = 0):  (I + A_kk)^-1 = (I + N)^-1 D = (I - N + N^2 - N^3) D.
-// Three rounds of independent 16 x 16 products on the first 192 threads (32 or 64 per product).
+// Three rounds of independent 16 x 16 products, 32 threads each.
 constexpr int kNB = 20;  // row stride of the N blocks (float4 rows, eight rows on distinct banks)
 __device__ __forceinline__ void t_offdiag(const float* A, float* T, float* nb, int tid) {
     auto Ablk = [&](int I, int J) { return Blk{A + 16 * I * kAS + 16 * J, kAS}; };
@@ -194,25 +182,24 @@ __device__ __forceinline__ void t_offdiag(const float* A, float* T, float* nb, i
     const int u = tid >> 5, t = tid & 31;
     if (u < 6) {  // N blocks: (1,0) (2,0) (3,0) (2,1) (3,1) (3,2)
         const int I = u < 3 ? u + 1 : (u < 5 ? u - 1 : 3), J = u < 3 ? 0 : (u < 5 ? 1 : 2);
-        blk_mma<1, false, 8>(nb + u * 16 * kNB, kNB, 1.f, Tblk(I, I), none, 0.f, none, 0.f, Ablk(I, J), none, none, t);
+        blk_mma<1, false>(nb + u * 16 * kNB, kNB, 1.f, Tblk(I, I), none, 0.f, none, 0.f, Ablk(I, J), none, none, t);
     }
     __syncthreads();
     switch (u) {
-        case 0: blk_mma<1, false, 8>(nb + 6 * 16 * kNB, kNB, 1.f, Nb(3), none, 0.f, none, 0.f, Nb(0), none, none, t); break;  // N21 N10
-        case 1: blk_mma<1, false, 8>(nb + 7 * 16 * kNB, kNB, 1.f, Nb(5), none, 0.f, none, 0.f, Nb(3), none, none, t); break;  // N32 N21
-        case 2: blk_mma<1, true, 8>(nb + 8 * 16 * kNB, kNB, 1.f, Nb(4), none, 0.f, none, 0.f, Nb(0), Nb(5), Nb(1), t); break; // N31 N10 + N32 N20
-        case 3: blk_mma<1, false, 8>(T + 16 * kAS * 1 + 0, kAS, -1.f, Nb(0), none, 0.f, none, 0.f, Tblk(0, 0), none, none, t); break;   // T10
-        case 4: blk_mma<1, false, 8>(T + 16 * kAS * 2 + 16, kAS, -1.f, Nb(3), none, 0.f, none, 0.f, Tblk(1, 1), none, none, t); break;  // T21
-        case 5: blk_mma<1, false, 8>(T + 16 * kAS * 3 + 32, kAS, -1.f, Nb(5), none, 0.f, none, 0.f, Tblk(2, 2), none, none, t); break;  // T32
+        case 0: blk_mma<1, false>(nb + 6 * 16 * kNB, kNB, 1.f, Nb(3), none, 0.f, none, 0.f, Nb(0), none, none, t); break;  // N21 N10
+        case 1: blk_mma<1, false>(nb + 7 * 16 * kNB, kNB, 1.f, Nb(5), none, 0.f, none, 0.f, Nb(3), none, none, t); break;  // N32 N21
+        case 2: blk_mma<1, true>(nb + 8 * 16 * kNB, kNB, 1.f, Nb(4), none, 0.f, none, 0.f, Nb(0), Nb(5), Nb(1), t); break; // N31 N10 + N32 N20
+        case 3: blk_mma<1, false>(T + 16 * kAS * 1 + 0, kAS, -1.f, Nb(0), none, 0.f, none, 0.f, Tblk(0, 0), none, none, t); break;   // T10
+        case 4: blk_mma<1, false>(T + 16 * kAS * 2 + 16, kAS, -1.f, Nb(3), none, 0.f, none, 0.f, Tblk(1, 1), none, none, t); break;  // T21
+        case 5: blk_mma<1, false>(T + 16 * kAS * 3 + 32, kAS, -1.f, Nb(5), none, 0.f, none, 0.f, Tblk(2, 2), none, none, t); break;  // T32
         default: break;
     }
     __syncthreads();
     // T_30 = (N^2_30 - N_30 - N^3_30) D_0 with N^3_30 D_0 = N^2_31 N_10 D_0 = -N^2_31 T_10
-    const int u3 = tid >> 6, t3 = tid & 63;
-    switch (u3) {
-        case 0: blk_mma<2, true, 4>(T + 16 * kAS * 3 + 0, kAS, 1.f, Nb(8), Nb(2), -1.f, none, 0.f, Tblk(0, 0), Nb(7), Tblk(1, 0), t3); break;
-        case 1: blk_mma<2, false, 4>(T + 16 * kAS * 2 + 0, kAS, 1.f, Nb(6), Nb(1), -1.f, none, 0.f, Tblk(0, 0), none, none, t3); break;  // T20
-        case 2: blk_mma<2, false, 4>(T + 16 * kAS * 3 + 16, kAS, 1.f, Nb(7), Nb(4), -1.f, none, 0.f, Tblk(1, 1), none, none, t3); break; // T31
+    switch (u) {
+        case 0: blk_mma<2, true>(T + 16 * kAS * 3 + 0, kAS, 1.f, Nb(8), Nb(2), -1.f, none, 0.f, Tblk(0, 0), Nb(7), Tblk(1, 0), t); break;
+        case 1: blk_mma<2, false>(T + 16 * kAS * 2 + 0, kAS, 1.f, Nb(6), Nb(1), -1.f, none, 0.f, Tblk(0, 0), none, none, t); break;  // T20
+        case 2: blk_mma<2, false>(T + 16 * kAS * 3 + 16, kAS, 1.f, Nb(7), Nb(4), -1.f, none, 0.f, Tblk(1, 1), none, none, t); break; // T31
         default: break;
     }
     __syncthreads();
@@ -279,65 +266,101 @@ __global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* __re
 }
 
 // =============================================================================================
-// chunk_prep_kernel: the S0-independent part of one (chunk, head)
+// chunk_prep_kernel: the S0-independent part of every (chunk, head); persistent, two CTAs per SM,
+// each taking items blockIdx.x, blockIdx.x + gridDim.x, ...; the next item's inputs are loaded while
+// the current one's W and U are stored.
 // =============================================================================================
 constexpr int kPrepThreads = 256;
 constexpr uint32_t P_RR = 0;          // k (rows 0-63) and q (rows 64-127) land here by TMA in the layout of the row
                                       // operand, two regions of 16 KB, and are scaled in place
-constexpr uint32_t P_KP = 32768;      // K e^{G_C - G} (two regions of [64][64])
-constexpr uint32_t P_G = 49152;       // g fp32, four TMA boxes of [64][32]
-constexpr uint32_t P_KG = 49152;      // then: K e^G (two regions of [64][64]), B (MN-major) of the W products
-constexpr uint32_t P_V = 65536;       // then: V by TMA (two regions of [64][64]), B (MN-major) of the U products
-constexpr uint32_t P_CC = 81920;      // column operands of row blocks 0..2 (24 KB)
-constexpr uint32_t P_BETA = P_CC + 24576;  // fp32 [64]
-constexpr uint32_t P_BAR = P_BETA + 256;   // mbarriers: k/q/g, v, A products, W/U products
+constexpr uint32_t P_G = 32768;       // g fp32, four TMA boxes of [64][32]; the running sum G in place
+constexpr uint32_t P_KG = 32768;      // then: K e^G (two regions of [64][64]), B (MN-major) of the W products
+constexpr uint32_t P_V = 49152;       // then: V by TMA (two regions of [64][64]), B (MN-major) of the U products
+constexpr uint32_t P_CT = 65536;      // column operands of the four row blocks stacked: 160 rows (block J from
+                                      // row 16 J (J+1) / 2), two regions of 160 x 128 bytes; block 3 is K e^{G_C - G}
+constexpr uint32_t kCTRegion = 160 * 128;
+constexpr uint32_t P_BETA = P_CT + 2 * kCTRegion;  // fp32 [64]
+constexpr uint32_t P_E = P_BETA + 256;     // fp32 [4][128]: G at the last token of each 16-token block
+constexpr uint32_t P_TOT = P_E + 2048;     // fp32 [128]: sum of the first 32 tokens
+constexpr uint32_t P_BAR = P_TOT + 512;    // mbarriers: k/q/g, v, A products, W/U products
 constexpr uint32_t P_MISC = P_BAR + 32;    // TMEM base, abort flag
 constexpr uint32_t kPrepSmem = P_MISC + 16 + 1024;
 // After the A products complete (row and column operands free):
 constexpr uint32_t P_AKK = 0;                    // A_kk fp32 [64][kAS]
-constexpr uint32_t P_TF = 17408;                 // T fp32 [64][kAS]
-constexpr uint32_t P_NB = 34816;                 // N blocks of the solve, 9 x [16][20] fp32
+constexpr uint32_t P_TF = P_CT;                  // T fp32 [64][kAS]
+constexpr uint32_t P_NB = P_CT + 64 * kAS * 4;   // N blocks of the solve, 9 x [16][20] fp32
 // Once T is in registers: T Diag(beta) as bf16 hi and lo, A operands of 128 rows (the first 64 used)
 constexpr uint32_t P_TH = 0, P_TL = 16384;
 constexpr uint32_t kPrepTmemCols = 256;
-constexpr uint32_t TM_A0 = 0, TM_A1 = 32, TM_A2 = 64, TM_A3 = 128;  // row blocks of A: 16, 32, 48, 64 columns
+// row block I of A: 16 (I + 1) columns from 16 I (I + 1) / 2 (one product of N = 160)
 constexpr uint32_t TM_W = 0, TM_U = 128;                            // then W and U (rows in lanes 0-63)
 constexpr uint32_t kKQGBytes = 4 * 8192 + 4 * 8192;
 
-static_assert(P_NB + 9 * 16 * kNB * 4 <= P_G, "solve work overflows its region");
-static_assert(P_CC + cc_off(2) + 2 * 48 * 128 <= P_BETA, "column operands overflow");
+static_assert(P_AKK + 64 * kAS * 4 <= P_G && P_NB + 9 * 16 * kNB * 4 <= P_BETA, "solve work overflows its region");
 static_assert(2 * (kPrepSmem + 1024) <= 233472, "two prep CTAs per SM");
+
+// Byte offset of g / G element (token i, channel c) in the four 128-byte-swizzled boxes of 32 channels.
+__device__ __forceinline__ uint32_t g_off(int i, int c) {
+    return (uint32_t)(c >> 5) * 8192u + sw128((uint32_t)i, (uint32_t)((c & 31) >> 2)) + (uint32_t)(c & 3) * 4u;
+}
 
 __global__ void __launch_bounds__(kPrepThreads, 2)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                   const float* __restrict__ beta, const int32_t* __restrict__ cu, const int32_t* __restrict__ off,
-                  int N, int64_t T_total, int H, int m0, uint8_t* __restrict__ blobs, unsigned int* err) {
+                  int N, int64_t T_total, int H, int m0, int n_items, uint8_t* __restrict__ blobs,
+                  unsigned int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x % H;
-    const int m = m0 + blockIdx.x / H;
-    if (m >= off[N]) return;  // past the last chunk (the grid covers an upper bound of the chunk count)
-    int lo = 0, hi = N;       // off[lo] <= m < off[hi]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (off[mid] <= m) lo = mid; else hi = mid;
-    }
-    int64_t bos, eos;
-    seq_bounds(cu, lo, T_total, bos, eos);
-    const int64_t c0 = bos + (int64_t)kC * (m - off[lo]);
-    const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
-    uint8_t* blob = blobs + ((int64_t)(m - m0) * H + h) * kBlobBytes;
+    const int offN = off[N];
 
     float* sBeta = reinterpret_cast<float*>(sm + P_BETA);
+    float* sE = reinterpret_cast<float*>(sm + P_E);
+    float* sTot = reinterpret_cast<float*>(sm + P_TOT);
     uint64_t* barL = reinterpret_cast<uint64_t*>(sm + P_BAR);
     uint64_t* barV = barL + 1;
     uint64_t* barA = barL + 2;
     uint64_t* barW = barL + 3;
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + P_MISC);
     volatile int* sAbort = reinterpret_cast<volatile int*>(sm + P_MISC + 4);
+
+    // item -> (head, chunk start, chunk length); false past the last chunk
+    auto locate = [&](int item, int& h, int64_t& c0, int& L) {
+        if (item >= n_items) return false;
+        h = item % H;
+        const int m = m0 + item / H;
+        if (m >= offN) return false;
+        int lo = 0, hi = N;  // off[lo] <= m < off[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (off[mid] <= m) lo = mid; else hi = mid;
+        }
+        int64_t bos, eos;
+        seq_bounds(cu, lo, T_total, bos, eos);
+        c0 = bos + (int64_t)kC * (m - off[lo]);
+        L = (eos - c0) < kC ? (int)(eos - c0) : kC;
+        return true;
+    };
+    // k, q (into the row-operand layout), g and beta of an item
+    auto load_inputs = [&](int h, int64_t c0, int L) {
+        if (tid == 0) {
+            fence_proxy_async();
+            mbar_arrive_expect_tx(barL, kKQGBytes);
+            tma_load_3d(sm + P_RR, &tm_k, 0, h, (int)c0, barL);             // k, channels 0-63  -> region 0 rows 0-63
+            tma_load_3d(sm + P_RR + 8192, &tm_q, 0, h, (int)c0, barL);      // q, channels 0-63  -> region 0 rows 64-127
+            tma_load_3d(sm + P_RR + 16384, &tm_k, 64, h, (int)c0, barL);    // k, channels 64-127 -> region 1
+            tma_load_3d(sm + P_RR + 24576, &tm_q, 64, h, (int)c0, barL);
+#pragma unroll
+            for (int b4 = 0; b4 < 4; ++b4) tma_load_3d(sm + P_G + b4 * 8192, &tm_g, 32 * b4, h, (int)c0, barL);
+        }
+        if (tid < kC) {
+            const bool ok = tid < L;
+            cp_async4(sBeta + tid, beta + (ok ? (c0 + tid) * H + h : 0), ok ? 4u : 0u);
+        }
+        cp_async_commit();
+    };
 
     if (tid == 0) {
         mbar_init(barL, 1);
@@ -346,144 +369,132 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         mbar_init(barW, 1);
         fence_mbar_init();
         *sAbort = 0;
-        mbar_arrive_expect_tx(barL, kKQGBytes);
-        tma_load_3d(sm + P_RR, &tm_k, 0, h, (int)c0, barL);             // k, channels 0-63  -> region 0 rows 0-63
-        tma_load_3d(sm + P_RR + 8192, &tm_q, 0, h, (int)c0, barL);      // q, channels 0-63  -> region 0 rows 64-127
-        tma_load_3d(sm + P_RR + 16384, &tm_k, 64, h, (int)c0, barL);    // k, channels 64-127 -> region 1
-        tma_load_3d(sm + P_RR + 24576, &tm_q, 64, h, (int)c0, barL);
-#pragma unroll
-        for (int b4 = 0; b4 < 4; ++b4) tma_load_3d(sm + P_G + b4 * 8192, &tm_g, 32 * b4, h, (int)c0, barL);
     }
-    if (tid < kC) {
-        const bool ok = tid < L;
-        cp_async4(sBeta + tid, beta + (ok ? (c0 + tid) * H + h : 0), ok ? 4u : 0u);
-    }
-    cp_async_commit();
     if (warp == 0) tmem_alloc(sTmem, kPrepTmemCols);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+    cta_sync_tc();
     const uint32_t tbase = *sTmem;
-    uint32_t issued = 1u;  // thread 0: which barriers have work in flight (1 = loads, 2 = v, 4 = A, 8 = W/U)
-    if (tid == 0) solo_wait(barL, 0, sAbort, err);
-    cp_async_wait_all();
-    __syncthreads();
-    do {
-        if (*sAbort) break;
-        // ---- running sum of g (log2 units).  Thread (cc, r4) owns channels 8cc .. 8cc+7 of rows r4 + 16 I
-        // (I = 0..3); the 16 lanes of a half-warp hold the 16 rows of a block, summed by shuffles.
-        const int cc = 2 * warp + (lane >> 4), r4 = lane & 15, c = 8 * cc;
-        const uint32_t reg = cc >> 3, ch = cc & 7;
-        float G[4][8], E[4][8];
-#pragma unroll
-        for (int I = 0; I < 4; ++I) {
-            const int i = r4 + 16 * I;
-            const uint8_t* gp = sm + P_G + (cc >> 2) * 8192;
-            const float4 x0 = *reinterpret_cast<const float4*>(gp + sw128(i, 2 * (cc & 3)));
-            const float4 x1 = *reinterpret_cast<const float4*>(gp + sw128(i, 2 * (cc & 3) + 1));
-            const float s = i < L ? kLog2e : 0.f;
-            G[I][0] = x0.x * s; G[I][1] = x0.y * s; G[I][2] = x0.z * s; G[I][3] = x0.w * s;
-            G[I][4] = x1.x * s; G[I][5] = x1.y * s; G[I][6] = x1.z * s; G[I][7] = x1.w * s;
-        }
-#pragma unroll
-        for (int d = 1; d < 16; d <<= 1) {
-#pragma unroll
-            for (int I = 0; I < 4; ++I)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float y = __shfl_up_sync(0xFFFFFFFFu, G[I][e], d, 16);
-                    if (r4 >= d) G[I][e] += y;
-                }
-        }
-        {
-            float base[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) base[e] = 0.f;
-#pragma unroll
-            for (int I = 0; I < 4; ++I)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float tot = __shfl_sync(0xFFFFFFFFu, G[I][e], 15, 16);
-                    G[I][e] += base[e];
-                    base[e] += tot;
-                    E[I][e] = base[e];  // G at the last token of block I
-                }
-        }
-        if (r4 == 0) {
-            float4* eg = reinterpret_cast<float4*>(blob + BLOB_EGL + 4 * c);
-            eg[0] = make_float4(exp2f(E[3][0]), exp2f(E[3][1]), exp2f(E[3][2]), exp2f(E[3][3]));
-            eg[1] = make_float4(exp2f(E[3][4]), exp2f(E[3][5]), exp2f(E[3][6]), exp2f(E[3][7]));
-        }
-        float dn[3][8];  // e^{E_{J+1} - E_J}
-#pragma unroll
-        for (int J = 0; J < 3; ++J)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) dn[J][e] = ex2(E[J + 1][e] - E[J][e]);
-        __syncthreads();  // every thread holds its g: the g boxes become K e^G and V
+    uint32_t pend = 0;  // thread 0: 1 = k/q/g loads in flight, 2 = v, 4 = A products, 8 = W/U products
+
+    int item = blockIdx.x, h = 0, L = 0;
+    int64_t c0 = 0;
+    bool have = locate(item, h, c0, L);
+    if (have) {
+        load_inputs(h, c0, L);
+        if (tid == 0) pend |= 1u;
+    }
+    for (uint32_t ph = 0; have; ph ^= 1u) {
+        uint8_t* blob = blobs + (int64_t)item * kBlobBytes;
         if (tid == 0) {
-            fence_proxy_async();
-            mbar_arrive_expect_tx(barV, 16384);
-            tma_load_3d(sm + P_V, &tm_v, 0, h, (int)c0, barV);
-            tma_load_3d(sm + P_V + 8192, &tm_v, 64, h, (int)c0, barV);
-            issued |= 2u;
+            solo_wait(barL, ph, sAbort, err);
+            pend &= ~1u;
         }
-        // ---- operands.  Row i = r4 + 16 I, channels 8cc ..:  row operand in place; K e^G (for W);
-        // Q e^G (workspace); column operands of blocks J >= I (KP also to the workspace).
+        cp_async_wait_all();
+        __syncthreads();
+        if (*sAbort) break;
+        // ---- running sum of g per key channel (log2 units): thread (c, half) sums tokens 32 half .. +31
+        {
+            const int c = tid & 127, hh = tid >> 7;
+            float gv[32];
 #pragma unroll
-        for (int I = 0; I < 4; ++I) {
-            const int i = r4 + 16 * I;
-            uint4* kp = reinterpret_cast<uint4*>(sm + P_RR + reg * 16384 + sw128(i, ch));
-            uint4* qp = reinterpret_cast<uint4*>(sm + P_RR + reg * 16384 + sw128(64 + i, ch));
-            float kv[8], qv[8];
-            unpack8(*kp, kv);
-            unpack8(*qp, qv);
-            float rk[8], rq[8], kg[8], qg[8], kr[8];
+            for (int r = 0; r < 32; ++r)
+                gv[r] = (32 * hh + r) < L ? *reinterpret_cast<const float*>(sm + P_G + g_off(32 * hh + r, c)) : 0.f;
+            float acc = 0.f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float f = ex2(G[I][e] - E[I][e]);   // >= 1
-                const float r = ex2(E[I][e] - G[I][e]);   // <= 1
-                const float eg = ex2(G[I][e]);            // <= 1
-                rk[e] = kv[e] * f;
-                rq[e] = qv[e] * f;
-                kg[e] = kv[e] * eg;
-                qg[e] = qv[e] * eg;
-                kr[e] = kv[e] * r;
+            for (int r = 0; r < 32; ++r) {
+                acc = fmaf(gv[r], kLog2e, acc);
+                gv[r] = acc;
             }
-            *kp = pack8(rk);
-            *qp = pack8(rq);
-            *reinterpret_cast<uint4*>(sm + P_KG + reg * 8192 + sw128(i, ch)) = pack8(kg);
-            *reinterpret_cast<uint4*>(blob + BLOB_B1 + reg * 16384 + sw128(64 + i, ch)) = pack8(qg);
-            // column operands of row blocks J >= I: k_j e^{E_J - G_j} = kr * e^{E_J - E_I}
+            if (hh == 0) sTot[c] = acc;
+            __syncthreads();
+            const float base = hh ? sTot[c] : 0.f;
 #pragma unroll
-            for (int J = 0; J < 4; ++J) {
-                if (J < I) continue;
-                if (J > I) {
+            for (int r = 0; r < 32; ++r) *reinterpret_cast<float*>(sm + P_G + g_off(32 * hh + r, c)) = gv[r] + base;
+            sE[(2 * hh) * kD + c] = gv[15] + base;
+            sE[(2 * hh + 1) * kD + c] = gv[31] + base;
+            if (hh == 1) reinterpret_cast<float*>(blob + BLOB_EGL)[c] = exp2f(gv[31] + base);
+            __syncthreads();
+        }
+        // ---- operands.  Thread (cc, r4): channels 8cc .. 8cc+7 of rows i = r4 + 16 I (I = 0..3): the row
+        // operand in place; Q e^G (workspace); column operands of blocks J >= I (KP also to the workspace);
+        // K e^G, held until the running sum is no longer read.
+        const int cc = 2 * warp + (lane >> 4), r4 = lane & 15, c8 = 8 * cc;
+        const uint32_t reg = cc >> 3, ch = cc & 7;
+        uint4 kg_hold[4];
+        {
+            float E[4][8], dn[3][8];  // E_I, and e^{E_{J+1} - E_J}
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) kr[e] *= dn[J - 1][e];
+            for (int I = 0; I < 4; ++I) {
+                *reinterpret_cast<float4*>(&E[I][0]) = *reinterpret_cast<const float4*>(sE + I * kD + c8);
+                *reinterpret_cast<float4*>(&E[I][4]) = *reinterpret_cast<const float4*>(sE + I * kD + c8 + 4);
+            }
+#pragma unroll
+            for (int J = 0; J < 3; ++J)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) dn[J][e] = ex2(E[J + 1][e] - E[J][e]);
+#pragma unroll
+            for (int I = 0; I < 4; ++I) {
+                const int i = r4 + 16 * I;
+                uint4* kp = reinterpret_cast<uint4*>(sm + P_RR + reg * 16384 + sw128(i, ch));
+                uint4* qp = reinterpret_cast<uint4*>(sm + P_RR + reg * 16384 + sw128(64 + i, ch));
+                float kv[8], qv[8], G[8];
+                unpack8(*kp, kv);
+                unpack8(*qp, qv);
+                const uint8_t* gp = sm + P_G + (cc >> 2) * 8192;
+                *reinterpret_cast<float4*>(&G[0]) = *reinterpret_cast<const float4*>(gp + sw128(i, 2 * (cc & 3)));
+                *reinterpret_cast<float4*>(&G[4]) = *reinterpret_cast<const float4*>(gp + sw128(i, 2 * (cc & 3) + 1));
+                float rk[8], rq[8], kg[8], qg[8], kr[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float f = ex2(G[e] - E[I][e]);   // >= 1
+                    const float r = ex2(E[I][e] - G[e]);   // <= 1
+                    const float eg = ex2(G[e]);            // <= 1
+                    rk[e] = kv[e] * f;
+                    rq[e] = qv[e] * f;
+                    kg[e] = kv[e] * eg;
+                    qg[e] = qv[e] * eg;
+                    kr[e] = kv[e] * r;
                 }
-                const uint4 u = pack8(kr);
-                if (J == 3) {
-                    *reinterpret_cast<uint4*>(sm + P_KP + reg * 8192 + sw128(i, ch)) = u;
-                    *reinterpret_cast<uint4*>(blob + BLOB_KP + reg * 8192 + sw128(i, ch)) = u;
-                } else {
-                    *reinterpret_cast<uint4*>(sm + P_CC + cc_off(J) + reg * (16u * (J + 1) * 128u) + sw128(i, ch)) = u;
+                *kp = pack8(rk);
+                *qp = pack8(rq);
+                kg_hold[I] = pack8(kg);
+                *reinterpret_cast<uint4*>(blob + BLOB_B1 + reg * 16384 + sw128(64 + i, ch)) = pack8(qg);
+                // column operands of row blocks J >= I: k_j e^{E_J - G_j} = kr * e^{E_J - E_I}
+#pragma unroll
+                for (int J = 0; J < 4; ++J) {
+                    if (J < I) continue;
+                    if (J > I) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) kr[e] *= dn[J - 1][e];
+                    }
+                    const uint4 u = pack8(kr);
+                    *reinterpret_cast<uint4*>(sm + P_CT + reg * kCTRegion + sw128(8 * J * (J + 1) + i, ch)) = u;
+                    if (J == 3) *reinterpret_cast<uint4*>(blob + BLOB_KP + reg * 8192 + sw128(i, ch)) = u;
                 }
             }
         }
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
-        // ---- the four row blocks of A
+        // ---- the four row blocks of A; then K e^G and v take the place of the running sum
         if (tid == 0) {
             tc_fence_after();
-            const uint64_t rr = kdesc(sbase + P_RR);
-            mma_k128(tbase + TM_A0, rr, 16384, kdesc(sbase + P_CC + cc_off(0)), 2048, idesc_bf16_f32(128, 16, false, false));
-            mma_k128(tbase + TM_A1, rr, 16384, kdesc(sbase + P_CC + cc_off(1)), 4096, idesc_bf16_f32(128, 32, false, false));
-            mma_k128(tbase + TM_A2, rr, 16384, kdesc(sbase + P_CC + cc_off(2)), 6144, idesc_bf16_f32(128, 48, false, false));
-            mma_k128(tbase + TM_A3, rr, 16384, kdesc(sbase + P_KP), 8192, idesc_bf16_f32(128, 64, false, false));
+            mma_k128(tbase, kdesc(sbase + P_RR), 16384, kdesc(sbase + P_CT), kCTRegion,
+                     idesc_bf16_f32(128, 160, false, false));
             mma_commit(barA);
-            issued |= 4u;
-            solo_wait(barA, 0, sAbort, err);
+            pend |= 4u;
+            fence_proxy_async();
+            mbar_arrive_expect_tx(barV, 16384);
+            tma_load_3d(sm + P_V, &tm_v, 0, h, (int)c0, barV);
+            tma_load_3d(sm + P_V + 8192, &tm_v, 64, h, (int)c0, barV);
+            pend |= 2u;
+        }
+#pragma unroll
+        for (int I = 0; I < 4; ++I)
+            *reinterpret_cast<uint4*>(sm + P_KG + reg * 8192 + sw128(r4 + 16 * I, ch)) = kg_hold[I];
+        fence_proxy_async();
+        if (tid == 0) {
+            solo_wait(barA, ph, sAbort, err);
+            pend &= ~4u;
         }
         cta_sync_tc();
         if (*sAbort) break;
@@ -499,7 +510,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const int i = r & 63;
             const bool is_k = r < 64;
             const uint32_t lane_base = (uint32_t)(32 * qt) << 16;
-            const uint32_t col0 = Ib == 0 ? TM_A0 : (Ib == 1 ? TM_A1 : (Ib == 2 ? TM_A2 : TM_A3));
+            const uint32_t col0 = 8 * Ib * (Ib + 1);
             uint32_t a[64];
             {
                 uint32_t t0[32], t1[32];
@@ -590,7 +601,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         __syncthreads();
         // ---- W = T Diag(beta) K e^G and U = T Diag(beta) V (rows of D in TMEM lanes 0-63)
         if (tid == 0) {
-            solo_wait(barV, 0, sAbort, err);
+            solo_wait(barV, ph, sAbort, err);
+            pend &= ~2u;
             tc_fence_after();
             const uint32_t id_w = idesc_bf16_f32(128, 128, false, true);
             const uint64_t th = kdesc(sbase + P_TH), tl = kdesc(sbase + P_TL);
@@ -604,13 +616,25 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) mma_bf16(tbase + TM_U, tl + ks * 2, vd + ks * 128, id_w, 1u);
             mma_commit(barW);
-            issued |= 8u;
-            solo_wait(barW, 0, sAbort, err);
+            pend |= 8u;
+            solo_wait(barW, ph, sAbort, err);
+            pend &= ~8u;
         }
         cta_sync_tc();
         if (*sAbort) break;
+        // ---- the next item's inputs land while W and U go out (every operand of this item is consumed)
+        const int this_item = item;
+        item += gridDim.x;
+        int h1 = 0, L1 = 0;
+        int64_t c01 = 0;
+        have = locate(item, h1, c01, L1);
+        if (have) {
+            load_inputs(h1, c01, L1);
+            if (tid == 0) pend |= 1u;
+        }
         // W (bf16, rows 0-63 of B1) by warps 0, 1; U (fp32 rows) by warps 4, 5
         if ((warp & 2) == 0) {
+            uint8_t* bl = blobs + (int64_t)this_item * kBlobBytes;
             const int i = 32 * (warp & 1) + lane;
             const uint32_t lane_base = (uint32_t)(32 * (warp & 1)) << 16;
 #pragma unroll
@@ -625,10 +649,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
                         for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(x[8 * q8 + e]);
                         const int cch = 4 * p + q8;  // 16-byte chunk of the row: channels 8 cch ..
-                        *reinterpret_cast<uint4*>(blob + BLOB_B1 + (cch >> 3) * 16384 + sw128(i, cch & 7)) = pack8(f);
+                        *reinterpret_cast<uint4*>(bl + BLOB_B1 + (cch >> 3) * 16384 + sw128(i, cch & 7)) = pack8(f);
                     }
                 } else {
-                    float4* up = reinterpret_cast<float4*>(blob + BLOB_U + i * 512 + 128 * p);
+                    float4* up = reinterpret_cast<float4*>(bl + BLOB_U + i * 512 + 128 * p);
 #pragma unroll
                     for (int q4 = 0; q4 < 8; ++q4)
                         up[q4] = make_float4(__uint_as_float(x[4 * q4]), __uint_as_float(x[4 * q4 + 1]),
@@ -636,12 +660,17 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 }
             }
         }
-    } while (0);
+        h = h1;
+        c0 = c01;
+        L = L1;
+        tc_fence_before();
+    }
+    cp_async_wait_all();
     if (*sAbort && tid == 0) {  // copies or products still in flight end before the CTA does (bounded)
-        if (issued & 1u) mbar_wait(barL, 0, kWaitLimit);
-        if (issued & 2u) mbar_wait(barV, 0, kWaitLimit);
-        if (issued & 4u) mbar_wait(barA, 0, kWaitLimit);
-        if (issued & 8u) mbar_wait(barW, 0, kWaitLimit);
+        if (pend & 1u) mbar_wait(barL, 0, kWaitLimit), mbar_wait(barL, 1, kWaitLimit);
+        if (pend & 2u) mbar_wait(barV, 0, kWaitLimit), mbar_wait(barV, 1, kWaitLimit);
+        if (pend & 4u) mbar_wait(barA, 0, kWaitLimit), mbar_wait(barA, 1, kWaitLimit);
+        if (pend & 8u) mbar_wait(barW, 0, kWaitLimit), mbar_wait(barW, 1, kWaitLimit);
     }
     tc_fence_before();
     __syncthreads();
@@ -1000,13 +1029,20 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStateSmem);
     if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
     chunk_offsets_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, T_total, off);
     int range = 0;
     for (int64_t r0 = 0; range == 0 || r0 < rows_max; r0 += rows, ++range) {
         const int64_t r1 = r0 + rows < rows_max ? r0 + rows : rows_max;
-        if (r1 > r0)
-            chunk_prep_kernel<<<(unsigned)((r1 - r0) * H), kPrepThreads, kPrepSmem, stream>>>(
-                tq, tk, tv, tg, beta, cu_seqlens, off, N, T_total, H, (int)r0, blobs, err);
+        if (r1 > r0) {
+            const int64_t items = (r1 - r0) * H;
+            const int64_t grid = items < 2 * sms ? items : 2 * sms;
+            chunk_prep_kernel<<<(unsigned)grid, kPrepThreads, kPrepSmem, stream>>>(
+                tq, tk, tv, tg, beta, cu_seqlens, off, N, T_total, H, (int)r0, (int)items, blobs, err);
+        }
         float* c_out = carry + (size_t)(range & 1) * H * kD * kD;
         const float* c_in = carry + (size_t)((range + 1) & 1) * H * kD * kD;
         chunk_state_kernel<<<(unsigned)((int64_t)N * H), kThreads, kStateSmem, stream>>>(
