@@ -357,7 +357,23 @@ def run_ours(args):
     ms_fe, ms_fe_launch, _ = timed(fstep, fsteps, args.warmup, stream, dist)
     fe_bytes = 2 * 3 * wf.T * Cw * 2 + 3 * Cw * 4 * 2   # raw in + normalised out (bf16) + weights
     fe_gbs = fe_bytes / (ms_fe_launch * 1e-3) / 1e9
-    del xf, outs
+
+    # ---------------- front end + prefill from raw inputs: fused vs two passes (the long workload's path) ----
+    gf = fill_device(wf.seed, ks.TID_G, ks.NEG_SOFTPLUS5, (wf.T, wf.H, wf.d), "f32", device=device)
+    bf = fill_device(wf.seed, ks.TID_BETA, ks.SIGMOID, (wf.T, wf.H), "f32", device=device)
+    of = torch.empty((wf.T, wf.H, wf.d), dtype=torch.bfloat16, device=device)
+    fsf = torch.empty((1, wf.H, wf.d, wf.d), dtype=torch.float32, device=device)
+    wsf = torch.empty(kda.kda_chunk_fwd_workspace_size(1, wf.T, wf.H, torch.bfloat16, False)[0], dtype=torch.uint8,
+                      device=device)
+    fused = lambda: kda.kda_chunk_fwd_frontend(*xf, cwf, gf, bf, wf.H, o=of, final_state=fsf, workspace=wsf,
+                                               stream=stream)
+    def two_pass():
+        kda.kda_shortconv_l2norm(*xf, cwf, wf.H, q=outs[0], k=outs[1], v=outs[2], stream=stream)
+        kda.kda_chunk_fwd(outs[0], outs[1], outs[2], gf, bf, o=of, final_state=fsf, workspace=wsf, stream=stream)
+    lsteps = max(10, args.steps // 10)
+    ms_fused, _, _ = timed(fused, lsteps, args.warmup, stream, dist)
+    ms_two, _, _ = timed(two_pass, lsteps, args.warmup, stream, dist)
+    del xf, outs, gf, bf, of, fsf, wsf
 
     if rank != 0:
         if dist is not None:
@@ -413,6 +429,12 @@ def run_ours(args):
                                   "traffic": measured_traffic("shortconv_kernel", "kda_frontend.cu", wf.name),
                                   "peak_source": peak_src}},
     }
+    line["fused_prefill"] = {
+        "workload": "frontend_32k raw q, k, v bf16 [32768, 12288] + g = max(-5, -softplus(z)), beta -> "
+                    "ShortConv(4)+SiLU+L2norm -> chunk_kda (the long workload's path at 32K tokens)",
+        "value": wf.T * world / (ms_fused * 1e-3), "unit": "tokens/s", "ms_per_step": ms_fused, "steps": lsteps,
+        "gpu_launches": lsteps * 3, "two_pass_value": wf.T * world / (ms_two * 1e-3), "two_pass_ms_per_step": ms_two,
+        "note": "kda_chunk_fwd_frontend vs kda_shortconv_l2norm + kda_chunk_fwd; same output bits"}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
     print(json.dumps(line), flush=True)

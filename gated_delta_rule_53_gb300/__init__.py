@@ -20,7 +20,8 @@ import os
 
 import torch
 
-__all__ = ["kda_shortconv_l2norm", "kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_chunk_fwd_workspace_size",
+__all__ = ["kda_shortconv_l2norm", "kda_chunk_fwd", "kda_chunk_fwd_frontend", "kda_chunk_fwd_noalloc",
+           "kda_chunk_fwd_workspace_size",
            "kda_recurrent_step", "library",
            "KDAError", "device_error", "LIB_PATH"]
 
@@ -44,12 +45,14 @@ def library() -> ctypes.CDLL:
         lib.kda_shortconv_l2norm.argtypes = [P, P, P, I64, P, P, I32, I64, I32, I32, P, P, F, I32, P, P, P, P]
         SZ = ctypes.c_size_t
         lib.kda_chunk_fwd.argtypes = [P, P, P, P, P, P, P, I32, I64, I32, I32, I32, F, I32, I32, P, P, P, P, SZ, P]
+        lib.kda_chunk_fwd_frontend.argtypes = [P, P, P, I64, P, P, P, F, P, P, P, P, I32, I64, I32, I32, F, I32, P, P,
+                                               P, P, SZ, P]
         lib.kda_chunk_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, I32, I64, I32, I32, I32, F, I32, I32, P, P, P, P]
         lib.kda_chunk_fwd_workspace_size.argtypes = [I32, I64, I32, I32, I32, I32, I32, I32, ctypes.POINTER(SZ),
                                                      ctypes.POINTER(SZ)]
         lib.kda_recurrent_step.argtypes = [P, P, P, I64, P, P, P, P, P, I32, I32, I32, I32, F, F, P, P]
         for f in (lib.kda_shortconv_l2norm, lib.kda_chunk_fwd, lib.kda_recurrent_step, lib.kda_device_error,
-                  lib.kda_chunk_fwd_workspace_size, lib.kda_chunk_fwd_noalloc):
+                  lib.kda_chunk_fwd_workspace_size, lib.kda_chunk_fwd_noalloc, lib.kda_chunk_fwd_frontend):
             f.restype = ctypes.c_int
         lib.kda_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         lib.kda_selftest_bounded_wait.argtypes = [ctypes.c_uint, ctypes.c_void_p]
@@ -182,6 +185,48 @@ def kda_chunk_fwd(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale: flo
                                  N, T, H, dk, dv, float(scale), int(chunk_size), dt, _ptr(out_gate), _ptr(o),
                                  _ptr(final_state), _ptr(workspace), ws_bytes, _stream(stream))
     _check(rc, "kda_chunk_fwd")
+    return o, final_state
+
+
+def kda_chunk_fwd_frontend(xq, xk, xv, conv_w, g, beta, H: int, init_state=None, cu_seqlens=None,
+                           conv_state_in=None, conv_state_out=None, eps: float = 1e-6, scale: float = 1.0,
+                           chunk_size: int = 64, out_gate=None, o=None, final_state=None,
+                           output_final_state: bool = True, workspace=None, workspace_limit: int = WORKSPACE_LIMIT,
+                           stream=None):
+    """kda_shortconv_l2norm (bf16) + kda_chunk_fwd (bf16) in one pass: raw bf16 xq, xk, xv [T, >=H*128]
+    (one row stride), conv_w bf16 [3*H*128, 4], g fp32 [T, H, 128], beta fp32 [T, H].
+    Returns (o bf16 [T, H, 128], final_state or None)."""
+    d = 128
+    T = xq.shape[0]
+    for name, x in (("xq", xq), ("xk", xk), ("xv", xv)):
+        if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2 or x.stride(1) != 1 or x.shape[0] != T:
+            raise KDAError(f"{name} must be a CUDA bf16 [T, width] tensor with unit inner stride")
+        if x.stride(0) != xq.stride(0):
+            raise KDAError("xq, xk, xv must share their row stride")
+    _dev(conv_w, "conv_w", torch.bfloat16, (3 * H * d, 4))
+    _dev(g, "g", torch.float32, (T, H, d)); _dev(beta, "beta", torch.float32, (T, H))
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    _dev(cu_seqlens, "cu_seqlens", torch.int32)
+    _dev(init_state, "init_state", torch.float32, (N, H, d, d))
+    _dev(conv_state_in, "conv_state_in", torch.bfloat16, (N, 3, 3 * H * d))
+    _dev(conv_state_out, "conv_state_out", torch.bfloat16, (N, 3, 3 * H * d))
+    _dev(out_gate, "out_gate", torch.bfloat16, (T, H * d))
+    if o is None:
+        o = torch.empty((T, H, d), dtype=torch.bfloat16, device=xq.device)
+    _dev(o, "o", torch.bfloat16, (T, H, d))
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, d, d), dtype=torch.float32, device=xq.device)
+    _dev(final_state, "final_state", torch.float32, (N, H, d, d))
+    if workspace is None:
+        full, least = kda_chunk_fwd_workspace_size(N, T, H, torch.bfloat16, cu_seqlens is not None, d, d, chunk_size)
+        workspace = torch.empty(max(least, min(full, int(workspace_limit))), dtype=torch.uint8, device=xq.device)
+    _dev(workspace, "workspace", torch.uint8)
+    rc = library().kda_chunk_fwd_frontend(_ptr(xq), _ptr(xk), _ptr(xv), xq.stride(0), _ptr(conv_w),
+                                          _ptr(conv_state_in), _ptr(conv_state_out), float(eps), _ptr(g), _ptr(beta),
+                                          _ptr(init_state), _ptr(cu_seqlens), N, T, H, d, float(scale),
+                                          int(chunk_size), _ptr(out_gate), _ptr(o), _ptr(final_state),
+                                          _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "kda_chunk_fwd_frontend")
     return o, final_state
 
 

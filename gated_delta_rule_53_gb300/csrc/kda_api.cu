@@ -196,9 +196,47 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const floa
     unsigned int* err = kda::device_error_word();
     if (!err) return set_error(KDA_ERR_CUDA, "device error word unavailable");
     return from_cuda(kda::launch_chunk_tc(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, scale, out_gate, o,
-                                          final_state, workspace, workspace_bytes, err,
+                                          final_state, workspace, workspace_bytes, nullptr, err,
                                           static_cast<cudaStream_t>(stream)),
                      "kda_chunk_fwd launch");
+}
+
+kda_status kda_chunk_fwd_frontend(const void* xq, const void* xk, const void* xv, int64_t x_row_stride,
+                                  const void* conv_w, const void* conv_state_in, void* conv_state_out, float eps,
+                                  const float* g, const float* beta, const float* init_state,
+                                  const int32_t* cu_seqlens, int N, int64_t T_total, int H, int d, float scale,
+                                  int chunk_size, const void* out_gate, void* o, float* final_state,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+    REQUIRE_PTR(xq); REQUIRE_PTR(xk); REQUIRE_PTR(xv); REQUIRE_PTR(conv_w); REQUIRE_PTR(g); REQUIRE_PTR(beta);
+    REQUIRE_PTR(o);
+    OPTIONAL_PTR(conv_state_in); OPTIONAL_PTR(conv_state_out); OPTIONAL_PTR(init_state); OPTIONAL_PTR(final_state);
+    OPTIONAL_PTR(out_gate);
+    kda_status s = check_batch(cu_seqlens, N, T_total, H);
+    if (s != KDA_OK) return s;
+    if (d != kda::kHeadDim) return set_error(KDA_ERR_UNSUPPORTED, "only d = 128 is supported (got %d)", d);
+    if (chunk_size != kda::kChunk)
+        return set_error(KDA_ERR_UNSUPPORTED, "only chunk_size = 64 is supported (got %d)", chunk_size);
+    REQUIRE(x_row_stride >= (int64_t)H * d && x_row_stride % 8 == 0,
+            "x_row_stride must be >= H*d and a multiple of 8 (got %lld)", (long long)x_row_stride);
+    REQUIRE(std::isfinite(eps) && eps >= 0.f, "eps must be finite and >= 0");
+    REQUIRE(std::isfinite(scale), "scale must be finite");
+    REQUIRE(T_total < ((int64_t)1 << 31), "T_total must be below 2^31 (tensor-map coordinates)");
+    REQUIRE(T_total / 64 + N <= 0x7FFFFFFF, "too many chunks");
+    size_t need = 0;
+    kda::chunk_tc_workspace(N, T_total, H, cu_seqlens != nullptr, nullptr, &need);
+    REQUIRE(workspace != nullptr && workspace_bytes >= need,
+            "workspace must hold at least %zu bytes for these sizes (got %zu)", need, workspace_bytes);
+    OPTIONAL_PTR(workspace);
+    unsigned int* err = kda::device_error_word();
+    if (!err) return set_error(KDA_ERR_CUDA, "device error word unavailable");
+    const kda::ChunkFrontend front{xq, xk, xv, x_row_stride, conv_w, conv_state_in, eps};
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = kda::launch_chunk_tc(nullptr, nullptr, nullptr, g, beta, init_state, cu_seqlens, N, T_total, H,
+                                         scale, out_gate, o, final_state, workspace, workspace_bytes, &front, err, st);
+    if (e == cudaSuccess && conv_state_out)  // after the chunk pass has read conv_state_in: the two may alias
+        e = kda::launch_conv_state_out(xq, xk, xv, x_row_stride, cu_seqlens, N, T_total, H, conv_state_in,
+                                       conv_state_out, st);
+    return from_cuda(e, "kda_chunk_fwd_frontend launch");
 }
 
 kda_status kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g, const float* beta,

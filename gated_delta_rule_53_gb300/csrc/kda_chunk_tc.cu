@@ -60,6 +60,7 @@
 #include <mutex>
 
 #include "kda_common.cuh"
+#include "kda_frontend.cuh"
 #include "kda_tc.cuh"
 
 namespace kda {
@@ -295,21 +296,36 @@ constexpr uint32_t kPrepTmemCols = 256;
 // row block I of A: 16 (I + 1) columns from 16 I (I + 1) / 2 (one product of N = 160)
 constexpr uint32_t TM_W = 0, TM_U = 128;                            // then W and U (rows in lanes 0-63)
 constexpr uint32_t kKQGBytes = 4 * 8192 + 4 * 8192;
+constexpr uint32_t kGBytes = 4 * 8192;
 
 static_assert(P_AKK + 64 * kAS * 4 <= P_G && P_NB + 9 * 16 * kNB * 4 <= P_BETA, "solve work overflows its region");
 static_assert(2 * (kPrepSmem + 1024) <= 233472, "two prep CTAs per SM");
+
+// Raw front-end inputs of the fused prefill (unused otherwise).
+struct FrontendArgs {
+    const __nv_bfloat16* xq;
+    const __nv_bfloat16* xk;
+    const __nv_bfloat16* xv;
+    int64_t x_stride;
+    const __nv_bfloat16* conv_w;
+    const __nv_bfloat16* cs_in;
+    float eps;
+};
 
 // Byte offset of g / G element (token i, channel c) in the four 128-byte-swizzled boxes of 32 channels.
 __device__ __forceinline__ uint32_t g_off(int i, int c) {
     return (uint32_t)(c >> 5) * 8192u + sw128((uint32_t)i, (uint32_t)((c & 31) >> 2)) + (uint32_t)(c & 3) * 4u;
 }
 
+// FE: q, k, v are computed here from the raw front-end rows (ShortConv4 + SiLU + L2 norm, the same
+// arithmetic as kda_shortconv_l2norm) instead of being read.
+template <bool FE>
 __global__ void __launch_bounds__(kPrepThreads, 2)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                   const float* __restrict__ beta, const int32_t* __restrict__ cu, const int32_t* __restrict__ off,
                   int N, int64_t T_total, int H, int m0, int n_items, uint8_t* __restrict__ blobs,
-                  unsigned int* err) {
+                  FrontendArgs fe, unsigned int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
@@ -343,15 +359,17 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         L = (eos - c0) < kC ? (int)(eos - c0) : kC;
         return true;
     };
-    // k, q (into the row-operand layout), g and beta of an item
+    // k, q (into the row-operand layout; unless FE), g and beta of an item
     auto load_inputs = [&](int h, int64_t c0, int L) {
         if (tid == 0) {
             fence_proxy_async();
-            mbar_arrive_expect_tx(barL, kKQGBytes);
-            tma_load_3d(sm + P_RR, &tm_k, 0, h, (int)c0, barL);             // k, channels 0-63  -> region 0 rows 0-63
-            tma_load_3d(sm + P_RR + 8192, &tm_q, 0, h, (int)c0, barL);      // q, channels 0-63  -> region 0 rows 64-127
-            tma_load_3d(sm + P_RR + 16384, &tm_k, 64, h, (int)c0, barL);    // k, channels 64-127 -> region 1
-            tma_load_3d(sm + P_RR + 24576, &tm_q, 64, h, (int)c0, barL);
+            mbar_arrive_expect_tx(barL, FE ? kGBytes : kKQGBytes);
+            if (!FE) {
+                tma_load_3d(sm + P_RR, &tm_k, 0, h, (int)c0, barL);             // k, channels 0-63  -> region 0 rows 0-63
+                tma_load_3d(sm + P_RR + 8192, &tm_q, 0, h, (int)c0, barL);      // q, channels 0-63  -> region 0 rows 64-127
+                tma_load_3d(sm + P_RR + 16384, &tm_k, 64, h, (int)c0, barL);    // k, channels 64-127 -> region 1
+                tma_load_3d(sm + P_RR + 24576, &tm_q, 64, h, (int)c0, barL);
+            }
 #pragma unroll
             for (int b4 = 0; b4 < 4; ++b4) tma_load_3d(sm + P_G + b4 * 8192, &tm_g, 32 * b4, h, (int)c0, barL);
         }
@@ -360,6 +378,23 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             cp_async4(sBeta + tid, beta + (ok ? (c0 + tid) * H + h : 0), ok ? 4u : 0u);
         }
         cp_async_commit();
+    };
+    // FE: part p of the chunk's 64 tokens, through the front end, as bf16 into a 128-byte-swizzled operand
+    // tile (two regions of `region` bytes; token i at row row0 + i).  Warp w takes tokens 8w .. 8w+7, lane
+    // the 4 channels from 4 lane.
+    auto frontend_tile = [&](int p, int h, int64_t c0, uint32_t tile, uint32_t region, int row0) {
+        const __nv_bfloat16* x = p == 0 ? fe.xq : (p == 1 ? fe.xk : fe.xv);
+        float y[fe::kFeRun][4], ss[fe::kFeRun];
+        fe::frontend_run<__nv_bfloat16>(x, fe.x_stride, fe.conv_w, cu, N, T_total, H, p, h, lane,
+                                        c0 + fe::kFeRun * warp, fe.cs_in, y, ss);
+#pragma unroll
+        for (int i = 0; i < fe::kFeRun; ++i) {
+            const float inv = p < 2 ? rsqrtf(ss[i] + fe.eps) : 1.0f;
+            const uint32_t at = tile + (lane >> 4) * region + sw128(row0 + fe::kFeRun * warp + i, (lane & 15) >> 1) +
+                                (lane & 1) * 8;
+            *reinterpret_cast<uint2*>(sm + at) =
+                make_uint2(pack_bf16x2(y[i][0] * inv, y[i][1] * inv), pack_bf16x2(y[i][2] * inv, y[i][3] * inv));
+        }
     };
 
     if (tid == 0) {
@@ -387,6 +422,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (tid == 0) {
             solo_wait(barL, ph, sAbort, err);
             pend &= ~1u;
+        }
+        if (FE) {  // k and q into the row operand's space (free: the previous item's W/U products are done)
+            frontend_tile(1, h, c0, P_RR, 16384, 0);
+            frontend_tile(0, h, c0, P_RR, 16384, 64);
         }
         cp_async_wait_all();
         __syncthreads();
@@ -482,15 +521,18 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                      idesc_bf16_f32(128, 160, false, false));
             mma_commit(barA);
             pend |= 4u;
-            fence_proxy_async();
-            mbar_arrive_expect_tx(barV, 16384);
-            tma_load_3d(sm + P_V, &tm_v, 0, h, (int)c0, barV);
-            tma_load_3d(sm + P_V + 8192, &tm_v, 64, h, (int)c0, barV);
-            pend |= 2u;
+            if (!FE) {
+                fence_proxy_async();
+                mbar_arrive_expect_tx(barV, 16384);
+                tma_load_3d(sm + P_V, &tm_v, 0, h, (int)c0, barV);
+                tma_load_3d(sm + P_V + 8192, &tm_v, 64, h, (int)c0, barV);
+                pend |= 2u;
+            }
         }
 #pragma unroll
         for (int I = 0; I < 4; ++I)
             *reinterpret_cast<uint4*>(sm + P_KG + reg * 8192 + sw128(r4 + 16 * I, ch)) = kg_hold[I];
+        if (FE) frontend_tile(2, h, c0, P_V, 8192, 0);  // v, while the A products run
         fence_proxy_async();
         if (tid == 0) {
             solo_wait(barA, ph, sAbort, err);
@@ -601,8 +643,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         __syncthreads();
         // ---- W = T Diag(beta) K e^G and U = T Diag(beta) V (rows of D in TMEM lanes 0-63)
         if (tid == 0) {
-            solo_wait(barV, ph, sAbort, err);
-            pend &= ~2u;
+            if (!FE) {
+                solo_wait(barV, ph, sAbort, err);
+                pend &= ~2u;
+            }
             tc_fence_after();
             const uint32_t id_w = idesc_bf16_f32(128, 128, false, true);
             const uint64_t th = kdesc(sbase + P_TH), tl = kdesc(sbase + P_TL);
@@ -1008,13 +1052,20 @@ void chunk_tc_workspace(int N, int64_t T_total, int H, bool have_cu, size_t* ful
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
                             const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
                             float scale, const void* out_gate, void* o, float* final_state, void* workspace,
-                            size_t workspace_bytes, unsigned int* err, cudaStream_t stream) {
-    CUtensorMap tq, tk, tv, tg;
-    if (!encode_chunk_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, T_total, H) ||
-        !encode_chunk_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, T_total, H) ||
-        !encode_chunk_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, T_total, H) ||
-        !encode_chunk_map(&tg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32, T_total, H))
+                            size_t workspace_bytes, const ChunkFrontend* front, unsigned int* err,
+                            cudaStream_t stream) {
+    CUtensorMap tq = {}, tk = {}, tv = {}, tg;
+    if (!front && (!encode_chunk_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, T_total, H) ||
+                   !encode_chunk_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, T_total, H) ||
+                   !encode_chunk_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, T_total, H)))
         return cudaErrorInvalidValue;
+    if (!encode_chunk_map(&tg, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 32, T_total, H)) return cudaErrorInvalidValue;
+    FrontendArgs fa = {};
+    if (front)
+        fa = FrontendArgs{static_cast<const __nv_bfloat16*>(front->xq), static_cast<const __nv_bfloat16*>(front->xk),
+                          static_cast<const __nv_bfloat16*>(front->xv), front->x_stride,
+                          static_cast<const __nv_bfloat16*>(front->conv_w),
+                          static_cast<const __nv_bfloat16*>(front->conv_state_in), front->eps};
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     float* carry = reinterpret_cast<float*>(ws);
     int32_t* off = reinterpret_cast<int32_t*>(ws + (size_t)2 * H * kStateBytes);
@@ -1025,7 +1076,8 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
     if (rows > rows_max) rows = rows_max > 0 ? rows_max : 1;
     if (rows * H > 0x7FFFFFFF) rows = 0x7FFFFFFF / H;  // grid size of the prep kernel
 
-    cudaError_t e = cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
+    auto prep = front ? chunk_prep_kernel<true> : chunk_prep_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStateSmem);
     if (e != cudaSuccess) return e;
@@ -1040,8 +1092,8 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
         if (r1 > r0) {
             const int64_t items = (r1 - r0) * H;
             const int64_t grid = items < 2 * sms ? items : 2 * sms;
-            chunk_prep_kernel<<<(unsigned)grid, kPrepThreads, kPrepSmem, stream>>>(
-                tq, tk, tv, tg, beta, cu_seqlens, off, N, T_total, H, (int)r0, (int)items, blobs, err);
+            prep<<<(unsigned)grid, kPrepThreads, kPrepSmem, stream>>>(
+                tq, tk, tv, tg, beta, cu_seqlens, off, N, T_total, H, (int)r0, (int)items, blobs, fa, err);
         }
         float* c_out = carry + (size_t)(range & 1) * H * kD * kD;
         const float* c_in = carry + (size_t)((range + 1) & 1) * H * kD * kD;

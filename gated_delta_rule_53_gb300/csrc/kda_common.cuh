@@ -87,10 +87,28 @@ cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, const
                               int H, float scale, kda_dtype dtype, const void* out_gate, void* o,
                               float* final_state, cudaStream_t stream);
 
+// Raw inputs of the fused prefill: q, k, v are computed from them by the front end of
+// kda_shortconv_l2norm (bf16) inside the chunk pass instead of being read.
+struct ChunkFrontend {
+    const void* xq;
+    const void* xk;
+    const void* xv;
+    int64_t x_stride;
+    const void* conv_w;
+    const void* conv_state_in;
+    float eps;
+};
+
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
                             const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
                             float scale, const void* out_gate, void* o, float* final_state, void* workspace,
-                            size_t workspace_bytes, unsigned int* err, cudaStream_t stream);
+                            size_t workspace_bytes, const ChunkFrontend* front, unsigned int* err,
+                            cudaStream_t stream);
+
+// conv_state_out of the front end (the last three raw inputs of each sequence), as a pass of its own.
+cudaError_t launch_conv_state_out(const void* xq, const void* xk, const void* xv, int64_t x_stride,
+                                  const int32_t* cu_seqlens, int N, int64_t T_total, int H,
+                                  const void* conv_state_in, void* conv_state_out, cudaStream_t stream);
 
 // Workspace of launch_chunk_tc: all chunks in one range / the least accepted.
 void chunk_tc_workspace(int N, int64_t T_total, int H, bool have_cu, size_t* full_bytes, size_t* min_bytes);

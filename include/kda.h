@@ -140,6 +140,25 @@ KDA_API kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, co
                          void* o, float* final_state, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The prefill with its front end fused in: the result of kda_shortconv_l2norm (bf16 outputs)
+ * followed by kda_chunk_fwd (bf16), without writing and re-reading q, k, v (the front end runs
+ * inside the chunk pass, on the same arithmetic, so the outputs are the same bits).  This is the
+ * pages' normalisation "in the kernel" taken one step further ("深入 Kimi-K3: Hugging Face 仓库
+ * 分析", paragraph on KDA).
+ *
+ *  xq, xk, xv, x_row_stride, conv_w, conv_state_in, conv_state_out, eps
+ *                  as kda_shortconv_l2norm (conv_state_out may alias conv_state_in)
+ *  g, beta, init_state, cu_seqlens, N, scale, chunk_size, out_gate, o, final_state, workspace
+ *                  as kda_chunk_fwd with dtype KDA_DTYPE_BF16 (o bf16 [T_total, H, d])
+ */
+KDA_API kda_status kda_chunk_fwd_frontend(const void* xq, const void* xk, const void* xv, int64_t x_row_stride,
+                                  const void* conv_w, const void* conv_state_in, void* conv_state_out,
+                                  float eps, const float* g, const float* beta, const float* init_state,
+                                  const int32_t* cu_seqlens, int N, int64_t T_total, int H, int d,
+                                  float scale, int chunk_size, const void* out_gate, void* o,
+                                  float* final_state, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * kda_chunk_fwd without a caller workspace (no counterpart in the sources; an interface
  * convenience).  The bf16 path uses a 64 MiB scratch array that is part of the library's
  * device image (so nothing is allocated), processing as many chunk rows per range as fit.

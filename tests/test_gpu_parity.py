@@ -178,6 +178,60 @@ def test_chunk_workspace_ranges(kda, orc, rows):
     assert kda.device_error() == 0
 
 
+@pytest.mark.parametrize("rows", [None, 2])
+def test_chunk_frontend_fused_equals_two_passes(kda, orc, rows):
+    """kda_chunk_fwd_frontend = kda_shortconv_l2norm (bf16) + kda_chunk_fwd, bit for bit: packed
+    sequences (one empty, two shorter than the 3-token history), carried conv state in and out, an
+    initial state, the output gate, a row stride wider than H*d; also with a workspace of 2 chunk rows.
+    Spot check against the oracle's front end + token loop."""
+    H, d = 2, 128
+    C = H * d
+    lengths = [70, 2, 0, 130, 1, 64]
+    T, N = sum(lengths), len(lengths)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    width = C + 16
+    xs = [ks.fill(109, tid, ks.NORMAL, (T, width), "bf16") for tid in (1, 2, 3)]
+    cw = ks.fill(109, ks.TID_CONV_W, ks.NORMAL, (3 * C, 4), "bf16", 0.0, 0.25)
+    cs = ks.fill(109, ks.TID_CONV_STATE, ks.NORMAL, (N, 3, 3 * C), "bf16")
+    g = ks.fill(109, ks.TID_G, ks.NEG5_SIGMOID, (T, H, d), "f32")
+    b = ks.fill(109, ks.TID_BETA, ks.SIGMOID, (T, H), "f32")
+    s0 = ks.fill(109, ks.TID_STATE, ks.NORMAL, (N, H, d, d), "f32", 0.0, 0.02)
+    gate = ks.fill(109, ks.TID_GATE, ks.NORMAL, (T, C), "bf16")
+    xd = [dev(x) for x in xs]
+    cu_d = dev(cu)
+    # two passes
+    cs_a = torch.empty((N, 3, 3 * C), dtype=torch.bfloat16, device="cuda")
+    q, k, v = kda.kda_shortconv_l2norm(*xd, dev(cw), H, cu_d, dev(cs), cs_a)
+    o1, f1 = kda.kda_chunk_fwd(q, k, v, dev(g), dev(b), dev(s0), cu_d, scale=0.5, out_gate=dev(gate))
+    # fused
+    ws = None
+    if rows is not None:
+        full, least = kda.kda_chunk_fwd_workspace_size(N, T, H)
+        per_row = (full - least) // (T // 64 + N - 1)
+        ws = torch.empty(least + (rows - 1) * per_row, dtype=torch.uint8, device="cuda")
+    cs_b = dev(cs)  # in place: conv_state_out aliases conv_state_in
+    o2, f2 = kda.kda_chunk_fwd_frontend(*xd, dev(cw), dev(g), dev(b), H, dev(s0), cu_d, conv_state_in=cs_b,
+                                        conv_state_out=cs_b, scale=0.5, out_gate=dev(gate), workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(f1, f2) and torch.equal(cs_a, cs_b)
+    assert kda.device_error() == 0
+    # sequence 3 (130 tokens), head 1, against the oracle
+    n, h = 3, 1
+    t0, t1 = int(cu[n]), int(cu[n + 1])
+    sel = lambda x: ks.to_f64(x)[t0:t1, h * d:(h + 1) * d]
+    wh = np.concatenate([ks.to_f64(cw)[p * C + h * d: p * C + (h + 1) * d] for p in range(3)])
+    csh = np.concatenate([ks.to_f64(cs)[n:n + 1, :, p * C + h * d: p * C + (h + 1) * d] for p in range(3)], axis=2)
+    fq, fk, fv = orc.shortconv_silu_l2norm(sel(xs[0]), sel(xs[1]), sel(xs[2]), wh, 1, d, None, csh,
+                                           want_state=False)[:3]
+    rq, rk, rv = (ks.bf16_to_f64(ks.f32_to_bf16(x.astype(np.float32))) for x in (fq, fk, fv))
+    o_ref, f_ref = orc.kda_tokenloop(rq, rk, rv, g[t0:t1, h:h + 1].astype(np.float64),
+                                     b[t0:t1, h:h + 1].astype(np.float64), s0[n:n + 1, h:h + 1].astype(np.float64),
+                                     None, 0.5)
+    o_ref = orc.output_gate(o_ref, ks.to_f64(gate)[t0:t1, h * d:(h + 1) * d])
+    assert orc.rel_l2(host(o2[t0:t1, h:h + 1]), o_ref) <= BF16_O_REL
+    assert orc.rel_l2(host(f2[n:n + 1, h:h + 1]), f_ref) <= BF16_S_REL
+
+
 # ------------------------------------------------------------------------------------------
 # kda_shortconv_l2norm
 # ------------------------------------------------------------------------------------------
@@ -356,7 +410,8 @@ def test_varlen_32_sampled_chains(kda, orc):
 
 def test_long_256k_frontend_gate_sampled_heads(kda, orc):
     """T = 262,144: raw q, k, v -> kda_shortconv_l2norm -> kda_chunk_fwd with the sigmoid
-    output gate, as one pass; heads 0 and 61 checked in full against front end + token loop."""
+    output gate; heads 0 and 61 checked in full against front end + token loop; the fused
+    kda_chunk_fwd_frontend gives the same bits."""
     w = ks.workload("long_256k")
     T, H, d = w.T, w.H, w.d
     C = H * d
@@ -368,10 +423,14 @@ def test_long_256k_frontend_gate_sampled_heads(kda, orc):
     b = fill_dev(w, ks.TID_BETA, ks.SIGMOID, (T, H), "f32")
     gate = fill_dev(w, ks.TID_GATE, ks.NORMAL, (T, C), "bf16")
     q, k, v = kda.kda_shortconv_l2norm(xq, xk, xv, cw, H)
-    del xq, xk, xv
     o, fs = kda.kda_chunk_fwd(q, k, v, g, b, out_gate=gate)
     torch.cuda.synchronize()
-    del q, k, v, g
+    del q, k, v
+    # the fused prefill computes the same bits
+    o2, fs2 = kda.kda_chunk_fwd_frontend(xq, xk, xv, cw, g, b, H, out_gate=gate)
+    torch.cuda.synchronize()
+    assert torch.equal(o2, o) and torch.equal(fs2, fs)
+    del xq, xk, xv, g, o2, fs2
     cw_h = ks.to_f64(w.conv_w())
     heads = (0, 61)
     fe = []
