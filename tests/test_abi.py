@@ -118,3 +118,24 @@ def test_recurrent_step_rejects_bad_arguments(lib):
     assert call(N=0) == 1
     assert call(dv=96) == 2
     assert call(stride=8) == 1
+
+
+def test_chunk_fwd_frontend_rejects_bad_arguments(lib):
+    def call(**over):
+        a = dict(x=P(4096), stride=256, w=P(4096), cs_in=None, cs_out=None, eps=1e-6, g=P(4096), b=P(4096),
+                 init=None, cu=None, N=1, T=64, H=2, d=128, scale=1.0, chunk=64, gate=None, o=P(4096), fs=None,
+                 ws=P(4096), wsb=1 << 30)
+        a.update(over)
+        return lib.kda_chunk_fwd_frontend(a["x"], a["x"], a["x"], a["stride"], a["w"], a["cs_in"], a["cs_out"],
+                                          a["eps"], a["g"], a["b"], a["init"], a["cu"], a["N"], a["T"], a["H"],
+                                          a["d"], a["scale"], a["chunk"], a["gate"], a["o"], a["fs"], a["ws"],
+                                          a["wsb"], None)
+    assert call(x=None) == 1
+    assert call(stride=200) == 1          # < H*d
+    assert call(stride=260) == 1          # not a multiple of 8
+    assert call(d=64) == 2
+    assert call(chunk=32) == 2
+    assert call(eps=-1.0) == 1
+    assert call(ws=None) == 1
+    assert call(wsb=1024) == 1
+    assert call(N=2) == 1                 # several sequences need cu_seqlens
