@@ -8,8 +8,8 @@
 namespace kda {
 namespace {
 
-using fe::kFeRun;
-constexpr int kWarps = 8;  // warps per CTA (64 tokens of one part and head); 4 CTAs per SM
+constexpr int kRun = 8;     // tokens per warp
+constexpr int kWarps = 1;   // one warp per CTA: 32 CTAs per SM schedule independently
 
 template <typename OutT>
 __device__ __forceinline__ void store4(OutT* p, float a, float b, float c, float d);
@@ -23,7 +23,7 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float a,
 }
 
 template <typename OutT>
-__global__ void __launch_bounds__(kWarps * 32, 4)
+__global__ void __launch_bounds__(kWarps * 32, 32)
 shortconv_kernel(const __nv_bfloat16* __restrict__ xq, const __nv_bfloat16* __restrict__ xk,
                  const __nv_bfloat16* __restrict__ xv, int64_t x_stride,
                  const __nv_bfloat16* __restrict__ conv_w, const int32_t* __restrict__ cu, int N,
@@ -31,14 +31,14 @@ shortconv_kernel(const __nv_bfloat16* __restrict__ xq, const __nv_bfloat16* __re
                  OutT* __restrict__ q_out, OutT* __restrict__ k_out, OutT* __restrict__ v_out) {
     const int p = blockIdx.z, h = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t t0 = ((int64_t)blockIdx.x * kWarps + warp) * kFeRun;
+    const int64_t t0 = ((int64_t)blockIdx.x * kWarps + warp) * kRun;
     if (t0 >= T_total) return;
     const __nv_bfloat16* x = p == 0 ? xq : (p == 1 ? xk : xv);
     OutT* out = p == 0 ? q_out : (p == 1 ? k_out : v_out);
-    float y[kFeRun][4], ss[kFeRun];
-    fe::frontend_run<OutT>(x, x_stride, conv_w, cu, N, T_total, H, p, h, lane, t0, cs_in, y, ss);
+    float y[kRun][4], ss[kRun];
+    fe::frontend_run<OutT, kRun>(x, x_stride, conv_w, cu, N, T_total, H, p, h, lane, t0, cs_in, y, ss);
 #pragma unroll
-    for (int i = 0; i < kFeRun; ++i) {
+    for (int i = 0; i < kRun; ++i) {
         const int64_t t = t0 + i;
         if (t < T_total) {
             const float inv = p < 2 ? rsqrtf(ss[i] + eps) : 1.0f;
@@ -89,7 +89,7 @@ cudaError_t launch_shortconv_l2norm(const void* xq, const void* xk, const void* 
     const auto* w = static_cast<const __nv_bfloat16*>(conv_w);
     const auto* cs_in = static_cast<const __nv_bfloat16*>(conv_state_in);
     if (T_total > 0) {
-        const int64_t per_cta = (int64_t)kWarps * kFeRun;
+        const int64_t per_cta = (int64_t)kWarps * kRun;
         dim3 grid((unsigned)((T_total + per_cta - 1) / per_cta), (unsigned)H, 3);
         if (out_dtype == KDA_DTYPE_BF16)
             shortconv_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, stream>>>(

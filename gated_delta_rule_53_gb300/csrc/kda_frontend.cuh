@@ -3,7 +3,7 @@
 // size 4 from "Kimi K3 架构全景", section 02).  Shared by the stand-alone front end
 // (kda_frontend.cu) and the fused prefill (kda_chunk_tc.cu), so both compute identical values.
 //
-// One warp owns one (part, head) and a run of kFeRun tokens; each lane owns 4 adjacent channels,
+// One warp owns one (part, head) and a run of RUN tokens; each lane owns 4 adjacent channels,
 // so a token row of the head is one 256-byte coalesced load.  The warp loads its rows and their
 // 3-token history up front, computes every token's convolution and SiLU, then reduces all the
 // run's squared norms together (the shuffles of different tokens overlap).  A run that crosses a
@@ -15,7 +15,7 @@
 namespace kda {
 namespace fe {
 
-constexpr int kFeRun = 8;  // tokens per warp run
+constexpr int kFeRun = 8;  // tokens per warp run of the fused prefill (8 warps x 8 = one 64-token chunk)
 
 __device__ __forceinline__ float4 bf16x4(uint2 u) {
     return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
@@ -49,19 +49,19 @@ __device__ __forceinline__ float silu<__nv_bfloat16>(float y) {
 // y[i][e]: part p (0 q, 1 k, 2 v) of token t0 + i, channel 4 lane + e of head h, after the convolution
 // and SiLU; for p < 2, ss[i] = the token's squared norm over the head (the caller scales by
 // 1 / sqrt(ss + eps)).  Tokens at or past T_total give zeros.  x: raw rows of part p.
-template <typename OutT>
+template <typename OutT, int RUN = kFeRun>
 __device__ __forceinline__ void frontend_run(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
                                              const __nv_bfloat16* __restrict__ conv_w,
                                              const int32_t* __restrict__ cu, int N, int64_t T_total, int H, int p,
                                              int h, int lane, int64_t t0, const __nv_bfloat16* __restrict__ cs_in,
-                                             float (&y)[kFeRun][4], float (&ss)[kFeRun]) {
+                                             float (&y)[RUN][4], float (&ss)[RUN]) {
     const int64_t C = (int64_t)H * kHeadDim;
     const int64_t ch = (int64_t)h * kHeadDim + 4 * lane;
     const int64_t gc = p * C + ch;
-    // raw rows t0 - 3 .. t0 + kFeRun - 1 (zero outside the tensor), loaded before any arithmetic
-    uint2 xr[kFeRun + 3];
+    // raw rows t0 - 3 .. t0 + RUN - 1 (zero outside the tensor), loaded before any arithmetic
+    uint2 xr[RUN + 3];
 #pragma unroll
-    for (int i = 0; i < kFeRun + 3; ++i) {
+    for (int i = 0; i < RUN + 3; ++i) {
         const int64_t s = t0 - 3 + i;
         xr[i] = (s >= 0 && s < T_total) ? *reinterpret_cast<const uint2*>(x + s * x_stride + ch) : make_uint2(0, 0);
     }
@@ -79,12 +79,12 @@ __device__ __forceinline__ void frontend_run(const __nv_bfloat16* __restrict__ x
     // Sequence bounds.  Fast path: the run and its 3-token history lie inside one sequence.
     int n = cu ? find_seq(cu, N, t0) : 0;
     int64_t bos = cu ? cu[n] : 0, eos = cu ? cu[n + 1] : T_total;
-    const int64_t t_last = (t0 + kFeRun < T_total ? t0 + kFeRun : T_total);  // one past the run's last real token
+    const int64_t t_last = (t0 + RUN < T_total ? t0 + RUN : T_total);  // one past the run's last real token
     const bool simple = (t0 - 3 >= bos) && (t_last <= eos);
 
     if (simple) {
 #pragma unroll
-        for (int i = 0; i < kFeRun; ++i) {
+        for (int i = 0; i < RUN; ++i) {
             const float4 a0 = bf16x4(xr[i]), a1 = bf16x4(xr[i + 1]), a2 = bf16x4(xr[i + 2]), a3 = bf16x4(xr[i + 3]);
             const float h0[4] = {a0.x, a0.y, a0.z, a0.w}, h1[4] = {a1.x, a1.y, a1.z, a1.w};
             const float h2[4] = {a2.x, a2.y, a2.z, a2.w}, h3[4] = {a3.x, a3.y, a3.z, a3.w};
@@ -101,7 +101,7 @@ __device__ __forceinline__ void frontend_run(const __nv_bfloat16* __restrict__ x
     } else {
         // general path: a sequence starts inside the window; earlier positions read the carried state (or zero)
 #pragma unroll
-        for (int i = 0; i < kFeRun; ++i) {
+        for (int i = 0; i < RUN; ++i) {
             const int64_t t = t0 + i;
             if (t < T_total && cu) {
                 while ((int64_t)cu[n + 1] <= t) ++n;
@@ -138,7 +138,7 @@ __device__ __forceinline__ void frontend_run(const __nv_bfloat16* __restrict__ x
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-            for (int i = 0; i < kFeRun; ++i) ss[i] += __shfl_xor_sync(0xFFFFFFFFu, ss[i], o);
+            for (int i = 0; i < RUN; ++i) ss[i] += __shfl_xor_sync(0xFFFFFFFFu, ss[i], o);
     }
 }
 
