@@ -1,30 +1,30 @@
 // kda_recurrent_step: one fused decode step (the fused_recurrent_kda operator of
 // "Kimi K3 架构全景", section 02) for N sequences of one token each.
 //
-// One CTA per (sequence, head), 16 warps (two CTAs per SM).  Warps 0-2 run the front end for q, k
-// and v of the head (ShortConv(4) + SiLU, L2 norm of q and k by warp shuffles,
-// "深入 Kimi-K3: Hugging Face 仓库分析", paragraph on KDA) and shift the
-// convolution state; warp 3 turns g into alpha = exp(g).  Meanwhile every warp
-// has already issued the 128-bit loads of its 8 state rows, so the 64 KB of
-// state per head is in flight while the front end runs.  Then each row r of
-// S (dv x dk) is updated on its own ("Kimi-K3 深度解析", section 三,
-// "KDA 的关键改进"):
+// Four CTAs of 4 warps per (sequence, head), 32 state rows each (eight such CTAs per SM).  Every CTA
+// runs the front end of its head on the token (warps 0-2: ShortConv(4) + SiLU for q, k and v, L2 norm
+// of q and k by warp shuffles, "深入 Kimi-K3: Hugging Face 仓库分析", paragraph on KDA; warp 3:
+// alpha = exp(g)) -- a few hundred values, recomputed rather than shared -- while the 128-bit loads
+// of its 32 state rows are already in flight.  Then each row r of S (dv x dk) is updated on its own
+// ("Kimi-K3 深度解析", section 三, "KDA 的关键改进"):
 //     s~ = s * alpha;  p = s~ . k;  s = s~ + beta (v_r - p) k;  o_r = scale s . q
-// with both dot products reduced by warp shuffles, and written back in place.
-// The kernel streams the state once in and once out: it is bound by HBM.
+// with both dot products reduced by warp shuffles, and written back in place.  The convolution
+// state is shifted by a second small kernel once every CTA has read it.  The step streams the state
+// once in and once out: it is bound by HBM.
 #include "kda_common.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kRowsPerWarp = kHeadDim / (kThreads / 32);  // 8
+constexpr int kThreads = 128;  // 4 warps
+constexpr int kParts = 4;      // CTAs per (sequence, head)
+constexpr int kRowsPerWarp = 8;
 
 __device__ __forceinline__ float4 bf16x4_to_f4(uint2 u) {
     return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 8)
 recurrent_step_kernel(const __nv_bfloat16* __restrict__ xq, const __nv_bfloat16* __restrict__ xk,
                       const __nv_bfloat16* __restrict__ xv, int64_t x_stride,
                       const __nv_bfloat16* __restrict__ conv_w, const float* __restrict__ g,
@@ -34,7 +34,7 @@ recurrent_step_kernel(const __nv_bfloat16* __restrict__ xq, const __nv_bfloat16*
     __shared__ float4 s_q[32], s_k[32], s_v[32], s_alpha[32];
     __shared__ float s_beta;
 
-    const int nh = blockIdx.x;
+    const int nh = blockIdx.x / kParts, pt = blockIdx.x % kParts;
     const int n = nh / H, h = nh % H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t C = (int64_t)H * kHeadDim;
@@ -44,11 +44,11 @@ recurrent_step_kernel(const __nv_bfloat16* __restrict__ xq, const __nv_bfloat16*
     float4 s[kRowsPerWarp];
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
-        const int r = warp * kRowsPerWarp + i;
+        const int r = (pt * (kThreads / 32) + warp) * kRowsPerWarp + i;
         s[i] = __ldcs(reinterpret_cast<const float4*>(S + r * kHeadDim) + lane);
     }
 
-    // 2. front end (warps 0..2) and decay (warp 3).
+    // 2. front end (warps 0..2) and decay (warp 3), for the whole head in every CTA.
     if (warp < 3) {
         const int p = warp;
         const __nv_bfloat16* x = p == 0 ? xq : (p == 1 ? xk : xv);
@@ -85,10 +85,7 @@ recurrent_step_kernel(const __nv_bfloat16* __restrict__ xq, const __nv_bfloat16*
         }
         float4* dst = p == 0 ? s_q : (p == 1 ? s_k : s_v);
         dst[lane] = make_float4(y[0] * inv, y[1] * inv, y[2] * inv, y[3] * inv);
-        // shift the convolution state: rows 1, 2 move up, the raw token enters as row 2.
-        *reinterpret_cast<uint2*>(cs + gc) = old1;
-        *reinterpret_cast<uint2*>(cs + 3 * C + gc) = old2;
-        *reinterpret_cast<uint2*>(cs + 6 * C + gc) = xt;
+
     } else if (warp == 3) {
         const float4 gv = *(reinterpret_cast<const float4*>(g + (int64_t)nh * kHeadDim) + lane);
         s_alpha[lane] = make_float4(expf(gv.x), expf(gv.y), expf(gv.z), expf(gv.w));
@@ -110,7 +107,7 @@ recurrent_step_kernel(const __nv_bfloat16* __restrict__ xq, const __nv_bfloat16*
     for (int i = 0; i < kRowsPerWarp; ++i) part[i] = warp_sum(part[i]);
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) {
-        const int r = warp * kRowsPerWarp + i;
+        const int r = (pt * (kThreads / 32) + warp) * kRowsPerWarp + i;
         const float e = b * (vrow[r] - part[i]);
         s[i].x = fmaf(e, kv.x, s[i].x); s[i].y = fmaf(e, kv.y, s[i].y);
         s[i].z = fmaf(e, kv.z, s[i].z); s[i].w = fmaf(e, kv.w, s[i].w);
@@ -119,10 +116,31 @@ recurrent_step_kernel(const __nv_bfloat16* __restrict__ xq, const __nv_bfloat16*
     }
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i) part[i] = warp_sum(part[i]);
-    __nv_bfloat16* orow = o + (int64_t)nh * kHeadDim + warp * kRowsPerWarp;
+    __nv_bfloat16* orow = o + (int64_t)nh * kHeadDim + (pt * (kThreads / 32) + warp) * kRowsPerWarp;
 #pragma unroll
     for (int i = 0; i < kRowsPerWarp; ++i)
         if (lane == i) orow[i] = __float2bfloat16_rn(scale * part[i]);
+}
+
+// conv_state[n]: rows 1, 2 move up, the raw token enters as row 2 (after recurrent_step_kernel has read it).
+__global__ void conv_shift_kernel(const __nv_bfloat16* __restrict__ xq, const __nv_bfloat16* __restrict__ xk,
+                                  const __nv_bfloat16* __restrict__ xv, int64_t x_stride,
+                                  __nv_bfloat16* __restrict__ conv_state, int H) {
+    const int n = blockIdx.y;
+    const int64_t C = (int64_t)H * kHeadDim;
+    const int64_t q4 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // 4-channel group within q|k|v
+    if (q4 * 4 >= 3 * C) return;
+    const int64_t gc = q4 * 4;
+    const int p = (int)(gc / C);
+    const int64_t ch = gc - p * C;
+    const __nv_bfloat16* x = p == 0 ? xq : (p == 1 ? xk : xv);
+    __nv_bfloat16* cs = conv_state + (int64_t)n * 3 * 3 * C;
+    const uint2 old1 = *reinterpret_cast<const uint2*>(cs + 3 * C + gc);
+    const uint2 old2 = *reinterpret_cast<const uint2*>(cs + 6 * C + gc);
+    const uint2 xt = *reinterpret_cast<const uint2*>(x + (int64_t)n * x_stride + ch);
+    *reinterpret_cast<uint2*>(cs + gc) = old1;
+    *reinterpret_cast<uint2*>(cs + 3 * C + gc) = old2;
+    *reinterpret_cast<uint2*>(cs + 6 * C + gc) = xt;
 }
 
 }  // namespace
@@ -133,10 +151,15 @@ cudaError_t launch_recurrent_step(const void* xq, const void* xk, const void* xv
                                   cudaStream_t stream) {
     const int64_t blocks = (int64_t)N * H;
     if (blocks == 0) return cudaSuccess;
-    recurrent_step_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(
+    if (blocks * kParts > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+    recurrent_step_kernel<<<(unsigned)(blocks * kParts), kThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(xq), static_cast<const __nv_bfloat16*>(xk),
         static_cast<const __nv_bfloat16*>(xv), x_stride, static_cast<const __nv_bfloat16*>(conv_w), g, beta, state,
         static_cast<__nv_bfloat16*>(conv_state), H, scale, eps, static_cast<__nv_bfloat16*>(o));
+    const int64_t groups = 3 * (int64_t)H * kHeadDim / 4;
+    conv_shift_kernel<<<dim3((unsigned)((groups + 255) / 256), (unsigned)N), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(xq), static_cast<const __nv_bfloat16*>(xk),
+        static_cast<const __nv_bfloat16*>(xv), x_stride, static_cast<__nv_bfloat16*>(conv_state), H);
     return cudaGetLastError();
 }
 
