@@ -515,18 +515,20 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tc_fence_before();
         __syncthreads();
         // ---- the four row blocks of A; then K e^G and v take the place of the running sum
-        if (tid == 0) {
+        if (warp == 0) {  // the products are issued by warp 0 (one elected lane), the copies by thread 0
             tc_fence_after();
             mma_k128(tbase, kdesc(sbase + P_RR), 16384, kdesc(sbase + P_CT), kCTRegion,
                      idesc_bf16_f32(128, 160, false, false));
             mma_commit(barA);
-            pend |= 4u;
-            if (!FE) {
-                fence_proxy_async();
-                mbar_arrive_expect_tx(barV, 16384);
-                tma_load_3d(sm + P_V, &tm_v, 0, h, (int)c0, barV);
-                tma_load_3d(sm + P_V + 8192, &tm_v, 64, h, (int)c0, barV);
-                pend |= 2u;
+            if (tid == 0) {
+                pend |= 4u;
+                if (!FE) {
+                    fence_proxy_async();
+                    mbar_arrive_expect_tx(barV, 16384);
+                    tma_load_3d(sm + P_V, &tm_v, 0, h, (int)c0, barV);
+                    tma_load_3d(sm + P_V + 8192, &tm_v, 64, h, (int)c0, barV);
+                    pend |= 2u;
+                }
             }
         }
 #pragma unroll
@@ -642,7 +644,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tc_fence_before();
         __syncthreads();
         // ---- W = T Diag(beta) K e^G and U = T Diag(beta) V (rows of D in TMEM lanes 0-63)
-        if (tid == 0) {
+        if (warp == 0) {
             if (!FE) {
                 solo_wait(barV, ph, sAbort, err);
                 pend &= ~2u;
@@ -788,31 +790,34 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
 
     auto blob_of = [&](int mm) { return blobs + ((int64_t)(mm - m0) * H + h) * kBlobBytes; };
     auto chunk_start = [&](int mm) { return bos + (int64_t)kC * (mm - on); };
-    // loads (thread 0 issues; the previous readers of each buffer are ordered before by a barrier or a
-    // completed product)
-    uint32_t pend = 0;  // copies in flight (thread 0): bit b = B1 buffer b, 4 = U, 8 = A_qk/KP/e^{G_C}
+    // Copies are issued by one thread of the last warp (warp 0 waits on the barriers and issues the
+    // products); every thread calls the load helpers after a barrier that orders the buffer's previous
+    // readers before the copy.  `iss` (loader only) flips a bit per copy issued, as the phase bits flip
+    // per copy consumed: bit b = B1 buffer b, 4 = U, 8 = A_qk/KP/e^{G_C}.
+    constexpr int kLoader = kThreads - 32;
+    uint32_t iss = 0;
     auto load_b1 = [&](int mm, int b) {
-        if (tid == 0) {
+        if (tid == kLoader) {
             fence_proxy_async();
             mbar_arrive_expect_tx(barB + b, 32768);
             bulk_load(sm + S_B1 + b * 32768, blob_of(mm) + BLOB_B1, 32768, barB + b);
-            pend |= 1u << b;
+            iss ^= 1u << b;
         }
     };
     auto load_u = [&](int mm) {
-        if (tid == 0) {
+        if (tid == kLoader) {
             fence_proxy_async();
             mbar_arrive_expect_tx(barU, 32768);
             bulk_load(sm + S_U, blob_of(mm) + BLOB_U, 32768, barU);
-            pend |= 4u;
+            iss ^= 4u;
         }
     };
     auto load_aqk = [&](int mm) {
-        if (tid == 0) {
+        if (tid == kLoader) {
             fence_proxy_async();
             mbar_arrive_expect_tx(barK, kAQKBytes);
             bulk_load(sm + S_AQ, blob_of(mm) + BLOB_AQ, kAQKBytes, barK);
-            pend |= 8u;
+            iss ^= 8u;
         }
     };
 
@@ -891,9 +896,8 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
     int b = 0;
     for (int mm = lo; mm < hi; ++mm, b ^= 1) {
         // ---- (1) [Y^T | O^T] = S0 [W ; Q e^G]^T into the columns of parity b
-        if (tid == 0) {
+        if (warp == 0) {
             solo_wait(barB + b, (phB >> b) & 1u, sAbort, err);
-            pend &= ~(1u << b);
             tc_fence_after();
             mma_k128(tbase + 128 * b, kdesc(sbase + S_S), 16384, kdesc(sbase + S_B1 + b * 32768), 16384, id_s);
             mma_commit(barM);
@@ -904,12 +908,11 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
         if (tid == 0) {
             solo_wait(barM, phM, sAbort, err);
             solo_wait(barU, phU, sAbort, err);
-            pend &= ~4u;
-            if (mm + 2 < hi) load_b1(mm + 2, b);
         }
         phM ^= 1u;
         phU ^= 1u;
         cta_sync_tc();
+        if (mm + 2 < hi) load_b1(mm + 2, b);  // the state product has read B1 buffer b
         // ---- (3) V'^T = U^T - Y^T; thread (row, qq) owns tokens 16qq .. 16qq+15
         {
             uint32_t y[16];
@@ -934,12 +937,11 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
+        if (mm + 1 < hi) load_u(mm + 1);  // every thread has read U
         if (*sAbort) break;
         // ---- (4) dS = V'^T (K e^{G_C - G}) first (the state waits for it), then O^T += V'^T A_qk^T
-        if (tid == 0) {
-            if (mm + 1 < hi) load_u(mm + 1);  // every thread has read U
+        if (warp == 0) {
             solo_wait(barK, phK, sAbort, err);
-            pend &= ~8u;
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
@@ -980,11 +982,11 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
     }
     if (lo < hi && !*sAbort) emit_o(hi - 1, (hi - 1 - lo) & 1);
 
-    if (*sAbort && tid == 0) {  // let copies still in flight land (bounded) before the CTA exits
-        if (pend & 1u) mbar_wait(barB, phB & 1u, kWaitLimit);
-        if (pend & 2u) mbar_wait(barB + 1, (phB >> 1) & 1u, kWaitLimit);
-        if (pend & 4u) mbar_wait(barU, phU, kWaitLimit);
-        if (pend & 8u) mbar_wait(barK, phK, kWaitLimit);
+    if (*sAbort && tid == kLoader) {  // let copies still in flight land (bounded) before the CTA exits
+        if ((iss ^ phB) & 1u) mbar_wait(barB, phB & 1u, kWaitLimit);
+        if ((iss ^ phB) & 2u) mbar_wait(barB + 1, (phB >> 1) & 1u, kWaitLimit);
+        if (((iss >> 2) ^ phU) & 1u) mbar_wait(barU, phU, kWaitLimit);
+        if (((iss >> 3) ^ phK) & 1u) mbar_wait(barK, phK, kWaitLimit);
     }
     __syncthreads();
     if (s_out && !*sAbort) {

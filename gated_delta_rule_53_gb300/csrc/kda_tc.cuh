@@ -62,9 +62,25 @@ __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
+// True when the phase with parity `parity` has completed (no suspension).
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // Waits for the phase with parity `parity` to complete; gives up after `limit`
 // polls and returns false (the caller reports a device error instead of hanging).
+// A phase that has already completed is seen by one test_wait (a try_wait costs about
+// 100 cycles even then); otherwise try_wait suspends the thread between polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
+    if (mbar_test(bar, parity)) return true;
     const uint32_t addr = smem_u32(bar);
     for (uint32_t it = 0; it < limit; ++it) {
         uint32_t done;
@@ -109,24 +125,31 @@ __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint
     return base + (lane << 16) + col;
 }
 
-// D (+)= A * B^T (both operands in shared memory), issued by one thread.
+// The MMA and commit helpers below are warp-collective: all 32 lanes of a converged warp call
+// them with the same arguments and one lane, chosen by elect.sync (the same lane every time for
+// a full warp), issues the instruction.  Issuing from a whole warp keeps the operands warp-uniform;
+// issuing from a lone thread (if (tid == 0)) measured about twice the cost per instruction.
+
+// D (+)= A * B^T (both operands in shared memory).
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "{\n\t.reg .pred pe, pa;\n\t"
+        "elect.sync _|pe, 0xffffffff;\n\t"
+        "setp.ne.b32 pa, %4, 0;\n\t"
+        "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pa;\n\t}\n" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
-// D (+)= A * B^T with tf32 operands (K = 8 per instruction), issued by one thread.
+// D (+)= A * B^T with tf32 operands (K = 8 per instruction).
 __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "{\n\t.reg .pred pe, pa;\n\t"
+        "elect.sync _|pe, 0xffffffff;\n\t"
+        "setp.ne.b32 pa, %4, 0;\n\t"
+        "@pe tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, pa;\n\t}\n" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
@@ -138,10 +161,15 @@ __device__ __forceinline__ float to_tf32(float x) {
     return __uint_as_float(y);
 }
 
-// The mbarrier receives one arrival when every MMA this thread issued before has completed.
+// Warp-collective: the mbarrier receives one arrival when every MMA the elected lane issued
+// before has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
+    asm volatile(
+        "{\n\t.reg .pred pe;\n\t"
+        "elect.sync _|pe, 0xffffffff;\n\t"
+        "@pe tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
+            smem_u32(bar))
+        : "memory");
 }
 
 // 32 consecutive fp32 columns of the warp's 32 lanes (lane quarter = warp % 4).
