@@ -85,7 +85,7 @@ __device__ __forceinline__ float ex2(float x) {
 // reader uses; the last three are contiguous so that one copy brings them in).
 constexpr uint32_t BLOB_B1 = 0;        // [W ; Q e^G] bf16, two regions of [128][64] (128-byte swizzle)
 constexpr uint32_t BLOB_U = 32768;     // U fp32 [64][128], row-major
-constexpr uint32_t BLOB_AQ = 65536;    // A_qk tf32, two regions of [64][32]
+constexpr uint32_t BLOB_AQ = 65536;    // A_qk as bf16 hi then lo, each [64][64] (one 128-byte-swizzled region)
 constexpr uint32_t BLOB_KP = 81920;    // K e^{G_C - G} bf16, two regions of [64][64]
 constexpr uint32_t BLOB_EGL = 98304;   // e^{G_C} fp32 [128]
 constexpr uint32_t kBlobBytes = 98816;
@@ -544,7 +544,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (*sAbort) break;
         float* sAkk = reinterpret_cast<float*>(sm + P_AKK);
         float* sTf = reinterpret_cast<float*>(sm + P_TF);
-        // ---- A_kk (fp32 work array) and A_qk (tf32 operand, to the workspace)
+        // ---- A_kk (fp32 work array) and A_qk (bf16 hi and lo operands, to the workspace)
         {
             // lane quarter qt holds rows 32qt .. 32qt+31 of [k-rows ; q-rows]: lanes 0-15 belong to row block
             // 2(qt%2) and lanes 16-31 to 2(qt%2)+1; warps 0-3 read the first block's columns, warps 4-7 the second's.
@@ -581,15 +581,17 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     }
                 } else {
 #pragma unroll
-                    for (int c4 = 0; c4 < 16; ++c4) {  // tf32: 32 columns per 128-byte region row
-                        float f[4];
+                    for (int c8 = 0; c8 < 8; ++c8) {  // hi and lo bf16 tiles, 8 columns per 16-byte chunk
+                        float fh[8], fl[8];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int j = 4 * c4 + e;
-                            f[e] = (j <= i && j < ncols) ? to_tf32(__uint_as_float(a[j])) : 0.f;
+                        for (int e = 0; e < 8; ++e) {
+                            const int j = 8 * c8 + e;
+                            const float x = (j <= i && j < ncols) ? __uint_as_float(a[j]) : 0.f;
+                            fh[e] = __bfloat162float(__float2bfloat16_rn(x));
+                            fl[e] = x - fh[e];
                         }
-                        *reinterpret_cast<float4*>(blob + BLOB_AQ + (c4 >> 3) * 8192 + sw128(i, c4 & 7)) =
-                            make_float4(f[0], f[1], f[2], f[3]);
+                        *reinterpret_cast<uint4*>(blob + BLOB_AQ + sw128(i, c8)) = pack8(fh);
+                        *reinterpret_cast<uint4*>(blob + BLOB_AQ + 8192 + sw128(i, c8)) = pack8(fl);
                     }
                 }
             }
@@ -726,26 +728,38 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 // =============================================================================================
 // chunk_state_kernel: one (sequence, head) chain through a range of its chunks
 // =============================================================================================
-constexpr int kThreads = 512;
-constexpr uint32_t S_S = 0;             // bf16 S0 [128][128], A operand of the S0 products
-constexpr uint32_t S_B1 = 32768;        // [W ; Q e^G] of two chunks, 32 KB each
-constexpr uint32_t S_U = 98304;         // U fp32 [64][128]
-constexpr uint32_t S_AQ = 131072;       // A_qk tf32          } one copy
-constexpr uint32_t S_KP = 147456;       // K e^{G_C - G} bf16 }
-constexpr uint32_t S_EGL = 163840;      // e^{G_C} fp32 [128] }
-constexpr uint32_t S_ZT = 164864;       // V'^T tf32 [128][64] (two regions of 16 KB), A of the output product
-constexpr uint32_t S_VB = 197632;       // V'^T bf16 [128][64], A of the state product
-constexpr uint32_t S_BAR = 214016;      // mbarriers: B1 x2, U, A_qk/KP/e^{G_C}, S0 products, dS, output product
+constexpr int kSimt = 512;               // 16 warps hold the state and do the element-wise work
+constexpr int kThreads = kSimt + 32;     // + one warp that issues the products and copies
+constexpr int kMmaWarp = kSimt / 32;
+// Named barriers between the two roles (id 0 is __syncthreads), each completed by all kThreads:
+constexpr int NB_S = 1;  // SIMT -> MMA warp: bf16 state operand stored (e^{G_C} and the old B1 buffer free)
+constexpr int NB_Y = 2;  // MMA warp -> SIMT: [Y | O] of the chunk in TMEM, U in shared memory
+constexpr int NB_V = 3;  // SIMT -> MMA warp: V' hi and lo stored, U consumed
+constexpr int NB_D = 4;  // MMA warp -> SIMT: dS in TMEM
+constexpr int NB_O = 5;  // MMA warp -> SIMT: the chunk's output product complete
+constexpr uint32_t S_B1 = 0;            // [W ; Q e^G] of two chunks, 32 KB each
+constexpr uint32_t S_U = 65536;         // U fp32 [64][128]
+constexpr uint32_t S_AQ = 98304;        // A_qk bf16 hi, lo    } one copy
+constexpr uint32_t S_KP = 114688;       // K e^{G_C - G} bf16  }
+constexpr uint32_t S_EGL = 131072;      // e^{G_C} fp32 [128] of two chunks (copied with that chunk's B1)
+constexpr uint32_t S_BAR = 132096;      // mbarriers: B1 x2, U, A_qk/KP, S0 products, dS, output product
 constexpr uint32_t S_MISC = S_BAR + 64; // TMEM base, abort flag
 constexpr uint32_t kStateSmem = S_MISC + 64 + 1024;
-constexpr uint32_t kAQKBytes = BLOB_EGL + 512 - BLOB_AQ;
-// TMEM columns: S0 products of chunk parity p at 128 p (Y^T in 64 columns, then O^T in 64); dS at 256
-constexpr uint32_t TM_DS = 256;
+constexpr uint32_t kAQKBytes = BLOB_EGL - BLOB_AQ;
+// TMEM columns: S0 products of chunk parity p at 128 p (Y^T in 64 columns, then O^T in 64); dS at 256;
+// the A operands of the products, bf16 packed two per column: S0 at 384 (64 columns), V'^T hi at 448
+// and V'^T lo at 480 (32 columns each)
+constexpr uint32_t TM_DS = 256, TM_SA = 384, TM_VH = 448, TM_VL = 480;
 constexpr uint32_t kTmemCols = 512;
 
-static_assert(S_KP - S_AQ == BLOB_KP - BLOB_AQ && S_EGL - S_AQ == BLOB_EGL - BLOB_AQ, "copy layout");
-static_assert(S_EGL + 512 <= S_ZT && S_ZT % 1024 == 0 && S_VB % 1024 == 0, "alignment");
+static_assert(S_KP - S_AQ == BLOB_KP - BLOB_AQ, "copy layout");
+static_assert(S_AQ % 1024 == 0 && S_KP % 1024 == 0 && S_EGL + 1024 <= S_BAR, "alignment");
 static_assert(kStateSmem <= 232448, "shared memory");
+
+__device__ __forceinline__ void nb_sync(int id) { asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kThreads) : "memory"); }
+__device__ __forceinline__ void nb_arrive(int id) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "n"(kThreads) : "memory");
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, const int32_t* __restrict__ off,
@@ -755,7 +769,7 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int chain = blockIdx.x, n = chain / H, h = chain % H;
     const int on = off[n], on1 = off[n + 1];
     int lo = on > m0 ? on : m0, hi = on1 < m1 ? on1 : m1;
@@ -768,7 +782,7 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
     }
     const bool starts = empty_seq || lo == on;   // the chain begins here: initial state
     const bool ends = empty_seq || hi == on1;    // the chain ends here: final state
-    const int row = tid & 127, qq = tid >> 7;    // state row / TMEM lane; quarter of the key channels / tokens
+    const int row = tid & 127, qq = (tid >> 7) & 3;  // state row / TMEM lane; quarter of the key channels / tokens
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const int64_t in_off = (starts ? (int64_t)chain : (int64_t)h) * kD * kD + (int64_t)row * kD + 32 * qq;
     const int64_t out_off = (ends ? (int64_t)chain : (int64_t)h) * kD * kD + (int64_t)row * kD + 32 * qq;
@@ -777,9 +791,7 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
     int64_t bos, eos;
     seq_bounds(cu, n, T_total, bos, eos);
 
-    const float* sU = reinterpret_cast<const float*>(sm + S_U);
-    const float* sEGl = reinterpret_cast<const float*>(sm + S_EGL);
-    uint64_t* barB = reinterpret_cast<uint64_t*>(sm + S_BAR);  // [2]
+    uint64_t* barB = reinterpret_cast<uint64_t*>(sm + S_BAR);  // [2] B1 and e^{G_C}
     uint64_t* barU = barB + 2;
     uint64_t* barK = barB + 3;
     uint64_t* barM = barB + 4;
@@ -788,214 +800,241 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + S_MISC);
     volatile int* sAbort = reinterpret_cast<volatile int*>(sm + S_MISC + 4);
 
-    auto blob_of = [&](int mm) { return blobs + ((int64_t)(mm - m0) * H + h) * kBlobBytes; };
-    auto chunk_start = [&](int mm) { return bos + (int64_t)kC * (mm - on); };
-    // Copies are issued by one thread of the last warp (warp 0 waits on the barriers and issues the
-    // products); every thread calls the load helpers after a barrier that orders the buffer's previous
-    // readers before the copy.  `iss` (loader only) flips a bit per copy issued, as the phase bits flip
-    // per copy consumed: bit b = B1 buffer b, 4 = U, 8 = A_qk/KP/e^{G_C}.
-    constexpr int kLoader = kThreads - 32;
-    uint32_t iss = 0;
-    auto load_b1 = [&](int mm, int b) {
-        if (tid == kLoader) {
-            fence_proxy_async();
-            mbar_arrive_expect_tx(barB + b, 32768);
-            bulk_load(sm + S_B1 + b * 32768, blob_of(mm) + BLOB_B1, 32768, barB + b);
-            iss ^= 1u << b;
-        }
-    };
-    auto load_u = [&](int mm) {
-        if (tid == kLoader) {
-            fence_proxy_async();
-            mbar_arrive_expect_tx(barU, 32768);
-            bulk_load(sm + S_U, blob_of(mm) + BLOB_U, 32768, barU);
-            iss ^= 4u;
-        }
-    };
-    auto load_aqk = [&](int mm) {
-        if (tid == kLoader) {
-            fence_proxy_async();
-            mbar_arrive_expect_tx(barK, kAQKBytes);
-            bulk_load(sm + S_AQ, blob_of(mm) + BLOB_AQ, kAQKBytes, barK);
-            iss ^= 8u;
-        }
-    };
-
     if (tid == 0) {
         for (int i = 0; i < 7; ++i) mbar_init(barB + i, 1);
         fence_mbar_init();
         *sAbort = 0;
     }
     if (warp == 0) tmem_alloc(sTmem, kTmemCols);
-    __syncthreads();  // barriers initialised before the first copy lands on them
-    if (lo < hi) {
-        load_b1(lo, 0);
-        if (lo + 1 < hi) load_b1(lo + 1, 1);
-        load_u(lo);
-        load_aqk(lo);
-    }
-
-    // state: row `row`, key channels [32 qq, 32 qq + 32) in registers; bf16 copy as the S0 operand
-    float s[32];
-#pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-        float4 x = s_in ? *reinterpret_cast<const float4*>(s_in + in_off + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-        s[j] = x.x; s[j + 1] = x.y; s[j + 2] = x.z; s[j + 3] = x.w;
-    }
-    auto write_state_operand = [&]() {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = s[8 * c + e];
-            *reinterpret_cast<uint4*>(sm + S_S + (qq >> 1) * 16384 + sw128(row, 4 * (qq & 1) + c)) = pack8(f);
-        }
-        fence_proxy_async();  // the products read it through the async proxy
-    };
-    write_state_operand();
     tc_fence_before();
-    __syncthreads();
+    __syncthreads();  // barriers initialised and TMEM allocated
     tc_fence_after();
     const uint32_t tbase = *sTmem;
-    uint32_t phB = 0, phU = 0, phK = 0, phM = 0, phD = 0, phO = 0;  // phB: bit b = phase of B1 buffer b
 
-    const uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
-    const uint32_t id_t64 = idesc_tf32_f32(128, 64);
-    const uint32_t id_ds = idesc_bf16_f32(128, 128, false, true);
-
-    // outputs of chunk mm (its product complete, in TMEM columns 128 p + 64): thread (row, qq) stores
-    // tokens 16qq .. 16qq+15 of value row `row`; a warp writes 64 contiguous bytes per token
-    auto emit_o = [&](int mm, int p) {
-        const int64_t c0 = chunk_start(mm);
-        const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
-        tc_fence_after();
-        uint32_t xo[16];
-        tmem_ld16_async(tbase + lane_base + 128 * p + 64 + 16 * qq, xo);
-        tmem_wait_ld(); reg_fence(xo);
-        const int64_t stride = (int64_t)H * kD;
-        const int64_t at0 = ((c0 + 16 * qq) * H + h) * kD + row;
-        __nv_bfloat16* op = o + at0;
-        if (gate) {
-            const __nv_bfloat16* gp = gate + at0;
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-                if (16 * qq + e < L) {
-                    const float gv = __bfloat162float(gp[e * stride]);
-                    op[e * stride] = __float2bfloat16_rn(scale * __uint_as_float(xo[e]) / (1.0f + __expf(-gv)));
-                }
-        } else if (L == kC) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) op[e * stride] = __float2bfloat16_rn(scale * __uint_as_float(xo[e]));
-        } else {
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-                if (16 * qq + e < L) op[e * stride] = __float2bfloat16_rn(scale * __uint_as_float(xo[e]));
-        }
-    };
-
-    int b = 0;
-    for (int mm = lo; mm < hi; ++mm, b ^= 1) {
-        // ---- (1) [Y^T | O^T] = S0 [W ; Q e^G]^T into the columns of parity b
-        if (warp == 0) {
-            solo_wait(barB + b, (phB >> b) & 1u, sAbort, err);
-            tc_fence_after();
-            mma_k128(tbase + 128 * b, kdesc(sbase + S_S), 16384, kdesc(sbase + S_B1 + b * 32768), 16384, id_s);
-            mma_commit(barM);
-        }
-        phB ^= 1u << b;
-        // ---- (2) the previous chunk's outputs while these products run
-        if (mm > lo) emit_o(mm - 1, b ^ 1);
-        if (tid == 0) {
-            solo_wait(barM, phM, sAbort, err);
-            solo_wait(barU, phU, sAbort, err);
-        }
-        phM ^= 1u;
-        phU ^= 1u;
-        cta_sync_tc();
-        if (mm + 2 < hi) load_b1(mm + 2, b);  // the state product has read B1 buffer b
-        // ---- (3) V'^T = U^T - Y^T; thread (row, qq) owns tokens 16qq .. 16qq+15
-        {
-            uint32_t y[16];
-            tmem_ld16_async(tbase + lane_base + 128 * b + 16 * qq, y);
-            tmem_wait_ld(); reg_fence(y);
-            float x[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) x[e] = sU[(16 * qq + e) * kD + row] - __uint_as_float(y[e]);
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)  // tf32 copy for the output product
-                *reinterpret_cast<float4*>(sm + S_ZT + (qq >> 1) * 16384 + sw128(row, 4 * (qq & 1) + c4)) =
-                    make_float4(to_tf32(x[4 * c4]), to_tf32(x[4 * c4 + 1]), to_tf32(x[4 * c4 + 2]),
-                                to_tf32(x[4 * c4 + 3]));
-#pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {  // bf16 copy for the state product
-                float f[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = x[8 * c2 + e];
-                *reinterpret_cast<uint4*>(sm + S_VB + sw128(row, 2 * qq + c2)) = pack8(f);
+    float s[32];  // SIMT threads: the state, row `row`, key channels [32 qq, 32 qq + 32)
+    if (warp == kMmaWarp) {
+        // ======== products and copies: one warp, MMAs from an elected lane, copies from lane 0 ========
+        auto blob_of = [&](int mm) { return blobs + ((int64_t)(mm - m0) * H + h) * kBlobBytes; };
+        uint32_t iss = 0;  // a bit flips per copy issued (B1 buffer b: bit b, U: 4, A_qk/KP: 8)
+        auto load_b1 = [&](int mm, int b) {
+            if (lane == 0) {
+                fence_proxy_async();
+                mbar_arrive_expect_tx(barB + b, 32768 + 512);
+                bulk_load(sm + S_B1 + b * 32768, blob_of(mm) + BLOB_B1, 32768, barB + b);
+                bulk_load(sm + S_EGL + b * 512, blob_of(mm) + BLOB_EGL, 512, barB + b);
             }
+            __syncwarp();
+            iss ^= 1u << b;
+        };
+        auto load_u = [&](int mm) {
+            if (lane == 0) {
+                fence_proxy_async();
+                mbar_arrive_expect_tx(barU, 32768);
+                bulk_load(sm + S_U, blob_of(mm) + BLOB_U, 32768, barU);
+            }
+            __syncwarp();
+            iss ^= 4u;
+        };
+        auto load_aq = [&](int mm) {
+            if (lane == 0) {
+                fence_proxy_async();
+                mbar_arrive_expect_tx(barK, kAQKBytes);
+                bulk_load(sm + S_AQ, blob_of(mm) + BLOB_AQ, kAQKBytes, barK);
+            }
+            __syncwarp();
+            iss ^= 8u;
+        };
+        auto wait = [&](uint64_t* bar, uint32_t ph) { solo_wait(bar, ph, sAbort, err); };
+        const uint32_t id_64 = idesc_bf16_f32(128, 64, false, false);
+        const uint32_t id_ds = idesc_bf16_f32(128, 128, false, true);
+        uint32_t phB = 0, phU = 0, phK = 0, phM = 0, phD = 0, phO = 0;  // phB: bit b = phase of B1 buffer b
+        if (lo < hi) {
+            load_b1(lo, 0);
+            load_u(lo);
+            load_aq(lo);
         }
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-        if (mm + 1 < hi) load_u(mm + 1);  // every thread has read U
-        if (*sAbort) break;
-        // ---- (4) dS = V'^T (K e^{G_C - G}) first (the state waits for it), then O^T += V'^T A_qk^T
-        if (warp == 0) {
-            solo_wait(barK, phK, sAbort, err);
+        int b = 0;
+        for (int mm = lo; mm < hi; ++mm, b ^= 1) {
+            const bool next = mm + 1 < hi;
+            // ---- Y^T = S0 W^T (the V' pass waits for it), then O^T = S0 (Q e^G)^T; A = S0 from TMEM
+            nb_sync(NB_S);
+            wait(barB + b, (phB >> b) & 1u);
+            phB ^= 1u << b;
+            tc_fence_after();
+            const uint32_t b1 = sbase + S_B1 + b * 32768;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16_ta(tbase + 128 * b, tbase + TM_SA + 8 * ks,
+                            kdesc(b1 + (ks >> 2) * 16384) + (ks & 3) * 2, id_64, ks > 0 ? 1u : 0u);
+            mma_commit(barM);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16_ta(tbase + 128 * b + 64, tbase + TM_SA + 8 * ks,
+                            kdesc(b1 + (ks >> 2) * 16384 + 8192) + (ks & 3) * 2, id_64, ks > 0 ? 1u : 0u);
+            wait(barM, phM);
+            phM ^= 1u;
+            wait(barU, phU);
+            phU ^= 1u;
+            const bool stop = *sAbort != 0;
+            tc_fence_before();
+            nb_arrive(NB_Y);
+            if (stop) break;
+            if (next) load_b1(mm + 1, b ^ 1);  // the previous chunk's B1 and e^{G_C} are consumed
+            // ---- dS = V'^T (K e^{G_C - G}) (the state waits for it), then O^T += V'^T A_qk^T as
+            //      hi.hi + hi.lo + lo.hi; A = V'^T from TMEM
+            nb_sync(NB_V);
+            wait(barK, phK);
+            phK ^= 1u;
             tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                mma_bf16(tbase + TM_DS, kdesc(sbase + S_VB) + ks * 2, sdesc_sw128(sbase + S_KP, 8192, 1024) + ks * 128,
-                         id_ds, ks > 0 ? 1u : 0u);
+                mma_bf16_ta(tbase + TM_DS, tbase + TM_VH + 8 * ks, sdesc_sw128(sbase + S_KP, 8192, 1024) + ks * 128,
+                            id_ds, ks > 0 ? 1u : 0u);
             mma_commit(barD);
-            const uint64_t va = kdesc(sbase + S_ZT), aq = kdesc(sbase + S_AQ);
+            wait(barD, phD);
+            phD ^= 1u;
+            tc_fence_before();
+            nb_arrive(NB_D);
+            if (next) load_u(mm + 1);  // every thread has read U
+            const uint32_t od = tbase + 128 * b + 64;
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t reg = ks >> 2, off2 = (ks & 3) * 32;
-                mma_tf32(tbase + 128 * b + 64, va + ((reg * 16384 + off2) >> 4), aq + ((reg * 8192 + off2) >> 4),
-                         id_t64, 1u);
-            }
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ta(od, tbase + TM_VH + 8 * ks, kdesc(sbase + S_AQ) + ks * 2, id_64, 1u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ta(od, tbase + TM_VH + 8 * ks, kdesc(sbase + S_AQ + 8192) + ks * 2, id_64, 1u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ta(od, tbase + TM_VL + 8 * ks, kdesc(sbase + S_AQ) + ks * 2, id_64, 1u);
             mma_commit(barO);
-            solo_wait(barD, phD, sAbort, err);
+            wait(barO, phO);
+            phO ^= 1u;
+            if (next) load_aq(mm + 1);  // A_qk and KP of this chunk are consumed
+            tc_fence_before();
+            nb_arrive(NB_O);
         }
-        phK ^= 1u;
-        phD ^= 1u;
-        cta_sync_tc();
-        // ---- (5) the state update
-        {
-            uint32_t d0[32];
-            tmem_ld32_async(tbase + lane_base + TM_DS + 32 * qq, d0);
-            float eg[32];
-#pragma unroll
-            for (int e4 = 0; e4 < 32; e4 += 4) *reinterpret_cast<float4*>(eg + e4) = *reinterpret_cast<const float4*>(sEGl + 32 * qq + e4);
-            tmem_wait_ld(); reg_fence(d0);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) s[e] = fmaf(s[e], eg[e], __uint_as_float(d0[e]));
+        if (*sAbort && lane == 0) {  // let copies still in flight land (bounded) before the CTA exits
+            if ((iss ^ phB) & 1u) mbar_wait(barB, phB & 1u, kWaitLimit);
+            if ((iss ^ phB) & 2u) mbar_wait(barB + 1, (phB >> 1) & 1u, kWaitLimit);
+            if (((iss >> 2) ^ phU) & 1u) mbar_wait(barU, phU, kWaitLimit);
+            if (((iss >> 3) ^ phK) & 1u) mbar_wait(barK, phK, kWaitLimit);
         }
-        write_state_operand();
-        if (tid == 0) solo_wait(barO, phO, sAbort, err);  // the output product is done: outputs ready, A_qk/KP free
-        phO ^= 1u;
-        tc_fence_before();
-        __syncthreads();
-        if (mm + 1 < hi) load_aqk(mm + 1);
-        if (*sAbort) break;
+        __syncwarp();
+    } else {
+        // ======== the state: thread (row, qq) holds row `row`, key channels [32 qq, 32 qq + 32) ========
+        const float* sU = reinterpret_cast<const float*>(sm + S_U);
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            float4 x = s_in ? *reinterpret_cast<const float4*>(s_in + in_off + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+            s[j] = x.x; s[j + 1] = x.y; s[j + 2] = x.z; s[j + 3] = x.w;
+        }
+        auto write_state_operand = [&]() {  // bf16 copy in TMEM, the A operand of the S0 products
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) w[j] = pack_bf16x2(s[2 * j], s[2 * j + 1]);
+            tmem_st16(tbase + lane_base + TM_SA + 16 * qq, w);
+            tmem_wait_st();
+        };
+        // outputs of chunk mm (its product complete, in TMEM columns 128 p + 64): thread (row, qq) stores
+        // tokens 16qq .. 16qq+15 of value row `row`; a warp writes 64 contiguous bytes per token
+        auto emit_o = [&](int mm, int p) {
+            const int64_t c0 = bos + (int64_t)kC * (mm - on);
+            const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
+            uint32_t xo[16];
+            tmem_ld16_async(tbase + lane_base + 128 * p + 64 + 16 * qq, xo);
+            tmem_wait_ld(); reg_fence(xo);
+            const int64_t stride = (int64_t)H * kD;
+            const int64_t at0 = ((c0 + 16 * qq) * H + h) * kD + row;
+            __nv_bfloat16* op = o + at0;
+            if (gate) {
+                const __nv_bfloat16* gp = gate + at0;
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (16 * qq + e < L) {
+                        const float gv = __bfloat162float(gp[e * stride]);
+                        op[e * stride] = __float2bfloat16_rn(scale * __uint_as_float(xo[e]) / (1.0f + __expf(-gv)));
+                    }
+            } else if (L == kC) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) op[e * stride] = __float2bfloat16_rn(scale * __uint_as_float(xo[e]));
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (16 * qq + e < L) op[e * stride] = __float2bfloat16_rn(scale * __uint_as_float(xo[e]));
+            }
+        };
+        if (lo < hi) write_state_operand();
+        int b = 0;
+        bool stopped = false;
+        for (int mm = lo; mm < hi; ++mm, b ^= 1) {
+            tc_fence_before();
+            nb_arrive(NB_S);
+            if (mm > lo) {  // the previous chunk's outputs while this chunk's S0 products run
+                nb_sync(NB_O);
+                tc_fence_after();
+                emit_o(mm - 1, b ^ 1);
+            }
+            nb_sync(NB_Y);
+            tc_fence_after();
+            if (*sAbort) {
+                stopped = true;
+                break;
+            }
+            // ---- V'^T = U^T - Y^T; thread (row, qq) owns tokens 16qq .. 16qq+15, stored to TMEM as bf16
+            //      hi and lo (x = hi + lo to about 16 bits)
+            {
+                uint32_t y[16];
+                tmem_ld16_async(tbase + lane_base + 128 * b + 16 * qq, y);
+                tmem_wait_ld(); reg_fence(y);
+                float hv[16], lv[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float x = sU[(16 * qq + e) * kD + row] - __uint_as_float(y[e]);
+                    hv[e] = __bfloat162float(__float2bfloat16_rn(x));
+                    lv[e] = x - hv[e];
+                }
+                uint32_t wh[8], wl[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    wh[j] = pack_bf16x2(hv[2 * j], hv[2 * j + 1]);
+                    wl[j] = pack_bf16x2(lv[2 * j], lv[2 * j + 1]);
+                }
+                tmem_st8(tbase + lane_base + TM_VH + 8 * qq, wh);
+                tmem_st8(tbase + lane_base + TM_VL + 8 * qq, wl);
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            nb_arrive(NB_V);
+            // ---- the state update
+            nb_sync(NB_D);
+            tc_fence_after();
+            {
+                const float* sEGl = reinterpret_cast<const float*>(sm + S_EGL + b * 512);
+                uint32_t d0[32];
+                tmem_ld32_async(tbase + lane_base + TM_DS + 32 * qq, d0);
+                float eg[32];
+#pragma unroll
+                for (int e4 = 0; e4 < 32; e4 += 4)
+                    *reinterpret_cast<float4*>(eg + e4) = *reinterpret_cast<const float4*>(sEGl + 32 * qq + e4);
+                tmem_wait_ld(); reg_fence(d0);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s[e] = fmaf(s[e], eg[e], __uint_as_float(d0[e]));
+            }
+            if (mm + 1 < hi) write_state_operand();
+        }
+        if (lo < hi && !stopped) {
+            nb_sync(NB_O);
+            tc_fence_after();
+            emit_o(hi - 1, (hi - 1 - lo) & 1);
+        }
     }
-    if (lo < hi && !*sAbort) emit_o(hi - 1, (hi - 1 - lo) & 1);
-
-    if (*sAbort && tid == kLoader) {  // let copies still in flight land (bounded) before the CTA exits
-        if ((iss ^ phB) & 1u) mbar_wait(barB, phB & 1u, kWaitLimit);
-        if ((iss ^ phB) & 2u) mbar_wait(barB + 1, (phB >> 1) & 1u, kWaitLimit);
-        if (((iss >> 2) ^ phU) & 1u) mbar_wait(barU, phU, kWaitLimit);
-        if (((iss >> 3) ^ phK) & 1u) mbar_wait(barK, phK, kWaitLimit);
-    }
+    tc_fence_before();
     __syncthreads();
-    if (s_out && !*sAbort) {
+    if (warp != kMmaWarp && s_out && !*sAbort) {
 #pragma unroll
         for (int j = 0; j < 32; j += 4)
             *reinterpret_cast<float4*>(s_out + out_off + j) = make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
     }
-    tc_fence_before();
-    __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, kTmemCols);
 }
 
