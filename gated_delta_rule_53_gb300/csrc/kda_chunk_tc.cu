@@ -272,33 +272,36 @@ __global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* __re
 // the current one's W and U are stored.
 // =============================================================================================
 constexpr int kPrepThreads = 256;
-constexpr uint32_t P_RR = 0;          // k (rows 0-63) and q (rows 64-127) land here by TMA in the layout of the row
-                                      // operand, two regions of 16 KB, and are scaled in place
-constexpr uint32_t P_G = 32768;       // g fp32, four TMA boxes of [64][32]; the running sum G in place
-constexpr uint32_t P_KG = 32768;      // then: K e^G (two regions of [64][64]), B (MN-major) of the W products
-constexpr uint32_t P_V = 49152;       // then: V by TMA (two regions of [64][64]), B (MN-major) of the U products
+// Two 32 KB regions trade roles from one item to the next (offsets rr and gb, 0 and 32768 in turn):
+//   rr: k (rows 0-63) and q (rows 64-127) land here by TMA in the layout of the row operand, two
+//       regions of 16 KB, and are scaled in place; after the A products, A_kk fp32 [64][kAS]
+//   gb: g fp32, four TMA boxes of [64][32]; the running sum G in place; then K e^G (two regions of
+//       [64][64]) and V by TMA (two regions at +16 KB): one MN-major B operand of N = 256 for W and U
+// The next item's g lands in this item's rr once the solve has consumed A_kk, its k and q in gb once the
+// W and U products are done.
 constexpr uint32_t P_CT = 65536;      // column operands of the four row blocks stacked: 160 rows (block J from
                                       // row 16 J (J+1) / 2), two regions of 160 x 128 bytes; block 3 is K e^{G_C - G}
 constexpr uint32_t kCTRegion = 160 * 128;
 constexpr uint32_t P_BETA = P_CT + 2 * kCTRegion;  // fp32 [64]
 constexpr uint32_t P_E = P_BETA + 256;     // fp32 [4][128]: G at the last token of each 16-token block
 constexpr uint32_t P_TOT = P_E + 2048;     // fp32 [128]: sum of the first 32 tokens
-constexpr uint32_t P_BAR = P_TOT + 512;    // mbarriers: k/q/g, v, A products, W/U products
-constexpr uint32_t P_MISC = P_BAR + 32;    // TMEM base, abort flag
+constexpr uint32_t P_BAR = P_TOT + 512;    // mbarriers: k/q, v, A products, W/U products, g
+constexpr uint32_t P_MISC = P_BAR + 40;    // TMEM base, abort flag
 constexpr uint32_t kPrepSmem = P_MISC + 16 + 1024;
-// After the A products complete (row and column operands free):
-constexpr uint32_t P_AKK = 0;                    // A_kk fp32 [64][kAS]
+// After the A products complete (column operands free):
 constexpr uint32_t P_TF = P_CT;                  // T fp32 [64][kAS]
 constexpr uint32_t P_NB = P_CT + 64 * kAS * 4;   // N blocks of the solve, 9 x [16][20] fp32
-// Once T is in registers: T Diag(beta) as bf16 hi and lo, A operands of 128 rows (the first 64 used)
-constexpr uint32_t P_TH = 0, P_TL = 16384;
+// Once T is in registers: T Diag(beta) as bf16 hi and lo, A operands of 128 rows (T twice, so that one
+// product of N = 256 over [K e^G | V] leaves W in lanes 0-63 and U in lanes 64-127)
+constexpr uint32_t P_TH = P_CT, P_TL = P_CT + 16384;
 constexpr uint32_t kPrepTmemCols = 256;
 // row block I of A: 16 (I + 1) columns from 16 I (I + 1) / 2 (one product of N = 160)
-constexpr uint32_t TM_W = 0, TM_U = 128;                            // then W and U (rows in lanes 0-63)
-constexpr uint32_t kKQGBytes = 4 * 8192 + 4 * 8192;
+// then [T ; T] [K e^G | V]: W = lanes 0-63 of columns 0-127, U = lanes 64-127 of columns 128-255
+constexpr uint32_t kKQBytes = 4 * 8192;
 constexpr uint32_t kGBytes = 4 * 8192;
 
-static_assert(P_AKK + 64 * kAS * 4 <= P_G && P_NB + 9 * 16 * kNB * 4 <= P_BETA, "solve work overflows its region");
+static_assert(64 * kAS * 4 <= 32768 && P_NB + 9 * 16 * kNB * 4 <= P_BETA && P_TL + 16384 <= P_BETA,
+              "solve work overflows its region");
 static_assert(2 * (kPrepSmem + 1024) <= 233472, "two prep CTAs per SM");
 
 // Raw front-end inputs of the fused prefill (unused otherwise).
@@ -339,6 +342,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     uint64_t* barV = barL + 1;
     uint64_t* barA = barL + 2;
     uint64_t* barW = barL + 3;
+    uint64_t* barG = barL + 4;
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + P_MISC);
     volatile int* sAbort = reinterpret_cast<volatile int*>(sm + P_MISC + 4);
 
@@ -359,25 +363,30 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         L = (eos - c0) < kC ? (int)(eos - c0) : kC;
         return true;
     };
-    // k, q (into the row-operand layout; unless FE), g and beta of an item
-    auto load_inputs = [&](int h, int64_t c0, int L) {
-        if (tid == 0) {
+    // Copies: issuing one takes its thread a few hundred cycles, so lane 0 of warps 0-3 issue one box each
+    // (a box that lands before thread 0's expect_tx only makes the transaction count negative for a while).
+    // g (into region gb) and beta of an item
+    auto load_g = [&](int h, int64_t c0, int L, uint32_t gb) {
+        if (tid == 0) mbar_arrive_expect_tx(barG, kGBytes);
+        if (lane == 0 && warp < 4) {
             fence_proxy_async();
-            mbar_arrive_expect_tx(barL, FE ? kGBytes : kKQGBytes);
-            if (!FE) {
-                tma_load_3d(sm + P_RR, &tm_k, 0, h, (int)c0, barL);             // k, channels 0-63  -> region 0 rows 0-63
-                tma_load_3d(sm + P_RR + 8192, &tm_q, 0, h, (int)c0, barL);      // q, channels 0-63  -> region 0 rows 64-127
-                tma_load_3d(sm + P_RR + 16384, &tm_k, 64, h, (int)c0, barL);    // k, channels 64-127 -> region 1
-                tma_load_3d(sm + P_RR + 24576, &tm_q, 64, h, (int)c0, barL);
-            }
-#pragma unroll
-            for (int b4 = 0; b4 < 4; ++b4) tma_load_3d(sm + P_G + b4 * 8192, &tm_g, 32 * b4, h, (int)c0, barL);
+            tma_load_3d(sm + gb + warp * 8192, &tm_g, 32 * warp, h, (int)c0, barG);
         }
         if (tid < kC) {
             const bool ok = tid < L;
             cp_async4(sBeta + tid, beta + (ok ? (c0 + tid) * H + h : 0), ok ? 4u : 0u);
         }
         cp_async_commit();
+    };
+    // k, q into region rr in the row-operand layout (FE computes them instead)
+    // box w: k (w even) or q (w odd), channels 64 (w / 2) ..; region w / 2, rows 0-63 (k) or 64-127 (q)
+    auto load_kq = [&](int h, int64_t c0, uint32_t rr) {
+        if (FE) return;
+        if (tid == 0) mbar_arrive_expect_tx(barL, kKQBytes);
+        if (lane == 0 && warp < 4) {
+            fence_proxy_async();
+            tma_load_3d(sm + rr + warp * 8192, (warp & 1) ? &tm_q : &tm_k, 64 * (warp >> 1), h, (int)c0, barL);
+        }
     };
     // FE: part p of the chunk's 64 tokens, through the front end, as bf16 into a 128-byte-swizzled operand
     // tile (two regions of `region` bytes; token i at row row0 + i).  Warp w takes tokens 8w .. 8w+7, lane
@@ -402,26 +411,36 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         mbar_init(barV, 1);
         mbar_init(barA, 1);
         mbar_init(barW, 1);
+        mbar_init(barG, 1);
         fence_mbar_init();
         *sAbort = 0;
     }
     if (warp == 0) tmem_alloc(sTmem, kPrepTmemCols);
     cta_sync_tc();
     const uint32_t tbase = *sTmem;
-    uint32_t pend = 0;  // thread 0: 1 = k/q/g loads in flight, 2 = v, 4 = A products, 8 = W/U products
+    // thread 0: 1 = k/q loads in flight, 2 = v, 4 = A products, 8 = W/U products, 16 = g
+    uint32_t pend = 0;
 
     int item = blockIdx.x, h = 0, L = 0;
     int64_t c0 = 0;
     bool have = locate(item, h, c0, L);
     if (have) {
-        load_inputs(h, c0, L);
-        if (tid == 0) pend |= 1u;
+        load_g(h, c0, L, 32768);
+        load_kq(h, c0, 0);
+        if (tid == 0) pend |= FE ? 16u : 17u;
     }
     for (uint32_t ph = 0; have; ph ^= 1u) {
+        const uint32_t P_RR = ph ? 32768u : 0u, P_G = 32768u - P_RR;  // this item's two regions
+        const uint32_t P_KG = P_G, P_V = P_G + 16384, P_AKK = P_RR;
         uint8_t* blob = blobs + (int64_t)item * kBlobBytes;
+        // the next item's place, early: its global reads complete while this item is worked on
+        const int next_item = item + gridDim.x;
+        int h1 = 0, L1 = 0;
+        int64_t c01 = 0;
+        const bool have_next = locate(next_item, h1, c01, L1);
         if (tid == 0) {
-            solo_wait(barL, ph, sAbort, err);
-            pend &= ~1u;
+            solo_wait(barG, ph, sAbort, err);
+            pend &= ~16u;
         }
         if (FE) {  // k and q into the row operand's space (free: the previous item's W/U products are done)
             frontend_tile(1, h, c0, P_RR, 16384, 0);
@@ -451,12 +470,16 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             sE[(2 * hh) * kD + c] = gv[15] + base;
             sE[(2 * hh + 1) * kD + c] = gv[31] + base;
             if (hh == 1) reinterpret_cast<float*>(blob + BLOB_EGL)[c] = exp2f(gv[31] + base);
+            if (!FE && tid == 0) {  // k and q before the operands are built
+                solo_wait(barL, ph, sAbort, err);
+                pend &= ~1u;
+            }
             __syncthreads();
         }
         // ---- operands.  Thread (cc, r4): channels 8cc .. 8cc+7 of rows i = r4 + 16 I (I = 0..3): the row
         // operand in place; Q e^G (workspace); column operands of blocks J >= I (KP also to the workspace);
         // K e^G, held until the running sum is no longer read.
-        const int cc = 2 * warp + (lane >> 4), r4 = lane & 15, c8 = 8 * cc;
+        const int cc = lane & 15, r4 = 2 * warp + (lane >> 4), c8 = 8 * cc;  // a warp: rows r4 + 16 I, r4 + 1 + 16 I
         const uint32_t reg = cc >> 3, ch = cc & 7;
         uint4 kg_hold[4];
         {
@@ -520,15 +543,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             mma_k128(tbase, kdesc(sbase + P_RR), 16384, kdesc(sbase + P_CT), kCTRegion,
                      idesc_bf16_f32(128, 160, false, false));
             mma_commit(barA);
-            if (tid == 0) {
-                pend |= 4u;
-                if (!FE) {
-                    fence_proxy_async();
-                    mbar_arrive_expect_tx(barV, 16384);
-                    tma_load_3d(sm + P_V, &tm_v, 0, h, (int)c0, barV);
-                    tma_load_3d(sm + P_V + 8192, &tm_v, 64, h, (int)c0, barV);
-                    pend |= 2u;
-                }
+            if (tid == 0) pend |= FE ? 4u : 6u;
+        }
+        if (!FE) {  // v into the second half of gb (the running sum is consumed)
+            if (tid == 0) mbar_arrive_expect_tx(barV, 16384);
+            if (lane == 0 && (warp == 1 || warp == 2)) {
+                fence_proxy_async();
+                tma_load_3d(sm + P_V + (warp - 1) * 8192, &tm_v, 64 * (warp - 1), h, (int)c0, barV);
             }
         }
 #pragma unroll
@@ -637,32 +658,39 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 float a8[8], b8[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) { a8[e] = hiv[8 * h8 + e]; b8[e] = lov[8 * h8 + e]; }
-                const uint32_t at = sw128(i, (j0 >> 3) + h8);
-                *reinterpret_cast<uint4*>(sm + P_TH + at) = pack8(a8);
-                *reinterpret_cast<uint4*>(sm + P_TL + at) = pack8(b8);
+                const uint32_t at = sw128(i, (j0 >> 3) + h8), at2 = sw128(64 + i, (j0 >> 3) + h8);
+                const uint4 hv = pack8(a8), lv = pack8(b8);
+                *reinterpret_cast<uint4*>(sm + P_TH + at) = hv;
+                *reinterpret_cast<uint4*>(sm + P_TH + at2) = hv;
+                *reinterpret_cast<uint4*>(sm + P_TL + at) = lv;
+                *reinterpret_cast<uint4*>(sm + P_TL + at2) = lv;
             }
         }
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
-        // ---- W = T Diag(beta) K e^G and U = T Diag(beta) V (rows of D in TMEM lanes 0-63)
+        // ---- the next item's g and beta: A_kk (this item's rr) and beta are consumed
+        const int this_item = item;
+        item = next_item;
+        have = have_next;
+        if (have) {
+            load_g(h1, c01, L1, P_RR);
+            if (tid == 0) pend |= 16u;
+        }
+        // ---- W = T Diag(beta) K e^G and U = T Diag(beta) V: [T ; T] [K e^G | V] (hi, then lo)
         if (warp == 0) {
             if (!FE) {
                 solo_wait(barV, ph, sAbort, err);
                 pend &= ~2u;
             }
             tc_fence_after();
-            const uint32_t id_w = idesc_bf16_f32(128, 128, false, true);
+            const uint32_t id_w = idesc_bf16_f32(128, 256, false, true);
             const uint64_t th = kdesc(sbase + P_TH), tl = kdesc(sbase + P_TL);
-            const uint64_t kgd = sdesc_sw128(sbase + P_KG, 8192, 1024), vd = sdesc_sw128(sbase + P_V, 8192, 1024);
+            const uint64_t kvd = sdesc_sw128(sbase + P_KG, 8192, 1024);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) mma_bf16(tbase + TM_W, th + ks * 2, kgd + ks * 128, id_w, ks > 0 ? 1u : 0u);
+            for (int ks = 0; ks < 4; ++ks) mma_bf16(tbase, th + ks * 2, kvd + ks * 128, id_w, ks > 0 ? 1u : 0u);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) mma_bf16(tbase + TM_W, tl + ks * 2, kgd + ks * 128, id_w, 1u);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) mma_bf16(tbase + TM_U, th + ks * 2, vd + ks * 128, id_w, ks > 0 ? 1u : 0u);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) mma_bf16(tbase + TM_U, tl + ks * 2, vd + ks * 128, id_w, 1u);
+            for (int ks = 0; ks < 4; ++ks) mma_bf16(tbase, tl + ks * 2, kvd + ks * 128, id_w, 1u);
             mma_commit(barW);
             pend |= 8u;
             solo_wait(barW, ph, sAbort, err);
@@ -670,41 +698,55 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         cta_sync_tc();
         if (*sAbort) break;
-        // ---- the next item's inputs land while W and U go out (every operand of this item is consumed)
-        const int this_item = item;
-        item += gridDim.x;
-        int h1 = 0, L1 = 0;
-        int64_t c01 = 0;
-        have = locate(item, h1, c01, L1);
+        // ---- the next item's k and q land in this item's gb while W and U go out
         if (have) {
-            load_inputs(h1, c01, L1);
-            if (tid == 0) pend |= 1u;
+            load_kq(h1, c01, P_G);
+            if (tid == 0 && !FE) pend |= 1u;
         }
-        // W (bf16, rows 0-63 of B1) by warps 0, 1; U (fp32 rows) by warps 4, 5
-        if ((warp & 2) == 0) {
+        // W (bf16, rows 0-63 of B1) from lanes 0-63, U (fp32 rows) from lanes 64-127; warps 0-3 take the
+        // first 64 columns of their rows, warps 4-7 the last 64.  Each warp stages its rows in 4 KB of the
+        // column-operand region (free: T hi/lo are consumed) and stores them back as whole rows.
+        {
             uint8_t* bl = blobs + (int64_t)this_item * kBlobBytes;
-            const int i = 32 * (warp & 1) + lane;
-            const uint32_t lane_base = (uint32_t)(32 * (warp & 1)) << 16;
+            const int q = warp & 3, hf = warp >> 2;
+            const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+            uint8_t* stg = sm + P_CT + warp * 4096;
+            if (q < 2) {  // W rows 32q + lane: one 128-byte row of region hf each, in the blob's swizzle
+                uint32_t x[32], y[32];
+                tmem_ld32_async(tbase + lane_base + 64 * hf, x);
+                tmem_ld32_async(tbase + lane_base + 64 * hf + 32, y);
+                tmem_wait_ld(); reg_fence(x); reg_fence(y);
 #pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                uint32_t x[32];
-                tmem_ld32_async(tbase + lane_base + (warp < 4 ? TM_W : TM_U) + 32 * p, x);
-                tmem_wait_ld(); reg_fence(x);
-                if (warp < 4) {
+                for (int c = 0; c < 8; ++c) {
+                    float f[8];
 #pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8) {
-                        float f[8];
+                    for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(c < 4 ? x[8 * c + e] : y[8 * (c - 4) + e]);
+                    *reinterpret_cast<uint4*>(stg + sw128(lane, c)) = pack8(f);
+                }
+                __syncwarp();
+                uint8_t* dst = bl + BLOB_B1 + hf * 16384 + 32 * q * 128;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(x[8 * q8 + e]);
-                        const int cch = 4 * p + q8;  // 16-byte chunk of the row: channels 8 cch ..
-                        *reinterpret_cast<uint4*>(bl + BLOB_B1 + (cch >> 3) * 16384 + sw128(i, cch & 7)) = pack8(f);
+                for (int k = 0; k < 8; ++k)
+                    *reinterpret_cast<uint4*>(dst + 512 * k + 16 * lane) =
+                        *reinterpret_cast<const uint4*>(stg + 512 * k + 16 * lane);
+            } else {  // U rows 32(q-2) + lane, fp32 columns 64hf .. +63, in two passes of 32
+                uint8_t* dst = bl + BLOB_U + (32 * (q - 2)) * 512 + 256 * hf;
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    uint32_t x[32];
+                    tmem_ld32_async(tbase + lane_base + 128 + 64 * hf + 32 * p, x);
+                    tmem_wait_ld(); reg_fence(x);
+                    if (p) __syncwarp();  // the first pass has been read back
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(stg + sw128(lane, c)) = make_uint4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
+                    __syncwarp();
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {  // rows 4k .. 4k+3, 128 bytes each
+                        const int r = 4 * k + (lane >> 3), c = lane & 7;
+                        *reinterpret_cast<uint4*>(dst + r * 512 + 128 * p + 16 * c) =
+                            *reinterpret_cast<const uint4*>(stg + sw128(r, c));
                     }
-                } else {
-                    float4* up = reinterpret_cast<float4*>(bl + BLOB_U + i * 512 + 128 * p);
-#pragma unroll
-                    for (int q4 = 0; q4 < 8; ++q4)
-                        up[q4] = make_float4(__uint_as_float(x[4 * q4]), __uint_as_float(x[4 * q4 + 1]),
-                                             __uint_as_float(x[4 * q4 + 2]), __uint_as_float(x[4 * q4 + 3]));
                 }
             }
         }
@@ -719,6 +761,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (pend & 2u) mbar_wait(barV, 0, kWaitLimit), mbar_wait(barV, 1, kWaitLimit);
         if (pend & 4u) mbar_wait(barA, 0, kWaitLimit), mbar_wait(barA, 1, kWaitLimit);
         if (pend & 8u) mbar_wait(barW, 0, kWaitLimit), mbar_wait(barW, 1, kWaitLimit);
+        if (pend & 16u) mbar_wait(barG, 0, kWaitLimit), mbar_wait(barG, 1, kWaitLimit);
     }
     tc_fence_before();
     __syncthreads();
@@ -737,23 +780,24 @@ constexpr int NB_Y = 2;  // MMA warp -> SIMT: [Y | O] of the chunk in TMEM, U in
 constexpr int NB_V = 3;  // SIMT -> MMA warp: V' hi and lo stored, U consumed
 constexpr int NB_D = 4;  // MMA warp -> SIMT: dS in TMEM
 constexpr int NB_O = 5;  // MMA warp -> SIMT: the chunk's output product complete
-constexpr uint32_t S_B1 = 0;            // [W ; Q e^G] of two chunks, 32 KB each
-constexpr uint32_t S_U = 65536;         // U fp32 [64][128]
-constexpr uint32_t S_AQ = 98304;        // A_qk bf16 hi, lo    } one copy
-constexpr uint32_t S_KP = 114688;       // K e^{G_C - G} bf16  }
-constexpr uint32_t S_EGL = 131072;      // e^{G_C} fp32 [128] of two chunks (copied with that chunk's B1)
-constexpr uint32_t S_BAR = 132096;      // mbarriers: B1 x2, U, A_qk/KP, S0 products, dS, output product
-constexpr uint32_t S_MISC = S_BAR + 64; // TMEM base, abort flag
-constexpr uint32_t kStateSmem = S_MISC + 64 + 1024;
+// Copies run ahead of their use: three B1 buffers, two of U and two of A_qk/KP, each chunk's data
+// issued two chunks before it is needed.
+constexpr uint32_t S_B1 = 0;            // [W ; Q e^G] of three chunks, 32 KB each
+constexpr uint32_t S_U = 98304;         // U fp32 [64][128] of two chunks
+constexpr uint32_t S_AQ = 163840;       // A_qk bf16 hi, lo (16 KB) then KP = K e^{G_C - G} bf16 (16 KB), two chunks
+constexpr uint32_t S_EGL = 229376;      // e^{G_C} fp32 [128] of three chunks (copied with that chunk's B1)
+constexpr uint32_t S_BAR = 230912;      // mbarriers: B1 x3, U x2, A_qk/KP x2, S0 products, dS, output product
+constexpr uint32_t S_MISC = S_BAR + 128; // TMEM base, abort flag
+constexpr uint32_t kStateSmem = S_MISC + 16 + 1008;
 constexpr uint32_t kAQKBytes = BLOB_EGL - BLOB_AQ;
+constexpr uint32_t kKPOff = BLOB_KP - BLOB_AQ;
 // TMEM columns: S0 products of chunk parity p at 128 p (Y^T in 64 columns, then O^T in 64); dS at 256;
 // the A operands of the products, bf16 packed two per column: S0 at 384 (64 columns), V'^T hi at 448
 // and V'^T lo at 480 (32 columns each)
 constexpr uint32_t TM_DS = 256, TM_SA = 384, TM_VH = 448, TM_VL = 480;
 constexpr uint32_t kTmemCols = 512;
 
-static_assert(S_KP - S_AQ == BLOB_KP - BLOB_AQ, "copy layout");
-static_assert(S_AQ % 1024 == 0 && S_KP % 1024 == 0 && S_EGL + 1024 <= S_BAR, "alignment");
+static_assert(kKPOff % 1024 == 0 && S_AQ % 1024 == 0 && S_U % 1024 == 0 && S_EGL + 1536 <= S_BAR, "alignment");
 static_assert(kStateSmem <= 232448, "shared memory");
 
 __device__ __forceinline__ void nb_sync(int id) { asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kThreads) : "memory"); }
@@ -791,17 +835,17 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
     int64_t bos, eos;
     seq_bounds(cu, n, T_total, bos, eos);
 
-    uint64_t* barB = reinterpret_cast<uint64_t*>(sm + S_BAR);  // [2] B1 and e^{G_C}
-    uint64_t* barU = barB + 2;
-    uint64_t* barK = barB + 3;
-    uint64_t* barM = barB + 4;
-    uint64_t* barD = barB + 5;
-    uint64_t* barO = barB + 6;
+    uint64_t* barB = reinterpret_cast<uint64_t*>(sm + S_BAR);  // [3] B1 and e^{G_C}
+    uint64_t* barU = barB + 3;                                 // [2]
+    uint64_t* barK = barB + 5;                                 // [2] A_qk and KP
+    uint64_t* barM = barB + 7;
+    uint64_t* barD = barB + 8;
+    uint64_t* barO = barB + 9;
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + S_MISC);
     volatile int* sAbort = reinterpret_cast<volatile int*>(sm + S_MISC + 4);
 
     if (tid == 0) {
-        for (int i = 0; i < 7; ++i) mbar_init(barB + i, 1);
+        for (int i = 0; i < 10; ++i) mbar_init(barB + i, 1);
         fence_mbar_init();
         *sAbort = 0;
     }
@@ -815,114 +859,117 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
     if (warp == kMmaWarp) {
         // ======== products and copies: one warp, MMAs from an elected lane, copies from lane 0 ========
         auto blob_of = [&](int mm) { return blobs + ((int64_t)(mm - m0) * H + h) * kBlobBytes; };
-        uint32_t iss = 0;  // a bit flips per copy issued (B1 buffer b: bit b, U: 4, A_qk/KP: 8)
-        auto load_b1 = [&](int mm, int b) {
+        // a bit flips per copy issued, as the phase bits flip per copy consumed: B1 buffers bits 0-2,
+        // U buffers bits 3-4, A_qk/KP buffers bits 5-6
+        uint32_t iss = 0;
+        auto load_b1 = [&](int mm, int j) {
             if (lane == 0) {
                 fence_proxy_async();
-                mbar_arrive_expect_tx(barB + b, 32768 + 512);
-                bulk_load(sm + S_B1 + b * 32768, blob_of(mm) + BLOB_B1, 32768, barB + b);
-                bulk_load(sm + S_EGL + b * 512, blob_of(mm) + BLOB_EGL, 512, barB + b);
+                mbar_arrive_expect_tx(barB + j, 32768 + 512);
+                bulk_load(sm + S_B1 + j * 32768, blob_of(mm) + BLOB_B1, 32768, barB + j);
+                bulk_load(sm + S_EGL + j * 512, blob_of(mm) + BLOB_EGL, 512, barB + j);
             }
             __syncwarp();
-            iss ^= 1u << b;
+            iss ^= 1u << j;
         };
-        auto load_u = [&](int mm) {
+        auto load_u = [&](int mm, int j) {
             if (lane == 0) {
                 fence_proxy_async();
-                mbar_arrive_expect_tx(barU, 32768);
-                bulk_load(sm + S_U, blob_of(mm) + BLOB_U, 32768, barU);
+                mbar_arrive_expect_tx(barU + j, 32768);
+                bulk_load(sm + S_U + j * 32768, blob_of(mm) + BLOB_U, 32768, barU + j);
             }
             __syncwarp();
-            iss ^= 4u;
+            iss ^= 8u << j;
         };
-        auto load_aq = [&](int mm) {
+        auto load_aq = [&](int mm, int j) {
             if (lane == 0) {
                 fence_proxy_async();
-                mbar_arrive_expect_tx(barK, kAQKBytes);
-                bulk_load(sm + S_AQ, blob_of(mm) + BLOB_AQ, kAQKBytes, barK);
+                mbar_arrive_expect_tx(barK + j, kAQKBytes);
+                bulk_load(sm + S_AQ + j * 32768, blob_of(mm) + BLOB_AQ, kAQKBytes, barK + j);
             }
             __syncwarp();
-            iss ^= 8u;
+            iss ^= 32u << j;
         };
         auto wait = [&](uint64_t* bar, uint32_t ph) { solo_wait(bar, ph, sAbort, err); };
         const uint32_t id_64 = idesc_bf16_f32(128, 64, false, false);
         const uint32_t id_ds = idesc_bf16_f32(128, 128, false, true);
-        uint32_t phB = 0, phU = 0, phK = 0, phM = 0, phD = 0, phO = 0;  // phB: bit b = phase of B1 buffer b
-        if (lo < hi) {
-            load_b1(lo, 0);
-            load_u(lo);
-            load_aq(lo);
+        uint32_t ph = 0;              // bit per buffer barrier, as iss
+        uint32_t phM = 0, phD = 0, phO = 0;
+        for (int i = 0; i < 2 && lo + i < hi; ++i) {
+            load_b1(lo + i, i);
+            load_u(lo + i, i);
+            load_aq(lo + i, i);
         }
-        int b = 0;
-        for (int mm = lo; mm < hi; ++mm, b ^= 1) {
-            const bool next = mm + 1 < hi;
+        int b = 0, b3 = 0;  // TMEM [Y | O] buffer and B1 buffer of this chunk; U and A_qk/KP buffers follow b
+        for (int mm = lo; mm < hi; ++mm, b ^= 1, b3 = b3 == 2 ? 0 : b3 + 1) {
+            const bool ahead = mm + 2 < hi;
             // ---- Y^T = S0 W^T (the V' pass waits for it), then O^T = S0 (Q e^G)^T; A = S0 from TMEM
             nb_sync(NB_S);
-            wait(barB + b, (phB >> b) & 1u);
-            phB ^= 1u << b;
+            wait(barB + b3, (ph >> b3) & 1u);
+            ph ^= 1u << b3;
             tc_fence_after();
-            const uint32_t b1 = sbase + S_B1 + b * 32768;
+            const uint32_t b1 = sbase + S_B1 + b3 * 32768;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
                 mma_bf16_ta(tbase + 128 * b, tbase + TM_SA + 8 * ks,
                             kdesc(b1 + (ks >> 2) * 16384) + (ks & 3) * 2, id_64, ks > 0 ? 1u : 0u);
             mma_commit(barM);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                mma_bf16_ta(tbase + 128 * b + 64, tbase + TM_SA + 8 * ks,
-                            kdesc(b1 + (ks >> 2) * 16384 + 8192) + (ks & 3) * 2, id_64, ks > 0 ? 1u : 0u);
             wait(barM, phM);
             phM ^= 1u;
-            wait(barU, phU);
-            phU ^= 1u;
+            wait(barU + b, (ph >> (3 + b)) & 1u);
+            ph ^= 8u << b;
             const bool stop = *sAbort != 0;
             tc_fence_before();
             nb_arrive(NB_Y);
             if (stop) break;
-            if (next) load_b1(mm + 1, b ^ 1);  // the previous chunk's B1 and e^{G_C} are consumed
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+                mma_bf16_ta(tbase + 128 * b + 64, tbase + TM_SA + 8 * ks,
+                            kdesc(b1 + (ks >> 2) * 16384 + 8192) + (ks & 3) * 2, id_64, ks > 0 ? 1u : 0u);
+            if (ahead) load_b1(mm + 2, b3 == 0 ? 2 : b3 - 1);  // the previous chunk's B1 and e^{G_C} are consumed
             // ---- dS = V'^T (K e^{G_C - G}) (the state waits for it), then O^T += V'^T A_qk^T as
             //      hi.hi + hi.lo + lo.hi; A = V'^T from TMEM
             nb_sync(NB_V);
-            wait(barK, phK);
-            phK ^= 1u;
+            wait(barK + b, (ph >> (5 + b)) & 1u);
+            ph ^= 32u << b;
             tc_fence_after();
+            const uint32_t aq = sbase + S_AQ + b * 32768;
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                mma_bf16_ta(tbase + TM_DS, tbase + TM_VH + 8 * ks, sdesc_sw128(sbase + S_KP, 8192, 1024) + ks * 128,
+                mma_bf16_ta(tbase + TM_DS, tbase + TM_VH + 8 * ks, sdesc_sw128(aq + kKPOff, 8192, 1024) + ks * 128,
                             id_ds, ks > 0 ? 1u : 0u);
             mma_commit(barD);
             wait(barD, phD);
             phD ^= 1u;
             tc_fence_before();
             nb_arrive(NB_D);
-            if (next) load_u(mm + 1);  // every thread has read U
+            if (ahead) load_u(mm + 2, b);  // every thread has read this chunk's U
             const uint32_t od = tbase + 128 * b + 64;
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16_ta(od, tbase + TM_VH + 8 * ks, kdesc(sbase + S_AQ) + ks * 2, id_64, 1u);
+            for (int ks = 0; ks < 4; ++ks) mma_bf16_ta(od, tbase + TM_VH + 8 * ks, kdesc(aq) + ks * 2, id_64, 1u);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                mma_bf16_ta(od, tbase + TM_VH + 8 * ks, kdesc(sbase + S_AQ + 8192) + ks * 2, id_64, 1u);
+                mma_bf16_ta(od, tbase + TM_VH + 8 * ks, kdesc(aq + 8192) + ks * 2, id_64, 1u);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                mma_bf16_ta(od, tbase + TM_VL + 8 * ks, kdesc(sbase + S_AQ) + ks * 2, id_64, 1u);
+            for (int ks = 0; ks < 4; ++ks) mma_bf16_ta(od, tbase + TM_VL + 8 * ks, kdesc(aq) + ks * 2, id_64, 1u);
             mma_commit(barO);
             wait(barO, phO);
             phO ^= 1u;
-            if (next) load_aq(mm + 1);  // A_qk and KP of this chunk are consumed
+            if (ahead) load_aq(mm + 2, b);  // A_qk and KP of this chunk are consumed
             tc_fence_before();
             nb_arrive(NB_O);
         }
         if (*sAbort && lane == 0) {  // let copies still in flight land (bounded) before the CTA exits
-            if ((iss ^ phB) & 1u) mbar_wait(barB, phB & 1u, kWaitLimit);
-            if ((iss ^ phB) & 2u) mbar_wait(barB + 1, (phB >> 1) & 1u, kWaitLimit);
-            if (((iss >> 2) ^ phU) & 1u) mbar_wait(barU, phU, kWaitLimit);
-            if (((iss >> 3) ^ phK) & 1u) mbar_wait(barK, phK, kWaitLimit);
+            for (int j = 0; j < 3; ++j)
+                if (((iss ^ ph) >> j) & 1u) mbar_wait(barB + j, (ph >> j) & 1u, kWaitLimit);
+            for (int j = 0; j < 2; ++j) {
+                if (((iss ^ ph) >> (3 + j)) & 1u) mbar_wait(barU + j, (ph >> (3 + j)) & 1u, kWaitLimit);
+                if (((iss ^ ph) >> (5 + j)) & 1u) mbar_wait(barK + j, (ph >> (5 + j)) & 1u, kWaitLimit);
+            }
         }
         __syncwarp();
     } else {
         // ======== the state: thread (row, qq) holds row `row`, key channels [32 qq, 32 qq + 32) ========
-        const float* sU = reinterpret_cast<const float*>(sm + S_U);
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
             float4 x = s_in ? *reinterpret_cast<const float4*>(s_in + in_off + j) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -936,43 +983,46 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
             tmem_wait_st();
         };
         // outputs of chunk mm (its product complete, in TMEM columns 128 p + 64): thread (row, qq) stores
-        // tokens 16qq .. 16qq+15 of value row `row`; a warp writes 64 contiguous bytes per token
-        auto emit_o = [&](int mm, int p) {
+        // tokens 16qq + 8 half .. + 7 of value row `row`; a warp writes 64 contiguous bytes per token.  The
+        // two halves go out while the products of the next chunk run.
+        auto emit_o = [&](int mm, int p, int half) {
             const int64_t c0 = bos + (int64_t)kC * (mm - on);
             const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
-            uint32_t xo[16];
-            tmem_ld16_async(tbase + lane_base + 128 * p + 64 + 16 * qq, xo);
+            const int t0 = 16 * qq + 8 * half;
+            uint32_t xo[8];
+            tmem_ld8_async(tbase + lane_base + 128 * p + 64 + t0, xo);
             tmem_wait_ld(); reg_fence(xo);
             const int64_t stride = (int64_t)H * kD;
-            const int64_t at0 = ((c0 + 16 * qq) * H + h) * kD + row;
+            const int64_t at0 = ((c0 + t0) * H + h) * kD + row;
             __nv_bfloat16* op = o + at0;
             if (gate) {
                 const __nv_bfloat16* gp = gate + at0;
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    if (16 * qq + e < L) {
+                for (int e = 0; e < 8; ++e)
+                    if (t0 + e < L) {
                         const float gv = __bfloat162float(gp[e * stride]);
                         op[e * stride] = __float2bfloat16_rn(scale * __uint_as_float(xo[e]) / (1.0f + __expf(-gv)));
                     }
             } else if (L == kC) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) op[e * stride] = __float2bfloat16_rn(scale * __uint_as_float(xo[e]));
+                for (int e = 0; e < 8; ++e) op[e * stride] = __float2bfloat16_rn(scale * __uint_as_float(xo[e]));
             } else {
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    if (16 * qq + e < L) op[e * stride] = __float2bfloat16_rn(scale * __uint_as_float(xo[e]));
+                for (int e = 0; e < 8; ++e)
+                    if (t0 + e < L) op[e * stride] = __float2bfloat16_rn(scale * __uint_as_float(xo[e]));
             }
         };
         if (lo < hi) write_state_operand();
-        int b = 0;
+        int b = 0, b3 = 0;
         bool stopped = false;
-        for (int mm = lo; mm < hi; ++mm, b ^= 1) {
+        for (int mm = lo; mm < hi; ++mm, b ^= 1, b3 = b3 == 2 ? 0 : b3 + 1) {
+            const float* sU = reinterpret_cast<const float*>(sm + S_U + b * 32768);
             tc_fence_before();
             nb_arrive(NB_S);
-            if (mm > lo) {  // the previous chunk's outputs while this chunk's S0 products run
+            if (mm > lo) {  // the previous chunk's outputs, first half, while this chunk's S0 products run
                 nb_sync(NB_O);
                 tc_fence_after();
-                emit_o(mm - 1, b ^ 1);
+                emit_o(mm - 1, b ^ 1, 0);
             }
             nb_sync(NB_Y);
             tc_fence_after();
@@ -1005,11 +1055,12 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
             }
             tc_fence_before();
             nb_arrive(NB_V);
+            if (mm > lo) emit_o(mm - 1, b ^ 1, 1);  // second half while dS runs
             // ---- the state update
             nb_sync(NB_D);
             tc_fence_after();
             {
-                const float* sEGl = reinterpret_cast<const float*>(sm + S_EGL + b * 512);
+                const float* sEGl = reinterpret_cast<const float*>(sm + S_EGL + b3 * 512);
                 uint32_t d0[32];
                 tmem_ld32_async(tbase + lane_base + TM_DS + 32 * qq, d0);
                 float eg[32];
@@ -1025,7 +1076,8 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
         if (lo < hi && !stopped) {
             nb_sync(NB_O);
             tc_fence_after();
-            emit_o(hi - 1, (hi - 1 - lo) & 1);
+            emit_o(hi - 1, (hi - 1 - lo) & 1, 0);
+            emit_o(hi - 1, (hi - 1 - lo) & 1, 1);
         }
     }
     tc_fence_before();
