@@ -117,91 +117,94 @@ __device__ __forceinline__ void mma_k128(uint32_t d, uint64_t a_desc, uint32_t a
 __device__ __forceinline__ uint64_t kdesc(uint32_t saddr) { return sdesc_sw128(saddr, 16, 1024); }
 
 // One 16 x 16 fp32 block product for 32 threads; thread t owns rows 2 (t / 4) and 2 (t / 4) + 1, columns
-// 4 (t % 4) .. +3:   out = sign * (A0 + w1 A1 + w2 A2) B  [+ A3 B3]
-// NA = number of A blocks combined on the fly (an entry of P = -N + N^2 - N^3); SECOND adds A3 B3.
-struct Blk {
-    const float* p;
-    int ld;
+// 4 (t % 4) .. +3:   out = sign * ((A0 + w1 A1) B + A3 B3), the A1 and A3 B3 terms optional.  One routine
+// with run-time operands serves every block of the solve (one copy of the code).
+struct BlkJob {
+    const float* a0; const float* a1; const float* b; const float* a3; const float* b3;
+    float* out;
+    int lda0, lda1, ldb, lda3, ldb3, ldo;
+    float w1, sign;
 };
-template <int NA>
-__device__ __forceinline__ void load_rows(float (&av)[2][16], Blk a0, Blk a1, float w1, Blk a2, float w2, int r0) {
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-        for (int m = 0; m < 16; m += 4) {
-            float4 x = *reinterpret_cast<const float4*>(a0.p + (r0 + rr) * a0.ld + m);
-            if (NA > 1) {
-                const float4 y = *reinterpret_cast<const float4*>(a1.p + (r0 + rr) * a1.ld + m);
-                x.x = fmaf(w1, y.x, x.x); x.y = fmaf(w1, y.y, x.y); x.z = fmaf(w1, y.z, x.z); x.w = fmaf(w1, y.w, x.w);
-            }
-            if (NA > 2) {
-                const float4 y = *reinterpret_cast<const float4*>(a2.p + (r0 + rr) * a2.ld + m);
-                x.x = fmaf(w2, y.x, x.x); x.y = fmaf(w2, y.y, x.y); x.z = fmaf(w2, y.z, x.z); x.w = fmaf(w2, y.w, x.w);
-            }
-            av[rr][m] = x.x; av[rr][m + 1] = x.y; av[rr][m + 2] = x.z; av[rr][m + 3] = x.w;
-        }
-}
-__device__ __forceinline__ void acc_rows(float (&acc)[2][4], const float (&av)[2][16], Blk b, int c) {
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-        const float4 bv = *reinterpret_cast<const float4*>(b.p + m * b.ld + c);
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-            acc[rr][0] = fmaf(av[rr][m], bv.x, acc[rr][0]); acc[rr][1] = fmaf(av[rr][m], bv.y, acc[rr][1]);
-            acc[rr][2] = fmaf(av[rr][m], bv.z, acc[rr][2]); acc[rr][3] = fmaf(av[rr][m], bv.w, acc[rr][3]);
-        }
-    }
-}
-template <int NA, bool SECOND>
-__device__ __forceinline__ void blk_mma(float* out, int ldo, float sign, Blk a0, Blk a1, float w1, Blk a2, float w2,
-                                        Blk b, Blk a3, Blk b3, int t) {
+__device__ __noinline__ void blk_job(BlkJob j, int t) {
     const int r0 = 2 * (t >> 2), c = 4 * (t & 3);
-    float av[2][16], acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    load_rows<NA>(av, a0, a1, w1, a2, w2, r0);
-    acc_rows(acc, av, b, c);
-    if (SECOND) {
-        load_rows<1>(av, a3, a3, 0.f, a3, 0.f, r0);
-        acc_rows(acc, av, b3, c);
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+        const float* a = pass ? j.a3 : j.a0;
+        if (!a) break;
+        const int lda = pass ? j.lda3 : j.lda0;
+        const float* bp = pass ? j.b3 : j.b;
+        const int ldb = pass ? j.ldb3 : j.ldb;
+        const float* a1 = pass ? nullptr : j.a1;
+        float av[2][16];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+            for (int m = 0; m < 16; m += 4) {
+                float4 x = *reinterpret_cast<const float4*>(a + (r0 + rr) * lda + m);
+                if (a1) {
+                    const float4 y = *reinterpret_cast<const float4*>(a1 + (r0 + rr) * j.lda1 + m);
+                    x.x = fmaf(j.w1, y.x, x.x); x.y = fmaf(j.w1, y.y, x.y);
+                    x.z = fmaf(j.w1, y.z, x.z); x.w = fmaf(j.w1, y.w, x.w);
+                }
+                av[rr][m] = x.x; av[rr][m + 1] = x.y; av[rr][m + 2] = x.z; av[rr][m + 3] = x.w;
+            }
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const float4 bv = *reinterpret_cast<const float4*>(bp + m * ldb + c);
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                acc[rr][0] = fmaf(av[rr][m], bv.x, acc[rr][0]); acc[rr][1] = fmaf(av[rr][m], bv.y, acc[rr][1]);
+                acc[rr][2] = fmaf(av[rr][m], bv.z, acc[rr][2]); acc[rr][3] = fmaf(av[rr][m], bv.w, acc[rr][3]);
+            }
+        }
     }
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr)
-        *reinterpret_cast<float4*>(out + (r0 + rr) * ldo + c) =
-            make_float4(sign * acc[rr][0], sign * acc[rr][1], sign * acc[rr][2], sign * acc[rr][3]);
+        *reinterpret_cast<float4*>(j.out + (r0 + rr) * j.ldo + c) =
+            make_float4(j.sign * acc[rr][0], j.sign * acc[rr][1], j.sign * acc[rr][2], j.sign * acc[rr][3]);
 }
 
 // Blocks of T below the diagonal.  With D = diag(T_00 .. T_33) (inverses of the diagonal blocks of
 // I + A_kk) and N = D A_off (A_off: the blocks of A_kk below the diagonal; N is strictly block-lower,
 // so N^4 = 0):  (I + A_kk)^-1 = (I + N)^-1 D = (I - N + N^2 - N^3) D.
-// Three rounds of independent 16 x 16 products, 32 threads each.
+// Three rounds of independent 16 x 16 products, one warp each.
 constexpr int kNB = 20;  // row stride of the N blocks (float4 rows, eight rows on distinct banks)
 __device__ __forceinline__ void t_offdiag(const float* A, float* T, float* nb, int tid) {
-    auto Ablk = [&](int I, int J) { return Blk{A + 16 * I * kAS + 16 * J, kAS}; };
-    auto Tblk = [&](int I, int J) { return Blk{T + 16 * I * kAS + 16 * J, kAS}; };
+    auto Ab = [&](int I, int J) { return A + 16 * I * kAS + 16 * J; };
+    auto Tb = [&](int I, int J) { return T + 16 * I * kAS + 16 * J; };
     // N_IJ at nb[slot]: (1,0) 0, (2,0) 1, (3,0) 2, (2,1) 3, (3,1) 4, (3,2) 5; N^2: (2,0) 6, (3,1) 7, (3,0) 8
-    auto Nb = [&](int slot) { return Blk{nb + slot * 16 * kNB, kNB}; };
-    const Blk none{nullptr, 0};
+    auto Nb = [&](int slot) { return nb + slot * 16 * kNB; };
     const int u = tid >> 5, t = tid & 31;
+    BlkJob j{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, kAS, kNB, kAS, kNB, kAS, kAS, 0.f, 1.f};
     if (u < 6) {  // N blocks: (1,0) (2,0) (3,0) (2,1) (3,1) (3,2)
         const int I = u < 3 ? u + 1 : (u < 5 ? u - 1 : 3), J = u < 3 ? 0 : (u < 5 ? 1 : 2);
-        blk_mma<1, false>(nb + u * 16 * kNB, kNB, 1.f, Tblk(I, I), none, 0.f, none, 0.f, Ablk(I, J), none, none, t);
+        j.a0 = Tb(I, I); j.b = Ab(I, J); j.out = Nb(u); j.ldo = kNB;
+        blk_job(j, t);
     }
     __syncthreads();
-    switch (u) {
-        case 0: blk_mma<1, false>(nb + 6 * 16 * kNB, kNB, 1.f, Nb(3), none, 0.f, none, 0.f, Nb(0), none, none, t); break;  // N21 N10
-        case 1: blk_mma<1, false>(nb + 7 * 16 * kNB, kNB, 1.f, Nb(5), none, 0.f, none, 0.f, Nb(3), none, none, t); break;  // N32 N21
-        case 2: blk_mma<1, true>(nb + 8 * 16 * kNB, kNB, 1.f, Nb(4), none, 0.f, none, 0.f, Nb(0), Nb(5), Nb(1), t); break; // N31 N10 + N32 N20
-        case 3: blk_mma<1, false>(T + 16 * kAS * 1 + 0, kAS, -1.f, Nb(0), none, 0.f, none, 0.f, Tblk(0, 0), none, none, t); break;   // T10
-        case 4: blk_mma<1, false>(T + 16 * kAS * 2 + 16, kAS, -1.f, Nb(3), none, 0.f, none, 0.f, Tblk(1, 1), none, none, t); break;  // T21
-        case 5: blk_mma<1, false>(T + 16 * kAS * 3 + 32, kAS, -1.f, Nb(5), none, 0.f, none, 0.f, Tblk(2, 2), none, none, t); break;  // T32
-        default: break;
+    if (u < 6) {
+        j = BlkJob{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, kNB, kNB, kNB, kNB, kNB, kNB, 0.f, 1.f};
+        switch (u) {
+            case 0: j.a0 = Nb(3); j.b = Nb(0); j.out = Nb(6); break;                            // N21 N10
+            case 1: j.a0 = Nb(5); j.b = Nb(3); j.out = Nb(7); break;                            // N32 N21
+            case 2: j.a0 = Nb(4); j.b = Nb(0); j.a3 = Nb(5); j.b3 = Nb(1); j.out = Nb(8); break; // N31 N10 + N32 N20
+            case 3: j.a0 = Nb(0); j.b = Tb(0, 0); j.ldb = kAS; j.out = Tb(1, 0); j.ldo = kAS; j.sign = -1.f; break;  // T10
+            case 4: j.a0 = Nb(3); j.b = Tb(1, 1); j.ldb = kAS; j.out = Tb(2, 1); j.ldo = kAS; j.sign = -1.f; break;  // T21
+            default: j.a0 = Nb(5); j.b = Tb(2, 2); j.ldb = kAS; j.out = Tb(3, 2); j.ldo = kAS; j.sign = -1.f; break; // T32
+        }
+        blk_job(j, t);
     }
     __syncthreads();
     // T_30 = (N^2_30 - N_30 - N^3_30) D_0 with N^3_30 D_0 = N^2_31 N_10 D_0 = -N^2_31 T_10
-    switch (u) {
-        case 0: blk_mma<2, true>(T + 16 * kAS * 3 + 0, kAS, 1.f, Nb(8), Nb(2), -1.f, none, 0.f, Tblk(0, 0), Nb(7), Tblk(1, 0), t); break;
-        case 1: blk_mma<2, false>(T + 16 * kAS * 2 + 0, kAS, 1.f, Nb(6), Nb(1), -1.f, none, 0.f, Tblk(0, 0), none, none, t); break;  // T20
-        case 2: blk_mma<2, false>(T + 16 * kAS * 3 + 16, kAS, 1.f, Nb(7), Nb(4), -1.f, none, 0.f, Tblk(1, 1), none, none, t); break; // T31
-        default: break;
+    if (u < 3) {
+        j = BlkJob{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, kNB, kNB, kAS, kNB, kAS, kAS, -1.f, 1.f};
+        switch (u) {
+            case 0: j.a0 = Nb(8); j.a1 = Nb(2); j.b = Tb(0, 0); j.a3 = Nb(7); j.b3 = Tb(1, 0); j.out = Tb(3, 0); break;
+            case 1: j.a0 = Nb(6); j.a1 = Nb(1); j.b = Tb(0, 0); j.out = Tb(2, 0); break;  // T20
+            default: j.a0 = Nb(7); j.a1 = Nb(4); j.b = Tb(1, 1); j.out = Tb(3, 1); break; // T31
+        }
+        blk_job(j, t);
     }
     __syncthreads();
 }
@@ -291,6 +294,7 @@ constexpr uint32_t kPrepSmem = P_MISC + 16 + 1024;
 // After the A products complete (column operands free):
 constexpr uint32_t P_TF = P_CT;                  // T fp32 [64][kAS]
 constexpr uint32_t P_NB = P_CT + 64 * kAS * 4;   // N blocks of the solve, 9 x [16][20] fp32
+constexpr uint32_t P_AQS = P_NB;                 // before them: A_qk hi, lo staged in the workspace layout (16 KB)
 // Once T is in registers: T Diag(beta) as bf16 hi and lo, A operands of 128 rows (T twice, so that one
 // product of N = 256 over [K e^G | V] leaves W in lanes 0-63 and U in lanes 64-127)
 constexpr uint32_t P_TH = P_CT, P_TL = P_CT + 16384;
@@ -300,7 +304,8 @@ constexpr uint32_t kPrepTmemCols = 256;
 constexpr uint32_t kKQBytes = 4 * 8192;
 constexpr uint32_t kGBytes = 4 * 8192;
 
-static_assert(64 * kAS * 4 <= 32768 && P_NB + 9 * 16 * kNB * 4 <= P_BETA && P_TL + 16384 <= P_BETA,
+static_assert(64 * kAS * 4 <= 32768 && P_NB + 9 * 16 * kNB * 4 <= P_BETA && P_TL + 16384 <= P_BETA &&
+                  P_AQS + 16384 <= P_BETA && P_AQS % 128 == 0,
               "solve work overflows its region");
 static_assert(2 * (kPrepSmem + 1024) <= 233472, "two prep CTAs per SM");
 
@@ -611,14 +616,21 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                             fh[e] = __bfloat162float(__float2bfloat16_rn(x));
                             fl[e] = x - fh[e];
                         }
-                        *reinterpret_cast<uint4*>(blob + BLOB_AQ + sw128(i, c8)) = pack8(fh);
-                        *reinterpret_cast<uint4*>(blob + BLOB_AQ + 8192 + sw128(i, c8)) = pack8(fl);
+                        *reinterpret_cast<uint4*>(sm + P_AQS + sw128(i, c8)) = pack8(fh);
+                        *reinterpret_cast<uint4*>(sm + P_AQS + 8192 + sw128(i, c8)) = pack8(fl);
                     }
                 }
             }
         }
         __syncthreads();
-        // ---- T = (I + A_kk)^-1 by 16 x 16 blocks (fp32)
+        // ---- T = (I + A_kk)^-1 by 16 x 16 blocks (fp32); meanwhile warps 4-7 copy A_qk out as whole rows
+        if (warp >= 4) {
+            const int t = tid - 128;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                *reinterpret_cast<uint4*>(blob + BLOB_AQ + 2048 * k + 16 * t) =
+                    *reinterpret_cast<const uint4*>(sm + P_AQS + 2048 * k + 16 * t);
+        }
         if (lane < 16 && warp < 4) {  // diagonal block `warp`, column `lane`, right-looking (independent updates)
             const int I = warp, cl = lane;
             const float* A = sAkk + 16 * I * kAS + 16 * I;
