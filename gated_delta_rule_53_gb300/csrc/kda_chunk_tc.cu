@@ -1031,10 +1031,9 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
             const float* sU = reinterpret_cast<const float*>(sm + S_U + b * 32768);
             tc_fence_before();
             nb_arrive(NB_S);
-            if (mm > lo) {  // the previous chunk's outputs, first half, while this chunk's S0 products run
+            if (mm > lo) {  // the previous chunk's output product is complete
                 nb_sync(NB_O);
                 tc_fence_after();
-                emit_o(mm - 1, b ^ 1, 0);
             }
             nb_sync(NB_Y);
             tc_fence_after();
@@ -1067,7 +1066,10 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
             }
             tc_fence_before();
             nb_arrive(NB_V);
-            if (mm > lo) emit_o(mm - 1, b ^ 1, 1);  // second half while dS runs
+            if (mm > lo) {  // the previous chunk's outputs while dS runs
+                emit_o(mm - 1, b ^ 1, 0);
+                emit_o(mm - 1, b ^ 1, 1);
+            }
             // ---- the state update
             nb_sync(NB_D);
             tc_fence_after();
