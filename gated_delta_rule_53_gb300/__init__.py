@@ -51,6 +51,8 @@ def library() -> ctypes.CDLL:
         lib.kda_chunk_fwd_workspace_size.argtypes = [I32, I64, I32, I32, I32, I32, I32, I32, ctypes.POINTER(SZ),
                                                      ctypes.POINTER(SZ)]
         lib.kda_recurrent_step.argtypes = [P, P, P, I64, P, P, P, P, P, I32, I32, I32, I32, F, F, P, P]
+        lib.kda_chunk_segment_summary.argtypes = [P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, P, P, P, SZ, P]
+        lib.kda_state_combine.argtypes = [P, P, P, P, I64, P]
         for f in (lib.kda_shortconv_l2norm, lib.kda_chunk_fwd, lib.kda_recurrent_step, lib.kda_device_error,
                   lib.kda_chunk_fwd_workspace_size, lib.kda_chunk_fwd_noalloc, lib.kda_chunk_fwd_frontend):
             f.restype = ctypes.c_int
@@ -186,6 +188,53 @@ def kda_chunk_fwd(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale: flo
                                  _ptr(final_state), _ptr(workspace), ws_bytes, _stream(stream))
     _check(rc, "kda_chunk_fwd")
     return o, final_state
+
+
+def kda_chunk_segment_summary(k, g, beta, v=None, q=None, cu_seqlens=None, end_state=True, transition=True,
+                              workspace=None, workspace_limit: int = WORKSPACE_LIMIT, stream=None):
+    """Per (sequence, head) segment: E = final state from a zero start and M = its transition operator
+    (the segment maps an entering state S to S M + E).  k, v (and optionally q) bf16 [T, H, 128], g fp32
+    [T, H, 128], beta fp32 [T, H].  end_state / transition: True (allocate), a fp32 [N, H, 128, 128]
+    CUDA tensor, or False/None (skip).  Returns (E or None, M or None)."""
+    T, H, dk = k.shape
+    _dev(k, "k", torch.bfloat16)
+    _dev(q, "q", torch.bfloat16, (T, H, dk)); _dev(v, "v", torch.bfloat16, (T, H, dk))
+    _dev(g, "g", torch.float32, (T, H, dk)); _dev(beta, "beta", torch.float32, (T, H))
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    _dev(cu_seqlens, "cu_seqlens", torch.int32)
+    outs = []
+    for want, name in ((end_state, "end_state"), (transition, "transition")):
+        if want is True:
+            want = torch.empty((N, H, dk, dk), dtype=torch.float32, device=k.device)
+        elif want is False:
+            want = None
+        _dev(want, name, torch.float32, (N, H, dk, dk))
+        outs.append(want)
+    E, M = outs
+    if workspace is None:
+        full, least = kda_chunk_fwd_workspace_size(N, T, H, torch.bfloat16, cu_seqlens is not None, dk, dk, 64)
+        workspace = torch.empty(max(least, min(full, int(workspace_limit))), dtype=torch.uint8, device=k.device)
+    _dev(workspace, "workspace", torch.uint8)
+    rc = library().kda_chunk_segment_summary(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N,
+                                             T, H, dk, dk, 64, _ptr(E), _ptr(M), _ptr(workspace), workspace.numel(),
+                                             _stream(stream))
+    _check(rc, "kda_chunk_segment_summary")
+    return E, M
+
+
+def kda_state_combine(S_in, M, E, out=None, stream=None):
+    """S_in M + E over the leading dimensions of fp32 [..., 128, 128] CUDA tensors (S_in None: E)."""
+    shape = E.shape
+    if len(shape) < 2 or tuple(shape[-2:]) != (128, 128):
+        raise KDAError("E must be [..., 128, 128]")
+    _dev(E, "E", torch.float32); _dev(M, "M", torch.float32, tuple(shape)); _dev(S_in, "S_in", torch.float32, tuple(shape))
+    if out is None:
+        out = torch.empty_like(E)
+    _dev(out, "out", torch.float32, tuple(shape))
+    count = E.numel() // (128 * 128)
+    _check(library().kda_state_combine(_ptr(S_in), _ptr(M), _ptr(E), _ptr(out), count, _stream(stream)),
+           "kda_state_combine")
+    return out
 
 
 def kda_chunk_fwd_frontend(xq, xk, xv, conv_w, g, beta, H: int, init_state=None, cu_seqlens=None,

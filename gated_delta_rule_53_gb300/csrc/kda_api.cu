@@ -201,6 +201,58 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const floa
                      "kda_chunk_fwd launch");
 }
 
+kda_status kda_chunk_segment_summary(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                     const int32_t* cu_seqlens, int N, int64_t T_total, int H, int dk, int dv,
+                                     int chunk_size, float* end_state, float* transition, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+    REQUIRE_PTR(k); REQUIRE_PTR(g); REQUIRE_PTR(beta);
+    OPTIONAL_PTR(q); OPTIONAL_PTR(v); OPTIONAL_PTR(end_state); OPTIONAL_PTR(transition);
+    REQUIRE(end_state != nullptr || transition != nullptr, "end_state and transition must not both be NULL");
+    if (end_state) REQUIRE_PTR(v);
+    kda_status s = check_batch(cu_seqlens, N, T_total, H);
+    if (s != KDA_OK) return s;
+    if (dk != kda::kHeadDim || dv != kda::kHeadDim)
+        return set_error(KDA_ERR_UNSUPPORTED, "only dk = dv = 128 is supported (got %d, %d)", dk, dv);
+    if (chunk_size != kda::kChunk)
+        return set_error(KDA_ERR_UNSUPPORTED, "only chunk_size = 64 is supported (got %d)", chunk_size);
+    REQUIRE(T_total < ((int64_t)1 << 31), "T_total must be below 2^31 (tensor-map coordinates)");
+    REQUIRE(T_total / 64 + N <= 0x7FFFFFFF, "too many chunks");
+    size_t full = 0, need = 0;
+    kda::chunk_tc_workspace(N, T_total, H, cu_seqlens != nullptr, &full, &need);
+    REQUIRE(workspace != nullptr && workspace_bytes >= need,
+            "workspace must hold at least %zu bytes for these sizes (got %zu)", need, workspace_bytes);
+    OPTIONAL_PTR(workspace);
+    unsigned int* err = kda::device_error_word();
+    if (!err) return set_error(KDA_ERR_CUDA, "device error word unavailable");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const void* qq = q ? q : k;   // the outputs asked for do not depend on q
+    const void* vv = v ? v : k;   // nor, for the transition alone, on v
+    const int tr_mode = kda::kStateZeroU | kda::kStateIdentity;
+    cudaError_t e;
+    if (end_state && transition && workspace_bytes >= full) {  // one pass of chunk operands, two state passes
+        e = kda::launch_chunk_tc(qq, k, vv, g, beta, nullptr, cu_seqlens, N, T_total, H, 1.0f, nullptr, nullptr,
+                                 end_state, workspace, workspace_bytes, nullptr, err, st, 0, transition, tr_mode);
+    } else {
+        e = cudaSuccess;
+        if (end_state)
+            e = kda::launch_chunk_tc(qq, k, vv, g, beta, nullptr, cu_seqlens, N, T_total, H, 1.0f, nullptr, nullptr,
+                                     end_state, workspace, workspace_bytes, nullptr, err, st, 0);
+        if (e == cudaSuccess && transition)
+            e = kda::launch_chunk_tc(qq, k, vv, g, beta, nullptr, cu_seqlens, N, T_total, H, 1.0f, nullptr, nullptr,
+                                     transition, workspace, workspace_bytes, nullptr, err, st, tr_mode);
+    }
+    return from_cuda(e, "kda_chunk_segment_summary launch");
+}
+
+kda_status kda_state_combine(const float* S_in, const float* M, const float* E, float* S_out, int64_t count,
+                             void* stream) {
+    OPTIONAL_PTR(S_in);
+    REQUIRE_PTR(M); REQUIRE_PTR(E); REQUIRE_PTR(S_out);
+    REQUIRE(count >= 0 && count <= 0x7FFFFFFF, "count must be in [0, 2^31) (got %lld)", (long long)count);
+    return from_cuda(kda::launch_state_combine(S_in, M, E, S_out, count, static_cast<cudaStream_t>(stream)),
+                     "kda_state_combine launch");
+}
+
 kda_status kda_chunk_fwd_frontend(const void* xq, const void* xk, const void* xv, int64_t x_row_stride,
                                   const void* conv_w, const void* conv_state_in, void* conv_state_out, float eps,
                                   const float* g, const float* beta, const float* init_state,

@@ -821,11 +821,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, const int32_t* __restrict__ off,
                    int64_t T_total, int H, float scale, const __nv_bfloat16* __restrict__ gate,
                    __nv_bfloat16* __restrict__ o, float* final_state, const float* carry_in, float* carry_out,
-                   int first_range, int m0, int m1, const uint8_t* __restrict__ blobs, unsigned int* err) {
+                   int first_range, int m0, int m1, const uint8_t* __restrict__ blobs, int mode, unsigned int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool zero_u = (mode & kStateZeroU) != 0;  // U taken as zero (v = 0): the transition operator
     const int chain = blockIdx.x, n = chain / H, h = chain % H;
     const int on = off[n], on1 = off[n + 1];
     int lo = on > m0 ? on : m0, hi = on1 < m1 ? on1 : m1;
@@ -909,7 +910,7 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
         uint32_t phM = 0, phD = 0, phO = 0;
         for (int i = 0; i < 2 && lo + i < hi; ++i) {
             load_b1(lo + i, i);
-            load_u(lo + i, i);
+            if (!zero_u) load_u(lo + i, i);
             load_aq(lo + i, i);
         }
         int b = 0, b3 = 0;  // TMEM [Y | O] buffer and B1 buffer of this chunk; U and A_qk/KP buffers follow b
@@ -928,8 +929,10 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
             mma_commit(barM);
             wait(barM, phM);
             phM ^= 1u;
-            wait(barU + b, (ph >> (3 + b)) & 1u);
-            ph ^= 8u << b;
+            if (!zero_u) {
+                wait(barU + b, (ph >> (3 + b)) & 1u);
+                ph ^= 8u << b;
+            }
             const bool stop = *sAbort != 0;
             tc_fence_before();
             nb_arrive(NB_Y);
@@ -955,7 +958,7 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
             phD ^= 1u;
             tc_fence_before();
             nb_arrive(NB_D);
-            if (ahead) load_u(mm + 2, b);  // every thread has read this chunk's U
+            if (ahead && !zero_u) load_u(mm + 2, b);  // every thread has read this chunk's U
             const uint32_t od = tbase + 128 * b + 64;
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) mma_bf16_ta(od, tbase + TM_VH + 8 * ks, kdesc(aq) + ks * 2, id_64, 1u);
@@ -982,10 +985,15 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
         __syncwarp();
     } else {
         // ======== the state: thread (row, qq) holds row `row`, key channels [32 qq, 32 qq + 32) ========
+        const bool ident = !s_in && (mode & kStateIdentity);  // a chain that starts from I (dv = dk)
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
             float4 x = s_in ? *reinterpret_cast<const float4*>(s_in + in_off + j) : make_float4(0.f, 0.f, 0.f, 0.f);
             s[j] = x.x; s[j + 1] = x.y; s[j + 2] = x.z; s[j + 3] = x.w;
+        }
+        if (ident) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) s[j] = (row == 32 * qq + j) ? 1.f : 0.f;
         }
         auto write_state_operand = [&]() {  // bf16 copy in TMEM, the A operand of the S0 products
             uint32_t w[16];
@@ -1050,7 +1058,7 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
                 float hv[16], lv[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float x = sU[(16 * qq + e) * kD + row] - __uint_as_float(y[e]);
+                    const float x = (zero_u ? 0.f : sU[(16 * qq + e) * kD + row]) - __uint_as_float(y[e]);
                     hv[e] = __bfloat162float(__float2bfloat16_rn(x));
                     lv[e] = x - hv[e];
                 }
@@ -1066,7 +1074,7 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
             }
             tc_fence_before();
             nb_arrive(NB_V);
-            if (mm > lo) {  // the previous chunk's outputs while dS runs
+            if (mm > lo && o) {  // the previous chunk's outputs while dS runs
                 emit_o(mm - 1, b ^ 1, 0);
                 emit_o(mm - 1, b ^ 1, 1);
             }
@@ -1090,8 +1098,10 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
         if (lo < hi && !stopped) {
             nb_sync(NB_O);
             tc_fence_after();
-            emit_o(hi - 1, (hi - 1 - lo) & 1, 0);
-            emit_o(hi - 1, (hi - 1 - lo) & 1, 1);
+            if (o) {
+                emit_o(hi - 1, (hi - 1 - lo) & 1, 0);
+                emit_o(hi - 1, (hi - 1 - lo) & 1, 1);
+            }
         }
     }
     tc_fence_before();
@@ -1160,7 +1170,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
                             const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
                             float scale, const void* out_gate, void* o, float* final_state, void* workspace,
                             size_t workspace_bytes, const ChunkFrontend* front, unsigned int* err,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, int state_mode, float* final_state2, int state_mode2) {
     CUtensorMap tq = {}, tk = {}, tv = {}, tg;
     if (!front && (!encode_chunk_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, T_total, H) ||
                    !encode_chunk_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, T_total, H) ||
@@ -1193,6 +1203,8 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     chunk_offsets_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, T_total, off);
+    // A second state pass on the same operands (final_state2, state_mode2) needs them all at once.
+    if (final_state2 && rows < rows_max) return cudaErrorInvalidValue;
     int range = 0;
     for (int64_t r0 = 0; range == 0 || r0 < rows_max; r0 += rows, ++range) {
         const int64_t r1 = r0 + rows < rows_max ? r0 + rows : rows_max;
@@ -1207,7 +1219,11 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
         chunk_state_kernel<<<(unsigned)((int64_t)N * H), kThreads, kStateSmem, stream>>>(
             init_state, cu_seqlens, off, T_total, H, scale, static_cast<const __nv_bfloat16*>(out_gate),
             static_cast<__nv_bfloat16*>(o), final_state, c_in, c_out, range == 0 ? 1 : 0, (int)r0, (int)r1, blobs,
-            err);
+            state_mode, err);
+        if (final_state2)
+            chunk_state_kernel<<<(unsigned)((int64_t)N * H), kThreads, kStateSmem, stream>>>(
+                nullptr, cu_seqlens, off, T_total, H, scale, nullptr, nullptr, final_state2, nullptr, nullptr, 1,
+                (int)r0, (int)r1, blobs, state_mode2, err);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

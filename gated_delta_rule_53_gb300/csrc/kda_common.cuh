@@ -99,11 +99,24 @@ struct ChunkFrontend {
     float eps;
 };
 
+// Modes of a state pass: U taken as zero (the effect of v = 0), and chains that start without an
+// initial state start from the identity (dv = dk).  Both together give a segment's transition
+// operator  prod_t Diag(alpha_t) (I - beta_t k_t k_t^T)  as the final state.
+constexpr int kStateZeroU = 1, kStateIdentity = 2;
+
+// o may be null (no outputs).  final_state2 (with state_mode2): a second state pass over the same
+// operands, from a zero / identity start, without outputs; it needs every chunk in one range of the
+// workspace (cudaErrorInvalidValue otherwise).
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
                             const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
                             float scale, const void* out_gate, void* o, float* final_state, void* workspace,
                             size_t workspace_bytes, const ChunkFrontend* front, unsigned int* err,
-                            cudaStream_t stream);
+                            cudaStream_t stream, int state_mode = 0, float* final_state2 = nullptr,
+                            int state_mode2 = 0);
+
+// S_out[i] = S_in[i] M[i] + E[i] for `count` 128 x 128 fp32 matrices (S_in null: S_out = E).
+cudaError_t launch_state_combine(const float* S_in, const float* M, const float* E, float* S_out, int64_t count,
+                                 cudaStream_t stream);
 
 // conv_state_out of the front end (the last three raw inputs of each sequence), as a pass of its own.
 cudaError_t launch_conv_state_out(const void* xq, const void* xk, const void* xv, int64_t x_stride,

@@ -184,6 +184,44 @@ KDA_API kda_status kda_chunk_fwd_workspace_size(int N, int64_t T_total, int H, i
                                         size_t* min_bytes);
 
 /*
+ * Summaries of segments of sequences, for carrying the state across them (a long sequence split
+ * into segments, each worked on separately, e.g. one per device).  The update of "Kimi-K3 深度
+ * 解析", section 三 ("KDA 的关键改进"), S_t = S_{t-1} Diag(alpha_t)(I - beta_t k_t k_t^T) +
+ * beta_t v_t k_t^T, is affine in S_{t-1}, so each (sequence, head) segment maps its entering state S
+ * to  S M + E  with
+ *   E = its final state from a zero start (what kda_chunk_fwd returns without init_state), and
+ *   M = X_1 X_2 ... X_L, X_t = Diag(exp g_t)(I - beta_t k_t k_t^T)  (its transition operator).
+ * M is the final state of the same recurrence with v = 0 from S = I, and is computed that way on
+ * the chunk path (bf16 products, fp32 state).
+ *
+ *  q               bf16 [T_total, H, 128] or NULL: M and E do not depend on it (k stands in)
+ *  k, g, beta, cu_seqlens, N, T_total, H, dk, dv, chunk_size
+ *                  as kda_chunk_fwd with dtype KDA_DTYPE_BF16 (dk = dv = 128, chunk_size 64)
+ *  v               bf16 [T_total, H, 128]; may be NULL when end_state is NULL
+ *  end_state       fp32 [N, H, 128, 128] out (E), or NULL
+ *  transition      fp32 [N, H, 128, 128] out (M), or NULL; not both NULL
+ *  workspace       as kda_chunk_fwd; with the `full_bytes` of kda_chunk_fwd_workspace_size the
+ *                  chunk operands are computed once for both outputs, with less twice
+ *
+ * Writes nothing else.  Errors as kda_chunk_fwd.
+ */
+KDA_API kda_status kda_chunk_segment_summary(const void* q, const void* k, const void* v, const float* g,
+                                             const float* beta, const int32_t* cu_seqlens, int N, int64_t T_total,
+                                             int H, int dk, int dv, int chunk_size, float* end_state,
+                                             float* transition, void* workspace, size_t workspace_bytes,
+                                             void* stream);
+
+/*
+ * The map of a segment applied to a state:  S_out[i] = S_in[i] M[i] + E[i]  for i < count, each a
+ * fp32 128 x 128 row-major matrix (S_in NULL: S_out = E).  Folding the segments of a sequence in
+ * order with it gives each segment's entering state (see kda_chunk_segment_summary).  Products in
+ * fp32, k summed in order.  S_out may alias any input.  All pointers 16-byte aligned device
+ * memory; count >= 0.
+ */
+KDA_API kda_status kda_state_combine(const float* S_in, const float* M, const float* E, float* S_out, int64_t count,
+                                     void* stream);
+
+/*
  * One decode step (the fused_recurrent_kda operator of "Kimi K3 架构全景",
  * section 02) for N sequences of one new token each, fused end to end: the
  * ShortConv(4) + SiLU + L2 norm front end on the token's raw q, k, v (shifting

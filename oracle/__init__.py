@@ -17,6 +17,10 @@ The arithmetic lives in ``kda_oracle.c`` (plain C99, fp64, one thread per
 * :func:`output_gate` — o * sigmoid(gate), the full-rank output gate (same paragraph).
 * :func:`recurrent_step` — one decode step: the front end on one token per
   sequence followed by one step of the token loop (``fused_recurrent_kda``).
+* :func:`transition` — a segment's transition operator M = X_1 ... X_L with
+  X_t = Diag(alpha_t)(I - beta_t k_t k_t^T), formed as a literal product of dense
+  matrices: a segment maps its entering state S to S M + E (E its end state from zero),
+  which is how a state is carried across segments of one sequence.
 
 All arrays are fp64 numpy arrays in the layouts of ``kda_oracle.c``.
 """
@@ -55,9 +59,11 @@ def _load():
         P, I, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_double
         lib.oracle_kda_tokenloop.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, D, P, P, ctypes.c_int]
         lib.oracle_kda_chunked.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, D, I, P, P, ctypes.c_int]
+        lib.oracle_kda_transition.argtypes = [P, P, P, P, I, I, I, I, P, ctypes.c_int]
         lib.oracle_shortconv_silu_l2norm.argtypes = [P, P, P, I, P, P, I, I, I, I, P, D, P, P, P, P,
                                                      ctypes.c_int]
-        for f in (lib.oracle_kda_tokenloop, lib.oracle_kda_chunked, lib.oracle_shortconv_silu_l2norm):
+        for f in (lib.oracle_kda_tokenloop, lib.oracle_kda_chunked, lib.oracle_shortconv_silu_l2norm,
+                  lib.oracle_kda_transition):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -118,6 +124,20 @@ def kda_tokenloop(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale=1.0,
 def kda_chunked(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale=1.0, chunk=64, nthreads=None):
     """The same pair computed chunk by chunk (unit-triangular solve per chunk)."""
     return _kda(_load().oracle_kda_chunked, q, k, v, g, beta, init_state, cu_seqlens, scale, chunk, nthreads)
+
+
+def transition(k, g, beta, cu_seqlens=None, nthreads=None):
+    """M [N, H, dk, dk]: each (sequence, head) segment's product X_1 ... X_L of
+    X_t = Diag(exp g_t)(I - beta_t k_t k_t^T), so that the segment maps S to S M + E."""
+    k, g, beta = (_f64(x) for x in (k, g, beta))
+    T, H, dk = k.shape
+    assert g.shape == (T, H, dk) and beta.shape == (T, H)
+    cu, N = _cu(cu_seqlens, T)
+    M = np.empty((N, H, dk, dk), np.float64)
+    if _load().oracle_kda_transition(_ptr(k), _ptr(g), _ptr(beta), _ptr(cu), N, T, H, dk, _ptr(M),
+                                     nthreads or threads()) != 0:
+        raise ValueError("oracle rejected its arguments")
+    return M
 
 
 def shortconv_silu_l2norm(xq, xk, xv, conv_w, H, d, cu_seqlens=None, conv_state_in=None, eps=1e-6,

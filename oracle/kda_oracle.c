@@ -350,3 +350,57 @@ int oracle_shortconv_silu_l2norm(const double* xq, const double* xk, const doubl
     fe_ctx c = {xq, xk, xv, w, conv_state_in, x_ld, cu_seqlens, N, T_total, H, d, eps, q, k, v, conv_state_out};
     return run_queue(frontend_chain, &c, N * H, (size_t)(9 * d), nthreads);
 }
+
+/* ---------------------------------------------------------------------------------------- */
+/* O4: a segment's transition operator, for carrying the state across segments              */
+/* ---------------------------------------------------------------------------------------- */
+
+/*
+ * The update of section 三 ("KDA 的关键改进") rewritten with S~ = S Diag(alpha):
+ *   S_t = S_{t-1} X_t + beta_t v_t k_t^T,   X_t = Diag(alpha_t) (I - beta_t k_t k_t^T)   (dk x dk)
+ * so a segment of tokens t = 1..L maps its entering state S to S M + E with
+ *   M = X_1 X_2 ... X_L   (time order, left to right)
+ * and E the segment's end state from a zero start.  Here M is formed literally: each X_t is
+ * written out as a dense matrix, X[a][b] = alpha_a (delta_ab - beta k_a k_b), and multiplied on
+ * the right of the running product.
+ */
+typedef struct {
+    const double *k, *g, *beta;
+    const int64_t* cu;
+    int64_t N, T, H, dk;
+    double* M;
+} tr_ctx;
+
+static void transition_chain(void* vctx, int64_t item, double* M) {
+    const tr_ctx* c = (const tr_ctx*)vctx;
+    const int64_t n = item / c->H, h = item % c->H, dk = c->dk, H = c->H;
+    double* X = M + dk * dk;
+    double* P = X + dk * dk;
+    const int64_t bos = c->cu ? c->cu[n] : 0, eos = c->cu ? c->cu[n + 1] : c->T;
+    for (int64_t a = 0; a < dk; ++a)
+        for (int64_t b = 0; b < dk; ++b) M[a * dk + b] = (a == b) ? 1.0 : 0.0;
+    for (int64_t t = bos; t < eos; ++t) {
+        const double* kt = c->k + (t * H + h) * dk;
+        const double* gt = c->g + (t * H + h) * dk;
+        const double bt = c->beta[t * H + h];
+        for (int64_t a = 0; a < dk; ++a)
+            for (int64_t b = 0; b < dk; ++b)
+                X[a * dk + b] = exp(gt[a]) * (((a == b) ? 1.0 : 0.0) - bt * kt[a] * kt[b]);
+        for (int64_t a = 0; a < dk; ++a)
+            for (int64_t b = 0; b < dk; ++b) {
+                double acc = 0.0;
+                for (int64_t m = 0; m < dk; ++m) acc += M[a * dk + m] * X[m * dk + b];
+                P[a * dk + b] = acc;
+            }
+        memcpy(M, P, sizeof(double) * dk * dk);
+    }
+    memcpy(c->M + (n * H + h) * dk * dk, M, sizeof(double) * dk * dk);
+}
+
+int oracle_kda_transition(const double* k, const double* g, const double* beta, const int64_t* cu_seqlens,
+                          int64_t N, int64_t T_total, int64_t H, int64_t dk, double* M, int nthreads) {
+    if (!k || !g || !beta || !M || H < 1 || dk < 1 || T_total < 0) return -1;
+    if (check_seqlens(cu_seqlens, N, T_total)) return -1;
+    tr_ctx c = {k, g, beta, cu_seqlens, N, T_total, H, dk, M};
+    return run_queue(transition_chain, &c, N * H, (size_t)(3 * dk * dk), nthreads);
+}

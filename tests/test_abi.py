@@ -139,3 +139,34 @@ def test_chunk_fwd_frontend_rejects_bad_arguments(lib):
     assert call(ws=None) == 1
     assert call(wsb=1024) == 1
     assert call(N=2) == 1                 # several sequences need cu_seqlens
+
+
+def test_segment_summary_and_combine_reject_bad_arguments(lib):
+    def summ(**over):
+        a = dict(q=None, k=P(4096), v=P(4096), g=P(4096), b=P(4096), cu=None, N=1, T=64, H=2, dk=128, dv=128,
+                 chunk=64, E=P(4096), M=P(4096), ws=P(4096), wsb=1 << 30)
+        a.update(over)
+        return lib.kda_chunk_segment_summary(a["q"], a["k"], a["v"], a["g"], a["b"], a["cu"], a["N"], a["T"],
+                                             a["H"], a["dk"], a["dv"], a["chunk"], a["E"], a["M"], a["ws"],
+                                             a["wsb"], None)
+    assert summ(k=None) == 1
+    assert summ(E=None, M=None) == 1       # nothing to compute
+    assert summ(v=None) == 1               # the end state needs v
+    assert summ(M=P(4100)) == 1            # misaligned
+    assert summ(dk=64) == 2
+    assert summ(chunk=32) == 2
+    assert summ(N=2) == 1                  # several sequences need cu_seqlens
+    assert summ(ws=None) == 1
+    assert summ(wsb=1024) == 1
+    assert summ(T=1 << 31) == 1
+
+    def comb(**over):
+        a = dict(S=None, M=P(4096), E=P(4096), out=P(4096), count=1)
+        a.update(over)
+        return lib.kda_state_combine(a["S"], a["M"], a["E"], a["out"], a["count"], None)
+    assert comb(M=None) == 1
+    assert comb(E=None) == 1
+    assert comb(out=None) == 1
+    assert comb(S=P(4100)) == 1            # misaligned
+    assert comb(count=-1) == 1
+    assert comb(count=1 << 31) == 1
