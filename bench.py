@@ -275,6 +275,53 @@ def run_ours(args):
     pflops = w.T * w.H * PREFILL_FLOPS_PER_TOKEN_HEAD
     achieved_tflops = pflops / (ms_launch * 1e-3) / 1e12
 
+    # ---------------- the same sequence cut into 4 segments (context-parallel ranks, played in turn) --------
+    # summaries (end state and transition operator, one operand pass for both), the fold by
+    # kda_state_combine, and each segment re-run from its entering state, written into o in place
+    seg = None
+    if w.N == 1:
+        nseg = 4
+        bnd = [w.T * i // nseg for i in range(nseg + 1)]
+        sE = [torch.empty_like(fs) for _ in range(nseg)]
+        sM = [torch.empty_like(fs) for _ in range(nseg)]
+        sS = [torch.empty_like(fs) for _ in range(nseg)]
+        sF = torch.empty_like(fs)   # states leaving the non-last segments (equal to the fold's; unused)
+
+        def summarise(i):
+            a, z = bnd[i], bnd[i + 1]
+            kda.kda_chunk_segment_summary(k[a:z], g[a:z], b[a:z], v=v[a:z], q=q[a:z], end_state=sE[i],
+                                          transition=sM[i], workspace=ws, stream=stream)
+
+        def rerun(i, S_in):
+            a, z = bnd[i], bnd[i + 1]
+            kda.kda_chunk_fwd(q[a:z], k[a:z], v[a:z], g[a:z], b[a:z], init_state=S_in, o=o[a:z],
+                              final_state=fs if i == nseg - 1 else sF, workspace=ws, stream=stream)
+
+        def segmented():
+            for i in range(nseg):
+                summarise(i)
+            S_in = None
+            for i in range(nseg):
+                if i:
+                    S_in = kda.kda_state_combine(S_in, sM[i - 1], sE[i - 1], out=sS[i - 1], stream=stream)
+                rerun(i, S_in)
+
+        ssteps = max(3, args.steps // 4)
+        ms_seg, _, _ = timed(segmented, ssteps, args.warmup, stream, dist)
+        ms_sum, _, _ = timed(lambda: summarise(nseg - 1), ssteps, args.warmup, stream, dist)
+        ms_comb, _, _ = timed(lambda: kda.kda_state_combine(sS[0], sM[1], sE[1], out=sS[1], stream=stream), ssteps,
+                              args.warmup, stream, dist)
+        ms_run, _, _ = timed(lambda: rerun(nseg - 1, sS[nseg - 2]), ssteps, args.warmup, stream, dist)
+        seg = {"workload": f"{w.name} cut into {nseg} segments of {w.T // nseg} tokens: context-parallel ranks "
+                           "played in turn on one GPU (no exchange between devices timed)",
+               "value": w.T / (ms_seg * 1e-3), "unit": "tokens/s", "ms_per_step": ms_seg, "steps": ssteps,
+               "gpu_launches": ssteps * (nseg * 4 + (nseg - 1) + nseg * 3),
+               "segment_summary_ms": ms_sum, "state_combine_ms": ms_comb, "segment_rerun_ms": ms_run,
+               "last_rank_ms": ms_sum + (nseg - 1) * ms_comb + ms_run,
+               "note": "last_rank_ms: the measured per-call times of the work on the last of the ranks (its "
+                       "summary, the fold of the three before it, its re-run), without the all-gather"}
+        del sE, sM, sS, sF
+
     # ---------------- end to end through the API with host buffers ----------------
     # Every step copies its inputs from pinned host memory and reads its result (o and the final
     # state) back.  Steps are pipelined as a serving loop would run them: the next step's
@@ -429,6 +476,8 @@ def run_ours(args):
                                   "traffic": measured_traffic("shortconv_kernel", "kda_frontend.cu", wf.name),
                                   "peak_source": peak_src}},
     }
+    if seg is not None:
+        line["segmented_prefill"] = seg
     line["fused_prefill"] = {
         "workload": "frontend_32k raw q, k, v bf16 [32768, 12288] + g = max(-5, -softplus(z)), beta -> "
                     "ShortConv(4)+SiLU+L2norm -> chunk_kda (the long workload's path at 32K tokens)",
