@@ -1148,6 +1148,57 @@ bool encode_chunk_map(CUtensorMap* m, const void* base, CUtensorMapDataType type
 
 }  // namespace
 
+// Overlapped ranges: about this many ranges of at least this many chunk rows.
+constexpr int64_t kPipeRanges = 8, kPipeMinRows = 64;
+
+// Two streams per device (created once): a low-priority one for the operand kernel and a
+// high-priority one for the state pass.
+static cudaError_t side_streams(int dev, cudaStream_t* s_low, cudaStream_t* s_high) {
+    static std::mutex mu;
+    static cudaStream_t streams[64][2] = {};
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!streams[dev][0]) {
+        int least = 0, greatest = 0;
+        cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+        if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&streams[dev][0], cudaStreamNonBlocking, least);
+        if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&streams[dev][1], cudaStreamNonBlocking, greatest);
+        if (e != cudaSuccess) {
+            streams[dev][0] = streams[dev][1] = nullptr;
+            return e;
+        }
+    }
+    *s_low = streams[dev][0];
+    *s_high = streams[dev][1];
+    return cudaSuccess;
+}
+
+// Events of one call (released when the set goes out of scope; the driver keeps an event alive
+// until the work it records has completed).
+struct EventSet {
+    explicit EventSet(int n) : n_(n), ev_(new cudaEvent_t[n]()) {
+        for (int i = 0; i < n; ++i)
+            if (cudaEventCreateWithFlags(&ev_[i], cudaEventDisableTiming) != cudaSuccess) ev_[i] = nullptr;
+    }
+    ~EventSet() {
+        for (int i = 0; i < n_; ++i)
+            if (ev_[i]) cudaEventDestroy(ev_[i]);
+        delete[] ev_;
+    }
+    bool ok() const {
+        for (int i = 0; i < n_; ++i)
+            if (!ev_[i]) return false;
+        return true;
+    }
+    cudaEvent_t operator[](int i) const { return ev_[i]; }
+    EventSet(const EventSet&) = delete;
+    EventSet& operator=(const EventSet&) = delete;
+
+  private:
+    int n_;
+    cudaEvent_t* ev_;
+};
+
 // Workspace: [carried states, 2 x H x 128 x 128 fp32][chunk offsets, int32 N + 1][operands of
 // `rows` chunk rows x H heads, kBlobBytes each].
 static size_t ws_header_bytes(int N, int H) {
@@ -1205,6 +1256,53 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
     chunk_offsets_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, T_total, off);
     // A second state pass on the same operands (final_state2, state_mode2) needs them all at once.
     if (final_state2 && rows < rows_max) return cudaErrorInvalidValue;
+    if (!front && !final_state2 && rows >= 2 && rows_max >= 2 * kPipeMinRows) {
+        // Overlapped ranges: the chunk rows in about kPipeRanges ranges (of at least kPipeMinRows rows:
+        // each extra range costs about 35 us of wave tails and state-pass start-up), their operands in
+        // two alternating halves of the workspace; range r's state pass (high-priority stream, 96 of
+        // the 152 SMs for 96 chains) runs while range r+1's operands are computed on the other SMs
+        // (low-priority stream, one CTA per item, so that the state pass's CTAs take SMs first as they
+        // free up).  Ordered by events only.  Not for the fused front end, whose operand kernel
+        // measured slower this way.
+        int64_t rr = (rows_max + kPipeRanges - 1) / kPipeRanges;
+        if (rr < kPipeMinRows) rr = kPipeMinRows;
+        if (rr > rows / 2) rr = rows / 2;
+        cudaStream_t s_prep, s_state;
+        e = side_streams(dev, &s_prep, &s_state);
+        if (e != cudaSuccess) return e;
+        const int nr = (int)((rows_max + rr - 1) / rr);
+        EventSet ev(2 * nr + 1);
+        if (!ev.ok()) return cudaErrorMemoryAllocation;
+        cudaEvent_t ev_start = ev[2 * nr];
+        e = cudaEventRecord(ev_start, stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s_prep, ev_start, 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s_state, ev_start, 0);
+        for (int r = 0; r < nr && e == cudaSuccess; ++r) {
+            const int64_t r0 = (int64_t)r * rr, r1 = r0 + rr < rows_max ? r0 + rr : rows_max;
+            uint8_t* buf = blobs + (size_t)(r & 1) * (size_t)rr * H * kBlobBytes;
+            if (r >= 2) e = cudaStreamWaitEvent(s_prep, ev[nr + r - 2], 0);  // that half's state pass is done
+            if (e != cudaSuccess) break;
+            const int64_t items = (r1 - r0) * H;
+            prep<<<(unsigned)items, kPrepThreads, kPrepSmem, s_prep>>>(tq, tk, tv, tg, beta, cu_seqlens, off, N,
+                                                                       T_total, H, (int)r0, (int)items, buf, fa, err);
+            e = cudaGetLastError();
+            if (e == cudaSuccess) e = cudaEventRecord(ev[r], s_prep);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(s_state, ev[r], 0);
+            if (e != cudaSuccess) break;
+            float* c_out = carry + (size_t)(r & 1) * H * kD * kD;
+            const float* c_in = carry + (size_t)((r + 1) & 1) * H * kD * kD;
+            chunk_state_kernel<<<(unsigned)((int64_t)N * H), kThreads, kStateSmem, s_state>>>(
+                init_state, cu_seqlens, off, T_total, H, scale, static_cast<const __nv_bfloat16*>(out_gate),
+                static_cast<__nv_bfloat16*>(o), final_state, c_in, c_out, r == 0 ? 1 : 0, (int)r0, (int)r1, buf,
+                state_mode, err);
+            e = cudaGetLastError();
+            if (e == cudaSuccess) e = cudaEventRecord(ev[nr + r], s_state);
+        }
+        // join: the caller's stream waits for both side streams' last work
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev[nr - 1], 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev[2 * nr - 1], 0);
+        return e;
+    }
     int range = 0;
     for (int64_t r0 = 0; range == 0 || r0 < rows_max; r0 += rows, ++range) {
         const int64_t r1 = r0 + rows < rows_max ? r0 + rows : rows_max;
