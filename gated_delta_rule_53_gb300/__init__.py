@@ -53,6 +53,7 @@ def library() -> ctypes.CDLL:
         lib.kda_recurrent_step.argtypes = [P, P, P, I64, P, P, P, P, P, I32, I32, I32, I32, F, F, P, P]
         lib.kda_chunk_segment_summary.argtypes = [P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, P, P, P, SZ, P]
         lib.kda_state_combine.argtypes = [P, P, P, P, I64, P]
+        lib.kda_gate_generator.argtypes = [P, I64, I32, P, P, P, I32, I32, I32, P, P, P, P]
         for f in (lib.kda_shortconv_l2norm, lib.kda_chunk_fwd, lib.kda_recurrent_step, lib.kda_device_error,
                   lib.kda_chunk_fwd_workspace_size, lib.kda_chunk_fwd_noalloc, lib.kda_chunk_fwd_frontend):
             f.restype = ctypes.c_int
@@ -235,6 +236,26 @@ def kda_state_combine(S_in, M, E, out=None, stream=None):
     _check(library().kda_state_combine(_ptr(S_in), _ptr(M), _ptr(E), _ptr(out), count, _stream(stream)),
            "kda_state_combine")
     return out
+
+
+def kda_gate_generator(x, w_gate_a, w_b, a_head, H: int, d: int = 128, gate=None, g=None, z=None, stream=None):
+    """Output gate bf16 [T, H*d] and decay gate g fp32 [T, H, d] = max(-5, -softplus(x W_a^T W_b^T + a_h))
+    from x bf16 [T, hidden]; w_gate_a bf16 [H*d + rank, hidden] (W_gate rows, then W_a rows), w_b bf16
+    [H*d, rank], a_head fp32 [H].  Returns (gate, g)."""
+    T, hidden = x.shape
+    rank = w_gate_a.shape[0] - H * d
+    _dev(x, "x", torch.bfloat16); _dev(w_gate_a, "w_gate_a", torch.bfloat16, (H * d + rank, hidden))
+    _dev(w_b, "w_b", torch.bfloat16, (H * d, rank)); _dev(a_head, "a_head", torch.float32, (H,))
+    if gate is None:
+        gate = torch.empty((T, H * d), dtype=torch.bfloat16, device=x.device)
+    if g is None:
+        g = torch.empty((T, H, d), dtype=torch.float32, device=x.device)
+    if z is None:
+        z = torch.empty((max(T, 1), rank), dtype=torch.bfloat16, device=x.device)
+    _dev(gate, "gate", torch.bfloat16, (T, H * d)); _dev(g, "g", torch.float32, (T, H, d)); _dev(z, "z", torch.bfloat16)
+    _check(library().kda_gate_generator(_ptr(x), T, hidden, _ptr(w_gate_a), _ptr(w_b), _ptr(a_head), H, d, rank,
+                                        _ptr(gate), _ptr(g), _ptr(z), _stream(stream)), "kda_gate_generator")
+    return gate, g
 
 
 def kda_chunk_fwd_frontend(xq, xk, xv, conv_w, g, beta, H: int, init_state=None, cu_seqlens=None,

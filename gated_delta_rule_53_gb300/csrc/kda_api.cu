@@ -244,6 +244,25 @@ kda_status kda_chunk_segment_summary(const void* q, const void* k, const void* v
     return from_cuda(e, "kda_chunk_segment_summary launch");
 }
 
+kda_status kda_gate_generator(const void* x, int64_t T, int hidden, const void* w_gate_a, const void* w_b,
+                              const float* a_head, int H, int d, int rank, void* gate, float* g, void* z_workspace,
+                              void* stream) {
+    REQUIRE(T >= 0 && T < ((int64_t)1 << 31), "T must be in [0, 2^31) (got %lld)", (long long)T);
+    REQUIRE(hidden >= 8 && hidden % 8 == 0, "hidden must be a positive multiple of 8 (got %d)", hidden);
+    if (d != kda::kHeadDim) return set_error(KDA_ERR_UNSUPPORTED, "only d = 128 is supported (got %d)", d);
+    REQUIRE(H >= 1 && H <= 65535, "H must be in [1, 65535] (got %d)", H);
+    REQUIRE(rank >= 32 && rank <= 4096 && rank % 32 == 0, "rank must be a multiple of 32 in [32, 4096] (got %d)",
+            rank);
+    REQUIRE_PTR(w_gate_a); REQUIRE_PTR(w_b); REQUIRE_PTR(a_head);
+    if (T == 0) return ok();  // nothing to compute; the per-token buffers may be empty
+    REQUIRE_PTR(x); REQUIRE_PTR(gate); REQUIRE_PTR(g); REQUIRE_PTR(z_workspace);
+    unsigned int* err = kda::device_error_word();
+    if (!err) return set_error(KDA_ERR_CUDA, "device error word unavailable");
+    return from_cuda(kda::launch_gate_generator(x, T, hidden, w_gate_a, w_b, a_head, H, d, rank, gate, g, z_workspace,
+                                                err, static_cast<cudaStream_t>(stream)),
+                     "kda_gate_generator launch");
+}
+
 kda_status kda_state_combine(const float* S_in, const float* M, const float* E, float* S_out, int64_t count,
                              void* stream) {
     OPTIONAL_PTR(S_in);

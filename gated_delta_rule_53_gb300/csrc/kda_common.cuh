@@ -114,6 +114,12 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
                             cudaStream_t stream, int state_mode = 0, float* final_state2 = nullptr,
                             int state_mode2 = 0);
 
+// gate = x W_gate^T (bf16), z = x W_a^T (bf16 scratch [T, rank]), g = max(-5, -softplus(z W_b^T + a_h))
+// (fp32); w_gate_a = [W_gate ; W_a] stacked, [H*d + rank, hidden].
+cudaError_t launch_gate_generator(const void* x, int64_t T, int hidden, const void* w_gate_a, const void* w_b,
+                                  const float* a_head, int H, int d, int rank, void* gate, float* g, void* z,
+                                  unsigned int* err, cudaStream_t stream);
+
 // S_out[i] = S_in[i] M[i] + E[i] for `count` 128 x 128 fp32 matrices (S_in null: S_out = E).
 cudaError_t launch_state_combine(const float* S_in, const float* M, const float* E, float* S_out, int64_t count,
                                  cudaStream_t stream);

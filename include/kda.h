@@ -212,6 +212,31 @@ KDA_API kda_status kda_chunk_segment_summary(const void* q, const void* k, const
                                              void* stream);
 
 /*
+ * The decay gate and the full-rank output gate from the layer input ("深入 Kimi-K3: Hugging Face 仓库
+ * 分析", paragraph on KDA: the decay is per channel, driven by a low-rank projection plus a per-head
+ * parameter, with a lower bound of -5; the output gate is full rank; "Kimi K3 架构全景", section 02:
+ * gate lower_bound -5.0).  The pages give no formula; read here as
+ *   gate = x W_gate^T,   z = x W_a^T (rank `rank`),   g = max(-5, -softplus(z W_b^T + a_h))
+ * with a_h one parameter per head (the same for the head's d channels); -softplus keeps every
+ * decay factor exp(g) at most 1 and the floor keeps it at least e^-5.  x W_gate^T and x W_a^T run as
+ * one tcgen05 GEMM over the stacked weights, z W_b^T as a second one with the gate in its epilogue;
+ * fp32 accumulation, z rounded to bf16 between the two.
+ *
+ *  x            bf16 [T, hidden] (row-major)
+ *  w_gate_a     bf16 [H*d + rank, hidden]: rows [0, H*d) W_gate, rows [H*d, H*d + rank) W_a
+ *  w_b          bf16 [H*d, rank]
+ *  a_head       fp32 [H]
+ *  gate         bf16 [T, H*d] out (the `out_gate` of kda_chunk_fwd)
+ *  g            fp32 [T, H, d] out (the `g` of kda_chunk_fwd), in [-5, 0]
+ *  z_workspace  bf16 [T, rank] scratch
+ *  T in [0, 2^31), hidden a positive multiple of 8, d = 128, rank a multiple of 32 in [32, 4096].
+ *  All pointers 16-byte aligned device memory (with T = 0, x, gate, g and z_workspace may be NULL).
+ */
+KDA_API kda_status kda_gate_generator(const void* x, int64_t T, int hidden, const void* w_gate_a, const void* w_b,
+                                      const float* a_head, int H, int d, int rank, void* gate, float* g,
+                                      void* z_workspace, void* stream);
+
+/*
  * The map of a segment applied to a state:  S_out[i] = S_in[i] M[i] + E[i]  for i < count, each a
  * fp32 128 x 128 row-major matrix (S_in NULL: S_out = E).  Folding the segments of a sequence in
  * order with it gives each segment's entering state (see kda_chunk_segment_summary).  Products in

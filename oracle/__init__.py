@@ -17,6 +17,9 @@ The arithmetic lives in ``kda_oracle.c`` (plain C99, fp64, one thread per
 * :func:`output_gate` — o * sigmoid(gate), the full-rank output gate (same paragraph).
 * :func:`recurrent_step` — one decode step: the front end on one token per
   sequence followed by one step of the token loop (``fused_recurrent_kda``).
+* :func:`gate_generator` — the decay gate and the full-rank output gate from the layer input,
+  as read from "深入 Kimi-K3: Hugging Face 仓库分析" (paragraph on KDA: a low-rank projection plus a
+  per-head parameter, floored at -5): gate = x W_gate^T, g = max(-5, -softplus(x W_a^T W_b^T + a_h)).
 * :func:`transition` — a segment's transition operator M = X_1 ... X_L with
   X_t = Diag(alpha_t)(I - beta_t k_t k_t^T), formed as a literal product of dense
   matrices: a segment maps its entering state S to S M + E (E its end state from zero),
@@ -138,6 +141,19 @@ def transition(k, g, beta, cu_seqlens=None, nthreads=None):
                                      nthreads or threads()) != 0:
         raise ValueError("oracle rejected its arguments")
     return M
+
+
+def gate_generator(x, w_gate_a, w_b, a_head, H, d):
+    """(gate [T, H*d], g [T, H, d]) in fp64: gate = x W_gate^T; z = x W_a^T; y = z W_b^T + a_h (a_h the
+    head's parameter on each of its d channels); g = max(-5, -softplus(y)), softplus(y) = log(1 + e^y).
+    w_gate_a stacks W_gate (H*d rows) over W_a (rank rows)."""
+    x, w_gate_a, w_b, a_head = (_f64(t) for t in (x, w_gate_a, w_b, a_head))
+    hd = H * d
+    gate = x @ w_gate_a[:hd].T
+    z = x @ w_gate_a[hd:].T
+    y = z @ w_b.T + np.repeat(a_head, d)[None, :]
+    g = np.maximum(-5.0, -np.logaddexp(0.0, y))
+    return gate, g.reshape(x.shape[0], H, d)
 
 
 def shortconv_silu_l2norm(xq, xk, xv, conv_w, H, d, cu_seqlens=None, conv_state_in=None, eps=1e-6,
