@@ -10,11 +10,12 @@
 // the second GEMM applies W_b with the bound in its epilogue.
 //
 // GEMM: C = A B^T, A [M, K] and B [N, K] bf16 with K innermost, fp32 accumulation in TMEM.
-// Persistent CTAs (one per SM), tiles of 128 x 256 over (M, N), M fastest (the CTAs running at
-// one time share B tiles in L2), K in blocks of 64 through a 4-stage TMA pipeline (128-byte
+// Persistent CTAs (one per SM), tiles of 128 x 256 over (M, N) in groups of 16 row tiles (the CTAs
+// running at one time share A and B bands in L2), K in blocks of 64 through a 4-stage TMA pipeline (128-byte
 // swizzle, the tcgen05 K-major operand layout).  Warp 0 loads, warp 1 issues the products from
-// one elected lane into one of two TMEM accumulators, warps 2-5 read the other accumulator out
-// (lane quarter = warp % 4) and store, so a tile's epilogue overlaps the next tile's products.
+// one elected lane into one of two TMEM accumulators, warps 2-9 read the other accumulator out
+// (lane quarter = warp % 4, half the columns each) and store it through shared memory as whole
+// row segments, so a tile's epilogue overlaps the next tile's products.
 // Every mbarrier wait is bounded; a wait that runs out stops the CTA and reports in the device
 // error word.
 #include <cuda.h>
@@ -30,10 +31,12 @@ namespace {
 
 using namespace tc;
 
-constexpr int kGemmThreads = 192;
+constexpr int kEpiWarps = 8;                           // two per TMEM lane quarter, each half of the columns
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 constexpr int BM = 128, BN = 256, BK = 64, kStages = 4;
 constexpr uint32_t kStageA = BM * BK * 2, kStageB = BN * BK * 2, kStageBytes = kStageA + kStageB;
-constexpr uint32_t G_BAR = kStages * kStageBytes;     // full[4], empty[4], acc_full[2], acc_empty[2], done
+constexpr uint32_t G_STG = kStages * kStageBytes;     // per epilogue warp: 32 rows x 128 bytes of staging
+constexpr uint32_t G_BAR = G_STG + kEpiWarps * 4096;  // full[4], empty[4], acc_full[2], acc_empty[2], done
 constexpr uint32_t G_MISC = G_BAR + 16 * 8;           // TMEM base, abort flag
 constexpr uint32_t kGemmSmem = G_MISC + 16 + 1024;
 constexpr uint32_t kGemmWait = 1u << 24;
@@ -48,33 +51,63 @@ struct GemmEpi {
     int d;
 };
 
-__device__ __forceinline__ float softplus(float x) { return x > 20.f ? x : log1pf(expf(x)); }
+// log(1 + e^x) by the hardware exponential and logarithm; above 15 it is x to fp32 precision
+__device__ __forceinline__ float softplus(float x) { return x > 15.f ? x : __logf(1.f + __expf(x)); }
+
+// Tile t of the persistent loop: groups of kGroupM m-tiles, n-tiles in turn inside a group, m fastest;
+// the CTAs running at one time share a few A row bands and B column bands, which stay in L2.
+constexpr int kGroupM = 16;
+__device__ __forceinline__ void tile_coords(int t, int mt, int nt, int& m0, int& n0) {
+    const int per_group = kGroupM * nt, gi = t / per_group, r = t - gi * per_group;
+    const int gm = mt - gi * kGroupM < kGroupM ? mt - gi * kGroupM : kGroupM;
+    m0 = (gi * kGroupM + r % gm) * BM;
+    n0 = (r / gm) * BN;
+}
 
 // shared-memory descriptor of a K-major 128-byte-swizzled operand tile (8-row groups 1024 bytes apart)
 __device__ __forceinline__ uint64_t kdesc_g(uint32_t saddr) { return sdesc_sw128(saddr, 16, 1024); }
 
-// 32 consecutive accumulator columns [col, col + 32) of one output row
-__device__ __forceinline__ void store_chunk(const GemmEpi& e, int64_t row, int col, int N, const uint32_t (&v)[32]) {
+// Columns [col, col + 32) of rows row0 .. row0 + 31 (this lane: row0 + lane) through the warp's
+// staging rows (128 bytes each, 16-byte chunks swizzled by row), written back as whole row segments.
+__device__ __forceinline__ void store_chunk(const GemmEpi& e, int64_t row0, int M, int col, int N,
+                                            const uint32_t (&v)[32], uint8_t* stg, int lane) {
+    __syncwarp();  // the previous chunk has been read back
     if (e.mode == 0) {
-        __nv_bfloat16* dst = col < e.n_split ? e.c0 + row * e.n_split + col
-                                             : e.c1 + row * (int64_t)(N - e.n_split) + (col - e.n_split);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             uint32_t w[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 w[i] = pack_bf16x2(__uint_as_float(v[8 * j + 2 * i]), __uint_as_float(v[8 * j + 2 * i + 1]));
-            reinterpret_cast<uint4*>(dst)[j] = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        __syncwarp();
+        const bool lo = col < e.n_split;
+        __nv_bfloat16* base = lo ? e.c0 + col : e.c1 + (col - e.n_split);
+        const int64_t ld = lo ? e.n_split : N - e.n_split;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {  // 8 rows of 64 bytes per instruction
+            const int r = 8 * k + (lane >> 2), c = lane & 3;
+            if (row0 + r < M)
+                *reinterpret_cast<uint4*>(base + (row0 + r) * ld + 8 * c) =
+                    *reinterpret_cast<const uint4*>(stg + r * 128 + ((c ^ (r & 7)) << 4));
         }
     } else {
         const float a = e.a_head[col / e.d];  // a chunk of 32 lies inside one head (d a multiple of 32)
-        float* dst = e.g + row * N + col;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             float o[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) o[i] = fmaxf(-5.f, -softplus(__uint_as_float(v[4 * j + i]) + a));
-            reinterpret_cast<float4*>(dst)[j] = make_float4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<float4*>(stg + lane * 128 + ((j ^ (lane & 7)) << 4)) = make_float4(o[0], o[1], o[2], o[3]);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // 4 rows of 128 bytes per instruction
+            const int r = 4 * k + (lane >> 3), c = lane & 7;
+            if (row0 + r < M)
+                *reinterpret_cast<float4*>(e.g + (row0 + r) * N + col + 4 * c) =
+                    *reinterpret_cast<const float4*>(stg + r * 128 + ((c ^ (r & 7)) << 4));
         }
     }
 }
@@ -103,7 +136,7 @@ gemm_gate_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(accf + i, 1);
-            mbar_init(acce + i, 4);  // one arrival per epilogue warp
+            mbar_init(acce + i, kEpiWarps);  // one arrival per epilogue warp
         }
         mbar_init(done, 1);
         fence_mbar_init();
@@ -130,7 +163,8 @@ gemm_gate_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             uint32_t ph = 0, issued = 0, issued_ph = 0;  // bit s: stage s has a load in flight / its round
             bool ok = true;
             for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
-                const int m0 = (t % mt) * BM, n0 = (t / mt) * BN;
+                int m0, n0;
+                tile_coords(t, mt, nt, m0, n0);
                 for (int kb = 0; kb < kbn; ++kb) {
                     if (!(ok = wait(empty + s, ph ^ 1u))) break;
                     fence_proxy_async();
@@ -179,8 +213,10 @@ gemm_gate_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         mma_commit(done);  // every product issued has completed before the TMEM is released
         mbar_wait(done, 0, kGemmWait);
     } else {
-        // ---- epilogue: warps 2-5, lane quarter q = warp % 4 holds rows 32 q .. 32 q + 31 of the tile
-        const int q = warp & 3;
+        // ---- epilogue: warps 2 .. 2 + kEpiWarps - 1; lane quarter q = warp % 4 holds rows 32 q .. 32 q + 31
+        //      of the tile, and warp half hf = (warp - 2) / 4 takes columns 128 hf .. 128 hf + 127
+        const int q = warp & 3, hf = (warp - 2) >> 2;
+        uint8_t* stg = sm + G_STG + (warp - 2) * 4096;
         int it = 0;
         uint32_t fph = 0;
         for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
@@ -188,15 +224,16 @@ gemm_gate_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             if (!wait(accf + a, (fph >> a) & 1u)) break;
             fph ^= 1u << a;
             tc_fence_after();
-            const int m0 = (t % mt) * BM, n0 = (t / mt) * BN;
-            const int64_t row = (int64_t)m0 + 32 * q + lane;
+            int m0, n0;
+            tile_coords(t, mt, nt, m0, n0);
+            const int64_t row0 = (int64_t)m0 + 32 * q;
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
+            for (int c = 128 * hf; c < 128 * hf + 128; c += 32) {
                 uint32_t v[32];
                 tmem_ld32_async(tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(a * BN + c), v);
                 tmem_wait_ld();
                 reg_fence(v);
-                if (row < M && n0 + c < N) store_chunk(epi, row, n0 + c, N, v);
+                if (row0 < M && n0 + c < N) store_chunk(epi, row0, M, n0 + c, N, v, stg, lane);
             }
             tc_fence_before();
             __syncwarp();
