@@ -31,14 +31,22 @@ namespace {
 
 using namespace tc;
 
-constexpr int kEpiWarps = 8;                           // two per TMEM lane quarter, each half of the columns
-constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
-constexpr int BM = 128, BN = 256, BK = 64, kStages = 4;
+constexpr int BM = 128, BN = 256, BK = 64;
 constexpr uint32_t kStageA = BM * BK * 2, kStageB = BN * BK * 2, kStageBytes = kStageA + kStageB;
-constexpr uint32_t G_STG = kStages * kStageBytes;     // per epilogue warp: 32 rows x 128 bytes of staging
-constexpr uint32_t G_BAR = G_STG + kEpiWarps * 4096;  // full[4], empty[4], acc_full[2], acc_empty[2], done
-constexpr uint32_t G_MISC = G_BAR + 16 * 8;           // TMEM base, abort flag
-constexpr uint32_t kGemmSmem = G_MISC + 16 + 1024;
+// Two configurations: the x-side product (K = hidden, long main loop) keeps four stages of operands
+// and eight epilogue warps; the rank product (K = rank, a short main loop and a transcendental epilogue)
+// two stages and sixteen epilogue warps.  Shared memory: stages, 4 KB of staging per epilogue warp
+// (32 rows x 128 bytes), then full[S], empty[S], acc_full[2], acc_empty[2], done, TMEM base, abort flag.
+template <int S, int EW>
+struct GemmCfg {
+    static constexpr int kStages = S, kEpiWarps = EW, kThreads = 64 + 32 * EW;
+    static constexpr uint32_t kStg = S * kStageBytes, kBar = kStg + EW * 4096, kMisc = kBar + 16 * 8;
+    static constexpr uint32_t kSmem = kMisc + 16 + 1024;
+    static_assert(kSmem <= 232448, "shared memory");
+    static_assert(2 * S + 5 <= 16, "barrier space");
+};
+using CfgX = GemmCfg<4, 8>;
+using CfgR = GemmCfg<2, 16>;
 constexpr uint32_t kGemmWait = 1u << 24;
 
 struct GemmEpi {
@@ -112,9 +120,12 @@ __device__ __forceinline__ void store_chunk(const GemmEpi& e, int64_t row0, int 
     }
 }
 
-__global__ void __launch_bounds__(kGemmThreads, 1)
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::kThreads, 1)
 gemm_gate_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N, int K,
                  GemmEpi epi, unsigned int* err) {
+    constexpr int kStages = Cfg::kStages, kEpiWarps = Cfg::kEpiWarps;
+    constexpr uint32_t G_STG = Cfg::kStg, G_BAR = Cfg::kBar, G_MISC = Cfg::kMisc;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
@@ -214,7 +225,8 @@ gemm_gate_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         mbar_wait(done, 0, kGemmWait);
     } else {
         // ---- epilogue: warps 2 .. 2 + kEpiWarps - 1; lane quarter q = warp % 4 holds rows 32 q .. 32 q + 31
-        //      of the tile, and warp half hf = (warp - 2) / 4 takes columns 128 hf .. 128 hf + 127
+        //      of the tile, and part hf = (warp - 2) / 4 of the kEpiWarps / 4 parts takes BN / parts columns
+        constexpr int kCols = BN / (kEpiWarps / 4);
         const int q = warp & 3, hf = (warp - 2) >> 2;
         uint8_t* stg = sm + G_STG + (warp - 2) * 4096;
         int it = 0;
@@ -228,7 +240,7 @@ gemm_gate_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             tile_coords(t, mt, nt, m0, n0);
             const int64_t row0 = (int64_t)m0 + 32 * q;
 #pragma unroll 1
-            for (int c = 128 * hf; c < 128 * hf + 128; c += 32) {
+            for (int c = kCols * hf; c < kCols * hf + kCols; c += 32) {
                 uint32_t v[32];
                 tmem_ld32_async(tbase + ((uint32_t)(32 * q) << 16) + (uint32_t)(a * BN + c), v);
                 tmem_wait_ld();
@@ -271,19 +283,21 @@ bool encode_operand(CUtensorMap* m, const void* base, int64_t rows, int64_t K, i
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <class Cfg>
 cudaError_t gemm(const void* A, const void* B, int M, int N, int K, const GemmEpi& epi, unsigned int* err,
                  cudaStream_t stream) {
     if (M <= 0 || N <= 0) return cudaSuccess;
     CUtensorMap ta, tb;
     if (!encode_operand(&ta, A, M, K, BM) || !encode_operand(&tb, B, N, K, BN)) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(gemm_gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_gate_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmem);
     int dev = 0, sms = 0;
     if (e == cudaSuccess) e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int grid = (int)(tiles < sms ? tiles : sms);
-    gemm_gate_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(ta, tb, M, N, K, epi, err);
+    gemm_gate_kernel<Cfg><<<grid, Cfg::kThreads, Cfg::kSmem, stream>>>(ta, tb, M, N, K, epi, err);
     return cudaGetLastError();
 }
 
@@ -294,10 +308,10 @@ cudaError_t launch_gate_generator(const void* x, int64_t T, int hidden, const vo
                                   unsigned int* err, cudaStream_t stream) {
     const int hd = H * d;
     GemmEpi e1{0, hd, static_cast<__nv_bfloat16*>(gate), static_cast<__nv_bfloat16*>(z), nullptr, nullptr, d};
-    cudaError_t e = gemm(x, w_gate_a, (int)T, hd + rank, hidden, e1, err, stream);
+    cudaError_t e = gemm<CfgX>(x, w_gate_a, (int)T, hd + rank, hidden, e1, err, stream);
     if (e != cudaSuccess) return e;
     GemmEpi e2{1, hd, nullptr, nullptr, g, a_head, d};
-    return gemm(z, w_b, (int)T, hd, rank, e2, err, stream);
+    return gemm<CfgR>(z, w_b, (int)T, hd, rank, e2, err, stream);
 }
 
 }  // namespace kda
