@@ -409,6 +409,24 @@ def run_ours(args):
     fe_bytes = 2 * 3 * wf.T * Cw * 2 + 3 * Cw * 4 * 2   # raw in + normalised out (bf16) + weights
     fe_gbs = fe_bytes / (ms_fe_launch * 1e-3) / 1e9
 
+    # ---------------- the gates from the layer input (kda_gate_generator): two tensor-core GEMMs ----------
+    # x [8192, 7168] -> output gate [8192, 12288] and, through a rank-128 projection, the decay gate g
+    Tg, hid, rk = 8192, 7168, 128
+    ggen = torch.Generator(device=device).manual_seed(53007)
+    xg = torch.randn(Tg, hid, device=device, generator=ggen).to(torch.bfloat16)
+    wga = (torch.randn(w.H * w.d + rk, hid, device=device, generator=ggen) / hid ** 0.5).to(torch.bfloat16)
+    wgb = (torch.randn(w.H * w.d, rk, device=device, generator=ggen) / rk ** 0.5).to(torch.bfloat16)
+    ah = torch.randn(w.H, device=device, generator=ggen)
+    gate_o = torch.empty((Tg, w.H * w.d), dtype=torch.bfloat16, device=device)
+    g_o = torch.empty((Tg, w.H, w.d), dtype=torch.float32, device=device)
+    z_o = torch.empty((Tg, rk), dtype=torch.bfloat16, device=device)
+    gstep = lambda: kda.kda_gate_generator(xg, wga, wgb, ah, w.H, w.d, gate=gate_o, g=g_o, z=z_o, stream=stream)
+    gsteps = max(10, args.steps // 4)
+    ms_gate, ms_gate_launch, _ = timed(gstep, gsteps, args.warmup, stream, dist)
+    gflops = 2 * Tg * hid * (w.H * w.d + rk) + 2 * Tg * rk * w.H * w.d
+    gate_tflops = gflops / (ms_gate_launch * 1e-3) / 1e12
+    del xg, wga, wgb, ah, gate_o, g_o, z_o
+
     # ---------------- front end + prefill from raw inputs: fused vs two passes (the long workload's path) ----
     gf = fill_device(wf.seed, ks.TID_G, ks.NEG_SOFTPLUS5, (wf.T, wf.H, wf.d), "f32", device=device)
     bf = fill_device(wf.seed, ks.TID_BETA, ks.SIGMOID, (wf.T, wf.H), "f32", device=device)
@@ -482,6 +500,14 @@ def run_ours(args):
     }
     if seg is not None:
         line["segmented_prefill"] = seg
+    line["gate_generator"] = {
+        "workload": f"x bf16 [{Tg}, {hid}] -> output gate bf16 [{Tg}, {w.H * w.d}] and decay gate g = max(-5, "
+                    f"-softplus(x W_a^T W_b^T + a_h)) fp32 [{Tg}, {w.H}, {w.d}], rank {rk}; random weights",
+        "value": gate_tflops, "unit": "TFLOP/s", "ms_per_step": ms_gate, "steps": gsteps, "gpu_launches": 2 * gsteps,
+        "algorithmic_flops_per_launch": gflops,
+        "roofline": {"bound": "tensor", "achieved": gate_tflops, "peak": tc_peak, "unit": "TFLOP/s",
+                     "frac": gate_tflops / tc_peak, "traffic": None, "peak_source": peak_src,
+                     "kernel": "gemm_gate_kernel x2 (x [W_gate ; W_a]^T, then the rank product with the gate epilogue)"}}
     line["fused_prefill"] = {
         "workload": "frontend_32k raw q, k, v bf16 [32768, 12288] + g = max(-5, -softplus(z)), beta -> "
                     "ShortConv(4)+SiLU+L2norm -> chunk_kda (the long workload's path at 32K tokens)",
