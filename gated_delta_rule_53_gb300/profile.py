@@ -1,7 +1,7 @@
 """Profiling harness: runs one entry point of the library on a named synthetic case a
 few times, so that a profiler can capture a handful of launches of one kernel.
 
-  python -m gated_delta_rule_53_gb300.profile {prefill_8k,prefill_2k,decode_64,decode_16,frontend_8k} [--iters N]
+  python -m gated_delta_rule_53_gb300.profile {prefill_8k,prefill_2k,decode_64,decode_16,frontend_8k,gates_8k} [--iters N]
 
 Cases (all inputs larger than the 129 MB L2, a few GB on the device at most):
   prefill_8k   kda_chunk_fwd, 1 x 8192 tokens x 96 heads, bf16
@@ -9,6 +9,7 @@ Cases (all inputs larger than the 129 MB L2, a few GB on the device at most):
   decode_64    kda_recurrent_step, 64 sequences x 96 heads
   decode_16    kda_recurrent_step, 16 sequences x 96 heads
   frontend_8k  kda_shortconv_l2norm, 8192 tokens x 96 heads, bf16 out
+  gates_8k     kda_gate_generator, x 8192 x 7168 -> 96 x 128 gate channels, rank 128 (bench.py's sizes)
 """
 from __future__ import annotations
 
@@ -29,7 +30,7 @@ def main():
     from kda_synth.device import fill_device
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["prefill_8k", "prefill_2k", "decode_64", "decode_16", "frontend_8k"])
+    ap.add_argument("case", choices=["prefill_8k", "prefill_2k", "decode_64", "decode_16", "frontend_8k", "gates_8k"])
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     torch.cuda.set_device(0)
@@ -54,6 +55,14 @@ def main():
         st = fill_device(w.seed, ks.TID_STATE, ks.NORMAL, (N, 96, 128, 128), "f32", 0.0, 0.02, device=dev)
         cs = fill_device(w.seed, ks.TID_CONV_STATE, ks.NORMAL, (N, 3, 3 * C), "bf16", device=dev)
         fn = lambda: kda.kda_recurrent_step(*xs, cw, g, b, st, cs)
+    elif args.case == "gates_8k":
+        T, hid, H, d, rk = 8192, 7168, 96, 128, 128
+        gen = torch.Generator(device=dev).manual_seed(53007)
+        x = torch.randn(T, hid, device=dev, generator=gen).to(torch.bfloat16)
+        wga = (torch.randn(H * d + rk, hid, device=dev, generator=gen) / hid ** 0.5).to(torch.bfloat16)
+        wgb = (torch.randn(H * d, rk, device=dev, generator=gen) / rk ** 0.5).to(torch.bfloat16)
+        ah = torch.randn(H, device=dev, generator=gen)
+        fn = lambda: kda.kda_gate_generator(x, wga, wgb, ah, H, d)
     else:
         T, C = 8192, 96 * 128
         xs = [fill_device(53005, t, ks.NORMAL, (T, C), "bf16", device=dev) for t in (1, 2, 3)]
