@@ -21,9 +21,11 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Every tensor pointer (and the prefill's workspace) is CALLER-OWNED DEVICE
- *    memory on the current CUDA device.  The library allocates nothing, frees
- *    nothing and keeps no state between calls (apart from one device error
- *    word, see kda_device_error).
+ *    memory on the current CUDA device.  The library allocates no device memory,
+ *    frees nothing and keeps no state between calls apart from one device error
+ *    word (see kda_device_error) and, per device, two CUDA streams that
+ *    kda_chunk_fwd creates on its first overlapped call (see kda_chunk_fwd; make
+ *    that first call outside a stream capture).
  *  - Calls are asynchronous: they check their arguments on the host, enqueue
  *    kernels on `stream` (a cudaStream_t; NULL = legacy default stream) and
  *    return.  An argument error returns before anything is enqueued.  A launch
@@ -127,6 +129,12 @@ KDA_API kda_status kda_shortconv_l2norm(const void* xq, const void* xk, const vo
  *                  least the `min_bytes` of kda_chunk_fwd_workspace_size and runs
  *                  fastest with `full_bytes`; with less, the chunks are processed in
  *                  several ranges.  KDA_DTYPE_F32 ignores it (may be NULL, 0).
+ *
+ * With the whole workspace (`full_bytes`) and at least 128 chunk rows, consecutive ranges of
+ * max(64, rows / 8) chunk rows overlap: the call forks two internal streams from `stream` with
+ * events (the operand kernel on a low-priority one, the state pass on a high-priority one) and
+ * makes `stream` wait for both before it returns; nothing else changes for the caller, and the
+ * results are the same bits as one range.
  *
  * The bf16 path runs two kernels per range of chunks: the first computes, for every
  * (chunk, head) at once, everything that does not depend on the carried state (the
