@@ -35,7 +35,7 @@
 // state path reads them (128-byte-swizzled tiles), so that one bulk copy brings each in:
 //   B1    [W ; Q e^G]       bf16 [128][128]   B of the S0 products
 //   U     fp32 [64][128]                      V' = U - Y
-//   A_qk  (tf32 words)           [64][64]     B of O^T += V'^T A_qk^T
+//   A_qk  hi, lo            bf16 [64][64] x2  B of O^T += V'^T A_qk^T
 //   KP    K e^{G_C - G}     bf16 [64][128]    B (MN-major) of dS = V'^T KP
 //   e^{G_C}                 fp32 [128]
 // chunk_state_kernel then walks each (sequence, head) chain in order, one CTA of 16 warps
@@ -46,8 +46,9 @@
 // the output product and its store overlap the next chunk's first product.
 //
 // Precision.  Products accumulate in fp32 in TMEM.  W and U come from T Diag(beta) split as
-// hi + lo in bf16 (two bf16 products each, T kept to about 16 bits); A_qk V' runs on
-// kind::tf32; the other operands are bf16.  T = (I + A_kk)^-1 is computed in fp32 on the CUDA
+// hi + lo in bf16 (two bf16 products each, T kept to about 16 bits); V'^T A_qk^T runs as
+// three bf16 products of the hi/lo splits of both (hi hi + hi lo + lo hi); the other
+// operands are bf16.  T = (I + A_kk)^-1 is computed in fp32 on the CUDA
 // cores by 16 x 16 blocks: the four diagonal blocks D by forward substitution, then the blocks
 // below them as (I - N + N^2 - N^3) D with N = D A_below (N^4 = 0).
 //

@@ -44,12 +44,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
            | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
 }
 
-// Instruction descriptor of tcgen05.mma kind::tf32: tf32 A and B (fp32 words, K-major), fp32 D.
-__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
-    return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
-           (static_cast<uint32_t>(M >> 4) << 24);
-}
-
 // ---------------------------------------------------------------------------------------------
 // mbarriers
 // ---------------------------------------------------------------------------------------------
@@ -153,25 +147,6 @@ __device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, ui
         "@pe tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pa;\n\t}\n" ::"r"(d_tmem),
         "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
-}
-
-// D (+)= A * B^T with tf32 operands (K = 8 per instruction).
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred pe, pa;\n\t"
-        "elect.sync _|pe, 0xffffffff;\n\t"
-        "setp.ne.b32 pa, %4, 0;\n\t"
-        "@pe tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, pa;\n\t}\n" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// fp32 -> tf32 (round to nearest, ties away from zero); the low 13 bits of the result are zero.
-__device__ __forceinline__ float to_tf32(float x) {
-    uint32_t y;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(y) : "f"(x));
-    return __uint_as_float(y);
 }
 
 // Warp-collective: the mbarrier receives one arrival when every MMA the elected lane issued
