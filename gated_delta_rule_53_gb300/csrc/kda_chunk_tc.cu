@@ -47,8 +47,9 @@
 //
 // Precision.  Products accumulate in fp32 in TMEM.  W and U come from T Diag(beta) split as
 // hi + lo in bf16 (two bf16 products each, T kept to about 16 bits); V'^T A_qk^T runs as
-// three bf16 products of the hi/lo splits of both (hi hi + hi lo + lo hi); the other
-// operands are bf16.  T = (I + A_kk)^-1 is computed in fp32 on the CUDA
+// three bf16 products of the hi/lo splits of both (hi hi + hi lo + lo hi); the state update
+// V'^T KP takes V' as hi + lo (two bf16 products), so the rounding of V' does not build up in
+// the state over a long chain; the other operands are bf16.  T = (I + A_kk)^-1 is computed in fp32 on the CUDA
 // cores by 16 x 16 blocks: the four diagonal blocks D by forward substitution, then the blocks
 // below them as (I - N + N^2 - N^3) D with N = D A_below (N^4 = 0).
 //
@@ -943,8 +944,8 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
                 mma_bf16_ta(tbase + 128 * b + 64, tbase + TM_SA + 8 * ks,
                             kdesc(b1 + (ks >> 2) * 16384 + 8192) + (ks & 3) * 2, id_64, ks > 0 ? 1u : 0u);
             if (ahead) load_b1(mm + 2, b3 == 0 ? 2 : b3 - 1);  // the previous chunk's B1 and e^{G_C} are consumed
-            // ---- dS = V'^T (K e^{G_C - G}) (the state waits for it), then O^T += V'^T A_qk^T as
-            //      hi.hi + hi.lo + lo.hi; A = V'^T from TMEM
+            // ---- dS = (V'_hi + V'_lo)^T (K e^{G_C - G}) (the state waits for it), then O^T += V'^T A_qk^T
+            //      as hi.hi + hi.lo + lo.hi; A = V'^T from TMEM
             nb_sync(NB_V);
             wait(barK + b, (ph >> (5 + b)) & 1u);
             ph ^= 32u << b;
@@ -954,6 +955,10 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
             for (int ks = 0; ks < 4; ++ks)
                 mma_bf16_ta(tbase + TM_DS, tbase + TM_VH + 8 * ks, sdesc_sw128(aq + kKPOff, 8192, 1024) + ks * 128,
                             id_ds, ks > 0 ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                mma_bf16_ta(tbase + TM_DS, tbase + TM_VL + 8 * ks, sdesc_sw128(aq + kKPOff, 8192, 1024) + ks * 128,
+                            id_ds, 1u);
             mma_commit(barD);
             wait(barD, phD);
             phD ^= 1u;

@@ -156,6 +156,50 @@ def test_chunk_packed_equals_separate(kda):
         assert torch.equal(o1, o[sl]) and torch.equal(f1[0], fs[n])
 
 
+DEGENERATE = ("no_decay", "floor", "mixed_channels", "beta0", "beta1", "repeated_key")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("case", DEGENERATE)
+def test_chunk_degenerate_gates_and_betas(kda, orc, case, dtype):
+    """The method's limiting cases, each against the oracle on the same bits:
+    no_decay (g = 0: the plain delta rule), floor (g = -5 everywhere: a 16-token block spans the
+    full e^75 of the split intra-chunk factor), mixed_channels (per key channel g is 0 or -5: some
+    channels never forget, the rest forget at once), beta0 (no writes: the state only decays),
+    beta1 (full overwrite along k), repeated_key (one key for a whole sequence, beta = 1: every
+    off-diagonal entry of A_kk is 1 and T = (I + A_kk)^-1 is bidiagonal)."""
+    lengths = [200, 64, 1, 130]
+    w, q, k, v, g, b, s0 = small_prefill(110, lengths, 2, dtype, init_std=0.02)
+    T, H, d = w.T, w.H, w.d
+    cu = w.cu_seqlens()
+    if case == "no_decay":
+        g = np.zeros_like(g)
+    elif case == "floor":
+        g = np.full_like(g, -5.0)
+    elif case == "mixed_channels":
+        mask = (ks.u64(110, ks.TID_G, 0, H * d) & 1).astype(bool).reshape(H, d)
+        g = np.broadcast_to(np.where(mask, np.float32(-5.0), np.float32(0.0)), g.shape).copy()
+    elif case == "beta0":
+        g = np.full_like(g, -0.02)
+        b = np.zeros_like(b)
+    elif case == "beta1":
+        b = np.ones_like(b)
+    elif case == "repeated_key":
+        g = np.zeros_like(g)
+        b = np.ones_like(b)
+        k = k.copy()
+        for n in range(w.N):
+            k[cu[n]:cu[n + 1]] = k[cu[n]]
+    o, fs = run_chunk(kda, w, q, k, v, g, b, s0)
+    o_ref, fs_ref = oracle_chunk(orc, w, q, k, v, g, b, s0)
+    if dtype == "f32":
+        assert orc.rel_l2(host(o), o_ref) <= F32_REL and orc.rel_l2(host(fs), fs_ref) <= F32_REL
+    else:
+        assert orc.rel_l2(host(o), o_ref) <= BF16_O_REL and orc.max_abs(host(o), o_ref) <= BF16_O_ABS
+        assert orc.rel_l2(host(fs), fs_ref) <= BF16_S_REL
+    assert kda.device_error() == 0
+
+
 @pytest.mark.parametrize("rows", [1, 3])
 def test_chunk_workspace_ranges(kda, orc, rows):
     """A workspace of `rows` chunk rows runs the chunks in ranges; chains that cross a range carry
@@ -289,8 +333,10 @@ def decode_inputs(w):
     return xs, w.conv_w(), g, b, w.init_state(), w.conv_state()
 
 
-def check_decode(kda, orc, w, scale=1.0, steps=1):
+def check_decode(kda, orc, w, scale=1.0, steps=1, gates=None):
     xs, cw, g, b, s0, cs = decode_inputs(w)
+    if gates is not None:
+        g, b = gates(g, b)
     s_dev, cs_dev = dev(s0), dev(cs)
     s_ref, cs_ref = s0.astype(np.float64), ks.to_f64(cs)
     for step in range(steps):
@@ -308,6 +354,16 @@ def check_decode(kda, orc, w, scale=1.0, steps=1):
 def test_decode_small(kda, orc):
     w = ks.Workload("d", "decode", 301, H=3, lengths=[1] * 5, init_state_std=0.02)
     check_decode(kda, orc, w, scale=0.5, steps=8)
+
+
+@pytest.mark.parametrize("case", ["no_decay_full_write", "floor_no_write", "floor_full_write"])
+def test_decode_degenerate_gates(kda, orc, case):
+    """g = 0 with beta = 1 (the plain delta rule overwriting along k), g = -5 with beta = 0 (the state
+    only decays, by e^-5 a step) and g = -5 with beta = 1, over four chained steps."""
+    g_val, b_val = {"no_decay_full_write": (0.0, 1.0), "floor_no_write": (-5.0, 0.0),
+                    "floor_full_write": (-5.0, 1.0)}[case]
+    w = ks.Workload("d", "decode", 303, H=3, lengths=[1] * 5, init_state_std=0.02)
+    check_decode(kda, orc, w, steps=4, gates=lambda g, b: (np.full_like(g, g_val), np.full_like(b, b_val)))
 
 
 def test_decode_full_workload(kda, orc):
