@@ -506,7 +506,8 @@ def run_ours(args):
         "value": gate_tflops, "unit": "TFLOP/s", "ms_per_step": ms_gate, "steps": gsteps, "gpu_launches": 2 * gsteps,
         "algorithmic_flops_per_launch": gflops,
         "roofline": {"bound": "tensor", "achieved": gate_tflops, "peak": tc_peak, "unit": "TFLOP/s",
-                     "frac": gate_tflops / tc_peak, "traffic": None, "peak_source": peak_src,
+                     "frac": gate_tflops / tc_peak,
+                     "traffic": measured_traffic("gemm_gate_kernel", "kda_gate.cu", "gates_8k"), "peak_source": peak_src,
                      "kernel": "gemm_gate_kernel x2 (x [W_gate ; W_a]^T, then the rank product with the gate epilogue)"}}
     line["fused_prefill"] = {
         "workload": "frontend_32k raw q, k, v bf16 [32768, 12288] + g = max(-5, -softplus(z)), beta -> "
