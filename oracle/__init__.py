@@ -20,6 +20,9 @@ The arithmetic lives in ``kda_oracle.c`` (plain C99, fp64, one thread per
 * :func:`gate_generator` — the decay gate and the full-rank output gate from the layer input,
   as read from "深入 Kimi-K3: Hugging Face 仓库分析" (paragraph on KDA: a low-rank projection plus a
   per-head parameter, floored at -5): gate = x W_gate^T, g = max(-5, -softplus(x W_a^T W_b^T + a_h)).
+* :func:`kda_tokenloop_bwd` — the gradients of a loss with respect to q, k, v, g, beta and the
+  initial state, by reverse mode through the token loop (the backward of ``chunk_kda``; the
+  pages name the operator and its training use, "月之暗面发布Kimi K3开源大模型技术报告", 架构).
 * :func:`transition` — a segment's transition operator M = X_1 ... X_L with
   X_t = Diag(alpha_t)(I - beta_t k_t k_t^T), formed as a literal product of dense
   matrices: a segment maps its entering state S to S M + E (E its end state from zero),
@@ -63,10 +66,12 @@ def _load():
         lib.oracle_kda_tokenloop.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, D, P, P, ctypes.c_int]
         lib.oracle_kda_chunked.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, D, I, P, P, ctypes.c_int]
         lib.oracle_kda_transition.argtypes = [P, P, P, P, I, I, I, I, P, ctypes.c_int]
+        lib.oracle_kda_tokenloop_bwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, D, P, P, P, P, P, P, P, P,
+                                                 ctypes.c_int]
         lib.oracle_shortconv_silu_l2norm.argtypes = [P, P, P, I, P, P, I, I, I, I, P, D, P, P, P, P,
                                                      ctypes.c_int]
         for f in (lib.oracle_kda_tokenloop, lib.oracle_kda_chunked, lib.oracle_shortconv_silu_l2norm,
-                  lib.oracle_kda_transition):
+                  lib.oracle_kda_transition, lib.oracle_kda_tokenloop_bwd):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -127,6 +132,30 @@ def kda_tokenloop(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale=1.0,
 def kda_chunked(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale=1.0, chunk=64, nthreads=None):
     """The same pair computed chunk by chunk (unit-triangular solve per chunk)."""
     return _kda(_load().oracle_kda_chunked, q, k, v, g, beta, init_state, cu_seqlens, scale, chunk, nthreads)
+
+
+def kda_tokenloop_bwd(q, k, v, g, beta, d_o, init_state=None, cu_seqlens=None, scale=1.0, d_final=None,
+                      nthreads=None):
+    """Gradients of a loss through the per-token recurrence, by reverse mode: given dL/do [T,H,dv] and
+    dL/dS_end [N,H,dv,dk] (None = 0), returns (dq, dk [T,H,dk], dv [T,H,dv], dg [T,H,dk],
+    dbeta [T,H], dL/dS0 [N,H,dv,dk])."""
+    q, k, v, g, beta, d_o = (_f64(x) for x in (q, k, v, g, beta, d_o))
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    assert k.shape == (T, H, dk) and g.shape == (T, H, dk) and v.shape == (T, H, dv) and d_o.shape == (T, H, dv)
+    assert beta.shape == (T, H)
+    cu, N = _cu(cu_seqlens, T)
+    s0, dfin = _f64(init_state), _f64(d_final)
+    for x in (s0, dfin):
+        if x is not None:
+            assert x.shape == (N, H, dv, dk)
+    dq, dkk, dg = (np.empty((T, H, dk)) for _ in range(3))
+    dvv, db, ds0 = np.empty((T, H, dv)), np.empty((T, H)), np.empty((N, H, dv, dk))
+    if _load().oracle_kda_tokenloop_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(s0), _ptr(cu), N, T,
+                                        H, dk, dv, float(scale), _ptr(d_o), _ptr(dfin), _ptr(dq), _ptr(dkk),
+                                        _ptr(dvv), _ptr(dg), _ptr(db), _ptr(ds0), nthreads or threads()) != 0:
+        raise ValueError("oracle rejected its arguments")
+    return dq, dkk, dvv, dg, db, ds0
 
 
 def transition(k, g, beta, cu_seqlens=None, nthreads=None):

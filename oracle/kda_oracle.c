@@ -404,3 +404,167 @@ int oracle_kda_transition(const double* k, const double* g, const double* beta, 
     tr_ctx c = {k, g, beta, cu_seqlens, N, T_total, H, dk, M};
     return run_queue(transition_chain, &c, N * H, (size_t)(3 * dk * dk), nthreads);
 }
+
+/* ---------------------------------------------------------------------------------------- */
+/* O1 backward: reverse mode through the token loop                                         */
+/* ---------------------------------------------------------------------------------------- */
+
+/*
+ * Gradients of a loss L through the recurrence of O1, given dL/do_t for every token and
+ * dL/dS_end for every chain (NULL = 0).  With Sb = dL/dS_t (starting from dL/dS_end), token
+ * by token from the last (the chain rule applied to each line of tokenloop_chain, in reverse):
+ *   Sb      += scale do_t q_t^T                        o_t = scale S_t q_t
+ *   dq_t     = scale S_t^T do_t
+ *   eb[i]    = sum_j Sb[i][j] k_t[j]                   S_t = S~ + e k_t^T
+ *   dk_t[j]  = sum_i Sb[i][j] e[i]
+ *   dbeta_t  = sum_i eb[i] (v_t[i] - p[i])             e = beta_t (v_t - p)
+ *   dv_t[i]  = beta_t eb[i]
+ *   pb[i]    = -beta_t eb[i]
+ *   S~b      = Sb + pb k_t^T                           p = S~ k_t
+ *   dk_t[j] += sum_i S~[i][j] pb[i]
+ *   dg_t[j]  = sum_i S~b[i][j] S~[i][j]                S~ = S_{t-1} Diag(exp g_t)
+ *   Sb       = S~b Diag(exp g_t)                       (now dL/dS_{t-1})
+ * and dL/dS0 = Sb after the first token.  The states S~_t are recomputed forward from
+ * checkpoints of S taken every kBwdBlock tokens (the same arithmetic as O1), so that a chain
+ * needs kBwdBlock states at a time instead of one per token.
+ */
+enum { kBwdBlock = 64 };
+
+typedef struct {
+    const double *q, *k, *v, *g, *beta, *init_state, *d_o, *d_final;
+    const int64_t* cu;
+    int64_t N, T, H, dk, dv, max_blocks;
+    double scale;
+    double *dq, *dkk, *dvv, *dg, *dbeta, *d_init;
+} bwd_ctx;
+
+static void tokenloop_bwd_chain(void* vctx, int64_t item, double* work) {
+    const bwd_ctx* c = (const bwd_ctx*)vctx;
+    const int64_t n = item / c->H, h = item % c->H, dk = c->dk, dv = c->dv, H = c->H, SZ = dv * dk;
+    const int64_t bos = c->cu ? c->cu[n] : 0, eos = c->cu ? c->cu[n + 1] : c->T;
+    double* ckpt = work;                          /* [max_blocks][dv*dk]: S at each block start */
+    double* St = ckpt + c->max_blocks * SZ;       /* [kBwdBlock][dv*dk]: S~_t of the block */
+    double* E = St + kBwdBlock * SZ;              /* [kBwdBlock][dv]: e_t */
+    double* Pv = E + kBwdBlock * dv;              /* [kBwdBlock][dv]: p_t */
+    double* S = Pv + kBwdBlock * dv;              /* [dv*dk] running state / S_t */
+    double* Sb = S + SZ;                          /* [dv*dk] dL/dS */
+    double* alpha = Sb + SZ;                      /* [dk] */
+    double* eb = alpha + dk;                      /* [dv] */
+    const int64_t L = eos - bos, nb = (L + kBwdBlock - 1) / kBwdBlock;
+    /* forward: S at every block start */
+    if (c->init_state) memcpy(S, c->init_state + (n * H + h) * SZ, sizeof(double) * SZ);
+    else memset(S, 0, sizeof(double) * SZ);
+    for (int64_t t = bos; t < eos; ++t) {
+        if ((t - bos) % kBwdBlock == 0) memcpy(ckpt + ((t - bos) / kBwdBlock) * SZ, S, sizeof(double) * SZ);
+        const double* kt = c->k + (t * H + h) * dk;
+        const double* gt = c->g + (t * H + h) * dk;
+        const double* vt = c->v + (t * H + h) * dv;
+        const double bt = c->beta[t * H + h];
+        for (int64_t j = 0; j < dk; ++j) alpha[j] = exp(gt[j]);
+        for (int64_t i = 0; i < dv; ++i) {
+            double p = 0.0;
+            for (int64_t j = 0; j < dk; ++j) {
+                S[i * dk + j] *= alpha[j];
+                p += S[i * dk + j] * kt[j];
+            }
+            const double e = bt * (vt[i] - p);
+            for (int64_t j = 0; j < dk; ++j) S[i * dk + j] += e * kt[j];
+        }
+    }
+    /* reverse */
+    if (c->d_final) memcpy(Sb, c->d_final + (n * H + h) * SZ, sizeof(double) * SZ);
+    else memset(Sb, 0, sizeof(double) * SZ);
+    for (int64_t b = nb - 1; b >= 0; --b) {
+        const int64_t t0 = bos + b * kBwdBlock, t1 = (t0 + kBwdBlock < eos) ? t0 + kBwdBlock : eos;
+        memcpy(S, ckpt + b * SZ, sizeof(double) * SZ);
+        for (int64_t t = t0; t < t1; ++t) {  /* the block's S~_t, p_t, e_t again */
+            const double* kt = c->k + (t * H + h) * dk;
+            const double* gt = c->g + (t * H + h) * dk;
+            const double* vt = c->v + (t * H + h) * dv;
+            const double bt = c->beta[t * H + h];
+            double* st = St + (t - t0) * SZ;
+            for (int64_t j = 0; j < dk; ++j) alpha[j] = exp(gt[j]);
+            for (int64_t i = 0; i < dv; ++i) {
+                double p = 0.0;
+                for (int64_t j = 0; j < dk; ++j) {
+                    st[i * dk + j] = S[i * dk + j] * alpha[j];
+                    p += st[i * dk + j] * kt[j];
+                }
+                Pv[(t - t0) * dv + i] = p;
+                E[(t - t0) * dv + i] = bt * (vt[i] - p);
+                for (int64_t j = 0; j < dk; ++j) S[i * dk + j] = st[i * dk + j] + E[(t - t0) * dv + i] * kt[j];
+            }
+        }
+        for (int64_t t = t1 - 1; t >= t0; --t) {
+            const double* kt = c->k + (t * H + h) * dk;
+            const double* qt = c->q + (t * H + h) * dk;
+            const double* vt = c->v + (t * H + h) * dv;
+            const double* gt = c->g + (t * H + h) * dk;
+            const double* dot = c->d_o + (t * H + h) * dv;
+            const double bt = c->beta[t * H + h];
+            const double* st = St + (t - t0) * SZ;
+            const double* e = E + (t - t0) * dv;
+            const double* p = Pv + (t - t0) * dv;
+            double* dqt = c->dq + (t * H + h) * dk;
+            double* dkt = c->dkk + (t * H + h) * dk;
+            double* dvt = c->dvv + (t * H + h) * dv;
+            double* dgt = c->dg + (t * H + h) * dk;
+            for (int64_t j = 0; j < dk; ++j) {
+                alpha[j] = exp(gt[j]);
+                dqt[j] = 0.0;
+                dkt[j] = 0.0;
+                dgt[j] = 0.0;
+            }
+            /* S_t = S~ + e k^T; dq = scale S_t^T do; Sb += scale do q^T */
+            for (int64_t i = 0; i < dv; ++i)
+                for (int64_t j = 0; j < dk; ++j) {
+                    const double s = st[i * dk + j] + e[i] * kt[j];
+                    dqt[j] += c->scale * s * dot[i];
+                    Sb[i * dk + j] += c->scale * dot[i] * qt[j];
+                }
+            double db = 0.0;
+            for (int64_t i = 0; i < dv; ++i) {
+                double acc = 0.0;
+                for (int64_t j = 0; j < dk; ++j) {
+                    acc += Sb[i * dk + j] * kt[j];
+                    dkt[j] += Sb[i * dk + j] * e[i];
+                }
+                eb[i] = acc;
+                db += acc * (vt[i] - p[i]);
+                dvt[i] = bt * acc;
+            }
+            c->dbeta[t * H + h] = db;
+            for (int64_t i = 0; i < dv; ++i) {
+                const double pb = -bt * eb[i];
+                for (int64_t j = 0; j < dk; ++j) {
+                    const double sb = Sb[i * dk + j] + pb * kt[j];   /* dL/dS~ */
+                    dkt[j] += st[i * dk + j] * pb;
+                    dgt[j] += sb * st[i * dk + j];
+                    Sb[i * dk + j] = sb * alpha[j];
+                }
+            }
+        }
+    }
+    if (c->d_init) memcpy(c->d_init + (n * H + h) * SZ, Sb, sizeof(double) * SZ);
+}
+
+int oracle_kda_tokenloop_bwd(const double* q, const double* k, const double* v, const double* g,
+                             const double* beta, const double* init_state, const int64_t* cu_seqlens,
+                             int64_t N, int64_t T_total, int64_t H, int64_t dk, int64_t dv, double scale,
+                             const double* d_o, const double* d_final, double* dq, double* dkk, double* dvv,
+                             double* dg, double* dbeta, double* d_init, int nthreads) {
+    if (!q || !k || !v || !g || !beta || !d_o || !dq || !dkk || !dvv || !dg || !dbeta || H < 1 || dk < 1 ||
+        dv < 1 || T_total < 0)
+        return -1;
+    if (check_seqlens(cu_seqlens, N, T_total)) return -1;
+    int64_t max_len = 0;
+    for (int64_t n = 0; n < N; ++n) {
+        const int64_t len = cu_seqlens ? cu_seqlens[n + 1] - cu_seqlens[n] : T_total;
+        if (len > max_len) max_len = len;
+    }
+    const int64_t max_blocks = (max_len + kBwdBlock - 1) / kBwdBlock;
+    bwd_ctx c = {q, k, v, g, beta, init_state, d_o, d_final, cu_seqlens, N, T_total, H, dk, dv, max_blocks,
+                 scale, dq, dkk, dvv, dg, dbeta, d_init};
+    const size_t scratch = (size_t)((max_blocks + kBwdBlock + 2) * dv * dk + 2 * kBwdBlock * dv + dk + dv);
+    return run_queue(tokenloop_bwd_chain, &c, N * H, scratch, nthreads);
+}
