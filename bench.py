@@ -73,6 +73,18 @@ def load_peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+def bwd_flops_per_token_head(C: int = 64, d: int = 128) -> float:
+    """The backward's own products per token and head (no recomputed forward): per chunk 12 C d^2
+    (dV' and dS0 from dS_next, dO and dZ: 6 C d^2; dQg, dKg, dKr: 6 C d^2) and 10 C^2 d (the
+    triangular products A_qk^T dO, the two solves, dA_qk, dA_kk and the four position-pair sums)."""
+    return (12 * C * d * d + 10 * C * C * d) / C
+
+
+def fp32_alu_peak_tflops(sms: int = 152, lanes: int = 128, mhz: float = 2070.0) -> float:
+    """fp32 FMA rate of the part: SMs x fp32 lanes per SM x 2 flop x the maximum SM clock."""
+    return sms * lanes * 2 * mhz * 1e6 / 1e12
+
+
 def kernel_source_hash(filename: str) -> str:
     import hashlib
     path = os.path.join(ROOT, "gated_delta_rule_53_gb300", "csrc", filename)
@@ -427,6 +439,17 @@ def run_ours(args):
     gate_tflops = gflops / (ms_gate_launch * 1e-3) / 1e12
     del xg, wga, wgb, ah, gate_o, g_o, z_o
 
+    # ---------------- backward of the prefill (kda_chunk_bwd): fp32 on the CUDA cores ----------------
+    qb, kb, vb, gb, bb = make_prefill_inputs(w, device)
+    dob = fill_device(w.seed, ks.TID_DO, ks.NORMAL, (w.T, w.H, w.d), "bf16", device=device)
+    wsb = torch.empty(kda.kda_chunk_bwd_workspace_size(1, w.T, w.H), dtype=torch.uint8, device=device)
+    bstep = lambda: kda.kda_chunk_bwd(qb, kb, vb, gb, bb, dob, workspace=wsb, stream=stream)
+    bsteps = max(5, args.steps // 10)
+    ms_bwd, ms_bwd_launch, _ = timed(bstep, bsteps, args.warmup, stream, dist)
+    bwd_flops = w.T * w.H * bwd_flops_per_token_head()
+    bwd_tflops = bwd_flops / (ms_bwd_launch * 1e-3) / 1e12
+    del qb, kb, vb, gb, bb, dob, wsb
+
     # ---------------- front end + prefill from raw inputs: fused vs two passes (the long workload's path) ----
     gf = fill_device(wf.seed, ks.TID_G, ks.NEG_SOFTPLUS5, (wf.T, wf.H, wf.d), "f32", device=device)
     bf = fill_device(wf.seed, ks.TID_BETA, ks.SIGMOID, (wf.T, wf.H), "f32", device=device)
@@ -509,6 +532,17 @@ def run_ours(args):
                      "frac": gate_tflops / tc_peak,
                      "traffic": measured_traffic("gemm_gate_kernel", "kda_gate.cu", "gates_8k"), "peak_source": peak_src,
                      "kernel": "gemm_gate_kernel x2 (x [W_gate ; W_a]^T, then the rank product with the gate epilogue)"}}
+    alu_peak = fp32_alu_peak_tflops()
+    line["backward"] = {
+        "workload": f"{w.name}: kda_chunk_bwd of the prefill (bf16 q, k, v and dL/do; fp32 gradients of q, k, v, g, "
+                    "beta, S0), dL/dS_final = 0",
+        "value": w.T * world / (ms_bwd * 1e-3), "unit": "tokens/s", "ms_per_step": ms_bwd, "steps": bsteps,
+        "gpu_launches": 4 * bsteps, "algorithmic_flops_per_launch": bwd_flops,
+        "roofline": {"bound": "alu", "achieved": bwd_tflops, "peak": alu_peak, "unit": "TFLOP/s",
+                     "frac": bwd_tflops / alu_peak, "traffic": None, "peak_source": "derived: 152 SMs x 128 fp32 "
+                     "lanes x 2 flop (FMA) x 2070 MHz",
+                     "kernel": "chunk_simt_kernel (forward, keeping chunk states) + bwd_state_kernel + "
+                               "bwd_chunk_a_kernel + bwd_chunk_b_kernel, timed as one call"}}
     line["fused_prefill"] = {
         "workload": "frontend_32k raw q, k, v bf16 [32768, 12288] + g = max(-5, -softplus(z)), beta -> "
                     "ShortConv(4)+SiLU+L2norm -> chunk_kda (the long workload's path at 32K tokens)",

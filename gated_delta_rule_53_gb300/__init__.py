@@ -21,7 +21,8 @@ import os
 import torch
 
 __all__ = ["kda_shortconv_l2norm", "kda_chunk_fwd", "kda_chunk_fwd_frontend", "kda_chunk_fwd_noalloc",
-           "kda_chunk_fwd_workspace_size",
+           "kda_chunk_fwd_workspace_size", "kda_chunk_bwd", "kda_chunk_bwd_workspace_size",
+           "kda_chunk_segment_summary", "kda_state_combine", "kda_gate_generator",
            "kda_recurrent_step", "library",
            "KDAError", "device_error", "LIB_PATH"]
 
@@ -53,6 +54,9 @@ def library() -> ctypes.CDLL:
         lib.kda_recurrent_step.argtypes = [P, P, P, I64, P, P, P, P, P, I32, I32, I32, I32, F, F, P, P]
         lib.kda_chunk_segment_summary.argtypes = [P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, P, P, P, SZ, P]
         lib.kda_state_combine.argtypes = [P, P, P, P, I64, P]
+        lib.kda_chunk_bwd.argtypes = [P, P, P, P, P, P, P, I32, I64, I32, I32, I32, F, I32, I32, P, P, P, P, P, P, P,
+                                      P, P, SZ, P]
+        lib.kda_chunk_bwd_workspace_size.argtypes = [I32, I64, I32, I32, I32, I32, ctypes.POINTER(SZ)]
         lib.kda_gate_generator.argtypes = [P, I64, I32, P, P, P, I32, I32, I32, P, P, P, P]
         for f in (lib.kda_shortconv_l2norm, lib.kda_chunk_fwd, lib.kda_recurrent_step, lib.kda_device_error,
                   lib.kda_chunk_fwd_workspace_size, lib.kda_chunk_fwd_noalloc, lib.kda_chunk_fwd_frontend):
@@ -189,6 +193,48 @@ def kda_chunk_fwd(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale: flo
                                  _ptr(final_state), _ptr(workspace), ws_bytes, _stream(stream))
     _check(rc, "kda_chunk_fwd")
     return o, final_state
+
+
+def kda_chunk_bwd_workspace_size(N: int, T: int, H: int, dk: int = 128, dv: int = 128, chunk_size: int = 64) -> int:
+    n = ctypes.c_size_t(0)
+    _check(library().kda_chunk_bwd_workspace_size(N, T, H, dk, dv, chunk_size, ctypes.byref(n)),
+           "kda_chunk_bwd_workspace_size")
+    return int(n.value)
+
+
+def kda_chunk_bwd(q, k, v, g, beta, d_o, init_state=None, cu_seqlens=None, d_final_state=None, scale: float = 1.0,
+                  chunk_size: int = 64, output_d_init_state: bool = True, workspace=None, stream=None):
+    """Backward of kda_chunk_fwd.  q, k, v, d_o [T, H, 128] in one dtype (bf16 or fp32); g, beta, init_state,
+    cu_seqlens as kda_chunk_fwd; d_final_state fp32 [N, H, 128, 128] or None (= zeros).  workspace: a uint8
+    CUDA tensor of at least kda_chunk_bwd_workspace_size bytes, or None to take one from PyTorch's allocator.
+    Returns fp32 (dq, dk, dv, dg, dbeta, d_init_state or None)."""
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    dtype = q.dtype
+    if dtype not in (torch.bfloat16, torch.float32):
+        raise KDAError("q, k, v, d_o must be bf16 or fp32")
+    _dev(q, "q", dtype); _dev(k, "k", dtype, (T, H, dk)); _dev(v, "v", dtype, (T, H, dv))
+    _dev(d_o, "d_o", dtype, (T, H, dv))
+    _dev(g, "g", torch.float32, (T, H, dk)); _dev(beta, "beta", torch.float32, (T, H))
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    _dev(cu_seqlens, "cu_seqlens", torch.int32)
+    _dev(init_state, "init_state", torch.float32, (N, H, dv, dk))
+    _dev(d_final_state, "d_final_state", torch.float32, (N, H, dv, dk))
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dq, dkk, dg = (torch.empty((T, H, dk), **f32) for _ in range(3))
+    dvv, db = torch.empty((T, H, dv), **f32), torch.empty((T, H), **f32)
+    d_init = torch.empty((N, H, dv, dk), **f32) if output_d_init_state else None
+    if workspace is None:
+        workspace = torch.empty(kda_chunk_bwd_workspace_size(N, T, H, dk, dv, chunk_size), dtype=torch.uint8,
+                                device=q.device)
+    _dev(workspace, "workspace", torch.uint8)
+    dt = KDA_DTYPE_BF16 if dtype == torch.bfloat16 else KDA_DTYPE_F32
+    rc = library().kda_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state), _ptr(cu_seqlens),
+                                 N, T, H, dk, dv, float(scale), int(chunk_size), dt, _ptr(d_o), _ptr(d_final_state),
+                                 _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dg), _ptr(db), _ptr(d_init), _ptr(workspace),
+                                 workspace.numel(), _stream(stream))
+    _check(rc, "kda_chunk_bwd")
+    return dq, dkk, dvv, dg, db, d_init
 
 
 def kda_chunk_segment_summary(k, g, beta, v=None, q=None, cu_seqlens=None, end_state=True, transition=True,

@@ -201,6 +201,46 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const floa
                      "kda_chunk_fwd launch");
 }
 
+kda_status kda_chunk_bwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv, int chunk_size,
+                                        size_t* bytes) {
+    REQUIRE_PTR(bytes);
+    REQUIRE(N >= 1 && H >= 1 && T_total >= 0 && (int64_t)N * H <= 0x7FFFFFFF, "bad N, H or T_total");
+    if (dk != kda::kHeadDim || dv != kda::kHeadDim)
+        return set_error(KDA_ERR_UNSUPPORTED, "only dk = dv = 128 is supported (got %d, %d)", dk, dv);
+    if (chunk_size != kda::kChunk)
+        return set_error(KDA_ERR_UNSUPPORTED, "only chunk_size = 64 is supported (got %d)", chunk_size);
+    REQUIRE(T_total / 64 + N < 0x7FFFFFFF, "T_total too large");
+    *bytes = kda::chunk_bwd_workspace_bytes(N, T_total, H);
+    return ok();
+}
+
+kda_status kda_chunk_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                         const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H, int dk,
+                         int dv, float scale, int chunk_size, kda_dtype dtype, const void* d_o,
+                         const float* d_final_state, float* dq, float* dk_out, float* dv_out, float* dg, float* dbeta,
+                         float* d_init_state, void* workspace, size_t workspace_bytes, void* stream) {
+    REQUIRE_PTR(q); REQUIRE_PTR(k); REQUIRE_PTR(v); REQUIRE_PTR(g); REQUIRE_PTR(beta); REQUIRE_PTR(d_o);
+    REQUIRE_PTR(dq); REQUIRE_PTR(dk_out); REQUIRE_PTR(dv_out); REQUIRE_PTR(dg); REQUIRE_PTR(dbeta);
+    OPTIONAL_PTR(init_state); OPTIONAL_PTR(d_final_state); OPTIONAL_PTR(d_init_state);
+    kda_status s = check_batch(cu_seqlens, N, T_total, H);
+    if (s != KDA_OK) return s;
+    if (dk != kda::kHeadDim || dv != kda::kHeadDim)
+        return set_error(KDA_ERR_UNSUPPORTED, "only dk = dv = 128 is supported (got %d, %d)", dk, dv);
+    if (chunk_size != kda::kChunk)
+        return set_error(KDA_ERR_UNSUPPORTED, "only chunk_size = 64 is supported (got %d)", chunk_size);
+    REQUIRE(dtype == KDA_DTYPE_F32 || dtype == KDA_DTYPE_BF16, "bad dtype");
+    REQUIRE(std::isfinite(scale), "scale must be finite");
+    REQUIRE(T_total / 64 + N < 0x7FFFFFFF, "T_total too large");
+    const size_t need = kda::chunk_bwd_workspace_bytes(N, T_total, H);
+    REQUIRE(workspace != nullptr && workspace_bytes >= need,
+            "workspace must hold at least %zu bytes for these sizes (got %zu)", need, workspace_bytes);
+    OPTIONAL_PTR(workspace);
+    return from_cuda(kda::launch_chunk_bwd(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, scale, dtype,
+                                           d_o, d_final_state, dq, dk_out, dv_out, dg, dbeta, d_init_state,
+                                           workspace, static_cast<cudaStream_t>(stream)),
+                     "kda_chunk_bwd launch");
+}
+
 kda_status kda_chunk_segment_summary(const void* q, const void* k, const void* v, const float* g, const float* beta,
                                      const int32_t* cu_seqlens, int N, int64_t T_total, int H, int dk, int dv,
                                      int chunk_size, float* end_state, float* transition, void* workspace,

@@ -20,6 +20,7 @@
 // (stored transposed so that a warp's lanes read consecutive words).  The key
 // side (A_kk, A_qk) is recomputed by each of the 4 slices of a head.
 #include "kda_common.cuh"
+#include "kda_simt_blocks.cuh"
 
 namespace kda {
 namespace {
@@ -38,7 +39,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 chunk_simt_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const InT* __restrict__ v,
                   const float* __restrict__ g, const float* __restrict__ beta, const float* init_state,
                   const int32_t* __restrict__ cu, int64_t T_total, int H, float scale,
-                  const __nv_bfloat16* __restrict__ gate, InT* __restrict__ o, float* final_state) {
+                  const __nv_bfloat16* __restrict__ gate, InT* __restrict__ o, float* final_state,
+                  float* __restrict__ save_S, float* __restrict__ save_R, float* __restrict__ save_V) {
     extern __shared__ float smem[];
     float* sQ = smem;                    // [C][D] q, then q * Gamma
     float* sK = sQ + kC * kD;            // [C][D] k, then k * Gamma
@@ -66,6 +68,13 @@ chunk_simt_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const In
     for (int64_t c0 = bos; c0 < eos; c0 += kC) {
         const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
         __syncthreads();  // previous chunk done with every buffer
+        if (save_S) {  // the state entering the chunk, at slot c0 / C + n (one per chunk of the batch)
+            const int64_t at = (((c0 / kC + n) * H + h) * kD + r0) * kD;
+            for (int idx = tid; idx < kSlice * kD; idx += kThreads) {
+                const int r = idx / kD, c = idx % kD;
+                save_S[at + (int64_t)r * kD + c] = sSt[c * kSlice + r];
+            }
+        }
         // ---- tiles of this chunk (rows past L are zero: they change nothing)
         for (int idx = tid; idx < kC * kD; idx += kThreads) {
             const int i = idx / kD, c = idx % kD;
@@ -95,45 +104,7 @@ chunk_simt_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const In
         }
         __syncthreads();
         // ---- A_kk and A_qk: 4x4 tiles of the lower triangle, position-pair decays
-        for (int idx = tid; idx < kC * kC; idx += kThreads) {  // zero the strict upper parts
-            const int i = idx / kC, j = idx % kC;
-            if ((j >> 2) > (i >> 2)) { sAk[idx] = 0.f; sAq[idx] = 0.f; }
-        }
-        if (tid < 136) {
-            int bi = (int)((sqrtf(8.f * tid + 1.f) - 1.f) * 0.5f);
-            while ((bi + 1) * (bi + 2) / 2 <= tid) ++bi;
-            while (bi * (bi + 1) / 2 > tid) --bi;
-            const int bj = tid - bi * (bi + 1) / 2;
-            float akk[4][4] = {}, aqk[4][4] = {};
-            for (int cc = 0; cc < kD; ++cc) {
-                const int c = (cc + tid) & (kD - 1);  // rotate so that threads hit different banks
-                float gi[4], ki[4], qi[4], gj[4], kj[4];
-#pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                    gi[a] = sG[(4 * bi + a) * kD + c];
-                    ki[a] = sK[(4 * bi + a) * kD + c];
-                    qi[a] = sQ[(4 * bi + a) * kD + c];
-                    gj[a] = sG[(4 * bj + a) * kD + c];
-                    kj[a] = sK[(4 * bj + a) * kD + c];
-                }
-#pragma unroll
-                for (int a = 0; a < 4; ++a)
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        const float e = expf(fminf(gi[a] - gj[b], 0.f));
-                        akk[a][b] = fmaf(ki[a] * kj[b], e, akk[a][b]);
-                        aqk[a][b] = fmaf(qi[a] * kj[b], e, aqk[a][b]);
-                    }
-            }
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const int i = 4 * bi + a, j = 4 * bj + b;
-                    sAk[i * kC + j] = j < i ? sB[i] * akk[a][b] : 0.f;
-                    sAq[i * kC + j] = j <= i ? aqk[a][b] : 0.f;
-                }
-        }
+        simt_pair_blocks(sQ, sK, sG, sB, sAk, sAq, tid);
         __syncthreads();
         // ---- decayed operands: q Gamma (sQ), k Gamma (sK), k e^{G_C - G} (sG)
         for (int idx = tid; idx < kC * kD; idx += kThreads) {
@@ -156,7 +127,9 @@ chunk_simt_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const In
 #pragma unroll
             for (int a = 0; a < 8; ++a) {
                 const int i = warp * 8 + a;
-                sU[i * kUStride + lane] = sB[i] * (sU[i * kUStride + lane] - acc[a]);
+                const float r = sU[i * kUStride + lane] - acc[a];
+                if (save_R && i < L) save_R[((c0 + i) * H + h) * kD + r0 + lane] = r;
+                sU[i * kUStride + lane] = sB[i] * r;
             }
         }
         __syncthreads();
@@ -174,8 +147,14 @@ chunk_simt_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const In
             }
         }
         __syncthreads();
+        if (save_V) {
+            for (int idx = tid; idx < kC * kSlice; idx += kThreads) {
+                const int i = idx / kSlice, r = idx % kSlice;
+                if (i < L) save_V[((c0 + i) * H + h) * kD + r0 + r] = sU[i * kUStride + r];
+            }
+        }
         // ---- O = scale ((Q Gamma) S0^T + A_qk U), optional output gate
-        {
+        if (o) {
             float acc[8] = {};
             for (int c = 0; c < kD; ++c) {
                 const float s = sSt[c * kSlice + lane];
@@ -235,14 +214,16 @@ chunk_simt_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const In
 template <typename InT>
 cudaError_t launch_typed(const void* q, const void* k, const void* v, const float* g, const float* beta,
                          const float* init_state, const int32_t* cu, int N, int64_t T_total, int H, float scale,
-                         const void* gate, void* o, float* final_state, cudaStream_t stream) {
+                         const void* gate, void* o, float* final_state, float* save_S, float* save_R, float* save_V,
+                         cudaStream_t stream) {
     auto kern = chunk_simt_kernel<InT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((int64_t)N * H), kD / kSlice);
     kern<<<grid, kThreads, kSmemBytes, stream>>>(
         static_cast<const InT*>(q), static_cast<const InT*>(k), static_cast<const InT*>(v), g, beta, init_state, cu,
-        T_total, H, scale, static_cast<const __nv_bfloat16*>(gate), static_cast<InT*>(o), final_state);
+        T_total, H, scale, static_cast<const __nv_bfloat16*>(gate), static_cast<InT*>(o), final_state, save_S, save_R,
+        save_V);
     return cudaGetLastError();
 }
 
@@ -251,12 +232,13 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, const floa
 cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, const float* g, const float* beta,
                               const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total,
                               int H, float scale, kda_dtype dtype, const void* out_gate, void* o,
-                              float* final_state, cudaStream_t stream) {
+                              float* final_state, cudaStream_t stream, float* save_S, float* save_R,
+                              float* save_V) {
     if (dtype == KDA_DTYPE_F32)
         return launch_typed<float>(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, scale, out_gate, o,
-                                   final_state, stream);
+                                   final_state, save_S, save_R, save_V, stream);
     return launch_typed<__nv_bfloat16>(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, scale, out_gate,
-                                       o, final_state, stream);
+                                       o, final_state, save_S, save_R, save_V, stream);
 }
 
 }  // namespace kda

@@ -220,6 +220,44 @@ KDA_API kda_status kda_chunk_segment_summary(const void* q, const void* k, const
                                              void* stream);
 
 /*
+ * Backward of kda_chunk_fwd (the chunk_kda operator is what trains the model, "月之暗面发布Kimi K3
+ * 开源大模型技术报告", 架构): given dL/do for every token and dL/dS_final for every sequence, the
+ * gradients of L with respect to q, k, v, g, beta and the initial state.  The result equals reverse
+ * mode through the token-by-token recurrence; the kernels take the chain rule through the chunk form
+ * (a forward pass that keeps the state entering every chunk, a reverse pass over the chunks for the
+ * gradient of the state, then every (chunk, head) at once).  fp32 arithmetic on the CUDA cores with
+ * explicit position-pair decays (no use of the -5 bound).
+ *
+ *  q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, dk, dv, scale, chunk_size
+ *                  as kda_chunk_fwd (q, k, v and d_o in storage `dtype`, F32 or BF16)
+ *  d_o             dL/do [T_total, H, dv], storage `dtype`
+ *  d_final_state   fp32 dL/dS_final [N, H, dv, dk] or NULL (= zeros)
+ *  dq, dk_out      fp32 [T_total, H, dk] out
+ *  dv_out          fp32 [T_total, H, dv] out
+ *  dg              fp32 [T_total, H, dk] out
+ *  dbeta           fp32 [T_total, H] out
+ *  d_init_state    fp32 dL/dS0 [N, H, dv, dk] out, or NULL
+ *  workspace       device scratch of at least kda_chunk_bwd_workspace_size bytes, 16-byte aligned,
+ *                  used only during the call (stream-ordered)
+ *
+ * Outputs must not alias inputs or each other.  Errors as kda_chunk_fwd.
+ */
+KDA_API kda_status kda_chunk_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                 const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
+                                 int dk, int dv, float scale, int chunk_size, kda_dtype dtype, const void* d_o,
+                                 const float* d_final_state, float* dq, float* dk_out, float* dv_out, float* dg,
+                                 float* dbeta, float* d_init_state, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
+/*
+ * Bytes of workspace kda_chunk_bwd needs for these sizes (into *bytes): the state entering each chunk
+ * and the gradient leaving it (64 KB each per chunk and head), six fp32 values per token, head and
+ * channel, and two 64 x 64 matrices per chunk and head.
+ */
+KDA_API kda_status kda_chunk_bwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv, int chunk_size,
+                                                size_t* bytes);
+
+/*
  * The decay gate and the full-rank output gate from the layer input ("深入 Kimi-K3: Hugging Face 仓库
  * 分析", paragraph on KDA: the decay is per channel, driven by a low-rank projection plus a per-head
  * parameter, with a lower bound of -5; the output gate is full rank; "Kimi K3 架构全景", section 02:

@@ -38,6 +38,8 @@ _DT = {"f64": (0, np.float64), "f32": (1, np.float32), "bf16": (2, np.uint16)}
 
 # tensor ids of the generator streams
 TID_Q, TID_K, TID_V, TID_G, TID_BETA, TID_STATE, TID_CONV_W, TID_CONV_STATE, TID_GATE, TID_LENGTHS = range(1, 11)
+# upstream gradients of a backward: dL/do and dL/dS_final
+TID_DO, TID_DSTATE = 11, 12
 
 
 def build(force: bool = False) -> str:

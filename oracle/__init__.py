@@ -139,6 +139,11 @@ def kda_tokenloop_bwd(q, k, v, g, beta, d_o, init_state=None, cu_seqlens=None, s
     """Gradients of a loss through the per-token recurrence, by reverse mode: given dL/do [T,H,dv] and
     dL/dS_end [N,H,dv,dk] (None = 0), returns (dq, dk [T,H,dk], dv [T,H,dv], dg [T,H,dk],
     dbeta [T,H], dL/dS0 [N,H,dv,dk])."""
+    return _bwd(_load().oracle_kda_tokenloop_bwd, q, k, v, g, beta, d_o, init_state, cu_seqlens, scale, d_final,
+                nthreads)
+
+
+def _bwd(fn, q, k, v, g, beta, d_o, init_state, cu_seqlens, scale, d_final, nthreads):
     q, k, v, g, beta, d_o = (_f64(x) for x in (q, k, v, g, beta, d_o))
     T, H, dk = q.shape
     dv = v.shape[-1]
@@ -151,9 +156,9 @@ def kda_tokenloop_bwd(q, k, v, g, beta, d_o, init_state=None, cu_seqlens=None, s
             assert x.shape == (N, H, dv, dk)
     dq, dkk, dg = (np.empty((T, H, dk)) for _ in range(3))
     dvv, db, ds0 = np.empty((T, H, dv)), np.empty((T, H)), np.empty((N, H, dv, dk))
-    if _load().oracle_kda_tokenloop_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(s0), _ptr(cu), N, T,
-                                        H, dk, dv, float(scale), _ptr(d_o), _ptr(dfin), _ptr(dq), _ptr(dkk),
-                                        _ptr(dvv), _ptr(dg), _ptr(db), _ptr(ds0), nthreads or threads()) != 0:
+    if fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(s0), _ptr(cu), N, T, H, dk, dv, float(scale),
+          _ptr(d_o), _ptr(dfin), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dg), _ptr(db), _ptr(ds0),
+          nthreads or threads()) != 0:
         raise ValueError("oracle rejected its arguments")
     return dq, dkk, dvv, dg, db, ds0
 

@@ -170,3 +170,31 @@ def test_segment_summary_and_combine_reject_bad_arguments(lib):
     assert comb(S=P(4100)) == 1            # misaligned
     assert comb(count=-1) == 1
     assert comb(count=1 << 31) == 1
+
+
+def test_chunk_bwd_rejects_bad_arguments(lib):
+    def bwd(**over):
+        a = dict(q=P(4096), k=P(4096), v=P(4096), g=P(4096), b=P(4096), init=None, cu=None, N=1, T=64, H=2,
+                 dk=128, dv=128, scale=1.0, chunk=64, dtype=1, do=P(4096), dfin=None, dq=P(4096), dk_=P(4096),
+                 dv_=P(4096), dg=P(4096), db=P(4096), dinit=None, ws=P(4096), wsb=1 << 40)
+        a.update(over)
+        return lib.kda_chunk_bwd(a["q"], a["k"], a["v"], a["g"], a["b"], a["init"], a["cu"], a["N"], a["T"], a["H"],
+                                 a["dk"], a["dv"], a["scale"], a["chunk"], a["dtype"], a["do"], a["dfin"], a["dq"],
+                                 a["dk_"], a["dv_"], a["dg"], a["db"], a["dinit"], a["ws"], a["wsb"], None)
+    for name in ("q", "k", "v", "g", "b", "do", "dq", "dk_", "dv_", "dg", "db", "ws"):
+        assert bwd(**{name: None}) == 1, name
+    assert bwd(dfin=P(4100)) == 1          # misaligned
+    assert bwd(dinit=P(4100)) == 1
+    assert bwd(dk=64) == 2
+    assert bwd(chunk=32) == 2
+    assert bwd(dtype=7) == 1
+    assert bwd(N=2) == 1                   # several sequences need cu_seqlens
+    assert bwd(scale=float("nan")) == 1
+    assert bwd(wsb=1024) == 1              # workspace too small
+    n = ctypes.c_size_t(0)
+    assert lib.kda_chunk_bwd_workspace_size(1, 8192, 96, 128, 128, 64, ctypes.byref(n)) == 0
+    # chunk states and their gradients (2 x 130 slots x 96 heads x 64 KB), six fp32 values per token, head and
+    # channel, dgamma and two 64 x 64 matrices per slot and head
+    assert n.value == 2 * 130 * 96 * 65536 + 6 * 8192 * 96 * 512 + 130 * 96 * 512 + 2 * 130 * 96 * 16384
+    assert lib.kda_chunk_bwd_workspace_size(1, 64, 2, 64, 128, 64, ctypes.byref(n)) == 2
+    assert lib.kda_chunk_bwd_workspace_size(0, 64, 2, 128, 128, 64, ctypes.byref(n)) == 1

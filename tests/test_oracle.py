@@ -194,10 +194,14 @@ MUTANTS = {
 
 def _build_mutant(tmp, name, old, new):
     src = open(os.path.join(os.path.dirname(HERE), "oracle", "kda_oracle.c")).read()
-    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    # the mutation goes into the token loop's chain function only
+    a = src.index("static void tokenloop_chain(")
+    z = src.index("\n}\n", a) + 3
+    body = src[a:z]
+    assert body.count(old) == 1, f"mutation anchor for {name} not found exactly once"
     path = os.path.join(tmp, f"{name}.c")
     with open(path, "w") as f:
-        f.write(src.replace(old, new))
+        f.write(src[:a] + body.replace(old, new) + src[z:])
     so = os.path.join(tmp, f"{name}.so")
     subprocess.check_call(["gcc", "-O1", "-std=c99", "-fPIC", "-shared", "-pthread", "-o", so, path, "-lm"])
     import ctypes

@@ -25,8 +25,9 @@ def _inputs(rng, lengths, H, dk, dv, decay=0.2):
     return q, k, v, g, b, s0, cu
 
 
-def test_backward_matches_central_differences(orc):
-    """L = sum(o * Wo) + sum(S_end * Ws); every input element perturbed by +-h in fp64."""
+def _central_differences(orc, bwd):
+    """L = sum(o * Wo) + sum(S_end * Ws); every input element perturbed by +-h in fp64 and compared
+    with bwd's gradients (AssertionError on the first mismatch)."""
     rng = np.random.default_rng(11)
     lengths, H, dk, dv, scale = [3, 0, 5], 2, 5, 4, 0.7
     q, k, v, g, b, s0, cu = _inputs(rng, lengths, H, dk, dv)
@@ -37,7 +38,7 @@ def test_backward_matches_central_differences(orc):
         o, fs = orc.kda_tokenloop(q, k, v, g, b, s0, cu, scale)
         return float(np.sum(o * Wo) + np.sum(fs * Ws))
 
-    grads = orc.kda_tokenloop_bwd(q, k, v, g, b, Wo, s0, cu, scale, d_final=Ws)
+    grads = bwd(q, k, v, g, b, Wo, s0, cu, scale, Ws)
     h = 1e-5
     args = [q, k, v, g, b, s0]
     names = ["q", "k", "v", "g", "beta", "S0"]
@@ -52,6 +53,56 @@ def test_backward_matches_central_differences(orc):
             num[idx] = (loss(*ap) - loss(*am)) / (2 * h)
         assert np.max(np.abs(num)) > 1e-3, names[a]   # the loss depends on every input
         assert np.max(np.abs(gx - num)) <= 1e-7 * (1.0 + np.max(np.abs(num))), names[a]
+
+
+def test_backward_matches_central_differences(orc):
+    _central_differences(orc, lambda *a: orc.kda_tokenloop_bwd(*a[:9], d_final=a[9]))
+
+
+BWD_MUTANTS = {
+    "dq_unscaled": ("dqt[j] += c->scale * s * dot[i];", "dqt[j] += s * dot[i];"),
+    "dbeta_drops_prediction": ("db += acc * (vt[i] - p[i]);", "db += acc * vt[i];"),
+    "dv_drops_beta": ("dvt[i] = bt * acc;", "dvt[i] = acc;"),
+    "dg_reads_wrong_gradient": ("dgt[j] += sb * st[i * dk + j];", "dgt[j] += Sb[i * dk + j] * st[i * dk + j];"),
+    "gradient_not_decayed": ("Sb[i * dk + j] = sb * alpha[j];", "Sb[i * dk + j] = sb;"),
+    "dk_drops_prediction_path": ("dkt[j] += st[i * dk + j] * pb;", "dkt[j] -= st[i * dk + j] * pb;"),
+    "output_gradient_transposed": ("Sb[i * dk + j] += c->scale * dot[i] * qt[j];",
+                                   "Sb[i * dk + j] += c->scale * dot[j % dv] * qt[i % dk];"),
+}
+
+
+def test_backward_mutants_are_caught(orc):
+    """A plausible slip in the reverse pass (planted in a copy of the oracle's C source) fails the
+    central-difference pin."""
+    import ctypes
+    import os
+    import shutil
+    import subprocess
+    import tempfile
+    src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle",
+                            "kda_oracle.c")).read()
+    a = src.index("static void tokenloop_bwd_chain(")
+    z = src.index("\n}\n", a) + 3
+    body = src[a:z]
+    tmp = tempfile.mkdtemp(prefix="kda_bwd_mutants_")
+    try:
+        for name, (old, new) in BWD_MUTANTS.items():
+            assert body.count(old) == 1, name
+            path = os.path.join(tmp, f"{name}.c")
+            with open(path, "w") as f:
+                f.write(src[:a] + body.replace(old, new) + src[z:])
+            so = os.path.join(tmp, f"{name}.so")
+            subprocess.check_call(["gcc", "-O1", "-std=c99", "-fPIC", "-shared", "-pthread", "-o", so, path, "-lm"])
+            lib = ctypes.CDLL(so)
+            P, I, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_double
+            lib.oracle_kda_tokenloop_bwd.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, D, P, P, P, P, P, P, P, P,
+                                                     ctypes.c_int]
+            lib.oracle_kda_tokenloop_bwd.restype = ctypes.c_int
+            fn = lib.oracle_kda_tokenloop_bwd
+            with pytest.raises(AssertionError):
+                _central_differences(orc, lambda *x: orc._bwd(fn, *x, 1))
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
 
 
 def test_backward_initial_state_through_the_transition(orc):
