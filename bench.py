@@ -537,12 +537,12 @@ def run_ours(args):
         "workload": f"{w.name}: kda_chunk_bwd of the prefill (bf16 q, k, v and dL/do; fp32 gradients of q, k, v, g, "
                     "beta, S0), dL/dS_final = 0",
         "value": w.T * world / (ms_bwd * 1e-3), "unit": "tokens/s", "ms_per_step": ms_bwd, "steps": bsteps,
-        "gpu_launches": 4 * bsteps, "algorithmic_flops_per_launch": bwd_flops,
+        "gpu_launches": 6 * bsteps, "algorithmic_flops_per_launch": bwd_flops,
         "roofline": {"bound": "alu", "achieved": bwd_tflops, "peak": alu_peak, "unit": "TFLOP/s",
                      "frac": bwd_tflops / alu_peak, "traffic": None, "peak_source": "derived: 152 SMs x 128 fp32 "
                      "lanes x 2 flop (FMA) x 2070 MHz",
-                     "kernel": "chunk_simt_kernel (forward, keeping chunk states) + bwd_state_kernel + "
-                               "bwd_chunk_a_kernel + bwd_chunk_b_kernel, timed as one call"}}
+                     "kernel": "bwd_prep_kernel + bwd_fwd_state_kernel + bwd_state_kernel + bwd_chunk_a_kernel + "
+                               "bwd_chunk_b_kernel + bwd_dbeta_kernel, timed as one call"}}
     line["fused_prefill"] = {
         "workload": "frontend_32k raw q, k, v bf16 [32768, 12288] + g = max(-5, -softplus(z)), beta -> "
                     "ShortConv(4)+SiLU+L2norm -> chunk_kda (the long workload's path at 32K tokens)",

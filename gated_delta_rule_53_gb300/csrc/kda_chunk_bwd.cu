@@ -17,14 +17,19 @@
 // and the position-pair products of A_qk and A_kk taken back to q, k and G channel by channel; dg is
 // the reverse running sum of dG inside the chunk.
 //
-// Four kernels (one stream, in order):
-//   1. the fp32 forward (chunk_simt_kernel) keeping S0 of every chunk, R and V';
-//   2. bwd_state_kernel: per (sequence, head, 32 value rows) the chunks in reverse, dS in shared
-//      memory (the state's rows are independent, as in the forward), keeping dS_next of every chunk
-//      and dZ;
-//   3. bwd_chunk_a_kernel: per (chunk, head) the products with S0 and dS_next, dA_qk, dA_kk, dv and
+// Six kernels (one stream, in order):
+//   1. bwd_prep_kernel: per (chunk, head) at once, what does not depend on the state: G, A_qk,
+//      T = (I + A_kk)^-1 (forward substitution, one column per thread), Qg, Kg, Kr, gamma;
+//   2. bwd_fwd_state_kernel: per (sequence, head, 32 value rows) the chunks in order from S0, keeping
+//      the state entering every chunk, R = V - Kg S0^T and V' = T Diag(beta) R;
+//   3. bwd_state_kernel: per (sequence, head, 32 value rows) the chunks in reverse, dS in shared
+//      memory (the state's rows are independent), keeping dS_next of every chunk and dZ = T^T dV';
+//   4. bwd_chunk_a_kernel: per (chunk, head) the products with S0 and dS_next, dA_qk, dA_kk, dv and
 //      the first term of dbeta;
-//   4. bwd_chunk_b_kernel: per (chunk, head) the position-pair products, dq, dk, dg, the rest of dbeta.
+//   5. bwd_chunk_b_kernel: per (chunk, head, half of the key channels) the position-pair products, dq,
+//      dk, dg and the channel half's part of dbeta's second term; bwd_dbeta_kernel adds the parts.
+// The two passes along the chains are plain products on shared-memory tiles (no exponentials, no
+// triangular solve), small enough in shared memory for two or three CTAs per SM.
 // Chunk slot of chunk j of sequence n: (bos_n + 64 j) / 64 + n, distinct for all chunks of a batch
 // and below T_total / 64 + N + 1.
 #include "kda_common.cuh"
@@ -58,27 +63,221 @@ __device__ bool slot_chunk(const int32_t* cu, int N, int64_t T_total, int64_t sl
     return slot >= bos / kC + lo && c0 < eos;
 }
 
-// ============================ reverse state pass ============================
-constexpr size_t kStateFloats = 3 * kC * kD + 2 * kC * kC + 2 * kC * kUS + kD * kSlice + kC + kD;
+// ============================ per chunk: what does not depend on the state ============================
+constexpr size_t kPrepFloats = 3 * kC * kD + kC * kC + kC + kD;
 
 template <typename InT>
-__global__ void __launch_bounds__(kThreads, 1)
-bwd_state_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const float* __restrict__ g,
-                 const float* __restrict__ beta, const InT* __restrict__ d_o, const float* __restrict__ d_final,
-                 const int32_t* __restrict__ cu, int64_t T_total, int H, float scale, float* __restrict__ d_init,
+__global__ void __launch_bounds__(kThreads, 2)
+bwd_prep_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const float* __restrict__ g,
+                const float* __restrict__ beta, const int32_t* __restrict__ cu, int N, int64_t T_total, int H,
+                float* __restrict__ gQg, float* __restrict__ gKg, float* __restrict__ gKr, float* __restrict__ gAqk,
+                float* __restrict__ gT, float* __restrict__ gGam) {
+    extern __shared__ float smem[];
+    float* sQ = smem;             // [C][D] q
+    float* sK = sQ + kC * kD;     // [C][D] k
+    float* sG = sK + kC * kD;     // [C][D] g, then G
+    float* sAk = sG + kC * kD;    // [C][C] A_kk (beta-scaled)
+    float* sB = sAk + kC * kC;    // [C]
+    float* sGl = sB + kC;         // [D]
+    const int64_t slot = blockIdx.x;
+    const int h = blockIdx.y;
+    int n;
+    int64_t c0, eos;
+    if (!slot_chunk(cu, N, T_total, slot, n, c0, eos)) return;
+    const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
+    const int tid = threadIdx.x;
+    const int64_t base = slot * H + h;
+    for (int idx = tid; idx < kC * kD; idx += kThreads) {
+        const int i = idx / kD, c = idx % kD;
+        if (i < L) {
+            const int64_t at = ((c0 + i) * H + h) * kD + c;
+            sQ[idx] = load_as_float(q + at);
+            sK[idx] = load_as_float(k + at);
+            sG[idx] = g[at];
+        } else {
+            sQ[idx] = 0.f; sK[idx] = 0.f; sG[idx] = 0.f;
+        }
+    }
+    if (tid < kC) sB[tid] = tid < L ? beta[(c0 + tid) * H + h] : 0.f;
+    __syncthreads();
+    if (tid < kD) {
+        float acc = 0.f;
+        for (int i = 0; i < kC; ++i) {
+            acc += sG[i * kD + tid];
+            sG[i * kD + tid] = acc;
+        }
+        sGl[tid] = acc;
+        gGam[base * kD + tid] = expf(acc);
+    }
+    __syncthreads();
+    simt_pair_blocks<true>(sQ, sK, sG, sB, sAk, gAqk + base * kC * kC, tid);  // A_qk straight to global memory
+    __syncthreads();
+    if (tid < kC) {  // column j = tid of T = (I + A_kk)^-1: x_i = [i == j] - sum_{m < i} A_kk[i][m] x_m
+        const int j = tid;
+        float x[kC];
+#pragma unroll
+        for (int i = 0; i < kC; ++i) {
+            float s = (i == j) ? 1.f : 0.f;
+#pragma unroll
+            for (int m = 0; m < i; ++m) s = fmaf(-sAk[i * kC + m], x[m], s);
+            x[i] = s;
+        }
+#pragma unroll
+        for (int i = 0; i < kC; ++i) gT[base * kC * kC + i * kC + j] = x[i];
+    }
+    for (int idx = tid; idx < kC * kD; idx += kThreads) {  // Qg, Kg, Kr
+        const int c = idx % kD;
+        const float G = sG[idx], kk = sK[idx];
+        const float gam = expf(G);
+        gQg[base * kC * kD + idx] = sQ[idx] * gam;
+        gKg[base * kC * kD + idx] = kk * gam;
+        gKr[base * kC * kD + idx] = kk * expf(sGl[c] - G);
+    }
+}
+
+// [C][D] (or [C][C]) fp32 tile from global memory into shared memory, 16-byte pieces
+__device__ __forceinline__ void tile_in(float* dst, const float* src, int floats, int tid) {
+    for (int idx = tid; idx < floats / 4; idx += kThreads)
+        reinterpret_cast<float4*>(dst)[idx] = reinterpret_cast<const float4*>(src)[idx];
+}
+
+// ============================ forward along the chains, keeping what the backward reads ============================
+constexpr size_t kFwdFloats = kD * kSlice + kC * kD + kC * kC + kC * kUS + kC + kD;
+
+template <typename InT>
+__global__ void __launch_bounds__(kThreads, 3)
+bwd_fwd_state_kernel(const InT* __restrict__ v, const float* __restrict__ beta, const float* __restrict__ init_state,
+                     const int32_t* __restrict__ cu, int64_t T_total, int H, const float* __restrict__ gKg,
+                     const float* __restrict__ gKr, const float* __restrict__ gT, const float* __restrict__ gGam,
+                     float* __restrict__ S0s, float* __restrict__ Rb, float* __restrict__ Vp) {
+    extern __shared__ float smem[];
+    float* sSt = smem;                 // [D][kSlice] sSt[c][r] = S[r0 + r][c]
+    float* sX = sSt + kD * kSlice;     // [C][D] Kg, then Kr
+    float* sA = sX + kC * kD;          // [C][C] T
+    float* sR = sA + kC * kC;          // [C][kUS] v, then beta R, then V'
+    float* sB = sR + kC * kUS;         // [C]
+    float* sGam = sB + kC;             // [D]
+    const int chain = blockIdx.x, n = chain / H, h = chain % H;
+    const int r0 = blockIdx.y * kSlice;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int64_t bos, eos;
+    seq_bounds(cu, n, T_total, bos, eos);
+    for (int idx = tid; idx < kSlice * kD; idx += kThreads) {
+        const int r = idx / kD, c = idx % kD;
+        sSt[c * kSlice + r] = init_state ? init_state[(int64_t)chain * kD * kD + (int64_t)(r0 + r) * kD + c] : 0.0f;
+    }
+    const int64_t nch = (eos - bos + kC - 1) / kC;
+    for (int64_t ci = 0; ci < nch; ++ci) {
+        const int64_t c0 = bos + ci * kC;
+        const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
+        const int64_t base = (c0 / kC + n) * H + h;
+        __syncthreads();  // the previous chunk is done with every buffer
+        for (int idx = tid; idx < kSlice * kD; idx += kThreads) {
+            const int r = idx / kD, c = idx % kD;
+            S0s[(base * kD + r0 + r) * kD + c] = sSt[c * kSlice + r];
+        }
+        tile_in(sX, gKg + base * kC * kD, kC * kD, tid);
+        for (int idx = tid; idx < kC * kSlice; idx += kThreads) {
+            const int i = idx / kSlice, r = idx % kSlice;
+            sR[i * kUS + r] = i < L ? load_as_float(v + ((c0 + i) * H + h) * kD + r0 + r) : 0.f;
+        }
+        if (tid < kC) sB[tid] = tid < L ? beta[(c0 + tid) * H + h] : 0.f;
+        if (tid < kD) sGam[tid] = gGam[base * kD + tid];
+        __syncthreads();
+        // ---- R = V - Kg S0^T: lanes over value rows, warps over tokens 8w .. 8w+7
+        float br[8];
+        {
+            float acc[8] = {};
+            for (int c = 0; c < kD; c += 4) {
+                const float s0 = sSt[c * kSlice + lane], s1 = sSt[(c + 1) * kSlice + lane];
+                const float s2 = sSt[(c + 2) * kSlice + lane], s3 = sSt[(c + 3) * kSlice + lane];
+#pragma unroll
+                for (int a = 0; a < 8; ++a) {
+                    const float4 x = *reinterpret_cast<const float4*>(sX + (warp * 8 + a) * kD + c);
+                    acc[a] = fmaf(x.x, s0, fmaf(x.y, s1, fmaf(x.z, s2, fmaf(x.w, s3, acc[a]))));
+                }
+            }
+#pragma unroll
+            for (int a = 0; a < 8; ++a) {
+                const int t = warp * 8 + a;
+                const float r = sR[t * kUS + lane] - acc[a];
+                if (t < L) Rb[((c0 + t) * H + h) * kD + r0 + lane] = r;
+                br[a] = sB[t] * r;
+            }
+        }
+        __syncthreads();  // v and Kg consumed
+#pragma unroll
+        for (int a = 0; a < 8; ++a) sR[(warp * 8 + a) * kUS + lane] = br[a];
+        tile_in(sA, gT + base * kC * kC, kC * kC, tid);
+        tile_in(sX, gKr + base * kC * kD, kC * kD, tid);
+        __syncthreads();
+        // ---- V' = T (beta R)
+        float vp[8];
+        {
+#pragma unroll
+            for (int a = 0; a < 8; ++a) vp[a] = 0.f;
+            for (int m = 0; m < kC; m += 4) {
+                const float x0 = sR[m * kUS + lane], x1 = sR[(m + 1) * kUS + lane];
+                const float x2 = sR[(m + 2) * kUS + lane], x3 = sR[(m + 3) * kUS + lane];
+#pragma unroll
+                for (int a = 0; a < 8; ++a) {
+                    const float4 t4 = *reinterpret_cast<const float4*>(sA + (warp * 8 + a) * kC + m);
+                    vp[a] = fmaf(t4.x, x0, fmaf(t4.y, x1, fmaf(t4.z, x2, fmaf(t4.w, x3, vp[a]))));
+                }
+            }
+        }
+        __syncthreads();  // beta R consumed
+#pragma unroll
+        for (int a = 0; a < 8; ++a) {
+            const int t = warp * 8 + a;
+            sR[t * kUS + lane] = vp[a];
+            if (t < L) Vp[((c0 + t) * H + h) * kD + r0 + lane] = vp[a];
+        }
+        __syncthreads();
+        // ---- S = S0 Diag(gamma) + V'^T Kr: lanes over value rows, warps over key channels 16w .. 16w+15
+        {
+            float acc[16];
+#pragma unroll
+            for (int a = 0; a < 16; ++a) {
+                const int c = warp * 16 + a;
+                acc[a] = sSt[c * kSlice + lane] * sGam[c];
+            }
+            for (int t = 0; t < kC; ++t) {
+                const float u = sR[t * kUS + lane];
+                const float4* kr = reinterpret_cast<const float4*>(sX + t * kD + warp * 16);
+#pragma unroll
+                for (int a4 = 0; a4 < 4; ++a4) {
+                    const float4 kv = kr[a4];
+                    acc[4 * a4 + 0] = fmaf(u, kv.x, acc[4 * a4 + 0]);
+                    acc[4 * a4 + 1] = fmaf(u, kv.y, acc[4 * a4 + 1]);
+                    acc[4 * a4 + 2] = fmaf(u, kv.z, acc[4 * a4 + 2]);
+                    acc[4 * a4 + 3] = fmaf(u, kv.w, acc[4 * a4 + 3]);
+                }
+            }
+#pragma unroll
+            for (int a = 0; a < 16; ++a) sSt[(warp * 16 + a) * kSlice + lane] = acc[a];
+        }
+    }
+}
+
+// ============================ reverse state pass ============================
+constexpr size_t kStateFloats = kD * kSlice + kC * kD + kC * kC + 2 * kC * kUS + kC + kD;
+
+template <typename InT>
+__global__ void __launch_bounds__(kThreads, 2)
+bwd_state_kernel(const InT* __restrict__ d_o, const float* __restrict__ beta, const float* __restrict__ d_final,
+                 const int32_t* __restrict__ cu, int64_t T_total, int H, float scale, const float* __restrict__ gQg,
+                 const float* __restrict__ gKg, const float* __restrict__ gKr, const float* __restrict__ gAqk,
+                 const float* __restrict__ gT, const float* __restrict__ gGam, float* __restrict__ d_init,
                  float* __restrict__ dS_next, float* __restrict__ dZ_out) {
     extern __shared__ float smem[];
-    float* sQ = smem;                // [C][D] q, then Qg
-    float* sK = sQ + kC * kD;        // [C][D] k, then Kg
-    float* sG = sK + kC * kD;        // [C][D] G, then Kr
-    float* sAk = sG + kC * kD;       // [C][C] A_kk (beta-scaled, strictly lower)
-    float* sAq = sAk + kC * kC;      // [C][C] A_qk
-    float* sDO = sAq + kC * kC;      // [C][kUS] dO, slice columns
-    float* sDV = sDO + kC * kUS;     // [C][kUS] dV', then dZ
-    float* sDS = sDV + kC * kUS;     // [D][kSlice] sDS[c][r] = dS[r0 + r][c]
-    float* sB = sDS + kD * kSlice;   // [C]
-    float* sGl = sB + kC;            // [D]
-
+    float* sDS = smem;                 // [D][kSlice] sDS[c][r] = dS[r0 + r][c]
+    float* sX = sDS + kD * kSlice;     // [C][D] Kr, then Qg, then Kg
+    float* sA = sX + kC * kD;          // [C][C] A_qk, then T
+    float* sDO = sA + kC * kC;         // [C][kUS] dO, slice columns
+    float* sDV = sDO + kC * kUS;       // [C][kUS] dV', then beta dZ
+    float* sB = sDV + kC * kUS;        // [C]
+    float* sGam = sB + kC;             // [D]
     const int chain = blockIdx.x, n = chain / H, h = chain % H;
     const int r0 = blockIdx.y * kSlice;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -93,112 +292,110 @@ bwd_state_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const flo
     for (int64_t ci = nch - 1; ci >= 0; --ci) {
         const int64_t c0 = bos + ci * kC;
         const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
+        const int64_t base = (c0 / kC + n) * H + h;
         __syncthreads();  // the previous (later) chunk is done with every buffer
-        {  // dS_next of this chunk
-            const int64_t at = (((c0 / kC + n) * H + h) * kD + r0) * kD;
-            for (int idx = tid; idx < kSlice * kD; idx += kThreads) {
-                const int r = idx / kD, c = idx % kD;
-                dS_next[at + (int64_t)r * kD + c] = sDS[c * kSlice + r];
-            }
+        for (int idx = tid; idx < kSlice * kD; idx += kThreads) {
+            const int r = idx / kD, c = idx % kD;
+            dS_next[(base * kD + r0 + r) * kD + c] = sDS[c * kSlice + r];
         }
-        for (int idx = tid; idx < kC * kD; idx += kThreads) {
-            const int i = idx / kD, c = idx % kD;
-            if (i < L) {
-                const int64_t base = ((c0 + i) * H + h) * kD + c;
-                sQ[idx] = load_as_float(q + base);
-                sK[idx] = load_as_float(k + base);
-                sG[idx] = g[base];
-            } else {
-                sQ[idx] = 0.f; sK[idx] = 0.f; sG[idx] = 0.f;
-            }
-        }
+        tile_in(sX, gKr + base * kC * kD, kC * kD, tid);
+        tile_in(sA, gAqk + base * kC * kC, kC * kC, tid);
         for (int idx = tid; idx < kC * kSlice; idx += kThreads) {
             const int i = idx / kSlice, r = idx % kSlice;
             sDO[i * kUS + r] = i < L ? load_as_float(d_o + ((c0 + i) * H + h) * kD + r0 + r) : 0.f;
         }
         if (tid < kC) sB[tid] = tid < L ? beta[(c0 + tid) * H + h] : 0.f;
-        __syncthreads();
-        if (tid < kD) {  // running sum of g per key channel
-            float acc = 0.f;
-            for (int i = 0; i < kC; ++i) {
-                acc += sG[i * kD + tid];
-                sG[i * kD + tid] = acc;
-            }
-            sGl[tid] = acc;
-        }
-        __syncthreads();
-        simt_pair_blocks(sQ, sK, sG, sB, sAk, sAq, tid);
-        __syncthreads();
-        for (int idx = tid; idx < kC * kD; idx += kThreads) {  // Qg, Kg, Kr
-            const int c = idx % kD;
-            const float G = sG[idx], kk = sK[idx];
-            const float gam = expf(G);
-            sQ[idx] *= gam;
-            sK[idx] = kk * gam;
-            sG[idx] = kk * expf(sGl[c] - G);
-        }
+        if (tid < kD) sGam[tid] = gGam[base * kD + tid];
         __syncthreads();
         // ---- dV'[t][r] = sum_c Kr[t][c] dS[r][c] + scale sum_s A_qk[s][t] dO[s][r]; lanes over r, warps over t
+        float dvp[8];
         {
-            float acc[8] = {};
-            for (int c = 0; c < kD; ++c) {
-                const float s = sDS[c * kSlice + lane];
+            float acc[8] = {}, acc2[8] = {};
+            for (int c = 0; c < kD; c += 4) {
+                const float s0 = sDS[c * kSlice + lane], s1 = sDS[(c + 1) * kSlice + lane];
+                const float s2 = sDS[(c + 2) * kSlice + lane], s3 = sDS[(c + 3) * kSlice + lane];
 #pragma unroll
-                for (int a = 0; a < 8; ++a) acc[a] = fmaf(sG[(warp * 8 + a) * kD + c], s, acc[a]);
-            }
-            float acc2[8] = {};
-            for (int s = 0; s < kC; ++s) {
-                const float x = sDO[s * kUS + lane];
-#pragma unroll
-                for (int a = 0; a < 8; ++a) acc2[a] = fmaf(sAq[s * kC + warp * 8 + a], x, acc2[a]);
-            }
-#pragma unroll
-            for (int a = 0; a < 8; ++a) sDV[(warp * 8 + a) * kUS + lane] = fmaf(scale, acc2[a], acc[a]);
-        }
-        __syncthreads();
-        // ---- dZ = (I + A_kk)^-T dV' by back substitution; warp w owns columns 4w .. 4w+3
-        {
-            const int col = warp * 4 + (lane & 3), grp = lane >> 2;
-            for (int t = kC - 2; t >= 0; --t) {
-                float part = 0.f;
-                for (int s = t + 1 + grp; s < kC; s += 8) part = fmaf(sAk[s * kC + t], sDV[s * kUS + col], part);
-                part += __shfl_xor_sync(0xFFFFFFFFu, part, 4);
-                part += __shfl_xor_sync(0xFFFFFFFFu, part, 8);
-                part += __shfl_xor_sync(0xFFFFFFFFu, part, 16);
-                if (grp == 0) sDV[t * kUS + col] -= part;
-                __syncwarp();
-            }
-        }
-        __syncthreads();
-        for (int idx = tid; idx < kC * kSlice; idx += kThreads) {
-            const int i = idx / kSlice, r = idx % kSlice;
-            if (i < L) dZ_out[((c0 + i) * H + h) * kD + r0 + r] = sDV[i * kUS + r];
-        }
-        // ---- dS <- dS Diag(gamma) + scale dO^T Qg - (Diag(beta) dZ)^T Kg; lanes over r, warps over c
-        {
-            float acc[16];
-#pragma unroll
-            for (int a = 0; a < 16; ++a) {
-                const int c = warp * 16 + a;
-                acc[a] = sDS[c * kSlice + lane] * expf(sGl[c]);
-            }
-            for (int t = 0; t < kC; ++t) {
-                const float x = scale * sDO[t * kUS + lane];
-                const float y = -sB[t] * sDV[t * kUS + lane];
-                const float4* qg = reinterpret_cast<const float4*>(sQ + t * kD + warp * 16);
-                const float4* kg = reinterpret_cast<const float4*>(sK + t * kD + warp * 16);
-#pragma unroll
-                for (int a4 = 0; a4 < 4; ++a4) {
-                    const float4 qv = qg[a4], kv = kg[a4];
-                    acc[4 * a4 + 0] = fmaf(y, kv.x, fmaf(x, qv.x, acc[4 * a4 + 0]));
-                    acc[4 * a4 + 1] = fmaf(y, kv.y, fmaf(x, qv.y, acc[4 * a4 + 1]));
-                    acc[4 * a4 + 2] = fmaf(y, kv.z, fmaf(x, qv.z, acc[4 * a4 + 2]));
-                    acc[4 * a4 + 3] = fmaf(y, kv.w, fmaf(x, qv.w, acc[4 * a4 + 3]));
+                for (int a = 0; a < 8; ++a) {
+                    const float4 x = *reinterpret_cast<const float4*>(sX + (warp * 8 + a) * kD + c);
+                    acc[a] = fmaf(x.x, s0, fmaf(x.y, s1, fmaf(x.z, s2, fmaf(x.w, s3, acc[a]))));
                 }
             }
+            for (int s = 0; s < kC; ++s) {
+                const float x = sDO[s * kUS + lane];
+                const float4 a0 = *reinterpret_cast<const float4*>(sA + s * kC + warp * 8);
+                const float4 a1 = *reinterpret_cast<const float4*>(sA + s * kC + warp * 8 + 4);
+                acc2[0] = fmaf(a0.x, x, acc2[0]); acc2[1] = fmaf(a0.y, x, acc2[1]);
+                acc2[2] = fmaf(a0.z, x, acc2[2]); acc2[3] = fmaf(a0.w, x, acc2[3]);
+                acc2[4] = fmaf(a1.x, x, acc2[4]); acc2[5] = fmaf(a1.y, x, acc2[5]);
+                acc2[6] = fmaf(a1.z, x, acc2[6]); acc2[7] = fmaf(a1.w, x, acc2[7]);
+            }
 #pragma unroll
-            for (int a = 0; a < 16; ++a) sDS[(warp * 16 + a) * kSlice + lane] = acc[a];
+            for (int a = 0; a < 8; ++a) dvp[a] = fmaf(scale, acc2[a], acc[a]);
         }
+        __syncthreads();  // Kr and A_qk consumed
+#pragma unroll
+        for (int a = 0; a < 8; ++a) sDV[(warp * 8 + a) * kUS + lane] = dvp[a];
+        tile_in(sA, gT + base * kC * kC, kC * kC, tid);
+        tile_in(sX, gQg + base * kC * kD, kC * kD, tid);
+        __syncthreads();
+        // ---- dZ = T^T dV': dZ[t][r] = sum_s T[s][t] dV'[s][r]
+        float bz[8];
+        {
+            float acc[8] = {};
+            for (int s = 0; s < kC; ++s) {
+                const float x = sDV[s * kUS + lane];
+                const float4 a0 = *reinterpret_cast<const float4*>(sA + s * kC + warp * 8);
+                const float4 a1 = *reinterpret_cast<const float4*>(sA + s * kC + warp * 8 + 4);
+                acc[0] = fmaf(a0.x, x, acc[0]); acc[1] = fmaf(a0.y, x, acc[1]);
+                acc[2] = fmaf(a0.z, x, acc[2]); acc[3] = fmaf(a0.w, x, acc[3]);
+                acc[4] = fmaf(a1.x, x, acc[4]); acc[5] = fmaf(a1.y, x, acc[5]);
+                acc[6] = fmaf(a1.z, x, acc[6]); acc[7] = fmaf(a1.w, x, acc[7]);
+            }
+#pragma unroll
+            for (int a = 0; a < 8; ++a) {
+                const int t = warp * 8 + a;
+                if (t < L) dZ_out[((c0 + t) * H + h) * kD + r0 + lane] = acc[a];
+                bz[a] = sB[t] * acc[a];
+            }
+        }
+        // ---- dS <- dS Diag(gamma) + scale dO^T Qg - (Diag(beta) dZ)^T Kg; lanes over r, warps over c
+        float ds[16];
+#pragma unroll
+        for (int a = 0; a < 16; ++a) {
+            const int c = warp * 16 + a;
+            ds[a] = sDS[c * kSlice + lane] * sGam[c];
+        }
+        for (int t = 0; t < kC; ++t) {
+            const float x = scale * sDO[t * kUS + lane];
+            const float4* qg = reinterpret_cast<const float4*>(sX + t * kD + warp * 16);
+#pragma unroll
+            for (int a4 = 0; a4 < 4; ++a4) {
+                const float4 qv = qg[a4];
+                ds[4 * a4 + 0] = fmaf(x, qv.x, ds[4 * a4 + 0]);
+                ds[4 * a4 + 1] = fmaf(x, qv.y, ds[4 * a4 + 1]);
+                ds[4 * a4 + 2] = fmaf(x, qv.z, ds[4 * a4 + 2]);
+                ds[4 * a4 + 3] = fmaf(x, qv.w, ds[4 * a4 + 3]);
+            }
+        }
+        __syncthreads();  // dV', T and Qg consumed
+#pragma unroll
+        for (int a = 0; a < 8; ++a) sDV[(warp * 8 + a) * kUS + lane] = bz[a];
+        tile_in(sX, gKg + base * kC * kD, kC * kD, tid);
+        __syncthreads();
+        for (int t = 0; t < kC; ++t) {
+            const float y = sDV[t * kUS + lane];
+            const float4* kg = reinterpret_cast<const float4*>(sX + t * kD + warp * 16);
+#pragma unroll
+            for (int a4 = 0; a4 < 4; ++a4) {
+                const float4 kv = kg[a4];
+                ds[4 * a4 + 0] = fmaf(-y, kv.x, ds[4 * a4 + 0]);
+                ds[4 * a4 + 1] = fmaf(-y, kv.y, ds[4 * a4 + 1]);
+                ds[4 * a4 + 2] = fmaf(-y, kv.z, ds[4 * a4 + 2]);
+                ds[4 * a4 + 3] = fmaf(-y, kv.w, ds[4 * a4 + 3]);
+            }
+        }
+#pragma unroll
+        for (int a = 0; a < 16; ++a) sDS[(warp * 16 + a) * kSlice + lane] = ds[a];
     }
     __syncthreads();
     if (d_init) {
@@ -210,7 +407,8 @@ bwd_state_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const flo
 }
 
 // ============================ per chunk: products with S0 and dS_next ============================
-constexpr size_t kChunkAFloats = 3 * kC * kPS + 2 * kSlice * kD + kC;
+constexpr int kSlab = 16;  // rows of S0 and dS_next in shared memory at a time
+constexpr size_t kChunkAFloats = 3 * kC * kPS + 2 * kSlab * kD + kC;
 
 template <typename InT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -224,9 +422,9 @@ bwd_chunk_a_kernel(const float* __restrict__ beta, const InT* __restrict__ d_o, 
     float* sDO = smem;               // [C][kPS]
     float* sDZ = sDO + kC * kPS;     // [C][kPS]
     float* sVP = sDZ + kC * kPS;     // [C][kPS]
-    float* sS = sVP + kC * kPS;      // [kSlice][D] rows of S0
-    float* sD = sS + kSlice * kD;    // [kSlice][D] rows of dS_next
-    float* sB = sD + kSlice * kD;    // [C]
+    float* sS = sVP + kC * kPS;      // [kSlab][D] rows of S0
+    float* sD = sS + kSlab * kD;     // [kSlab][D] rows of dS_next
+    float* sB = sD + kSlab * kD;     // [C]
     const int64_t slot = blockIdx.x;
     const int h = blockIdx.y;
     int n;
@@ -261,44 +459,59 @@ bwd_chunk_a_kernel(const float* __restrict__ beta, const InT* __restrict__ d_o, 
             if (lane == 0) dbeta[(c0 + i) * H + h] = s;
         }
     }
-    // ---- dQg = scale dO S0, dKg = -Diag(beta) dZ S0, dKr = V' dS_next, dgamma; thread (c, half of the tokens)
-    const int c = tid & (kD - 1), hf = tid >> 7;
-    float aq[32], ak[32], ar[32];
+    // ---- dQg = scale dO S0, dKg = -Diag(beta) dZ S0, dKr = V' dS_next, dgamma: thread (channels 4 cq .. 4 cq + 3,
+    //      tokens 8 tg .. 8 tg + 7); a warp shares its tokens, so their values are broadcast loads
+    {
+        const int cq = tid & 31, tg = tid >> 5;
+        float aq[8][4], ak[8][4], ar[8][4];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) { aq[e] = 0.f; ak[e] = 0.f; ar[e] = 0.f; }
-    float dgc = 0.f;
-    const int64_t sbase = ((slot * H + h) * kD) * kD;
-    for (int sb = 0; sb < kD / kSlice; ++sb) {
-        __syncthreads();  // previous slab consumed (and, the first time, the tiles above stored)
-        for (int idx = tid; idx < kSlice * kD; idx += kThreads) {
-            const int64_t at = sbase + (int64_t)(kSlice * sb) * kD + idx;
-            sS[idx] = S0s[at];
-            sD[idx] = dS_next[at];
-        }
-        __syncthreads();
+        for (int a = 0; a < 8; ++a)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) { aq[a][e] = 0.f; ak[a][e] = 0.f; ar[a][e] = 0.f; }
+        float4 dg4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int64_t sbase = ((slot * H + h) * kD) * kD;
+        for (int sb = 0; sb < kD / kSlab; ++sb) {
+            __syncthreads();  // previous slab consumed (and, the first time, the tiles above stored)
+            for (int idx = tid; idx < kSlab * kD / 4; idx += kThreads) {
+                const int64_t at = sbase + (int64_t)(kSlab * sb) * kD;
+                reinterpret_cast<float4*>(sS)[idx] = reinterpret_cast<const float4*>(S0s + at)[idx];
+                reinterpret_cast<float4*>(sD)[idx] = reinterpret_cast<const float4*>(dS_next + at)[idx];
+            }
+            __syncthreads();
 #pragma unroll 2
-        for (int r = 0; r < kSlice; ++r) {
-            const float s = sS[r * kD + c], d = sD[r * kD + c];
-            dgc = fmaf(s, d, dgc);
-            const int rr = kSlice * sb + r;
+            for (int r = 0; r < kSlab; ++r) {
+                const float4 s4 = *reinterpret_cast<const float4*>(sS + r * kD + 4 * cq);
+                const float4 d4 = *reinterpret_cast<const float4*>(sD + r * kD + 4 * cq);
+                if (tg == 0) {
+                    dg4.x = fmaf(s4.x, d4.x, dg4.x); dg4.y = fmaf(s4.y, d4.y, dg4.y);
+                    dg4.z = fmaf(s4.z, d4.z, dg4.z); dg4.w = fmaf(s4.w, d4.w, dg4.w);
+                }
+                const int rr = kSlab * sb + r;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                const int t = 32 * hf + e;
-                aq[e] = fmaf(sDO[t * kPS + rr], s, aq[e]);
-                ak[e] = fmaf(sDZ[t * kPS + rr], s, ak[e]);
-                ar[e] = fmaf(sVP[t * kPS + rr], d, ar[e]);
+                for (int a = 0; a < 8; ++a) {
+                    const int t = 8 * tg + a;
+                    const float o = sDO[t * kPS + rr], z = sDZ[t * kPS + rr], p = sVP[t * kPS + rr];
+                    aq[a][0] = fmaf(o, s4.x, aq[a][0]); aq[a][1] = fmaf(o, s4.y, aq[a][1]);
+                    aq[a][2] = fmaf(o, s4.z, aq[a][2]); aq[a][3] = fmaf(o, s4.w, aq[a][3]);
+                    ak[a][0] = fmaf(z, s4.x, ak[a][0]); ak[a][1] = fmaf(z, s4.y, ak[a][1]);
+                    ak[a][2] = fmaf(z, s4.z, ak[a][2]); ak[a][3] = fmaf(z, s4.w, ak[a][3]);
+                    ar[a][0] = fmaf(p, d4.x, ar[a][0]); ar[a][1] = fmaf(p, d4.y, ar[a][1]);
+                    ar[a][2] = fmaf(p, d4.z, ar[a][2]); ar[a][3] = fmaf(p, d4.w, ar[a][3]);
+                }
             }
         }
-    }
-    if (hf == 0) dgam[(slot * H + h) * kD + c] = dgc;
+        if (tg == 0) *reinterpret_cast<float4*>(dgam + (slot * H + h) * kD + 4 * cq) = dg4;
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-        const int t = 32 * hf + e;
-        if (t < L) {
-            const int64_t at = ((c0 + t) * H + h) * kD + c;
-            XQ[at] = scale * aq[e];
-            XK[at] = -sB[t] * ak[e];
-            XR[at] = ar[e];
+        for (int a = 0; a < 8; ++a) {
+            const int t = 8 * tg + a;
+            if (t < L) {
+                const int64_t at = ((c0 + t) * H + h) * kD + 4 * cq;
+                const float b = -sB[t];
+                *reinterpret_cast<float4*>(XQ + at) =
+                    make_float4(scale * aq[a][0], scale * aq[a][1], scale * aq[a][2], scale * aq[a][3]);
+                *reinterpret_cast<float4*>(XK + at) = make_float4(b * ak[a][0], b * ak[a][1], b * ak[a][2], b * ak[a][3]);
+                *reinterpret_cast<float4*>(XR + at) = make_float4(ar[a][0], ar[a][1], ar[a][2], ar[a][3]);
+            }
         }
     }
     // ---- dA_qk = scale dO V'^T (j <= i), dA_kk = -dZ V'^T (j < i): thread (i, j = jq + 4 e)
@@ -328,83 +541,92 @@ bwd_chunk_a_kernel(const float* __restrict__ beta, const InT* __restrict__ d_o, 
 }
 
 // ============================ per chunk: position-pair products and the inputs' gradients ==========
-constexpr size_t kChunkBFloats = 3 * kC * kD + 2 * kC * kC + kC + kC * 4 + 2 * kD;
+// One CTA per (chunk, head, half of the key channels): the pair sums run channel by channel, so the two
+// halves are independent except for dbeta's sum over channels, which each half leaves as a part.
+constexpr int kHalf = kD / 2;
+constexpr size_t kChunkBFloats = 4 * kC * kHalf + 2 * kC * kC + kC + kC * 2 + 4 * kHalf;
 
 template <typename InT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 bwd_chunk_b_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const float* __restrict__ g,
                    const float* __restrict__ beta, const int32_t* __restrict__ cu, int N, int64_t T_total, int H,
                    const float* __restrict__ XQ, const float* __restrict__ XK, const float* __restrict__ XR,
                    const float* __restrict__ dgam, const float* __restrict__ dAqk, const float* __restrict__ dAkk,
                    float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dg,
-                   float* __restrict__ dbeta) {
+                   float* __restrict__ dbeta_part) {
     extern __shared__ float smem[];
-    float* sQ = smem;                 // [C][D] q (then dG, for the reverse running sum)
-    float* sK = sQ + kC * kD;         // [C][D] k
-    float* sG = sK + kC * kD;         // [C][D] G
-    float* sAq = sG + kC * kD;        // [C][C] dA_qk
+    float* sQ = smem;                 // [C][kHalf] q (then dG, for the reverse running sum)
+    float* sK = sQ + kC * kHalf;      // [C][kHalf] k
+    float* sG = sK + kC * kHalf;      // [C][kHalf] G
+    float* sAl = sG + kC * kHalf;     // [C][kHalf] alpha = e^g: the decay of a pair is a product of these
+    float* sAq = sAl + kC * kHalf;    // [C][C] dA_qk
     float* sAk = sAq + kC * kC;       // [C][C] dA_kk
     float* sB = sAk + kC * kC;        // [C]
-    float* sRed = sB + kC;            // [C][4] per-warp parts of sum_c k_ic rowK'_ic
-    float* sLast = sRed + kC * 4;     // [2][D] parts of sum_t dKr_t Kr_t
+    float* sRed = sB + kC;            // [C][2] per-warp parts of sum_c k_ic rowK'_ic
+    float* sLast = sRed + kC * 2;     // [4][kHalf] parts of sum_t dKr_t Kr_t
     const int64_t slot = blockIdx.x;
-    const int h = blockIdx.y;
+    const int h = blockIdx.y, half = blockIdx.z;
     int n;
     int64_t c0, eos;
     if (!slot_chunk(cu, N, T_total, slot, n, c0, eos)) return;
     const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int idx = tid; idx < kC * kD; idx += kThreads) {
-        const int i = idx / kD, c = idx % kD;
+    const int cb = kHalf * half;  // first channel of this half
+    for (int idx = tid; idx < kC * kHalf; idx += kThreads) {
+        const int i = idx / kHalf, cl = idx % kHalf;
         if (i < L) {
-            const int64_t at = ((c0 + i) * H + h) * kD + c;
+            const int64_t at = ((c0 + i) * H + h) * kD + cb + cl;
             sQ[idx] = load_as_float(q + at);
             sK[idx] = load_as_float(k + at);
-            sG[idx] = g[at];
+            const float gv = g[at];
+            sG[idx] = gv;
+            sAl[idx] = expf(gv);
         } else {
-            sQ[idx] = 0.f; sK[idx] = 0.f; sG[idx] = 0.f;
+            sQ[idx] = 0.f; sK[idx] = 0.f; sG[idx] = 0.f; sAl[idx] = 1.f;
         }
     }
     {
         const int64_t at = (slot * H + h) * kC * kC;
-        for (int idx = tid; idx < kC * kC; idx += kThreads) {
-            sAq[idx] = dAqk[at + idx];
-            sAk[idx] = dAkk[at + idx];
+        for (int idx = tid; idx < kC * kC / 4; idx += kThreads) {
+            reinterpret_cast<float4*>(sAq)[idx] = reinterpret_cast<const float4*>(dAqk + at)[idx];
+            reinterpret_cast<float4*>(sAk)[idx] = reinterpret_cast<const float4*>(dAkk + at)[idx];
         }
     }
     if (tid < kC) sB[tid] = tid < L ? beta[(c0 + tid) * H + h] : 0.f;
     __syncthreads();
-    if (tid < kD) {
+    if (tid < kHalf) {
         float acc = 0.f;
         for (int i = 0; i < kC; ++i) {
-            acc += sG[i * kD + tid];
-            sG[i * kD + tid] = acc;
+            acc += sG[i * kHalf + tid];
+            sG[i * kHalf + tid] = acc;
         }
     }
     __syncthreads();
-    // thread (c, parity p): tokens i = p + 2 m of channel c, as rows and then as columns of the pairs
-    const int c = tid & (kD - 1), p = tid >> 7;
-    const float Gl = sG[(kC - 1) * kD + c];
-    float dka[32], dGa[32];
+    // thread (channel cl, group p): tokens i = p + 4 m of channel cl, as rows and then as columns of the pairs
+    const int cl = tid & (kHalf - 1), p = tid >> 6;
+    const float Gl = sG[(kC - 1) * kHalf + cl];
+    float dka[16], dGa[16];
     float last = 0.f;
 #pragma unroll
-    for (int m = 0; m < 32; ++m) {
-        const int i = p + 2 * m;
-        if (i >= L) {  // warp-uniform: i depends on the warp's parity only
+    for (int m = 0; m < 16; ++m) {
+        const int i = p + 4 * m;
+        if (i >= L) {  // warp-uniform: i depends on the warp's group only
             dka[m] = 0.f;
             dGa[m] = 0.f;
             continue;
         }
-        const float Gi = sG[i * kD + c];
-        float rq = 0.f, rk = 0.f;  // sum_j dA_qk[i][j] k_jc e_ij (j <= i), sum_j dA_kk[i][j] k_jc e_ij (j < i)
-        for (int j = 0; j <= i; ++j) {
-            const float e = expf(fminf(Gi - sG[j * kD + c], 0.f));
-            const float kj = sK[j * kD + c] * e;
+        const float Gi = sG[i * kHalf + cl];
+        // sum_j dA_qk[i][j] k_jc e_ij (j <= i) and sum_j dA_kk[i][j] k_jc e_ij (j < i), with
+        // e_ij = e^{G_ic - G_jc} = alpha_{j+1} ... alpha_i taken as a running product from j = i down
+        float rq = 0.f, rk = 0.f, e = 1.f;
+        for (int j = i; j >= 0; --j) {
+            const float kj = sK[j * kHalf + cl] * e;
             rq = fmaf(sAq[i * kC + j], kj, rq);
             rk = fmaf(sAk[i * kC + j], kj, rk);  // dA_kk is zero on the diagonal
+            e *= sAl[j * kHalf + cl];
         }
-        const float qi = sQ[i * kD + c], ki = sK[i * kD + c], bi = sB[i];
-        const int64_t at = ((c0 + i) * H + h) * kD + c;
+        const float qi = sQ[i * kHalf + cl], ki = sK[i * kHalf + cl], bi = sB[i];
+        const int64_t at = ((c0 + i) * H + h) * kD + cb + cl;
         const float xq = XQ[at], xk = XK[at], xr = XR[at];
         const float gam = expf(Gi), red = expf(fminf(Gl - Gi, 0.f));
         dq[at] = fmaf(xq, gam, rq);
@@ -412,53 +634,58 @@ bwd_chunk_b_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const f
         dGa[m] = qi * rq + ki * bi * rk + (xq * qi + xk * ki) * gam - xr * ki * red;
         last = fmaf(xr * ki, red, last);
         const float part = warp_sum(ki * rk);
-        if (lane == 0) sRed[i * 4 + (warp & 3)] = part;
+        if (lane == 0) sRed[i * 2 + (warp & 1)] = part;
     }
 #pragma unroll
-    for (int m = 0; m < 32; ++m) {
-        const int j = p + 2 * m;
+    for (int m = 0; m < 16; ++m) {
+        const int j = p + 4 * m;
         if (j >= L) continue;
-        const float Gj = sG[j * kD + c];
-        float cq = 0.f, ck = 0.f;  // sum_i dA_qk[i][j] q_ic e_ij (i >= j), sum_i dA_kk[i][j] beta_i k_ic e_ij (i > j)
+        // sum_i dA_qk[i][j] q_ic e_ij (i >= j) and sum_i dA_kk[i][j] beta_i k_ic e_ij (i > j), e_ij again
+        // a running product, from i = j up
+        float cq = 0.f, ck = 0.f, e = 1.f;
         for (int i = j; i < L; ++i) {
-            const float e = expf(fminf(sG[i * kD + c] - Gj, 0.f));
-            cq = fmaf(sAq[i * kC + j], sQ[i * kD + c] * e, cq);
-            ck = fmaf(sAk[i * kC + j] * sB[i], sK[i * kD + c] * e, ck);
+            cq = fmaf(sAq[i * kC + j], sQ[i * kHalf + cl] * e, cq);
+            ck = fmaf(sAk[i * kC + j] * sB[i], sK[i * kHalf + cl] * e, ck);
+            if (i + 1 < L) e *= sAl[(i + 1) * kHalf + cl];
         }
         dka[m] += cq + ck;
-        dGa[m] -= sK[j * kD + c] * (cq + ck);
+        dGa[m] -= sK[j * kHalf + cl] * (cq + ck);
     }
-    sLast[p * kD + c] = last;
+    sLast[p * kHalf + cl] = last;
     __syncthreads();  // every read of q, dA_qk and dA_kk done; sLast, sRed complete
-    if (((L - 1) & 1) == p) {  // G_last = G at the chunk's last token: dKr and dgamma reach it
-        const int m = (L - 1) >> 1;
-        const float extra = sLast[c] + sLast[kD + c] + dgam[(slot * H + h) * kD + c] * expf(Gl);
+    if (((L - 1) & 3) == p) {  // G_last = G at the chunk's last token: dKr and dgamma reach it
+        const int m = (L - 1) >> 2;
+        const float extra = sLast[cl] + sLast[kHalf + cl] + sLast[2 * kHalf + cl] + sLast[3 * kHalf + cl] +
+                            dgam[(slot * H + h) * kD + cb + cl] * expf(Gl);
 #pragma unroll
-        for (int mm = 0; mm < 32; ++mm)
+        for (int mm = 0; mm < 16; ++mm)
             if (mm == m) dGa[mm] += extra;
     }
 #pragma unroll
-    for (int m = 0; m < 32; ++m) {
-        const int i = p + 2 * m;
-        if (i < L) dk[((c0 + i) * H + h) * kD + c] = dka[m];
-        sQ[i * kD + c] = i < L ? dGa[m] : 0.f;
+    for (int m = 0; m < 16; ++m) {
+        const int i = p + 4 * m;
+        if (i < L) dk[((c0 + i) * H + h) * kD + cb + cl] = dka[m];
+        sQ[i * kHalf + cl] = i < L ? dGa[m] : 0.f;
     }
-    if (tid < L) {
-        const float s = sRed[tid * 4] + sRed[tid * 4 + 1] + sRed[tid * 4 + 2] + sRed[tid * 4 + 3];
-        dbeta[(c0 + tid) * H + h] += s;
-    }
+    if (tid < L) dbeta_part[((int64_t)half * T_total + c0 + tid) * H + h] = sRed[tid * 2] + sRed[tid * 2 + 1];
     __syncthreads();
-    if (tid < kD) {  // dg_t = sum_{s >= t} dG_s inside the chunk
+    if (tid < kHalf) {  // dg_t = sum_{s >= t} dG_s inside the chunk
         float acc = 0.f;
         for (int t = L - 1; t >= 0; --t) {
-            acc += sQ[t * kD + tid];
-            dg[((c0 + t) * H + h) * kD + tid] = acc;
+            acc += sQ[t * kHalf + tid];
+            dg[((c0 + t) * H + h) * kD + cb + tid] = acc;
         }
     }
 }
 
+// dbeta = its first term (from bwd_chunk_a_kernel) + the two channel halves' parts, in that order
+__global__ void bwd_dbeta_kernel(float* __restrict__ dbeta, const float* __restrict__ part, int64_t n) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) dbeta[i] = (dbeta[i] + part[i]) + part[n + i];
+}
+
 struct BwdWorkspace {
-    float *S0, *dSn, *R, *Vp, *dZ, *XQ, *XK, *XR, *dgam, *dAqk, *dAkk;
+    float *S0, *dSn, *R, *Vp, *dZ, *XQ, *XK, *XR, *dgam, *dAqk, *dAkk, *Qg, *Kg, *Kr, *Aqk, *T, *gam, *dbp;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -467,6 +694,7 @@ size_t layout(int N, int64_t T_total, int H, uint8_t* base, BwdWorkspace* w) {
     const int64_t S = n_slots(N, T_total);
     const size_t state = align256((size_t)S * H * kD * kD * 4), tok = align256((size_t)T_total * H * kD * 4);
     const size_t gam = align256((size_t)S * H * kD * 4), amat = align256((size_t)S * H * kC * kC * 4);
+    const size_t tile = align256((size_t)S * H * kC * kD * 4);
     size_t off = 0;
     auto take = [&](size_t bytes) {
         float* p = base ? reinterpret_cast<float*>(base + off) : nullptr;
@@ -477,6 +705,8 @@ size_t layout(int N, int64_t T_total, int H, uint8_t* base, BwdWorkspace* w) {
     x.S0 = take(state); x.dSn = take(state);
     x.R = take(tok); x.Vp = take(tok); x.dZ = take(tok); x.XQ = take(tok); x.XK = take(tok); x.XR = take(tok);
     x.dgam = take(gam); x.dAqk = take(amat); x.dAkk = take(amat);
+    x.Qg = take(tile); x.Kg = take(tile); x.Kr = take(tile); x.Aqk = take(amat); x.T = take(amat); x.gam = take(gam);
+    x.dbp = take(align256((size_t)2 * T_total * H * 4));
     if (w) *w = x;
     return off;
 }
@@ -489,11 +719,14 @@ cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const 
                              cudaStream_t stream) {
     BwdWorkspace w;
     layout(N, T_total, H, static_cast<uint8_t*>(workspace), &w);
-    cudaError_t e = launch_chunk_simt(q, k, v, g, beta, init_state, cu, N, T_total, H, scale, dtype, nullptr,
-                                      nullptr, nullptr, stream, w.S0, w.R, w.Vp);
-    if (e != cudaSuccess) return e;
-    const size_t smS = kStateFloats * 4, smA = kChunkAFloats * 4, smB = kChunkBFloats * 4;
-    if ((e = cudaFuncSetAttribute(bwd_state_kernel<InT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smS)) !=
+    cudaError_t e;
+    const size_t smP = kPrepFloats * 4, smF = kFwdFloats * 4, smS = kStateFloats * 4, smA = kChunkAFloats * 4,
+                 smB = kChunkBFloats * 4;
+    if ((e = cudaFuncSetAttribute(bwd_prep_kernel<InT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smP)) !=
+            cudaSuccess ||
+        (e = cudaFuncSetAttribute(bwd_fwd_state_kernel<InT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)smF)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(bwd_state_kernel<InT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smS)) !=
             cudaSuccess ||
         (e = cudaFuncSetAttribute(bwd_chunk_a_kernel<InT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smA)) !=
             cudaSuccess ||
@@ -502,18 +735,31 @@ cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const 
         return e;
     const InT* qt = static_cast<const InT*>(q);
     const InT* kt = static_cast<const InT*>(k);
+    const InT* vt = static_cast<const InT*>(v);
     const InT* ot = static_cast<const InT*>(d_o);
-    bwd_state_kernel<InT><<<dim3((unsigned)((int64_t)N * H), kD / kSlice), kThreads, smS, stream>>>(
-        qt, kt, g, beta, ot, d_final, cu, T_total, H, scale, d_init, w.dSn, w.dZ);
+    const dim3 grid((unsigned)n_slots(N, T_total), (unsigned)H);
+    const dim3 chains((unsigned)((int64_t)N * H), kD / kSlice);
+    if (T_total > 0) {
+        bwd_prep_kernel<InT><<<grid, kThreads, smP, stream>>>(qt, kt, g, beta, cu, N, T_total, H, w.Qg, w.Kg, w.Kr,
+                                                              w.Aqk, w.T, w.gam);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        bwd_fwd_state_kernel<InT><<<chains, kThreads, smF, stream>>>(vt, beta, init_state, cu, T_total, H, w.Kg,
+                                                                     w.Kr, w.T, w.gam, w.S0, w.R, w.Vp);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    bwd_state_kernel<InT><<<chains, kThreads, smS, stream>>>(ot, beta, d_final, cu, T_total, H, scale, w.Qg, w.Kg,
+                                                             w.Kr, w.Aqk, w.T, w.gam, d_init, w.dSn, w.dZ);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (T_total == 0) return cudaSuccess;
-    const dim3 grid((unsigned)n_slots(N, T_total), (unsigned)H);
     bwd_chunk_a_kernel<InT><<<grid, kThreads, smA, stream>>>(beta, ot, cu, N, T_total, H, scale, w.S0, w.dSn, w.R,
                                                              w.Vp, w.dZ, w.XQ, w.XK, w.XR, w.dgam, w.dAqk, w.dAkk, dv,
                                                              dbeta);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_chunk_b_kernel<InT><<<grid, kThreads, smB, stream>>>(qt, kt, g, beta, cu, N, T_total, H, w.XQ, w.XK, w.XR,
-                                                             w.dgam, w.dAqk, w.dAkk, dq, dk, dg, dbeta);
+    bwd_chunk_b_kernel<InT><<<dim3(grid.x, grid.y, 2), kThreads, smB, stream>>>(
+        qt, kt, g, beta, cu, N, T_total, H, w.XQ, w.XK, w.XR, w.dgam, w.dAqk, w.dAkk, dq, dk, dg, w.dbp);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int64_t nb = T_total * H;
+    bwd_dbeta_kernel<<<(unsigned)((nb + 255) / 256), 256, 0, stream>>>(dbeta, w.dbp, nb);
     return cudaGetLastError();
 }
 

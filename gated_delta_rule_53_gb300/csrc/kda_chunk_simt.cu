@@ -39,8 +39,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 chunk_simt_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const InT* __restrict__ v,
                   const float* __restrict__ g, const float* __restrict__ beta, const float* init_state,
                   const int32_t* __restrict__ cu, int64_t T_total, int H, float scale,
-                  const __nv_bfloat16* __restrict__ gate, InT* __restrict__ o, float* final_state,
-                  float* __restrict__ save_S, float* __restrict__ save_R, float* __restrict__ save_V) {
+                  const __nv_bfloat16* __restrict__ gate, InT* __restrict__ o, float* final_state) {
     extern __shared__ float smem[];
     float* sQ = smem;                    // [C][D] q, then q * Gamma
     float* sK = sQ + kC * kD;            // [C][D] k, then k * Gamma
@@ -68,13 +67,6 @@ chunk_simt_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const In
     for (int64_t c0 = bos; c0 < eos; c0 += kC) {
         const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
         __syncthreads();  // previous chunk done with every buffer
-        if (save_S) {  // the state entering the chunk, at slot c0 / C + n (one per chunk of the batch)
-            const int64_t at = (((c0 / kC + n) * H + h) * kD + r0) * kD;
-            for (int idx = tid; idx < kSlice * kD; idx += kThreads) {
-                const int r = idx / kD, c = idx % kD;
-                save_S[at + (int64_t)r * kD + c] = sSt[c * kSlice + r];
-            }
-        }
         // ---- tiles of this chunk (rows past L are zero: they change nothing)
         for (int idx = tid; idx < kC * kD; idx += kThreads) {
             const int i = idx / kD, c = idx % kD;
@@ -127,9 +119,7 @@ chunk_simt_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const In
 #pragma unroll
             for (int a = 0; a < 8; ++a) {
                 const int i = warp * 8 + a;
-                const float r = sU[i * kUStride + lane] - acc[a];
-                if (save_R && i < L) save_R[((c0 + i) * H + h) * kD + r0 + lane] = r;
-                sU[i * kUStride + lane] = sB[i] * r;
+                sU[i * kUStride + lane] = sB[i] * (sU[i * kUStride + lane] - acc[a]);
             }
         }
         __syncthreads();
@@ -147,14 +137,8 @@ chunk_simt_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const In
             }
         }
         __syncthreads();
-        if (save_V) {
-            for (int idx = tid; idx < kC * kSlice; idx += kThreads) {
-                const int i = idx / kSlice, r = idx % kSlice;
-                if (i < L) save_V[((c0 + i) * H + h) * kD + r0 + r] = sU[i * kUStride + r];
-            }
-        }
         // ---- O = scale ((Q Gamma) S0^T + A_qk U), optional output gate
-        if (o) {
+        {
             float acc[8] = {};
             for (int c = 0; c < kD; ++c) {
                 const float s = sSt[c * kSlice + lane];
@@ -214,16 +198,14 @@ chunk_simt_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const In
 template <typename InT>
 cudaError_t launch_typed(const void* q, const void* k, const void* v, const float* g, const float* beta,
                          const float* init_state, const int32_t* cu, int N, int64_t T_total, int H, float scale,
-                         const void* gate, void* o, float* final_state, float* save_S, float* save_R, float* save_V,
-                         cudaStream_t stream) {
+                         const void* gate, void* o, float* final_state, cudaStream_t stream) {
     auto kern = chunk_simt_kernel<InT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((int64_t)N * H), kD / kSlice);
     kern<<<grid, kThreads, kSmemBytes, stream>>>(
         static_cast<const InT*>(q), static_cast<const InT*>(k), static_cast<const InT*>(v), g, beta, init_state, cu,
-        T_total, H, scale, static_cast<const __nv_bfloat16*>(gate), static_cast<InT*>(o), final_state, save_S, save_R,
-        save_V);
+        T_total, H, scale, static_cast<const __nv_bfloat16*>(gate), static_cast<InT*>(o), final_state);
     return cudaGetLastError();
 }
 
@@ -232,13 +214,12 @@ cudaError_t launch_typed(const void* q, const void* k, const void* v, const floa
 cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, const float* g, const float* beta,
                               const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total,
                               int H, float scale, kda_dtype dtype, const void* out_gate, void* o,
-                              float* final_state, cudaStream_t stream, float* save_S, float* save_R,
-                              float* save_V) {
+                              float* final_state, cudaStream_t stream) {
     if (dtype == KDA_DTYPE_F32)
         return launch_typed<float>(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, scale, out_gate, o,
-                                   final_state, save_S, save_R, save_V, stream);
+                                   final_state, stream);
     return launch_typed<__nv_bfloat16>(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, scale, out_gate,
-                                       o, final_state, save_S, save_R, save_V, stream);
+                                       o, final_state, stream);
 }
 
 }  // namespace kda

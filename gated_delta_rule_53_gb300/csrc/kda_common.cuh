@@ -82,14 +82,10 @@ cudaError_t launch_shortconv_l2norm(const void* xq, const void* xk, const void* 
                                     int H, const void* conv_state_in, void* conv_state_out, float eps,
                                     kda_dtype out_dtype, void* q, void* k, void* v, cudaStream_t stream);
 
-// o may be null (no outputs).  save_S / save_R / save_V (each optional) keep what the backward reads:
-// the state entering each chunk at slot c0 / 64 + n ([slots, H, 128, 128]), and per token R = v - (k e^G) S0^T
-// and V' = (I + A_kk)^-1 Diag(beta) R ([T_total, H, 128]).
 cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, const float* g, const float* beta,
                               const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total,
                               int H, float scale, kda_dtype dtype, const void* out_gate, void* o,
-                              float* final_state, cudaStream_t stream, float* save_S = nullptr,
-                              float* save_R = nullptr, float* save_V = nullptr);
+                              float* final_state, cudaStream_t stream);
 
 // Backward of the chunk prefill (fp32 on the CUDA cores): gradients of q, k, v, g, beta and the initial
 // state from those of o and of the final state.  Workspace: chunk_bwd_workspace_bytes().

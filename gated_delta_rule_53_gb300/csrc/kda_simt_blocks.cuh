@@ -14,7 +14,10 @@ namespace kda {
 
 // sQ, sK, sG: [kChunk][kHeadDim] (q, k and the running sum G; rows past the chunk are zero);
 // sB: beta [kChunk].  Writes sAk = A_kk and sAq = A_qk, [kChunk][kChunk], zero above their
-// diagonals.  256 threads; the first 136 each take one 4 x 4 tile of the lower triangle.
+// diagonals (either may be in global memory).  256 threads; the first 136 each take one 4 x 4 tile
+// of the lower triangle.  kFastExp: the decays by the hardware exponential (__expf, relative error
+// of order 1e-6 for these arguments) instead of expf.
+template <bool kFastExp = false>
 __device__ __forceinline__ void simt_pair_blocks(const float* sQ, const float* sK, const float* sG, const float* sB,
                                                  float* sAk, float* sAq, int tid) {
     constexpr int C = kChunk, D = kHeadDim;
@@ -43,7 +46,8 @@ __device__ __forceinline__ void simt_pair_blocks(const float* sQ, const float* s
             for (int a = 0; a < 4; ++a)
 #pragma unroll
                 for (int b = 0; b < 4; ++b) {
-                    const float e = expf(fminf(gi[a] - gj[b], 0.f));
+                    const float x = fminf(gi[a] - gj[b], 0.f);
+                    const float e = kFastExp ? __expf(x) : expf(x);
                     akk[a][b] = fmaf(ki[a] * kj[b], e, akk[a][b]);
                     aqk[a][b] = fmaf(qi[a] * kj[b], e, aqk[a][b]);
                 }

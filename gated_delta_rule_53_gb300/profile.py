@@ -1,7 +1,8 @@
 """Profiling harness: runs one entry point of the library on a named synthetic case a
 few times, so that a profiler can capture a handful of launches of one kernel.
 
-  python -m gated_delta_rule_53_gb300.profile {prefill_8k,prefill_2k,decode_64,decode_16,frontend_8k,gates_8k} [--iters N]
+  python -m gated_delta_rule_53_gb300.profile {prefill_8k,prefill_2k,decode_64,decode_16,frontend_8k,gates_8k,
+                                               bwd_8k,bwd_2k} [--iters N]
 
 Cases (all inputs larger than the 129 MB L2, a few GB on the device at most):
   prefill_8k   kda_chunk_fwd, 1 x 8192 tokens x 96 heads, bf16
@@ -10,6 +11,8 @@ Cases (all inputs larger than the 129 MB L2, a few GB on the device at most):
   decode_16    kda_recurrent_step, 16 sequences x 96 heads
   frontend_8k  kda_shortconv_l2norm, 8192 tokens x 96 heads, bf16 out
   gates_8k     kda_gate_generator, x 8192 x 7168 -> 96 x 128 gate channels, rank 128 (bench.py's sizes)
+  bwd_8k       kda_chunk_bwd of prefill_8k (bf16 inputs and dL/do), as bench.py's backward leg
+  bwd_2k       kda_chunk_bwd, 1 x 2048 tokens x 96 heads
 """
 from __future__ import annotations
 
@@ -30,13 +33,14 @@ def main():
     from kda_synth.device import fill_device
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["prefill_8k", "prefill_2k", "decode_64", "decode_16", "frontend_8k", "gates_8k"])
+    ap.add_argument("case", choices=["prefill_8k", "prefill_2k", "decode_64", "decode_16", "frontend_8k", "gates_8k",
+                                     "bwd_8k", "bwd_2k"])
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
-    if args.case.startswith("prefill"):
-        T = 8192 if args.case == "prefill_8k" else 2048
+    if args.case.startswith("prefill") or args.case.startswith("bwd"):
+        T = 8192 if args.case.endswith("8k") else 2048
         w = ks.Workload(args.case, "prefill", 53002, H=96, lengths=[T])
         q = fill_device(w.seed, ks.TID_Q, ks.UNIT_GROUPS, (T, 96, 128), "bf16", 0.0, 128.0, device=dev)
         k = fill_device(w.seed, ks.TID_K, ks.UNIT_GROUPS, (T, 96, 128), "bf16", 0.0, 128.0, device=dev)
@@ -44,6 +48,10 @@ def main():
         g = fill_device(w.seed, ks.TID_G, w.g_kind, (T, 96, 128), "f32", device=dev)
         b = fill_device(w.seed, ks.TID_BETA, ks.SIGMOID, (T, 96), "f32", device=dev)
         fn = lambda: kda.kda_chunk_fwd(q, k, v, g, b)
+        if args.case.startswith("bwd"):
+            do = fill_device(w.seed, ks.TID_DO, ks.NORMAL, (T, 96, 128), "bf16", device=dev)
+            ws = torch.empty(kda.kda_chunk_bwd_workspace_size(1, T, 96), dtype=torch.uint8, device=dev)
+            fn = lambda: kda.kda_chunk_bwd(q, k, v, g, b, do, workspace=ws)
     elif args.case.startswith("decode"):
         N = 64 if args.case == "decode_64" else 16
         w = ks.Workload(args.case, "decode", 53003, H=96, lengths=[1] * N, init_state_std=0.02)

@@ -252,7 +252,8 @@ KDA_API kda_status kda_chunk_bwd(const void* q, const void* k, const void* v, co
 /*
  * Bytes of workspace kda_chunk_bwd needs for these sizes (into *bytes): the state entering each chunk
  * and the gradient leaving it (64 KB each per chunk and head), six fp32 values per token, head and
- * channel, and two 64 x 64 matrices per chunk and head.
+ * channel, two per token and head, and per chunk and head three 64 x 128 and four 64 x 64 fp32 tiles
+ * and two vectors of 128.
  */
 KDA_API kda_status kda_chunk_bwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv, int chunk_size,
                                                 size_t* bytes);

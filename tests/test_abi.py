@@ -194,7 +194,10 @@ def test_chunk_bwd_rejects_bad_arguments(lib):
     n = ctypes.c_size_t(0)
     assert lib.kda_chunk_bwd_workspace_size(1, 8192, 96, 128, 128, 64, ctypes.byref(n)) == 0
     # chunk states and their gradients (2 x 130 slots x 96 heads x 64 KB), six fp32 values per token, head and
-    # channel, dgamma and two 64 x 64 matrices per slot and head
-    assert n.value == 2 * 130 * 96 * 65536 + 6 * 8192 * 96 * 512 + 130 * 96 * 512 + 2 * 130 * 96 * 16384
+    # channel, two per token and head; per slot and head: dgamma and gamma (512 B each), four 64 x 64 matrices,
+    # three 64 x 128 tiles
+    S = 130 * 96
+    assert n.value == (2 * S * 65536 + 6 * 8192 * 96 * 512 + 2 * S * 512 + 4 * S * 16384 + 3 * S * 32768 +
+                       2 * 8192 * 96 * 4)
     assert lib.kda_chunk_bwd_workspace_size(1, 64, 2, 64, 128, 64, ctypes.byref(n)) == 2
     assert lib.kda_chunk_bwd_workspace_size(0, 64, 2, 128, 128, 64, ctypes.byref(n)) == 1
