@@ -539,7 +539,9 @@ def run_ours(args):
         "value": w.T * world / (ms_bwd * 1e-3), "unit": "tokens/s", "ms_per_step": ms_bwd, "steps": bsteps,
         "gpu_launches": 6 * bsteps, "algorithmic_flops_per_launch": bwd_flops,
         "roofline": {"bound": "alu", "achieved": bwd_tflops, "peak": alu_peak, "unit": "TFLOP/s",
-                     "frac": bwd_tflops / alu_peak, "traffic": None, "peak_source": "derived: 152 SMs x 128 fp32 "
+                     "frac": bwd_tflops / alu_peak,
+                     "traffic": measured_traffic("kda_chunk_bwd", "kda_chunk_bwd.cu", w.name),
+                     "peak_source": "derived: 152 SMs x 128 fp32 "
                      "lanes x 2 flop (FMA) x 2070 MHz",
                      "kernel": "bwd_prep_kernel + bwd_fwd_state_kernel + bwd_state_kernel + bwd_chunk_a_kernel + "
                                "bwd_chunk_b_kernel + bwd_dbeta_kernel, timed as one call"}}
