@@ -1,8 +1,9 @@
 // kda_chunk_bwd: the backward of the chunk prefill, fp32 on the CUDA cores.
 //
 // The forward ("Kimi-K3 深度解析", section 三, "KDA 的关键改进", unrolled over chunks of
-// C = 64 tokens; the chunk_kda operator of "Kimi K3 架构全景", section 02, whose training speed
-// "月之暗面发布Kimi K3开源大模型技术报告", 架构, is about) maps, per chunk with S0 entering it,
+// C = 64 tokens: the chunk_kda operator of "Kimi K3 架构全景", section 02, which
+// "月之暗面发布Kimi K3开源大模型技术报告", 架构, presents as a training-speed design) maps, per
+// chunk with S0 entering it,
 // G the running sum of g, Gamma = e^G, gamma = e^{G_last}, Kg = K Gamma, Qg = Q Gamma,
 // Kr = K e^{G_last - G}:
 //   R  = V - Kg S0^T,   V' = (I + A_kk)^-1 Diag(beta) R
@@ -13,7 +14,7 @@
 // and, inside the chunk,
 //   dQg = scale dO S0,  dKg = -Diag(beta) dZ S0,  dKr = V' dS_next,  dgamma = colsum(dS_next . S0)
 //   dA_qk = scale dO V'^T (j <= i),  dA_kk = -dZ V'^T (j < i),  dv = Diag(beta) dZ
-//   dbeta_i = sum_r dZ_ir R_ir + sum_j dA_kk[i][j] A_kk[i][j] / beta_i
+//   dbeta_i = sum_r dZ_ir R_ir + sum_j dA_kk[i][j] B[i][j]      (A_kk = Diag(beta) B)
 // and the position-pair products of A_qk and A_kk taken back to q, k and G channel by channel; dg is
 // the reverse running sum of dG inside the chunk.
 //
