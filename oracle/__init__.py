@@ -23,6 +23,8 @@ The arithmetic lives in ``kda_oracle.c`` (plain C99, fp64, one thread per
 * :func:`kda_tokenloop_bwd` — the gradients of a loss with respect to q, k, v, g, beta and the
   initial state, by reverse mode through the token loop (the backward of ``chunk_kda``; the
   pages name the operator and its training use, "月之暗面发布Kimi K3开源大模型技术报告", 架构).
+* :func:`kda_chunked_bwd` — the same gradients by the chain rule through the chunk form (fp64
+  numpy), checked against the token loop's reverse mode: the algebra the GPU backward follows.
 * :func:`transition` — a segment's transition operator M = X_1 ... X_L with
   X_t = Diag(alpha_t)(I - beta_t k_t k_t^T), formed as a literal product of dense
   matrices: a segment maps its entering state S to S M + E (E its end state from zero),
@@ -160,6 +162,88 @@ def _bwd(fn, q, k, v, g, beta, d_o, init_state, cu_seqlens, scale, d_final, nthr
           _ptr(d_o), _ptr(dfin), _ptr(dq), _ptr(dkk), _ptr(dvv), _ptr(dg), _ptr(db), _ptr(ds0),
           nthreads or threads()) != 0:
         raise ValueError("oracle rejected its arguments")
+    return dq, dkk, dvv, dg, db, ds0
+
+
+def _chunk_bwd_chain(q, k, v, g, beta, S0, d_o, d_final, scale, C):
+    """One (sequence, head) chain: the chain rule through the chunk form, chunk by chunk.
+
+    Per chunk with S0 entering it, G the running sum of g, A the pair products with their decays
+    e^{G_ic - G_jc} (A_kk = Diag(beta) B strictly below the diagonal, A_qk on and below it):
+      forward  R = V - (K e^G) S0^T,  V' = (I + A_kk)^-1 Diag(beta) R,
+               O = scale ((Q e^G) S0^T + A_qk V'),  S_next = S0 Diag(e^{G_last}) + V'^T (K e^{G_last - G})
+      reverse  dV' = scale A_qk^T dO + (K e^{G_last - G}) dS_next^T,  dZ = (I + A_kk)^-T dV',
+               dS0 = dS_next Diag(e^{G_last}) + scale dO^T (Q e^G) - (Diag(beta) dZ)^T (K e^G)
+    and inside the chunk the gradients of every factor above, with G's gradient summed backwards
+    into g's.  Every exponent e^{G_ic - G_jc} used has j <= i (never positive)."""
+    T, dk = q.shape
+    fw, S = [], S0.copy()
+    for a in range(0, T, C):
+        z = min(a + C, T)
+        L = z - a
+        qq, kk, vv, gg, bb = q[a:z], k[a:z], v[a:z], g[a:z], beta[a:z]
+        G = np.cumsum(gg, 0)
+        low, lowd = np.tril(np.ones((L, L)), -1), np.tril(np.ones((L, L)))
+        D = G[:, None, :] - G[None, :, :]                         # [i, j, c]
+        E = np.exp(np.where(lowd[:, :, None] > 0, D, -np.inf))     # e^{G_ic - G_jc} for j <= i, else 0
+        B = np.einsum("ic,jc,ijc->ij", kk, kk, E) * low
+        Aqk = np.einsum("ic,jc,ijc->ij", qq, kk, E)
+        Akk = bb[:, None] * B
+        Kg, Qg, Kr, gam = kk * np.exp(G), qq * np.exp(G), kk * np.exp(G[-1] - G), np.exp(G[-1])
+        R = vv - Kg @ S.T
+        Vp = np.linalg.solve(np.eye(L) + Akk, bb[:, None] * R)
+        fw.append((a, z, S.copy(), G, E, B, Aqk, Akk, Kg, Qg, Kr, gam, R, Vp, low, lowd))
+        S = S * gam[None, :] + Vp.T @ Kr
+    dq, dkk, dg = np.zeros_like(q), np.zeros_like(k), np.zeros_like(g)
+    dvv, db = np.zeros_like(v), np.zeros_like(beta)
+    dS = d_final.copy()
+    for (a, z, S0c, G, E, B, Aqk, Akk, Kg, Qg, Kr, gam, R, Vp, low, lowd) in reversed(fw):
+        L = z - a
+        qq, kk, bb, dO = q[a:z], k[a:z], beta[a:z], d_o[a:z]
+        dVp = scale * Aqk.T @ dO + Kr @ dS.T
+        dZ = np.linalg.solve((np.eye(L) + Akk).T, dVp)
+        dQg, dKg, dKr = scale * dO @ S0c, -(bb[:, None] * dZ) @ S0c, Vp @ dS
+        dgam = np.sum(dS * S0c, axis=0)
+        dAqk = scale * (dO @ Vp.T) * lowd
+        dAkk = -(dZ @ Vp.T) * low
+        dB = bb[:, None] * dAkk
+        dvv[a:z] = bb[:, None] * dZ
+        db[a:z] = np.sum(dZ * R, axis=1) + np.sum(dAkk * B, axis=1)
+        rowQ = np.einsum("ij,jc,ijc->ic", dAqk, kk, E)
+        colQ = np.einsum("ij,ic,ijc->jc", dAqk, qq, E)
+        rowK = np.einsum("ij,jc,ijc->ic", dB, kk, E)
+        colK = np.einsum("ij,ic,ijc->jc", dB, kk, E)
+        dq[a:z] = rowQ + dQg * np.exp(G)
+        dkk[a:z] = rowK + colQ + colK + dKg * np.exp(G) + dKr * np.exp(G[-1] - G)
+        dG = qq * rowQ + kk * rowK - kk * (colQ + colK) + dQg * Qg + dKg * Kg - dKr * Kr
+        dG[-1] += np.sum(dKr * Kr, axis=0) + dgam * gam
+        dg[a:z] = np.cumsum(dG[::-1], 0)[::-1]
+        dS = dS * gam[None, :] + scale * dO.T @ Qg - (bb[:, None] * dZ).T @ Kg
+    return dq, dkk, dvv, dg, db, dS
+
+
+def kda_chunked_bwd(q, k, v, g, beta, d_o, init_state=None, cu_seqlens=None, scale=1.0, d_final=None, chunk=64):
+    """The same gradients as kda_tokenloop_bwd, by the chain rule through the chunk form (fp64 numpy):
+    the algebra the GPU backward follows, checked against the token loop's reverse mode."""
+    q, k, v, g, beta, d_o = (_f64(x) for x in (q, k, v, g, beta, d_o))
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    cu, N = _cu(cu_seqlens, T)
+    bounds = [0, T] if cu is None else list(cu)
+    s0, dfin = _f64(init_state), _f64(d_final)
+    dq, dkk, dg = (np.zeros((T, H, dk)) for _ in range(3))
+    dvv, db, ds0 = np.zeros((T, H, dv)), np.zeros((T, H)), np.zeros((N, H, dv, dk))
+    for n in range(N):
+        a, z = bounds[n], bounds[n + 1]
+        for h in range(H):
+            S0 = s0[n, h] if s0 is not None else np.zeros((dv, dk))
+            dF = dfin[n, h] if dfin is not None else np.zeros((dv, dk))
+            if z == a:
+                ds0[n, h] = dF
+                continue
+            out = _chunk_bwd_chain(q[a:z, h], k[a:z, h], v[a:z, h], g[a:z, h], beta[a:z, h], S0, d_o[a:z, h], dF,
+                                   float(scale), int(chunk))
+            dq[a:z, h], dkk[a:z, h], dvv[a:z, h], dg[a:z, h], db[a:z, h], ds0[n, h] = out
     return dq, dkk, dvv, dg, db, ds0
 
 

@@ -179,3 +179,19 @@ def test_backward_across_recompute_blocks(orc):
             ap[a], am[a] = xp, xm
             num = (loss(*ap) - loss(*am)) / (2 * h)
             assert abs(gx[idx] - num) <= 1e-7 * (1.0 + abs(num)), (a, idx)
+
+
+@pytest.mark.parametrize("chunk", [1, 5, 16, 64])
+def test_chunked_backward_equals_token_loop(orc, chunk):
+    """The chunk form's chain rule (the GPU backward's algebra) against reverse mode through the token
+    loop: ragged packed sequences (1, 63, 64, 65, 130 tokens and an empty one), decays of both strengths."""
+    rng = np.random.default_rng(30 + chunk)
+    lengths, H, dk, dv = [1, 63, 0, 64, 65, 130], 2, 8, 6
+    for decay in (1.0, 0.05):
+        q, k, v, g, b, s0, cu = _inputs(rng, lengths, H, dk, dv, decay=decay)
+        do = rng.standard_normal(v.shape)
+        dfin = rng.standard_normal(s0.shape)
+        ref = orc.kda_tokenloop_bwd(q, k, v, g, b, do, s0, cu, 0.7, d_final=dfin)
+        got = orc.kda_chunked_bwd(q, k, v, g, b, do, s0, cu, 0.7, d_final=dfin, chunk=chunk)
+        for name, x, r in zip(("dq", "dk", "dv", "dg", "dbeta", "dS0"), got, ref):
+            assert orc.rel_l2(x, r) < 1e-12, (name, decay)
