@@ -65,3 +65,26 @@ def test_traffic_lookup_follows_the_kernel_source(tmp_path, monkeypatch):
     assert bench.measured_traffic("recurrent_step_kernel", "kda_recurrent.cu", "other") is None
     (csrc / "kda_recurrent.cu").write_bytes(src + b"\n// changed\n")
     assert bench.measured_traffic("recurrent_step_kernel", "kda_recurrent.cu", "decode_64") is None
+
+
+def test_backward_chunk_slots_are_distinct_and_bounded():
+    """The backward keeps per-chunk data at slot (bos_n + 64 j) // 64 + n for chunk j of sequence n: over
+    random packed batches (empty sequences included) the slots are distinct and below T // 64 + N + 1,
+    the size its workspace allocates."""
+    import numpy as np
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        N = int(rng.integers(1, 40))
+        lengths = rng.integers(0, 300, size=N) * (rng.random(N) > 0.2)
+        bos = np.concatenate([[0], np.cumsum(lengths)])
+        T = int(bos[-1])
+        slots = [(int(bos[n]) + 64 * j) // 64 + n for n in range(N) for j in range((int(lengths[n]) + 63) // 64)]
+        assert len(set(slots)) == len(slots)
+        assert all(0 <= s < T // 64 + N + 1 for s in slots)
+
+
+def test_backward_roofline_constants():
+    import bench
+    # per chunk of 64 tokens and head: 12 C d^2 + 10 C^2 d flop, per token-head
+    assert bench.bwd_flops_per_token_head() == (12 * 64 * 128 * 128 + 10 * 64 * 64 * 128) / 64
+    assert abs(bench.fp32_alu_peak_tflops() - 80.54784) < 1e-9
