@@ -9,9 +9,16 @@ sum over ranks).  The same JSON line carries the decode half of the metric:
 one fused kda_recurrent_step of 64 sequences x 96 heads, in place on the
 403 MB fp32 state, as state GB/s.
 
-Inputs are synthetic (seeded counter-based generator, kda_synth) and larger
-than the 129 MB L2 (1.2 GB per prefill step, 0.84 GB per decode step), so L2 is
-not flushed between iterations.
+The line also times every other configuration at full size: the tiny fp32
+prefill (4 heads x 256 tokens), the 32 packed sequences of 1K..32K tokens with
+initial states, and the 262,144-token prefill from raw inputs through the fused
+front end with the sigmoid output gate; the last key, ``per_config``, repeats
+each configuration's figure compactly.
+
+Inputs are synthetic (seeded counter-based generator, kda_synth; the two largest
+workloads draw their values on the device with torch's seeded generator, same
+distributions) and larger than the 129 MB L2 (1.2 GB per prefill step, 0.84 GB
+per decode step), so L2 is not flushed between iterations.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -210,6 +217,28 @@ def make_decode_inputs(w, device):
     st = fill_device(w.seed, ks.TID_STATE, ks.NORMAL, (N, H, d, d), "f32", 0.0, w.init_state_std, device=device)
     cs = fill_device(w.seed, ks.TID_CONV_STATE, ks.NORMAL, (N, 3, 3 * C), "bf16", device=device)
     return xs, cw, g, b, st, cs
+
+
+def device_draws(shape, kind, dtype, gen, rows_per=1 << 14):
+    """A tensor of ``shape`` drawn on the device by torch's seeded generator ``gen``, slice by slice
+    (no full-size fp32 temporary): ``kind`` "normal" N(0,1), "unit" rows N(0,1) normalised over the
+    last axis, "neg5sig" -5 sigmoid(z), "negsp5" max(-5, -softplus(z)), "sigmoid" sigmoid(z)."""
+    import torch
+    out = torch.empty(shape, dtype=dtype, device=gen.device)
+    flat = out.view(shape[0], -1)
+    for r0 in range(0, shape[0], rows_per):
+        r1 = min(shape[0], r0 + rows_per)
+        z = torch.randn((r1 - r0,) + tuple(shape[1:]), device=gen.device, generator=gen, dtype=torch.float32)
+        if kind == "unit":
+            z = z / z.norm(dim=-1, keepdim=True)
+        elif kind == "neg5sig":
+            z = -5.0 * torch.sigmoid(z)
+        elif kind == "negsp5":
+            z = torch.clamp(-torch.nn.functional.softplus(z), min=-5.0)
+        elif kind == "sigmoid":
+            z = torch.sigmoid(z)
+        flat[r0:r1] = z.reshape(r1 - r0, -1).to(dtype)
+    return out
 
 
 def timed(fn, steps, warmup, stream, dist=None):
@@ -467,6 +496,82 @@ def run_ours(args):
     ms_two, _, _ = timed(two_pass, lsteps, args.warmup, stream, dist)
     del xf, outs, gf, bf, of, fsf, wsf
 
+    # ---------------- the same 8K prefill through kda_chunk_fwd_noalloc (static 64 MiB scratch) ----------
+    qn, kn, vn, gn, bn = make_prefill_inputs(w, device)
+    nsteps = max(5, args.steps // 4)
+    ms_na, _, _ = timed(lambda: kda.kda_chunk_fwd_noalloc(qn, kn, vn, gn, bn, o=o, final_state=fs, stream=stream),
+                        nsteps, args.warmup, stream, dist)
+    del qn, kn, vn, gn, bn
+
+    # ---------------- the tiny fp32 workload (fp32 path on the CUDA cores; latency-bound) ----------------
+    wt = ks.workload("tiny_fp32")
+    from kda_synth.device import to_device
+    tin = [to_device(x) for x in (wt.qkv("q"), wt.qkv("k"), wt.qkv("v"), wt.g(), wt.beta())]
+    ot = torch.empty((wt.T, wt.H, wt.d), dtype=torch.float32, device=device)
+    fst = torch.empty((1, wt.H, wt.d, wt.d), dtype=torch.float32, device=device)
+    tsteps = max(50, args.steps)
+    ms_tiny, _, _ = timed(lambda: kda.kda_chunk_fwd(*tin, o=ot, final_state=fst, stream=stream), tsteps,
+                          args.warmup, stream, dist)
+    tiny_bytes = prefill_bytes(wt.T, wt.H, 1) + wt.T * wt.H * (2 * 3 * 128 + 2 * 128)  # fp32 q, k, v, o
+    del tin, ot, fst
+
+    # ---------------- varlen_32 at full size: 32 packed sequences, per-sequence initial states ----------------
+    # Values are drawn on the device (torch's seeded generator, the workload's distributions): the host
+    # generator would take minutes for 65 GB of inputs; the parity tests check this workload's bits.
+    wv = ks.workload("varlen_32")
+    gv_ = torch.Generator(device=device).manual_seed(53004)
+    Tv, Nv = wv.T, wv.N
+    qv = device_draws((Tv, wv.H, wv.d), "unit", torch.bfloat16, gv_)
+    kv = device_draws((Tv, wv.H, wv.d), "unit", torch.bfloat16, gv_)
+    vv = device_draws((Tv, wv.H, wv.d), "normal", torch.bfloat16, gv_)
+    gvv = device_draws((Tv, wv.H, wv.d), "neg5sig", torch.float32, gv_)
+    bv = device_draws((Tv, wv.H), "sigmoid", torch.float32, gv_)
+    s0v = device_draws((Nv, wv.H, wv.d, wv.d), "normal", torch.float32, gv_) * wv.init_state_std
+    cuv = torch.from_numpy(wv.cu_seqlens()).to(device)
+    ov = torch.empty((Tv, wv.H, wv.d), dtype=torch.bfloat16, device=device)
+    fsv = torch.empty_like(s0v)
+    full_v, _ = kda.kda_chunk_fwd_workspace_size(Nv, Tv, wv.H, torch.bfloat16, True)
+    wsv = torch.empty(min(full_v, 24 << 30), dtype=torch.uint8, device=device)
+    vsteps = max(3, args.steps // 10)
+    ms_var, ms_var_launch, _ = timed(lambda: kda.kda_chunk_fwd(qv, kv, vv, gvv, bv, s0v, cuv, o=ov, final_state=fsv,
+                                                               workspace=wsv, stream=stream),
+                                     vsteps, args.warmup, stream, dist)
+    var_bytes = prefill_bytes(Tv, wv.H, Nv, init_state=True)
+    var_gbs = var_bytes / (ms_var_launch * 1e-3) / 1e9
+    del qv, kv, vv, gvv, bv, s0v, cuv, ov, fsv, wsv
+    torch.cuda.empty_cache()
+
+    # ---------------- long_256k at full size: raw q, k, v -> front end -> chunk_kda -> sigmoid output gate ----------
+    wl = ks.workload("long_256k")
+    gl_ = torch.Generator(device=device).manual_seed(53005)
+    Tl, Cl = wl.T, wl.H * wl.d
+    xl = [device_draws((Tl, Cl), "normal", torch.bfloat16, gl_) for _ in range(3)]
+    cwl = (device_draws((3 * Cl, 4), "normal", torch.float32, gl_) * wl.conv_w_std).to(torch.bfloat16)
+    gll = device_draws((Tl, wl.H, wl.d), "negsp5", torch.float32, gl_)
+    bl = device_draws((Tl, wl.H), "sigmoid", torch.float32, gl_)
+    gatel = device_draws((Tl, Cl), "normal", torch.bfloat16, gl_)
+    ol = torch.empty((Tl, wl.H, wl.d), dtype=torch.bfloat16, device=device)
+    fsl = torch.empty((1, wl.H, wl.d, wl.d), dtype=torch.float32, device=device)
+    full_l, _ = kda.kda_chunk_fwd_workspace_size(1, Tl, wl.H, torch.bfloat16, False)
+    wsl = torch.empty(full_l, dtype=torch.uint8, device=device)
+    lsteps5 = max(3, args.steps // 10)
+    ms_long, ms_long_launch, _ = timed(lambda: kda.kda_chunk_fwd_frontend(*xl, cwl, gll, bl, wl.H, out_gate=gatel, o=ol,
+                                                                          final_state=fsl, workspace=wsl,
+                                                                          stream=stream),
+                                       lsteps5, args.warmup, stream, dist)
+    qkv_l = [torch.empty((Tl, wl.H, wl.d), dtype=torch.bfloat16, device=device) for _ in range(3)]
+
+    def long_two_pass():
+        kda.kda_shortconv_l2norm(*xl, cwl, wl.H, q=qkv_l[0], k=qkv_l[1], v=qkv_l[2], stream=stream)
+        kda.kda_chunk_fwd(*qkv_l, gll, bl, out_gate=gatel, o=ol, final_state=fsl, workspace=wsl, stream=stream)
+    ms_long2, _, _ = timed(long_two_pass, lsteps5, args.warmup, stream, dist)
+    # fused minimum per token: raw q, k, v (3 x 12288 bf16) + g fp32 + beta + gate bf16 + o bf16
+    long_bytes_tok = 3 * Cl * 2 + Cl * 4 + wl.H * 4 + Cl * 2 + Cl * 2
+    long_bytes = Tl * long_bytes_tok + 3 * Cl * 4 * 2 + wl.H * wl.d * wl.d * 4
+    long_gbs = long_bytes / (ms_long_launch * 1e-3) / 1e9
+    del xl, cwl, gll, bl, gatel, ol, fsl, wsl, qkv_l
+    torch.cuda.empty_cache()
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -551,8 +656,42 @@ def run_ours(args):
         "value": wf.T * world / (ms_fused * 1e-3), "unit": "tokens/s", "ms_per_step": ms_fused, "steps": lsteps,
         "gpu_launches": lsteps * 3, "two_pass_value": wf.T * world / (ms_two * 1e-3), "two_pass_ms_per_step": ms_two,
         "note": "kda_chunk_fwd_frontend vs kda_shortconv_l2norm + kda_chunk_fwd; same output bits"}
+    line["noalloc_prefill"] = {
+        "workload": f"{w.name} through kda_chunk_fwd_noalloc: the library's static 64 MiB scratch, chunk ranges "
+                    "of 5 rows one after the other on the caller's stream",
+        "value": w.T * world / (ms_na * 1e-3), "unit": "tokens/s", "ms_per_step": ms_na, "steps": nsteps}
+    line["varlen_32"] = {
+        "workload": f"varlen_32: {Nv} packed sequences (1K..32K tokens, sum {Tv}), H={wv.H}, bf16 q,k,v, fp32 g, beta, "
+                    "initial states N(0, 0.02); values drawn on the device with the workload's distributions",
+        "value": Tv * world / (ms_var * 1e-3), "unit": "tokens/s", "ms_per_step": ms_var, "steps": vsteps,
+        "algorithmic_bytes_per_launch": var_bytes,
+        "roofline": {"bound": "hbm", "achieved": var_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": var_gbs / hbm_peak,
+                     "traffic": measured_traffic("kda_chunk_fwd", "kda_chunk_tc.cu", "varlen_32"),
+                     "peak_source": peak_src}}
+    line["long_256k"] = {
+        "workload": f"long_256k: T={Tl}, raw q,k,v bf16 [{Tl}, {Cl}] -> ShortConv(4)+SiLU+L2norm -> chunk_kda with "
+                    "g = max(-5, -softplus(z)) -> o * sigmoid(gate); kda_chunk_fwd_frontend (fused)",
+        "value": Tl * world / (ms_long * 1e-3), "unit": "tokens/s", "ms_per_step": ms_long, "steps": lsteps5,
+        "algorithmic_bytes_per_launch": long_bytes,
+        "two_pass_value": Tl * world / (ms_long2 * 1e-3), "two_pass_ms_per_step": ms_long2,
+        "roofline": {"bound": "hbm", "achieved": long_gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": long_gbs / hbm_peak,
+                     "traffic": measured_traffic("kda_chunk_fwd_frontend", "kda_chunk_tc.cu", "long_256k"),
+                     "peak_source": peak_src}}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+    r3 = lambda x: float(f"{x:.4g}")
+    # every configuration's figure, last and compact (it must survive a truncated log tail)
+    line["per_config"] = {
+        "tiny_fp32": {"tok_s": r3(wt.T * world / (ms_tiny * 1e-3)), "ms": r3(ms_tiny), "bound": "latency",
+                      "hbm_frac": r3(tiny_bytes / (ms_tiny * 1e-3) / 1e9 / hbm_peak)},
+        "prefill_8k": {"tok_s": r3(value), "ms": r3(ms_step), "hbm_frac": r3(achieved_gbs / hbm_peak),
+                       "tensor_frac": r3(achieved_tflops / tc_peak)},
+        "decode_64": {"GB_s": r3(dec_gbs), "ms": r3(ms_dec), "hbm_frac": r3(dec_gbs / hbm_peak)},
+        "varlen_32": {"tok_s": r3(Tv * world / (ms_var * 1e-3)), "ms": r3(ms_var), "hbm_frac": r3(var_gbs / hbm_peak)},
+        "long_256k": {"tok_s": r3(Tl * world / (ms_long * 1e-3)), "ms": r3(ms_long),
+                      "hbm_frac": r3(long_gbs / hbm_peak), "two_pass_ms": r3(ms_long2)},
+        "noalloc_8k_ms": r3(ms_na), "backward_8k_ms": r3(ms_bwd), "peak_GB_s": hbm_peak}
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -54,6 +54,27 @@ namespace {
 constexpr size_t kStaticScratchBytes = size_t(64) << 20;
 static __device__ __align__(256) uint8_t g_chunk_scratch[kStaticScratchBytes];
 
+// Device address of g_chunk_scratch on the current device.  In host code the array's name stands for a
+// host-side shadow, not device memory, so the address is looked up once per device (the first call
+// on that device, with it current) and kept.
+cudaError_t static_scratch(void** out) {
+    static std::mutex mu;
+    static void* cache[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_chunk_scratch);
+        if (e != cudaSuccess) return e;
+        cache[dev] = p;
+    }
+    *out = cache[dev];
+    return cudaSuccess;
+}
+
 }  // namespace
 
 namespace {
@@ -106,6 +127,43 @@ kda_status check_batch(const int32_t* cu, int N, int64_t T_total, int H) {
     REQUIRE((int64_t)N * H <= 0x7FFFFFFF, "N * H too large");
     REQUIRE(T_total <= ((int64_t)1 << 40), "T_total too large");
     return KDA_OK;
+}
+
+}  // namespace
+
+namespace {
+
+// kda_chunk_fwd after its pointer checks; `overlap` as launch_chunk_tc.
+kda_status chunk_fwd_checked(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                             const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
+                             int dk, int dv, float scale, int chunk_size, kda_dtype dtype, const void* out_gate,
+                             void* o, float* final_state, void* workspace, size_t workspace_bytes, void* stream,
+                             bool overlap) {
+    kda_status s = check_batch(cu_seqlens, N, T_total, H);
+    if (s != KDA_OK) return s;
+    if (dk != kda::kHeadDim || dv != kda::kHeadDim)
+        return set_error(KDA_ERR_UNSUPPORTED, "only dk = dv = 128 is supported (got %d, %d)", dk, dv);
+    if (chunk_size != kda::kChunk)
+        return set_error(KDA_ERR_UNSUPPORTED, "only chunk_size = 64 is supported (got %d)", chunk_size);
+    REQUIRE(dtype == KDA_DTYPE_F32 || dtype == KDA_DTYPE_BF16, "bad dtype");
+    REQUIRE(std::isfinite(scale), "scale must be finite");
+    if (dtype == KDA_DTYPE_F32)
+        return from_cuda(kda::launch_chunk_simt(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, scale, dtype,
+                                                out_gate, o, final_state, static_cast<cudaStream_t>(stream)),
+                         "kda_chunk_fwd launch");
+    REQUIRE(T_total < ((int64_t)1 << 31), "T_total must be below 2^31 for the bf16 path (tensor-map coordinates)");
+    REQUIRE(T_total / 64 + N <= 0x7FFFFFFF, "too many chunks");
+    size_t need = 0;
+    kda::chunk_tc_workspace(N, T_total, H, cu_seqlens != nullptr, nullptr, &need);
+    REQUIRE(workspace != nullptr && workspace_bytes >= need,
+            "workspace must hold at least %zu bytes for these sizes (got %zu)", need, workspace_bytes);
+    OPTIONAL_PTR(workspace);
+    unsigned int* err = kda::device_error_word();
+    if (!err) return set_error(KDA_ERR_CUDA, "device error word unavailable");
+    return from_cuda(kda::launch_chunk_tc(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, scale, out_gate, o,
+                                          final_state, workspace, workspace_bytes, nullptr, err,
+                                          static_cast<cudaStream_t>(stream), 0, nullptr, 0, overlap),
+                     "kda_chunk_fwd launch");
 }
 
 }  // namespace
@@ -174,31 +232,8 @@ kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const floa
                          void* o, float* final_state, void* workspace, size_t workspace_bytes, void* stream) {
     REQUIRE_PTR(q); REQUIRE_PTR(k); REQUIRE_PTR(v); REQUIRE_PTR(g); REQUIRE_PTR(beta); REQUIRE_PTR(o);
     OPTIONAL_PTR(init_state); OPTIONAL_PTR(final_state); OPTIONAL_PTR(out_gate);
-    kda_status s = check_batch(cu_seqlens, N, T_total, H);
-    if (s != KDA_OK) return s;
-    if (dk != kda::kHeadDim || dv != kda::kHeadDim)
-        return set_error(KDA_ERR_UNSUPPORTED, "only dk = dv = 128 is supported (got %d, %d)", dk, dv);
-    if (chunk_size != kda::kChunk)
-        return set_error(KDA_ERR_UNSUPPORTED, "only chunk_size = 64 is supported (got %d)", chunk_size);
-    REQUIRE(dtype == KDA_DTYPE_F32 || dtype == KDA_DTYPE_BF16, "bad dtype");
-    REQUIRE(std::isfinite(scale), "scale must be finite");
-    if (dtype == KDA_DTYPE_F32)
-        return from_cuda(kda::launch_chunk_simt(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, scale, dtype,
-                                                out_gate, o, final_state, static_cast<cudaStream_t>(stream)),
-                         "kda_chunk_fwd launch");
-    REQUIRE(T_total < ((int64_t)1 << 31), "T_total must be below 2^31 for the bf16 path (tensor-map coordinates)");
-    REQUIRE(T_total / 64 + N <= 0x7FFFFFFF, "too many chunks");
-    size_t need = 0;
-    kda::chunk_tc_workspace(N, T_total, H, cu_seqlens != nullptr, nullptr, &need);
-    REQUIRE(workspace != nullptr && workspace_bytes >= need,
-            "workspace must hold at least %zu bytes for these sizes (got %zu)", need, workspace_bytes);
-    OPTIONAL_PTR(workspace);
-    unsigned int* err = kda::device_error_word();
-    if (!err) return set_error(KDA_ERR_CUDA, "device error word unavailable");
-    return from_cuda(kda::launch_chunk_tc(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, scale, out_gate, o,
-                                          final_state, workspace, workspace_bytes, nullptr, err,
-                                          static_cast<cudaStream_t>(stream)),
-                     "kda_chunk_fwd launch");
+    return chunk_fwd_checked(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, dk, dv, scale, chunk_size,
+                             dtype, out_gate, o, final_state, workspace, workspace_bytes, stream, true);
 }
 
 kda_status kda_chunk_bwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv, int chunk_size,
@@ -354,10 +389,11 @@ kda_status kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, co
                                  const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
                                  int dk, int dv, float scale, int chunk_size, kda_dtype dtype, const void* out_gate,
                                  void* o, float* final_state, void* stream) {
-    if (dtype == KDA_DTYPE_F32)  // the fp32 path needs no workspace
-        return kda_chunk_fwd(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, dk, dv, scale, chunk_size,
-                             dtype, out_gate, o, final_state, nullptr, 0, stream);
     REQUIRE_PTR(q); REQUIRE_PTR(k); REQUIRE_PTR(v); REQUIRE_PTR(g); REQUIRE_PTR(beta); REQUIRE_PTR(o);
+    OPTIONAL_PTR(init_state); OPTIONAL_PTR(final_state); OPTIONAL_PTR(out_gate);
+    if (dtype == KDA_DTYPE_F32)  // the fp32 path needs no workspace
+        return chunk_fwd_checked(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, dk, dv, scale, chunk_size,
+                                 dtype, out_gate, o, final_state, nullptr, 0, stream, false);
     kda_status s = check_batch(cu_seqlens, N, T_total, H);
     if (s != KDA_OK) return s;
     REQUIRE(dtype == KDA_DTYPE_BF16, "bad dtype");
@@ -368,10 +404,11 @@ kda_status kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, co
         return set_error(KDA_ERR_UNSUPPORTED, "the static scratch holds %zu bytes; these sizes need at least %zu",
                          kStaticScratchBytes, need);
     void* scratch = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&scratch, g_chunk_scratch);
-    if (e != cudaSuccess) return from_cuda(e, "kda_chunk_fwd_noalloc scratch");
-    return kda_chunk_fwd(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, dk, dv, scale, chunk_size, dtype,
-                         out_gate, o, final_state, scratch, kStaticScratchBytes, stream);
+    cudaError_t e = static_scratch(&scratch);
+    if (e != cudaSuccess) return from_cuda(e, "kda_chunk_fwd_noalloc: device address of the static scratch");
+    // every range one after the other on `stream`: no internal streams or events
+    return chunk_fwd_checked(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, dk, dv, scale, chunk_size,
+                             dtype, out_gate, o, final_state, scratch, kStaticScratchBytes, stream, false);
 }
 
 kda_status kda_chunk_fwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv, int chunk_size,
@@ -405,8 +442,10 @@ kda_status kda_recurrent_step(const void* xq, const void* xk, const void* xv, in
     REQUIRE(x_row_stride >= (int64_t)H * dk && x_row_stride % 8 == 0,
             "x_row_stride must be >= H*d and a multiple of 8 (got %lld)", (long long)x_row_stride);
     REQUIRE(std::isfinite(scale) && std::isfinite(eps) && eps >= 0.f, "scale and eps must be finite, eps >= 0");
+    unsigned int* err = kda::device_error_word();
+    if (!err) return set_error(KDA_ERR_CUDA, "device error word unavailable");
     return from_cuda(kda::launch_recurrent_step(xq, xk, xv, x_row_stride, conv_w, g, beta, state, conv_state, N,
-                                                H, scale, eps, o, static_cast<cudaStream_t>(stream)),
+                                                H, scale, eps, o, err, static_cast<cudaStream_t>(stream)),
                      "kda_recurrent_step launch");
 }
 

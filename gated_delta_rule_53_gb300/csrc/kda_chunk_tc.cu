@@ -456,6 +456,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         cp_async_wait_all();
         __syncthreads();
         if (*sAbort) break;
+        // beta in [0, 1] (tokens past the chunk's end read as 0)
+        if (warp < 2 && __any_sync(0xFFFFFFFFu, !(sBeta[tid] >= 0.f && sBeta[tid] <= 1.f)) && lane == 0)
+            raise_device_error(err, kErrBetaRange);
         // ---- running sum of g per key channel (log2 units): thread (c, half) sums tokens 32 half .. +31
         {
             const int c = tid & 127, hh = tid >> 7;
@@ -463,12 +466,17 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
             for (int r = 0; r < 32; ++r)
                 gv[r] = (32 * hh + r) < L ? *reinterpret_cast<const float*>(sm + P_G + g_off(32 * hh + r, c)) : 0.f;
-            float acc = 0.f;
+            float acc = 0.f, gmin = 0.f, gmax = 0.f;
 #pragma unroll
             for (int r = 0; r < 32; ++r) {
+                gmin = fminf(gmin, gv[r]);
+                gmax = fmaxf(gmax, gv[r]);
                 acc = fmaf(gv[r], kLog2e, acc);
                 gv[r] = acc;
             }
+            // g in [-5, 0]: min and max skip a NaN, the running sum does not
+            if (__any_sync(0xFFFFFFFFu, !(gmin >= -5.f && gmax <= 0.f && acc == acc)) && lane == 0)
+                raise_device_error(err, kErrGateRange);
             if (hh == 0) sTot[c] = acc;
             __syncthreads();
             const float base = hh ? sTot[c] : 0.f;
@@ -1227,7 +1235,8 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
                             const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
                             float scale, const void* out_gate, void* o, float* final_state, void* workspace,
                             size_t workspace_bytes, const ChunkFrontend* front, unsigned int* err,
-                            cudaStream_t stream, int state_mode, float* final_state2, int state_mode2) {
+                            cudaStream_t stream, int state_mode, float* final_state2, int state_mode2,
+                            bool overlap) {
     CUtensorMap tq = {}, tk = {}, tv = {}, tg;
     if (!front && (!encode_chunk_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, T_total, H) ||
                    !encode_chunk_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, T_total, H) ||
@@ -1262,10 +1271,11 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
     chunk_offsets_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, T_total, off);
     // A second state pass on the same operands (final_state2, state_mode2) needs them all at once.
     if (final_state2 && rows < rows_max) return cudaErrorInvalidValue;
-    if (!front && !final_state2 && rows >= 2 && rows_max >= 2 * kPipeMinRows) {
-        // Overlapped ranges: the chunk rows in about kPipeRanges ranges (of at least kPipeMinRows rows:
-        // each extra range costs about 35 us of wave tails and state-pass start-up), their operands in
-        // two alternating halves of the workspace; range r's state pass (high-priority stream, 96 of
+    if (overlap && !front && !final_state2 && rows >= 2 * kPipeMinRows && rows_max >= 2 * kPipeMinRows) {
+        // Overlapped ranges (when the call has, and the workspace holds, at least two ranges of
+        // kPipeMinRows chunk rows): the chunk rows in about kPipeRanges ranges (of at least kPipeMinRows
+        // rows: each extra range costs about 35 us of wave tails and state-pass start-up), their operands
+        // in two alternating halves of the workspace; range r's state pass (high-priority stream, 96 of
         // the 152 SMs for 96 chains) runs while range r+1's operands are computed on the other SMs
         // (low-priority stream, one CTA per item, so that the state pass's CTAs take SMs first as they
         // free up).  Ordered by events only.  Not for the fused front end, whose operand kernel

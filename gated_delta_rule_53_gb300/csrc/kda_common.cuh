@@ -12,16 +12,19 @@ namespace kda {
 constexpr int kHeadDim = 128;  // d = dk = dv supported by every kernel
 constexpr int kChunk = 64;     // chunk length of the prefill
 
-// Kernels that wait on a barrier get a pointer to the library's device error
-// word (kda_api.cu); a wait that runs out sets it instead of spinning forever,
-// and the host reads it through kda_device_error().
+// Kernels get a pointer to the library's device error word (kda_api.cu) and OR a
+// bit into it: a wait that runs out (instead of spinning forever), an input outside
+// the range the arithmetic relies on.  The host reads and clears it through
+// kda_device_error().  The bits are the KDA_DEVICE_ERR_* values of kda.h.
 enum DeviceError : unsigned int {
     kErrNone = 0,
-    kErrMbarTimeout = 1,
+    kErrMbarTimeout = KDA_DEVICE_ERR_WAIT_TIMEOUT,
+    kErrGateRange = KDA_DEVICE_ERR_GATE_RANGE,
+    kErrBetaRange = KDA_DEVICE_ERR_BETA_RANGE,
 };
 
 __device__ __forceinline__ void raise_device_error(unsigned int* err, unsigned int code) {
-    if (err) atomicCAS(err, 0u, code);
+    if (err) atomicOr(err, code);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
@@ -75,7 +78,7 @@ namespace kda {
 cudaError_t launch_recurrent_step(const void* xq, const void* xk, const void* xv, int64_t x_stride,
                                   const void* conv_w, const float* g, const float* beta, float* state,
                                   void* conv_state, int N, int H, float scale, float eps, void* o,
-                                  cudaStream_t stream);
+                                  unsigned int* err, cudaStream_t stream);
 
 cudaError_t launch_shortconv_l2norm(const void* xq, const void* xk, const void* xv, int64_t x_stride,
                                     const void* conv_w, const int32_t* cu_seqlens, int N, int64_t T_total,
@@ -115,13 +118,14 @@ constexpr int kStateZeroU = 1, kStateIdentity = 2;
 
 // o may be null (no outputs).  final_state2 (with state_mode2): a second state pass over the same
 // operands, from a zero / identity start, without outputs; it needs every chunk in one range of the
-// workspace (cudaErrorInvalidValue otherwise).
+// workspace (cudaErrorInvalidValue otherwise).  overlap = false keeps every range on `stream`, one
+// after the other (no internal streams or events).
 cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const float* g, const float* beta,
                             const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
                             float scale, const void* out_gate, void* o, float* final_state, void* workspace,
                             size_t workspace_bytes, const ChunkFrontend* front, unsigned int* err,
                             cudaStream_t stream, int state_mode = 0, float* final_state2 = nullptr,
-                            int state_mode2 = 0);
+                            int state_mode2 = 0, bool overlap = true);
 
 // gate = x W_gate^T (bf16), z = x W_a^T (bf16 scratch [T, rank]), g = max(-5, -softplus(z W_b^T + a_h))
 // (fp32); w_gate_a = [W_gate ; W_a] stacked, [H*d + rank, hidden].

@@ -10,7 +10,8 @@
 //     s~ = s * alpha;  p = s~ . k;  s = s~ + beta (v_r - p) k;  o_r = scale s . q
 // with both dot products reduced by warp shuffles, and written back in place.  The convolution
 // state is shifted by a second small kernel once every CTA has read it.  The step streams the state
-// once in and once out: it is bound by HBM.
+// once in and once out: it is bound by HBM.  g outside [-5, 0] or beta outside [0, 1] sets a bit of
+// the device error word (the update itself needs neither bound).
 #include "kda_common.cuh"
 
 namespace kda {
@@ -30,7 +31,7 @@ recurrent_step_kernel(const __nv_bfloat16* __restrict__ xq, const __nv_bfloat16*
                       const __nv_bfloat16* __restrict__ conv_w, const float* __restrict__ g,
                       const float* __restrict__ beta, float* __restrict__ state,
                       __nv_bfloat16* __restrict__ conv_state, int H, float scale, float eps,
-                      __nv_bfloat16* __restrict__ o) {
+                      __nv_bfloat16* __restrict__ o, unsigned int* err) {
     __shared__ float4 s_q[32], s_k[32], s_v[32], s_alpha[32];
     __shared__ float s_beta;
 
@@ -89,7 +90,16 @@ recurrent_step_kernel(const __nv_bfloat16* __restrict__ xq, const __nv_bfloat16*
     } else if (warp == 3) {
         const float4 gv = *(reinterpret_cast<const float4*>(g + (int64_t)nh * kHeadDim) + lane);
         s_alpha[lane] = make_float4(expf(gv.x), expf(gv.y), expf(gv.z), expf(gv.w));
-        if (lane == 0) s_beta = beta[nh];
+        const float bv = beta[nh];
+        if (lane == 0) s_beta = bv;
+        if (pt == 0) {  // inputs in the ranges of the pages (g in [-5, 0], beta in [0, 1]), once per head
+            const float lo = fminf(fminf(gv.x, gv.y), fminf(gv.z, gv.w));
+            const float hi = fmaxf(fmaxf(gv.x, gv.y), fmaxf(gv.z, gv.w));
+            const float sum = gv.x + gv.y + gv.z + gv.w;  // NaN-propagating
+            if (__any_sync(0xFFFFFFFFu, !(lo >= -5.f && hi <= 0.f && sum == sum)) && lane == 0)
+                raise_device_error(err, kErrGateRange);
+            if (lane == 0 && !(bv >= 0.f && bv <= 1.f)) raise_device_error(err, kErrBetaRange);
+        }
     }
     __syncthreads();
 
@@ -148,14 +158,14 @@ __global__ void conv_shift_kernel(const __nv_bfloat16* __restrict__ xq, const __
 cudaError_t launch_recurrent_step(const void* xq, const void* xk, const void* xv, int64_t x_stride,
                                   const void* conv_w, const float* g, const float* beta, float* state,
                                   void* conv_state, int N, int H, float scale, float eps, void* o,
-                                  cudaStream_t stream) {
+                                  unsigned int* err, cudaStream_t stream) {
     const int64_t blocks = (int64_t)N * H;
     if (blocks == 0) return cudaSuccess;
     if (blocks * kParts > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
     recurrent_step_kernel<<<(unsigned)(blocks * kParts), kThreads, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(xq), static_cast<const __nv_bfloat16*>(xk),
         static_cast<const __nv_bfloat16*>(xv), x_stride, static_cast<const __nv_bfloat16*>(conv_w), g, beta, state,
-        static_cast<__nv_bfloat16*>(conv_state), H, scale, eps, static_cast<__nv_bfloat16*>(o));
+        static_cast<__nv_bfloat16*>(conv_state), H, scale, eps, static_cast<__nv_bfloat16*>(o), err);
     const int64_t groups = 3 * (int64_t)H * kHeadDim / 4;
     conv_shift_kernel<<<dim3((unsigned)((groups + 255) / 256), (unsigned)N), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(xq), static_cast<const __nv_bfloat16*>(xk),

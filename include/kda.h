@@ -73,6 +73,11 @@ typedef enum {
 
 typedef enum { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype;
 
+/* Bits of the device error word (see kda_device_error). */
+#define KDA_DEVICE_ERR_WAIT_TIMEOUT 1u
+#define KDA_DEVICE_ERR_GATE_RANGE 2u
+#define KDA_DEVICE_ERR_BETA_RANGE 4u
+
 /*
  * Front end of a prefill: ShortConv(kernel 4) + SiLU on each of q, k, v, then
  * L2 normalisation of q and k over each head's d channels ("深入 Kimi-K3: Hugging
@@ -130,11 +135,15 @@ KDA_API kda_status kda_shortconv_l2norm(const void* xq, const void* xk, const vo
  *                  fastest with `full_bytes`; with less, the chunks are processed in
  *                  several ranges.  KDA_DTYPE_F32 ignores it (may be NULL, 0).
  *
- * With the whole workspace (`full_bytes`) and at least 128 chunk rows, consecutive ranges of
- * max(64, rows / 8) chunk rows overlap: the call forks two internal streams from `stream` with
- * events (the operand kernel on a low-priority one, the state pass on a high-priority one) and
- * makes `stream` wait for both before it returns; nothing else changes for the caller, and the
- * results are the same bits as one range.
+ * Overlapped ranges: when the call has at least 128 chunk rows (a chunk row is 64 tokens of
+ * every sequence's chunk numbering, all heads) and the workspace holds at least 128 of them,
+ * consecutive ranges of max(64, rows / 8) chunk rows overlap (at most half of what the workspace
+ * holds).  The call then forks two internal streams from `stream` with events (the operand kernel
+ * on a low-priority one, the state pass on a high-priority one) and makes `stream` wait for both
+ * before it returns; nothing else changes for the caller, and the results are the same bits as
+ * one range.  The two internal streams are per device and shared by every call: overlapped calls
+ * on one device are serialised through them even when the callers use independent streams.
+ * Otherwise every range runs on `stream`, one after the other.
  *
  * The bf16 path runs two kernels per range of chunks: the first computes, for every
  * (chunk, head) at once, everything that does not depend on the carried state (the
@@ -168,11 +177,18 @@ KDA_API kda_status kda_chunk_fwd_frontend(const void* xq, const void* xk, const 
 
 /*
  * kda_chunk_fwd without a caller workspace (no counterpart in the sources; an interface
- * convenience).  The bf16 path uses a 64 MiB scratch array that is part of the library's
- * device image (so nothing is allocated), processing as many chunk rows per range as fit.
+ * convenience for callers that cannot allocate device memory, e.g. code running inside an
+ * allocator-free runtime or under a memory pool it does not own).  The bf16 path uses a
+ * 64 MiB scratch array that is part of the library's device image (every GPU that loads the
+ * library holds it until exit), so neither the caller nor the library allocates anything: no
+ * cudaMalloc, no internal streams, no events.  Its chunk ranges (as many chunk rows per range
+ * as fit in 64 MiB; about 5 rows at H = 96) run one after the other on `stream`.
+ * The first call on a device looks up the array's device address (with that device current)
+ * and keeps it; make that first call before any stream capture.
  * Returns KDA_ERR_UNSUPPORTED, before enqueueing anything, when even one chunk row of all
  * heads does not fit (the `min_bytes` of kda_chunk_fwd_workspace_size exceeds 64 MiB: H above
- * about 290).  Calls share the scratch: they must not run concurrently on one device.
+ * about 290).  Calls share the scratch, which keeps the last call's contents: calls that
+ * overlap on one device race and must be ordered (one stream, or streams ordered by events).
  * Arguments and layouts as kda_chunk_fwd.
  */
 KDA_API kda_status kda_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g,
@@ -322,9 +338,20 @@ KDA_API const char* kda_last_error(void);
 
 /*
  * Reads and clears the device error word of the current device (synchronous:
- * waits for all work on the device).  0 = no fault.  A kernel sets it instead
- * of hanging when one of its bounded waits runs out.  Returns KDA_ERR_CUDA if
- * the read itself fails.
+ * waits for all work on the device).  0 = no fault; otherwise the OR of the
+ * KDA_DEVICE_ERR_* bits (defined after kda_dtype) raised since the last read:
+ *   KDA_DEVICE_ERR_WAIT_TIMEOUT  one of a kernel's bounded waits ran out (the kernel
+ *                                stopped instead of hanging; its outputs are incomplete)
+ *   KDA_DEVICE_ERR_GATE_RANGE    a log-decay g outside [-5, 0], or not finite (the bf16
+ *                                chunk path relies on the bound, "Kimi K3 架构全景",
+ *                                section 02, gate lower bound -5.0; "月之暗面发布Kimi K3
+ *                                开源大模型技术报告", 架构)
+ *   KDA_DEVICE_ERR_BETA_RANGE    a beta outside [0, 1], or not finite
+ * The range bits are raised by kda_chunk_fwd, kda_chunk_fwd_frontend,
+ * kda_chunk_fwd_noalloc and kda_chunk_segment_summary with bf16 inputs (every g
+ * and beta of every token is checked as it is read) and by kda_recurrent_step; the
+ * call still completes (nothing traps) and its results are then unspecified.
+ * Returns KDA_ERR_CUDA if the read itself fails.
  */
 KDA_API kda_status kda_device_error(unsigned int* code);
 
@@ -336,7 +363,7 @@ KDA_API kda_status kda_device_error(unsigned int* code);
  * and returns; kda_device_error() then reports it.  It exercises the path a kernel takes
  * instead of hanging, without faulting the GPU.  Asynchronous on `stream`.
  */
-#define KDA_DEVICE_ERR_WAIT_TIMEOUT 1u
+
 KDA_API kda_status kda_selftest_bounded_wait(unsigned int poll_limit, void* stream);
 
 /* Library version, e.g. "0.1.0". */

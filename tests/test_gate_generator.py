@@ -136,3 +136,48 @@ def test_gate_generator_matches_oracle(orc, T, hidden, H, rank):
     assert rel(gg, g_ref) <= 5e-3 and np.abs(gg - g_ref).max() <= 2e-2
     assert np.all(gg[:, 0, :] == -5.0)
     assert np.all((gg >= -5.0) & (gg <= 0.0))
+
+
+@pytest.mark.gpu
+def test_gate_generator_full_size_persistent_tiles(orc):
+    """x [8192, 7168] with 96 heads and rank 128, as the benchmark runs it: 64 row tiles x 49 column
+    tiles (3,136) in the x-side product and 64 x 48 in the rank product, on at most one CTA per SM, so
+    every CTA runs many tiles: the persistent loop past its first tile, both TMEM accumulators and
+    their phase flips, and every group of 16 row tiles.  Checked against the oracle on four rows of
+    every 128-row tile (one in each 32-lane quarter of the accumulator, at a position that moves from
+    tile to tile), over all columns."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_delta_rule_53_gb300 import build
+    build.build()
+    import gated_delta_rule_53_gb300 as kda
+    T, hidden, H, d, rank = 8192, 7168, 96, 128, 128
+    rng = np.random.default_rng(53107)
+    xq = bf16_round(rng.standard_normal((T, hidden), dtype=np.float32))
+    wgaq = bf16_round(rng.standard_normal((H * d + rank, hidden), dtype=np.float32) / np.sqrt(hidden))
+    wbq = bf16_round(rng.standard_normal((H * d, rank), dtype=np.float32) / np.sqrt(rank))
+    a = 2.0 * rng.standard_normal(H)
+    a[7] = 30.0   # one head at the floor
+    to = lambda m, dt: torch.from_numpy(np.ascontiguousarray(m)).to(dt).cuda()
+    gate, g = kda.kda_gate_generator(to(xq, torch.bfloat16), to(wgaq, torch.bfloat16), to(wbq, torch.bfloat16),
+                                     to(a, torch.float32), H, d)
+    torch.cuda.synchronize()
+    assert kda.device_error() == 0
+    mt = T // 128
+    rows = np.array([128 * i + 32 * qt + (7 * i + 11 * qt) % 32 for i in range(mt) for qt in range(4)])
+    assert len(np.unique(rows // 2048)) == T // 2048          # every group of 16 row tiles
+    idx = torch.from_numpy(rows).cuda()
+    gh = gate.index_select(0, idx).double().cpu().numpy()
+    gg = g.index_select(0, idx).double().cpu().numpy()
+    gate_ref, g_ref = orc.gate_generator(xq[rows], wgaq, wbq, a.astype(np.float32), H, d)
+    assert rel(gh, gate_ref) <= 5e-3
+    assert rel(gg, g_ref) <= 5e-3 and np.abs(gg - g_ref).max() <= 2e-2
+    # per tile as well: no 128 x 256 tile of either output is off on its own
+    nt = (H * d) // 256
+    for i in range(mt):
+        for j in range(nt):
+            r, c = slice(4 * i, 4 * i + 4), slice(256 * j, 256 * j + 256)
+            assert rel(gh[r, c], gate_ref[r, c]) <= 1e-2, (i, j)
+            gr = g_ref.reshape(len(rows), H * d)[r, c]
+            assert np.abs(gg.reshape(len(rows), H * d)[r, c] - gr).max() <= 2e-2, (i, j)
+    assert np.all(gg[:, 7, :] == -5.0)

@@ -438,6 +438,30 @@ def test_prefill_8k_sampled_heads(kda, orc):
         assert orc.rel_l2(host(fs[:, h:h + 1]), fs_ref) <= BF16_S_REL
 
 
+def test_prefill_4k_persistent_operand_pass_sampled_heads(kda, orc):
+    """4096 tokens x 96 heads with the whole workspace: 64 chunk rows, one range, so the operand
+    kernel runs persistently (two CTAs per SM, each taking about 20 (chunk, head) items with the
+    next item's loads in flight).  Heads 0, 50 and 95 checked in full against the oracle."""
+    w = ks.Workload("prefill_4k", "prefill", 53102, H=96, lengths=[4096])
+    T, H, d = w.T, w.H, w.d
+    q = fill_dev(w, ks.TID_Q, ks.UNIT_GROUPS, (T, H, d), "bf16", 0.0, float(d))
+    k = fill_dev(w, ks.TID_K, ks.UNIT_GROUPS, (T, H, d), "bf16", 0.0, float(d))
+    v = fill_dev(w, ks.TID_V, ks.NORMAL, (T, H, d), "bf16")
+    g = fill_dev(w, ks.TID_G, w.g_kind, (T, H, d), "f32")
+    b = fill_dev(w, ks.TID_BETA, ks.SIGMOID, (T, H), "f32")
+    full = kda.kda_chunk_fwd_workspace_size(1, T, H, torch.bfloat16, False)[0]
+    ws = torch.empty(full, dtype=torch.uint8, device="cuda")
+    o, fs = kda.kda_chunk_fwd(q, k, v, g, b, workspace=ws)
+    torch.cuda.synchronize()
+    assert kda.device_error() == 0
+    for h in (0, 50, 95):
+        qh, kh, vh, gh, bh = head_inputs(w, h, 0, T)
+        o_ref, fs_ref = orc.kda_tokenloop(qh, kh, vh, gh, bh)
+        o_h = host(o[:, h:h + 1, :])
+        assert orc.rel_l2(o_h, o_ref) <= BF16_O_REL and orc.max_abs(o_h, o_ref) <= BF16_O_ABS
+        assert orc.rel_l2(host(fs[:, h:h + 1]), fs_ref) <= BF16_S_REL
+
+
 def test_varlen_32_sampled_chains(kda, orc):
     """32 packed sequences (1K..32K tokens), H=96, initial states N(0, 0.02); the shortest,
     a middle and the longest sequence checked in full on heads 0 and 95."""

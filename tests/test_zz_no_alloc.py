@@ -4,7 +4,9 @@ It has no counterpart in the sources; it is the workspace path with the workspac
 a scratch array in the library's device image.  CPU tests: the symbol is exported and sizes
 whose smallest range does not fit are refused before anything is enqueued.  GPU tests: the
 result is bit-identical to kda_chunk_fwd with a caller workspace, also when the static
-scratch forces several ranges of chunks.
+scratch forces several ranges of chunks (8192 tokens x 96 heads: the workspace path overlaps
+its ranges on internal streams, the scratch path runs ranges of 5 chunk rows one after the
+other on the caller's stream), and on two calls in a row.
 """
 import ctypes
 
@@ -56,7 +58,7 @@ def test_oversize_is_refused_on_the_host(kda):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("lengths,H", [([130, 1, 0, 257, 5], 3), ([4096], 96)])
+@pytest.mark.parametrize("lengths,H", [([130, 1, 0, 257, 5], 3), ([4096], 96), ([8192], 96)])
 def test_noalloc_equals_workspace_path(kda, lengths, H):
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
@@ -73,4 +75,8 @@ def test_noalloc_equals_workspace_path(kda, lengths, H):
     assert np.isfinite(o2.float().cpu().numpy()).all()
     if H == 96:
         assert full > SCRATCH   # 4096 tokens x 96 heads need several ranges in the static scratch
+    # the same call twice in a row: the scratch keeps the last call's contents, which must not matter
+    o3, f3 = kda.kda_chunk_fwd_noalloc(*args, cu)
+    torch.cuda.synchronize()
+    assert torch.equal(o3, o1) and torch.equal(f3, f1)
     assert kda.device_error() == 0
