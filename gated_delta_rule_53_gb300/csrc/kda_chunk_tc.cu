@@ -28,25 +28,29 @@
 // K e^{G_C - G}, the same tile the state update uses.
 //
 // Two kernels.  Everything except the state path is independent of S0: the running sum,
-// the operand tiles, A_kk, A_qk, T, and with them the two products
-//   W = T Diag(beta) (K . e^G)     U = T Diag(beta) V           (so that V'^T = U^T - S0 W^T).
+// the operand tiles, A_kk, A_qk, T, and with them
+//   T_b = T Diag(beta)     W = T_b (K . e^G)     U = T_b V     (so that V'^T = U^T - S0 W^T).
 // chunk_prep_kernel computes them for every (chunk, head) at once (256-thread CTAs, two per
 // SM) and stores each chunk's state-path operands in the workspace, laid out exactly as the
 // state path reads them (128-byte-swizzled tiles), so that one bulk copy brings each in:
-//   B1    [W ; Q e^G]       bf16 [128][128]   B of the S0 products
-//   U     fp32 [64][128]                      V' = U - Y
+//   B1    [-W ; Q e^G]      bf16 [128][128]   B of the S0 products
+//   T_b   hi, lo            bf16 [64][64] x2  B of U^T = V^T T_b^T
 //   A_qk  hi, lo            bf16 [64][64] x2  B of O^T += V'^T A_qk^T
 //   KP    K e^{G_C - G}     bf16 [64][128]    B (MN-major) of dS = V'^T KP
 //   e^{G_C}                 fp32 [128]
+//   (v    bf16 [64][128], only when the front end runs inside the prep kernel)
 // chunk_state_kernel then walks each (sequence, head) chain in order, one CTA of 16 warps
 // per chain, with S0 (fp32) in registers: thread (r, quarter) holds row r, key channels
-// [32 quarter, 32 quarter + 32); a bf16 copy in shared memory is the A operand of the S0
-// products, so every product has M = 128 = dv and maps row r to TMEM lane r.  Per chunk the
-// serial path is one product (S0 B1^T), V' = U - Y, one product (dS) and the state update;
-// the output product and its store overlap the next chunk's first product.
+// [32 quarter, 32 quarter + 32); a bf16 copy in TMEM is the A operand of the S0 products, so
+// every product has M = 128 = dv and maps row r to TMEM lane r.  Per chunk, U^T = V^T T_b^T is
+// formed in TMEM ahead of time (v read straight from its tensor) and S0 (-W)^T is accumulated
+// onto it, which leaves V'^T in TMEM; the serial path is that one product, the hi/lo split of
+// V', one product (dS) and the state update; the output product and its store overlap the next
+// chunk's first product.
 //
 // Precision.  Products accumulate in fp32 in TMEM.  W and U come from T Diag(beta) split as
-// hi + lo in bf16 (two bf16 products each, T kept to about 16 bits); V'^T A_qk^T runs as
+// hi + lo in bf16 (two bf16 products each, T kept to about 16 bits; U - S0 W^T is summed in one
+// fp32 accumulator); V'^T A_qk^T runs as
 // three bf16 products of the hi/lo splits of both (hi hi + hi lo + lo hi); the state update
 // V'^T KP takes V' as hi + lo (two bf16 products), so the rounding of V' does not build up in
 // the state over a long chain; the other operands are bf16.  T = (I + A_kk)^-1 is computed in fp32 on the CUDA
@@ -84,13 +88,15 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // Operands of one (chunk, head) in the workspace, byte offsets (each tile in the layout its
-// reader uses; the last three are contiguous so that one copy brings them in).
-constexpr uint32_t BLOB_B1 = 0;        // [W ; Q e^G] bf16, two regions of [128][64] (128-byte swizzle)
-constexpr uint32_t BLOB_U = 32768;     // U fp32 [64][128], row-major
-constexpr uint32_t BLOB_AQ = 65536;    // A_qk as bf16 hi then lo, each [64][64] (one 128-byte-swizzled region)
-constexpr uint32_t BLOB_KP = 81920;    // K e^{G_C - G} bf16, two regions of [64][64]
-constexpr uint32_t BLOB_EGL = 98304;   // e^{G_C} fp32 [128]
-constexpr uint32_t kBlobBytes = 98816;
+// reader uses; A_qk and KP are contiguous so that one copy brings them in).
+constexpr uint32_t BLOB_B1 = 0;        // [-W ; Q e^G] bf16, two regions of [128][64] (128-byte swizzle)
+constexpr uint32_t BLOB_TB = 32768;    // T Diag(beta) as bf16 hi then lo, each [64][64] (one swizzled region)
+constexpr uint32_t BLOB_AQ = 49152;    // A_qk as bf16 hi then lo, each [64][64]
+constexpr uint32_t BLOB_KP = 65536;    // K e^{G_C - G} bf16, two regions of [64][64]
+constexpr uint32_t BLOB_EGL = 81920;   // e^{G_C} fp32 [128]
+constexpr uint32_t BLOB_V = 82944;     // fused front end only: v bf16, two regions of [64 tokens][64]
+constexpr uint32_t kBlobBytes = 82432;     // stride of the operands of one (chunk, head)
+constexpr uint32_t kBlobBytesFE = 99328;   // the same with v (fused front end)
 constexpr uint32_t kStateBytes = kD * kD * 4;
 
 
@@ -281,28 +287,28 @@ constexpr int kPrepThreads = 256;
 //   rr: k (rows 0-63) and q (rows 64-127) land here by TMA in the layout of the row operand, two
 //       regions of 16 KB, and are scaled in place; after the A products, A_kk fp32 [64][kAS]
 //   gb: g fp32, four TMA boxes of [64][32]; the running sum G in place; then K e^G (two regions of
-//       [64][64]) and V by TMA (two regions at +16 KB): one MN-major B operand of N = 256 for W and U
+//       [64][64]): the MN-major B operand (N = 128) of W
 // The next item's g lands in this item's rr once the solve has consumed A_kk, its k and q in gb once the
-// W and U products are done.
+// W product is done.
 constexpr uint32_t P_CT = 65536;      // column operands of the four row blocks stacked: 160 rows (block J from
                                       // row 16 J (J+1) / 2), two regions of 160 x 128 bytes; block 3 is K e^{G_C - G}
 constexpr uint32_t kCTRegion = 160 * 128;
 constexpr uint32_t P_BETA = P_CT + 2 * kCTRegion;  // fp32 [64]
 constexpr uint32_t P_E = P_BETA + 256;     // fp32 [4][128]: G at the last token of each 16-token block
 constexpr uint32_t P_TOT = P_E + 2048;     // fp32 [128]: sum of the first 32 tokens
-constexpr uint32_t P_BAR = P_TOT + 512;    // mbarriers: k/q, v, A products, W/U products, g
+constexpr uint32_t P_BAR = P_TOT + 512;    // mbarriers: k/q, (unused), A products, W product, g
 constexpr uint32_t P_MISC = P_BAR + 40;    // TMEM base, abort flag
 constexpr uint32_t kPrepSmem = P_MISC + 16 + 1024;
 // After the A products complete (column operands free):
 constexpr uint32_t P_TF = P_CT;                  // T fp32 [64][kAS]
 constexpr uint32_t P_NB = P_CT + 64 * kAS * 4;   // N blocks of the solve, 9 x [16][20] fp32
 constexpr uint32_t P_AQS = P_NB;                 // before them: A_qk hi, lo staged in the workspace layout (16 KB)
-// Once T is in registers: T Diag(beta) as bf16 hi and lo, A operands of 128 rows (T twice, so that one
-// product of N = 256 over [K e^G | V] leaves W in lanes 0-63 and U in lanes 64-127)
+// Once T is in registers: T Diag(beta) as bf16 hi and lo, A operands of 128 rows (T twice: the product
+// is M = 128, W lands in TMEM lanes 0-63 and again in 64-127)
 constexpr uint32_t P_TH = P_CT, P_TL = P_CT + 16384;
 constexpr uint32_t kPrepTmemCols = 256;
 // row block I of A: 16 (I + 1) columns from 16 I (I + 1) / 2 (one product of N = 160)
-// then [T ; T] [K e^G | V]: W = lanes 0-63 of columns 0-127, U = lanes 64-127 of columns 128-255
+// then [T ; T] K e^G: W = lanes 0-63 of columns 0-127
 constexpr uint32_t kKQBytes = 4 * 8192;
 constexpr uint32_t kGBytes = 4 * 8192;
 
@@ -332,7 +338,7 @@ __device__ __forceinline__ uint32_t g_off(int i, int c) {
 template <bool FE>
 __global__ void __launch_bounds__(kPrepThreads, 2)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                  const __grid_constant__ CUtensorMap tm_g,
                   const float* __restrict__ beta, const int32_t* __restrict__ cu, const int32_t* __restrict__ off,
                   int N, int64_t T_total, int H, int m0, int n_items, uint8_t* __restrict__ blobs,
                   FrontendArgs fe, unsigned int* err) {
@@ -341,12 +347,12 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t sbase = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int offN = off[N];
+    constexpr uint32_t kStride = FE ? kBlobBytesFE : kBlobBytes;
 
     float* sBeta = reinterpret_cast<float*>(sm + P_BETA);
     float* sE = reinterpret_cast<float*>(sm + P_E);
     float* sTot = reinterpret_cast<float*>(sm + P_TOT);
     uint64_t* barL = reinterpret_cast<uint64_t*>(sm + P_BAR);
-    uint64_t* barV = barL + 1;
     uint64_t* barA = barL + 2;
     uint64_t* barW = barL + 3;
     uint64_t* barG = barL + 4;
@@ -396,9 +402,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
     };
     // FE: part p of the chunk's 64 tokens, through the front end, as bf16 into a 128-byte-swizzled operand
-    // tile (two regions of `region` bytes; token i at row row0 + i).  Warp w takes tokens 8w .. 8w+7, lane
-    // the 4 channels from 4 lane.
-    auto frontend_tile = [&](int p, int h, int64_t c0, uint32_t tile, uint32_t region, int row0) {
+    // tile at `dst` (shared or global; two regions of `region` bytes; token i at row row0 + i).  Warp w
+    // takes tokens 8w .. 8w+7, lane the 4 channels from 4 lane.
+    auto frontend_tile = [&](int p, int h, int64_t c0, uint8_t* dst, uint32_t region, int row0) {
         const __nv_bfloat16* x = p == 0 ? fe.xq : (p == 1 ? fe.xk : fe.xv);
         float y[fe::kFeRun][4], ss[fe::kFeRun];
         fe::frontend_run<__nv_bfloat16>(x, fe.x_stride, fe.conv_w, cu, N, T_total, H, p, h, lane,
@@ -406,16 +412,15 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
         for (int i = 0; i < fe::kFeRun; ++i) {
             const float inv = p < 2 ? rsqrtf(ss[i] + fe.eps) : 1.0f;
-            const uint32_t at = tile + (lane >> 4) * region + sw128(row0 + fe::kFeRun * warp + i, (lane & 15) >> 1) +
+            const uint32_t at = (lane >> 4) * region + sw128(row0 + fe::kFeRun * warp + i, (lane & 15) >> 1) +
                                 (lane & 1) * 8;
-            *reinterpret_cast<uint2*>(sm + at) =
+            *reinterpret_cast<uint2*>(dst + at) =
                 make_uint2(pack_bf16x2(y[i][0] * inv, y[i][1] * inv), pack_bf16x2(y[i][2] * inv, y[i][3] * inv));
         }
     };
 
     if (tid == 0) {
         mbar_init(barL, 1);
-        mbar_init(barV, 1);
         mbar_init(barA, 1);
         mbar_init(barW, 1);
         mbar_init(barG, 1);
@@ -425,7 +430,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     if (warp == 0) tmem_alloc(sTmem, kPrepTmemCols);
     cta_sync_tc();
     const uint32_t tbase = *sTmem;
-    // thread 0: 1 = k/q loads in flight, 2 = v, 4 = A products, 8 = W/U products, 16 = g
+    // thread 0: 1 = k/q loads in flight, 4 = A products, 8 = W product, 16 = g
     uint32_t pend = 0;
 
     int item = blockIdx.x, h = 0, L = 0;
@@ -438,8 +443,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     for (uint32_t ph = 0; have; ph ^= 1u) {
         const uint32_t P_RR = ph ? 32768u : 0u, P_G = 32768u - P_RR;  // this item's two regions
-        const uint32_t P_KG = P_G, P_V = P_G + 16384, P_AKK = P_RR;
-        uint8_t* blob = blobs + (int64_t)item * kBlobBytes;
+        const uint32_t P_KG = P_G, P_AKK = P_RR;
+        uint8_t* blob = blobs + (int64_t)item * kStride;
         // the next item's place, early: its global reads complete while this item is worked on
         const int next_item = item + gridDim.x;
         int h1 = 0, L1 = 0;
@@ -450,8 +455,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             pend &= ~16u;
         }
         if (FE) {  // k and q into the row operand's space (free: the previous item's W/U products are done)
-            frontend_tile(1, h, c0, P_RR, 16384, 0);
-            frontend_tile(0, h, c0, P_RR, 16384, 64);
+            frontend_tile(1, h, c0, sm + P_RR, 16384, 0);
+            frontend_tile(0, h, c0, sm + P_RR, 16384, 64);
         }
         cp_async_wait_all();
         __syncthreads();
@@ -552,25 +557,18 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
-        // ---- the four row blocks of A; then K e^G and v take the place of the running sum
-        if (warp == 0) {  // the products are issued by warp 0 (one elected lane), the copies by thread 0
+        // ---- the four row blocks of A; then K e^G takes the place of the running sum
+        if (warp == 0) {  // the products are issued by warp 0 (one elected lane)
             tc_fence_after();
             mma_k128(tbase, kdesc(sbase + P_RR), 16384, kdesc(sbase + P_CT), kCTRegion,
                      idesc_bf16_f32(128, 160, false, false));
             mma_commit(barA);
-            if (tid == 0) pend |= FE ? 4u : 6u;
-        }
-        if (!FE) {  // v into the second half of gb (the running sum is consumed)
-            if (tid == 0) mbar_arrive_expect_tx(barV, 16384);
-            if (lane == 0 && (warp == 1 || warp == 2)) {
-                fence_proxy_async();
-                tma_load_3d(sm + P_V + (warp - 1) * 8192, &tm_v, 64 * (warp - 1), h, (int)c0, barV);
-            }
+            if (tid == 0) pend |= 4u;
         }
 #pragma unroll
         for (int I = 0; I < 4; ++I)
             *reinterpret_cast<uint4*>(sm + P_KG + reg * 8192 + sw128(r4 + 16 * I, ch)) = kg_hold[I];
-        if (FE) frontend_tile(2, h, c0, P_V, 8192, 0);  // v, while the A products run
+        if (FE) frontend_tile(2, h, c0, blob + BLOB_V, 8192, 0);  // v to the workspace, while the A products run
         fence_proxy_async();
         if (tid == 0) {
             solo_wait(barA, ph, sAbort, err);
@@ -686,6 +684,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                 *reinterpret_cast<uint4*>(sm + P_TH + at2) = hv;
                 *reinterpret_cast<uint4*>(sm + P_TL + at) = lv;
                 *reinterpret_cast<uint4*>(sm + P_TL + at2) = lv;
+                *reinterpret_cast<uint4*>(blob + BLOB_TB + at) = hv;         // the state pass's U^T = V^T T_b^T
+                *reinterpret_cast<uint4*>(blob + BLOB_TB + 8192 + at) = lv;
             }
         }
         fence_proxy_async();
@@ -699,14 +699,10 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             load_g(h1, c01, L1, P_RR);
             if (tid == 0) pend |= 16u;
         }
-        // ---- W = T Diag(beta) K e^G and U = T Diag(beta) V: [T ; T] [K e^G | V] (hi, then lo)
+        // ---- W = T Diag(beta) K e^G: [T ; T] K e^G (hi, then lo)
         if (warp == 0) {
-            if (!FE) {
-                solo_wait(barV, ph, sAbort, err);
-                pend &= ~2u;
-            }
             tc_fence_after();
-            const uint32_t id_w = idesc_bf16_f32(128, 256, false, true);
+            const uint32_t id_w = idesc_bf16_f32(128, 128, false, true);
             const uint64_t th = kdesc(sbase + P_TH), tl = kdesc(sbase + P_TL);
             const uint64_t kvd = sdesc_sw128(sbase + P_KG, 8192, 1024);
 #pragma unroll
@@ -720,56 +716,39 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         }
         cta_sync_tc();
         if (*sAbort) break;
-        // ---- the next item's k and q land in this item's gb while W and U go out
+        // ---- the next item's k and q land in this item's gb while W goes out
         if (have) {
             load_kq(h1, c01, P_G);
             if (tid == 0 && !FE) pend |= 1u;
         }
-        // W (bf16, rows 0-63 of B1) from lanes 0-63, U (fp32 rows) from lanes 64-127; warps 0-3 take the
-        // first 64 columns of their rows, warps 4-7 the last 64.  Each warp stages its rows in 4 KB of the
-        // column-operand region (free: T hi/lo are consumed) and stores them back as whole rows.
+        // -W (bf16, rows 0-63 of B1): warp w reads TMEM lanes 32 (w % 4) .. +31, i.e. rows 32 (w % 2) + lane
+        // (lanes 64-127 hold rows 0-63 again), and columns 32 (w / 2) .. +31, stages them in 2 KB of the
+        // column-operand region (free: T hi/lo are consumed; 16-byte chunks rotated by lane pair against
+        // bank conflicts) and stores them as half rows of 64 bytes.
         {
-            uint8_t* bl = blobs + (int64_t)this_item * kBlobBytes;
-            const int q = warp & 3, hf = warp >> 2;
+            uint8_t* bl = blobs + (int64_t)this_item * kStride;
+            const int q = warp & 3, cq = warp >> 1;  // lane quarter; column quarter
             const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-            uint8_t* stg = sm + P_CT + warp * 4096;
-            if (q < 2) {  // W rows 32q + lane: one 128-byte row of region hf each, in the blob's swizzle
-                uint32_t x[32], y[32];
-                tmem_ld32_async(tbase + lane_base + 64 * hf, x);
-                tmem_ld32_async(tbase + lane_base + 64 * hf + 32, y);
-                tmem_wait_ld(); reg_fence(x); reg_fence(y);
+            uint8_t* stg = sm + P_CT + warp * 2048;
+            uint32_t x[32];
+            tmem_ld32_async(tbase + lane_base + 32 * cq, x);
+            tmem_wait_ld(); reg_fence(x);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    float f[8];
+            for (int c = 0; c < 4; ++c) {
+                float f[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(c < 4 ? x[8 * c + e] : y[8 * (c - 4) + e]);
-                    *reinterpret_cast<uint4*>(stg + sw128(lane, c)) = pack8(f);
-                }
-                __syncwarp();
-                uint8_t* dst = bl + BLOB_B1 + hf * 16384 + 32 * q * 128;
+                for (int e = 0; e < 8; ++e) f[e] = -__uint_as_float(x[8 * c + e]);
+                *reinterpret_cast<uint4*>(stg + 64 * lane + 16 * (c ^ ((lane >> 1) & 3))) = pack8(f);
+            }
+            __syncwarp();
+            // row 32 (q % 2) + r of region cq / 2, 16-byte chunks 4 (cq % 2) .. +3 of it (in the row's swizzle)
+            uint8_t* dst = bl + BLOB_B1 + (cq >> 1) * 16384;
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    *reinterpret_cast<uint4*>(dst + 512 * k + 16 * lane) =
-                        *reinterpret_cast<const uint4*>(stg + 512 * k + 16 * lane);
-            } else {  // U rows 32(q-2) + lane, fp32 columns 64hf .. +63, in two passes of 32
-                uint8_t* dst = bl + BLOB_U + (32 * (q - 2)) * 512 + 256 * hf;
-#pragma unroll
-                for (int p = 0; p < 2; ++p) {
-                    uint32_t x[32];
-                    tmem_ld32_async(tbase + lane_base + 128 + 64 * hf + 32 * p, x);
-                    tmem_wait_ld(); reg_fence(x);
-                    if (p) __syncwarp();  // the first pass has been read back
-#pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(stg + sw128(lane, c)) = make_uint4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
-                    __syncwarp();
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {  // rows 4k .. 4k+3, 128 bytes each
-                        const int r = 4 * k + (lane >> 3), c = lane & 7;
-                        *reinterpret_cast<uint4*>(dst + r * 512 + 128 * p + 16 * c) =
-                            *reinterpret_cast<const uint4*>(stg + sw128(r, c));
-                    }
-                }
+            for (int k = 0; k < 4; ++k) {  // rows 8k .. 8k+7 of the warp's 32, four lanes per row
+                const int r = 8 * k + (lane >> 2), c = lane & 3;
+                const int row = 32 * (q & 1) + r;
+                *reinterpret_cast<uint4*>(dst + sw128(row, 4 * (cq & 1) + c)) =
+                    *reinterpret_cast<const uint4*>(stg + 64 * r + 16 * (c ^ ((r >> 1) & 3)));
             }
         }
         h = h1;
@@ -780,7 +759,6 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     cp_async_wait_all();
     if (*sAbort && tid == 0) {  // copies or products still in flight end before the CTA does (bounded)
         if (pend & 1u) mbar_wait(barL, 0, kWaitLimit), mbar_wait(barL, 1, kWaitLimit);
-        if (pend & 2u) mbar_wait(barV, 0, kWaitLimit), mbar_wait(barV, 1, kWaitLimit);
         if (pend & 4u) mbar_wait(barA, 0, kWaitLimit), mbar_wait(barA, 1, kWaitLimit);
         if (pend & 8u) mbar_wait(barW, 0, kWaitLimit), mbar_wait(barW, 1, kWaitLimit);
         if (pend & 16u) mbar_wait(barG, 0, kWaitLimit), mbar_wait(barG, 1, kWaitLimit);
@@ -798,28 +776,30 @@ constexpr int kThreads = kSimt + 32;     // + one warp that issues the products 
 constexpr int kMmaWarp = kSimt / 32;
 // Named barriers between the two roles (id 0 is __syncthreads), each completed by all kThreads:
 constexpr int NB_S = 1;  // SIMT -> MMA warp: bf16 state operand stored (e^{G_C} and the old B1 buffer free)
-constexpr int NB_Y = 2;  // MMA warp -> SIMT: [Y | O] of the chunk in TMEM, U in shared memory
-constexpr int NB_V = 3;  // SIMT -> MMA warp: V' hi and lo stored, U consumed
+constexpr int NB_Y = 2;  // MMA warp -> SIMT: V'^T of the chunk in TMEM
+constexpr int NB_V = 3;  // SIMT -> MMA warp: V' hi and lo stored
 constexpr int NB_D = 4;  // MMA warp -> SIMT: dS in TMEM
 constexpr int NB_O = 5;  // MMA warp -> SIMT: the chunk's output product complete
-// Copies run ahead of their use: three B1 buffers, two of U and two of A_qk/KP, each chunk's data
+// Copies run ahead of their use: three B1 buffers, two of T_b/v and two of A_qk/KP, each chunk's data
 // issued two chunks before it is needed.
-constexpr uint32_t S_B1 = 0;            // [W ; Q e^G] of three chunks, 32 KB each
-constexpr uint32_t S_U = 98304;         // U fp32 [64][128] of two chunks
+constexpr uint32_t S_B1 = 0;            // [-W ; Q e^G] of three chunks, 32 KB each
+constexpr uint32_t S_TB = 98304;        // T Diag(beta) bf16 hi, lo ([64][64] each) of two chunks
+constexpr uint32_t S_V = 131072;        // v bf16, two regions of [64 tokens][64], of two chunks
 constexpr uint32_t S_AQ = 163840;       // A_qk bf16 hi, lo (16 KB) then KP = K e^{G_C - G} bf16 (16 KB), two chunks
 constexpr uint32_t S_EGL = 229376;      // e^{G_C} fp32 [128] of three chunks (copied with that chunk's B1)
-constexpr uint32_t S_BAR = 230912;      // mbarriers: B1 x3, U x2, A_qk/KP x2, S0 products, dS, output product
+constexpr uint32_t S_BAR = 230912;      // mbarriers: B1 x3, T_b/v x2, A_qk/KP x2, S0 products, dS, output product
 constexpr uint32_t S_MISC = S_BAR + 128; // TMEM base, abort flag
 constexpr uint32_t kStateSmem = S_MISC + 16 + 1008;
 constexpr uint32_t kAQKBytes = BLOB_EGL - BLOB_AQ;
 constexpr uint32_t kKPOff = BLOB_KP - BLOB_AQ;
-// TMEM columns: S0 products of chunk parity p at 128 p (Y^T in 64 columns, then O^T in 64); dS at 256;
+// TMEM columns: products of chunk parity p at 128 p (V'^T = U^T - S0 W^T in 64 columns, then O^T in 64); dS at 256;
 // the A operands of the products, bf16 packed two per column: S0 at 384 (64 columns), V'^T hi at 448
 // and V'^T lo at 480 (32 columns each)
 constexpr uint32_t TM_DS = 256, TM_SA = 384, TM_VH = 448, TM_VL = 480;
 constexpr uint32_t kTmemCols = 512;
 
-static_assert(kKPOff % 1024 == 0 && S_AQ % 1024 == 0 && S_U % 1024 == 0 && S_EGL + 1536 <= S_BAR, "alignment");
+static_assert(kKPOff % 1024 == 0 && S_AQ % 1024 == 0 && S_TB % 1024 == 0 && S_V % 1024 == 0 &&
+                  S_V + 2 * 16384 <= S_AQ && S_EGL + 1536 <= S_BAR, "alignment");
 static_assert(kStateSmem <= 232448, "shared memory");
 
 __device__ __forceinline__ void nb_sync(int id) { asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kThreads) : "memory"); }
@@ -828,10 +808,12 @@ __device__ __forceinline__ void nb_arrive(int id) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, const int32_t* __restrict__ off,
-                   int64_t T_total, int H, float scale, const __nv_bfloat16* __restrict__ gate,
-                   __nv_bfloat16* __restrict__ o, float* final_state, const float* carry_in, float* carry_out,
-                   int first_range, int m0, int m1, const uint8_t* __restrict__ blobs, int mode, unsigned int* err) {
+chunk_state_kernel(const __grid_constant__ CUtensorMap tm_v, const float* init_state, const int32_t* __restrict__ cu,
+                   const int32_t* __restrict__ off, int64_t T_total, int H, float scale,
+                   const __nv_bfloat16* __restrict__ gate, __nv_bfloat16* __restrict__ o, float* final_state,
+                   const float* carry_in, float* carry_out, int first_range, int m0, int m1,
+                   const uint8_t* __restrict__ blobs, uint32_t blob_bytes, int v_in_blob, int mode,
+                   unsigned int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
@@ -859,7 +841,7 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
     seq_bounds(cu, n, T_total, bos, eos);
 
     uint64_t* barB = reinterpret_cast<uint64_t*>(sm + S_BAR);  // [3] B1 and e^{G_C}
-    uint64_t* barU = barB + 3;                                 // [2]
+    uint64_t* barV = barB + 3;                                 // [2] T_b and v
     uint64_t* barK = barB + 5;                                 // [2] A_qk and KP
     uint64_t* barM = barB + 7;
     uint64_t* barD = barB + 8;
@@ -881,9 +863,9 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
     float s[32];  // SIMT threads: the state, row `row`, key channels [32 qq, 32 qq + 32)
     if (warp == kMmaWarp) {
         // ======== products and copies: one warp, MMAs from an elected lane, copies from lane 0 ========
-        auto blob_of = [&](int mm) { return blobs + ((int64_t)(mm - m0) * H + h) * kBlobBytes; };
+        auto blob_of = [&](int mm) { return blobs + ((int64_t)(mm - m0) * H + h) * blob_bytes; };
         // a bit flips per copy issued, as the phase bits flip per copy consumed: B1 buffers bits 0-2,
-        // U buffers bits 3-4, A_qk/KP buffers bits 5-6
+        // T_b/v buffers bits 3-4, A_qk/KP buffers bits 5-6
         uint32_t iss = 0;
         auto load_b1 = [&](int mm, int j) {
             if (lane == 0) {
@@ -895,11 +877,20 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
             __syncwarp();
             iss ^= 1u << j;
         };
-        auto load_u = [&](int mm, int j) {
+        // T_b from the workspace; v straight from its tensor (token rows of the chunk; rows past the end of the
+        // sequence meet zero columns of T_b) or, with the fused front end, from the workspace
+        auto load_v = [&](int mm, int j) {
             if (lane == 0) {
                 fence_proxy_async();
-                mbar_arrive_expect_tx(barU + j, 32768);
-                bulk_load(sm + S_U + j * 32768, blob_of(mm) + BLOB_U, 32768, barU + j);
+                mbar_arrive_expect_tx(barV + j, 32768);
+                bulk_load(sm + S_TB + j * 16384, blob_of(mm) + BLOB_TB, 16384, barV + j);
+                if (v_in_blob) {
+                    bulk_load(sm + S_V + j * 16384, blob_of(mm) + BLOB_V, 16384, barV + j);
+                } else {
+                    const int tok = (int)(bos + (int64_t)kC * (mm - on));
+                    tma_load_3d(sm + S_V + j * 16384, &tm_v, 0, h, tok, barV + j);
+                    tma_load_3d(sm + S_V + j * 16384 + 8192, &tm_v, 64, h, tok, barV + j);
+                }
             }
             __syncwarp();
             iss ^= 8u << j;
@@ -915,18 +906,32 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
         };
         auto wait = [&](uint64_t* bar, uint32_t ph) { solo_wait(bar, ph, sAbort, err); };
         const uint32_t id_64 = idesc_bf16_f32(128, 64, false, false);
+        const uint32_t id_u = idesc_bf16_f32(128, 64, true, false);   // A = V^T (MN-major), B = T_b (K-major)
         const uint32_t id_ds = idesc_bf16_f32(128, 128, false, true);
         uint32_t ph = 0;              // bit per buffer barrier, as iss
         uint32_t phM = 0, phD = 0, phO = 0;
         for (int i = 0; i < 2 && lo + i < hi; ++i) {
             load_b1(lo + i, i);
-            if (!zero_u) load_u(lo + i, i);
+            if (!zero_u) load_v(lo + i, i);
             load_aq(lo + i, i);
         }
-        int b = 0, b3 = 0;  // TMEM [Y | O] buffer and B1 buffer of this chunk; U and A_qk/KP buffers follow b
+        int b = 0, b3 = 0;  // TMEM [V' | O] buffer and B1 buffer of this chunk; T_b/v and A_qk/KP buffers follow b
         for (int mm = lo; mm < hi; ++mm, b ^= 1, b3 = b3 == 2 ? 0 : b3 + 1) {
             const bool ahead = mm + 2 < hi;
-            // ---- Y^T = S0 W^T (the V' pass waits for it), then O^T = S0 (Q e^G)^T; A = S0 from TMEM
+            // ---- U^T = V^T T_b^T (hi, then lo) into the V' columns, while the state warps finish the previous
+            //      chunk (those columns were last read two chunks ago)
+            if (!zero_u) {
+                wait(barV + b, (ph >> (3 + b)) & 1u);
+                ph ^= 8u << b;
+                tc_fence_after();
+                const uint64_t vd = sdesc_sw128(sbase + S_V + b * 16384, 8192, 1024);
+                const uint64_t th = kdesc(sbase + S_TB + b * 16384), tl = kdesc(sbase + S_TB + b * 16384 + 8192);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) mma_bf16(tbase + 128 * b, vd + ks * 128, th + ks * 2, id_u, ks > 0 ? 1u : 0u);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) mma_bf16(tbase + 128 * b, vd + ks * 128, tl + ks * 2, id_u, 1u);
+            }
+            // ---- V'^T = U^T + S0 (-W)^T (the V' pass waits for it), then O^T = S0 (Q e^G)^T; A = S0 from TMEM
             nb_sync(NB_S);
             wait(barB + b3, (ph >> b3) & 1u);
             ph ^= 1u << b3;
@@ -935,18 +940,15 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
                 mma_bf16_ta(tbase + 128 * b, tbase + TM_SA + 8 * ks,
-                            kdesc(b1 + (ks >> 2) * 16384) + (ks & 3) * 2, id_64, ks > 0 ? 1u : 0u);
+                            kdesc(b1 + (ks >> 2) * 16384) + (ks & 3) * 2, id_64, (ks > 0 || !zero_u) ? 1u : 0u);
             mma_commit(barM);
             wait(barM, phM);
             phM ^= 1u;
-            if (!zero_u) {
-                wait(barU + b, (ph >> (3 + b)) & 1u);
-                ph ^= 8u << b;
-            }
             const bool stop = *sAbort != 0;
             tc_fence_before();
             nb_arrive(NB_Y);
             if (stop) break;
+            if (ahead && !zero_u) load_v(mm + 2, b);  // T_b and v of this chunk are consumed (U^T is complete)
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
                 mma_bf16_ta(tbase + 128 * b + 64, tbase + TM_SA + 8 * ks,
@@ -972,7 +974,6 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
             phD ^= 1u;
             tc_fence_before();
             nb_arrive(NB_D);
-            if (ahead && !zero_u) load_u(mm + 2, b);  // every thread has read this chunk's U
             const uint32_t od = tbase + 128 * b + 64;
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) mma_bf16_ta(od, tbase + TM_VH + 8 * ks, kdesc(aq) + ks * 2, id_64, 1u);
@@ -992,7 +993,7 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
             for (int j = 0; j < 3; ++j)
                 if (((iss ^ ph) >> j) & 1u) mbar_wait(barB + j, (ph >> j) & 1u, kWaitLimit);
             for (int j = 0; j < 2; ++j) {
-                if (((iss ^ ph) >> (3 + j)) & 1u) mbar_wait(barU + j, (ph >> (3 + j)) & 1u, kWaitLimit);
+                if (((iss ^ ph) >> (3 + j)) & 1u) mbar_wait(barV + j, (ph >> (3 + j)) & 1u, kWaitLimit);
                 if (((iss ^ ph) >> (5 + j)) & 1u) mbar_wait(barK + j, (ph >> (5 + j)) & 1u, kWaitLimit);
             }
         }
@@ -1050,7 +1051,6 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
         int b = 0, b3 = 0;
         bool stopped = false;
         for (int mm = lo; mm < hi; ++mm, b ^= 1, b3 = b3 == 2 ? 0 : b3 + 1) {
-            const float* sU = reinterpret_cast<const float*>(sm + S_U + b * 32768);
             tc_fence_before();
             nb_arrive(NB_S);
             if (mm > lo) {  // the previous chunk's output product is complete
@@ -1063,7 +1063,7 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
                 stopped = true;
                 break;
             }
-            // ---- V'^T = U^T - Y^T; thread (row, qq) owns tokens 16qq .. 16qq+15, stored to TMEM as bf16
+            // ---- V'^T (from TMEM); thread (row, qq) owns tokens 16qq .. 16qq+15, stored back to TMEM as bf16
             //      hi and lo (x = hi + lo to about 16 bits)
             {
                 uint32_t y[16];
@@ -1072,7 +1072,7 @@ chunk_state_kernel(const float* init_state, const int32_t* __restrict__ cu, cons
                 float hv[16], lv[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float x = (zero_u ? 0.f : sU[(16 * qq + e) * kD + row]) - __uint_as_float(y[e]);
+                    const float x = __uint_as_float(y[e]);
                     hv[e] = __bfloat162float(__float2bfloat16_rn(x));
                     lv[e] = x - hv[e];
                 }
@@ -1214,7 +1214,8 @@ struct EventSet {
 };
 
 // Workspace: [carried states, 2 x H x 128 x 128 fp32][chunk offsets, int32 N + 1][operands of
-// `rows` chunk rows x H heads, kBlobBytes each].
+// `rows` chunk rows x H heads, kBlobBytes each (kBlobBytesFE with the fused front end)].  The size
+// query counts rows of the larger blob, so one workspace serves both.
 static size_t ws_header_bytes(int N, int H) {
     return (size_t)2 * H * kStateBytes + (((size_t)(N + 1) * 4 + 1023) / 1024) * 1024;
 }
@@ -1225,7 +1226,7 @@ static int64_t max_chunk_rows(int N, int64_t T_total, bool have_cu) {
 }
 
 void chunk_tc_workspace(int N, int64_t T_total, int H, bool have_cu, size_t* full_bytes, size_t* min_bytes) {
-    const size_t row = (size_t)H * kBlobBytes, hdr = ws_header_bytes(N, H);
+    const size_t row = (size_t)H * kBlobBytesFE, hdr = ws_header_bytes(N, H);
     const int64_t rows = max_chunk_rows(N, T_total, have_cu);
     if (full_bytes) *full_bytes = hdr + row * (size_t)(rows > 0 ? rows : 1);
     if (min_bytes) *min_bytes = hdr + row;
@@ -1238,6 +1239,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
                             cudaStream_t stream, int state_mode, float* final_state2, int state_mode2,
                             bool overlap) {
     CUtensorMap tq = {}, tk = {}, tv = {}, tg;
+    const uint32_t blob_bytes = front ? kBlobBytesFE : kBlobBytes;
     if (!front && (!encode_chunk_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, T_total, H) ||
                    !encode_chunk_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, T_total, H) ||
                    !encode_chunk_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, T_total, H)))
@@ -1254,7 +1256,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
     int32_t* off = reinterpret_cast<int32_t*>(ws + (size_t)2 * H * kStateBytes);
     uint8_t* blobs = ws + ws_header_bytes(N, H);
     const int64_t rows_max = max_chunk_rows(N, T_total, cu_seqlens != nullptr);
-    int64_t rows = (int64_t)((workspace_bytes - ws_header_bytes(N, H)) / ((size_t)H * kBlobBytes));
+    int64_t rows = (int64_t)((workspace_bytes - ws_header_bytes(N, H)) / ((size_t)H * blob_bytes));
     if (rows < 1) return cudaErrorInvalidValue;
     if (rows > rows_max) rows = rows_max > 0 ? rows_max : 1;
     if (rows * H > 0x7FFFFFFF) rows = 0x7FFFFFFF / H;  // grid size of the prep kernel
@@ -1295,11 +1297,11 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
         if (e == cudaSuccess) e = cudaStreamWaitEvent(s_state, ev_start, 0);
         for (int r = 0; r < nr && e == cudaSuccess; ++r) {
             const int64_t r0 = (int64_t)r * rr, r1 = r0 + rr < rows_max ? r0 + rr : rows_max;
-            uint8_t* buf = blobs + (size_t)(r & 1) * (size_t)rr * H * kBlobBytes;
+            uint8_t* buf = blobs + (size_t)(r & 1) * (size_t)rr * H * blob_bytes;
             if (r >= 2) e = cudaStreamWaitEvent(s_prep, ev[nr + r - 2], 0);  // that half's state pass is done
             if (e != cudaSuccess) break;
             const int64_t items = (r1 - r0) * H;
-            prep<<<(unsigned)items, kPrepThreads, kPrepSmem, s_prep>>>(tq, tk, tv, tg, beta, cu_seqlens, off, N,
+            prep<<<(unsigned)items, kPrepThreads, kPrepSmem, s_prep>>>(tq, tk, tg, beta, cu_seqlens, off, N,
                                                                        T_total, H, (int)r0, (int)items, buf, fa, err);
             e = cudaGetLastError();
             if (e == cudaSuccess) e = cudaEventRecord(ev[r], s_prep);
@@ -1308,9 +1310,9 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
             float* c_out = carry + (size_t)(r & 1) * H * kD * kD;
             const float* c_in = carry + (size_t)((r + 1) & 1) * H * kD * kD;
             chunk_state_kernel<<<(unsigned)((int64_t)N * H), kThreads, kStateSmem, s_state>>>(
-                init_state, cu_seqlens, off, T_total, H, scale, static_cast<const __nv_bfloat16*>(out_gate),
+                tv, init_state, cu_seqlens, off, T_total, H, scale, static_cast<const __nv_bfloat16*>(out_gate),
                 static_cast<__nv_bfloat16*>(o), final_state, c_in, c_out, r == 0 ? 1 : 0, (int)r0, (int)r1, buf,
-                state_mode, err);
+                blob_bytes, front ? 1 : 0, state_mode, err);
             e = cudaGetLastError();
             if (e == cudaSuccess) e = cudaEventRecord(ev[nr + r], s_state);
         }
@@ -1326,18 +1328,18 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
             const int64_t items = (r1 - r0) * H;
             const int64_t grid = items < 2 * sms ? items : 2 * sms;
             prep<<<(unsigned)grid, kPrepThreads, kPrepSmem, stream>>>(
-                tq, tk, tv, tg, beta, cu_seqlens, off, N, T_total, H, (int)r0, (int)items, blobs, fa, err);
+                tq, tk, tg, beta, cu_seqlens, off, N, T_total, H, (int)r0, (int)items, blobs, fa, err);
         }
         float* c_out = carry + (size_t)(range & 1) * H * kD * kD;
         const float* c_in = carry + (size_t)((range + 1) & 1) * H * kD * kD;
         chunk_state_kernel<<<(unsigned)((int64_t)N * H), kThreads, kStateSmem, stream>>>(
-            init_state, cu_seqlens, off, T_total, H, scale, static_cast<const __nv_bfloat16*>(out_gate),
+            tv, init_state, cu_seqlens, off, T_total, H, scale, static_cast<const __nv_bfloat16*>(out_gate),
             static_cast<__nv_bfloat16*>(o), final_state, c_in, c_out, range == 0 ? 1 : 0, (int)r0, (int)r1, blobs,
-            state_mode, err);
+            blob_bytes, front ? 1 : 0, state_mode, err);
         if (final_state2)
             chunk_state_kernel<<<(unsigned)((int64_t)N * H), kThreads, kStateSmem, stream>>>(
-                nullptr, cu_seqlens, off, T_total, H, scale, nullptr, nullptr, final_state2, nullptr, nullptr, 1,
-                (int)r0, (int)r1, blobs, state_mode2, err);
+                tv, nullptr, cu_seqlens, off, T_total, H, scale, nullptr, nullptr, final_state2, nullptr, nullptr, 1,
+                (int)r0, (int)r1, blobs, blob_bytes, front ? 1 : 0, state_mode2, err);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

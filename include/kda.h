@@ -148,8 +148,9 @@ KDA_API kda_status kda_shortconv_l2norm(const void* xq, const void* xk, const vo
  * The bf16 path runs two kernels per range of chunks: the first computes, for every
  * (chunk, head) at once, everything that does not depend on the carried state (the
  * in-chunk decays, the A_kk / A_qk blocks, T = (I + A_kk)^-1, W = T diag(beta) K e^G and
- * U = T diag(beta) V) and stores the chunk's operands in the workspace (98,816 bytes per
- * chunk and head); the second walks each sequence's chunks in order with the state.
+ * T diag(beta) itself) and stores the chunk's operands in the workspace (82,432 bytes per
+ * chunk and head; 99,328 with the fused front end, which also stores v); the second walks
+ * each sequence's chunks in order with the state, forming U = T diag(beta) V from v itself.
  */
 KDA_API kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                          const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,

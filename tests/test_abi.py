@@ -60,14 +60,15 @@ def _ws(lib, N, T, H, dtype=1, cu=1):
 
 
 def test_workspace_size(lib):
-    # carried states 2 x H x 64 KiB, chunk offsets rounded to 1 KiB, 82,432 bytes per chunk and head
+    # carried states 2 x H x 64 KiB, chunk offsets rounded to 1 KiB, 99,328 bytes per chunk and head (the
+    # operands of the fused front-end path, the larger of the two layouts)
     hdr = 2 * 96 * 65536 + 1024
-    assert _ws(lib, 1, 8192, 96, cu=0) == (0, hdr + 128 * 96 * 98816, hdr + 96 * 98816)
-    assert _ws(lib, 1, 8193, 96, cu=0) == (0, hdr + 129 * 96 * 98816, hdr + 96 * 98816)
+    assert _ws(lib, 1, 8192, 96, cu=0) == (0, hdr + 128 * 96 * 99328, hdr + 96 * 99328)
+    assert _ws(lib, 1, 8193, 96, cu=0) == (0, hdr + 129 * 96 * 99328, hdr + 96 * 99328)
     # with cu_seqlens the chunk count is bounded by T / 64 + N
-    assert _ws(lib, 32, 520949, 96)[1] == hdr + (520949 // 64 + 32) * 96 * 98816
-    assert _ws(lib, 300, 1000, 4)[2] == 2 * 4 * 65536 + 2048 + 4 * 98816
-    assert _ws(lib, 1, 0, 96, cu=0)[1] == hdr + 96 * 98816
+    assert _ws(lib, 32, 520949, 96)[1] == hdr + (520949 // 64 + 32) * 96 * 99328
+    assert _ws(lib, 300, 1000, 4)[2] == 2 * 4 * 65536 + 2048 + 4 * 99328
+    assert _ws(lib, 1, 0, 96, cu=0)[1] == hdr + 96 * 99328
     assert _ws(lib, 1, 256, 4, dtype=0) == (0, 0, 0)      # the fp32 path needs none
     assert _ws(lib, 2, 256, 4, cu=0)[0] == 1               # several sequences need cu_seqlens
     assert _ws(lib, 1, 256, 4, cu=0)[0] == 0
