@@ -450,6 +450,16 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         int h1 = 0, L1 = 0;
         int64_t c01 = 0;
         const bool have_next = locate(next_item, h1, c01, L1);
+        if (FE && have_next) {  // the next item's raw rows (3 of history + 64; q, k, v; this head's 256 bytes) into L2
+            for (int i = tid; i < 3 * 67 * 2; i += kPrepThreads) {
+                const int p = i / 134, r = (i % 134) >> 1, half = i & 1;
+                const int64_t t = c01 - 3 + r;
+                if (t >= 0 && t < T_total) {
+                    const __nv_bfloat16* x = p == 0 ? fe.xq : (p == 1 ? fe.xk : fe.xv);
+                    prefetch_l2(x + t * fe.x_stride + (int64_t)h1 * kD + 64 * half);
+                }
+            }
+        }
         if (tid == 0) {
             solo_wait(barG, ph, sAbort, err);
             pend &= ~16u;
@@ -1020,6 +1030,25 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_v, const float* init_s
         // outputs of chunk mm (its product complete, in TMEM columns 128 p + 64): thread (row, qq) stores
         // tokens 16qq + 8 half .. + 7 of value row `row`; a warp writes 64 contiguous bytes per token.  The
         // two halves go out while the products of the next chunk run.
+        // The output gate of chunk mm (when given), loaded right after the previous chunk's outputs are stored
+        // and used when this chunk's are, an iteration later (the loads complete meanwhile, off the state
+        // warps' path): thread (row, qq) holds tokens 16qq .. 16qq + 15 of value row `row` as bf16 pairs
+        // (zero past the end of the sequence).  One buffer: the state warps' 96 registers hold no more.
+        uint32_t g_cur[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g_cur[j] = 0u;
+        auto load_gate = [&](int mm) {
+            const int64_t c0 = bos + (int64_t)kC * (mm - on);
+            const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
+            const int64_t stride = (int64_t)H * kD;
+            const unsigned short* gp = reinterpret_cast<const unsigned short*>(gate) + ((c0 + 16 * qq) * H + h) * kD + row;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t a = (16 * qq + 2 * j < L) ? (uint32_t)__ldcs(gp + (2 * j) * stride) : 0u;
+                const uint32_t c = (16 * qq + 2 * j + 1 < L) ? (uint32_t)__ldcs(gp + (2 * j + 1) * stride) : 0u;
+                g_cur[j] = a | (c << 16);
+            }
+        };
         auto emit_o = [&](int mm, int p, int half) {
             const int64_t c0 = bos + (int64_t)kC * (mm - on);
             const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
@@ -1031,11 +1060,11 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_v, const float* init_s
             const int64_t at0 = ((c0 + t0) * H + h) * kD + row;
             __nv_bfloat16* op = o + at0;
             if (gate) {
-                const __nv_bfloat16* gp = gate + at0;
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
                     if (t0 + e < L) {
-                        const float gv = __bfloat162float(gp[e * stride]);
+                        const uint32_t pr = half ? g_cur[4 + (e >> 1)] : g_cur[e >> 1];  // static indices
+                        const float gv = (e & 1) ? bf16_hi(pr) : bf16_lo(pr);
                         op[e * stride] = __float2bfloat16_rn(scale * __uint_as_float(xo[e]) / (1.0f + __expf(-gv)));
                     }
             } else if (L == kC) {
@@ -1092,6 +1121,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_v, const float* init_s
                 emit_o(mm - 1, b ^ 1, 0);
                 emit_o(mm - 1, b ^ 1, 1);
             }
+            if (gate && o) load_gate(mm);
             // ---- the state update
             nb_sync(NB_D);
             tc_fence_after();
@@ -1273,15 +1303,14 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
     chunk_offsets_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, T_total, off);
     // A second state pass on the same operands (final_state2, state_mode2) needs them all at once.
     if (final_state2 && rows < rows_max) return cudaErrorInvalidValue;
-    if (overlap && !front && !final_state2 && rows >= 2 * kPipeMinRows && rows_max >= 2 * kPipeMinRows) {
+    if (overlap && !final_state2 && rows >= 2 * kPipeMinRows && rows_max >= 2 * kPipeMinRows) {
         // Overlapped ranges (when the call has, and the workspace holds, at least two ranges of
         // kPipeMinRows chunk rows): the chunk rows in about kPipeRanges ranges (of at least kPipeMinRows
         // rows: each extra range costs about 35 us of wave tails and state-pass start-up), their operands
         // in two alternating halves of the workspace; range r's state pass (high-priority stream, 96 of
         // the 152 SMs for 96 chains) runs while range r+1's operands are computed on the other SMs
         // (low-priority stream, one CTA per item, so that the state pass's CTAs take SMs first as they
-        // free up).  Ordered by events only.  Not for the fused front end, whose operand kernel
-        // measured slower this way.
+        // free up).  Ordered by events only.
         int64_t rr = (rows_max + kPipeRanges - 1) / kPipeRanges;
         if (rr < kPipeMinRows) rr = kPipeMinRows;
         if (rr > rows / 2) rr = rows / 2;
