@@ -1192,8 +1192,12 @@ bool encode_chunk_map(CUtensorMap* m, const void* base, CUtensorMapDataType type
 
 }  // namespace
 
-// Overlapped ranges: about this many ranges of at least this many chunk rows.
-constexpr int64_t kPipeRanges = 8, kPipeMinRows = 64;
+// Overlapped ranges: about this many ranges of at least this many chunk rows, and (chunk, head) items per
+// operand-kernel CTA there.  Measured on one GB300 (96 heads): 8K tokens (128 rows) run fastest as one
+// range (0.842 ms against 0.863 for two overlapped ranges of 64 rows); 32K tokens (512 rows) in four
+// ranges of 128 rows with four items per CTA (3.11 ms against 3.25 for eight ranges of 64 rows and one
+// item per CTA, 3.30 for one range).
+constexpr int64_t kPipeRanges = 4, kPipeMinRows = 128, kPipeItemsPerCta = 4;
 
 // Two streams per device (created once): a low-priority one for the operand kernel and a
 // high-priority one for the state pass.
@@ -1309,8 +1313,9 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
         // rows: each extra range costs about 35 us of wave tails and state-pass start-up), their operands
         // in two alternating halves of the workspace; range r's state pass (high-priority stream, 96 of
         // the 152 SMs for 96 chains) runs while range r+1's operands are computed on the other SMs
-        // (low-priority stream, one CTA per item, so that the state pass's CTAs take SMs first as they
-        // free up).  Ordered by events only.
+        // (low-priority stream, short-lived CTAs of a few items each, so that the state pass's CTAs take SMs
+        // first as they free up, while each item still loads the next one's inputs early).  Ordered by
+        // events only.
         int64_t rr = (rows_max + kPipeRanges - 1) / kPipeRanges;
         if (rr < kPipeMinRows) rr = kPipeMinRows;
         if (rr > rows / 2) rr = rows / 2;
@@ -1330,8 +1335,9 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
             if (r >= 2) e = cudaStreamWaitEvent(s_prep, ev[nr + r - 2], 0);  // that half's state pass is done
             if (e != cudaSuccess) break;
             const int64_t items = (r1 - r0) * H;
-            prep<<<(unsigned)items, kPrepThreads, kPrepSmem, s_prep>>>(tq, tk, tg, beta, cu_seqlens, off, N,
-                                                                       T_total, H, (int)r0, (int)items, buf, fa, err);
+            const int64_t grid = (items + kPipeItemsPerCta - 1) / kPipeItemsPerCta;
+            prep<<<(unsigned)grid, kPrepThreads, kPrepSmem, s_prep>>>(tq, tk, tg, beta, cu_seqlens, off, N, T_total,
+                                                                      H, (int)r0, (int)items, buf, fa, err);
             e = cudaGetLastError();
             if (e == cudaSuccess) e = cudaEventRecord(ev[r], s_prep);
             if (e == cudaSuccess) e = cudaStreamWaitEvent(s_state, ev[r], 0);
