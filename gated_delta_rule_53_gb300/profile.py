@@ -1,12 +1,16 @@
 """Profiling harness: runs one entry point of the library on a named synthetic case a
 few times, so that a profiler can capture a handful of launches of one kernel.
 
-  python -m gated_delta_rule_53_gb300.profile {prefill_8k,prefill_2k,decode_64,decode_16,frontend_8k,gates_8k,
-                                               bwd_8k,bwd_2k} [--iters N]
+  python -m gated_delta_rule_53_gb300.profile {prefill_8k,prefill_2k,varlen_small,long_16k,decode_64,decode_16,
+                                               frontend_8k,gates_8k,bwd_8k,bwd_2k} [--iters N]
 
 Cases (all inputs larger than the 129 MB L2, a few GB on the device at most):
   prefill_8k   kda_chunk_fwd, 1 x 8192 tokens x 96 heads, bf16
   prefill_2k   kda_chunk_fwd, 1 x 2048 tokens x 96 heads, bf16
+  varlen_small kda_chunk_fwd, 4 packed sequences (1500, 3000, 2100, 2600 tokens) x 96 heads, bf16, initial
+               states N(0, 0.02): the packed path of the 32-sequence workload at about 1/57 of its tokens
+  long_16k     kda_chunk_fwd_frontend with the sigmoid output gate, 16384 tokens x 96 heads from raw bf16 rows:
+               the long workload's path at 1/16 of its tokens (one range of 256 chunk rows, overlapped)
   decode_64    kda_recurrent_step, 64 sequences x 96 heads
   decode_16    kda_recurrent_step, 16 sequences x 96 heads
   frontend_8k  kda_shortconv_l2norm, 8192 tokens x 96 heads, bf16 out
@@ -33,8 +37,8 @@ def main():
     from kda_synth.device import fill_device
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["prefill_8k", "prefill_2k", "decode_64", "decode_16", "frontend_8k", "gates_8k",
-                                     "bwd_8k", "bwd_2k"])
+    ap.add_argument("case", choices=["prefill_8k", "prefill_2k", "varlen_small", "long_16k", "decode_64", "decode_16",
+                                     "frontend_8k", "gates_8k", "bwd_8k", "bwd_2k"])
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     torch.cuda.set_device(0)
@@ -52,6 +56,26 @@ def main():
             do = fill_device(w.seed, ks.TID_DO, ks.NORMAL, (T, 96, 128), "bf16", device=dev)
             ws = torch.empty(kda.kda_chunk_bwd_workspace_size(1, T, 96), dtype=torch.uint8, device=dev)
             fn = lambda: kda.kda_chunk_bwd(q, k, v, g, b, do, workspace=ws)
+    elif args.case == "varlen_small":
+        w = ks.Workload(args.case, "prefill", 53004, H=96, lengths=[1500, 3000, 2100, 2600], init_state_std=0.02)
+        T, N = w.T, w.N
+        q = fill_device(w.seed, ks.TID_Q, ks.UNIT_GROUPS, (T, 96, 128), "bf16", 0.0, 128.0, device=dev)
+        k = fill_device(w.seed, ks.TID_K, ks.UNIT_GROUPS, (T, 96, 128), "bf16", 0.0, 128.0, device=dev)
+        v = fill_device(w.seed, ks.TID_V, ks.NORMAL, (T, 96, 128), "bf16", device=dev)
+        g = fill_device(w.seed, ks.TID_G, w.g_kind, (T, 96, 128), "f32", device=dev)
+        b = fill_device(w.seed, ks.TID_BETA, ks.SIGMOID, (T, 96), "f32", device=dev)
+        s0 = fill_device(w.seed, ks.TID_STATE, ks.NORMAL, (N, 96, 128, 128), "f32", 0.0, 0.02, device=dev)
+        cu = torch.from_numpy(w.cu_seqlens()).to(dev)
+        fn = lambda: kda.kda_chunk_fwd(q, k, v, g, b, s0, cu)
+    elif args.case == "long_16k":
+        T, C = 16384, 96 * 128
+        w = ks.Workload(args.case, "frontend", 53005, H=96, lengths=[T], g_kind=ks.NEG_SOFTPLUS5)
+        xs = [fill_device(w.seed, t, ks.NORMAL, (T, C), "bf16", device=dev) for t in (1, 2, 3)]
+        cw = fill_device(w.seed, ks.TID_CONV_W, ks.NORMAL, (3 * C, 4), "bf16", 0.0, 0.25, device=dev)
+        g = fill_device(w.seed, ks.TID_G, w.g_kind, (T, 96, 128), "f32", device=dev)
+        b = fill_device(w.seed, ks.TID_BETA, ks.SIGMOID, (T, 96), "f32", device=dev)
+        gate = fill_device(w.seed, ks.TID_GATE, ks.NORMAL, (T, C), "bf16", device=dev)
+        fn = lambda: kda.kda_chunk_fwd_frontend(*xs, cw, g, b, 96, out_gate=gate)
     elif args.case.startswith("decode"):
         N = 64 if args.case == "decode_64" else 16
         w = ks.Workload(args.case, "decode", 53003, H=96, lengths=[1] * N, init_state_std=0.02)
