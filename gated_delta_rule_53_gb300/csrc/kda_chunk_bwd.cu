@@ -43,7 +43,9 @@ constexpr int kThreads = 256;
 constexpr int kC = kChunk;    // 64
 constexpr int kD = kHeadDim;  // 128
 constexpr int kSlice = 32;
+constexpr int kSS = kSlice + 1;  // row stride of the [D][kSlice] state tiles (consecutive channels on distinct banks)
 constexpr int kUS = 36;       // row stride of [C][kSlice] tiles
+constexpr int kHC = kD / 2;   // channels of a half-width [C][kHC] tile
 constexpr int kPS = 132;      // row stride of [C][D] tiles read across rows (float4 rows on distinct banks)
 
 int64_t n_slots(int N, int64_t T_total) { return T_total / kC + N + 1; }
@@ -143,7 +145,7 @@ __device__ __forceinline__ void tile_in(float* dst, const float* src, int floats
 }
 
 // ============================ forward along the chains, keeping what the backward reads ============================
-constexpr size_t kFwdFloats = kD * kSlice + kC * kD + kC * kC + kC * kUS + kC + kD;
+constexpr size_t kFwdFloats = kD * kSS + kC * kD + kC * kC + kC * kUS + kC + kD;
 
 template <typename InT>
 __global__ void __launch_bounds__(kThreads, 3)
@@ -152,8 +154,8 @@ bwd_fwd_state_kernel(const InT* __restrict__ v, const float* __restrict__ beta, 
                      const float* __restrict__ gKr, const float* __restrict__ gT, const float* __restrict__ gGam,
                      float* __restrict__ S0s, float* __restrict__ Rb, float* __restrict__ Vp) {
     extern __shared__ float smem[];
-    float* sSt = smem;                 // [D][kSlice] sSt[c][r] = S[r0 + r][c]
-    float* sX = sSt + kD * kSlice;     // [C][D] Kg, then Kr
+    float* sSt = smem;                 // [D][kSS] sSt[c][r] = S[r0 + r][c]
+    float* sX = sSt + kD * kSS;        // [C][D] Kg, then Kr
     float* sA = sX + kC * kD;          // [C][C] T
     float* sR = sA + kC * kC;          // [C][kUS] v, then beta R, then V'
     float* sB = sR + kC * kUS;         // [C]
@@ -165,7 +167,7 @@ bwd_fwd_state_kernel(const InT* __restrict__ v, const float* __restrict__ beta, 
     seq_bounds(cu, n, T_total, bos, eos);
     for (int idx = tid; idx < kSlice * kD; idx += kThreads) {
         const int r = idx / kD, c = idx % kD;
-        sSt[c * kSlice + r] = init_state ? init_state[(int64_t)chain * kD * kD + (int64_t)(r0 + r) * kD + c] : 0.0f;
+        sSt[c * kSS + r] = init_state ? init_state[(int64_t)chain * kD * kD + (int64_t)(r0 + r) * kD + c] : 0.0f;
     }
     const int64_t nch = (eos - bos + kC - 1) / kC;
     for (int64_t ci = 0; ci < nch; ++ci) {
@@ -175,7 +177,7 @@ bwd_fwd_state_kernel(const InT* __restrict__ v, const float* __restrict__ beta, 
         __syncthreads();  // the previous chunk is done with every buffer
         for (int idx = tid; idx < kSlice * kD; idx += kThreads) {
             const int r = idx / kD, c = idx % kD;
-            S0s[(base * kD + r0 + r) * kD + c] = sSt[c * kSlice + r];
+            S0s[(base * kD + r0 + r) * kD + c] = sSt[c * kSS + r];
         }
         tile_in(sX, gKg + base * kC * kD, kC * kD, tid);
         for (int idx = tid; idx < kC * kSlice; idx += kThreads) {
@@ -190,8 +192,8 @@ bwd_fwd_state_kernel(const InT* __restrict__ v, const float* __restrict__ beta, 
         {
             float acc[8] = {};
             for (int c = 0; c < kD; c += 4) {
-                const float s0 = sSt[c * kSlice + lane], s1 = sSt[(c + 1) * kSlice + lane];
-                const float s2 = sSt[(c + 2) * kSlice + lane], s3 = sSt[(c + 3) * kSlice + lane];
+                const float s0 = sSt[c * kSS + lane], s1 = sSt[(c + 1) * kSS + lane];
+                const float s2 = sSt[(c + 2) * kSS + lane], s3 = sSt[(c + 3) * kSS + lane];
 #pragma unroll
                 for (int a = 0; a < 8; ++a) {
                     const float4 x = *reinterpret_cast<const float4*>(sX + (warp * 8 + a) * kD + c);
@@ -241,7 +243,7 @@ bwd_fwd_state_kernel(const InT* __restrict__ v, const float* __restrict__ beta, 
 #pragma unroll
             for (int a = 0; a < 16; ++a) {
                 const int c = warp * 16 + a;
-                acc[a] = sSt[c * kSlice + lane] * sGam[c];
+                acc[a] = sSt[c * kSS + lane] * sGam[c];
             }
             for (int t = 0; t < kC; ++t) {
                 const float u = sR[t * kUS + lane];
@@ -256,25 +258,35 @@ bwd_fwd_state_kernel(const InT* __restrict__ v, const float* __restrict__ beta, 
                 }
             }
 #pragma unroll
-            for (int a = 0; a < 16; ++a) sSt[(warp * 16 + a) * kSlice + lane] = acc[a];
+            for (int a = 0; a < 16; ++a) sSt[(warp * 16 + a) * kSS + lane] = acc[a];
         }
     }
 }
 
 // ============================ reverse state pass ============================
-constexpr size_t kStateFloats = kD * kSlice + kC * kD + kC * kC + 2 * kC * kUS + kC + kD;
+// Three CTAs per SM (384 CTAs for 96 chains fit one wave of 456): registers capped at 80 by the launch
+// bounds, and the [C][D] tiles staged half a row (64 channels) at a time, 69 KB of shared memory.
+constexpr size_t kStateFloats = kD * kSS + kC * kHC + kC * kC + 2 * kC * kUS + kC + kD;
+
+// [C][kHC] half-width tile: channels hc * kHC .. + kHC - 1 of a [C][D] fp32 tile, 16-byte pieces
+__device__ __forceinline__ void half_tile_in(float* dst, const float* src, int hc, int tid) {
+    for (int idx = tid; idx < kC * kHC / 4; idx += kThreads) {
+        const int i = idx / (kHC / 4), c4 = idx % (kHC / 4);
+        reinterpret_cast<float4*>(dst)[idx] = reinterpret_cast<const float4*>(src + i * kD + hc * kHC)[c4];
+    }
+}
 
 template <typename InT>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
 bwd_state_kernel(const InT* __restrict__ d_o, const float* __restrict__ beta, const float* __restrict__ d_final,
                  const int32_t* __restrict__ cu, int64_t T_total, int H, float scale, const float* __restrict__ gQg,
                  const float* __restrict__ gKg, const float* __restrict__ gKr, const float* __restrict__ gAqk,
                  const float* __restrict__ gT, const float* __restrict__ gGam, float* __restrict__ d_init,
                  float* __restrict__ dS_next, float* __restrict__ dZ_out) {
     extern __shared__ float smem[];
-    float* sDS = smem;                 // [D][kSlice] sDS[c][r] = dS[r0 + r][c]
-    float* sX = sDS + kD * kSlice;     // [C][D] Kr, then Qg, then Kg
-    float* sA = sX + kC * kD;          // [C][C] A_qk, then T
+    float* sDS = smem;                 // [D][kSS] sDS[c][r] = dS[r0 + r][c]
+    float* sX = sDS + kD * kSS;        // [C][kHC] half of Kr, Qg or Kg
+    float* sA = sX + kC * kHC;         // [C][C] A_qk, then T
     float* sDO = sA + kC * kC;         // [C][kUS] dO, slice columns
     float* sDV = sDO + kC * kUS;       // [C][kUS] dV', then beta dZ
     float* sB = sDV + kC * kUS;        // [C]
@@ -287,19 +299,22 @@ bwd_state_kernel(const InT* __restrict__ d_o, const float* __restrict__ beta, co
     const int64_t state_off = (int64_t)chain * kD * kD;
     for (int idx = tid; idx < kSlice * kD; idx += kThreads) {
         const int r = idx / kD, c = idx % kD;
-        sDS[c * kSlice + r] = d_final ? d_final[state_off + (int64_t)(r0 + r) * kD + c] : 0.0f;
+        sDS[c * kSS + r] = d_final ? d_final[state_off + (int64_t)(r0 + r) * kD + c] : 0.0f;
     }
     const int64_t nch = (eos - bos + kC - 1) / kC;
     for (int64_t ci = nch - 1; ci >= 0; --ci) {
         const int64_t c0 = bos + ci * kC;
         const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
         const int64_t base = (c0 / kC + n) * H + h;
+        const float* Kr = gKr + base * kC * kD;
+        const float* Qg = gQg + base * kC * kD;
+        const float* Kg = gKg + base * kC * kD;
         __syncthreads();  // the previous (later) chunk is done with every buffer
         for (int idx = tid; idx < kSlice * kD; idx += kThreads) {
             const int r = idx / kD, c = idx % kD;
-            dS_next[(base * kD + r0 + r) * kD + c] = sDS[c * kSlice + r];
+            dS_next[(base * kD + r0 + r) * kD + c] = sDS[c * kSS + r];
         }
-        tile_in(sX, gKr + base * kC * kD, kC * kD, tid);
+        half_tile_in(sX, Kr, 0, tid);
         tile_in(sA, gAqk + base * kC * kC, kC * kC, tid);
         for (int idx = tid; idx < kC * kSlice; idx += kThreads) {
             const int i = idx / kSlice, r = idx % kSlice;
@@ -312,15 +327,6 @@ bwd_state_kernel(const InT* __restrict__ d_o, const float* __restrict__ beta, co
         float dvp[8];
         {
             float acc[8] = {}, acc2[8] = {};
-            for (int c = 0; c < kD; c += 4) {
-                const float s0 = sDS[c * kSlice + lane], s1 = sDS[(c + 1) * kSlice + lane];
-                const float s2 = sDS[(c + 2) * kSlice + lane], s3 = sDS[(c + 3) * kSlice + lane];
-#pragma unroll
-                for (int a = 0; a < 8; ++a) {
-                    const float4 x = *reinterpret_cast<const float4*>(sX + (warp * 8 + a) * kD + c);
-                    acc[a] = fmaf(x.x, s0, fmaf(x.y, s1, fmaf(x.z, s2, fmaf(x.w, s3, acc[a]))));
-                }
-            }
             for (int s = 0; s < kC; ++s) {
                 const float x = sDO[s * kUS + lane];
                 const float4 a0 = *reinterpret_cast<const float4*>(sA + s * kC + warp * 8);
@@ -330,6 +336,24 @@ bwd_state_kernel(const InT* __restrict__ d_o, const float* __restrict__ beta, co
                 acc2[4] = fmaf(a1.x, x, acc2[4]); acc2[5] = fmaf(a1.y, x, acc2[5]);
                 acc2[6] = fmaf(a1.z, x, acc2[6]); acc2[7] = fmaf(a1.w, x, acc2[7]);
             }
+#pragma unroll 1
+            for (int hc = 0; hc < 2; ++hc) {
+                if (hc) {
+                    __syncthreads();  // the first half of Kr consumed
+                    half_tile_in(sX, Kr, 1, tid);
+                    __syncthreads();
+                }
+                for (int c = 0; c < kHC; c += 4) {
+                    const int cc = hc * kHC + c;
+                    const float s0 = sDS[cc * kSS + lane], s1 = sDS[(cc + 1) * kSS + lane];
+                    const float s2 = sDS[(cc + 2) * kSS + lane], s3 = sDS[(cc + 3) * kSS + lane];
+#pragma unroll
+                    for (int a = 0; a < 8; ++a) {
+                        const float4 x = *reinterpret_cast<const float4*>(sX + (warp * 8 + a) * kHC + c);
+                        acc[a] = fmaf(x.x, s0, fmaf(x.y, s1, fmaf(x.z, s2, fmaf(x.w, s3, acc[a]))));
+                    }
+                }
+            }
 #pragma unroll
             for (int a = 0; a < 8; ++a) dvp[a] = fmaf(scale, acc2[a], acc[a]);
         }
@@ -337,7 +361,7 @@ bwd_state_kernel(const InT* __restrict__ d_o, const float* __restrict__ beta, co
 #pragma unroll
         for (int a = 0; a < 8; ++a) sDV[(warp * 8 + a) * kUS + lane] = dvp[a];
         tile_in(sA, gT + base * kC * kC, kC * kC, tid);
-        tile_in(sX, gQg + base * kC * kD, kC * kD, tid);
+        half_tile_in(sX, Qg, 0, tid);
         __syncthreads();
         // ---- dZ = T^T dV': dZ[t][r] = sum_s T[s][t] dV'[s][r]
         float bz[8];
@@ -359,50 +383,56 @@ bwd_state_kernel(const InT* __restrict__ d_o, const float* __restrict__ beta, co
                 bz[a] = sB[t] * acc[a];
             }
         }
-        // ---- dS <- dS Diag(gamma) + scale dO^T Qg - (Diag(beta) dZ)^T Kg; lanes over r, warps over c
-        float ds[16];
-#pragma unroll
-        for (int a = 0; a < 16; ++a) {
-            const int c = warp * 16 + a;
-            ds[a] = sDS[c * kSlice + lane] * sGam[c];
-        }
-        for (int t = 0; t < kC; ++t) {
-            const float x = scale * sDO[t * kUS + lane];
-            const float4* qg = reinterpret_cast<const float4*>(sX + t * kD + warp * 16);
-#pragma unroll
-            for (int a4 = 0; a4 < 4; ++a4) {
-                const float4 qv = qg[a4];
-                ds[4 * a4 + 0] = fmaf(x, qv.x, ds[4 * a4 + 0]);
-                ds[4 * a4 + 1] = fmaf(x, qv.y, ds[4 * a4 + 1]);
-                ds[4 * a4 + 2] = fmaf(x, qv.z, ds[4 * a4 + 2]);
-                ds[4 * a4 + 3] = fmaf(x, qv.w, ds[4 * a4 + 3]);
+        // ---- dS <- dS Diag(gamma) + scale dO^T Qg - (Diag(beta) dZ)^T Kg, one half of the channels at a time;
+        //      lanes over r, warps over channels hc * 64 + 8w .. + 7
+#pragma unroll 1
+        for (int hc = 0; hc < 2; ++hc) {
+            if (hc) {
+                __syncthreads();  // Kg's first half consumed
+                half_tile_in(sX, Qg, 1, tid);
+                __syncthreads();
             }
-        }
-        __syncthreads();  // dV', T and Qg consumed
+            float ds[8];
 #pragma unroll
-        for (int a = 0; a < 8; ++a) sDV[(warp * 8 + a) * kUS + lane] = bz[a];
-        tile_in(sX, gKg + base * kC * kD, kC * kD, tid);
-        __syncthreads();
-        for (int t = 0; t < kC; ++t) {
-            const float y = sDV[t * kUS + lane];
-            const float4* kg = reinterpret_cast<const float4*>(sX + t * kD + warp * 16);
-#pragma unroll
-            for (int a4 = 0; a4 < 4; ++a4) {
-                const float4 kv = kg[a4];
-                ds[4 * a4 + 0] = fmaf(-y, kv.x, ds[4 * a4 + 0]);
-                ds[4 * a4 + 1] = fmaf(-y, kv.y, ds[4 * a4 + 1]);
-                ds[4 * a4 + 2] = fmaf(-y, kv.z, ds[4 * a4 + 2]);
-                ds[4 * a4 + 3] = fmaf(-y, kv.w, ds[4 * a4 + 3]);
+            for (int a = 0; a < 8; ++a) {
+                const int c = hc * kHC + warp * 8 + a;
+                ds[a] = sDS[c * kSS + lane] * sGam[c];
             }
-        }
+            for (int t = 0; t < kC; ++t) {
+                const float x = scale * sDO[t * kUS + lane];
+                const float4 q0 = *reinterpret_cast<const float4*>(sX + t * kHC + warp * 8);
+                const float4 q1 = *reinterpret_cast<const float4*>(sX + t * kHC + warp * 8 + 4);
+                ds[0] = fmaf(x, q0.x, ds[0]); ds[1] = fmaf(x, q0.y, ds[1]);
+                ds[2] = fmaf(x, q0.z, ds[2]); ds[3] = fmaf(x, q0.w, ds[3]);
+                ds[4] = fmaf(x, q1.x, ds[4]); ds[5] = fmaf(x, q1.y, ds[5]);
+                ds[6] = fmaf(x, q1.z, ds[6]); ds[7] = fmaf(x, q1.w, ds[7]);
+            }
+            __syncthreads();  // this half of Qg consumed (and, the first time, dV' and T)
+            if (hc == 0) {
 #pragma unroll
-        for (int a = 0; a < 16; ++a) sDS[(warp * 16 + a) * kSlice + lane] = ds[a];
+                for (int a = 0; a < 8; ++a) sDV[(warp * 8 + a) * kUS + lane] = bz[a];
+            }
+            half_tile_in(sX, Kg, hc, tid);
+            __syncthreads();
+            for (int t = 0; t < kC; ++t) {
+                const float y = sDV[t * kUS + lane];
+                const float4 k0 = *reinterpret_cast<const float4*>(sX + t * kHC + warp * 8);
+                const float4 k1 = *reinterpret_cast<const float4*>(sX + t * kHC + warp * 8 + 4);
+                ds[0] = fmaf(-y, k0.x, ds[0]); ds[1] = fmaf(-y, k0.y, ds[1]);
+                ds[2] = fmaf(-y, k0.z, ds[2]); ds[3] = fmaf(-y, k0.w, ds[3]);
+                ds[4] = fmaf(-y, k1.x, ds[4]); ds[5] = fmaf(-y, k1.y, ds[5]);
+                ds[6] = fmaf(-y, k1.z, ds[6]); ds[7] = fmaf(-y, k1.w, ds[7]);
+            }
+            // only this thread reads these channels of its row again (the other half's terms read their own)
+#pragma unroll
+            for (int a = 0; a < 8; ++a) sDS[(hc * kHC + warp * 8 + a) * kSS + lane] = ds[a];
+        }
     }
     __syncthreads();
     if (d_init) {
         for (int idx = tid; idx < kSlice * kD; idx += kThreads) {
             const int r = idx / kD, c = idx % kD;
-            d_init[state_off + (int64_t)(r0 + r) * kD + c] = sDS[c * kSlice + r];
+            d_init[state_off + (int64_t)(r0 + r) * kD + c] = sDS[c * kSS + r];
         }
     }
 }
