@@ -176,21 +176,25 @@ __device__ __noinline__ void blk_job(BlkJob j, int t) {
 // Blocks of T below the diagonal.  With D = diag(T_00 .. T_33) (inverses of the diagonal blocks of
 // I + A_kk) and N = D A_off (A_off: the blocks of A_kk below the diagonal; N is strictly block-lower,
 // so N^4 = 0):  (I + A_kk)^-1 = (I + N)^-1 D = (I - N + N^2 - N^3) D.
-// Three rounds of independent 16 x 16 products, one warp each.
+// Three rounds of independent 16 x 16 products, one warp each: round 1 (the last reader of A) here,
+// rounds 2 and 3 in t_offdiag_23.
 constexpr int kNB = 20;  // row stride of the N blocks (float4 rows, eight rows on distinct banks)
-__device__ __forceinline__ void t_offdiag(const float* A, float* T, float* nb, int tid) {
-    auto Ab = [&](int I, int J) { return A + 16 * I * kAS + 16 * J; };
-    auto Tb = [&](int I, int J) { return T + 16 * I * kAS + 16 * J; };
-    // N_IJ at nb[slot]: (1,0) 0, (2,0) 1, (3,0) 2, (2,1) 3, (3,1) 4, (3,2) 5; N^2: (2,0) 6, (3,1) 7, (3,0) 8
-    auto Nb = [&](int slot) { return nb + slot * 16 * kNB; };
+// N_IJ at nb[slot]: (1,0) 0, (2,0) 1, (3,0) 2, (2,1) 3, (3,1) 4, (3,2) 5; N^2: (2,0) 6, (3,1) 7, (3,0) 8
+__device__ __forceinline__ void t_offdiag_1(const float* A, const float* T, float* nb, int tid) {
     const int u = tid >> 5, t = tid & 31;
     BlkJob j{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, kAS, kNB, kAS, kNB, kAS, kAS, 0.f, 1.f};
     if (u < 6) {  // N blocks: (1,0) (2,0) (3,0) (2,1) (3,1) (3,2)
         const int I = u < 3 ? u + 1 : (u < 5 ? u - 1 : 3), J = u < 3 ? 0 : (u < 5 ? 1 : 2);
-        j.a0 = Tb(I, I); j.b = Ab(I, J); j.out = Nb(u); j.ldo = kNB;
+        j.a0 = T + 16 * I * kAS + 16 * I; j.b = A + 16 * I * kAS + 16 * J; j.out = nb + u * 16 * kNB; j.ldo = kNB;
         blk_job(j, t);
     }
     __syncthreads();
+}
+__device__ __forceinline__ void t_offdiag_23(float* T, float* nb, int tid) {
+    auto Tb = [&](int I, int J) { return T + 16 * I * kAS + 16 * J; };
+    auto Nb = [&](int slot) { return nb + slot * 16 * kNB; };
+    const int u = tid >> 5, t = tid & 31;
+    BlkJob j;
     if (u < 6) {
         j = BlkJob{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, kNB, kNB, kNB, kNB, kNB, kNB, 0.f, 1.f};
         switch (u) {
@@ -378,13 +382,15 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     };
     // Copies: issuing one takes its thread a few hundred cycles, so lane 0 of warps 0-3 issue one box each
     // (a box that lands before thread 0's expect_tx only makes the transaction count negative for a while).
-    // g (into region gb) and beta of an item
-    auto load_g = [&](int h, int64_t c0, int L, uint32_t gb) {
+    // g of an item (into region gb), and its beta (tokens past the chunk's end read as 0)
+    auto load_g_tma = [&](int h, int64_t c0, uint32_t gb) {
         if (tid == 0) mbar_arrive_expect_tx(barG, kGBytes);
         if (lane == 0 && warp < 4) {
             fence_proxy_async();
             tma_load_3d(sm + gb + warp * 8192, &tm_g, 32 * warp, h, (int)c0, barG);
         }
+    };
+    auto load_beta = [&](int h, int64_t c0, int L) {
         if (tid < kC) {
             const bool ok = tid < L;
             cp_async4(sBeta + tid, beta + (ok ? (c0 + tid) * H + h : 0), ok ? 4u : 0u);
@@ -437,7 +443,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     int64_t c0 = 0;
     bool have = locate(item, h, c0, L);
     if (have) {
-        load_g(h, c0, L, 32768);
+        load_g_tma(h, c0, 32768);
+        load_beta(h, c0, L);
         load_kq(h, c0, 0);
         if (tid == 0) pend |= FE ? 16u : 17u;
     }
@@ -591,52 +598,51 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // ---- A_kk (fp32 work array) and A_qk (bf16 hi and lo operands, to the workspace)
         {
             // lane quarter qt holds rows 32qt .. 32qt+31 of [k-rows ; q-rows]: lanes 0-15 belong to row block
-            // 2(qt%2) and lanes 16-31 to 2(qt%2)+1; warps 0-3 read the first block's columns, warps 4-7 the second's.
-            const int qt = warp & 3, hq = warp >> 2, Ib = 2 * (qt & 1) + hq;
-            const bool mine = ((lane >> 4) == hq);
+            // IbA = 2(qt%2), lanes 16-31 to IbA + 1; warp half hq takes columns 32hq .. 32hq+31 of each lane's own
+            // block (both blocks' columns are loaded, each lane keeps its block's), so every lane works.
+            const int qt = warp & 3, hq = warp >> 2, IbA = 2 * (qt & 1);
             const int r = 32 * qt + lane;
             const int i = r & 63;
             const bool is_k = r < 64;
+            const int Ib = IbA + (lane >> 4);
             const uint32_t lane_base = (uint32_t)(32 * qt) << 16;
-            const uint32_t col0 = 8 * Ib * (Ib + 1);
-            uint32_t a[64];
+            uint32_t a[32];
             {
                 uint32_t t0[32], t1[32];
-                tmem_ld32_async(tbase + lane_base + col0, t0);
-                tmem_ld32_async(tbase + lane_base + col0 + 32, t1);
+                tmem_ld32_async(tbase + lane_base + 8 * IbA * (IbA + 1) + 32 * hq, t0);
+                tmem_ld32_async(tbase + lane_base + 8 * (IbA + 1) * (IbA + 2) + 32 * hq, t1);
                 tmem_wait_ld(); reg_fence(t0); reg_fence(t1);
+                const bool second = lane >= 16;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) { a[e] = t0[e]; a[32 + e] = t1[e]; }
+                for (int e = 0; e < 32; ++e) a[e] = second ? t1[e] : t0[e];
             }
-            const int ncols = 16 * (Ib + 1);
-            if (mine) {
-                if (is_k) {
-                    const float b = sBeta[i];
+            const int ncols = 16 * (Ib + 1), j0 = 32 * hq;
+            if (is_k) {  // columns past the block's are never read by the solve
+                const float b = sBeta[i];
 #pragma unroll
-                    for (int j4 = 0; j4 < 16; ++j4) {
-                        float4 w;
-                        float* wp = reinterpret_cast<float*>(&w);
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    float4 w;
+                    float* wp = reinterpret_cast<float*>(&w);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int j = 4 * j4 + e;
-                            wp[e] = (j < i && j < ncols) ? b * __uint_as_float(a[j]) : 0.f;
-                        }
-                        *reinterpret_cast<float4*>(sAkk + i * kAS + 4 * j4) = w;
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = j0 + 4 * j4 + e;
+                        wp[e] = (j < i && j < ncols) ? b * __uint_as_float(a[4 * j4 + e]) : 0.f;
                     }
-                } else {
+                    *reinterpret_cast<float4*>(sAkk + i * kAS + j0 + 4 * j4) = w;
+                }
+            } else {
 #pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {  // hi and lo bf16 tiles, 8 columns per 16-byte chunk
-                        float fh[8], fl[8];
+                for (int c8 = 0; c8 < 4; ++c8) {  // hi and lo bf16 tiles, 8 columns per 16-byte chunk
+                    float fh[8], fl[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int j = 8 * c8 + e;
-                            const float x = (j <= i && j < ncols) ? __uint_as_float(a[j]) : 0.f;
-                            fh[e] = __bfloat162float(__float2bfloat16_rn(x));
-                            fl[e] = x - fh[e];
-                        }
-                        *reinterpret_cast<uint4*>(sm + P_AQS + sw128(i, c8)) = pack8(fh);
-                        *reinterpret_cast<uint4*>(sm + P_AQS + 8192 + sw128(i, c8)) = pack8(fl);
+                    for (int e = 0; e < 8; ++e) {
+                        const int j = j0 + 8 * c8 + e;
+                        const float x = (j <= i && j < ncols) ? __uint_as_float(a[8 * c8 + e]) : 0.f;
+                        fh[e] = __bfloat162float(__float2bfloat16_rn(x));
+                        fl[e] = x - fh[e];
                     }
+                    *reinterpret_cast<uint4*>(sm + P_AQS + sw128(i, 4 * hq + c8)) = pack8(fh);
+                    *reinterpret_cast<uint4*>(sm + P_AQS + 8192 + sw128(i, 4 * hq + c8)) = pack8(fl);
                 }
             }
         }
@@ -663,7 +669,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             for (int r2 = 0; r2 < 16; ++r2) sTf[(16 * I + r2) * kAS + 16 * I + cl] = x[r2];
         }
         __syncthreads();
-        t_offdiag(sAkk, sTf, reinterpret_cast<float*>(sm + P_NB), tid);
+        t_offdiag_1(sAkk, sTf, reinterpret_cast<float*>(sm + P_NB), tid);
+        // A_kk (this item's rr) is consumed: the next item's g lands there while the solve goes on
+        if (have_next) {
+            load_g_tma(h1, c01, P_RR);
+            if (tid == 0) pend |= 16u;
+        }
+        t_offdiag_23(sTf, reinterpret_cast<float*>(sm + P_NB), tid);
         // ---- T Diag(beta) = hi + lo (bf16 each): thread owns row tid / 4, columns 16 (tid % 4) ..
         {
             const int i = tid >> 2, j0 = 16 * (tid & 3);
@@ -701,14 +713,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
-        // ---- the next item's g and beta: A_kk (this item's rr) and beta are consumed
+        // ---- the next item's beta (this item's is consumed); its g is on the way since the solve
         const int this_item = item;
         item = next_item;
         have = have_next;
-        if (have) {
-            load_g(h1, c01, L1, P_RR);
-            if (tid == 0) pend |= 16u;
-        }
+        if (have) load_beta(h1, c01, L1);
         // ---- W = T Diag(beta) K e^G: [T ; T] K e^G (hi, then lo)
         if (warp == 0) {
             tc_fence_after();
