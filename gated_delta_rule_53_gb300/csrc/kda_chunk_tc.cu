@@ -1091,10 +1091,9 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_v, const float* init_s
         for (int mm = lo; mm < hi; ++mm, b ^= 1, b3 = b3 == 2 ? 0 : b3 + 1) {
             tc_fence_before();
             nb_arrive(NB_S);
-            if (mm > lo) {  // the previous chunk's output product is complete: its first half goes out while the
-                nb_sync(NB_O);  // V' product of this chunk runs, its second half while the dS product does
+            if (mm > lo) {
+                nb_sync(NB_O);
                 tc_fence_after();
-                if (o) emit_o(mm - 1, b ^ 1, 0);
             }
             nb_sync(NB_Y);
             tc_fence_after();
@@ -1127,7 +1126,10 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_v, const float* init_s
             }
             tc_fence_before();
             nb_arrive(NB_V);
-            if (mm > lo && o) emit_o(mm - 1, b ^ 1, 1);
+            if (mm > lo && o) {
+                emit_o(mm - 1, b ^ 1, 0);
+                emit_o(mm - 1, b ^ 1, 1);
+            }
             if (gate && o) load_gate(mm);
             // ---- the state update
             nb_sync(NB_D);
