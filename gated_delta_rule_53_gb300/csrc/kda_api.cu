@@ -270,9 +270,11 @@ kda_status kda_chunk_bwd(const void* q, const void* k, const void* v, const floa
     REQUIRE(workspace != nullptr && workspace_bytes >= need,
             "workspace must hold at least %zu bytes for these sizes (got %zu)", need, workspace_bytes);
     OPTIONAL_PTR(workspace);
+    unsigned int* err = kda::device_error_word();
+    if (!err) return set_error(KDA_ERR_CUDA, "device error word unavailable");
     return from_cuda(kda::launch_chunk_bwd(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, scale, dtype,
                                            d_o, d_final_state, dq, dk_out, dv_out, dg, dbeta, d_init_state,
-                                           workspace, static_cast<cudaStream_t>(stream)),
+                                           workspace, err, static_cast<cudaStream_t>(stream)),
                      "kda_chunk_bwd launch");
 }
 

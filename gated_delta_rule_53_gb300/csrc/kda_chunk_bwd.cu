@@ -25,6 +25,8 @@
 //      the state entering every chunk, R = V - Kg S0^T and V' = T Diag(beta) R;
 //   3. bwd_state_kernel: per (sequence, head, 32 value rows) the chunks in reverse, dS in shared
 //      memory (the state's rows are independent), keeping dS_next of every chunk and dZ = T^T dV';
+//      with bf16 inputs bwd_state_tc_kernel (kda_chunk_bwd_tc.cu) does this pass on the tensor cores
+//      instead, one CTA per chain, from bf16 hi/lo tiles that bwd_prep_kernel writes for it;
 //   4. bwd_chunk_a_kernel: per (chunk, head) the products with S0 and dS_next, dA_qk, dA_kk, dv and
 //      the first term of dbeta;
 //   5. bwd_chunk_b_kernel: per (chunk, head, half of the key channels) the position-pair products, dq,
@@ -33,8 +35,10 @@
 // triangular solve), small enough in shared memory for two or three CTAs per SM.
 // Chunk slot of chunk j of sequence n: (bos_n + 64 j) / 64 + n, distinct for all chunks of a batch
 // and below T_total / 64 + N + 1.
+#include "kda_bwd_tc.cuh"
 #include "kda_common.cuh"
 #include "kda_simt_blocks.cuh"
+#include "kda_tc.cuh"
 
 namespace kda {
 namespace {
@@ -69,12 +73,25 @@ __device__ bool slot_chunk(const int32_t* cu, int N, int64_t T_total, int64_t sl
 // ============================ per chunk: what does not depend on the state ============================
 constexpr size_t kPrepFloats = 3 * kC * kD + kC * kC + kC + kD;
 
+// x = hi + lo as two bf16 tiles `tile` bytes apart; 8 values into the 16-byte chunk at `at`
+__device__ __forceinline__ void store_hi_lo(uint8_t* dst, uint32_t at, uint32_t tile, const float (&x)[8]) {
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        hi[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
+        lo[j] = pack_bf16x2(x[2 * j] - bf16_lo(hi[j]), x[2 * j + 1] - bf16_hi(hi[j]));
+    }
+    *reinterpret_cast<uint4*>(dst + at) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(dst + at + tile) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+}
+
+// bb (may be null): the tensor-core reverse pass's tiles of this chunk (kda_bwd_tc.cuh)
 template <typename InT>
 __global__ void __launch_bounds__(kThreads, 2)
 bwd_prep_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const float* __restrict__ g,
                 const float* __restrict__ beta, const int32_t* __restrict__ cu, int N, int64_t T_total, int H,
-                float* __restrict__ gQg, float* __restrict__ gKg, float* __restrict__ gKr, float* __restrict__ gAqk,
-                float* __restrict__ gT, float* __restrict__ gGam) {
+                float scale, float* __restrict__ gQg, float* __restrict__ gKg, float* __restrict__ gKr,
+                float* __restrict__ gAqk, float* __restrict__ gT, float* __restrict__ gGam, uint8_t* __restrict__ bb) {
     extern __shared__ float smem[];
     float* sQ = smem;             // [C][D] q
     float* sK = sQ + kC * kD;     // [C][D] k
@@ -135,6 +152,40 @@ bwd_prep_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const floa
         gQg[base * kC * kD + idx] = sQ[idx] * gam;
         gKg[base * kC * kD + idx] = kk * gam;
         gKr[base * kC * kD + idx] = kk * expf(sGl[c] - G);
+    }
+    if (bb) {  // the same values as bf16 hi + lo tiles, in the layouts the tensor-core reverse pass reads
+        __syncthreads();  // this CTA's global writes of A_qk and T are visible to all of it
+        uint8_t* blob = bb + base * (int64_t)kBwdBlobBytes;
+        for (int idx = tid; idx < kC * kD / 8; idx += kThreads) {  // row i, channels 8 c8 .. 8 c8 + 7
+            const int i = idx >> 4, c8 = idx & 15;
+            float kr[8], qg[8], kg[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int c = 8 * c8 + e;
+                const float G = sG[i * kD + c], kk = sK[i * kD + c];
+                const float gam = expf(G);
+                qg[e] = scale * (sQ[i * kD + c] * gam);
+                kg[e] = kk * gam;
+                kr[e] = kk * expf(sGl[c] - G);
+            }
+            const uint32_t at = (uint32_t)(c8 >> 3) * 8192u + tc::sw128((uint32_t)i, (uint32_t)(c8 & 7));
+            store_hi_lo(blob + kBB_KR, at, 16384, kr);
+            store_hi_lo(blob + kBB_QG, at, 16384, qg);
+            store_hi_lo(blob + kBB_KG, at, 16384, kg);
+        }
+        for (int idx = tid; idx < kC * kC / 8; idx += kThreads) {  // row s, columns 8 t8 .. 8 t8 + 7
+            const int s8 = idx >> 3, t8 = idx & 7;
+            const float* aq = gAqk + base * kC * kC + s8 * kC + 8 * t8;
+            const float* tt = gT + base * kC * kC + s8 * kC + 8 * t8;
+            float a[8], t[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) { a[e] = scale * aq[e]; t[e] = tt[e]; }
+            const uint32_t at = tc::sw128((uint32_t)s8, (uint32_t)t8);
+            store_hi_lo(blob + kBB_AQ, at, 8192, a);
+            store_hi_lo(blob + kBB_TT, at, 8192, t);
+        }
+        if (tid < kD) reinterpret_cast<float*>(blob + kBB_GAM)[tid] = expf(sGl[tid]);
+        if (tid < kC) reinterpret_cast<float*>(blob + kBB_BETA)[tid] = sB[tid];
     }
 }
 
@@ -717,6 +768,7 @@ __global__ void bwd_dbeta_kernel(float* __restrict__ dbeta, const float* __restr
 
 struct BwdWorkspace {
     float *S0, *dSn, *R, *Vp, *dZ, *XQ, *XK, *XR, *dgam, *dAqk, *dAkk, *Qg, *Kg, *Kr, *Aqk, *T, *gam, *dbp;
+    uint8_t* tc;  // the tensor-core reverse pass's tiles, kBwdBlobBytes per (chunk slot, head)
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -738,6 +790,7 @@ size_t layout(int N, int64_t T_total, int H, uint8_t* base, BwdWorkspace* w) {
     x.dgam = take(gam); x.dAqk = take(amat); x.dAkk = take(amat);
     x.Qg = take(tile); x.Kg = take(tile); x.Kr = take(tile); x.Aqk = take(amat); x.T = take(amat); x.gam = take(gam);
     x.dbp = take(align256((size_t)2 * T_total * H * 4));
+    x.tc = reinterpret_cast<uint8_t*>(take(align256((size_t)S * H * kBwdBlobBytes)));
     if (w) *w = x;
     return off;
 }
@@ -746,9 +799,11 @@ template <typename InT>
 cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const float* g, const float* beta,
                              const float* init_state, const int32_t* cu, int N, int64_t T_total, int H, float scale,
                              kda_dtype dtype, const void* d_o, const float* d_final, float* dq, float* dk,
-                             float* dv, float* dg, float* dbeta, float* d_init, void* workspace,
+                             float* dv, float* dg, float* dbeta, float* d_init, void* workspace, unsigned int* err,
                              cudaStream_t stream) {
     BwdWorkspace w;
+    // bf16 inputs: the reverse pass on the tensor cores (dO reaches it by TMA: 32-bit token coordinates)
+    const bool tc_state = sizeof(InT) == 2 && T_total > 0 && T_total < ((int64_t)1 << 31);
     layout(N, T_total, H, static_cast<uint8_t*>(workspace), &w);
     cudaError_t e;
     const size_t smP = kPrepFloats * 4, smF = kFwdFloats * 4, smS = kStateFloats * 4, smA = kChunkAFloats * 4,
@@ -771,16 +826,21 @@ cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const 
     const dim3 grid((unsigned)n_slots(N, T_total), (unsigned)H);
     const dim3 chains((unsigned)((int64_t)N * H), kD / kSlice);
     if (T_total > 0) {
-        bwd_prep_kernel<InT><<<grid, kThreads, smP, stream>>>(qt, kt, g, beta, cu, N, T_total, H, w.Qg, w.Kg, w.Kr,
-                                                              w.Aqk, w.T, w.gam);
+        bwd_prep_kernel<InT><<<grid, kThreads, smP, stream>>>(qt, kt, g, beta, cu, N, T_total, H, scale, w.Qg, w.Kg,
+                                                              w.Kr, w.Aqk, w.T, w.gam, tc_state ? w.tc : nullptr);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         bwd_fwd_state_kernel<InT><<<chains, kThreads, smF, stream>>>(vt, beta, init_state, cu, T_total, H, w.Kg,
                                                                      w.Kr, w.T, w.gam, w.S0, w.R, w.Vp);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    bwd_state_kernel<InT><<<chains, kThreads, smS, stream>>>(ot, beta, d_final, cu, T_total, H, scale, w.Qg, w.Kg,
-                                                             w.Kr, w.Aqk, w.T, w.gam, d_init, w.dSn, w.dZ);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (tc_state) {
+        e = launch_bwd_state_tc(d_o, d_final, cu, N, T_total, H, w.tc, d_init, w.dSn, w.dZ, err, stream);
+    } else {
+        bwd_state_kernel<InT><<<chains, kThreads, smS, stream>>>(ot, beta, d_final, cu, T_total, H, scale, w.Qg, w.Kg,
+                                                                 w.Kr, w.Aqk, w.T, w.gam, d_init, w.dSn, w.dZ);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return e;
     if (T_total == 0) return cudaSuccess;
     bwd_chunk_a_kernel<InT><<<grid, kThreads, smA, stream>>>(beta, ot, cu, N, T_total, H, scale, w.S0, w.dSn, w.R,
                                                              w.Vp, w.dZ, w.XQ, w.XK, w.XR, w.dgam, w.dAqk, w.dAkk, dv,
@@ -802,12 +862,12 @@ cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const 
                              const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
                              float scale, kda_dtype dtype, const void* d_o, const float* d_final, float* dq,
                              float* dk, float* dv, float* dg, float* dbeta, float* d_init, void* workspace,
-                             cudaStream_t stream) {
+                             unsigned int* err, cudaStream_t stream) {
     if (dtype == KDA_DTYPE_F32)
         return launch_bwd_typed<float>(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, scale, dtype, d_o,
-                                       d_final, dq, dk, dv, dg, dbeta, d_init, workspace, stream);
+                                       d_final, dq, dk, dv, dg, dbeta, d_init, workspace, err, stream);
     return launch_bwd_typed<__nv_bfloat16>(q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, scale, dtype, d_o,
-                                           d_final, dq, dk, dv, dg, dbeta, d_init, workspace, stream);
+                                           d_final, dq, dk, dv, dg, dbeta, d_init, workspace, err, stream);
 }
 
 }  // namespace kda

@@ -1,0 +1,423 @@
+// The reverse pass of kda_chunk_bwd on the tcgen05 tensor cores (bf16 inputs).
+//
+// Per chunk of a (sequence, head) chain, taken from the last chunk to the first, with dS the gradient of
+// the state at the chunk's end ("Kimi-K3 深度解析", section 三, "KDA 的关键改进", unrolled over a chunk
+// as in the chunk_kda operator of "Kimi K3 架构全景", section 02; the chain rule through the chunk form):
+//   dV'^T = dS Kr^T + scale dO^T A_qk                      [dv x C]
+//   dZ^T  = dV'^T T                                        [dv x C]   (T = (I + A_kk)^-1)
+//   dS   <- dS Diag(gamma) + scale dO^T Qg - (Diag(beta) dZ)^T Kg      [dv x dk]
+// One CTA per chain: 16 warps hold dS in fp32 registers (thread (r, quarter): row r, key channels
+// 32 quarter .. +31) and do the element-wise work, one warp issues every product and copy.  Every
+// product has M = dv = 128 (row r in TMEM lane r) and keeps fp32-level accuracy: each fp32 operand is
+// split into bf16 hi + lo (x = hi + lo to about 16 bits) and the product taken as hi.hi + hi.lo + lo.hi
+// (the bf16 dO is exact and enters once).  The state-side operands (dS, dV', -beta dZ) are written to
+// TMEM by the state warps; the chunk's tiles (Kr, scale Qg, Kg, scale A_qk, T as bf16 hi/lo) come from
+// bwd_prep_kernel in the layouts the products read, and dO by TMA from its tensor.
+//
+// Outputs as the CUDA-core reverse pass: dS_next of every chunk (the gradient at the chunk's end), dZ
+// for every token, the gradient of the initial state.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "kda_bwd_tc.cuh"
+#include "kda_common.cuh"
+#include "kda_tc.cuh"
+
+namespace kda {
+namespace {
+
+using namespace tc;
+
+constexpr int kC = kChunk;    // 64
+constexpr int kD = kHeadDim;  // 128
+constexpr int kSimt = 512;
+constexpr int kThreads = kSimt + 32;
+constexpr int kMmaWarp = kSimt / 32;
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+// named barriers between the state warps and the product warp (id 0 is __syncthreads), all kThreads each
+constexpr int NB_S = 1;  // state -> products: dS hi/lo in TMEM (and the previous chunk's gamma, beta read)
+constexpr int NB_1 = 2;  // products -> state: dV'^T in TMEM
+constexpr int NB_V = 3;  // state -> products: dV' hi/lo in TMEM
+constexpr int NB_2 = 4;  // products -> state: dZ^T in TMEM
+constexpr int NB_Z = 5;  // state -> products: -beta dZ hi/lo in TMEM (beta read)
+constexpr int NB_3 = 6;  // products -> state: the dS increment in TMEM
+
+// shared memory: one buffer per tile, two for scale A_qk + dO (the first product of a chunk is issued
+// during the chunk after it)
+constexpr uint32_t R_KR = 0;            // Kr hi, lo                     [64 t][128 c] x 2
+constexpr uint32_t R_QG = 32768;        // scale Qg hi, lo               [64 t][128 c] x 2
+constexpr uint32_t R_KG = 65536;        // Kg hi, lo                     [64 t][128 c] x 2
+constexpr uint32_t R_TT = 98304;        // T hi, lo                      [64 s][64 t] x 2
+constexpr uint32_t R_AQ = 114688;       // scale A_qk hi, lo, two chunks [64 s][64 t] x 2 x 2
+constexpr uint32_t R_DO = 147456;       // dO, two chunks                [64 t][64 r] x 2 regions x 2
+constexpr uint32_t R_GAM = 180224;      // gamma fp32 [128] (with Kg)
+constexpr uint32_t R_BETA = 180736;     // beta fp32 [64] (with T)
+constexpr uint32_t R_BAR = 181248;      // mbarriers: KR, QG, KG, TT, AQ/DO x2, D1, D2, D3
+constexpr uint32_t R_MISC = R_BAR + 128;
+constexpr uint32_t kSmem = R_MISC + 16 + 1024;
+static_assert(R_AQ % 1024 == 0 && R_DO % 1024 == 0 && R_TT % 1024 == 0 && R_BAR % 8 == 0, "alignment");
+static_assert(kSmem <= 232448, "shared memory");
+
+// TMEM columns
+constexpr uint32_t TM_D1 = 0, TM_D2 = 64, TM_D3 = 128, TM_SH = 256, TM_SL = 320, TM_VH = 384, TM_VL = 416,
+                   TM_ZH = 448, TM_ZL = 480;
+
+__device__ __forceinline__ void nb_sync(int id) { asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kThreads) : "memory"); }
+__device__ __forceinline__ void nb_arrive(int id) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "n"(kThreads) : "memory");
+}
+__device__ __forceinline__ uint64_t kdesc(uint32_t saddr) { return sdesc_sw128(saddr, 16, 1024); }
+
+// x = hi + lo, both bf16 (round to nearest even), packed in pairs
+__device__ __forceinline__ void split_pairs(const float* x, int n2, uint32_t* hi, uint32_t* lo) {
+    for (int j = 0; j < n2; ++j) {
+        const float a = x[2 * j], b = x[2 * j + 1];
+        const uint32_t h = pack_bf16x2(a, b);
+        hi[j] = h;
+        lo[j] = pack_bf16x2(a - bf16_lo(h), b - bf16_hi(h));
+    }
+}
+
+template <typename InT>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ d_final,
+                    const int32_t* __restrict__ cu, int64_t T_total, int H, const uint8_t* __restrict__ blobs,
+                    float* __restrict__ d_init, float* __restrict__ dS_next, float* __restrict__ dZ_out,
+                    unsigned int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int chain = blockIdx.x, n = chain / H, h = chain % H;
+    int64_t bos, eos;
+    seq_bounds(cu, n, T_total, bos, eos);
+    const int nch = (int)((eos - bos + kC - 1) / kC);
+    const int row = tid & 127, qq = (tid >> 7) & 3;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const int64_t state_off = (int64_t)chain * kD * kD;
+
+    // copy barriers bKR + w: 0 Kr, 1 scale Qg, 2 Kg and gamma, 3 T and beta, 4 + j scale A_qk and dO (two)
+    uint64_t* bKR = reinterpret_cast<uint64_t*>(sm + R_BAR);
+    uint64_t* bAD = bKR + 4;
+    uint64_t* bD1 = bKR + 6;
+    uint64_t* bD2 = bKR + 7;
+    uint64_t* bD3 = bKR + 8;
+    uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + R_MISC);
+    volatile int* sAbort = reinterpret_cast<volatile int*>(sm + R_MISC + 4);  // a wait ran out (product warp)
+    volatile int* sStop = reinterpret_cast<volatile int*>(sm + R_MISC + 8);   // both sides stop after this chunk
+    if (tid == 0) {
+        for (int i = 0; i < 9; ++i) mbar_init(bKR + i, 1);
+        fence_mbar_init();
+        *sAbort = 0;
+        *sStop = 0;
+    }
+    if (warp == 0) tmem_alloc(sTmem, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *sTmem;
+    // chunk ci of the chain (0 = first): its slot's operands and its first token
+    auto blob_of = [&](int ci) {
+        const int64_t c0 = bos + (int64_t)kC * ci;
+        return blobs + ((c0 / kC + n) * H + h) * (int64_t)kBwdBlobBytes;
+    };
+
+    if (warp == kMmaWarp) {
+        // ======== products and copies (one warp; products from an elected lane, copies from lane 0) ========
+        auto wait = [&](uint64_t* b, uint32_t ph) {
+            if (!mbar_wait(b, ph, kWaitLimit)) {
+                *sAbort = 1;
+                raise_device_error(err, kErrMbarTimeout);
+            }
+        };
+        // phase bit per barrier, flipped when the copy it counts is consumed; `iss` flips when one is issued
+        uint32_t ph = 0, iss = 0;
+        auto copy = [&](int which, uint32_t dst, const uint8_t* src, uint32_t bytes, uint32_t dst2, const uint8_t* src2,
+                        uint32_t bytes2) {
+            if (lane == 0) {
+                fence_proxy_async();
+                mbar_arrive_expect_tx(bKR + which, bytes + bytes2);
+                bulk_load(sm + dst, src, bytes, bKR + which);
+                if (bytes2) bulk_load(sm + dst2, src2, bytes2, bKR + which);
+            }
+            __syncwarp();
+            iss ^= 1u << which;
+        };
+        auto load_kr = [&](int ci) { copy(0, R_KR, blob_of(ci) + kBB_KR, 32768, 0, nullptr, 0); };
+        auto load_qg = [&](int ci) { copy(1, R_QG, blob_of(ci) + kBB_QG, 32768, 0, nullptr, 0); };
+        auto load_kg = [&](int ci) { copy(2, R_KG, blob_of(ci) + kBB_KG, 32768, R_GAM, blob_of(ci) + kBB_GAM, 512); };
+        auto load_tt = [&](int ci) { copy(3, R_TT, blob_of(ci) + kBB_TT, 16384, R_BETA, blob_of(ci) + kBB_BETA, 256); };
+        auto load_ad = [&](int ci, int j) {  // scale A_qk from the workspace, dO by TMA from its tensor
+            if (lane == 0) {
+                fence_proxy_async();
+                mbar_arrive_expect_tx(bAD + j, 16384 + 16384);
+                bulk_load(sm + R_AQ + j * 16384, blob_of(ci) + kBB_AQ, 16384, bAD + j);
+                const int tok = (int)(bos + (int64_t)kC * ci);
+                tma_load_3d(sm + R_DO + j * 16384, &tm_do, 0, h, tok, bAD + j);
+                tma_load_3d(sm + R_DO + j * 16384 + 8192, &tm_do, 64, h, tok, bAD + j);
+            }
+            __syncwarp();
+            iss ^= 1u << (4 + j);
+        };
+        auto use = [&](int which) {
+            wait(bKR + which, (ph >> which) & 1u);
+            ph ^= 1u << which;
+        };
+        const uint32_t id_d1s = idesc_bf16_f32(128, 64, false, false);  // A = dS (TMEM), B = Kr (K-major)
+        const uint32_t id_do64 = idesc_bf16_f32(128, 64, true, true);   // A = dO^T (MN-major), B = A_qk (MN-major)
+        const uint32_t id_t = idesc_bf16_f32(128, 64, false, true);     // A = dV'^T (TMEM), B = T (MN-major)
+        const uint32_t id_do128 = idesc_bf16_f32(128, 128, true, true); // A = dO^T, B = scale Qg (MN-major)
+        const uint32_t id_z = idesc_bf16_f32(128, 128, false, true);    // A = -beta dZ^T (TMEM), B = Kg (MN-major)
+        uint32_t p1 = 0, p2 = 0, p3 = 0;
+        // D1 <- scale dO^T A_qk of chunk ci (buffer j): the part of dV' that does not depend on dS
+        auto issue_1b = [&](int j) {
+            use(4 + j);
+            tc_fence_after();
+            const uint64_t dd = sdesc_sw128(sbase + R_DO + j * 16384, 8192, 1024);
+            const uint64_t ah = sdesc_sw128(sbase + R_AQ + j * 16384, 8192, 1024);
+            const uint64_t al = sdesc_sw128(sbase + R_AQ + j * 16384 + 8192, 8192, 1024);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) mma_bf16(tbase + TM_D1, dd + ks * 128, ah + ks * 128, id_do64, ks > 0 ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) mma_bf16(tbase + TM_D1, dd + ks * 128, al + ks * 128, id_do64, 1u);
+        };
+        const int last = nch - 1;
+        if (nch > 0) {
+            load_ad(last, last & 1);
+            load_kr(last);
+            load_qg(last);
+            load_kg(last);
+            load_tt(last);
+            if (last >= 1) load_ad(last - 1, (last - 1) & 1);
+            issue_1b(last & 1);
+        }
+        for (int ci = last; ci >= 0; --ci) {
+            const int j = ci & 1;
+            const bool more = ci >= 1;
+            nb_sync(NB_S);  // dS hi/lo of this chunk in TMEM; gamma and beta of the chunk after it read
+            if (ci < last) load_kg(ci);
+            // ---- D1 += dS Kr^T (hi.hi + hi.lo + lo.hi): dV'^T
+            use(0);
+            tc_fence_after();
+            {
+                const uint32_t kh = sbase + R_KR, kl = sbase + R_KR + 16384;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16_ta(tbase + TM_D1, tbase + TM_SH + 8 * ks, kdesc(kh + (ks >> 2) * 8192) + (ks & 3) * 2, id_d1s, 1u);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16_ta(tbase + TM_D1, tbase + TM_SH + 8 * ks, kdesc(kl + (ks >> 2) * 8192) + (ks & 3) * 2, id_d1s, 1u);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16_ta(tbase + TM_D1, tbase + TM_SL + 8 * ks, kdesc(kh + (ks >> 2) * 8192) + (ks & 3) * 2, id_d1s, 1u);
+            }
+            mma_commit(bD1);
+            // ---- D3 <- scale dO^T Qg (independent of the chain): issued behind D1, before it is read
+            use(1);
+            tc_fence_after();
+            {
+                const uint64_t dd = sdesc_sw128(sbase + R_DO + j * 16384, 8192, 1024);
+                const uint64_t qh = sdesc_sw128(sbase + R_QG, 8192, 1024), ql = sdesc_sw128(sbase + R_QG + 16384, 8192, 1024);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) mma_bf16(tbase + TM_D3, dd + ks * 128, qh + ks * 128, id_do128, ks > 0 ? 1u : 0u);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) mma_bf16(tbase + TM_D3, dd + ks * 128, ql + ks * 128, id_do128, 1u);
+            }
+            wait(bD1, p1);
+            p1 ^= 1u;
+            tc_fence_before();
+            nb_arrive(NB_1);
+            if (more) load_kr(ci - 1);  // Kr consumed
+            // ---- D2 = dV'^T T (hi.hi + hi.lo + lo.hi): dZ^T
+            nb_sync(NB_V);
+            use(3);
+            tc_fence_after();
+            {
+                const uint64_t th = sdesc_sw128(sbase + R_TT, 8192, 1024), tl = sdesc_sw128(sbase + R_TT + 8192, 8192, 1024);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) mma_bf16_ta(tbase + TM_D2, tbase + TM_VH + 8 * ks, th + ks * 128, id_t, ks > 0 ? 1u : 0u);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) mma_bf16_ta(tbase + TM_D2, tbase + TM_VH + 8 * ks, tl + ks * 128, id_t, 1u);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) mma_bf16_ta(tbase + TM_D2, tbase + TM_VL + 8 * ks, th + ks * 128, id_t, 1u);
+            }
+            mma_commit(bD2);
+            wait(bD2, p2);
+            p2 ^= 1u;
+            tc_fence_before();
+            nb_arrive(NB_2);
+            if (more) load_qg(ci - 1);         // scale Qg consumed (the dO^T Qg product is complete)
+            if (ci >= 2) load_ad(ci - 2, j);   // this chunk's A_qk and dO consumed
+            // ---- D3 += (-beta dZ)^T Kg (hi.hi + hi.lo + lo.hi): the dS increment
+            nb_sync(NB_Z);  // the state warps have read this chunk's beta
+            if (more) load_tt(ci - 1);
+            use(2);
+            tc_fence_after();
+            {
+                const uint64_t gh = sdesc_sw128(sbase + R_KG, 8192, 1024), gl = sdesc_sw128(sbase + R_KG + 16384, 8192, 1024);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) mma_bf16_ta(tbase + TM_D3, tbase + TM_ZH + 8 * ks, gh + ks * 128, id_z, 1u);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) mma_bf16_ta(tbase + TM_D3, tbase + TM_ZH + 8 * ks, gl + ks * 128, id_z, 1u);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) mma_bf16_ta(tbase + TM_D3, tbase + TM_ZL + 8 * ks, gh + ks * 128, id_z, 1u);
+            }
+            mma_commit(bD3);
+            wait(bD3, p3);
+            p3 ^= 1u;
+            const bool stop = *sAbort != 0;
+            if (stop) *sStop = 1;  // written only here, read by the state warps after this hand-off
+            tc_fence_before();
+            nb_arrive(NB_3);
+            if (stop) break;
+            if (more) issue_1b(j ^ 1);  // D1 of the chunk before this one (D1 was read before NB_V)
+        }
+        if (*sAbort && lane == 0) {  // let copies still in flight land (bounded) before the CTA exits
+            for (int w = 0; w < 6; ++w)
+                if (((iss ^ ph) >> w) & 1u) mbar_wait(bKR + w, (ph >> w) & 1u, kWaitLimit);
+        }
+        __syncwarp();
+    } else {
+        // ======== the gradient of the state: thread (row, qq) holds row `row`, key channels 32 qq .. +31 ========
+        float s[32];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+            const float4 x = d_final ? *reinterpret_cast<const float4*>(d_final + state_off + (int64_t)row * kD + 32 * qq + e)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+            s[e] = x.x; s[e + 1] = x.y; s[e + 2] = x.z; s[e + 3] = x.w;
+        }
+        const float* sGam = reinterpret_cast<const float*>(sm + R_GAM);
+        const float* sBeta = reinterpret_cast<const float*>(sm + R_BETA);
+        for (int ci = nch - 1; ci >= 0; --ci) {
+            const int64_t c0 = bos + (int64_t)kC * ci;
+            const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
+            const int64_t base = (c0 / kC + n) * H + h;
+            // dS at the chunk's end, for the per-chunk kernel
+            {
+                float* dst = dS_next + (base * kD + row) * kD + 32 * qq;
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4*>(dst + e) = make_float4(s[e], s[e + 1], s[e + 2], s[e + 3]);
+            }
+            {  // dS as bf16 hi + lo, the A operand of dS Kr^T
+                uint32_t hi[16], lo[16];
+                split_pairs(s, 16, hi, lo);
+                tmem_st16(tbase + lane_base + TM_SH + 16 * qq, hi);
+                tmem_st16(tbase + lane_base + TM_SL + 16 * qq, lo);
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            nb_arrive(NB_S);
+            // ---- dV'^T: tokens 16 qq .. +15 of row `row`, back to TMEM as hi + lo
+            nb_sync(NB_1);
+            tc_fence_after();
+            {
+                uint32_t y[16];
+                tmem_ld16_async(tbase + lane_base + TM_D1 + 16 * qq, y);
+                tmem_wait_ld(); reg_fence(y);
+                float x[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) x[e] = __uint_as_float(y[e]);
+                uint32_t hi[8], lo[8];
+                split_pairs(x, 8, hi, lo);
+                tmem_st8(tbase + lane_base + TM_VH + 8 * qq, hi);
+                tmem_st8(tbase + lane_base + TM_VL + 8 * qq, lo);
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            nb_arrive(NB_V);
+            // ---- dZ^T: out for every token of the chunk; -beta dZ back to TMEM as hi + lo
+            nb_sync(NB_2);
+            tc_fence_after();
+            {
+                uint32_t y[16];
+                tmem_ld16_async(tbase + lane_base + TM_D2 + 16 * qq, y);
+                tmem_wait_ld(); reg_fence(y);
+                float z[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int t = 16 * qq + e;
+                    const float dz = __uint_as_float(y[e]);
+                    if (t < L) dZ_out[((c0 + t) * H + h) * kD + row] = dz;
+                    z[e] = -sBeta[t] * dz;
+                }
+                uint32_t hi[8], lo[8];
+                split_pairs(z, 8, hi, lo);
+                tmem_st8(tbase + lane_base + TM_ZH + 8 * qq, hi);
+                tmem_st8(tbase + lane_base + TM_ZL + 8 * qq, lo);
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            nb_arrive(NB_Z);
+            // ---- dS <- dS Diag(gamma) + increment.  A stop is taken here only, where the product warp
+            //      takes it (it reads the flag before this hand-off), so both sides leave at the same barrier.
+            nb_sync(NB_3);
+            tc_fence_after();
+            if (*sStop) break;
+            {
+                uint32_t d3[32];
+                tmem_ld32_async(tbase + lane_base + TM_D3 + 32 * qq, d3);
+                float gm[32];
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4*>(gm + e) = *reinterpret_cast<const float4*>(sGam + 32 * qq + e);
+                tmem_wait_ld(); reg_fence(d3);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s[e] = fmaf(s[e], gm[e], __uint_as_float(d3[e]));
+            }
+        }
+        if (!*sStop && d_init) {
+            float* dst = d_init + state_off + (int64_t)row * kD + 32 * qq;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(s[e], s[e + 1], s[e + 2], s[e + 3]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_state_tc(const void* d_o, const float* d_final, const int32_t* cu_seqlens, int N,
+                                int64_t T_total, int H, const void* blobs, float* d_init, float* dS_next, float* dZ,
+                                unsigned int* err, cudaStream_t stream) {
+    // dO [T, H, 128] bf16: boxes of [64 tokens][1 head][64 channels] with the 128-byte swizzle
+    auto fn = encoder();
+    if (!fn) return cudaErrorInvalidValue;
+    CUtensorMap tm;
+    const cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)(T_total > 0 ? T_total : 1)};
+    const cuuint64_t strides[2] = {(cuuint64_t)128 * 2, (cuuint64_t)H * 128 * 2};
+    const cuuint32_t box[3] = {64, 1, 64};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (fn(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(d_o), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(bwd_state_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t chains = (int64_t)N * H;
+    if (chains == 0) return cudaSuccess;
+    bwd_state_tc_kernel<__nv_bfloat16><<<(unsigned)chains, kThreads, kSmem, stream>>>(
+        tm, d_final, cu_seqlens, T_total, H, static_cast<const uint8_t*>(blobs), d_init, dS_next, dZ, err);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -97,7 +97,7 @@ cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const 
                              const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
                              float scale, kda_dtype dtype, const void* d_o, const float* d_final, float* dq,
                              float* dk, float* dv, float* dg, float* dbeta, float* d_init, void* workspace,
-                             cudaStream_t stream);
+                             unsigned int* err, cudaStream_t stream);
 
 // Raw inputs of the fused prefill: q, k, v are computed from them by the front end of
 // kda_shortconv_l2norm (bf16) inside the chunk pass instead of being read.

@@ -243,7 +243,8 @@ KDA_API kda_status kda_chunk_segment_summary(const void* q, const void* k, const
  * mode through the token-by-token recurrence; the kernels take the chain rule through the chunk form
  * (a forward pass that keeps the state entering every chunk, a reverse pass over the chunks for the
  * gradient of the state, then every (chunk, head) at once).  fp32 arithmetic on the CUDA cores with
- * explicit position-pair decays (no use of the -5 bound).
+ * explicit position-pair decays (no use of the -5 bound); with bf16 inputs the reverse pass runs on
+ * the tensor cores, every product split as bf16 hi + lo (three bf16 products) to keep fp32 accuracy.
  *
  *  q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, dk, dv, scale, chunk_size
  *                  as kda_chunk_fwd (q, k, v and d_o in storage `dtype`, F32 or BF16)
@@ -269,8 +270,8 @@ KDA_API kda_status kda_chunk_bwd(const void* q, const void* k, const void* v, co
 /*
  * Bytes of workspace kda_chunk_bwd needs for these sizes (into *bytes): the state entering each chunk
  * and the gradient leaving it (64 KB each per chunk and head), six fp32 values per token, head and
- * channel, two per token and head, and per chunk and head three 64 x 128 and four 64 x 64 fp32 tiles
- * and two vectors of 128.
+ * channel, two per token and head, and per chunk and head three 64 x 128 and four 64 x 64 fp32 tiles,
+ * two vectors of 128, and 131,840 bytes of bf16 tiles for the tensor-core reverse pass (bf16 inputs).
  */
 KDA_API kda_status kda_chunk_bwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv, int chunk_size,
                                                 size_t* bytes);

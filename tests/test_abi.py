@@ -196,9 +196,9 @@ def test_chunk_bwd_rejects_bad_arguments(lib):
     assert lib.kda_chunk_bwd_workspace_size(1, 8192, 96, 128, 128, 64, ctypes.byref(n)) == 0
     # chunk states and their gradients (2 x 130 slots x 96 heads x 64 KB), six fp32 values per token, head and
     # channel, two per token and head; per slot and head: dgamma and gamma (512 B each), four 64 x 64 matrices,
-    # three 64 x 128 tiles
+    # three 64 x 128 tiles; and per slot and head the tensor-core reverse pass's bf16 hi/lo tiles (131,840 B)
     S = 130 * 96
     assert n.value == (2 * S * 65536 + 6 * 8192 * 96 * 512 + 2 * S * 512 + 4 * S * 16384 + 3 * S * 32768 +
-                       2 * 8192 * 96 * 4)
+                       2 * 8192 * 96 * 4 + S * 131840)
     assert lib.kda_chunk_bwd_workspace_size(1, 64, 2, 64, 128, 64, ctypes.byref(n)) == 2
     assert lib.kda_chunk_bwd_workspace_size(0, 64, 2, 128, 128, 64, ctypes.byref(n)) == 1
