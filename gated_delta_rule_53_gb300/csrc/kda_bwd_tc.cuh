@@ -19,6 +19,12 @@ constexpr uint32_t kBB_GAM = 131072;    // gamma = e^{G_last}, fp32 [128]
 constexpr uint32_t kBB_BETA = 131584;   // beta, fp32 [64] (0 past the chunk's end)
 constexpr uint32_t kBwdBlobBytes = 131840;
 
+// The forward pass along the chains on the tensor cores for bf16 v (v [T_total, H, 128]): the state entering
+// every chunk, R and V'; outputs as the CUDA-core pass.
+cudaError_t launch_bwd_fwd_state_tc(const void* v, const float* init_state, const int32_t* cu_seqlens, int N,
+                                    int64_t T_total, int H, const void* blobs, float* S0s, float* R, float* Vp,
+                                    unsigned int* err, cudaStream_t stream);
+
 // The reverse pass on the tensor cores for bf16 dO (dO [T_total, H, 128]); outputs as the CUDA-core pass.
 cudaError_t launch_bwd_state_tc(const void* d_o, const float* d_final, const int32_t* cu_seqlens, int N,
                                 int64_t T_total, int H, const void* blobs, float* d_init, float* dS_next, float* dZ,

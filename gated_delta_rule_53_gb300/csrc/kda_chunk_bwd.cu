@@ -25,8 +25,9 @@
 //      the state entering every chunk, R = V - Kg S0^T and V' = T Diag(beta) R;
 //   3. bwd_state_kernel: per (sequence, head, 32 value rows) the chunks in reverse, dS in shared
 //      memory (the state's rows are independent), keeping dS_next of every chunk and dZ = T^T dV';
-//      with bf16 inputs bwd_state_tc_kernel (kda_chunk_bwd_tc.cu) does this pass on the tensor cores
-//      instead, one CTA per chain, from bf16 hi/lo tiles that bwd_prep_kernel writes for it;
+//      with bf16 inputs bwd_fwd_state_tc_kernel and bwd_state_tc_kernel (kda_chunk_bwd_tc.cu) do passes 2
+//      and 3 on the tensor cores instead, one CTA per chain, from bf16 hi/lo tiles that bwd_prep_kernel
+//      writes for them;
 //   4. bwd_chunk_a_kernel: per (chunk, head) the products with S0 and dS_next, dA_qk, dA_kk, dv and
 //      the first term of dbeta;
 //   5. bwd_chunk_b_kernel: per (chunk, head, half of the key channels) the position-pair products, dq,
@@ -829,9 +830,14 @@ cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const 
         bwd_prep_kernel<InT><<<grid, kThreads, smP, stream>>>(qt, kt, g, beta, cu, N, T_total, H, scale, w.Qg, w.Kg,
                                                               w.Kr, w.Aqk, w.T, w.gam, tc_state ? w.tc : nullptr);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        bwd_fwd_state_kernel<InT><<<chains, kThreads, smF, stream>>>(vt, beta, init_state, cu, T_total, H, w.Kg,
-                                                                     w.Kr, w.T, w.gam, w.S0, w.R, w.Vp);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (tc_state) {
+            e = launch_bwd_fwd_state_tc(v, init_state, cu, N, T_total, H, w.tc, w.S0, w.R, w.Vp, err, stream);
+        } else {
+            bwd_fwd_state_kernel<InT><<<chains, kThreads, smF, stream>>>(vt, beta, init_state, cu, T_total, H, w.Kg,
+                                                                         w.Kr, w.T, w.gam, w.S0, w.R, w.Vp);
+            e = cudaGetLastError();
+        }
+        if (e != cudaSuccess) return e;
     }
     if (tc_state) {
         e = launch_bwd_state_tc(d_o, d_final, cu, N, T_total, H, w.tc, d_init, w.dSn, w.dZ, err, stream);

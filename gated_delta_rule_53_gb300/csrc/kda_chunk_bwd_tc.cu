@@ -1,4 +1,4 @@
-// The reverse pass of kda_chunk_bwd on the tcgen05 tensor cores (bf16 inputs).
+// The two passes of kda_chunk_bwd along the chains on the tcgen05 tensor cores (bf16 inputs).
 //
 // Per chunk of a (sequence, head) chain, taken from the last chunk to the first, with dS the gradient of
 // the state at the chunk's end ("Kimi-K3 深度解析", section 三, "KDA 的关键改进", unrolled over a chunk
@@ -15,7 +15,8 @@
 // bwd_prep_kernel in the layouts the products read, and dO by TMA from its tensor.
 //
 // Outputs as the CUDA-core reverse pass: dS_next of every chunk (the gradient at the chunk's end), dZ
-// for every token, the gradient of the initial state.
+// for every token, the gradient of the initial state.  The forward pass along the chains that the
+// backward recomputes first (the state entering every chunk, R and V') runs the same way, below.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -380,6 +381,288 @@ bwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const float* __re
     if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
+// ============================ the forward pass along the chains ============================
+// Per chunk, from the chain's initial state S0, the values the per-chunk gradient kernels read:
+//   R^T  = V^T - S0 Kg^T            (kept, fp32)
+//   V'^T = (Diag(beta) R)^T T^T     (kept, fp32; V' = T Diag(beta) R)
+//   S   <- S0 Diag(gamma) + V'^T Kr  (S0 of every chunk kept, fp32)
+// The same structure as the reverse pass: 16 state warps hold S in fp32 registers, one warp issues the
+// products (bf16 hi.hi + hi.lo + lo.hi) and copies; v arrives by TMA from its tensor.
+constexpr uint32_t F_KG = 0;          // Kg hi, lo      [64 t][128 c] x 2 (K-major B of S Kg^T)
+constexpr uint32_t F_KR = 32768;      // Kr hi, lo      [64 t][128 c] x 2 (MN-major B of V'^T Kr)
+constexpr uint32_t F_TT = 65536;      // T hi, lo       [64][64] x 2 (K-major B of (beta R)^T T^T)
+constexpr uint32_t F_V = 81920;       // v              [64 t][64 r] x 2 regions
+constexpr uint32_t F_GAM = 98304;     // gamma fp32 [128] (with Kr)
+constexpr uint32_t F_BETA = 98816;    // beta fp32 [64] (with T)
+constexpr uint32_t F_BAR = 99328;     // mbarriers: KG, KR, TT, V, D1, D2, D3
+constexpr uint32_t F_MISC = F_BAR + 64;
+constexpr uint32_t kFwdSmem = F_MISC + 16 + 1024;
+static_assert(F_V % 1024 == 0 && F_TT % 1024 == 0 && F_BAR % 8 == 0, "alignment");
+
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const float* __restrict__ init_state,
+                        const int32_t* __restrict__ cu, int64_t T_total, int H, const uint8_t* __restrict__ blobs,
+                        float* __restrict__ S0s, float* __restrict__ Rb, float* __restrict__ Vp, unsigned int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int chain = blockIdx.x, n = chain / H, h = chain % H;
+    int64_t bos, eos;
+    seq_bounds(cu, n, T_total, bos, eos);
+    const int nch = (int)((eos - bos + kC - 1) / kC);
+    const int row = tid & 127, qq = (tid >> 7) & 3;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    // copy barriers bB + w: 0 Kg, 1 Kr and gamma, 2 T and beta, 3 v; then the three product barriers
+    uint64_t* bB = reinterpret_cast<uint64_t*>(sm + F_BAR);
+    uint64_t* bD1 = bB + 4;
+    uint64_t* bD2 = bB + 5;
+    uint64_t* bD3 = bB + 6;
+    uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + F_MISC);
+    volatile int* sAbort = reinterpret_cast<volatile int*>(sm + F_MISC + 4);
+    volatile int* sStop = reinterpret_cast<volatile int*>(sm + F_MISC + 8);
+    if (tid == 0) {
+        for (int i = 0; i < 7; ++i) mbar_init(bB + i, 1);
+        fence_mbar_init();
+        *sAbort = 0;
+        *sStop = 0;
+    }
+    if (warp == 0) tmem_alloc(sTmem, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *sTmem;
+    auto blob_of = [&](int ci) {
+        const int64_t c0 = bos + (int64_t)kC * ci;
+        return blobs + ((c0 / kC + n) * H + h) * (int64_t)kBwdBlobBytes;
+    };
+    // TMEM: D1 = S Kg^T, D2 = V'^T, D3 = the state increment; S, beta R and V' as bf16 hi/lo
+    constexpr uint32_t F_D1 = 0, F_D2 = 64, F_D3 = 128, F_SH = 256, F_SL = 320, F_RH = 384, F_RL = 416,
+                       F_VH = 448, F_VL = 480;
+
+    if (warp == kMmaWarp) {
+        auto wait = [&](uint64_t* b, uint32_t ph) {
+            if (!mbar_wait(b, ph, kWaitLimit)) {
+                *sAbort = 1;
+                raise_device_error(err, kErrMbarTimeout);
+            }
+        };
+        uint32_t ph = 0, iss = 0;
+        auto copy = [&](int which, uint32_t dst, const uint8_t* src, uint32_t bytes, uint32_t dst2, const uint8_t* src2,
+                        uint32_t bytes2) {
+            if (lane == 0) {
+                fence_proxy_async();
+                mbar_arrive_expect_tx(bB + which, bytes + bytes2);
+                bulk_load(sm + dst, src, bytes, bB + which);
+                if (bytes2) bulk_load(sm + dst2, src2, bytes2, bB + which);
+            }
+            __syncwarp();
+            iss ^= 1u << which;
+        };
+        auto load_kg = [&](int ci) { copy(0, F_KG, blob_of(ci) + kBB_KG, 32768, 0, nullptr, 0); };
+        auto load_kr = [&](int ci) { copy(1, F_KR, blob_of(ci) + kBB_KR, 32768, F_GAM, blob_of(ci) + kBB_GAM, 512); };
+        auto load_tt = [&](int ci) { copy(2, F_TT, blob_of(ci) + kBB_TT, 16384, F_BETA, blob_of(ci) + kBB_BETA, 256); };
+        auto load_v = [&](int ci) {
+            if (lane == 0) {
+                fence_proxy_async();
+                mbar_arrive_expect_tx(bB + 3, 16384);
+                const int tok = (int)(bos + (int64_t)kC * ci);
+                tma_load_3d(sm + F_V, &tm_v, 0, h, tok, bB + 3);
+                tma_load_3d(sm + F_V + 8192, &tm_v, 64, h, tok, bB + 3);
+            }
+            __syncwarp();
+            iss ^= 1u << 3;
+        };
+        auto use = [&](int which) {
+            wait(bB + which, (ph >> which) & 1u);
+            ph ^= 1u << which;
+        };
+        const uint32_t id_kg = idesc_bf16_f32(128, 64, false, false);   // A = S (TMEM), B = Kg (K-major)
+        const uint32_t id_tt = idesc_bf16_f32(128, 64, false, false);   // A = (beta R)^T (TMEM), B = T (K-major)
+        const uint32_t id_kr = idesc_bf16_f32(128, 128, false, true);   // A = V'^T (TMEM), B = Kr (MN-major)
+        uint32_t p1 = 0, p2 = 0, p3 = 0;
+        if (nch > 0) {
+            load_kg(0);
+            load_v(0);
+            load_tt(0);
+            load_kr(0);
+        }
+        for (int ci = 0; ci < nch; ++ci) {
+            const bool more = ci + 1 < nch;
+            nb_sync(NB_S);  // S hi/lo in TMEM; gamma of the chunk before read
+            if (ci > 0) load_kr(ci);
+            // ---- D1 = S Kg^T (hi.hi + hi.lo + lo.hi)
+            use(0);
+            tc_fence_after();
+            {
+                const uint32_t kh = sbase + F_KG, kl = sbase + F_KG + 16384;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16_ta(tbase + F_D1, tbase + F_SH + 8 * ks, kdesc(kh + (ks >> 2) * 8192) + (ks & 3) * 2, id_kg, ks > 0 ? 1u : 0u);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16_ta(tbase + F_D1, tbase + F_SH + 8 * ks, kdesc(kl + (ks >> 2) * 8192) + (ks & 3) * 2, id_kg, 1u);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    mma_bf16_ta(tbase + F_D1, tbase + F_SL + 8 * ks, kdesc(kh + (ks >> 2) * 8192) + (ks & 3) * 2, id_kg, 1u);
+            }
+            mma_commit(bD1);
+            use(3);  // v, read by the state warps after the next hand-off
+            use(2);  // T and beta (beta read by the state warps)
+            wait(bD1, p1);
+            p1 ^= 1u;
+            tc_fence_before();
+            nb_arrive(NB_1);
+            if (more) load_kg(ci + 1);  // Kg consumed
+            // ---- D2 = (beta R)^T T^T (hi.hi + hi.lo + lo.hi) = V'^T
+            nb_sync(NB_V);  // beta R hi/lo in TMEM; v and beta read
+            if (more) load_v(ci + 1);
+            tc_fence_after();
+            {
+                const uint32_t th = sbase + F_TT, tl = sbase + F_TT + 8192;
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) mma_bf16_ta(tbase + F_D2, tbase + F_RH + 8 * ks, kdesc(th) + ks * 2, id_tt, ks > 0 ? 1u : 0u);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) mma_bf16_ta(tbase + F_D2, tbase + F_RH + 8 * ks, kdesc(tl) + ks * 2, id_tt, 1u);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) mma_bf16_ta(tbase + F_D2, tbase + F_RL + 8 * ks, kdesc(th) + ks * 2, id_tt, 1u);
+            }
+            mma_commit(bD2);
+            wait(bD2, p2);
+            p2 ^= 1u;
+            tc_fence_before();
+            nb_arrive(NB_2);
+            if (more) load_tt(ci + 1);  // T consumed, beta read before NB_V
+            // ---- D3 = V'^T Kr (hi.hi + hi.lo + lo.hi)
+            nb_sync(NB_Z);  // V' hi/lo in TMEM
+            use(1);
+            tc_fence_after();
+            {
+                const uint64_t rh = sdesc_sw128(sbase + F_KR, 8192, 1024), rl = sdesc_sw128(sbase + F_KR + 16384, 8192, 1024);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) mma_bf16_ta(tbase + F_D3, tbase + F_VH + 8 * ks, rh + ks * 128, id_kr, ks > 0 ? 1u : 0u);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) mma_bf16_ta(tbase + F_D3, tbase + F_VH + 8 * ks, rl + ks * 128, id_kr, 1u);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) mma_bf16_ta(tbase + F_D3, tbase + F_VL + 8 * ks, rh + ks * 128, id_kr, 1u);
+            }
+            mma_commit(bD3);
+            wait(bD3, p3);
+            p3 ^= 1u;
+            const bool stop = *sAbort != 0;
+            if (stop) *sStop = 1;
+            tc_fence_before();
+            nb_arrive(NB_3);
+            if (stop) break;
+        }
+        if (*sAbort && lane == 0) {
+            for (int w = 0; w < 4; ++w)
+                if (((iss ^ ph) >> w) & 1u) mbar_wait(bB + w, (ph >> w) & 1u, kWaitLimit);
+        }
+        __syncwarp();
+    } else {
+        float s[32];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+            const float4 x = init_state ? *reinterpret_cast<const float4*>(init_state + (int64_t)chain * kD * kD +
+                                                                            (int64_t)row * kD + 32 * qq + e)
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+            s[e] = x.x; s[e + 1] = x.y; s[e + 2] = x.z; s[e + 3] = x.w;
+        }
+        const float* sGam = reinterpret_cast<const float*>(sm + F_GAM);
+        const float* sBeta = reinterpret_cast<const float*>(sm + F_BETA);
+        for (int ci = 0; ci < nch; ++ci) {
+            const int64_t c0 = bos + (int64_t)kC * ci;
+            const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
+            const int64_t base = (c0 / kC + n) * H + h;
+            {  // the state entering the chunk
+                float* dst = S0s + (base * kD + row) * kD + 32 * qq;
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4*>(dst + e) = make_float4(s[e], s[e + 1], s[e + 2], s[e + 3]);
+                uint32_t hi[16], lo[16];
+                split_pairs(s, 16, hi, lo);
+                tmem_st16(tbase + lane_base + F_SH + 16 * qq, hi);
+                tmem_st16(tbase + lane_base + F_SL + 16 * qq, lo);
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            nb_arrive(NB_S);
+            // ---- R = V - Kg S^T (kept), beta R to TMEM as hi + lo
+            nb_sync(NB_1);
+            tc_fence_after();
+            {
+                // v[t][row] of the chunk's tokens 16 qq .. +15 (the TMA tile: [64 t][64 r] per half of the rows)
+                const uint8_t* vt = sm + F_V + (row >> 6) * 8192;
+                float x[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int t = 16 * qq + e;
+                    const uint32_t at = sw128((uint32_t)t, (uint32_t)((row & 63) >> 3)) + (uint32_t)(row & 7) * 2u;
+                    x[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(vt + at));
+                }
+                uint32_t y[16];
+                tmem_ld16_async(tbase + lane_base + F_D1 + 16 * qq, y);
+                tmem_wait_ld(); reg_fence(y);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int t = 16 * qq + e;
+                    const float r = x[e] - __uint_as_float(y[e]);
+                    if (t < L) Rb[((c0 + t) * H + h) * kD + row] = r;
+                    x[e] = sBeta[t] * r;
+                }
+                uint32_t hi[8], lo[8];
+                split_pairs(x, 8, hi, lo);
+                tmem_st8(tbase + lane_base + F_RH + 8 * qq, hi);
+                tmem_st8(tbase + lane_base + F_RL + 8 * qq, lo);
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            nb_arrive(NB_V);
+            // ---- V' (kept), to TMEM as hi + lo
+            nb_sync(NB_2);
+            tc_fence_after();
+            {
+                uint32_t y[16];
+                tmem_ld16_async(tbase + lane_base + F_D2 + 16 * qq, y);
+                tmem_wait_ld(); reg_fence(y);
+                float x[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int t = 16 * qq + e;
+                    x[e] = __uint_as_float(y[e]);
+                    if (t < L) Vp[((c0 + t) * H + h) * kD + row] = x[e];
+                }
+                uint32_t hi[8], lo[8];
+                split_pairs(x, 8, hi, lo);
+                tmem_st8(tbase + lane_base + F_VH + 8 * qq, hi);
+                tmem_st8(tbase + lane_base + F_VL + 8 * qq, lo);
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            nb_arrive(NB_Z);
+            // ---- S <- S Diag(gamma) + V'^T Kr
+            nb_sync(NB_3);
+            tc_fence_after();
+            if (*sStop) break;
+            {
+                uint32_t d3[32];
+                tmem_ld32_async(tbase + lane_base + F_D3 + 32 * qq, d3);
+                float gm[32];
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4*>(gm + e) = *reinterpret_cast<const float4*>(sGam + 32 * qq + e);
+                tmem_wait_ld(); reg_fence(d3);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s[e] = fmaf(s[e], gm[e], __uint_as_float(d3[e]));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     static std::once_flag once;
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -395,21 +678,39 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 
 }  // namespace
 
-cudaError_t launch_bwd_state_tc(const void* d_o, const float* d_final, const int32_t* cu_seqlens, int N,
-                                int64_t T_total, int H, const void* blobs, float* d_init, float* dS_next, float* dZ,
-                                unsigned int* err, cudaStream_t stream) {
-    // dO [T, H, 128] bf16: boxes of [64 tokens][1 head][64 channels] with the 128-byte swizzle
+// [T, H, 128] bf16 tensor: boxes of [64 tokens][1 head][64 channels] with the 128-byte swizzle
+static bool encode_token_map(CUtensorMap* tm, const void* base, int64_t T_total, int H) {
     auto fn = encoder();
-    if (!fn) return cudaErrorInvalidValue;
-    CUtensorMap tm;
+    if (!fn) return false;
     const cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)(T_total > 0 ? T_total : 1)};
     const cuuint64_t strides[2] = {(cuuint64_t)128 * 2, (cuuint64_t)H * 128 * 2};
     const cuuint32_t box[3] = {64, 1, 64};
     const cuuint32_t estr[3] = {1, 1, 1};
-    if (fn(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(d_o), dims, strides, box, estr,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_bwd_fwd_state_tc(const void* v, const float* init_state, const int32_t* cu_seqlens, int N,
+                                    int64_t T_total, int H, const void* blobs, float* S0s, float* R, float* Vp,
+                                    unsigned int* err, cudaStream_t stream) {
+    CUtensorMap tm;
+    if (!encode_token_map(&tm, v, T_total, H)) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(bwd_fwd_state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kFwdSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t chains = (int64_t)N * H;
+    if (chains == 0) return cudaSuccess;
+    bwd_fwd_state_tc_kernel<<<(unsigned)chains, kThreads, kFwdSmem, stream>>>(
+        tm, init_state, cu_seqlens, T_total, H, static_cast<const uint8_t*>(blobs), S0s, R, Vp, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_state_tc(const void* d_o, const float* d_final, const int32_t* cu_seqlens, int N,
+                                int64_t T_total, int H, const void* blobs, float* d_init, float* dS_next, float* dZ,
+                                unsigned int* err, cudaStream_t stream) {
+    CUtensorMap tm;
+    if (!encode_token_map(&tm, d_o, T_total, H)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(bwd_state_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmem);
     if (e != cudaSuccess) return e;
