@@ -30,4 +30,12 @@ cudaError_t launch_bwd_state_tc(const void* d_o, const float* d_final, const int
                                 int64_t T_total, int H, const void* blobs, float* d_init, float* dS_next, float* dZ,
                                 unsigned int* err, cudaStream_t stream);
 
+// Per (chunk, head) the products with S0 and dS_next, dA_qk, dA_kk, dv and dbeta's first term, on the
+// tensor cores for bf16 dO; outputs as bwd_chunk_a_kernel.
+cudaError_t launch_bwd_chunk_a_tc(const float* beta, const void* d_o, const int32_t* cu_seqlens, int N, int64_t T_total,
+                                  int H, float scale, const float* S0s, const float* dS_next, const float* R,
+                                  const float* Vp, const float* dZ, float* XQ, float* XK, float* XR, float* dgam,
+                                  float* dAqk, float* dAkk, float* dv, float* dbeta, unsigned int* err,
+                                  cudaStream_t stream);
+
 }  // namespace kda

@@ -27,7 +27,7 @@
 //      memory (the state's rows are independent), keeping dS_next of every chunk and dZ = T^T dV';
 //      with bf16 inputs bwd_fwd_state_tc_kernel and bwd_state_tc_kernel (kda_chunk_bwd_tc.cu) do passes 2
 //      and 3 on the tensor cores instead, one CTA per chain, from bf16 hi/lo tiles that bwd_prep_kernel
-//      writes for them;
+//      writes for them, and bwd_chunk_a_tc_kernel does step 4;
 //   4. bwd_chunk_a_kernel: per (chunk, head) the products with S0 and dS_next, dA_qk, dA_kk, dv and
 //      the first term of dbeta;
 //   5. bwd_chunk_b_kernel: per (chunk, head, half of the key channels) the position-pair products, dq,
@@ -848,10 +848,16 @@ cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const 
     }
     if (e != cudaSuccess) return e;
     if (T_total == 0) return cudaSuccess;
-    bwd_chunk_a_kernel<InT><<<grid, kThreads, smA, stream>>>(beta, ot, cu, N, T_total, H, scale, w.S0, w.dSn, w.R,
-                                                             w.Vp, w.dZ, w.XQ, w.XK, w.XR, w.dgam, w.dAqk, w.dAkk, dv,
-                                                             dbeta);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (tc_state) {
+        e = launch_bwd_chunk_a_tc(beta, d_o, cu, N, T_total, H, scale, w.S0, w.dSn, w.R, w.Vp, w.dZ, w.XQ, w.XK, w.XR,
+                                  w.dgam, w.dAqk, w.dAkk, dv, dbeta, err, stream);
+    } else {
+        bwd_chunk_a_kernel<InT><<<grid, kThreads, smA, stream>>>(beta, ot, cu, N, T_total, H, scale, w.S0, w.dSn,
+                                                                 w.R, w.Vp, w.dZ, w.XQ, w.XK, w.XR, w.dgam, w.dAqk,
+                                                                 w.dAkk, dv, dbeta);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return e;
     bwd_chunk_b_kernel<InT><<<dim3(grid.x, grid.y, 2), kThreads, smB, stream>>>(
         qt, kt, g, beta, cu, N, T_total, H, w.XQ, w.XK, w.XR, w.dgam, w.dAqk, w.dAkk, dq, dk, dg, w.dbp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

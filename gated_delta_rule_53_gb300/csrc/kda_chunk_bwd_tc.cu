@@ -663,6 +663,266 @@ bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const float* _
     if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
+// ============================ per chunk: the products with S0 and dS_next ============================
+// Per (chunk, head), the products of bwd_chunk_a_kernel, with the channel (or token) dimension as M = 128:
+//   [XQ / scale | -XK / beta]^T = S0^T [dO ; dZ]^T      (S0 as an MN-major A operand, [dO ; dZ] K-major)
+//   XR^T                        = dS_next^T V'^T
+//   [dA_qk / scale ; -dA_kk]    = [dO ; dZ] V'^T        (rows 0-63 dO, 64-127 dZ)
+// every fp32 operand split as bf16 hi + lo (the bf16 dO is exact), products hi.hi + hi.lo + lo.hi.  S0 and
+// dS_next take one shared-memory buffer in turn; dgamma = colsum(S0 . dS_next) and the first term of dbeta
+// on the CUDA cores, in a fixed order.
+constexpr int kAThreads = 512;
+constexpr uint32_t A_BUF = 0;         // S0, then dS_next: hi, lo, each [128 r][128 c] (two regions of [128][64])
+constexpr uint32_t A_QZH = 65536;     // [dO ; dZ_hi]  [128][128 r] K-major (two regions of [128][64])
+constexpr uint32_t A_QZL = 98304;     // [0 ; dZ_lo]
+constexpr uint32_t A_VH = 131072;     // V'_hi [64 s][128 r] (two regions of [64][64])
+constexpr uint32_t A_VL = 147456;     // V'_lo
+constexpr uint32_t A_RED = 163840;    // dgamma parts [32][128] fp32
+constexpr uint32_t A_BETA = 180224;   // beta [64]
+constexpr uint32_t A_BAR = 180480;    // mbarriers: X and dA products, XR product
+constexpr uint32_t A_MISC = A_BAR + 16;
+constexpr uint32_t kASmem = A_MISC + 16 + 1024;
+// TMEM: X^T 128 columns, XR^T 64, dA 64
+constexpr uint32_t A_TX = 0, A_TR = 128, A_TA = 192;
+
+// 8 values as bf16 hi + lo, 16-byte chunks at `at` of two tiles `tile` bytes apart
+__device__ __forceinline__ void put_hi_lo(uint8_t* base, uint32_t at, uint32_t tile, const float (&x)[8]) {
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        hi[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
+        lo[j] = pack_bf16x2(x[2 * j] - bf16_lo(hi[j]), x[2 * j + 1] - bf16_hi(hi[j]));
+    }
+    *reinterpret_cast<uint4*>(base + at) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(base + at + tile) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+}
+
+__global__ void __launch_bounds__(kAThreads, 1)
+bwd_chunk_a_tc_kernel(const float* __restrict__ beta, const __nv_bfloat16* __restrict__ d_o,
+                      const int32_t* __restrict__ cu, int N, int64_t T_total, int H, float scale,
+                      const float* __restrict__ S0s, const float* __restrict__ dS_next, const float* __restrict__ Rb,
+                      const float* __restrict__ Vp, const float* __restrict__ dZ, float* __restrict__ XQ,
+                      float* __restrict__ XK, float* __restrict__ XR, float* __restrict__ dgam,
+                      float* __restrict__ dAqk, float* __restrict__ dAkk, float* __restrict__ dv,
+                      float* __restrict__ dbeta, unsigned int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t slot = blockIdx.x;
+    const int h = blockIdx.y;
+    // the chunk of this slot (as bwd_prep_kernel): sequence n with bos_n / 64 + n <= slot
+    int n = 0;
+    {
+        int lo = 0, hi = N;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            const int64_t b = cu ? (int64_t)cu[mid] : 0;
+            if (b / kC + mid <= slot) lo = mid; else hi = mid;
+        }
+        n = lo;
+    }
+    int64_t bos, eos;
+    seq_bounds(cu, n, T_total, bos, eos);
+    const int64_t c0 = bos + (slot - (bos / kC + n)) * kC;
+    if (slot < bos / kC + n || c0 >= eos) return;
+    const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
+    const int64_t base = slot * H + h;
+    float* sRed = reinterpret_cast<float*>(sm + A_RED);
+    float* sBeta = reinterpret_cast<float*>(sm + A_BETA);
+    uint64_t* bX = reinterpret_cast<uint64_t*>(sm + A_BAR);
+    uint64_t* bR = bX + 1;
+    uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + A_MISC);
+    if (tid == 0) {
+        mbar_init(bX, 1);
+        mbar_init(bR, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(sTmem, 256);
+    if (tid < kC) sBeta[tid] = tid < L ? beta[(c0 + tid) * H + h] : 0.f;
+    const float* S0 = S0s + base * kD * kD;
+    const float* dSn = dS_next + base * kD * kD;
+    // ---- S0 -> the buffer (MN-major A: row r, channels c)
+    for (int idx = tid; idx < kD * 16; idx += kAThreads) {
+        const int r = idx >> 4, c8 = idx & 15;
+        const float4 a = *reinterpret_cast<const float4*>(S0 + r * kD + 8 * c8);
+        const float4 b = *reinterpret_cast<const float4*>(S0 + r * kD + 8 * c8 + 4);
+        const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        put_hi_lo(sm + A_BUF, (uint32_t)(c8 >> 3) * 16384u + sw128((uint32_t)r, (uint32_t)(c8 & 7)), 32768, x);
+    }
+    // ---- [dO ; dZ] (rows past the chunk's end zero), V'; dv = beta dZ; dbeta's first term sum_r dZ R
+    for (int idx = tid; idx < kC * 16; idx += kAThreads) {
+        const int t = idx >> 4, r8 = idx & 15;
+        const bool ok = t < L;
+        const int64_t at = ((c0 + t) * H + h) * kD + 8 * r8;
+        float z[8], vp[8];
+        uint4 o = make_uint4(0, 0, 0, 0);
+        float part = 0.f;
+        if (ok) {
+            o = *reinterpret_cast<const uint4*>(d_o + at);
+            const float4 z0 = *reinterpret_cast<const float4*>(dZ + at), z1 = *reinterpret_cast<const float4*>(dZ + at + 4);
+            const float4 p0 = *reinterpret_cast<const float4*>(Vp + at), p1 = *reinterpret_cast<const float4*>(Vp + at + 4);
+            const float4 q0 = *reinterpret_cast<const float4*>(Rb + at), q1 = *reinterpret_cast<const float4*>(Rb + at + 4);
+            z[0] = z0.x; z[1] = z0.y; z[2] = z0.z; z[3] = z0.w; z[4] = z1.x; z[5] = z1.y; z[6] = z1.z; z[7] = z1.w;
+            vp[0] = p0.x; vp[1] = p0.y; vp[2] = p0.z; vp[3] = p0.w; vp[4] = p1.x; vp[5] = p1.y; vp[6] = p1.z; vp[7] = p1.w;
+            const float rr[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) part = fmaf(z[e], rr[e], part);
+            const float bt = beta[(c0 + t) * H + h];
+            *reinterpret_cast<float4*>(dv + at) = make_float4(bt * z[0], bt * z[1], bt * z[2], bt * z[3]);
+            *reinterpret_cast<float4*>(dv + at + 4) = make_float4(bt * z[4], bt * z[5], bt * z[6], bt * z[7]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) { z[e] = 0.f; vp[e] = 0.f; }
+        }
+        const uint32_t c = (uint32_t)(r8 & 7), reg = (uint32_t)(r8 >> 3);
+        *reinterpret_cast<uint4*>(sm + A_QZH + reg * 16384 + sw128((uint32_t)t, c)) = o;
+        *reinterpret_cast<uint4*>(sm + A_QZL + reg * 16384 + sw128((uint32_t)t, c)) = make_uint4(0, 0, 0, 0);
+        {
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                hi[j] = pack_bf16x2(z[2 * j], z[2 * j + 1]);
+                lo[j] = pack_bf16x2(z[2 * j] - bf16_lo(hi[j]), z[2 * j + 1] - bf16_hi(hi[j]));
+            }
+            *reinterpret_cast<uint4*>(sm + A_QZH + reg * 16384 + sw128((uint32_t)(64 + t), c)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(sm + A_QZL + reg * 16384 + sw128((uint32_t)(64 + t), c)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        put_hi_lo(sm + A_VH, reg * 8192 + sw128((uint32_t)t, c), 16384, vp);
+        // a row's 16 parts are 16 consecutive lanes: reduce them in a fixed order
+#pragma unroll
+        for (int o2 = 8; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o2);
+        if (r8 == 0 && ok) dbeta[(c0 + t) * H + h] = part;
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *sTmem;
+    const uint32_t id_x = idesc_bf16_f32(128, 128, true, false);   // A = S0^T (MN-major), B = [dO ; dZ] (K-major)
+    const uint32_t id_r = idesc_bf16_f32(128, 64, true, false);    // A = dS_next^T (MN-major), B = V' (K-major)
+    const uint32_t id_a = idesc_bf16_f32(128, 64, false, false);   // A = [dO ; dZ], B = V' (K-major)
+    auto kd = [&](uint32_t tile, uint32_t region, int ks) { return sdesc_sw128(tile + (ks >> 2) * region, 16, 1024) + (ks & 3) * 2; };
+    if (warp == 0) {
+        const uint64_t sh = sdesc_sw128(sbase + A_BUF, 16384, 1024), sl = sdesc_sw128(sbase + A_BUF + 32768, 16384, 1024);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) mma_bf16(tbase + A_TX, sh + ks * 128, kd(sbase + A_QZH, 16384, ks), id_x, ks > 0 ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) mma_bf16(tbase + A_TX, sl + ks * 128, kd(sbase + A_QZH, 16384, ks), id_x, 1u);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) mma_bf16(tbase + A_TX, sh + ks * 128, kd(sbase + A_QZL, 16384, ks), id_x, 1u);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+            mma_bf16(tbase + A_TA, kd(sbase + A_QZH, 16384, ks), kd(sbase + A_VH, 8192, ks), id_a, ks > 0 ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) mma_bf16(tbase + A_TA, kd(sbase + A_QZH, 16384, ks), kd(sbase + A_VL, 8192, ks), id_a, 1u);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) mma_bf16(tbase + A_TA, kd(sbase + A_QZL, 16384, ks), kd(sbase + A_VH, 8192, ks), id_a, 1u);
+        mma_commit(bX);
+    }
+    // ---- dgamma parts: sum over rows r of S0 . dS_next (S0 read again, from L2); 32 row groups x 128 channels
+    {
+        const int c4 = tid & 31, rg = tid >> 5;  // channels 4 c4 .. +3, rows rg, rg + 16, ...
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r = rg; r < kD; r += 16) {
+            const float4 a = *reinterpret_cast<const float4*>(S0 + r * kD + 4 * c4);
+            const float4 b = *reinterpret_cast<const float4*>(dSn + r * kD + 4 * c4);
+            acc.x = fmaf(a.x, b.x, acc.x); acc.y = fmaf(a.y, b.y, acc.y);
+            acc.z = fmaf(a.z, b.z, acc.z); acc.w = fmaf(a.w, b.w, acc.w);
+        }
+        *reinterpret_cast<float4*>(sRed + rg * kD + 4 * c4) = acc;
+    }
+    // ---- the buffer takes dS_next once the S0 products are done
+    if (tid == 0 && !mbar_wait(bX, 0, kWaitLimit)) raise_device_error(err, kErrMbarTimeout);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    for (int idx = tid; idx < kD * 16; idx += kAThreads) {
+        const int r = idx >> 4, c8 = idx & 15;
+        const float4 a = *reinterpret_cast<const float4*>(dSn + r * kD + 8 * c8);
+        const float4 b = *reinterpret_cast<const float4*>(dSn + r * kD + 8 * c8 + 4);
+        const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        put_hi_lo(sm + A_BUF, (uint32_t)(c8 >> 3) * 16384u + sw128((uint32_t)r, (uint32_t)(c8 & 7)), 32768, x);
+    }
+    if (tid < kD) {  // dgamma: the 16 row groups' parts in order
+        float sum = 0.f;
+        for (int g = 0; g < 16; ++g) sum += sRed[g * kD + tid];
+        dgam[base * kD + tid] = sum;
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) {
+        const uint64_t dh = sdesc_sw128(sbase + A_BUF, 16384, 1024), dl = sdesc_sw128(sbase + A_BUF + 32768, 16384, 1024);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) mma_bf16(tbase + A_TR, dh + ks * 128, kd(sbase + A_VH, 8192, ks), id_r, ks > 0 ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) mma_bf16(tbase + A_TR, dh + ks * 128, kd(sbase + A_VL, 8192, ks), id_r, 1u);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) mma_bf16(tbase + A_TR, dl + ks * 128, kd(sbase + A_VH, 8192, ks), id_r, 1u);
+        mma_commit(bR);
+    }
+    // ---- X^T out while XR^T is computed: warp w reads lanes 32 (w % 4) .. (channels c), columns 32 (w / 4) ..
+    {
+        const int q = warp & 3, cb = warp >> 2;  // column block: 0, 1 -> XQ tokens 0-31, 32-63; 2, 3 -> XK
+        const int c = 32 * q + lane;
+        uint32_t x[32];
+        tmem_ld32_async(tbase + ((uint32_t)(32 * q) << 16) + A_TX + 32 * cb, x);
+        tmem_wait_ld(); reg_fence(x);
+        const bool is_q = cb < 2;
+        const int t0 = 32 * (cb & 1);
+        float* outp = is_q ? XQ : XK;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const int t = t0 + e;
+            if (t < L) outp[((c0 + t) * H + h) * kD + c] = (is_q ? scale : -sBeta[t]) * __uint_as_float(x[e]);
+        }
+    }
+    // ---- dA: lanes 0-63 dO V'^T (dA_qk / scale, j <= i), lanes 64-127 dZ V'^T (-dA_kk, j < i)
+    if (warp < 8) {
+        const int q = warp & 3, hb = warp >> 2;  // columns 32 hb .. +31
+        const int m = 32 * q + lane, i = m & 63;
+        const bool is_q = m < 64;
+        uint32_t x[32];
+        tmem_ld32_async(tbase + ((uint32_t)(32 * q) << 16) + A_TA + 32 * hb, x);
+        tmem_wait_ld(); reg_fence(x);
+        float* row = (is_q ? dAqk : dAkk) + (base * kC + i) * kC + 32 * hb;
+#pragma unroll
+        for (int e4 = 0; e4 < 32; e4 += 4) {
+            float4 w;
+            float* wp = reinterpret_cast<float*>(&w);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = 32 * hb + e4 + e;
+                const float v = __uint_as_float(x[e4 + e]);
+                wp[e] = is_q ? (j <= i ? scale * v : 0.f) : (j < i ? -v : 0.f);
+            }
+            *reinterpret_cast<float4*>(row + e4) = w;
+        }
+    }
+    if (tid == 0 && !mbar_wait(bR, 0, kWaitLimit)) raise_device_error(err, kErrMbarTimeout);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // ---- XR^T out: warp w reads lanes 32 (w % 4) .. (channels), tokens 16 (w / 4) .. +15
+    {
+        const int q = warp & 3, tb = warp >> 2;
+        const int c = 32 * q + lane;
+        uint32_t x[16];
+        tmem_ld16_async(tbase + ((uint32_t)(32 * q) << 16) + A_TR + 16 * tb, x);
+        tmem_wait_ld(); reg_fence(x);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int t = 16 * tb + e;
+            if (t < L) XR[((c0 + t) * H + h) * kD + c] = __uint_as_float(x[e]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 256);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     static std::once_flag once;
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -718,6 +978,24 @@ cudaError_t launch_bwd_state_tc(const void* d_o, const float* d_final, const int
     if (chains == 0) return cudaSuccess;
     bwd_state_tc_kernel<__nv_bfloat16><<<(unsigned)chains, kThreads, kSmem, stream>>>(
         tm, d_final, cu_seqlens, T_total, H, static_cast<const uint8_t*>(blobs), d_init, dS_next, dZ, err);
+    return cudaGetLastError();
+}
+
+}  // namespace kda
+
+namespace kda {
+
+cudaError_t launch_bwd_chunk_a_tc(const float* beta, const void* d_o, const int32_t* cu_seqlens, int N, int64_t T_total,
+                                  int H, float scale, const float* S0s, const float* dS_next, const float* R,
+                                  const float* Vp, const float* dZ, float* XQ, float* XK, float* XR, float* dgam,
+                                  float* dAqk, float* dAkk, float* dv, float* dbeta, unsigned int* err,
+                                  cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_chunk_a_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kASmem);
+    if (e != cudaSuccess) return e;
+    const int64_t slots = T_total / kC + N + 1;
+    bwd_chunk_a_tc_kernel<<<dim3((unsigned)slots, (unsigned)H), kAThreads, kASmem, stream>>>(
+        beta, static_cast<const __nv_bfloat16*>(d_o), cu_seqlens, N, T_total, H, scale, S0s, dS_next, R, Vp, dZ, XQ, XK,
+        XR, dgam, dAqk, dAkk, dv, dbeta, err);
     return cudaGetLastError();
 }
 
