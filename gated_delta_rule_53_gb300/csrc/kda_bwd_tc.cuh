@@ -38,4 +38,11 @@ cudaError_t launch_bwd_chunk_a_tc(const float* beta, const void* d_o, const int3
                                   float* dAqk, float* dAkk, float* dv, float* dbeta, unsigned int* err,
                                   cudaStream_t stream);
 
+// Per (chunk, head) the position-pair sums, dq, dk, dg and the two channel halves' parts of dbeta's second
+// term, on the tensor cores for bf16 q, k; outputs as bwd_chunk_b_kernel.
+cudaError_t launch_bwd_chunk_b_tc(const void* q, const void* k, const float* g, const float* beta, const int32_t* cu_seqlens,
+                                  int N, int64_t T_total, int H, const float* XQ, const float* XK, const float* XR,
+                                  const float* dgam, const float* dAqk, const float* dAkk, float* dq, float* dk,
+                                  float* dg, float* dbeta_part, unsigned int* err, cudaStream_t stream);
+
 }  // namespace kda

@@ -27,7 +27,7 @@
 //      memory (the state's rows are independent), keeping dS_next of every chunk and dZ = T^T dV';
 //      with bf16 inputs bwd_fwd_state_tc_kernel and bwd_state_tc_kernel (kda_chunk_bwd_tc.cu) do passes 2
 //      and 3 on the tensor cores instead, one CTA per chain, from bf16 hi/lo tiles that bwd_prep_kernel
-//      writes for them, and bwd_chunk_a_tc_kernel does step 4;
+//      writes for them, and bwd_chunk_a_tc_kernel and bwd_chunk_b_tc_kernel do steps 4 and 5;
 //   4. bwd_chunk_a_kernel: per (chunk, head) the products with S0 and dS_next, dA_qk, dA_kk, dv and
 //      the first term of dbeta;
 //   5. bwd_chunk_b_kernel: per (chunk, head, half of the key channels) the position-pair products, dq,
@@ -146,13 +146,15 @@ bwd_prep_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const floa
 #pragma unroll
         for (int i = 0; i < kC; ++i) gT[base * kC * kC + i * kC + j] = x[i];
     }
-    for (int idx = tid; idx < kC * kD; idx += kThreads) {  // Qg, Kg, Kr
-        const int c = idx % kD;
-        const float G = sG[idx], kk = sK[idx];
-        const float gam = expf(G);
-        gQg[base * kC * kD + idx] = sQ[idx] * gam;
-        gKg[base * kC * kD + idx] = kk * gam;
-        gKr[base * kC * kD + idx] = kk * expf(sGl[c] - G);
+    if (!bb) {  // Qg, Kg, Kr in fp32 for the CUDA-core passes along the chains (the tensor-core ones read bb)
+        for (int idx = tid; idx < kC * kD; idx += kThreads) {
+            const int c = idx % kD;
+            const float G = sG[idx], kk = sK[idx];
+            const float gam = expf(G);
+            gQg[base * kC * kD + idx] = sQ[idx] * gam;
+            gKg[base * kC * kD + idx] = kk * gam;
+            gKr[base * kC * kD + idx] = kk * expf(sGl[c] - G);
+        }
     }
     if (bb) {  // the same values as bf16 hi + lo tiles, in the layouts the tensor-core reverse pass reads
         __syncthreads();  // this CTA's global writes of A_qk and T are visible to all of it
@@ -858,9 +860,15 @@ cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const 
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
-    bwd_chunk_b_kernel<InT><<<dim3(grid.x, grid.y, 2), kThreads, smB, stream>>>(
-        qt, kt, g, beta, cu, N, T_total, H, w.XQ, w.XK, w.XR, w.dgam, w.dAqk, w.dAkk, dq, dk, dg, w.dbp);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (tc_state) {
+        e = launch_bwd_chunk_b_tc(q, k, g, beta, cu, N, T_total, H, w.XQ, w.XK, w.XR, w.dgam, w.dAqk, w.dAkk, dq, dk, dg,
+                                  w.dbp, err, stream);
+    } else {
+        bwd_chunk_b_kernel<InT><<<dim3(grid.x, grid.y, 2), kThreads, smB, stream>>>(
+            qt, kt, g, beta, cu, N, T_total, H, w.XQ, w.XK, w.XR, w.dgam, w.dAqk, w.dAkk, dq, dk, dg, w.dbp);
+        e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return e;
     const int64_t nb = T_total * H;
     bwd_dbeta_kernel<<<(unsigned)((nb + 255) / 256), 256, 0, stream>>>(dbeta, w.dbp, nb);
     return cudaGetLastError();

@@ -923,6 +923,297 @@ bwd_chunk_a_tc_kernel(const float* __restrict__ beta, const __nv_bfloat16* __res
     if (warp == 0) tmem_dealloc(tbase, 256);
 }
 
+// ============================ per chunk: the position-pair sums ============================
+// Per (chunk, head), the sums of bwd_chunk_b_kernel over position pairs with the decay e^{G_ic - G_jc}:
+//   rq_ic = sum_{j<=i} dA_qk[i][j] k_jc e^{G_ic-G_jc},   rk_ic = sum_{j<i} dA_kk[i][j] k_jc e^{G_ic-G_jc}
+//   cq_jc = sum_{i>=j} dA_qk[i][j] q_ic e^{G_ic-G_jc},   ck_jc = sum_{i>j} dA_kk[i][j] beta_i k_ic e^{G_ic-G_jc}
+// as tensor-core products, block by block of 16 tokens with the forward's factorisation around E_b, G at
+// the block's last token (the -5 bound keeps every factor within fp32: "月之暗面发布Kimi K3开源大模型
+// 技术报告", 架构): for rows i of block b, e^{G_i-G_j} = e^{G_i-E_b} e^{E_b-G_j} with the second factor
+// at most 1 for j <= 16b+15, so the column operand k e^{E_b-G} (zero past the block) times dA_qk^T and
+// dA_kk^T gives rq and rk of the block's rows up to e^{G_i-E_b}; for columns j of block b the row operands
+// q e^{G-E_b} and beta k e^{G-E_b} (zero before the block) give cq and ck up to e^{E_b-G_j}.  Every product
+// is taken transposed, channels as M = 128, and from three-piece bf16 splits (x = p1 + p2 + p3 to about
+// 2^-27; p1p1 + p1p2 + p2p1 + p1p3 + p3p1 + p2p2): the gradient of G is a difference of these sums, where a
+// two-piece split (2^-17) would leave too little.  Then, per (i, c), the element-wise part of
+// bwd_chunk_b_kernel: dq, dk, the gradient of G, dbeta's second term (a part per channel half) and dg as the
+// reverse running sum of the G gradient inside the chunk.  Only the rows a block's products reach are built and
+// multiplied: the column operand of block b is zero past 16b+15, the row operands before 16b.
+constexpr int kBThreads = 512;
+constexpr uint32_t B_AR = 0;          // [dA_qk ; dA_kk]: [128 rows i][64 j], three pieces of 16 KB
+constexpr uint32_t B_OP = 49152;      // the block's operand (k e^{E_b-G}, q e^{G-E_b} or beta k e^{G-E_b}):
+                                      // [64 rows][128 c] (two regions of [64][64]), three pieces of 16 KB
+constexpr uint32_t B_G = 98304;       // G (log2 units) fp32 [64][128]
+constexpr uint32_t B_Q = 131072;      // q, k bf16 [64][128] each
+constexpr uint32_t B_K = 147456;
+constexpr uint32_t B_DG = 163840;     // the gradient of G, fp32 [64][128]
+constexpr uint32_t B_BETA = 196608;   // beta [64]
+constexpr uint32_t B_LAST = 196864;   // per (row group, channel): sum over its rows of xr k e^{G_last - G}, fp32 [4][128]
+constexpr uint32_t B_DBP = 198912;    // dbeta parts per (row, lane quarter): fp32 [64][4]
+constexpr uint32_t B_BAR = 199936;
+constexpr uint32_t B_MISC = B_BAR + 16;
+constexpr uint32_t kBSmem = B_MISC + 16 + 1024;
+constexpr uint32_t B_T1 = 0, B_T2 = 64, B_T3 = 128, B_T4 = 192;  // TMEM: rq^T, rk^T, cq^T, ck^T [c][row]
+
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// 8 values as three bf16 pieces (x = p1 + p2 + p3), 16-byte chunks at `at` of three tiles `tile` bytes apart
+__device__ __forceinline__ void put_3(uint8_t* base, uint32_t at, uint32_t tile, const float (&x)[8]) {
+    uint32_t p1[4], p2[4], p3[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float a = x[2 * j], b = x[2 * j + 1];
+        p1[j] = pack_bf16x2(a, b);
+        const float ra = a - bf16_lo(p1[j]), rb = b - bf16_hi(p1[j]);
+        p2[j] = pack_bf16x2(ra, rb);
+        p3[j] = pack_bf16x2(ra - bf16_lo(p2[j]), rb - bf16_hi(p2[j]));
+    }
+    *reinterpret_cast<uint4*>(base + at) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
+    *reinterpret_cast<uint4*>(base + at + tile) = make_uint4(p2[0], p2[1], p2[2], p2[3]);
+    *reinterpret_cast<uint4*>(base + at + 2 * tile) = make_uint4(p3[0], p3[1], p3[2], p3[3]);
+}
+
+__global__ void __launch_bounds__(kBThreads, 1)
+bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                      const float* __restrict__ g, const float* __restrict__ beta, const int32_t* __restrict__ cu, int N,
+                      int64_t T_total, int H, const float* __restrict__ XQ, const float* __restrict__ XK,
+                      const float* __restrict__ XR, const float* __restrict__ dgam, const float* __restrict__ dAqk,
+                      const float* __restrict__ dAkk, float* __restrict__ dq, float* __restrict__ dk,
+                      float* __restrict__ dg, float* __restrict__ dbeta_part, unsigned int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t slot = blockIdx.x;
+    const int h = blockIdx.y;
+    int n = 0;
+    {
+        int lo = 0, hi = N;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            const int64_t b = cu ? (int64_t)cu[mid] : 0;
+            if (b / kC + mid <= slot) lo = mid; else hi = mid;
+        }
+        n = lo;
+    }
+    int64_t bos, eos;
+    seq_bounds(cu, n, T_total, bos, eos);
+    const int64_t c0 = bos + (slot - (bos / kC + n)) * kC;
+    if (slot < bos / kC + n || c0 >= eos) return;
+    const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
+    const int64_t base = slot * H + h;
+    constexpr float kLog2e = 1.4426950408889634f;
+    float* sG = reinterpret_cast<float*>(sm + B_G);
+    float* sDG = reinterpret_cast<float*>(sm + B_DG);
+    const __nv_bfloat16* sQ = reinterpret_cast<const __nv_bfloat16*>(sm + B_Q);
+    const __nv_bfloat16* sK = reinterpret_cast<const __nv_bfloat16*>(sm + B_K);
+    float* sBeta = reinterpret_cast<float*>(sm + B_BETA);
+    float* sLast = reinterpret_cast<float*>(sm + B_LAST);
+    float* sDBP = reinterpret_cast<float*>(sm + B_DBP);
+    uint64_t* bM = reinterpret_cast<uint64_t*>(sm + B_BAR);
+    uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + B_MISC);
+    if (tid == 0) {
+        mbar_init(bM, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(sTmem, 256);
+    if (tid < kC) sBeta[tid] = tid < L ? beta[(c0 + tid) * H + h] : 0.f;
+    // ---- q, k rows (zero past the sequence's end): thread (row, 16-byte chunk), two per tensor
+    for (int idx = tid; idx < 2 * kC * 16; idx += kBThreads) {
+        const int which = idx >> 10, r = (idx >> 4) & 63, c8 = idx & 15;
+        uint4 xv = make_uint4(0, 0, 0, 0);
+        if (r < L) xv = *reinterpret_cast<const uint4*>((which ? k : q) + ((c0 + r) * H + h) * kD + 8 * c8);
+        *reinterpret_cast<uint4*>(sm + (which ? B_K : B_Q) + r * 256 + 16 * c8) = xv;
+    }
+    // ---- G: running sum of g per channel (log2 units), thread (c, half): tokens 32 half .. +31
+    if (tid < 256) {
+        const int c = tid & 127, hh = tid >> 7;
+        float gv[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            const int t = 32 * hh + r;
+            gv[r] = t < L ? g[((c0 + t) * H + h) * kD + c] * kLog2e : 0.f;
+        }
+#pragma unroll
+        for (int r = 1; r < 32; ++r) gv[r] += gv[r - 1];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) sG[(32 * hh + r) * kD + c] = gv[r];
+    }
+    // ---- dA_qk (rows 0-63), dA_kk (rows 64-127) as three bf16 pieces
+    for (int idx = tid; idx < 2 * kC * 8; idx += kBThreads) {  // row m, columns 8 j8 ..
+        const int m = idx >> 3, j8 = idx & 7;
+        const float* src = (m < kC ? dAqk + (base * kC + m) * kC : dAkk + (base * kC + m - kC) * kC) + 8 * j8;
+        const float4 a = *reinterpret_cast<const float4*>(src), b = *reinterpret_cast<const float4*>(src + 4);
+        const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        put_3(sm + B_AR, sw128((uint32_t)m, (uint32_t)j8), 16384, x);
+    }
+    __syncthreads();
+    if (tid >= 128 && tid < 256) {  // the second half's running sum continues from the first's total
+        const int c = tid & 127;
+        const float t0 = sG[31 * kD + c];
+#pragma unroll 4
+        for (int r = 32; r < 64; ++r) sG[r * kD + c] += t0;
+    }
+    __syncthreads();
+    const uint32_t tbase = *sTmem;
+    const uint32_t id_k = idesc_bf16_f32(128, 64, true, false);  // A = operand^T (MN-major), B = dA rows (K-major)
+    const uint32_t id_m = idesc_bf16_f32(128, 64, true, true);   // A = operand^T, B = dA columns (MN-major)
+    // pieces (of the operand, of dA) of the six products p: nibble p of kPa, kPb
+    // (11, 12, 21, 13, 31, 22 in one-based pieces)
+    constexpr uint32_t kPa = 0x120100u, kPb = 0x102010u;
+    uint32_t phase = 0;
+    const int qr = warp & 3, rg = warp >> 2;  // lane quarter (channels 32 qr ..), row group of the epilogue
+    const int c_me = 32 * qr + lane;
+    const int c8_me = tid & 15;               // the operand builder's 8 channels
+    float last_acc = 0.f;
+    for (int b = 0; b < 4; ++b) {
+        // the element-wise part's inputs, fetched while the block's products are formed
+        const int i0 = 16 * b + 4 * rg;
+        float xq[4], xk[4], xr[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const int64_t at = ((c0 + i0 + a) * H + h) * kD + c_me;
+            const bool in = i0 + a < L;
+            xq[a] = in ? XQ[at] : 0.f;
+            xk[a] = in ? XK[at] : 0.f;
+            xr[a] = in ? XR[at] : 0.f;
+        }
+        float eb8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) eb8[e] = sG[(16 * b + 15) * kD + 8 * c8_me + e];
+        // three stages: 0 the column operand k e^{E_b-G}, rows 0 .. 16b+15 -> rq^T, rk^T;
+        // 1 q e^{G-E_b}, rows 16b .. 63 -> cq^T; 2 beta k e^{G-E_b}, rows 16b .. 63 -> ck^T
+#pragma unroll 1
+        for (int stage = 0; stage < 3; ++stage) {
+            const int r0 = stage == 0 ? 0 : 16 * b, rows = stage == 0 ? 16 * (b + 1) : kC - 16 * b;
+            for (int idx = tid; idx < rows * 16; idx += kBThreads) {  // row r, channels 8 c8_me .. +7
+                const int r = r0 + (idx >> 4);
+                const uint4 xv = *reinterpret_cast<const uint4*>(sm + (stage == 1 ? B_Q : B_K) + r * 256 + 16 * c8_me);
+                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                const float br = stage == 2 ? sBeta[r] : 1.f;
+                const float4 ga = *reinterpret_cast<const float4*>(sG + r * kD + 8 * c8_me);
+                const float4 gb = *reinterpret_cast<const float4*>(sG + r * kD + 8 * c8_me + 4);
+                const float gr[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+                float val[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float x = (e & 1) ? bf16_hi(xw[e >> 1]) : bf16_lo(xw[e >> 1]);
+                    val[e] = stage == 0 ? x * ex2f(eb8[e] - gr[e]) : br * x * ex2f(gr[e] - eb8[e]);
+                }
+                put_3(sm + B_OP, (uint32_t)(c8_me >> 3) * 8192u + sw128((uint32_t)r, (uint32_t)(c8_me & 7)), 16384, val);
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            if (warp == 0) {
+                const int ks0 = stage == 0 ? 0 : b, ks1 = stage == 0 ? b : 3;
+#pragma unroll 1
+                for (int p = 0; p < 6; ++p) {
+                    const uint64_t ad = sdesc_sw128(sbase + B_OP + 16384 * ((kPa >> (4 * p)) & 15u), 8192, 1024);
+                    const uint32_t bt = sbase + B_AR + 16384 * ((kPb >> (4 * p)) & 15u);
+                    if (stage == 0) {
+                        for (int ks = ks0; ks <= ks1; ++ks)
+                            mma_bf16(tbase + B_T1, ad + ks * 128, kdesc(bt) + ks * 2, id_k, (p || ks > ks0) ? 1u : 0u);
+                        for (int ks = ks0; ks <= ks1; ++ks)
+                            mma_bf16(tbase + B_T2, ad + ks * 128, kdesc(bt + 8192) + ks * 2, id_k,
+                                     (p || ks > ks0) ? 1u : 0u);
+                    } else {
+                        const uint64_t bd = sdesc_sw128(bt + (stage == 2 ? 8192 : 0), 8192, 1024);
+                        const uint32_t dst = tbase + (stage == 1 ? B_T3 : B_T4);
+                        for (int ks = ks0; ks <= ks1; ++ks)
+                            mma_bf16(dst, ad + ks * 128, bd + ks * 128, id_m, (p || ks > ks0) ? 1u : 0u);
+                    }
+                }
+                mma_commit(bM);
+            }
+            if (tid == 0 && !mbar_wait(bM, phase, kWaitLimit)) raise_device_error(err, kErrMbarTimeout);
+            phase ^= 1u;
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+        }
+        // ---- the element-wise part: thread (channel c_me, rows i0 .. i0 + 3)
+        {
+            const uint32_t lb = (uint32_t)(32 * qr) << 16;
+            uint32_t t1[4], t2[4], t3[4], t4[4];
+            tmem_ld4_async(tbase + lb + B_T1 + i0, t1);
+            tmem_ld4_async(tbase + lb + B_T2 + i0, t2);
+            tmem_ld4_async(tbase + lb + B_T3 + i0, t3);
+            tmem_ld4_async(tbase + lb + B_T4 + i0, t4);
+            tmem_wait_ld(); reg_fence(t1); reg_fence(t2); reg_fence(t3); reg_fence(t4);
+            const int c = c_me;
+            const float Eb = sG[(16 * b + 15) * kD + c], Gl = sG[(kC - 1) * kD + c];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const int i = i0 + a;
+                float dbp = 0.f, dG = 0.f;
+                if (i < L) {
+                    const int64_t at = ((c0 + i) * H + h) * kD + c;
+                    const float qi = __bfloat162float(sQ[i * kD + c]), ki = __bfloat162float(sK[i * kD + c]);
+                    const float bi = sBeta[i];
+                    const float Gi = sG[i * kD + c];
+                    const float up = ex2f(Gi - Eb), down = ex2f(Eb - Gi);
+                    const float rq = up * __uint_as_float(t1[a]), rk = up * __uint_as_float(t2[a]);
+                    const float cs = down * (__uint_as_float(t3[a]) + __uint_as_float(t4[a]));  // cq + ck
+                    const float gam = ex2f(Gi), red = ex2f(fminf(Gl - Gi, 0.f));
+                    dq[at] = fmaf(xq[a], gam, rq);
+                    dk[at] = bi * rk + xk[a] * gam + xr[a] * red + cs;
+                    dG = qi * rq + ki * bi * rk + (xq[a] * qi + xk[a] * ki) * gam - xr[a] * ki * red - ki * cs;
+                    last_acc = fmaf(xr[a] * ki, red, last_acc);
+                    dbp = ki * rk;
+                }
+                sDG[i * kD + c] = dG;
+                // dbeta's second term of row i: this warp's 32 channels, in a fixed order
+#pragma unroll
+                for (int o2 = 16; o2 > 0; o2 >>= 1) dbp += __shfl_xor_sync(0xFFFFFFFFu, dbp, o2);
+                if (lane == 0) sDBP[i * 4 + qr] = dbp;
+            }
+        }
+    }
+    sLast[rg * kD + c_me] = last_acc;
+    __syncthreads();
+    // ---- the last token's extra (every row's xr k e^{G_last - G} and dgamma e^{G_last}); G_t is the sum of g_s for
+    //      s <= t and the factors above are natural exponentials, so sDG is the gradient with respect to G in
+    //      natural units
+    if (tid < kD && L > 0) {
+        const int c = tid;
+        sDG[(L - 1) * kD + c] += (sLast[c] + sLast[kD + c] + sLast[2 * kD + c] + sLast[3 * kD + c]) +
+                                 dgam[base * kD + c] * ex2f(sG[(kC - 1) * kD + c]);
+    }
+    if (tid < L) {  // channel half 0 = lane quarters 0, 1; half 1 = 2, 3
+        dbeta_part[(c0 + tid) * H + h] = sDBP[tid * 4] + sDBP[tid * 4 + 1];
+        dbeta_part[(T_total + c0 + tid) * H + h] = sDBP[tid * 4 + 2] + sDBP[tid * 4 + 3];
+    }
+    __syncthreads();
+    // ---- dg_t = sum_{s >= t} dG_s inside the chunk: thread (channel, quarter of 16 tokens) sums its own
+    //      tokens from the end, then adds the totals of the later quarters
+    {
+        const int c = tid & 127, pq = tid >> 7;
+        float acc = 0.f;
+#pragma unroll
+        for (int t = 15; t >= 0; --t) {
+            acc += sDG[(16 * pq + t) * kD + c];
+            sDG[(16 * pq + t) * kD + c] = acc;
+        }
+        __syncthreads();
+        float off = 0.f;
+        for (int p2 = 3; p2 > pq; --p2) off += sDG[(16 * p2) * kD + c];
+#pragma unroll 4
+        for (int t = 0; t < 16; ++t) {
+            const int r = 16 * pq + t;
+            if (r < L) dg[((c0 + r) * H + h) * kD + c] = sDG[r * kD + c] + off;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 256);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     static std::once_flag once;
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -996,6 +1287,23 @@ cudaError_t launch_bwd_chunk_a_tc(const float* beta, const void* d_o, const int3
     bwd_chunk_a_tc_kernel<<<dim3((unsigned)slots, (unsigned)H), kAThreads, kASmem, stream>>>(
         beta, static_cast<const __nv_bfloat16*>(d_o), cu_seqlens, N, T_total, H, scale, S0s, dS_next, R, Vp, dZ, XQ, XK,
         XR, dgam, dAqk, dAkk, dv, dbeta, err);
+    return cudaGetLastError();
+}
+
+}  // namespace kda
+
+namespace kda {
+
+cudaError_t launch_bwd_chunk_b_tc(const void* q, const void* k, const float* g, const float* beta, const int32_t* cu_seqlens,
+                                  int N, int64_t T_total, int H, const float* XQ, const float* XK, const float* XR,
+                                  const float* dgam, const float* dAqk, const float* dAkk, float* dq, float* dk,
+                                  float* dg, float* dbeta_part, unsigned int* err, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_chunk_b_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t slots = T_total / kC + N + 1;
+    bwd_chunk_b_tc_kernel<<<dim3((unsigned)slots, (unsigned)H), kBThreads, kBSmem, stream>>>(
+        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), g, beta, cu_seqlens, N, T_total, H,
+        XQ, XK, XR, dgam, dAqk, dAkk, dq, dk, dg, dbeta_part, err);
     return cudaGetLastError();
 }
 
