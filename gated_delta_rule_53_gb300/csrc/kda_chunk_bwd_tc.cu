@@ -927,33 +927,36 @@ bwd_chunk_a_tc_kernel(const float* __restrict__ beta, const __nv_bfloat16* __res
 // Per (chunk, head), the sums of bwd_chunk_b_kernel over position pairs with the decay e^{G_ic - G_jc}:
 //   rq_ic = sum_{j<=i} dA_qk[i][j] k_jc e^{G_ic-G_jc},   rk_ic = sum_{j<i} dA_kk[i][j] k_jc e^{G_ic-G_jc}
 //   cq_jc = sum_{i>=j} dA_qk[i][j] q_ic e^{G_ic-G_jc},   ck_jc = sum_{i>j} dA_kk[i][j] beta_i k_ic e^{G_ic-G_jc}
-// as tensor-core products, block by block of 16 tokens with the forward's factorisation around E_b, G at
-// the block's last token (the -5 bound keeps every factor within fp32: "月之暗面发布Kimi K3开源大模型
-// 技术报告", 架构): for rows i of block b, e^{G_i-G_j} = e^{G_i-E_b} e^{E_b-G_j} with the second factor
-// at most 1 for j <= 16b+15, so the column operand k e^{E_b-G} (zero past the block) times dA_qk^T and
-// dA_kk^T gives rq and rk of the block's rows up to e^{G_i-E_b}; for columns j of block b the row operands
-// q e^{G-E_b} and beta k e^{G-E_b} (zero before the block) give cq and ck up to e^{E_b-G_j}.  Every product
-// is taken transposed, channels as M = 128, and from three-piece bf16 splits (x = p1 + p2 + p3 to about
+// as tensor-core products over blocks of 16 tokens.  E_b is G at block b's last token; the -5 bound on g keeps
+// e^{+-(G_t - E_b)} for t in block b within fp32 ("月之暗面发布Kimi K3开源大模型技术报告", 架构).  With the
+// block operands
+//   K_b[j] = k_j e^{E_b - G_j},  Q_b[i] = q_i e^{G_i - E_b},  B_b[i] = beta_i k_i e^{G_i - E_b}  (t in block b)
+// and, for blocks x >= y, the per-channel factor s_xy = e^{E_x - E_y} <= 1:
+//   rq_i = e^{G_i - E_b} sum_{y <= b} s_by (K_y^T dA_qk[block b rows][block y cols])_i      (i in block b)
+//   cq_j = e^{E_b - G_j} sum_{x >= b} s_xb (Q_x^T dA_qk[block x rows][block b cols])_j      (j in block b)
+// and rk, ck alike with dA_kk and B_x.  Each operand is therefore built once, and every block pair is one
+// 128 x 16 x 16 product (channels as M = 128), taken from three-piece bf16 splits (x = p1 + p2 + p3 to about
 // 2^-27; p1p1 + p1p2 + p2p1 + p1p3 + p3p1 + p2p2): the gradient of G is a difference of these sums, where a
-// two-piece split (2^-17) would leave too little.  Then, per (i, c), the element-wise part of
-// bwd_chunk_b_kernel: dq, dk, the gradient of G, dbeta's second term (a part per channel half) and dg as the
-// reverse running sum of the G gradient inside the chunk.  Only the rows a block's products reach are built and
-// multiplied: the column operand of block b is zero past 16b+15, the row operands before 16b.
+// two-piece split (2^-17) leaves too little.  The pairs land in their own TMEM columns and the epilogue weighs
+// them in fp32.  Then, per (i, c), the element-wise part of bwd_chunk_b_kernel: dq, dk, the gradient of G,
+// dbeta's second term (a part per channel half) and dg as the reverse running sum of the G gradient.
 constexpr int kBThreads = 512;
 constexpr uint32_t B_AR = 0;          // [dA_qk ; dA_kk]: [128 rows i][64 j], three pieces of 16 KB
-constexpr uint32_t B_OP = 49152;      // the block's operand (k e^{E_b-G}, q e^{G-E_b} or beta k e^{G-E_b}):
-                                      // [64 rows][128 c] (two regions of [64][64]), three pieces of 16 KB
-constexpr uint32_t B_G = 98304;       // G (log2 units) fp32 [64][128]
-constexpr uint32_t B_Q = 131072;      // q, k bf16 [64][128] each
-constexpr uint32_t B_K = 147456;
-constexpr uint32_t B_DG = 163840;     // the gradient of G, fp32 [64][128]
-constexpr uint32_t B_BETA = 196608;   // beta [64]
-constexpr uint32_t B_LAST = 196864;   // per (row group, channel): sum over its rows of xr k e^{G_last - G}, fp32 [4][128]
-constexpr uint32_t B_DBP = 198912;    // dbeta parts per (row, lane quarter): fp32 [64][4]
-constexpr uint32_t B_BAR = 199936;
-constexpr uint32_t B_MISC = B_BAR + 16;
+constexpr uint32_t B_OPA = 49152;     // K then B operands: [64 rows][128 c] (two regions of [64][64]), three
+constexpr uint32_t B_OPB = 98304;     // pieces of 16 KB; Q operand
+constexpr uint32_t B_G = 147456;      // G (log2 units) fp32 [64][128]
+constexpr uint32_t B_TOT = 180224;    // dG totals of the 16 four-row groups, fp32 [16][128]
+constexpr uint32_t B_BETA = 188416;   // beta [64]
+constexpr uint32_t B_LAST = 188672;   // per (row group, channel): sum over its rows of xr k e^{G_last - G}, fp32 [4][128]
+constexpr uint32_t B_DBP = 190720;    // dbeta parts per (row, lane quarter): fp32 [64][4]
+constexpr uint32_t B_BAR = 191744;    // three mbarriers
+constexpr uint32_t B_MISC = B_BAR + 32;
 constexpr uint32_t kBSmem = B_MISC + 16 + 1024;
-constexpr uint32_t B_T1 = 0, B_T2 = 64, B_T3 = 128, B_T4 = 192;  // TMEM: rq^T, rk^T, cq^T, ck^T [c][row]
+// TMEM columns, 16 per block pair: RQ (b, y <= b) at 16 (b (b+1)/2 + y), RK at 160 + the same; CQ (b, x >= b)
+// at 320 + 16 (4b - b (b-1)/2 + x - b); CK at 0 + the same (after RQ has been read)
+constexpr uint32_t B_RK = 160, B_CQ = 320;
+__host__ __device__ constexpr int pair_lo(int b, int y) { return b * (b + 1) / 2 + y; }
+__host__ __device__ constexpr int pair_hi(int b, int x) { return 4 * b - b * (b - 1) / 2 + x - b; }
 
 __device__ __forceinline__ float ex2f(float x) {
     float y;
@@ -975,6 +978,54 @@ __device__ __forceinline__ void put_3(uint8_t* base, uint32_t at, uint32_t tile,
     *reinterpret_cast<uint4*>(base + at) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
     *reinterpret_cast<uint4*>(base + at + tile) = make_uint4(p2[0], p2[1], p2[2], p2[3]);
     *reinterpret_cast<uint4*>(base + at + 2 * tile) = make_uint4(p3[0], p3[1], p3[2], p3[3]);
+}
+
+// One block operand (kOp 0: K_b, 1: Q_b, 2: B_b) of the chunk's 64 rows into `dst`; thread (row, 8 channels),
+// two per thread.  Rows past the sequence's end are zero.
+template <int kOp>
+__device__ __forceinline__ void build_operand(uint8_t* sm, uint32_t dst, const __nv_bfloat16* __restrict__ x,  // the head's row 0
+                                              int64_t row0, int64_t row_stride, int L, int tid) {
+    const float* sG = reinterpret_cast<const float*>(sm + B_G);
+    const float* sBeta = reinterpret_cast<const float*>(sm + B_BETA);
+    uint4 xv[2];
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        const int idx = tid + kBThreads * it, r = idx >> 4, c8 = idx & 15;
+        xv[it] = make_uint4(0, 0, 0, 0);
+        if (r < L) xv[it] = *reinterpret_cast<const uint4*>(x + (row0 + r) * row_stride + 8 * c8);
+    }
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        const int idx = tid + kBThreads * it, r = idx >> 4, c8 = idx & 15;
+        const uint32_t xw[4] = {xv[it].x, xv[it].y, xv[it].z, xv[it].w};
+        const float* gr = sG + r * kD + 8 * c8;
+        const float* er = sG + (16 * (r >> 4) + 15) * kD + 8 * c8;
+        const float4 g0 = *reinterpret_cast<const float4*>(gr), g1 = *reinterpret_cast<const float4*>(gr + 4);
+        const float4 e0 = *reinterpret_cast<const float4*>(er), e1 = *reinterpret_cast<const float4*>(er + 4);
+        const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+        const float br = kOp == 2 ? sBeta[r] : 1.f;
+        float val[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float xe = (e & 1) ? bf16_hi(xw[e >> 1]) : bf16_lo(xw[e >> 1]);
+            const float f = kOp == 0 ? ex2f(ev[e] - gv[e]) : ex2f(gv[e] - ev[e]);
+            val[e] = kOp == 2 ? (br * xe) * f : xe * f;
+        }
+        put_3(sm + dst, (uint32_t)(c8 >> 3) * 8192u + sw128((uint32_t)r, (uint32_t)(c8 & 7)), 16384, val);
+    }
+}
+
+// Sum over the warp's 32 lanes of four values v[0..3]; lane l returns the total of v[(l >> 3) & 3].
+__device__ __forceinline__ float warp_sum4(const float (&v)[4], int lane) {
+    const bool u16 = lane & 16, u8 = lane & 8;
+    float w0 = (u16 ? v[2] : v[0]) + __shfl_xor_sync(0xFFFFFFFFu, u16 ? v[0] : v[2], 16);
+    float w1 = (u16 ? v[3] : v[1]) + __shfl_xor_sync(0xFFFFFFFFu, u16 ? v[1] : v[3], 16);
+    float w = (u8 ? w1 : w0) + __shfl_xor_sync(0xFFFFFFFFu, u8 ? w0 : w1, 8);
+    w += __shfl_xor_sync(0xFFFFFFFFu, w, 4);
+    w += __shfl_xor_sync(0xFFFFFFFFu, w, 2);
+    w += __shfl_xor_sync(0xFFFFFFFFu, w, 1);
+    return w;
 }
 
 __global__ void __launch_bounds__(kBThreads, 1)
@@ -1006,29 +1057,33 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     if (slot < bos / kC + n || c0 >= eos) return;
     const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
     const int64_t base = slot * H + h;
+    const int64_t rs = (int64_t)H * kD;  // row stride of q, k, g and the per-channel tensors
+    const int64_t hoff = (int64_t)h * kD;
     constexpr float kLog2e = 1.4426950408889634f;
     float* sG = reinterpret_cast<float*>(sm + B_G);
-    float* sDG = reinterpret_cast<float*>(sm + B_DG);
-    const __nv_bfloat16* sQ = reinterpret_cast<const __nv_bfloat16*>(sm + B_Q);
-    const __nv_bfloat16* sK = reinterpret_cast<const __nv_bfloat16*>(sm + B_K);
+    float* sTot = reinterpret_cast<float*>(sm + B_TOT);
     float* sBeta = reinterpret_cast<float*>(sm + B_BETA);
     float* sLast = reinterpret_cast<float*>(sm + B_LAST);
     float* sDBP = reinterpret_cast<float*>(sm + B_DBP);
-    uint64_t* bM = reinterpret_cast<uint64_t*>(sm + B_BAR);
+    uint64_t* bM = reinterpret_cast<uint64_t*>(sm + B_BAR);  // [0] K products, [1] Q products, [2] B products
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + B_MISC);
     if (tid == 0) {
         mbar_init(bM, 1);
+        mbar_init(bM + 1, 1);
+        mbar_init(bM + 2, 1);
         fence_mbar_init();
     }
-    if (warp == 0) tmem_alloc(sTmem, 256);
-    if (tid < kC) sBeta[tid] = tid < L ? beta[(c0 + tid) * H + h] : 0.f;
-    // ---- q, k rows (zero past the sequence's end): thread (row, 16-byte chunk), two per tensor
-    for (int idx = tid; idx < 2 * kC * 16; idx += kBThreads) {
-        const int which = idx >> 10, r = (idx >> 4) & 63, c8 = idx & 15;
-        uint4 xv = make_uint4(0, 0, 0, 0);
-        if (r < L) xv = *reinterpret_cast<const uint4*>((which ? k : q) + ((c0 + r) * H + h) * kD + 8 * c8);
-        *reinterpret_cast<uint4*>(sm + (which ? B_K : B_Q) + r * 256 + 16 * c8) = xv;
+    if (warp == 0) tmem_alloc(sTmem, 512);
+    // the epilogue's per-token inputs and q, k on their way to L2 (two 128-byte lines of five tiles per thread)
+    for (int idx = tid; idx < 5 * kC * 4; idx += kBThreads) {
+        const int which = idx >> 8, r = (idx >> 2) & 63, part = idx & 3;
+        if (r < L) {
+            const int64_t at = (c0 + r) * rs + hoff;
+            if (which < 3) prefetch_l2((which == 0 ? XQ : which == 1 ? XK : XR) + at + 32 * part);
+            else if (part < 2) prefetch_l2((which == 3 ? q : k) + at + 64 * part);
+        }
     }
+    if (tid < kC) sBeta[tid] = tid < L ? beta[(c0 + tid) * H + h] : 0.f;
     // ---- G: running sum of g per channel (log2 units), thread (c, half): tokens 32 half .. +31
     if (tid < 256) {
         const int c = tid & 127, hh = tid >> 7;
@@ -1036,7 +1091,7 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
 #pragma unroll
         for (int r = 0; r < 32; ++r) {
             const int t = 32 * hh + r;
-            gv[r] = t < L ? g[((c0 + t) * H + h) * kD + c] * kLog2e : 0.f;
+            gv[r] = t < L ? g[(c0 + t) * rs + hoff + c] * kLog2e : 0.f;
         }
 #pragma unroll
         for (int r = 1; r < 32; ++r) gv[r] += gv[r - 1];
@@ -1044,12 +1099,22 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
         for (int r = 0; r < 32; ++r) sG[(32 * hh + r) * kD + c] = gv[r];
     }
     // ---- dA_qk (rows 0-63), dA_kk (rows 64-127) as three bf16 pieces
-    for (int idx = tid; idx < 2 * kC * 8; idx += kBThreads) {  // row m, columns 8 j8 ..
-        const int m = idx >> 3, j8 = idx & 7;
-        const float* src = (m < kC ? dAqk + (base * kC + m) * kC : dAkk + (base * kC + m - kC) * kC) + 8 * j8;
-        const float4 a = *reinterpret_cast<const float4*>(src), b = *reinterpret_cast<const float4*>(src + 4);
-        const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        put_3(sm + B_AR, sw128((uint32_t)m, (uint32_t)j8), 16384, x);
+    {
+        float4 av[2][2];
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int idx = tid + kBThreads * it, m = idx >> 3, j8 = idx & 7;
+            const float* src = (m < kC ? dAqk + (base * kC + m) * kC : dAkk + (base * kC + m - kC) * kC) + 8 * j8;
+            av[it][0] = *reinterpret_cast<const float4*>(src);
+            av[it][1] = *reinterpret_cast<const float4*>(src + 4);
+        }
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {
+            const int idx = tid + kBThreads * it, m = idx >> 3, j8 = idx & 7;
+            const float x[8] = {av[it][0].x, av[it][0].y, av[it][0].z, av[it][0].w,
+                                av[it][1].x, av[it][1].y, av[it][1].z, av[it][1].w};
+            put_3(sm + B_AR, sw128((uint32_t)m, (uint32_t)j8), 16384, x);
+        }
     }
     __syncthreads();
     if (tid >= 128 && tid < 256) {  // the second half's running sum continues from the first's total
@@ -1060,158 +1125,202 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     }
     __syncthreads();
     const uint32_t tbase = *sTmem;
-    const uint32_t id_k = idesc_bf16_f32(128, 64, true, false);  // A = operand^T (MN-major), B = dA rows (K-major)
-    const uint32_t id_m = idesc_bf16_f32(128, 64, true, true);   // A = operand^T, B = dA columns (MN-major)
+    const uint32_t id_k = idesc_bf16_f32(128, 16, true, false);  // A = operand^T (MN-major), B = dA rows (K-major)
+    const uint32_t id_m = idesc_bf16_f32(128, 16, true, true);   // A = operand^T, B = dA columns (MN-major)
     // pieces (of the operand, of dA) of the six products p: nibble p of kPa, kPb
     // (11, 12, 21, 13, 31, 22 in one-based pieces)
     constexpr uint32_t kPa = 0x120100u, kPb = 0x102010u;
-    uint32_t phase = 0;
-    const int qr = warp & 3, rg = warp >> 2;  // lane quarter (channels 32 qr ..), row group of the epilogue
-    const int c_me = 32 * qr + lane;
-    const int c8_me = tid & 15;               // the operand builder's 8 channels
-    float last_acc = 0.f;
+    // ---- K operand, then its products: RQ and RK of every pair (b, y <= b)
+    build_operand<0>(sm, B_OPA, k + hoff, c0, rs, L, tid);
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) {
+#pragma unroll 1
+        for (int p = 0; p < 6; ++p) {
+            const uint64_t ad = sdesc_sw128(sbase + B_OPA + 16384 * ((kPa >> (4 * p)) & 15u), 8192, 1024);
+            const uint32_t bt = sbase + B_AR + 16384 * ((kPb >> (4 * p)) & 15u);
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+#pragma unroll
+                for (int y = 0; y <= b; ++y) {
+                    mma_bf16(tbase + 16 * pair_lo(b, y), ad + y * 128, kdesc(bt + 2048 * b) + y * 2, id_k, p ? 1u : 0u);
+                    mma_bf16(tbase + B_RK + 16 * pair_lo(b, y), ad + y * 128, kdesc(bt + 8192 + 2048 * b) + y * 2,
+                             id_k, p ? 1u : 0u);
+                }
+        }
+        mma_commit(bM);
+    }
+    // ---- Q operand, then CQ of every pair (b, x >= b)
+    build_operand<1>(sm, B_OPB, q + hoff, c0, rs, L, tid);
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) {
+#pragma unroll 1
+        for (int p = 0; p < 6; ++p) {
+            const uint64_t ad = sdesc_sw128(sbase + B_OPB + 16384 * ((kPa >> (4 * p)) & 15u), 8192, 1024);
+            const uint32_t bt = sbase + B_AR + 16384 * ((kPb >> (4 * p)) & 15u);
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+#pragma unroll
+                for (int x = b; x < 4; ++x)
+                    mma_bf16(tbase + B_CQ + 16 * pair_hi(b, x), ad + x * 128,
+                             sdesc_sw128(bt + 2048 * x + 32 * b, 8192, 1024), id_m, p ? 1u : 0u);
+        }
+        mma_commit(bM + 1);
+    }
+    // ---- first epilogue: thread (channel c, row group rg), rows 16 b + 4 rg + a
+    const int qr = warp & 3, rg = warp >> 2;
+    const int c = 32 * qr + lane;
+    const uint32_t lb = (uint32_t)(32 * qr) << 16;
+    float E[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) E[b] = sG[(16 * b + 15) * kD + c];
+    float sf[4][4];  // s_xy = e^{E_x - E_y}, x >= y
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y <= x; ++y) sf[x][y] = ex2f(E[x] - E[y]);
+    const float Gl = sG[(kC - 1) * kD + c];
+    float dkp[16], dGp[16], last_acc = 0.f;
+    if (!mbar_wait(bM, 0, kWaitLimit)) raise_device_error(err, kErrMbarTimeout);
+    tc_fence_after();
+#pragma unroll
     for (int b = 0; b < 4; ++b) {
-        // the element-wise part's inputs, fetched while the block's products are formed
-        const int i0 = 16 * b + 4 * rg;
-        float xq[4], xk[4], xr[4];
+        uint32_t tq[4][4], tk[4][4];
+#pragma unroll
+        for (int y = 0; y <= b; ++y) {
+            tmem_ld4_async(tbase + lb + 16 * pair_lo(b, y) + 4 * rg, tq[y]);
+            tmem_ld4_async(tbase + lb + B_RK + 16 * pair_lo(b, y) + 4 * rg, tk[y]);
+        }
+        tmem_wait_ld();
+#pragma unroll
+        for (int y = 0; y <= b; ++y) { reg_fence(tq[y]); reg_fence(tk[y]); }
+        float dbv[4];
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
-            const int64_t at = ((c0 + i0 + a) * H + h) * kD + c_me;
-            const bool in = i0 + a < L;
-            xq[a] = in ? XQ[at] : 0.f;
-            xk[a] = in ? XK[at] : 0.f;
-            xr[a] = in ? XR[at] : 0.f;
-        }
-        float eb8[8];
+            const int i = 16 * b + 4 * rg + a, m = 4 * b + a;
+            float sq = 0.f, sk = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) eb8[e] = sG[(16 * b + 15) * kD + 8 * c8_me + e];
-        // three stages: 0 the column operand k e^{E_b-G}, rows 0 .. 16b+15 -> rq^T, rk^T;
-        // 1 q e^{G-E_b}, rows 16b .. 63 -> cq^T; 2 beta k e^{G-E_b}, rows 16b .. 63 -> ck^T
-#pragma unroll 1
-        for (int stage = 0; stage < 3; ++stage) {
-            const int r0 = stage == 0 ? 0 : 16 * b, rows = stage == 0 ? 16 * (b + 1) : kC - 16 * b;
-            for (int idx = tid; idx < rows * 16; idx += kBThreads) {  // row r, channels 8 c8_me .. +7
-                const int r = r0 + (idx >> 4);
-                const uint4 xv = *reinterpret_cast<const uint4*>(sm + (stage == 1 ? B_Q : B_K) + r * 256 + 16 * c8_me);
-                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                const float br = stage == 2 ? sBeta[r] : 1.f;
-                const float4 ga = *reinterpret_cast<const float4*>(sG + r * kD + 8 * c8_me);
-                const float4 gb = *reinterpret_cast<const float4*>(sG + r * kD + 8 * c8_me + 4);
-                const float gr[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-                float val[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float x = (e & 1) ? bf16_hi(xw[e >> 1]) : bf16_lo(xw[e >> 1]);
-                    val[e] = stage == 0 ? x * ex2f(eb8[e] - gr[e]) : br * x * ex2f(gr[e] - eb8[e]);
-                }
-                put_3(sm + B_OP, (uint32_t)(c8_me >> 3) * 8192u + sw128((uint32_t)r, (uint32_t)(c8_me & 7)), 16384, val);
+            for (int y = 0; y <= b; ++y) {
+                sq = fmaf(sf[b][y], __uint_as_float(tq[y][a]), sq);
+                sk = fmaf(sf[b][y], __uint_as_float(tk[y][a]), sk);
             }
-            fence_proxy_async();
-            tc_fence_before();
-            __syncthreads();
-            tc_fence_after();
-            if (warp == 0) {
-                const int ks0 = stage == 0 ? 0 : b, ks1 = stage == 0 ? b : 3;
-#pragma unroll 1
-                for (int p = 0; p < 6; ++p) {
-                    const uint64_t ad = sdesc_sw128(sbase + B_OP + 16384 * ((kPa >> (4 * p)) & 15u), 8192, 1024);
-                    const uint32_t bt = sbase + B_AR + 16384 * ((kPb >> (4 * p)) & 15u);
-                    if (stage == 0) {
-                        for (int ks = ks0; ks <= ks1; ++ks)
-                            mma_bf16(tbase + B_T1, ad + ks * 128, kdesc(bt) + ks * 2, id_k, (p || ks > ks0) ? 1u : 0u);
-                        for (int ks = ks0; ks <= ks1; ++ks)
-                            mma_bf16(tbase + B_T2, ad + ks * 128, kdesc(bt + 8192) + ks * 2, id_k,
-                                     (p || ks > ks0) ? 1u : 0u);
-                    } else {
-                        const uint64_t bd = sdesc_sw128(bt + (stage == 2 ? 8192 : 0), 8192, 1024);
-                        const uint32_t dst = tbase + (stage == 1 ? B_T3 : B_T4);
-                        for (int ks = ks0; ks <= ks1; ++ks)
-                            mma_bf16(dst, ad + ks * 128, bd + ks * 128, id_m, (p || ks > ks0) ? 1u : 0u);
-                    }
-                }
-                mma_commit(bM);
+            dkp[m] = 0.f;
+            dGp[m] = 0.f;
+            dbv[a] = 0.f;
+            if (i < L) {
+                const int64_t at = (c0 + i) * rs + hoff + c;
+                const float qi = __bfloat162float(q[at]), ki = __bfloat162float(k[at]);
+                const float xq = XQ[at], xk = XK[at], xr = XR[at], bi = sBeta[i];
+                const float Gi = sG[i * kD + c];
+                const float up = ex2f(Gi - E[b]);
+                const float rq = up * sq, rk = up * sk;
+                const float gam = ex2f(Gi), red = ex2f(fminf(Gl - Gi, 0.f));
+                dq[at] = fmaf(xq, gam, rq);
+                dkp[m] = bi * rk + xk * gam + xr * red;
+                dGp[m] = qi * rq + ki * bi * rk + (xq * qi + xk * ki) * gam - xr * ki * red;
+                last_acc = fmaf(xr * ki, red, last_acc);
+                dbv[a] = ki * rk;
             }
-            if (tid == 0 && !mbar_wait(bM, phase, kWaitLimit)) raise_device_error(err, kErrMbarTimeout);
-            phase ^= 1u;
-            tc_fence_before();
-            __syncthreads();
-            tc_fence_after();
         }
-        // ---- the element-wise part: thread (channel c_me, rows i0 .. i0 + 3)
-        {
-            const uint32_t lb = (uint32_t)(32 * qr) << 16;
-            uint32_t t1[4], t2[4], t3[4], t4[4];
-            tmem_ld4_async(tbase + lb + B_T1 + i0, t1);
-            tmem_ld4_async(tbase + lb + B_T2 + i0, t2);
-            tmem_ld4_async(tbase + lb + B_T3 + i0, t3);
-            tmem_ld4_async(tbase + lb + B_T4 + i0, t4);
-            tmem_wait_ld(); reg_fence(t1); reg_fence(t2); reg_fence(t3); reg_fence(t4);
-            const int c = c_me;
-            const float Eb = sG[(16 * b + 15) * kD + c], Gl = sG[(kC - 1) * kD + c];
+        // dbeta's second term of rows 16 b + 4 rg + a: this warp's 32 channels, in a fixed order
+        const float tot = warp_sum4(dbv, lane);
+        if ((lane & 7) == 0) sDBP[(16 * b + 4 * rg + ((lane >> 3) & 3)) * 4 + qr] = tot;
+    }
+    sLast[rg * kD + c] = last_acc;
+    // ---- B operand (the K operand's products are complete), then CK of every pair into RQ's columns
+    build_operand<2>(sm, B_OPA, k + hoff, c0, rs, L, tid);
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) {
+#pragma unroll 1
+        for (int p = 0; p < 6; ++p) {
+            const uint64_t ad = sdesc_sw128(sbase + B_OPA + 16384 * ((kPa >> (4 * p)) & 15u), 8192, 1024);
+            const uint32_t bt = sbase + B_AR + 8192 + 16384 * ((kPb >> (4 * p)) & 15u);
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+#pragma unroll
+                for (int x = b; x < 4; ++x)
+                    mma_bf16(tbase + 16 * pair_hi(b, x), ad + x * 128, sdesc_sw128(bt + 2048 * x + 32 * b, 8192, 1024),
+                             id_m, p ? 1u : 0u);
+        }
+        mma_commit(bM + 2);
+    }
+    // the last token's extra: every row's xr k e^{G_last - G}, and dgamma e^{G_last}
+    const float extra = ((sLast[c] + sLast[kD + c]) + (sLast[2 * kD + c] + sLast[3 * kD + c])) +
+                        dgam[base * kD + c] * ex2f(Gl);
+    if (!mbar_wait(bM + 1, 0, kWaitLimit)) raise_device_error(err, kErrMbarTimeout);
+    if (!mbar_wait(bM + 2, 0, kWaitLimit)) raise_device_error(err, kErrMbarTimeout);
+    tc_fence_after();
+    // ---- second epilogue: cq + ck, dk, the G gradient; its running sums inside each four-row group
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        uint32_t tq[4][4], tk[4][4];
+#pragma unroll
+        for (int x = b; x < 4; ++x) {
+            tmem_ld4_async(tbase + lb + B_CQ + 16 * pair_hi(b, x) + 4 * rg, tq[x - b]);
+            tmem_ld4_async(tbase + lb + 16 * pair_hi(b, x) + 4 * rg, tk[x - b]);
+        }
+        tmem_wait_ld();
+#pragma unroll
+        for (int x = b; x < 4; ++x) { reg_fence(tq[x - b]); reg_fence(tk[x - b]); }
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const int j = 16 * b + 4 * rg + a, m = 4 * b + a;
+            float sc = 0.f;
+#pragma unroll
+            for (int x = b; x < 4; ++x)
+                sc = fmaf(sf[x][b], __uint_as_float(tq[x - b][a]) + __uint_as_float(tk[x - b][a]), sc);
+            if (j < L) {
+                const int64_t at = (c0 + j) * rs + hoff + c;
+                const float kj = __bfloat162float(k[at]);
+                const float cs = ex2f(E[b] - sG[j * kD + c]) * sc;  // cq + ck
+                dk[at] = dkp[m] + cs;
+                dGp[m] -= kj * cs;
+            }
+        }
+        // running sum from the group's last row; the group total goes to shared memory
+        dGp[4 * b + 2] += dGp[4 * b + 3];
+        dGp[4 * b + 1] += dGp[4 * b + 2];
+        dGp[4 * b] += dGp[4 * b + 1];
+        sTot[(4 * b + rg) * kD + c] = dGp[4 * b];
+    }
+    tc_fence_before();
+    __syncthreads();
+    // ---- dg_t = sum_{s >= t} dG_s inside the chunk, with the extra at the last token (so in every dg_t);
+    //      G_t is the sum of g_s for s <= t and the factors above are natural exponentials, so dG is the
+    //      gradient with respect to G in natural units
+    {
+        // totals of groups 4 b + rg + 1 .. 15, for each b, in a fixed order (from the chunk's end)
+        float suff[4] = {0.f, 0.f, 0.f, 0.f};
+        float acc = 0.f;
+#pragma unroll
+        for (int gi = 15; gi >= 0; --gi) {
+            const int bb = gi >> 2, r2 = gi & 3;
+            if (r2 == rg) suff[bb] = acc;
+            acc += sTot[gi * kD + c];
+        }
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
-                const int i = i0 + a;
-                float dbp = 0.f, dG = 0.f;
-                if (i < L) {
-                    const int64_t at = ((c0 + i) * H + h) * kD + c;
-                    const float qi = __bfloat162float(sQ[i * kD + c]), ki = __bfloat162float(sK[i * kD + c]);
-                    const float bi = sBeta[i];
-                    const float Gi = sG[i * kD + c];
-                    const float up = ex2f(Gi - Eb), down = ex2f(Eb - Gi);
-                    const float rq = up * __uint_as_float(t1[a]), rk = up * __uint_as_float(t2[a]);
-                    const float cs = down * (__uint_as_float(t3[a]) + __uint_as_float(t4[a]));  // cq + ck
-                    const float gam = ex2f(Gi), red = ex2f(fminf(Gl - Gi, 0.f));
-                    dq[at] = fmaf(xq[a], gam, rq);
-                    dk[at] = bi * rk + xk[a] * gam + xr[a] * red + cs;
-                    dG = qi * rq + ki * bi * rk + (xq[a] * qi + xk[a] * ki) * gam - xr[a] * ki * red - ki * cs;
-                    last_acc = fmaf(xr[a] * ki, red, last_acc);
-                    dbp = ki * rk;
-                }
-                sDG[i * kD + c] = dG;
-                // dbeta's second term of row i: this warp's 32 channels, in a fixed order
-#pragma unroll
-                for (int o2 = 16; o2 > 0; o2 >>= 1) dbp += __shfl_xor_sync(0xFFFFFFFFu, dbp, o2);
-                if (lane == 0) sDBP[i * 4 + qr] = dbp;
+                const int t = 16 * b + 4 * rg + a;
+                if (t < L) dg[(c0 + t) * rs + hoff + c] = dGp[4 * b + a] + (suff[b] + extra);
             }
-        }
-    }
-    sLast[rg * kD + c_me] = last_acc;
-    __syncthreads();
-    // ---- the last token's extra (every row's xr k e^{G_last - G} and dgamma e^{G_last}); G_t is the sum of g_s for
-    //      s <= t and the factors above are natural exponentials, so sDG is the gradient with respect to G in
-    //      natural units
-    if (tid < kD && L > 0) {
-        const int c = tid;
-        sDG[(L - 1) * kD + c] += (sLast[c] + sLast[kD + c] + sLast[2 * kD + c] + sLast[3 * kD + c]) +
-                                 dgam[base * kD + c] * ex2f(sG[(kC - 1) * kD + c]);
     }
     if (tid < L) {  // channel half 0 = lane quarters 0, 1; half 1 = 2, 3
         dbeta_part[(c0 + tid) * H + h] = sDBP[tid * 4] + sDBP[tid * 4 + 1];
         dbeta_part[(T_total + c0 + tid) * H + h] = sDBP[tid * 4 + 2] + sDBP[tid * 4 + 3];
     }
-    __syncthreads();
-    // ---- dg_t = sum_{s >= t} dG_s inside the chunk: thread (channel, quarter of 16 tokens) sums its own
-    //      tokens from the end, then adds the totals of the later quarters
-    {
-        const int c = tid & 127, pq = tid >> 7;
-        float acc = 0.f;
-#pragma unroll
-        for (int t = 15; t >= 0; --t) {
-            acc += sDG[(16 * pq + t) * kD + c];
-            sDG[(16 * pq + t) * kD + c] = acc;
-        }
-        __syncthreads();
-        float off = 0.f;
-        for (int p2 = 3; p2 > pq; --p2) off += sDG[(16 * p2) * kD + c];
-#pragma unroll 4
-        for (int t = 0; t < 16; ++t) {
-            const int r = 16 * pq + t;
-            if (r < L) dg[((c0 + r) * H + h) * kD + c] = sDG[r * kD + c] + off;
-        }
-    }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 256);
+    if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
