@@ -949,12 +949,12 @@ constexpr uint32_t B_TOT = 180224;    // dG totals of the 16 four-row groups, fp
 constexpr uint32_t B_BETA = 188416;   // beta [64]
 constexpr uint32_t B_LAST = 188672;   // per (row group, channel): sum over its rows of xr k e^{G_last - G}, fp32 [4][128]
 constexpr uint32_t B_DBP = 190720;    // dbeta parts per (row, lane quarter): fp32 [64][4]
-constexpr uint32_t B_BAR = 191744;    // three mbarriers
+constexpr uint32_t B_BAR = 191744;    // two mbarriers
 constexpr uint32_t B_MISC = B_BAR + 32;
 constexpr uint32_t kBSmem = B_MISC + 16 + 1024;
-// TMEM columns, 16 per block pair: RQ (b, y <= b) at 16 (b (b+1)/2 + y), RK at 160 + the same; CQ (b, x >= b)
-// at 320 + 16 (4b - b (b-1)/2 + x - b); CK at 0 + the same (after RQ has been read)
-constexpr uint32_t B_RK = 160, B_CQ = 320;
+// TMEM columns, 16 per block pair: RQ (b, y <= b) at 16 (b (b+1)/2 + y), RK at 160 + the same; CQ + CK (b, x >= b)
+// at 320 + 16 (4b - b (b-1)/2 + x - b): cq and ck carry the same weights, so their products share columns
+constexpr uint32_t B_RK = 160, B_CS = 320;
 __host__ __device__ constexpr int pair_lo(int b, int y) { return b * (b + 1) / 2 + y; }
 __host__ __device__ constexpr int pair_hi(int b, int x) { return 4 * b - b * (b - 1) / 2 + x - b; }
 
@@ -1065,12 +1065,11 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     float* sBeta = reinterpret_cast<float*>(sm + B_BETA);
     float* sLast = reinterpret_cast<float*>(sm + B_LAST);
     float* sDBP = reinterpret_cast<float*>(sm + B_DBP);
-    uint64_t* bM = reinterpret_cast<uint64_t*>(sm + B_BAR);  // [0] K products, [1] Q products, [2] B products
+    uint64_t* bM = reinterpret_cast<uint64_t*>(sm + B_BAR);  // [0] the K operand's products, [1] every product
     uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + B_MISC);
     if (tid == 0) {
         mbar_init(bM, 1);
         mbar_init(bM + 1, 1);
-        mbar_init(bM + 2, 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(sTmem, 512);
@@ -1167,72 +1166,12 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
             for (int b = 0; b < 4; ++b)
 #pragma unroll
                 for (int x = b; x < 4; ++x)
-                    mma_bf16(tbase + B_CQ + 16 * pair_hi(b, x), ad + x * 128,
+                    mma_bf16(tbase + B_CS + 16 * pair_hi(b, x), ad + x * 128,
                              sdesc_sw128(bt + 2048 * x + 32 * b, 8192, 1024), id_m, p ? 1u : 0u);
         }
-        mma_commit(bM + 1);
     }
-    // ---- first epilogue: thread (channel c, row group rg), rows 16 b + 4 rg + a
-    const int qr = warp & 3, rg = warp >> 2;
-    const int c = 32 * qr + lane;
-    const uint32_t lb = (uint32_t)(32 * qr) << 16;
-    float E[4];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) E[b] = sG[(16 * b + 15) * kD + c];
-    float sf[4][4];  // s_xy = e^{E_x - E_y}, x >= y
-#pragma unroll
-    for (int x = 0; x < 4; ++x)
-#pragma unroll
-        for (int y = 0; y <= x; ++y) sf[x][y] = ex2f(E[x] - E[y]);
-    const float Gl = sG[(kC - 1) * kD + c];
-    float dkp[16], dGp[16], last_acc = 0.f;
+    // ---- B operand once the K operand's products are complete, then CK of every pair onto CQ's columns
     if (!mbar_wait(bM, 0, kWaitLimit)) raise_device_error(err, kErrMbarTimeout);
-    tc_fence_after();
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        uint32_t tq[4][4], tk[4][4];
-#pragma unroll
-        for (int y = 0; y <= b; ++y) {
-            tmem_ld4_async(tbase + lb + 16 * pair_lo(b, y) + 4 * rg, tq[y]);
-            tmem_ld4_async(tbase + lb + B_RK + 16 * pair_lo(b, y) + 4 * rg, tk[y]);
-        }
-        tmem_wait_ld();
-#pragma unroll
-        for (int y = 0; y <= b; ++y) { reg_fence(tq[y]); reg_fence(tk[y]); }
-        float dbv[4];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            const int i = 16 * b + 4 * rg + a, m = 4 * b + a;
-            float sq = 0.f, sk = 0.f;
-#pragma unroll
-            for (int y = 0; y <= b; ++y) {
-                sq = fmaf(sf[b][y], __uint_as_float(tq[y][a]), sq);
-                sk = fmaf(sf[b][y], __uint_as_float(tk[y][a]), sk);
-            }
-            dkp[m] = 0.f;
-            dGp[m] = 0.f;
-            dbv[a] = 0.f;
-            if (i < L) {
-                const int64_t at = (c0 + i) * rs + hoff + c;
-                const float qi = __bfloat162float(q[at]), ki = __bfloat162float(k[at]);
-                const float xq = XQ[at], xk = XK[at], xr = XR[at], bi = sBeta[i];
-                const float Gi = sG[i * kD + c];
-                const float up = ex2f(Gi - E[b]);
-                const float rq = up * sq, rk = up * sk;
-                const float gam = ex2f(Gi), red = ex2f(fminf(Gl - Gi, 0.f));
-                dq[at] = fmaf(xq, gam, rq);
-                dkp[m] = bi * rk + xk * gam + xr * red;
-                dGp[m] = qi * rq + ki * bi * rk + (xq * qi + xk * ki) * gam - xr * ki * red;
-                last_acc = fmaf(xr * ki, red, last_acc);
-                dbv[a] = ki * rk;
-            }
-        }
-        // dbeta's second term of rows 16 b + 4 rg + a: this warp's 32 channels, in a fixed order
-        const float tot = warp_sum4(dbv, lane);
-        if ((lane & 7) == 0) sDBP[(16 * b + 4 * rg + ((lane >> 3) & 3)) * 4 + qr] = tot;
-    }
-    sLast[rg * kD + c] = last_acc;
-    // ---- B operand (the K operand's products are complete), then CK of every pair into RQ's columns
     build_operand<2>(sm, B_OPA, k + hoff, c0, rs, L, tid);
     fence_proxy_async();
     tc_fence_before();
@@ -1247,63 +1186,106 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
             for (int b = 0; b < 4; ++b)
 #pragma unroll
                 for (int x = b; x < 4; ++x)
-                    mma_bf16(tbase + 16 * pair_hi(b, x), ad + x * 128, sdesc_sw128(bt + 2048 * x + 32 * b, 8192, 1024),
-                             id_m, p ? 1u : 0u);
+                    mma_bf16(tbase + B_CS + 16 * pair_hi(b, x), ad + x * 128,
+                             sdesc_sw128(bt + 2048 * x + 32 * b, 8192, 1024), id_m, 1u);
         }
-        mma_commit(bM + 2);
+        mma_commit(bM + 1);
     }
-    // the last token's extra: every row's xr k e^{G_last - G}, and dgamma e^{G_last}
-    const float extra = ((sLast[c] + sLast[kD + c]) + (sLast[2 * kD + c] + sLast[3 * kD + c])) +
-                        dgam[base * kD + c] * ex2f(Gl);
-    if (!mbar_wait(bM + 1, 0, kWaitLimit)) raise_device_error(err, kErrMbarTimeout);
-    if (!mbar_wait(bM + 2, 0, kWaitLimit)) raise_device_error(err, kErrMbarTimeout);
+    // ---- epilogue: thread (channel c, row group rg), rows 16 b + 4 rg + a
+    const int qr = warp & 3, rg = warp >> 2;
+    const int c = 32 * qr + lane;
+    const uint32_t lb = (uint32_t)(32 * qr) << 16;
+    float E[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) E[b] = sG[(16 * b + 15) * kD + c];
+    float sf[4][4];  // s_xy = e^{E_x - E_y}, x >= y
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+#pragma unroll
+        for (int y = 0; y <= x; ++y) sf[x][y] = ex2f(E[x] - E[y]);
+    const float Gl = sG[(kC - 1) * kD + c];
+    const uint16_t* k16 = reinterpret_cast<const uint16_t*>(k);
+    float dGs[16], last_acc = 0.f;  // the G gradient's running sums inside each four-row group
+    if (!mbar_wait(bM + 1, 0, kWaitLimit)) raise_device_error(err, kErrMbarTimeout);  // every product complete
     tc_fence_after();
-    // ---- second epilogue: cq + ck, dk, the G gradient; its running sums inside each four-row group
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-        uint32_t tq[4][4], tk[4][4];
-#pragma unroll
-        for (int x = b; x < 4; ++x) {
-            tmem_ld4_async(tbase + lb + B_CQ + 16 * pair_hi(b, x) + 4 * rg, tq[x - b]);
-            tmem_ld4_async(tbase + lb + 16 * pair_hi(b, x) + 4 * rg, tk[x - b]);
-        }
-        tmem_wait_ld();
-#pragma unroll
-        for (int x = b; x < 4; ++x) { reg_fence(tq[x - b]); reg_fence(tk[x - b]); }
+        // the block's per-token inputs, all loads issued together (rows past the end read the last row)
+        float xqv[4], xkv[4], xrv[4], qv[4], kv[4];
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
-            const int j = 16 * b + 4 * rg + a, m = 4 * b + a;
-            float sc = 0.f;
-#pragma unroll
-            for (int x = b; x < 4; ++x)
-                sc = fmaf(sf[x][b], __uint_as_float(tq[x - b][a]) + __uint_as_float(tk[x - b][a]), sc);
-            if (j < L) {
-                const int64_t at = (c0 + j) * rs + hoff + c;
-                const float kj = __bfloat162float(k[at]);
-                const float cs = ex2f(E[b] - sG[j * kD + c]) * sc;  // cq + ck
-                dk[at] = dkp[m] + cs;
-                dGp[m] -= kj * cs;
-            }
+            const int i = min(16 * b + 4 * rg + a, L - 1);
+            const int64_t at = (c0 + i) * rs + hoff + c;
+            xqv[a] = XQ[at];
+            xkv[a] = XK[at];
+            xrv[a] = XR[at];
+            qv[a] = __bfloat162float(q[at]);
+            kv[a] = __uint_as_float((uint32_t)k16[at] << 16);
         }
+        uint32_t tq[4][4], tk[4][4], ts[4][4];
+#pragma unroll
+        for (int y = 0; y <= b; ++y) {
+            tmem_ld4_async(tbase + lb + 16 * pair_lo(b, y) + 4 * rg, tq[y]);
+            tmem_ld4_async(tbase + lb + B_RK + 16 * pair_lo(b, y) + 4 * rg, tk[y]);
+        }
+#pragma unroll
+        for (int x = b; x < 4; ++x) tmem_ld4_async(tbase + lb + B_CS + 16 * pair_hi(b, x) + 4 * rg, ts[x - b]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int y = 0; y <= b; ++y) { reg_fence(tq[y]); reg_fence(tk[y]); }
+#pragma unroll
+        for (int x = b; x < 4; ++x) reg_fence(ts[x - b]);
+        float dbv[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const int i = 16 * b + 4 * rg + a, m = 4 * b + a;
+            float sq = 0.f, sk = 0.f, sc = 0.f;
+#pragma unroll
+            for (int y = 0; y <= b; ++y) {
+                sq = fmaf(sf[b][y], __uint_as_float(tq[y][a]), sq);
+                sk = fmaf(sf[b][y], __uint_as_float(tk[y][a]), sk);
+            }
+#pragma unroll
+            for (int x = b; x < 4; ++x) sc = fmaf(sf[x][b], __uint_as_float(ts[x - b][a]), sc);
+            const bool in = i < L;
+            const float qi = qv[a], ki = kv[a], xq = xqv[a], xk = xkv[a], xr = xrv[a], bi = sBeta[i];
+            const float Gi = sG[i * kD + c];
+            const float rq = ex2f(Gi - E[b]) * sq, rk = ex2f(Gi - E[b]) * sk;
+            const float cs = ex2f(E[b] - Gi) * sc;  // cq + ck
+            const float gam = ex2f(Gi), red = ex2f(fminf(Gl - Gi, 0.f));
+            const int64_t at = (c0 + i) * rs + hoff + c;
+            if (in) {
+                dq[at] = fmaf(xq, gam, rq);
+                dk[at] = bi * rk + xk * gam + xr * red + cs;
+                last_acc = fmaf(xr * ki, red, last_acc);
+            }
+            dGs[m] = in ? qi * rq + ki * bi * rk + (xq * qi + xk * ki) * gam - xr * ki * red - ki * cs : 0.f;
+            dbv[a] = in ? ki * rk : 0.f;
+        }
+        // dbeta's second term of rows 16 b + 4 rg + a: this warp's 32 channels, in a fixed order
+        const float tot = warp_sum4(dbv, lane);
+        if ((lane & 7) == 0) sDBP[(16 * b + 4 * rg + ((lane >> 3) & 3)) * 4 + qr] = tot;
         // running sum from the group's last row; the group total goes to shared memory
-        dGp[4 * b + 2] += dGp[4 * b + 3];
-        dGp[4 * b + 1] += dGp[4 * b + 2];
-        dGp[4 * b] += dGp[4 * b + 1];
-        sTot[(4 * b + rg) * kD + c] = dGp[4 * b];
+        dGs[4 * b + 2] += dGs[4 * b + 3];
+        dGs[4 * b + 1] += dGs[4 * b + 2];
+        dGs[4 * b] += dGs[4 * b + 1];
+        sTot[(4 * b + rg) * kD + c] = dGs[4 * b];
     }
+    sLast[rg * kD + c] = last_acc;
     tc_fence_before();
     __syncthreads();
-    // ---- dg_t = sum_{s >= t} dG_s inside the chunk, with the extra at the last token (so in every dg_t);
-    //      G_t is the sum of g_s for s <= t and the factors above are natural exponentials, so dG is the
-    //      gradient with respect to G in natural units
+    // ---- dg_t = sum_{s >= t} dG_s inside the chunk, with the last token's extra (every row's
+    //      xr k e^{G_last - G}, and dgamma e^{G_last}) in every dg_t.  G_t is the sum of g_s for s <= t and the
+    //      factors above are natural exponentials, so dG is the gradient with respect to G in natural units.
     {
+        const float extra = ((sLast[c] + sLast[kD + c]) + (sLast[2 * kD + c] + sLast[3 * kD + c])) +
+                            dgam[base * kD + c] * ex2f(Gl);
         // totals of groups 4 b + rg + 1 .. 15, for each b, in a fixed order (from the chunk's end)
         float suff[4] = {0.f, 0.f, 0.f, 0.f};
         float acc = 0.f;
 #pragma unroll
         for (int gi = 15; gi >= 0; --gi) {
-            const int bb = gi >> 2, r2 = gi & 3;
-            if (r2 == rg) suff[bb] = acc;
+            if ((gi & 3) == rg) suff[gi >> 2] = acc;
             acc += sTot[gi * kD + c];
         }
 #pragma unroll
@@ -1311,7 +1293,7 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
 #pragma unroll
             for (int a = 0; a < 4; ++a) {
                 const int t = 16 * b + 4 * rg + a;
-                if (t < L) dg[(c0 + t) * rs + hoff + c] = dGp[4 * b + a] + (suff[b] + extra);
+                if (t < L) dg[(c0 + t) * rs + hoff + c] = dGs[4 * b + a] + (suff[b] + extra);
             }
     }
     if (tid < L) {  // channel half 0 = lane quarters 0, 1; half 1 = 2, 3
