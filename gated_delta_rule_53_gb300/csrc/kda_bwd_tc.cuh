@@ -19,6 +19,12 @@ constexpr uint32_t kBB_GAM = 131072;    // gamma = e^{G_last}, fp32 [128]
 constexpr uint32_t kBB_BETA = 131584;   // beta, fp32 [64] (0 past the chunk's end)
 constexpr uint32_t kBwdBlobBytes = 131840;
 
+// Per (chunk, head) the tiles above (Kr, scale Qg, Kg, scale A_qk, T, gamma, beta) for bf16 q, k, with the
+// products A_qk and A_kk on the tensor cores; raises the gate and beta range bits of `err` as the forward does.
+cudaError_t launch_bwd_prep_tc(const void* q, const void* k, const float* g, const float* beta, const int32_t* cu_seqlens,
+                               int N, int64_t T_total, int H, float scale, void* blobs, unsigned int* err,
+                               cudaStream_t stream);
+
 // The forward pass along the chains on the tensor cores for bf16 v (v [T_total, H, 128]): the state entering
 // every chunk, R and V'; outputs as the CUDA-core pass.
 cudaError_t launch_bwd_fwd_state_tc(const void* v, const float* init_state, const int32_t* cu_seqlens, int N,

@@ -829,9 +829,14 @@ cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const 
     const dim3 grid((unsigned)n_slots(N, T_total), (unsigned)H);
     const dim3 chains((unsigned)((int64_t)N * H), kD / kSlice);
     if (T_total > 0) {
-        bwd_prep_kernel<InT><<<grid, kThreads, smP, stream>>>(qt, kt, g, beta, cu, N, T_total, H, scale, w.Qg, w.Kg,
-                                                              w.Kr, w.Aqk, w.T, w.gam, tc_state ? w.tc : nullptr);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (tc_state) {
+            e = launch_bwd_prep_tc(q, k, g, beta, cu, N, T_total, H, scale, w.tc, err, stream);
+        } else {
+            bwd_prep_kernel<InT><<<grid, kThreads, smP, stream>>>(qt, kt, g, beta, cu, N, T_total, H, scale, w.Qg,
+                                                                  w.Kg, w.Kr, w.Aqk, w.T, w.gam, nullptr);
+            e = cudaGetLastError();
+        }
+        if (e != cudaSuccess) return e;
         if (tc_state) {
             e = launch_bwd_fwd_state_tc(v, init_state, cu, N, T_total, H, w.tc, w.S0, w.R, w.Vp, err, stream);
         } else {

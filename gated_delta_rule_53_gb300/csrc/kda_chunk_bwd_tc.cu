@@ -25,6 +25,7 @@
 #include "kda_bwd_tc.cuh"
 #include "kda_common.cuh"
 #include "kda_tc.cuh"
+#include "kda_tsolve.cuh"
 
 namespace kda {
 namespace {
@@ -923,6 +924,276 @@ bwd_chunk_a_tc_kernel(const float* __restrict__ beta, const __nv_bfloat16* __res
     if (warp == 0) tmem_dealloc(tbase, 256);
 }
 
+// 2^x by the hardware approximation (results below 2^-126 flush to 0)
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ============================ per chunk: what does not depend on the state ============================
+// bwd_prep_tc_kernel: per (chunk, head) the tiles the tensor-core passes read, as bf16 hi + lo in their
+// layouts (kda_bwd_tc.cuh): Kr, scale Qg, Kg, gamma, beta, scale A_qk and T = (I + A_kk)^-1.  A_qk and A_kk
+// are one tensor-core product with the block factorisation of the decay around E_I, G at the last token of
+// 16-token block I ("月之暗面发布Kimi K3开源大模型技术报告", 架构: the -5 bound keeps the factors within fp32):
+// for rows i of block I and columns j <= 16 I + 15,
+//   e^{G_ic - G_jc} = e^{G_ic - E_Ic} e^{E_Ic - G_jc}     (the first factor >= 1, the second <= 1),
+// so the row operand [k ; q] e^{G - E_I} (M = 128) meets, per row block, its own column operand
+// k_j e^{E_I - G_j} (the four stacked, 16 + 32 + 48 + 64 = 160 rows, N = 160), K = 128 channels; each
+// operand as bf16 hi + lo and the product hi.hi + hi.lo + lo.hi (fp32-level).  T by 16 x 16 blocks on the
+// CUDA cores (kda_tsolve.cuh).
+constexpr int kPThreads = 512;
+constexpr uint32_t Q_ROW = 0;                 // [k ; q] e^{G - E_I}: hi, lo, each two regions of [128][64]
+constexpr uint32_t Q_COL = 65536;             // stacked k e^{E_I - G}: hi, lo, each two regions of [160][64]
+constexpr uint32_t kColRegion = 160 * 128;
+constexpr uint32_t Q_G = Q_COL + 4 * kColRegion;  // G (log2 units) fp32 [64][128]
+constexpr uint32_t Q_BETA = Q_G + 32768;      // beta [64]
+constexpr uint32_t Q_BAR = Q_BETA + 256;
+constexpr uint32_t Q_MISC = Q_BAR + 16;
+constexpr uint32_t kQSmem = Q_MISC + 16 + 1024;
+// once the product is complete (its operands are free)
+constexpr uint32_t Q_AKK = 0;                 // beta-scaled A_kk fp32 [64][kAS] (blocks on and below the diagonal)
+constexpr uint32_t Q_TF = 64 * kAS * 4;       // T fp32 [64][kAS]
+constexpr uint32_t Q_NB = 2 * 64 * kAS * 4;   // N blocks of the solve, 9 x [16][kNB] fp32
+constexpr uint32_t Q_AQS = Q_COL;             // scale A_qk hi, lo staged in the blob's layout (16 KB)
+static_assert(Q_NB + 9 * 16 * kNB * 4 <= Q_COL && Q_G % 1024 == 0 && kQSmem <= 232448, "prep layout");
+
+// 8 values as bf16 hi + lo (x = hi + lo), 16-byte chunks at `at` of two tiles `tile` bytes apart
+__device__ __forceinline__ void put_2(uint8_t* base, uint32_t at, uint32_t tile, const float (&x)[8]) {
+    uint32_t p1[4], p2[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        p1[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
+        p2[j] = pack_bf16x2(x[2 * j] - bf16_lo(p1[j]), x[2 * j + 1] - bf16_hi(p1[j]));
+    }
+    *reinterpret_cast<uint4*>(base + at) = make_uint4(p1[0], p1[1], p1[2], p1[3]);
+    *reinterpret_cast<uint4*>(base + at + tile) = make_uint4(p2[0], p2[1], p2[2], p2[3]);
+}
+
+__device__ __forceinline__ void load8f(const float* p, float (&f)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+__global__ void __launch_bounds__(kPThreads, 1)
+bwd_prep_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                   const float* __restrict__ g, const float* __restrict__ beta, const int32_t* __restrict__ cu, int N,
+                   int64_t T_total, int H, float scale, uint8_t* __restrict__ blobs, unsigned int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t slot = blockIdx.x;
+    const int h = blockIdx.y;
+    int n = 0;
+    {
+        int lo = 0, hi = N;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            const int64_t b = cu ? (int64_t)cu[mid] : 0;
+            if (b / kC + mid <= slot) lo = mid; else hi = mid;
+        }
+        n = lo;
+    }
+    int64_t bos, eos;
+    seq_bounds(cu, n, T_total, bos, eos);
+    const int64_t c0 = bos + (slot - (bos / kC + n)) * kC;
+    if (slot < bos / kC + n || c0 >= eos) return;
+    const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
+    const int64_t base = slot * H + h;
+    const int64_t rs = (int64_t)H * kD, hoff = (int64_t)h * kD;
+    constexpr float kLog2e = 1.4426950408889634f;
+    uint8_t* blob = blobs + base * (int64_t)kBwdBlobBytes;
+    float* sG = reinterpret_cast<float*>(sm + Q_G);
+    float* sBeta = reinterpret_cast<float*>(sm + Q_BETA);
+    uint64_t* bM = reinterpret_cast<uint64_t*>(sm + Q_BAR);
+    uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + Q_MISC);
+    if (tid == 0) {
+        mbar_init(bM, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(sTmem, 256);
+    // k and q of the thread's two (row, 8 channels) items, in flight while G is formed
+    uint4 kx[2], qx[2];
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        const int idx = tid + kPThreads * it, i = idx >> 4, c8 = idx & 15;
+        kx[it] = make_uint4(0, 0, 0, 0);
+        qx[it] = make_uint4(0, 0, 0, 0);
+        if (i < L) {
+            const int64_t at = (c0 + i) * rs + hoff + 8 * c8;
+            kx[it] = *reinterpret_cast<const uint4*>(k + at);
+            qx[it] = *reinterpret_cast<const uint4*>(q + at);
+        }
+    }
+    if (tid < kC) {
+        const float b = tid < L ? beta[(c0 + tid) * H + h] : 0.f;
+        sBeta[tid] = b;
+        if (__any_sync(0xFFFFFFFFu, !(b >= 0.f && b <= 1.f)) && lane == 0) raise_device_error(err, kErrBetaRange);
+    }
+    // ---- G: running sum of g per channel (log2 units), thread (c, half): tokens 32 half .. +31
+    if (tid < 256) {
+        const int c = tid & 127, hh = tid >> 7;
+        float gv[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            const int t = 32 * hh + r;
+            gv[r] = t < L ? g[(c0 + t) * rs + hoff + c] : 0.f;
+        }
+        float acc = 0.f, gmin = 0.f, gmax = 0.f;
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            gmin = fminf(gmin, gv[r]);
+            gmax = fmaxf(gmax, gv[r]);
+            acc = fmaf(gv[r], kLog2e, acc);
+            gv[r] = acc;
+        }
+        // g in [-5, 0]: min and max skip a NaN, the running sum does not
+        if (__any_sync(0xFFFFFFFFu, !(gmin >= -5.f && gmax <= 0.f && acc == acc)) && lane == 0)
+            raise_device_error(err, kErrGateRange);
+#pragma unroll
+        for (int r = 0; r < 32; ++r) sG[(32 * hh + r) * kD + c] = gv[r];
+    }
+    __syncthreads();
+    if (tid >= 128 && tid < 256) {  // the second half's running sum continues from the first's total
+        const int c = tid & 127;
+        const float t0 = sG[31 * kD + c];
+#pragma unroll 4
+        for (int r = 32; r < 64; ++r) sG[r * kD + c] += t0;
+    }
+    __syncthreads();
+    if (tid < kD) reinterpret_cast<float*>(blob + kBB_GAM)[tid] = ex2f(sG[(kC - 1) * kD + tid]);
+    if (tid < kC) reinterpret_cast<float*>(blob + kBB_BETA)[tid] = sBeta[tid];
+    // ---- operands, and Kr, scale Qg, Kg to the blob
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        const int idx = tid + kPThreads * it, i = idx >> 4, c8 = idx & 15, I = i >> 4;
+        const uint32_t reg = (uint32_t)(c8 >> 3), ch = (uint32_t)(c8 & 7);
+        float G[8], Gl[8], EI[8], kv[8], qv[8];
+        load8f(sG + i * kD + 8 * c8, G);
+        load8f(sG + (kC - 1) * kD + 8 * c8, Gl);
+        load8f(sG + (16 * I + 15) * kD + 8 * c8, EI);
+        const uint32_t kw[4] = {kx[it].x, kx[it].y, kx[it].z, kx[it].w};
+        const uint32_t qw[4] = {qx[it].x, qx[it].y, qx[it].z, qx[it].w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            kv[e] = (e & 1) ? bf16_hi(kw[e >> 1]) : bf16_lo(kw[e >> 1]);
+            qv[e] = (e & 1) ? bf16_hi(qw[e >> 1]) : bf16_lo(qw[e >> 1]);
+        }
+        float rk[8], rq[8], kr[8], qg[8], kg[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float f = ex2f(G[e] - EI[e]), eg = ex2f(G[e]);
+            rk[e] = kv[e] * f;
+            rq[e] = qv[e] * f;
+            kr[e] = kv[e] * ex2f(Gl[e] - G[e]);
+            qg[e] = scale * (qv[e] * eg);
+            kg[e] = kv[e] * eg;
+        }
+        put_2(sm + Q_ROW, reg * 16384u + sw128((uint32_t)i, ch), 32768, rk);
+        put_2(sm + Q_ROW, reg * 16384u + sw128((uint32_t)(kC + i), ch), 32768, rq);
+        for (int J = I; J < 4; ++J) {  // column operand of row block J >= I
+            float EJ[8], cv[8];
+            load8f(sG + (16 * J + 15) * kD + 8 * c8, EJ);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) cv[e] = kv[e] * ex2f(EJ[e] - G[e]);
+            put_2(sm + Q_COL, reg * kColRegion + sw128((uint32_t)(8 * J * (J + 1) + i), ch), 2 * kColRegion, cv);
+        }
+        const uint32_t at = reg * 8192u + sw128((uint32_t)i, ch);
+        put_2(blob + kBB_KR, at, 16384, kr);
+        put_2(blob + kBB_QG, at, 16384, qg);
+        put_2(blob + kBB_KG, at, 16384, kg);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *sTmem;
+    if (warp == 0) {  // D = [k ; q] rows x stacked columns: hi.hi + hi.lo + lo.hi, K = 128 in 8 steps
+        const uint32_t id = idesc_bf16_f32(128, 160, false, false);
+#pragma unroll
+        for (int pr = 0; pr < 3; ++pr) {
+            const uint32_t pa = pr == 2 ? 1u : 0u, pb = pr == 1 ? 1u : 0u;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t rg2 = (uint32_t)(ks >> 2), off = (uint32_t)(ks & 3) * 32u;
+                mma_bf16(tbase, kdesc(sbase + Q_ROW + pa * 32768u + rg2 * 16384u + off),
+                         kdesc(sbase + Q_COL + pb * 2u * kColRegion + rg2 * kColRegion + off), id,
+                         (pr | ks) ? 1u : 0u);
+            }
+        }
+        mma_commit(bM);
+    }
+    if (!mbar_wait(bM, 0, kWaitLimit)) raise_device_error(err, kErrMbarTimeout);
+    tc_fence_after();
+    float* sAkk = reinterpret_cast<float*>(sm + Q_AKK);
+    float* sTf = reinterpret_cast<float*>(sm + Q_TF);
+    // ---- A_kk (fp32 work array) and scale A_qk (bf16 hi, lo staged): lane quarter qt holds rows 32 qt .. +31
+    //      of [k-rows ; q-rows], lanes 0-15 of row block IbA = 2 (qt % 2), lanes 16-31 of IbA + 1; warp
+    //      slice sl takes columns 16 sl .. +15 of each lane's own block (both blocks' columns are loaded)
+    {
+        const int qt = warp & 3, sl = warp >> 2, IbA = 2 * (qt & 1);
+        const int r = 32 * qt + lane, i = r & 63, Ib = IbA + (lane >> 4);
+        const bool is_k = r < kC;
+        const uint32_t lane_base = (uint32_t)(32 * qt) << 16;
+        uint32_t t0[16], t1[16];
+        tmem_ld16_async(tbase + lane_base + 8 * IbA * (IbA + 1) + 16 * sl, t0);
+        tmem_ld16_async(tbase + lane_base + 8 * (IbA + 1) * (IbA + 2) + 16 * sl, t1);
+        tmem_wait_ld(); reg_fence(t0); reg_fence(t1);
+        const bool second = lane >= 16, inb = sl <= Ib;  // this column block is one of the row block's
+        float a[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) a[e] = __uint_as_float(second ? t1[e] : t0[e]);
+        if (is_k) {
+            if (inb) {
+                const float b = sBeta[i];
+#pragma unroll
+                for (int j4 = 0; j4 < 16; j4 += 4) {
+                    float4 w;
+                    float* wp = reinterpret_cast<float*>(&w);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) wp[e] = (16 * sl + j4 + e < i) ? b * a[j4 + e] : 0.f;
+                    *reinterpret_cast<float4*>(sAkk + i * kAS + 16 * sl + j4) = w;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int h8 = 0; h8 < 2; ++h8) {
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = (inb && 16 * sl + 8 * h8 + e <= i) ? scale * a[8 * h8 + e] : 0.f;
+                put_2(sm + Q_AQS, sw128((uint32_t)i, (uint32_t)(2 * sl + h8)), 8192, x);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    // ---- T = (I + A_kk)^-1 (warps 0-5); warps 8-15 copy scale A_qk out as whole rows meanwhile
+    if (warp >= 8) {
+        const int t = tid - 256;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+            *reinterpret_cast<uint4*>(blob + kBB_AQ + 4096 * kk + 16 * t) =
+                *reinterpret_cast<const uint4*>(sm + Q_AQS + 4096 * kk + 16 * t);
+    }
+    t_diag_blocks(sAkk, sTf, warp, lane);
+    __syncthreads();
+    t_offdiag_1(sAkk, sTf, reinterpret_cast<float*>(sm + Q_NB), tid);
+    t_offdiag_23(sTf, reinterpret_cast<float*>(sm + Q_NB), tid);
+    // ---- T as bf16 hi + lo: thread (row tid / 8, columns 8 (tid % 8) ..), zero above the diagonal blocks
+    {
+        const int i = tid >> 3, t8 = tid & 7;
+        float x[8];
+        const bool zero = (t8 >> 1) > (i >> 4);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = zero ? 0.f : sTf[i * kAS + 8 * t8 + e];
+        put_2(blob + kBB_TT, sw128((uint32_t)i, (uint32_t)t8), 8192, x);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tbase, 256);
+}
+
 // ============================ per chunk: the position-pair sums ============================
 // Per (chunk, head), the sums of bwd_chunk_b_kernel over position pairs with the decay e^{G_ic - G_jc}:
 //   rq_ic = sum_{j<=i} dA_qk[i][j] k_jc e^{G_ic-G_jc},   rk_ic = sum_{j<i} dA_kk[i][j] k_jc e^{G_ic-G_jc}
@@ -957,12 +1228,6 @@ constexpr uint32_t kBSmem = B_MISC + 16 + 1024;
 constexpr uint32_t B_RK = 160, B_CS = 320;
 __host__ __device__ constexpr int pair_lo(int b, int y) { return b * (b + 1) / 2 + y; }
 __host__ __device__ constexpr int pair_hi(int b, int x) { return 4 * b - b * (b - 1) / 2 + x - b; }
-
-__device__ __forceinline__ float ex2f(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 
 // 8 values as three bf16 pieces (x = p1 + p2 + p3), 16-byte chunks at `at` of three tiles `tile` bytes apart
 __device__ __forceinline__ void put_3(uint8_t* base, uint32_t at, uint32_t tile, const float (&x)[8]) {
@@ -1395,6 +1660,18 @@ cudaError_t launch_bwd_chunk_b_tc(const void* q, const void* k, const float* g, 
     bwd_chunk_b_tc_kernel<<<dim3((unsigned)slots, (unsigned)H), kBThreads, kBSmem, stream>>>(
         static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), g, beta, cu_seqlens, N, T_total, H,
         XQ, XK, XR, dgam, dAqk, dAkk, dq, dk, dg, dbeta_part, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_prep_tc(const void* q, const void* k, const float* g, const float* beta, const int32_t* cu_seqlens,
+                               int N, int64_t T_total, int H, float scale, void* blobs, unsigned int* err,
+                               cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_prep_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t slots = T_total / kC + N + 1;
+    bwd_prep_tc_kernel<<<dim3((unsigned)slots, (unsigned)H), kPThreads, kQSmem, stream>>>(
+        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), g, beta, cu_seqlens, N, T_total, H,
+        scale, static_cast<uint8_t*>(blobs), err);
     return cudaGetLastError();
 }
 
