@@ -743,33 +743,61 @@ bwd_chunk_a_tc_kernel(const float* __restrict__ beta, const __nv_bfloat16* __res
     if (tid < kC) sBeta[tid] = tid < L ? beta[(c0 + tid) * H + h] : 0.f;
     const float* S0 = S0s + base * kD * kD;
     const float* dSn = dS_next + base * kD * kD;
+    prefetch_l2(dSn + 32 * tid);  // dS_next (64 KB) on its way to L2: one 128-byte line per thread
+    // ---- loads first (S0: thread (row r = tid / 16 + 32 it, channels 8 (tid % 16) ..); the chunk's tokens:
+    //      (token t = tid / 16 + 32 it, value rows 8 (tid % 16) ..)), then the buffers
+    float4 s0v[4][2];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int idx = tid + kAThreads * it, r = idx >> 4, c8 = idx & 15;
+        s0v[it][0] = *reinterpret_cast<const float4*>(S0 + r * kD + 8 * c8);
+        s0v[it][1] = *reinterpret_cast<const float4*>(S0 + r * kD + 8 * c8 + 4);
+    }
+    uint4 ov[2];
+    float4 zv[2][2], pv[2][2], rv[2][2];
+    float btv[2];
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        const int idx = tid + kAThreads * it, t = idx >> 4, r8 = idx & 15;
+        const int tc = t < L ? t : L - 1;  // rows past the end read the last row and are zeroed below
+        const int64_t at = ((c0 + tc) * H + h) * kD + 8 * r8;
+        ov[it] = *reinterpret_cast<const uint4*>(d_o + at);
+        zv[it][0] = *reinterpret_cast<const float4*>(dZ + at);
+        zv[it][1] = *reinterpret_cast<const float4*>(dZ + at + 4);
+        pv[it][0] = *reinterpret_cast<const float4*>(Vp + at);
+        pv[it][1] = *reinterpret_cast<const float4*>(Vp + at + 4);
+        rv[it][0] = *reinterpret_cast<const float4*>(Rb + at);
+        rv[it][1] = *reinterpret_cast<const float4*>(Rb + at + 4);
+        btv[it] = beta[(c0 + tc) * H + h];
+    }
     // ---- S0 -> the buffer (MN-major A: row r, channels c)
-    for (int idx = tid; idx < kD * 16; idx += kAThreads) {
-        const int r = idx >> 4, c8 = idx & 15;
-        const float4 a = *reinterpret_cast<const float4*>(S0 + r * kD + 8 * c8);
-        const float4 b = *reinterpret_cast<const float4*>(S0 + r * kD + 8 * c8 + 4);
-        const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int idx = tid + kAThreads * it, r = idx >> 4, c8 = idx & 15;
+        const float x[8] = {s0v[it][0].x, s0v[it][0].y, s0v[it][0].z, s0v[it][0].w,
+                            s0v[it][1].x, s0v[it][1].y, s0v[it][1].z, s0v[it][1].w};
         put_hi_lo(sm + A_BUF, (uint32_t)(c8 >> 3) * 16384u + sw128((uint32_t)r, (uint32_t)(c8 & 7)), 32768, x);
     }
     // ---- [dO ; dZ] (rows past the chunk's end zero), V'; dv = beta dZ; dbeta's first term sum_r dZ R
-    for (int idx = tid; idx < kC * 16; idx += kAThreads) {
-        const int t = idx >> 4, r8 = idx & 15;
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        const int idx = tid + kAThreads * it, t = idx >> 4, r8 = idx & 15;
         const bool ok = t < L;
         const int64_t at = ((c0 + t) * H + h) * kD + 8 * r8;
         float z[8], vp[8];
         uint4 o = make_uint4(0, 0, 0, 0);
         float part = 0.f;
         if (ok) {
-            o = *reinterpret_cast<const uint4*>(d_o + at);
-            const float4 z0 = *reinterpret_cast<const float4*>(dZ + at), z1 = *reinterpret_cast<const float4*>(dZ + at + 4);
-            const float4 p0 = *reinterpret_cast<const float4*>(Vp + at), p1 = *reinterpret_cast<const float4*>(Vp + at + 4);
-            const float4 q0 = *reinterpret_cast<const float4*>(Rb + at), q1 = *reinterpret_cast<const float4*>(Rb + at + 4);
-            z[0] = z0.x; z[1] = z0.y; z[2] = z0.z; z[3] = z0.w; z[4] = z1.x; z[5] = z1.y; z[6] = z1.z; z[7] = z1.w;
-            vp[0] = p0.x; vp[1] = p0.y; vp[2] = p0.z; vp[3] = p0.w; vp[4] = p1.x; vp[5] = p1.y; vp[6] = p1.z; vp[7] = p1.w;
-            const float rr[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+            o = ov[it];
+            z[0] = zv[it][0].x; z[1] = zv[it][0].y; z[2] = zv[it][0].z; z[3] = zv[it][0].w;
+            z[4] = zv[it][1].x; z[5] = zv[it][1].y; z[6] = zv[it][1].z; z[7] = zv[it][1].w;
+            vp[0] = pv[it][0].x; vp[1] = pv[it][0].y; vp[2] = pv[it][0].z; vp[3] = pv[it][0].w;
+            vp[4] = pv[it][1].x; vp[5] = pv[it][1].y; vp[6] = pv[it][1].z; vp[7] = pv[it][1].w;
+            const float rr[8] = {rv[it][0].x, rv[it][0].y, rv[it][0].z, rv[it][0].w,
+                                 rv[it][1].x, rv[it][1].y, rv[it][1].z, rv[it][1].w};
 #pragma unroll
             for (int e = 0; e < 8; ++e) part = fmaf(z[e], rr[e], part);
-            const float bt = beta[(c0 + t) * H + h];
+            const float bt = btv[it];
             *reinterpret_cast<float4*>(dv + at) = make_float4(bt * z[0], bt * z[1], bt * z[2], bt * z[3]);
             *reinterpret_cast<float4*>(dv + at + 4) = make_float4(bt * z[4], bt * z[5], bt * z[6], bt * z[7]);
         } else {
@@ -821,33 +849,47 @@ bwd_chunk_a_tc_kernel(const float* __restrict__ beta, const __nv_bfloat16* __res
         for (int ks = 0; ks < 8; ++ks) mma_bf16(tbase + A_TA, kd(sbase + A_QZL, 16384, ks), kd(sbase + A_VH, 8192, ks), id_a, 1u);
         mma_commit(bX);
     }
-    // ---- dgamma parts: sum over rows r of S0 . dS_next (S0 read again, from L2); 32 row groups x 128 channels
-    {
-        const int c4 = tid & 31, rg = tid >> 5;  // channels 4 c4 .. +3, rows rg, rg + 16, ...
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int r = rg; r < kD; r += 16) {
-            const float4 a = *reinterpret_cast<const float4*>(S0 + r * kD + 4 * c4);
-            const float4 b = *reinterpret_cast<const float4*>(dSn + r * kD + 4 * c4);
-            acc.x = fmaf(a.x, b.x, acc.x); acc.y = fmaf(a.y, b.y, acc.y);
-            acc.z = fmaf(a.z, b.z, acc.z); acc.w = fmaf(a.w, b.w, acc.w);
+    // ---- dS_next (and S0 again, from L2, for dgamma) in flight while the S0 products run; thread (row
+    //      r = tid / 16 + 32 it, channels 8 (tid % 16) ..)
+    float4 dv4[4][2];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int idx = tid + kAThreads * it, r = idx >> 4, c8 = idx & 15;
+        dv4[it][0] = *reinterpret_cast<const float4*>(dSn + r * kD + 8 * c8);
+        dv4[it][1] = *reinterpret_cast<const float4*>(dSn + r * kD + 8 * c8 + 4);
+    }
+    {  // dgamma parts: sum over the thread's four rows of S0 . dS_next, per channel; 32 row groups x 128 channels
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        const int c8 = tid & 15;
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int r = (tid >> 4) + 32 * it;
+            const float4 a0 = *reinterpret_cast<const float4*>(S0 + r * kD + 8 * c8);
+            const float4 a1 = *reinterpret_cast<const float4*>(S0 + r * kD + 8 * c8 + 4);
+            acc[0] = fmaf(a0.x, dv4[it][0].x, acc[0]); acc[1] = fmaf(a0.y, dv4[it][0].y, acc[1]);
+            acc[2] = fmaf(a0.z, dv4[it][0].z, acc[2]); acc[3] = fmaf(a0.w, dv4[it][0].w, acc[3]);
+            acc[4] = fmaf(a1.x, dv4[it][1].x, acc[4]); acc[5] = fmaf(a1.y, dv4[it][1].y, acc[5]);
+            acc[6] = fmaf(a1.z, dv4[it][1].z, acc[6]); acc[7] = fmaf(a1.w, dv4[it][1].w, acc[7]);
         }
-        *reinterpret_cast<float4*>(sRed + rg * kD + 4 * c4) = acc;
+        float* dst = sRed + (tid >> 4) * kD + 8 * c8;
+        *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
     // ---- the buffer takes dS_next once the S0 products are done
     if (tid == 0 && !mbar_wait(bX, 0, kWaitLimit)) raise_device_error(err, kErrMbarTimeout);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    for (int idx = tid; idx < kD * 16; idx += kAThreads) {
-        const int r = idx >> 4, c8 = idx & 15;
-        const float4 a = *reinterpret_cast<const float4*>(dSn + r * kD + 8 * c8);
-        const float4 b = *reinterpret_cast<const float4*>(dSn + r * kD + 8 * c8 + 4);
-        const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int idx = tid + kAThreads * it, r = idx >> 4, c8 = idx & 15;
+        const float x[8] = {dv4[it][0].x, dv4[it][0].y, dv4[it][0].z, dv4[it][0].w,
+                            dv4[it][1].x, dv4[it][1].y, dv4[it][1].z, dv4[it][1].w};
         put_hi_lo(sm + A_BUF, (uint32_t)(c8 >> 3) * 16384u + sw128((uint32_t)r, (uint32_t)(c8 & 7)), 32768, x);
     }
-    if (tid < kD) {  // dgamma: the 16 row groups' parts in order
+    if (tid < kD) {  // dgamma: the 32 row groups' parts in order
         float sum = 0.f;
-        for (int g = 0; g < 16; ++g) sum += sRed[g * kD + tid];
+        for (int g = 0; g < 32; ++g) sum += sRed[g * kD + tid];
         dgam[base * kD + tid] = sum;
     }
     fence_proxy_async();
