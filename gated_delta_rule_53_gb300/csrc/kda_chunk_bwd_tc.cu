@@ -1288,19 +1288,11 @@ __device__ __forceinline__ void put_3(uint8_t* base, uint32_t at, uint32_t tile,
 }
 
 // One block operand (kOp 0: K_b, 1: Q_b, 2: B_b) of the chunk's 64 rows into `dst`; thread (row, 8 channels),
-// two per thread.  Rows past the sequence's end are zero.
+// two per thread, from the rows xv (k or q; zero past the sequence's end).
 template <int kOp>
-__device__ __forceinline__ void build_operand(uint8_t* sm, uint32_t dst, const __nv_bfloat16* __restrict__ x,  // the head's row 0
-                                              int64_t row0, int64_t row_stride, int L, int tid) {
+__device__ __forceinline__ void build_operand(uint8_t* sm, uint32_t dst, const uint4 (&xv)[2], int tid) {
     const float* sG = reinterpret_cast<const float*>(sm + B_G);
     const float* sBeta = reinterpret_cast<const float*>(sm + B_BETA);
-    uint4 xv[2];
-#pragma unroll
-    for (int it = 0; it < 2; ++it) {
-        const int idx = tid + kBThreads * it, r = idx >> 4, c8 = idx & 15;
-        xv[it] = make_uint4(0, 0, 0, 0);
-        if (r < L) xv[it] = *reinterpret_cast<const uint4*>(x + (row0 + r) * row_stride + 8 * c8);
-    }
 #pragma unroll
     for (int it = 0; it < 2; ++it) {
         const int idx = tid + kBThreads * it, r = idx >> 4, c8 = idx & 15;
@@ -1380,16 +1372,24 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(sTmem, 512);
-    // the epilogue's per-token inputs and q, k on their way to L2 (two 128-byte lines of five tiles per thread)
-    for (int idx = tid; idx < 5 * kC * 4; idx += kBThreads) {
+    // the epilogue's per-token inputs on their way to L2 (768 128-byte lines)
+    for (int idx = tid; idx < 3 * kC * 4; idx += kBThreads) {
         const int which = idx >> 8, r = (idx >> 2) & 63, part = idx & 3;
-        if (r < L) {
-            const int64_t at = (c0 + r) * rs + hoff;
-            if (which < 3) prefetch_l2((which == 0 ? XQ : which == 1 ? XK : XR) + at + 32 * part);
-            else if (part < 2) prefetch_l2((which == 3 ? q : k) + at + 64 * part);
-        }
+        if (r < L) prefetch_l2((which == 0 ? XQ : which == 1 ? XK : XR) + (c0 + r) * rs + hoff + 32 * part);
     }
     if (tid < kC) sBeta[tid] = tid < L ? beta[(c0 + tid) * H + h] : 0.f;
+    // k and q of the operand builder's two (row, 8 channels) items, held for the three builds
+    uint4 kx[2], qx[2];
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        const int idx = tid + kBThreads * it, r = idx >> 4, c8 = idx & 15;
+        kx[it] = make_uint4(0, 0, 0, 0);
+        qx[it] = make_uint4(0, 0, 0, 0);
+        if (r < L) {
+            kx[it] = *reinterpret_cast<const uint4*>(k + (c0 + r) * rs + hoff + 8 * c8);
+            qx[it] = *reinterpret_cast<const uint4*>(q + (c0 + r) * rs + hoff + 8 * c8);
+        }
+    }
     // ---- G: running sum of g per channel (log2 units), thread (c, half): tokens 32 half .. +31
     if (tid < 256) {
         const int c = tid & 127, hh = tid >> 7;
@@ -1437,7 +1437,7 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     // (11, 12, 21, 13, 31, 22 in one-based pieces)
     constexpr uint32_t kPa = 0x120100u, kPb = 0x102010u;
     // ---- K operand, then its products: RQ and RK of every pair (b, y <= b)
-    build_operand<0>(sm, B_OPA, k + hoff, c0, rs, L, tid);
+    build_operand<0>(sm, B_OPA, kx, tid);
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
@@ -1459,7 +1459,7 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
         mma_commit(bM);
     }
     // ---- Q operand, then CQ of every pair (b, x >= b)
-    build_operand<1>(sm, B_OPB, q + hoff, c0, rs, L, tid);
+    build_operand<1>(sm, B_OPB, qx, tid);
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
@@ -1479,7 +1479,7 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     }
     // ---- B operand once the K operand's products are complete, then CK of every pair onto CQ's columns
     if (!mbar_wait(bM, 0, kWaitLimit)) raise_device_error(err, kErrMbarTimeout);
-    build_operand<2>(sm, B_OPA, k + hoff, c0, rs, L, tid);
+    build_operand<2>(sm, B_OPA, kx, tid);
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
@@ -1513,22 +1513,32 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     const float Gl = sG[(kC - 1) * kD + c];
     const uint16_t* k16 = reinterpret_cast<const uint16_t*>(k);
     float dGs[16], last_acc = 0.f;  // the G gradient's running sums inside each four-row group
-    if (!mbar_wait(bM + 1, 0, kWaitLimit)) raise_device_error(err, kErrMbarTimeout);  // every product complete
-    tc_fence_after();
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        // the block's per-token inputs, all loads issued together (rows past the end read the last row)
-        float xqv[4], xkv[4], xrv[4], qv[4], kv[4];
+    // a block's per-token inputs, all loads issued together (rows past the end read the last row); the next
+    // block's are in flight while one block is worked on
+    float nxq[4], nxk[4], nxr[4], nq[4], nk[4];
+    auto load_block = [&](int b) {
 #pragma unroll
         for (int a = 0; a < 4; ++a) {
             const int i = min(16 * b + 4 * rg + a, L - 1);
             const int64_t at = (c0 + i) * rs + hoff + c;
-            xqv[a] = XQ[at];
-            xkv[a] = XK[at];
-            xrv[a] = XR[at];
-            qv[a] = __bfloat162float(q[at]);
-            kv[a] = __uint_as_float((uint32_t)k16[at] << 16);
+            nxq[a] = XQ[at];
+            nxk[a] = XK[at];
+            nxr[a] = XR[at];
+            nq[a] = __bfloat162float(q[at]);
+            nk[a] = __uint_as_float((uint32_t)k16[at] << 16);
         }
+    };
+    load_block(0);
+    if (!mbar_wait(bM + 1, 0, kWaitLimit)) raise_device_error(err, kErrMbarTimeout);  // every product complete
+    tc_fence_after();
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        float xqv[4], xkv[4], xrv[4], qv[4], kv[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            xqv[a] = nxq[a]; xkv[a] = nxk[a]; xrv[a] = nxr[a]; qv[a] = nq[a]; kv[a] = nk[a];
+        }
+        if (b < 3) load_block(b + 1);
         uint32_t tq[4][4], tk[4][4], ts[4][4];
 #pragma unroll
         for (int y = 0; y <= b; ++y) {
