@@ -1111,9 +1111,8 @@ bwd_prep_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
     for (int it = 0; it < 2; ++it) {
         const int idx = tid + kPThreads * it, i = idx >> 4, c8 = idx & 15, I = i >> 4;
         const uint32_t reg = (uint32_t)(c8 >> 3), ch = (uint32_t)(c8 & 7);
-        float G[8], Gl[8], EI[8], kv[8], qv[8];
+        float G[8], EI[8], kv[8], qv[8];
         load8f(sG + i * kD + 8 * c8, G);
-        load8f(sG + (kC - 1) * kD + 8 * c8, Gl);
         load8f(sG + (16 * I + 15) * kD + 8 * c8, EI);
         const uint32_t kw[4] = {kx[it].x, kx[it].y, kx[it].z, kx[it].w};
         const uint32_t qw[4] = {qx[it].x, qx[it].y, qx[it].z, qx[it].w};
@@ -1122,15 +1121,12 @@ bwd_prep_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
             kv[e] = (e & 1) ? bf16_hi(kw[e >> 1]) : bf16_lo(kw[e >> 1]);
             qv[e] = (e & 1) ? bf16_hi(qw[e >> 1]) : bf16_lo(qw[e >> 1]);
         }
-        float rk[8], rq[8], kr[8], qg[8], kg[8];
+        float rk[8], rq[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const float f = ex2f(G[e] - EI[e]), eg = ex2f(G[e]);
+            const float f = ex2f(G[e] - EI[e]);
             rk[e] = kv[e] * f;
             rq[e] = qv[e] * f;
-            kr[e] = kv[e] * ex2f(Gl[e] - G[e]);
-            qg[e] = scale * (qv[e] * eg);
-            kg[e] = kv[e] * eg;
         }
         put_2(sm + Q_ROW, reg * 16384u + sw128((uint32_t)i, ch), 32768, rk);
         put_2(sm + Q_ROW, reg * 16384u + sw128((uint32_t)(kC + i), ch), 32768, rq);
@@ -1141,10 +1137,6 @@ bwd_prep_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
             for (int e = 0; e < 8; ++e) cv[e] = kv[e] * ex2f(EJ[e] - G[e]);
             put_2(sm + Q_COL, reg * kColRegion + sw128((uint32_t)(8 * J * (J + 1) + i), ch), 2 * kColRegion, cv);
         }
-        const uint32_t at = reg * 8192u + sw128((uint32_t)i, ch);
-        put_2(blob + kBB_KR, at, 16384, kr);
-        put_2(blob + kBB_QG, at, 16384, qg);
-        put_2(blob + kBB_KG, at, 16384, kg);
     }
     fence_proxy_async();
     tc_fence_before();
@@ -1165,6 +1157,30 @@ bwd_prep_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
             }
         }
         mma_commit(bM);
+    }
+    // ---- Kr, scale Qg, Kg to the blob while the product runs
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+        const int idx = tid + kPThreads * it, i = idx >> 4, c8 = idx & 15;
+        float G[8], Gl[8], kv[8], qv[8];
+        load8f(sG + i * kD + 8 * c8, G);
+        load8f(sG + (kC - 1) * kD + 8 * c8, Gl);
+        const uint32_t kw[4] = {kx[it].x, kx[it].y, kx[it].z, kx[it].w};
+        const uint32_t qw[4] = {qx[it].x, qx[it].y, qx[it].z, qx[it].w};
+        float kr[8], qg[8], kg[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            kv[e] = (e & 1) ? bf16_hi(kw[e >> 1]) : bf16_lo(kw[e >> 1]);
+            qv[e] = (e & 1) ? bf16_hi(qw[e >> 1]) : bf16_lo(qw[e >> 1]);
+            const float eg = ex2f(G[e]);
+            kr[e] = kv[e] * ex2f(Gl[e] - G[e]);
+            qg[e] = scale * (qv[e] * eg);
+            kg[e] = kv[e] * eg;
+        }
+        const uint32_t at = (uint32_t)(c8 >> 3) * 8192u + sw128((uint32_t)i, (uint32_t)(c8 & 7));
+        put_2(blob + kBB_KR, at, 16384, kr);
+        put_2(blob + kBB_QG, at, 16384, qg);
+        put_2(blob + kBB_KG, at, 16384, kg);
     }
     if (!mbar_wait(bM, 0, kWaitLimit)) raise_device_error(err, kErrMbarTimeout);
     tc_fence_after();
