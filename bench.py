@@ -87,16 +87,29 @@ def bwd_flops_per_token_head(C: int = 64, d: int = 128) -> float:
     return (12 * C * d * d + 10 * C * C * d) / C
 
 
+def bwd_bytes_per_token_head(d: int = 128) -> int:
+    """What the backward must move per token and head: q, k, v and dL/do in bf16, g and beta in fp32 read; the
+    fp32 gradients of q, k, v, g and beta written (the chunk states and tiles its kernels hand to one another
+    through the workspace are not counted)."""
+    return 4 * d * 2 + d * 4 + 4 + 4 * d * 4 + 4
+
+
+BWD_SOURCES = "kda_chunk_bwd.cu+kda_chunk_bwd_tc.cu+kda_bwd_tc.cuh+kda_tsolve.cuh"
+
+
 def fp32_alu_peak_tflops(sms: int = 152, lanes: int = 128, mhz: float = 2070.0) -> float:
     """fp32 FMA rate of the part: SMs x fp32 lanes per SM x 2 flop x the maximum SM clock."""
     return sms * lanes * 2 * mhz * 1e6 / 1e12
 
 
 def kernel_source_hash(filename: str) -> str:
+    """First 16 hex digits of the SHA-256 of a source file, or of several joined by '+' (their bytes in order)."""
     import hashlib
-    path = os.path.join(ROOT, "gated_delta_rule_53_gb300", "csrc", filename)
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in filename.split("+"):
+        with open(os.path.join(ROOT, "gated_delta_rule_53_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def measured_traffic(kernel: str, source: str, workload: str):
@@ -468,7 +481,7 @@ def run_ours(args):
     gate_tflops = gflops / (ms_gate_launch * 1e-3) / 1e12
     del xg, wga, wgb, ah, gate_o, g_o, z_o
 
-    # ---------------- backward of the prefill (kda_chunk_bwd): fp32 on the CUDA cores ----------------
+    # ---------------- backward of the prefill (kda_chunk_bwd): bf16 inputs, products on the tensor cores ----------------
     qb, kb, vb, gb, bb = make_prefill_inputs(w, device)
     dob = fill_device(w.seed, ks.TID_DO, ks.NORMAL, (w.T, w.H, w.d), "bf16", device=device)
     wsb = torch.empty(kda.kda_chunk_bwd_workspace_size(1, w.T, w.H), dtype=torch.uint8, device=device)
@@ -477,6 +490,8 @@ def run_ours(args):
     ms_bwd, ms_bwd_launch, _ = timed(bstep, bsteps, args.warmup, stream, dist)
     bwd_flops = w.T * w.H * bwd_flops_per_token_head()
     bwd_tflops = bwd_flops / (ms_bwd_launch * 1e-3) / 1e12
+    bwd_bytes = w.T * w.H * bwd_bytes_per_token_head()
+    bwd_gbs = bwd_bytes / (ms_bwd_launch * 1e-3) / 1e9
     del qb, kb, vb, gb, bb, dob, wsb
 
     # ---------------- front end + prefill from raw inputs: fused vs two passes (the long workload's path) ----
@@ -637,19 +652,19 @@ def run_ours(args):
                      "frac": gate_tflops / tc_peak,
                      "traffic": measured_traffic("gemm_gate_kernel", "kda_gate.cu", "gates_8k"), "peak_source": peak_src,
                      "kernel": "gemm_gate_kernel x2 (x [W_gate ; W_a]^T, then the rank product with the gate epilogue)"}}
-    alu_peak = fp32_alu_peak_tflops()
+    bwd_traffic = measured_traffic("kda_chunk_bwd", BWD_SOURCES, w.name)
     line["backward"] = {
         "workload": f"{w.name}: kda_chunk_bwd of the prefill (bf16 q, k, v and dL/do; fp32 gradients of q, k, v, g, "
                     "beta, S0), dL/dS_final = 0",
         "value": w.T * world / (ms_bwd * 1e-3), "unit": "tokens/s", "ms_per_step": ms_bwd, "steps": bsteps,
-        "gpu_launches": 6 * bsteps, "algorithmic_flops_per_launch": bwd_flops,
-        "roofline": {"bound": "alu", "achieved": bwd_tflops, "peak": alu_peak, "unit": "TFLOP/s",
-                     "frac": bwd_tflops / alu_peak,
-                     "traffic": measured_traffic("kda_chunk_bwd", "kda_chunk_bwd.cu", w.name),
-                     "peak_source": "derived: 152 SMs x 128 fp32 "
-                     "lanes x 2 flop (FMA) x 2070 MHz",
-                     "kernel": "bwd_prep_kernel + bwd_fwd_state_kernel + bwd_state_kernel + bwd_chunk_a_kernel + "
-                               "bwd_chunk_b_kernel + bwd_dbeta_kernel, timed as one call"}}
+        "gpu_launches": 6 * bsteps, "algorithmic_bytes_per_launch": bwd_bytes,
+        "algorithmic_flops_per_launch": bwd_flops, "products_tflops": bwd_tflops,
+        "roofline": {"bound": "hbm", "achieved": bwd_gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": bwd_gbs / hbm_peak, "traffic": bwd_traffic,
+                     "traffic_GB_s": (bwd_traffic / (ms_bwd_launch * 1e-3) / 1e9) if bwd_traffic else None,
+                     "peak_source": peak_src,
+                     "kernel": "bwd_prep_tc_kernel + bwd_fwd_state_tc_kernel + bwd_state_tc_kernel + "
+                               "bwd_chunk_a_tc_kernel + bwd_chunk_b_tc_kernel + bwd_dbeta_kernel, timed as one call"}}
     line["fused_prefill"] = {
         "workload": "frontend_32k raw q, k, v bf16 [32768, 12288] + g = max(-5, -softplus(z)), beta -> "
                     "ShortConv(4)+SiLU+L2norm -> chunk_kda (the long workload's path at 32K tokens)",

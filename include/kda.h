@@ -242,9 +242,12 @@ KDA_API kda_status kda_chunk_segment_summary(const void* q, const void* k, const
  * gradients of L with respect to q, k, v, g, beta and the initial state.  The result equals reverse
  * mode through the token-by-token recurrence; the kernels take the chain rule through the chunk form
  * (a forward pass that keeps the state entering every chunk, a reverse pass over the chunks for the
- * gradient of the state, then every (chunk, head) at once).  fp32 arithmetic on the CUDA cores with
- * explicit position-pair decays (no use of the -5 bound); with bf16 inputs the reverse pass runs on
- * the tensor cores, every product split as bf16 hi + lo (three bf16 products) to keep fp32 accuracy.
+ * gradient of the state, then every (chunk, head) at once).  fp32 inputs: fp32 arithmetic on the CUDA
+ * cores with explicit position-pair decays (no use of the -5 bound).  bf16 inputs: every product on the
+ * tensor cores with fp32 accumulation, each fp32 operand split into bf16 pieces to keep fp32-level
+ * accuracy (hi + lo, three bf16 products; three pieces and six products in the position-pair sums), the
+ * decays factorised around 16-token blocks as in kda_chunk_fwd (so g must respect the -5 bound there);
+ * with bf16 inputs the g and beta range checks of kda_chunk_fwd run too (the bits of kda_device_error).
  *
  *  q, k, v, g, beta, init_state, cu_seqlens, N, T_total, H, dk, dv, scale, chunk_size
  *                  as kda_chunk_fwd (q, k, v and d_o in storage `dtype`, F32 or BF16)
@@ -271,7 +274,7 @@ KDA_API kda_status kda_chunk_bwd(const void* q, const void* k, const void* v, co
  * Bytes of workspace kda_chunk_bwd needs for these sizes (into *bytes): the state entering each chunk
  * and the gradient leaving it (64 KB each per chunk and head), six fp32 values per token, head and
  * channel, two per token and head, and per chunk and head three 64 x 128 and four 64 x 64 fp32 tiles,
- * two vectors of 128, and 131,840 bytes of bf16 tiles for the tensor-core reverse pass (bf16 inputs).
+ * two vectors of 128, and 131,840 bytes of bf16 tiles for the tensor-core passes (bf16 inputs).
  */
 KDA_API kda_status kda_chunk_bwd_workspace_size(int N, int64_t T_total, int H, int dk, int dv, int chunk_size,
                                                 size_t* bytes);
@@ -350,8 +353,8 @@ KDA_API const char* kda_last_error(void);
  *                                开源大模型技术报告", 架构)
  *   KDA_DEVICE_ERR_BETA_RANGE    a beta outside [0, 1], or not finite
  * The range bits are raised by kda_chunk_fwd, kda_chunk_fwd_frontend,
- * kda_chunk_fwd_noalloc and kda_chunk_segment_summary with bf16 inputs (every g
- * and beta of every token is checked as it is read) and by kda_recurrent_step; the
+ * kda_chunk_fwd_noalloc, kda_chunk_segment_summary and kda_chunk_bwd with bf16 inputs
+ * (every g and beta of every token is checked as it is read) and by kda_recurrent_step; the
  * call still completes (nothing traps) and its results are then unspecified.
  * Returns KDA_ERR_CUDA if the read itself fails.
  */

@@ -87,4 +87,17 @@ def test_backward_roofline_constants():
     import bench
     # per chunk of 64 tokens and head: 12 C d^2 + 10 C^2 d flop, per token-head
     assert bench.bwd_flops_per_token_head() == (12 * 64 * 128 * 128 + 10 * 64 * 64 * 128) / 64
+    # bytes per token-head: q, k, v, dL/do bf16 (4 x 256) + g fp32 (512) + beta (4) read; dq, dk, dv, dg fp32
+    # (4 x 512) + dbeta (4) written
+    assert bench.bwd_bytes_per_token_head() == 1024 + 512 + 4 + 2048 + 4
     assert abs(bench.fp32_alu_peak_tflops() - 80.54784) < 1e-9
+
+
+def test_source_hash_of_several_files():
+    import hashlib
+    import bench
+    csrc = os.path.join(bench.ROOT, "gated_delta_rule_53_gb300", "csrc")
+    names = bench.BWD_SOURCES.split("+")
+    joined = b"".join(open(os.path.join(csrc, n), "rb").read() for n in names)
+    assert bench.kernel_source_hash(bench.BWD_SOURCES) == hashlib.sha256(joined).hexdigest()[:16]
+    assert bench.kernel_source_hash(names[0]) == hashlib.sha256(open(os.path.join(csrc, names[0]), "rb").read()).hexdigest()[:16]

@@ -127,6 +127,26 @@ def test_out_of_range_gates_and_betas_are_reported():
     bad_g[1, 1, 1], bad_b[2, 0] = -6.0, 2.0
     assert run(bad_g, bad_b) == GATE_RANGE | BETA_RANGE   # both bits, one read
 
+    # the bf16 backward checks the same ranges as it reads g and beta
+    d_o = to_device(w.qkv("v"))
+
+    def bwd(gg, bb):
+        kda.kda_chunk_bwd(to_device(q), to_device(k), to_device(v), to_device(gg), to_device(bb), d_o, cu_seqlens=cu)
+        torch.cuda.synchronize()
+        return kda.device_error()
+
+    assert bwd(g, b) == 0
+    assert bwd(edge_g, edge_b) == 0
+    bad = g.copy()
+    bad[5, 1, 7] = -5.25
+    assert bwd(bad, b) == GATE_RANGE
+    bad = g.copy()
+    bad[200, 0, 127] = np.nan
+    assert bwd(bad, b) == GATE_RANGE
+    bad = b.copy()
+    bad[130, 1] = -0.5
+    assert bwd(g, bad) == BETA_RANGE
+
     # the decode step checks the same ranges
     wd = ks.Workload("range_dec", "decode", 5303, H=2, lengths=[1] * 3, init_state_std=0.02)
     xs = [to_device(ks.fill(wd.seed, tid, ks.NORMAL, (wd.N, wd.H * wd.d), "bf16")) for tid in (1, 2, 3)]
