@@ -1281,8 +1281,10 @@ constexpr uint32_t B_DBP = 190720;    // dbeta parts per (row, lane quarter): fp
 constexpr uint32_t B_BAR = 191744;    // two mbarriers
 constexpr uint32_t B_MISC = B_BAR + 32;
 constexpr uint32_t kBSmem = B_MISC + 16 + 1024;
-// TMEM columns, 16 per block pair: RQ (b, y <= b) at 16 (b (b+1)/2 + y), RK at 160 + the same; CQ + CK (b, x >= b)
-// at 320 + 16 (4b - b (b-1)/2 + x - b): cq and ck carry the same weights, so their products share columns
+// TMEM columns, 16 per block pair, laid out so that one product per operand block covers all of its pairs:
+// RQ (b, y <= b) at 16 pair_hi(y, b) (block y's pairs: rows 16 y .. 63 from column 16 pair_hi(y, y)), RK at
+// 160 + the same; CQ + CK (b, x >= b) at 320 + 16 pair_lo(x, b) (block x's pairs: columns 0 .. 16 x + 15 from
+// 320 + 16 pair_lo(x, 0)); cq and ck carry the same weights, so their products share columns
 constexpr uint32_t B_RK = 160, B_CS = 320;
 __host__ __device__ constexpr int pair_lo(int b, int y) { return b * (b + 1) / 2 + y; }
 __host__ __device__ constexpr int pair_hi(int b, int x) { return 4 * b - b * (b - 1) / 2 + x - b; }
@@ -1447,8 +1449,6 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     }
     __syncthreads();
     const uint32_t tbase = *sTmem;
-    const uint32_t id_k = idesc_bf16_f32(128, 16, true, false);  // A = operand^T (MN-major), B = dA rows (K-major)
-    const uint32_t id_m = idesc_bf16_f32(128, 16, true, true);   // A = operand^T, B = dA columns (MN-major)
     // pieces (of the operand, of dA) of the six products p: nibble p of kPa, kPb
     // (11, 12, 21, 13, 31, 22 in one-based pieces)
     constexpr uint32_t kPa = 0x120100u, kPb = 0x102010u;
@@ -1464,13 +1464,12 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
             const uint64_t ad = sdesc_sw128(sbase + B_OPA + 16384 * ((kPa >> (4 * p)) & 15u), 8192, 1024);
             const uint32_t bt = sbase + B_AR + 16384 * ((kPb >> (4 * p)) & 15u);
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
-#pragma unroll
-                for (int y = 0; y <= b; ++y) {
-                    mma_bf16(tbase + 16 * pair_lo(b, y), ad + y * 128, kdesc(bt + 2048 * b) + y * 2, id_k, p ? 1u : 0u);
-                    mma_bf16(tbase + B_RK + 16 * pair_lo(b, y), ad + y * 128, kdesc(bt + 8192 + 2048 * b) + y * 2,
-                             id_k, p ? 1u : 0u);
-                }
+            for (int y = 0; y < 4; ++y) {  // block y's columns j against every row i >= 16 y: N = 64 - 16 y
+                const uint32_t id = idesc_bf16_f32(128, 64 - 16 * y, true, false);
+                mma_bf16(tbase + 16 * pair_hi(y, y), ad + y * 128, kdesc(bt + 2048 * y) + y * 2, id, p ? 1u : 0u);
+                mma_bf16(tbase + B_RK + 16 * pair_hi(y, y), ad + y * 128, kdesc(bt + 8192 + 2048 * y) + y * 2, id,
+                         p ? 1u : 0u);
+            }
         }
         mma_commit(bM);
     }
@@ -1486,11 +1485,9 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
             const uint64_t ad = sdesc_sw128(sbase + B_OPB + 16384 * ((kPa >> (4 * p)) & 15u), 8192, 1024);
             const uint32_t bt = sbase + B_AR + 16384 * ((kPb >> (4 * p)) & 15u);
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
-#pragma unroll
-                for (int x = b; x < 4; ++x)
-                    mma_bf16(tbase + B_CS + 16 * pair_hi(b, x), ad + x * 128,
-                             sdesc_sw128(bt + 2048 * x + 32 * b, 8192, 1024), id_m, p ? 1u : 0u);
+            for (int x = 0; x < 4; ++x)  // block x's rows i against every column j < 16 (x + 1): N = 16 (x + 1)
+                mma_bf16(tbase + B_CS + 16 * pair_lo(x, 0), ad + x * 128, sdesc_sw128(bt + 2048 * x, 8192, 1024),
+                         idesc_bf16_f32(128, 16 * (x + 1), true, true), p ? 1u : 0u);
         }
     }
     // ---- B operand once the K operand's products are complete, then CK of every pair onto CQ's columns
@@ -1506,11 +1503,9 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
             const uint64_t ad = sdesc_sw128(sbase + B_OPA + 16384 * ((kPa >> (4 * p)) & 15u), 8192, 1024);
             const uint32_t bt = sbase + B_AR + 8192 + 16384 * ((kPb >> (4 * p)) & 15u);
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
-#pragma unroll
-                for (int x = b; x < 4; ++x)
-                    mma_bf16(tbase + B_CS + 16 * pair_hi(b, x), ad + x * 128,
-                             sdesc_sw128(bt + 2048 * x + 32 * b, 8192, 1024), id_m, 1u);
+            for (int x = 0; x < 4; ++x)
+                mma_bf16(tbase + B_CS + 16 * pair_lo(x, 0), ad + x * 128, sdesc_sw128(bt + 2048 * x, 8192, 1024),
+                         idesc_bf16_f32(128, 16 * (x + 1), true, true), 1u);
         }
         mma_commit(bM + 1);
     }
@@ -1558,11 +1553,11 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
         uint32_t tq[4][4], tk[4][4], ts[4][4];
 #pragma unroll
         for (int y = 0; y <= b; ++y) {
-            tmem_ld4_async(tbase + lb + 16 * pair_lo(b, y) + 4 * rg, tq[y]);
-            tmem_ld4_async(tbase + lb + B_RK + 16 * pair_lo(b, y) + 4 * rg, tk[y]);
+            tmem_ld4_async(tbase + lb + 16 * pair_hi(y, b) + 4 * rg, tq[y]);
+            tmem_ld4_async(tbase + lb + B_RK + 16 * pair_hi(y, b) + 4 * rg, tk[y]);
         }
 #pragma unroll
-        for (int x = b; x < 4; ++x) tmem_ld4_async(tbase + lb + B_CS + 16 * pair_hi(b, x) + 4 * rg, ts[x - b]);
+        for (int x = b; x < 4; ++x) tmem_ld4_async(tbase + lb + B_CS + 16 * pair_lo(x, b) + 4 * rg, ts[x - b]);
         tmem_wait_ld();
 #pragma unroll
         for (int y = 0; y <= b; ++y) { reg_fence(tq[y]); reg_fence(tk[y]); }
