@@ -73,6 +73,23 @@ __device__ __forceinline__ void nb_arrive(int id) {
 }
 __device__ __forceinline__ uint64_t kdesc(uint32_t saddr) { return sdesc_sw128(saddr, 16, 1024); }
 
+// One chunk's tiles on their way to L2 ahead of the copies that read them: its blob (131,840 bytes) and its
+// 64 rows of a bf16 [T, H, 128] tensor (rows past the sequence's end skipped); one 128-byte line per thread
+// per round.
+__device__ __forceinline__ void prefetch_chunk(const uint8_t* blob, const __nv_bfloat16* x, int64_t tok0, int L, int H,
+                                               int h, int tid, int nthreads) {
+    constexpr int kBlobLines = (int)(kBwdBlobBytes / 128);
+    static_assert(kBwdBlobBytes % 128 == 0, "whole lines");
+    for (int i = tid; i < kBlobLines + 2 * kC; i += nthreads) {
+        if (i < kBlobLines) {
+            prefetch_l2(blob + 128 * i);
+        } else {
+            const int r = (i - kBlobLines) >> 1;
+            if (r < L) prefetch_l2(x + ((tok0 + r) * H + h) * kD + 64 * ((i - kBlobLines) & 1));
+        }
+    }
+}
+
 // x = hi + lo, both bf16 (round to nearest even), packed in pairs
 __device__ __forceinline__ void split_pairs(const float* x, int n2, uint32_t* hi, uint32_t* lo) {
     for (int j = 0; j < n2; ++j) {
@@ -85,10 +102,10 @@ __device__ __forceinline__ void split_pairs(const float* x, int n2, uint32_t* hi
 
 template <typename InT>
 __global__ void __launch_bounds__(kThreads, 1)
-bwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const float* __restrict__ d_final,
-                    const int32_t* __restrict__ cu, int64_t T_total, int H, const uint8_t* __restrict__ blobs,
-                    float* __restrict__ d_init, float* __restrict__ dS_next, float* __restrict__ dZ_out,
-                    unsigned int* err) {
+bwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __nv_bfloat16* __restrict__ d_o,
+                    const float* __restrict__ d_final, const int32_t* __restrict__ cu, int64_t T_total, int H,
+                    const uint8_t* __restrict__ blobs, float* __restrict__ d_init, float* __restrict__ dS_next,
+                    float* __restrict__ dZ_out, unsigned int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
@@ -297,12 +314,9 @@ bwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const float* __re
             const int64_t c0 = bos + (int64_t)kC * ci;
             const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
             const int64_t base = (c0 / kC + n) * H + h;
-            // dS at the chunk's end, for the per-chunk kernel
-            {
-                float* dst = dS_next + (base * kD + row) * kD + 32 * qq;
-#pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    *reinterpret_cast<float4*>(dst + e) = make_float4(s[e], s[e + 1], s[e + 2], s[e + 3]);
+            if (ci >= 2) {  // the tiles two chunks on (in this pass's order) on their way to L2
+                const int64_t c2 = c0 - 2 * kC;
+                prefetch_chunk(blob_of(ci - 2), d_o, c2, kC, H, h, tid, kSimt);
             }
             {  // dS as bf16 hi + lo, the A operand of dS Kr^T
                 uint32_t hi[16], lo[16];
@@ -313,6 +327,13 @@ bwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const float* __re
             }
             tc_fence_before();
             nb_arrive(NB_S);
+            // dS at the chunk's end, for the per-chunk kernel (stored once the product warp has it)
+            {
+                float* dst = dS_next + (base * kD + row) * kD + 32 * qq;
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4*>(dst + e) = make_float4(s[e], s[e + 1], s[e + 2], s[e + 3]);
+            }
             // ---- dV'^T: tokens 16 qq .. +15 of row `row`, back to TMEM as hi + lo
             nb_sync(NB_1);
             tc_fence_after();
@@ -340,20 +361,20 @@ bwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const float* __re
                 tmem_wait_ld(); reg_fence(y);
                 float z[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int t = 16 * qq + e;
-                    const float dz = __uint_as_float(y[e]);
-                    if (t < L) dZ_out[((c0 + t) * H + h) * kD + row] = dz;
-                    z[e] = -sBeta[t] * dz;
-                }
+                for (int e = 0; e < 16; ++e) z[e] = -sBeta[16 * qq + e] * __uint_as_float(y[e]);
                 uint32_t hi[8], lo[8];
                 split_pairs(z, 8, hi, lo);
                 tmem_st8(tbase + lane_base + TM_ZH + 8 * qq, hi);
                 tmem_st8(tbase + lane_base + TM_ZL + 8 * qq, lo);
                 tmem_wait_st();
+                tc_fence_before();
+                nb_arrive(NB_Z);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {  // dZ out, once the product warp has -beta dZ
+                    const int t = 16 * qq + e;
+                    if (t < L) dZ_out[((c0 + t) * H + h) * kD + row] = __uint_as_float(y[e]);
+                }
             }
-            tc_fence_before();
-            nb_arrive(NB_Z);
             // ---- dS <- dS Diag(gamma) + increment.  A stop is taken here only, where the product warp
             //      takes it (it reads the flag before this hand-off), so both sides leave at the same barrier.
             nb_sync(NB_3);
@@ -395,15 +416,18 @@ constexpr uint32_t F_TT = 65536;      // T hi, lo       [64][64] x 2 (K-major B 
 constexpr uint32_t F_V = 81920;       // v              [64 t][64 r] x 2 regions
 constexpr uint32_t F_GAM = 98304;     // gamma fp32 [128] (with Kr)
 constexpr uint32_t F_BETA = 98816;    // beta fp32 [64] (with T)
-constexpr uint32_t F_BAR = 99328;     // mbarriers: KG, KR, TT, V, D1, D2, D3
+constexpr uint32_t F_BAR = 99328;     // mbarriers: KG (even chunks), KR, TT, V, D1, D2, D3, KG (odd chunks)
 constexpr uint32_t F_MISC = F_BAR + 64;
-constexpr uint32_t kFwdSmem = F_MISC + 16 + 1024;
-static_assert(F_V % 1024 == 0 && F_TT % 1024 == 0 && F_BAR % 8 == 0, "alignment");
+constexpr uint32_t F_KG1 = 100352;    // Kg hi, lo of odd chunks (even ones at F_KG): copied two chunks ahead
+constexpr uint32_t kFwdSmem = F_KG1 + 32768 + 1024;
+static_assert(F_V % 1024 == 0 && F_TT % 1024 == 0 && F_BAR % 8 == 0 && F_KG1 % 1024 == 0 && F_MISC + 16 <= F_KG1,
+              "alignment");
 
 __global__ void __launch_bounds__(kThreads, 1)
-bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const float* __restrict__ init_state,
-                        const int32_t* __restrict__ cu, int64_t T_total, int H, const uint8_t* __restrict__ blobs,
-                        float* __restrict__ S0s, float* __restrict__ Rb, float* __restrict__ Vp, unsigned int* err) {
+bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16* __restrict__ v,
+                        const float* __restrict__ init_state, const int32_t* __restrict__ cu, int64_t T_total, int H,
+                        const uint8_t* __restrict__ blobs, float* __restrict__ S0s, float* __restrict__ Rb,
+                        float* __restrict__ Vp, unsigned int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
@@ -414,7 +438,8 @@ bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const float* _
     const int nch = (int)((eos - bos + kC - 1) / kC);
     const int row = tid & 127, qq = (tid >> 7) & 3;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    // copy barriers bB + w: 0 Kg, 1 Kr and gamma, 2 T and beta, 3 v; then the three product barriers
+    // copy barriers bB + w: 0 Kg (even chunks), 1 Kr and gamma, 2 T and beta, 3 v; then the three product barriers;
+    // bB + 7 Kg (odd chunks)
     uint64_t* bB = reinterpret_cast<uint64_t*>(sm + F_BAR);
     uint64_t* bD1 = bB + 4;
     uint64_t* bD2 = bB + 5;
@@ -423,7 +448,7 @@ bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const float* _
     volatile int* sAbort = reinterpret_cast<volatile int*>(sm + F_MISC + 4);
     volatile int* sStop = reinterpret_cast<volatile int*>(sm + F_MISC + 8);
     if (tid == 0) {
-        for (int i = 0; i < 7; ++i) mbar_init(bB + i, 1);
+        for (int i = 0; i < 8; ++i) mbar_init(bB + i, 1);
         fence_mbar_init();
         *sAbort = 0;
         *sStop = 0;
@@ -460,7 +485,9 @@ bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const float* _
             __syncwarp();
             iss ^= 1u << which;
         };
-        auto load_kg = [&](int ci) { copy(0, F_KG, blob_of(ci) + kBB_KG, 32768, 0, nullptr, 0); };
+        auto load_kg = [&](int ci) {
+            copy((ci & 1) ? 7 : 0, (ci & 1) ? F_KG1 : F_KG, blob_of(ci) + kBB_KG, 32768, 0, nullptr, 0);
+        };
         auto load_kr = [&](int ci) { copy(1, F_KR, blob_of(ci) + kBB_KR, 32768, F_GAM, blob_of(ci) + kBB_GAM, 512); };
         auto load_tt = [&](int ci) { copy(2, F_TT, blob_of(ci) + kBB_TT, 16384, F_BETA, blob_of(ci) + kBB_BETA, 256); };
         auto load_v = [&](int ci) {
@@ -487,16 +514,17 @@ bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const float* _
             load_v(0);
             load_tt(0);
             load_kr(0);
+            if (nch > 1) load_kg(1);
         }
         for (int ci = 0; ci < nch; ++ci) {
             const bool more = ci + 1 < nch;
             nb_sync(NB_S);  // S hi/lo in TMEM; gamma of the chunk before read
             if (ci > 0) load_kr(ci);
             // ---- D1 = S Kg^T (hi.hi + hi.lo + lo.hi)
-            use(0);
+            use((ci & 1) ? 7 : 0);
             tc_fence_after();
             {
-                const uint32_t kh = sbase + F_KG, kl = sbase + F_KG + 16384;
+                const uint32_t kh = sbase + ((ci & 1) ? F_KG1 : F_KG), kl = kh + 16384;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
                     mma_bf16_ta(tbase + F_D1, tbase + F_SH + 8 * ks, kdesc(kh + (ks >> 2) * 8192) + (ks & 3) * 2, id_kg, ks > 0 ? 1u : 0u);
@@ -514,7 +542,7 @@ bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const float* _
             p1 ^= 1u;
             tc_fence_before();
             nb_arrive(NB_1);
-            if (more) load_kg(ci + 1);  // Kg consumed
+            if (ci + 2 < nch) load_kg(ci + 2);  // this buffer's Kg consumed
             // ---- D2 = (beta R)^T T^T (hi.hi + hi.lo + lo.hi) = V'^T
             nb_sync(NB_V);  // beta R hi/lo in TMEM; v and beta read
             if (more) load_v(ci + 1);
@@ -557,8 +585,9 @@ bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const float* _
             if (stop) break;
         }
         if (*sAbort && lane == 0) {
-            for (int w = 0; w < 4; ++w)
-                if (((iss ^ ph) >> w) & 1u) mbar_wait(bB + w, (ph >> w) & 1u, kWaitLimit);
+            for (int w = 0; w < 8; ++w)
+                if (w < 4 || w == 7)
+                    if (((iss ^ ph) >> w) & 1u) mbar_wait(bB + w, (ph >> w) & 1u, kWaitLimit);
         }
         __syncwarp();
     } else {
@@ -572,15 +601,13 @@ bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const float* _
         }
         const float* sGam = reinterpret_cast<const float*>(sm + F_GAM);
         const float* sBeta = reinterpret_cast<const float*>(sm + F_BETA);
+        // Each operand goes to TMEM first and is handed to the product warp; its global copy (S0, R, V') is
+        // stored after the hand-off, while the next product runs.
         for (int ci = 0; ci < nch; ++ci) {
             const int64_t c0 = bos + (int64_t)kC * ci;
             const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
             const int64_t base = (c0 / kC + n) * H + h;
-            {  // the state entering the chunk
-                float* dst = S0s + (base * kD + row) * kD + 32 * qq;
-#pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    *reinterpret_cast<float4*>(dst + e) = make_float4(s[e], s[e + 1], s[e + 2], s[e + 3]);
+            {  // the state entering the chunk, as hi + lo
                 uint32_t hi[16], lo[16];
                 split_pairs(s, 16, hi, lo);
                 tmem_st16(tbase + lane_base + F_SH + 16 * qq, hi);
@@ -589,37 +616,51 @@ bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const float* _
             }
             tc_fence_before();
             nb_arrive(NB_S);
-            // ---- R = V - Kg S^T (kept), beta R to TMEM as hi + lo
-            nb_sync(NB_1);
-            tc_fence_after();
+            {  // ... and kept
+                float* dst = S0s + (base * kD + row) * kD + 32 * qq;
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    *reinterpret_cast<float4*>(dst + e) = make_float4(s[e], s[e + 1], s[e + 2], s[e + 3]);
+            }
+            // v[t][row] of the chunk's tokens 16 qq .. +15 (the TMA tile: [64 t][64 r] per half of the rows), read
+            // as soon as its copy has landed (phase ci % 2 of its barrier), before the product S Kg^T is ready
+            float x[16];
             {
-                // v[t][row] of the chunk's tokens 16 qq .. +15 (the TMA tile: [64 t][64 r] per half of the rows)
+                if (!mbar_wait(bB + 3, (uint32_t)(ci & 1), kWaitLimit)) raise_device_error(err, kErrMbarTimeout);
                 const uint8_t* vt = sm + F_V + (row >> 6) * 8192;
-                float x[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int t = 16 * qq + e;
                     const uint32_t at = sw128((uint32_t)t, (uint32_t)((row & 63) >> 3)) + (uint32_t)(row & 7) * 2u;
                     x[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(vt + at));
                 }
+            }
+            // ---- R = V - Kg S^T (kept), beta R to TMEM as hi + lo
+            nb_sync(NB_1);
+            tc_fence_after();
+            {
                 uint32_t y[16];
                 tmem_ld16_async(tbase + lane_base + F_D1 + 16 * qq, y);
                 tmem_wait_ld(); reg_fence(y);
+                float br[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const int t = 16 * qq + e;
-                    const float r = x[e] - __uint_as_float(y[e]);
-                    if (t < L) Rb[((c0 + t) * H + h) * kD + row] = r;
-                    x[e] = sBeta[t] * r;
+                    x[e] -= __uint_as_float(y[e]);
+                    br[e] = sBeta[16 * qq + e] * x[e];
                 }
                 uint32_t hi[8], lo[8];
-                split_pairs(x, 8, hi, lo);
+                split_pairs(br, 8, hi, lo);
                 tmem_st8(tbase + lane_base + F_RH + 8 * qq, hi);
                 tmem_st8(tbase + lane_base + F_RL + 8 * qq, lo);
                 tmem_wait_st();
             }
             tc_fence_before();
             nb_arrive(NB_V);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int t = 16 * qq + e;
+                if (t < L) Rb[((c0 + t) * H + h) * kD + row] = x[e];
+            }
             // ---- V' (kept), to TMEM as hi + lo
             nb_sync(NB_2);
             tc_fence_after();
@@ -627,13 +668,8 @@ bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const float* _
                 uint32_t y[16];
                 tmem_ld16_async(tbase + lane_base + F_D2 + 16 * qq, y);
                 tmem_wait_ld(); reg_fence(y);
-                float x[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int t = 16 * qq + e;
-                    x[e] = __uint_as_float(y[e]);
-                    if (t < L) Vp[((c0 + t) * H + h) * kD + row] = x[e];
-                }
+                for (int e = 0; e < 16; ++e) x[e] = __uint_as_float(y[e]);
                 uint32_t hi[8], lo[8];
                 split_pairs(x, 8, hi, lo);
                 tmem_st8(tbase + lane_base + F_VH + 8 * qq, hi);
@@ -642,6 +678,11 @@ bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const float* _
             }
             tc_fence_before();
             nb_arrive(NB_Z);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int t = 16 * qq + e;
+                if (t < L) Vp[((c0 + t) * H + h) * kD + row] = x[e];
+            }
             // ---- S <- S Diag(gamma) + V'^T Kr
             nb_sync(NB_3);
             tc_fence_after();
@@ -1672,7 +1713,8 @@ cudaError_t launch_bwd_fwd_state_tc(const void* v, const float* init_state, cons
     const int64_t chains = (int64_t)N * H;
     if (chains == 0) return cudaSuccess;
     bwd_fwd_state_tc_kernel<<<(unsigned)chains, kThreads, kFwdSmem, stream>>>(
-        tm, init_state, cu_seqlens, T_total, H, static_cast<const uint8_t*>(blobs), S0s, R, Vp, err);
+        tm, static_cast<const __nv_bfloat16*>(v), init_state, cu_seqlens, T_total, H, static_cast<const uint8_t*>(blobs),
+        S0s, R, Vp, err);
     return cudaGetLastError();
 }
 
@@ -1687,7 +1729,8 @@ cudaError_t launch_bwd_state_tc(const void* d_o, const float* d_final, const int
     const int64_t chains = (int64_t)N * H;
     if (chains == 0) return cudaSuccess;
     bwd_state_tc_kernel<__nv_bfloat16><<<(unsigned)chains, kThreads, kSmem, stream>>>(
-        tm, d_final, cu_seqlens, T_total, H, static_cast<const uint8_t*>(blobs), d_init, dS_next, dZ, err);
+        tm, static_cast<const __nv_bfloat16*>(d_o), d_final, cu_seqlens, T_total, H, static_cast<const uint8_t*>(blobs),
+        d_init, dS_next, dZ, err);
     return cudaGetLastError();
 }
 
