@@ -68,6 +68,8 @@ constexpr uint32_t TM_D1 = 0, TM_D2 = 64, TM_D3 = 128, TM_SH = 256, TM_SL = 320,
                    TM_ZH = 448, TM_ZL = 480;
 
 __device__ __forceinline__ void nb_sync(int id) { asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kThreads) : "memory"); }
+// The 16 state warps among themselves (named barrier 7; the product warp does not take part).
+__device__ __forceinline__ void state_sync() { asm volatile("bar.sync 7, %0;" ::"n"(kSimt) : "memory"); }
 __device__ __forceinline__ void nb_arrive(int id) {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "n"(kThreads) : "memory");
 }
@@ -419,12 +421,16 @@ constexpr uint32_t F_BETA = 98816;    // beta fp32 [64] (with T)
 constexpr uint32_t F_BAR = 99328;     // mbarriers: KG (even chunks), KR, TT, V, D1, D2, D3, KG (odd chunks)
 constexpr uint32_t F_MISC = F_BAR + 64;
 constexpr uint32_t F_KG1 = 100352;    // Kg hi, lo of odd chunks (even ones at F_KG): copied two chunks ahead
-constexpr uint32_t kFwdSmem = F_KG1 + 32768 + 1024;
-static_assert(F_V % 1024 == 0 && F_TT % 1024 == 0 && F_BAR % 8 == 0 && F_KG1 % 1024 == 0 && F_MISC + 16 <= F_KG1,
+constexpr uint32_t F_S0 = 133120;     // S0 fp32 staged for its TMA store: four boxes of [128 rows][32 channels],
+                                      // 128-byte swizzle
+constexpr uint32_t kFwdSmem = F_S0 + 65536 + 1024;
+static_assert(F_V % 1024 == 0 && F_TT % 1024 == 0 && F_BAR % 8 == 0 && F_KG1 % 1024 == 0 && F_MISC + 16 <= F_KG1 &&
+                  F_S0 % 1024 == 0 && F_S0 >= F_KG1 + 32768 && kFwdSmem <= 232448,
               "alignment");
 
 __global__ void __launch_bounds__(kThreads, 1)
-bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const __nv_bfloat16* __restrict__ v,
+bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_s0,
+                        const __nv_bfloat16* __restrict__ v,
                         const float* __restrict__ init_state, const int32_t* __restrict__ cu, int64_t T_total, int H,
                         const uint8_t* __restrict__ blobs, float* __restrict__ S0s, float* __restrict__ Rb,
                         float* __restrict__ Vp, unsigned int* err) {
@@ -616,11 +622,20 @@ bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const __nv_bfl
             }
             tc_fence_before();
             nb_arrive(NB_S);
-            {  // ... and kept
-                float* dst = S0s + (base * kD + row) * kD + 32 * qq;
+            {  // ... and kept: staged (the tile is free: its previous copies finished reading before NB_3), then
+               // stored by TMA as four boxes of channels 32 qq .. +31
+                uint8_t* box = sm + F_S0 + qq * 16384 + row * 128;
 #pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    *reinterpret_cast<float4*>(dst + e) = make_float4(s[e], s[e + 1], s[e + 2], s[e + 3]);
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<float4*>(box + ((c ^ (row & 7)) << 4)) =
+                        make_float4(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
+                fence_proxy_async();
+                state_sync();
+                if (tid == 0) {
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) tma_store_2d(&tm_s0, sm + F_S0 + b * 16384, 32 * b, (int)(base * kD));
+                    bulk_commit();
+                }
             }
             // v[t][row] of the chunk's tokens 16 qq .. +15 (the TMA tile: [64 t][64 r] per half of the rows), read
             // as soon as its copy has landed (phase ci % 2 of its barrier), before the product S Kg^T is ready
@@ -684,6 +699,7 @@ bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const __nv_bfl
                 if (t < L) Vp[((c0 + t) * H + h) * kD + row] = x[e];
             }
             // ---- S <- S Diag(gamma) + V'^T Kr
+            if (tid == 0) bulk_wait_read();  // the S0 tile is free for the next chunk once every thread is past NB_3
             nb_sync(NB_3);
             tc_fence_after();
             if (*sStop) break;
@@ -699,6 +715,7 @@ bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const __nv_bfl
                 for (int e = 0; e < 32; ++e) s[e] = fmaf(s[e], gm[e], __uint_as_float(d3[e]));
             }
         }
+        if (tid == 0) bulk_wait_all();  // the S0 copies are complete before the CTA ends
     }
     tc_fence_before();
     __syncthreads();
@@ -1705,15 +1722,30 @@ static bool encode_token_map(CUtensorMap* tm, const void* base, int64_t T_total,
 cudaError_t launch_bwd_fwd_state_tc(const void* v, const float* init_state, const int32_t* cu_seqlens, int N,
                                     int64_t T_total, int H, const void* blobs, float* S0s, float* R, float* Vp,
                                     unsigned int* err, cudaStream_t stream) {
-    CUtensorMap tm;
+    CUtensorMap tm, tm_s0;
     if (!encode_token_map(&tm, v, T_total, H)) return cudaErrorInvalidValue;
+    {  // S0s as rows of 128 fp32 (slot, head, row), stored in boxes of [128 rows][32 channels] with the 128-byte
+       // swizzle
+        auto fn = encoder();
+        if (!fn) return cudaErrorInvalidValue;
+        const cuuint64_t rows = (cuuint64_t)(T_total / kC + N + 1) * (cuuint64_t)H * kD;
+        const cuuint64_t dims[2] = {128, rows};
+        const cuuint64_t strides[1] = {128 * 4};
+        const cuuint32_t box[2] = {32, 128};
+        const cuuint32_t estr[2] = {1, 1};
+        if (rows >= ((cuuint64_t)1 << 31) ||
+            fn(&tm_s0, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, S0s, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+                CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     cudaError_t e = cudaFuncSetAttribute(bwd_fwd_state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kFwdSmem);
     if (e != cudaSuccess) return e;
     const int64_t chains = (int64_t)N * H;
     if (chains == 0) return cudaSuccess;
     bwd_fwd_state_tc_kernel<<<(unsigned)chains, kThreads, kFwdSmem, stream>>>(
-        tm, static_cast<const __nv_bfloat16*>(v), init_state, cu_seqlens, T_total, H, static_cast<const uint8_t*>(blobs),
+        tm, tm_s0, static_cast<const __nv_bfloat16*>(v), init_state, cu_seqlens, T_total, H, static_cast<const uint8_t*>(blobs),
         S0s, R, Vp, err);
     return cudaGetLastError();
 }

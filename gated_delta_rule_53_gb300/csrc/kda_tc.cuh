@@ -280,6 +280,20 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
         : "memory");
 }
 
+// TMA store: one thread copies a shared-memory box to the tensor described by a CUtensorMap (the box's
+// layout and swizzle as for a load).  Stores are grouped per thread: bulk_commit() closes a group,
+// bulk_wait_read() waits until every committed group has finished reading shared memory (the source
+// may be overwritten), bulk_wait_all() until their writes are done.  The innermost coordinate times
+// the element size must be a multiple of 16 bytes, and no coordinate may be negative.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, const void* src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // One arrival on an mbarrier (no transaction bytes).
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
