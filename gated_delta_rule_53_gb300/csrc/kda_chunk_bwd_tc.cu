@@ -59,8 +59,12 @@ constexpr uint32_t R_GAM = 180224;      // gamma fp32 [128] (with Kg)
 constexpr uint32_t R_BETA = 180736;     // beta fp32 [64] (with T)
 constexpr uint32_t R_BAR = 181248;      // mbarriers: KR, QG, KG, TT, AQ/DO x2, D1, D2, D3
 constexpr uint32_t R_MISC = R_BAR + 128;
-constexpr uint32_t kSmem = R_MISC + 16 + 1024;
-static_assert(R_AQ % 1024 == 0 && R_DO % 1024 == 0 && R_TT % 1024 == 0 && R_BAR % 8 == 0, "alignment");
+constexpr uint32_t R_DSN = 182272;      // dS_next fp32 staged for its TMA store: two boxes of [128 rows][32 channels]
+                                        // at a time (channels 0-63, then 64-127), 128-byte swizzle
+constexpr uint32_t kSmem = R_DSN + 32768 + 1024;
+static_assert(R_AQ % 1024 == 0 && R_DO % 1024 == 0 && R_TT % 1024 == 0 && R_BAR % 8 == 0 && R_DSN % 1024 == 0 &&
+                  R_MISC + 16 <= R_DSN,
+              "alignment");
 static_assert(kSmem <= 232448, "shared memory");
 
 // TMEM columns
@@ -104,7 +108,8 @@ __device__ __forceinline__ void split_pairs(const float* x, int n2, uint32_t* hi
 
 template <typename InT>
 __global__ void __launch_bounds__(kThreads, 1)
-bwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __nv_bfloat16* __restrict__ d_o,
+bwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dsn,
+                    const __nv_bfloat16* __restrict__ d_o,
                     const float* __restrict__ d_final, const int32_t* __restrict__ cu, int64_t T_total, int H,
                     const uint8_t* __restrict__ blobs, float* __restrict__ d_init, float* __restrict__ dS_next,
                     float* __restrict__ dZ_out, unsigned int* err) {
@@ -329,12 +334,29 @@ bwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __nv_bfloat
             }
             tc_fence_before();
             nb_arrive(NB_S);
-            // dS at the chunk's end, for the per-chunk kernel (stored once the product warp has it)
-            {
-                float* dst = dS_next + (base * kD + row) * kD + 32 * qq;
+            // dS at the chunk's end, for the per-chunk kernel, once the product warp has it: staged and stored by
+            // TMA, channels 0-63 (quarters 0, 1) then 64-127 (the tile is free at the start: its previous copies
+            // finished reading before NB_3)
 #pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    *reinterpret_cast<float4*>(dst + e) = make_float4(s[e], s[e + 1], s[e + 2], s[e + 3]);
+            for (int half = 0; half < 2; ++half) {
+                if (half) {
+                    if (tid == 0) bulk_wait_read();
+                    state_sync();
+                }
+                if ((qq >> 1) == half) {
+                    uint8_t* box = sm + R_DSN + (qq & 1) * 16384 + row * 128;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<float4*>(box + ((c ^ (row & 7)) << 4)) =
+                            make_float4(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
+                }
+                fence_proxy_async();
+                state_sync();
+                if (tid == 0) {
+                    tma_store_2d(&tm_dsn, sm + R_DSN, 64 * half, (int)(base * kD));
+                    tma_store_2d(&tm_dsn, sm + R_DSN + 16384, 64 * half + 32, (int)(base * kD));
+                    bulk_commit();
+                }
             }
             // ---- dV'^T: tokens 16 qq .. +15 of row `row`, back to TMEM as hi + lo
             nb_sync(NB_1);
@@ -379,6 +401,7 @@ bwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __nv_bfloat
             }
             // ---- dS <- dS Diag(gamma) + increment.  A stop is taken here only, where the product warp
             //      takes it (it reads the flag before this hand-off), so both sides leave at the same barrier.
+            if (tid == 0) bulk_wait_read();  // the dS_next tile is free for the next chunk past NB_3
             nb_sync(NB_3);
             tc_fence_after();
             if (*sStop) break;
@@ -394,6 +417,7 @@ bwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __nv_bfloat
                 for (int e = 0; e < 32; ++e) s[e] = fmaf(s[e], gm[e], __uint_as_float(d3[e]));
             }
         }
+        if (tid == 0) bulk_wait_all();  // the dS_next copies are complete before the CTA ends
         if (!*sStop && d_init) {
             float* dst = d_init + state_off + (int64_t)row * kD + 32 * qq;
 #pragma unroll
@@ -1719,26 +1743,28 @@ static bool encode_token_map(CUtensorMap* tm, const void* base, int64_t T_total,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Per-chunk states ([slot][head] of 128 x 128 fp32, slots below T_total / 64 + N + 1) as rows of 128 fp32, stored
+// in boxes of [128 rows][32 channels] with the 128-byte swizzle.
+static bool encode_state_rows_map(CUtensorMap* tm, void* base, int N, int64_t T_total, int H) {
+    auto fn = encoder();
+    if (!fn) return false;
+    const cuuint64_t rows = (cuuint64_t)(T_total / kC + N + 1) * (cuuint64_t)H * kD;
+    if (rows >= ((cuuint64_t)1 << 31)) return false;  // 32-bit box coordinates
+    const cuuint64_t dims[2] = {128, rows};
+    const cuuint64_t strides[1] = {128 * 4};
+    const cuuint32_t box[2] = {32, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 cudaError_t launch_bwd_fwd_state_tc(const void* v, const float* init_state, const int32_t* cu_seqlens, int N,
                                     int64_t T_total, int H, const void* blobs, float* S0s, float* R, float* Vp,
                                     unsigned int* err, cudaStream_t stream) {
     CUtensorMap tm, tm_s0;
     if (!encode_token_map(&tm, v, T_total, H)) return cudaErrorInvalidValue;
-    {  // S0s as rows of 128 fp32 (slot, head, row), stored in boxes of [128 rows][32 channels] with the 128-byte
-       // swizzle
-        auto fn = encoder();
-        if (!fn) return cudaErrorInvalidValue;
-        const cuuint64_t rows = (cuuint64_t)(T_total / kC + N + 1) * (cuuint64_t)H * kD;
-        const cuuint64_t dims[2] = {128, rows};
-        const cuuint64_t strides[1] = {128 * 4};
-        const cuuint32_t box[2] = {32, 128};
-        const cuuint32_t estr[2] = {1, 1};
-        if (rows >= ((cuuint64_t)1 << 31) ||
-            fn(&tm_s0, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, S0s, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-                CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
+    if (!encode_state_rows_map(&tm_s0, S0s, N, T_total, H)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(bwd_fwd_state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kFwdSmem);
     if (e != cudaSuccess) return e;
@@ -1753,15 +1779,16 @@ cudaError_t launch_bwd_fwd_state_tc(const void* v, const float* init_state, cons
 cudaError_t launch_bwd_state_tc(const void* d_o, const float* d_final, const int32_t* cu_seqlens, int N,
                                 int64_t T_total, int H, const void* blobs, float* d_init, float* dS_next, float* dZ,
                                 unsigned int* err, cudaStream_t stream) {
-    CUtensorMap tm;
+    CUtensorMap tm, tm_dsn;
     if (!encode_token_map(&tm, d_o, T_total, H)) return cudaErrorInvalidValue;
+    if (!encode_state_rows_map(&tm_dsn, dS_next, N, T_total, H)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(bwd_state_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmem);
     if (e != cudaSuccess) return e;
     const int64_t chains = (int64_t)N * H;
     if (chains == 0) return cudaSuccess;
     bwd_state_tc_kernel<__nv_bfloat16><<<(unsigned)chains, kThreads, kSmem, stream>>>(
-        tm, static_cast<const __nv_bfloat16*>(d_o), d_final, cu_seqlens, T_total, H, static_cast<const uint8_t*>(blobs),
+        tm, tm_dsn, static_cast<const __nv_bfloat16*>(d_o), d_final, cu_seqlens, T_total, H, static_cast<const uint8_t*>(blobs),
         d_init, dS_next, dZ, err);
     return cudaGetLastError();
 }
