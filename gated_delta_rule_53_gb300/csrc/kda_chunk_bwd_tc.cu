@@ -72,6 +72,18 @@ constexpr uint32_t TM_D1 = 0, TM_D2 = 64, TM_D3 = 128, TM_SH = 256, TM_SL = 320,
                    TM_ZH = 448, TM_ZL = 480;
 
 __device__ __forceinline__ void nb_sync(int id) { asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kThreads) : "memory"); }
+// Element (token t, value row r) of a chunk's [64 t][128 r] fp32 tile staged as four boxes of [64 t][32 r]
+// (boxes 8 KB apart, 128-byte swizzle): thread (r, quarter) writes its tokens 16 quarter .. +15.
+__device__ __forceinline__ void stage_token_tile(uint8_t* tile, int r, int quarter, const float (&x)[16]) {
+    uint8_t* box = tile + (r >> 5) * 8192;
+    const int col = r & 31;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        const int t = 16 * quarter + e;
+        *reinterpret_cast<float*>(box + t * 128 + ((((col >> 2) ^ (t & 7))) << 4) + (col & 3) * 4) = x[e];
+    }
+}
+
 // The 16 state warps among themselves (named barrier 7; the product warp does not take part).
 __device__ __forceinline__ void state_sync() { asm volatile("bar.sync 7, %0;" ::"n"(kSimt) : "memory"); }
 __device__ __forceinline__ void nb_arrive(int id) {
@@ -109,6 +121,7 @@ __device__ __forceinline__ void split_pairs(const float* x, int n2, uint32_t* hi
 template <typename InT>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dsn,
+                    const __grid_constant__ CUtensorMap tm_dz,
                     const __nv_bfloat16* __restrict__ d_o,
                     const float* __restrict__ d_final, const int32_t* __restrict__ cu, int64_t T_total, int H,
                     const uint8_t* __restrict__ blobs, float* __restrict__ d_init, float* __restrict__ dS_next,
@@ -393,15 +406,33 @@ bwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_cons
                 tmem_wait_st();
                 tc_fence_before();
                 nb_arrive(NB_Z);
+                // dZ out, once the product warp has -beta dZ: a whole chunk through the dS_next tile by TMA (once
+                // dS_next's copies have read it), the sequence's partial last chunk row by row
+                float dzv[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {  // dZ out, once the product warp has -beta dZ
-                    const int t = 16 * qq + e;
-                    if (t < L) dZ_out[((c0 + t) * H + h) * kD + row] = __uint_as_float(y[e]);
+                for (int e = 0; e < 16; ++e) dzv[e] = __uint_as_float(y[e]);
+                if (L == kC) {
+                    if (tid == 0) bulk_wait_read();
+                    state_sync();
+                    stage_token_tile(sm + R_DSN, row, qq, dzv);
+                    fence_proxy_async();
+                    state_sync();
+                    if (tid == 0) {
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) tma_store_3d(&tm_dz, sm + R_DSN + b * 8192, 32 * b, h, (int)c0);
+                        bulk_commit();
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int t = 16 * qq + e;
+                        if (t < L) dZ_out[((c0 + t) * H + h) * kD + row] = dzv[e];
+                    }
                 }
             }
             // ---- dS <- dS Diag(gamma) + increment.  A stop is taken here only, where the product warp
             //      takes it (it reads the flag before this hand-off), so both sides leave at the same barrier.
-            if (tid == 0) bulk_wait_read();  // the dS_next tile is free for the next chunk past NB_3
+            if (tid == 0) bulk_wait_read();  // the staging tile is free for the next chunk past NB_3
             nb_sync(NB_3);
             tc_fence_after();
             if (*sStop) break;
@@ -447,13 +478,17 @@ constexpr uint32_t F_MISC = F_BAR + 64;
 constexpr uint32_t F_KG1 = 100352;    // Kg hi, lo of odd chunks (even ones at F_KG): copied two chunks ahead
 constexpr uint32_t F_S0 = 133120;     // S0 fp32 staged for its TMA store: four boxes of [128 rows][32 channels],
                                       // 128-byte swizzle
-constexpr uint32_t kFwdSmem = F_S0 + 65536 + 1024;
+constexpr uint32_t F_RV = 198656;     // R, then V', of a whole chunk staged for their TMA stores: four boxes of
+                                      // [64 tokens][32 rows], 128-byte swizzle
+constexpr uint32_t kFwdSmem = F_RV + 32768 + 1024;
 static_assert(F_V % 1024 == 0 && F_TT % 1024 == 0 && F_BAR % 8 == 0 && F_KG1 % 1024 == 0 && F_MISC + 16 <= F_KG1 &&
-                  F_S0 % 1024 == 0 && F_S0 >= F_KG1 + 32768 && kFwdSmem <= 232448,
+                  F_S0 % 1024 == 0 && F_S0 >= F_KG1 + 32768 && F_RV % 1024 == 0 && F_RV >= F_S0 + 65536 &&
+                  kFwdSmem <= 232448,
               "alignment");
 
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_s0,
+                        const __grid_constant__ CUtensorMap tm_r, const __grid_constant__ CUtensorMap tm_vp,
                         const __nv_bfloat16* __restrict__ v,
                         const float* __restrict__ init_state, const int32_t* __restrict__ cu, int64_t T_total, int H,
                         const uint8_t* __restrict__ blobs, float* __restrict__ S0s, float* __restrict__ Rb,
@@ -695,10 +730,21 @@ bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_c
             }
             tc_fence_before();
             nb_arrive(NB_V);
+            if (L == kC) {  // a whole chunk: staged and stored by TMA (the tile is free: see NB_3)
+                stage_token_tile(sm + F_RV, row, qq, x);
+                fence_proxy_async();
+                state_sync();
+                if (tid == 0) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int t = 16 * qq + e;
-                if (t < L) Rb[((c0 + t) * H + h) * kD + row] = x[e];
+                    for (int b = 0; b < 4; ++b) tma_store_3d(&tm_r, sm + F_RV + b * 8192, 32 * b, h, (int)c0);
+                    bulk_commit();
+                }
+            } else {  // the sequence's last, partial chunk: the rows past its end belong to the next sequence
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int t = 16 * qq + e;
+                    if (t < L) Rb[((c0 + t) * H + h) * kD + row] = x[e];
+                }
             }
             // ---- V' (kept), to TMEM as hi + lo
             nb_sync(NB_2);
@@ -717,13 +763,26 @@ bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_c
             }
             tc_fence_before();
             nb_arrive(NB_Z);
+            if (L == kC) {  // as R, once R's copies have read the tile
+                if (tid == 0) bulk_wait_read();
+                state_sync();
+                stage_token_tile(sm + F_RV, row, qq, x);
+                fence_proxy_async();
+                state_sync();
+                if (tid == 0) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int t = 16 * qq + e;
-                if (t < L) Vp[((c0 + t) * H + h) * kD + row] = x[e];
+                    for (int b = 0; b < 4; ++b) tma_store_3d(&tm_vp, sm + F_RV + b * 8192, 32 * b, h, (int)c0);
+                    bulk_commit();
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int t = 16 * qq + e;
+                    if (t < L) Vp[((c0 + t) * H + h) * kD + row] = x[e];
+                }
             }
             // ---- S <- S Diag(gamma) + V'^T Kr
-            if (tid == 0) bulk_wait_read();  // the S0 tile is free for the next chunk once every thread is past NB_3
+            if (tid == 0) bulk_wait_read();  // the S0 and R/V' tiles are free for the next chunk past NB_3
             nb_sync(NB_3);
             tc_fence_after();
             if (*sStop) break;
@@ -1743,6 +1802,19 @@ static bool encode_token_map(CUtensorMap* tm, const void* base, int64_t T_total,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A fp32 [T_total, H, 128] tensor stored in boxes of [64 tokens][1 head][32 channels] with the 128-byte swizzle.
+static bool encode_token_rows_f32(CUtensorMap* tm, void* base, int64_t T_total, int H) {
+    auto fn = encoder();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)(T_total > 0 ? T_total : 1)};
+    const cuuint64_t strides[2] = {(cuuint64_t)128 * 4, (cuuint64_t)H * 128 * 4};
+    const cuuint32_t box[3] = {32, 1, 64};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 // Per-chunk states ([slot][head] of 128 x 128 fp32, slots below T_total / 64 + N + 1) as rows of 128 fp32, stored
 // in boxes of [128 rows][32 channels] with the 128-byte swizzle.
 static bool encode_state_rows_map(CUtensorMap* tm, void* base, int N, int64_t T_total, int H) {
@@ -1762,16 +1834,18 @@ static bool encode_state_rows_map(CUtensorMap* tm, void* base, int N, int64_t T_
 cudaError_t launch_bwd_fwd_state_tc(const void* v, const float* init_state, const int32_t* cu_seqlens, int N,
                                     int64_t T_total, int H, const void* blobs, float* S0s, float* R, float* Vp,
                                     unsigned int* err, cudaStream_t stream) {
-    CUtensorMap tm, tm_s0;
+    CUtensorMap tm, tm_s0, tm_r, tm_vp;
     if (!encode_token_map(&tm, v, T_total, H)) return cudaErrorInvalidValue;
     if (!encode_state_rows_map(&tm_s0, S0s, N, T_total, H)) return cudaErrorInvalidValue;
+    if (!encode_token_rows_f32(&tm_r, R, T_total, H) || !encode_token_rows_f32(&tm_vp, Vp, T_total, H))
+        return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(bwd_fwd_state_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kFwdSmem);
     if (e != cudaSuccess) return e;
     const int64_t chains = (int64_t)N * H;
     if (chains == 0) return cudaSuccess;
     bwd_fwd_state_tc_kernel<<<(unsigned)chains, kThreads, kFwdSmem, stream>>>(
-        tm, tm_s0, static_cast<const __nv_bfloat16*>(v), init_state, cu_seqlens, T_total, H, static_cast<const uint8_t*>(blobs),
+        tm, tm_s0, tm_r, tm_vp, static_cast<const __nv_bfloat16*>(v), init_state, cu_seqlens, T_total, H, static_cast<const uint8_t*>(blobs),
         S0s, R, Vp, err);
     return cudaGetLastError();
 }
@@ -1782,13 +1856,15 @@ cudaError_t launch_bwd_state_tc(const void* d_o, const float* d_final, const int
     CUtensorMap tm, tm_dsn;
     if (!encode_token_map(&tm, d_o, T_total, H)) return cudaErrorInvalidValue;
     if (!encode_state_rows_map(&tm_dsn, dS_next, N, T_total, H)) return cudaErrorInvalidValue;
+    CUtensorMap tm_dz;
+    if (!encode_token_rows_f32(&tm_dz, dZ, T_total, H)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(bwd_state_tc_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmem);
     if (e != cudaSuccess) return e;
     const int64_t chains = (int64_t)N * H;
     if (chains == 0) return cudaSuccess;
     bwd_state_tc_kernel<__nv_bfloat16><<<(unsigned)chains, kThreads, kSmem, stream>>>(
-        tm, tm_dsn, static_cast<const __nv_bfloat16*>(d_o), d_final, cu_seqlens, T_total, H, static_cast<const uint8_t*>(blobs),
+        tm, tm_dsn, tm_dz, static_cast<const __nv_bfloat16*>(d_o), d_final, cu_seqlens, T_total, H, static_cast<const uint8_t*>(blobs),
         d_init, dS_next, dZ, err);
     return cudaGetLastError();
 }
