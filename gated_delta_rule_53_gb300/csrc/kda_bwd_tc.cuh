@@ -36,19 +36,15 @@ cudaError_t launch_bwd_state_tc(const void* d_o, const float* d_final, const int
                                 int64_t T_total, int H, const void* blobs, float* d_init, float* dS_next, float* dZ,
                                 unsigned int* err, cudaStream_t stream);
 
-// Per (chunk, head) the products with S0 and dS_next, dA_qk, dA_kk, dv and dbeta's first term, on the
-// tensor cores for bf16 dO; outputs as bwd_chunk_a_kernel.
-cudaError_t launch_bwd_chunk_a_tc(const float* beta, const void* d_o, const int32_t* cu_seqlens, int N, int64_t T_total,
-                                  int H, float scale, const float* S0s, const float* dS_next, const float* R,
-                                  const float* Vp, const float* dZ, float* XQ, float* XK, float* XR, float* dgam,
-                                  float* dAqk, float* dAkk, float* dv, float* dbeta, unsigned int* err,
-                                  cudaStream_t stream);
-
-// Per (chunk, head) the position-pair sums, dq, dk, dg and the two channel halves' parts of dbeta's second
-// term, on the tensor cores for bf16 q, k; outputs as bwd_chunk_b_kernel.
-cudaError_t launch_bwd_chunk_b_tc(const void* q, const void* k, const float* g, const float* beta, const int32_t* cu_seqlens,
-                                  int N, int64_t T_total, int H, const float* XQ, const float* XK, const float* XR,
-                                  const float* dgam, const float* dAqk, const float* dAkk, float* dq, float* dk,
-                                  float* dg, float* dbeta_part, unsigned int* err, cudaStream_t stream);
+// Per (chunk, head), on the tensor cores for bf16 q, k and dO: the products with S0 and dS_next, dA_qk, dA_kk,
+// dv, dgamma and dbeta's first term (outputs as bwd_chunk_a_kernel), then the position-pair sums, dq, dk, dg and
+// the two channel halves' parts of dbeta's second term (as bwd_chunk_b_kernel), one CTA per item: XQ, XK, XR
+// and dA pass through the workspace but are read back by the CTA that wrote them.
+cudaError_t launch_bwd_chunk_ab_tc(const void* q, const void* k, const float* g, const float* beta, const void* d_o,
+                                   const int32_t* cu_seqlens, int N, int64_t T_total, int H, float scale,
+                                   const float* S0s, const float* dS_next, const float* R, const float* Vp,
+                                   const float* dZ, float* XQ, float* XK, float* XR, float* dgam, float* dAqk,
+                                   float* dAkk, float* dv, float* dbeta, float* dq, float* dk, float* dg,
+                                   float* dbeta_part, unsigned int* err, cudaStream_t stream);
 
 }  // namespace kda

@@ -855,9 +855,9 @@ cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const 
     }
     if (e != cudaSuccess) return e;
     if (T_total == 0) return cudaSuccess;
-    if (tc_state) {
-        e = launch_bwd_chunk_a_tc(beta, d_o, cu, N, T_total, H, scale, w.S0, w.dSn, w.R, w.Vp, w.dZ, w.XQ, w.XK, w.XR,
-                                  w.dgam, w.dAqk, w.dAkk, dv, dbeta, err, stream);
+    if (tc_state) {  // both per-chunk steps in one kernel
+        e = launch_bwd_chunk_ab_tc(q, k, g, beta, d_o, cu, N, T_total, H, scale, w.S0, w.dSn, w.R, w.Vp, w.dZ, w.XQ,
+                                   w.XK, w.XR, w.dgam, w.dAqk, w.dAkk, dv, dbeta, dq, dk, dg, w.dbp, err, stream);
     } else {
         bwd_chunk_a_kernel<InT><<<grid, kThreads, smA, stream>>>(beta, ot, cu, N, T_total, H, scale, w.S0, w.dSn,
                                                                  w.R, w.Vp, w.dZ, w.XQ, w.XK, w.XR, w.dgam, w.dAqk,
@@ -865,10 +865,7 @@ cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const 
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
-    if (tc_state) {
-        e = launch_bwd_chunk_b_tc(q, k, g, beta, cu, N, T_total, H, w.XQ, w.XK, w.XR, w.dgam, w.dAqk, w.dAkk, dq, dk, dg,
-                                  w.dbp, err, stream);
-    } else {
+    if (!tc_state) {
         bwd_chunk_b_kernel<InT><<<dim3(grid.x, grid.y, 2), kThreads, smB, stream>>>(
             qt, kt, g, beta, cu, N, T_total, H, w.XQ, w.XK, w.XR, w.dgam, w.dAqk, w.dAkk, dq, dk, dg, w.dbp);
         e = cudaGetLastError();

@@ -839,48 +839,29 @@ __device__ __forceinline__ void put_hi_lo(uint8_t* base, uint32_t at, uint32_t t
     *reinterpret_cast<uint4*>(base + at + tile) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
 }
 
-__global__ void __launch_bounds__(kAThreads, 1)
-bwd_chunk_a_tc_kernel(const float* __restrict__ beta, const __nv_bfloat16* __restrict__ d_o,
-                      const int32_t* __restrict__ cu, int N, int64_t T_total, int H, float scale,
-                      const float* __restrict__ S0s, const float* __restrict__ dS_next, const float* __restrict__ Rb,
-                      const float* __restrict__ Vp, const float* __restrict__ dZ, float* __restrict__ XQ,
-                      float* __restrict__ XK, float* __restrict__ XR, float* __restrict__ dgam,
-                      float* __restrict__ dAqk, float* __restrict__ dAkk, float* __restrict__ dv,
-                      float* __restrict__ dbeta, unsigned int* err) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+// Phase A of the per-chunk work (item (chunk at c0 with L tokens, head h; base = slot * H + h)): the products
+// with S0 and dS_next, dA, dgamma, dv and dbeta's first term; XQ, XK, XR and dA go to global memory for phase B.
+// TMEM columns 0-255 of the caller's allocation; ends with every thread past a barrier.
+__device__ __forceinline__ void chunk_a_phase(const float* __restrict__ beta, const __nv_bfloat16* __restrict__ d_o,
+                                              int64_t T_total, int H, float scale, const float* __restrict__ S0s,
+                                              const float* __restrict__ dS_next, const float* __restrict__ Rb,
+                                              const float* __restrict__ Vp, const float* __restrict__ dZ,
+                                              float* __restrict__ XQ, float* __restrict__ XK, float* __restrict__ XR,
+                                              float* __restrict__ dgam, float* __restrict__ dAqk,
+                                              float* __restrict__ dAkk, float* __restrict__ dv,
+                                              float* __restrict__ dbeta, unsigned int* err, uint8_t* sm, uint32_t tbase,
+                                              int64_t c0, int L, int64_t base, int h) {
     const uint32_t sbase = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t slot = blockIdx.x;
-    const int h = blockIdx.y;
-    // the chunk of this slot (as bwd_prep_kernel): sequence n with bos_n / 64 + n <= slot
-    int n = 0;
-    {
-        int lo = 0, hi = N;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            const int64_t b = cu ? (int64_t)cu[mid] : 0;
-            if (b / kC + mid <= slot) lo = mid; else hi = mid;
-        }
-        n = lo;
-    }
-    int64_t bos, eos;
-    seq_bounds(cu, n, T_total, bos, eos);
-    const int64_t c0 = bos + (slot - (bos / kC + n)) * kC;
-    if (slot < bos / kC + n || c0 >= eos) return;
-    const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
-    const int64_t base = slot * H + h;
     float* sRed = reinterpret_cast<float*>(sm + A_RED);
     float* sBeta = reinterpret_cast<float*>(sm + A_BETA);
     uint64_t* bX = reinterpret_cast<uint64_t*>(sm + A_BAR);
     uint64_t* bR = bX + 1;
-    uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + A_MISC);
     if (tid == 0) {
         mbar_init(bX, 1);
         mbar_init(bR, 1);
         fence_mbar_init();
     }
-    if (warp == 0) tmem_alloc(sTmem, 256);
     if (tid < kC) sBeta[tid] = tid < L ? beta[(c0 + tid) * H + h] : 0.f;
     const float* S0 = S0s + base * kD * kD;
     const float* dSn = dS_next + base * kD * kD;
@@ -968,7 +949,6 @@ bwd_chunk_a_tc_kernel(const float* __restrict__ beta, const __nv_bfloat16* __res
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tbase = *sTmem;
     const uint32_t id_x = idesc_bf16_f32(128, 128, true, false);   // A = S0^T (MN-major), B = [dO ; dZ] (K-major)
     const uint32_t id_r = idesc_bf16_f32(128, 64, true, false);    // A = dS_next^T (MN-major), B = V' (K-major)
     const uint32_t id_a = idesc_bf16_f32(128, 64, false, false);   // A = [dO ; dZ], B = V' (K-major)
@@ -1102,9 +1082,12 @@ bwd_chunk_a_tc_kernel(const float* __restrict__ beta, const __nv_bfloat16* __res
             if (t < L) XR[((c0 + t) * H + h) * kD + c] = __uint_as_float(x[e]);
         }
     }
+    if (tid == 0) {  // phase B reuses this shared memory
+        mbar_inval(bX);
+        mbar_inval(bR);
+    }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tbase, 256);
 }
 
 // 2^x by the hardware approximation (results below 2^-126 flush to 0)
@@ -1486,35 +1469,20 @@ __device__ __forceinline__ float warp_sum4(const float (&v)[4], int lane) {
     return w;
 }
 
-__global__ void __launch_bounds__(kBThreads, 1)
-bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                      const float* __restrict__ g, const float* __restrict__ beta, const int32_t* __restrict__ cu, int N,
-                      int64_t T_total, int H, const float* __restrict__ XQ, const float* __restrict__ XK,
-                      const float* __restrict__ XR, const float* __restrict__ dgam, const float* __restrict__ dAqk,
-                      const float* __restrict__ dAkk, float* __restrict__ dq, float* __restrict__ dk,
-                      float* __restrict__ dg, float* __restrict__ dbeta_part, unsigned int* err) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+// Phase B of the per-chunk work: the position-pair sums, dq, dk, dg and dbeta's second term, reading phase A's
+// XQ, XK, XR and dA back (from L2: this CTA has just written them) and then dropping their L2 lines, which
+// nothing reads again, instead of writing them back.  TMEM columns 0-479 of the caller's allocation.
+__device__ __forceinline__ void chunk_b_phase(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                                              const float* __restrict__ g, const float* __restrict__ beta,
+                                              int64_t T_total, int H, const float* __restrict__ XQ,
+                                              const float* __restrict__ XK, const float* __restrict__ XR,
+                                              const float* __restrict__ dgam, const float* __restrict__ dAqk,
+                                              const float* __restrict__ dAkk, float* __restrict__ dq,
+                                              float* __restrict__ dk, float* __restrict__ dg,
+                                              float* __restrict__ dbeta_part, unsigned int* err, uint8_t* sm,
+                                              uint32_t tbase, int64_t c0, int L, int64_t base, int h) {
     const uint32_t sbase = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t slot = blockIdx.x;
-    const int h = blockIdx.y;
-    int n = 0;
-    {
-        int lo = 0, hi = N;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            const int64_t b = cu ? (int64_t)cu[mid] : 0;
-            if (b / kC + mid <= slot) lo = mid; else hi = mid;
-        }
-        n = lo;
-    }
-    int64_t bos, eos;
-    seq_bounds(cu, n, T_total, bos, eos);
-    const int64_t c0 = bos + (slot - (bos / kC + n)) * kC;
-    if (slot < bos / kC + n || c0 >= eos) return;
-    const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
-    const int64_t base = slot * H + h;
     const int64_t rs = (int64_t)H * kD;  // row stride of q, k, g and the per-channel tensors
     const int64_t hoff = (int64_t)h * kD;
     constexpr float kLog2e = 1.4426950408889634f;
@@ -1524,17 +1492,10 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     float* sLast = reinterpret_cast<float*>(sm + B_LAST);
     float* sDBP = reinterpret_cast<float*>(sm + B_DBP);
     uint64_t* bM = reinterpret_cast<uint64_t*>(sm + B_BAR);  // [0] the K operand's products, [1] every product
-    uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + B_MISC);
     if (tid == 0) {
         mbar_init(bM, 1);
         mbar_init(bM + 1, 1);
         fence_mbar_init();
-    }
-    if (warp == 0) tmem_alloc(sTmem, 512);
-    // the epilogue's per-token inputs on their way to L2 (768 128-byte lines)
-    for (int idx = tid; idx < 3 * kC * 4; idx += kBThreads) {
-        const int which = idx >> 8, r = (idx >> 2) & 63, part = idx & 3;
-        if (r < L) prefetch_l2((which == 0 ? XQ : which == 1 ? XK : XR) + (c0 + r) * rs + hoff + 32 * part);
     }
     if (tid < kC) sBeta[tid] = tid < L ? beta[(c0 + tid) * H + h] : 0.f;
     // k and q of the operand builder's two (row, 8 channels) items, held for the three builds
@@ -1589,7 +1550,6 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
         for (int r = 32; r < 64; ++r) sG[r * kD + c] += t0;
     }
     __syncthreads();
-    const uint32_t tbase = *sTmem;
     // pieces (of the operand, of dA) of the six products p: nibble p of kPa, kPb
     // (11, 12, 21, 13, 31, 22 in one-based pieces)
     constexpr uint32_t kPa = 0x120100u, kPb = 0x102010u;
@@ -1771,6 +1731,64 @@ bwd_chunk_b_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* 
     }
     tc_fence_before();
     __syncthreads();
+    // XQ, XK, XR (the item's rows of its head) and dA: every read is done
+    for (int idx = tid; idx < 3 * kC * 4 + 256; idx += kBThreads) {
+        if (idx < 3 * kC * 4) {
+            const int which = idx >> 8, r = (idx >> 2) & 63, part = idx & 3;
+            if (r < L) discard_l2((which == 0 ? XQ : which == 1 ? XK : XR) + (c0 + r) * rs + hoff + 32 * part);
+        } else {
+            const int l = idx - 3 * kC * 4;
+            discard_l2((l < 128 ? dAqk : dAkk) + base * kC * kC + 32 * (l & 127));
+        }
+    }
+}
+
+// The per-chunk work of one item, phase A then phase B on one CTA (512 threads; shared memory and TMEM
+// reused from one phase to the next).
+__global__ void __launch_bounds__(kBThreads, 1)
+bwd_chunk_ab_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                       const float* __restrict__ g, const float* __restrict__ beta,
+                       const __nv_bfloat16* __restrict__ d_o, const int32_t* __restrict__ cu, int N, int64_t T_total,
+                       int H, float scale, const float* __restrict__ S0s, const float* __restrict__ dS_next,
+                       const float* __restrict__ Rb, const float* __restrict__ Vp, const float* __restrict__ dZ,
+                       float* __restrict__ XQ, float* __restrict__ XK, float* __restrict__ XR, float* __restrict__ dgam,
+                       float* __restrict__ dAqk, float* __restrict__ dAkk, float* __restrict__ dv,
+                       float* __restrict__ dbeta, float* __restrict__ dq, float* __restrict__ dk,
+                       float* __restrict__ dg, float* __restrict__ dbeta_part, unsigned int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5;
+    const int64_t slot = blockIdx.x;
+    const int h = blockIdx.y;
+    int n = 0;
+    {
+        int lo = 0, hi = N;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            const int64_t b = cu ? (int64_t)cu[mid] : 0;
+            if (b / kC + mid <= slot) lo = mid; else hi = mid;
+        }
+        n = lo;
+    }
+    int64_t bos, eos;
+    seq_bounds(cu, n, T_total, bos, eos);
+    const int64_t c0 = bos + (slot - (bos / kC + n)) * kC;
+    if (slot < bos / kC + n || c0 >= eos) return;
+    const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
+    const int64_t base = slot * H + h;
+    uint32_t* sTmem = reinterpret_cast<uint32_t*>(sm + B_MISC);  // outside phase A's shared memory
+    if (warp == 0) tmem_alloc(sTmem, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *sTmem;
+    chunk_a_phase(beta, d_o, T_total, H, scale, S0s, dS_next, Rb, Vp, dZ, XQ, XK, XR, dgam, dAqk, dAkk, dv, dbeta, err,
+                  sm, tbase, c0, L, base, h);
+    tc_fence_after();
+    chunk_b_phase(q, k, g, beta, T_total, H, XQ, XK, XR, dgam, dAqk, dAkk, dq, dk, dg, dbeta_part, err, sm, tbase, c0,
+                  L, base, h);
+    tc_fence_before();
+    __syncthreads();
     if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
@@ -1873,34 +1891,22 @@ cudaError_t launch_bwd_state_tc(const void* d_o, const float* d_final, const int
 
 namespace kda {
 
-cudaError_t launch_bwd_chunk_a_tc(const float* beta, const void* d_o, const int32_t* cu_seqlens, int N, int64_t T_total,
-                                  int H, float scale, const float* S0s, const float* dS_next, const float* R,
-                                  const float* Vp, const float* dZ, float* XQ, float* XK, float* XR, float* dgam,
-                                  float* dAqk, float* dAkk, float* dv, float* dbeta, unsigned int* err,
-                                  cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_chunk_a_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kASmem);
+cudaError_t launch_bwd_chunk_ab_tc(const void* q, const void* k, const float* g, const float* beta, const void* d_o,
+                                   const int32_t* cu_seqlens, int N, int64_t T_total, int H, float scale,
+                                   const float* S0s, const float* dS_next, const float* R, const float* Vp,
+                                   const float* dZ, float* XQ, float* XK, float* XR, float* dgam, float* dAqk,
+                                   float* dAkk, float* dv, float* dbeta, float* dq, float* dk, float* dg,
+                                   float* dbeta_part, unsigned int* err, cudaStream_t stream) {
+    static_assert(kAThreads == kBThreads && kASmem <= kBSmem && A_MISC + 16 <= B_MISC,
+                  "phase A fits the fused kernel's block and shared memory below its TMEM address slot");
+    cudaError_t e =
+        cudaFuncSetAttribute(bwd_chunk_ab_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBSmem);
     if (e != cudaSuccess) return e;
     const int64_t slots = T_total / kC + N + 1;
-    bwd_chunk_a_tc_kernel<<<dim3((unsigned)slots, (unsigned)H), kAThreads, kASmem, stream>>>(
-        beta, static_cast<const __nv_bfloat16*>(d_o), cu_seqlens, N, T_total, H, scale, S0s, dS_next, R, Vp, dZ, XQ, XK,
-        XR, dgam, dAqk, dAkk, dv, dbeta, err);
-    return cudaGetLastError();
-}
-
-}  // namespace kda
-
-namespace kda {
-
-cudaError_t launch_bwd_chunk_b_tc(const void* q, const void* k, const float* g, const float* beta, const int32_t* cu_seqlens,
-                                  int N, int64_t T_total, int H, const float* XQ, const float* XK, const float* XR,
-                                  const float* dgam, const float* dAqk, const float* dAkk, float* dq, float* dk,
-                                  float* dg, float* dbeta_part, unsigned int* err, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_chunk_b_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBSmem);
-    if (e != cudaSuccess) return e;
-    const int64_t slots = T_total / kC + N + 1;
-    bwd_chunk_b_tc_kernel<<<dim3((unsigned)slots, (unsigned)H), kBThreads, kBSmem, stream>>>(
-        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), g, beta, cu_seqlens, N, T_total, H,
-        XQ, XK, XR, dgam, dAqk, dAkk, dq, dk, dg, dbeta_part, err);
+    bwd_chunk_ab_tc_kernel<<<dim3((unsigned)slots, (unsigned)H), kBThreads, kBSmem, stream>>>(
+        static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), g, beta,
+        static_cast<const __nv_bfloat16*>(d_o), cu_seqlens, N, T_total, H, scale, S0s, dS_next, R, Vp, dZ, XQ, XK, XR,
+        dgam, dAqk, dAkk, dv, dbeta, dq, dk, dg, dbeta_part, err);
     return cudaGetLastError();
 }
 
