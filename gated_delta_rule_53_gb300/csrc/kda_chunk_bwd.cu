@@ -26,8 +26,8 @@
 //   3. bwd_state_kernel: per (sequence, head, 32 value rows) the chunks in reverse, dS in shared
 //      memory (the state's rows are independent), keeping dS_next of every chunk and dZ = T^T dV';
 //      with bf16 inputs bwd_fwd_state_tc_kernel and bwd_state_tc_kernel (kda_chunk_bwd_tc.cu) do passes 2
-//      and 3 on the tensor cores instead, one CTA per chain, from bf16 hi/lo tiles that bwd_prep_kernel
-//      writes for them, and bwd_chunk_a_tc_kernel and bwd_chunk_b_tc_kernel do steps 4 and 5;
+//      and 3 on the tensor cores instead, one CTA per chain, from bf16 hi/lo tiles that bwd_prep_tc_kernel
+//      writes for them, and bwd_chunk_ab_tc_kernel does steps 4 and 5 on one CTA per (chunk, head);
 //   4. bwd_chunk_a_kernel: per (chunk, head) the products with S0 and dS_next, dA_qk, dA_kk, dv and
 //      the first term of dbeta;
 //   5. bwd_chunk_b_kernel: per (chunk, head, half of the key channels) the position-pair products, dq,
