@@ -1,9 +1,11 @@
 """GPU parity of kda_chunk_bwd (through its C ABI) against the oracle's reverse mode through the
 token loop, on the same seeded inputs.
 
-The backward computes in fp32 on the CUDA cores from the same input bits as the oracle (bf16 or
-fp32 storage), so every gradient is held to rel-L2 <= 1e-4 over the whole tensor, the bound of the
-fp32 forward; an fp32 emulation of the same chunked algorithm gives 1e-7 .. 3e-6.
+The backward computes from the same input bits as the oracle (bf16 or fp32 storage) with fp32-level
+accuracy: fp32 on the CUDA cores for fp32 inputs; for bf16 inputs on the tensor cores with every fp32
+operand split into bf16 pieces (hi + lo, three pieces in the position-pair sums).  Every gradient is held
+to rel-L2 <= 1e-4 over the whole tensor, the bound of the fp32 forward; an fp32 emulation of the chunked
+algorithm gives 1e-7 .. 3e-6.
 """
 import math
 
@@ -81,6 +83,15 @@ def test_bwd_ragged_varlen_with_state_and_scale(kda, orc, dtype):
     got = run_and_check(kda, orc, w, arrays, scale=1.0 / math.sqrt(128))
     # the empty sequence passes dL/dS_final straight to dL/dS0
     assert torch.equal(got[5][5], dev(arrays[7])[5])
+
+
+def test_bwd_packed_sequences_many_chunks(kda, orc):
+    """Five packed sequences of 1 to 2,000 tokens with initial states and dL/dS_final (bf16): the chain
+    passes store whole chunks by TMA and each sequence's partial last chunk row by row, the reverse pass
+    prefetches two chunks ahead through sequences of up to 32 chunks, and the per-chunk kernel runs chunks
+    at every position of a sequence."""
+    w, arrays = case(5307, [700, 1, 1300, 64, 2000], 4, "bf16")
+    run_and_check(kda, orc, w, arrays, scale=1.0 / math.sqrt(128))
 
 
 def test_bwd_single_sequence_without_state(kda, orc):
