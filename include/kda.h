@@ -145,6 +145,12 @@ KDA_API kda_status kda_shortconv_l2norm(const void* xq, const void* xk, const vo
  * on one device are serialised through them even when the callers use independent streams.
  * Otherwise every range runs on `stream`, one after the other.
  *
+ * Device resets: the library carries its own (statically linked) CUDA runtime, whose loaded kernels and
+ * device variables belong to the device context of the process's first call, and it keeps the
+ * addresses of its device error word and static scratch and its two streams per device.  None of
+ * that survives a reset of the device (cudaDeviceReset by the caller's runtime destroys the context):
+ * do not call the library in a process after resetting a device it has been used on.
+ *
  * The bf16 path runs two kernels per range of chunks: the first computes, for every
  * (chunk, head) at once, everything that does not depend on the carried state (the
  * in-chunk decays, the A_kk / A_qk blocks, T = (I + A_kk)^-1, W = T diag(beta) K e^G and
