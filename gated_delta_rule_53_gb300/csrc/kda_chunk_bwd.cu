@@ -74,25 +74,12 @@ __device__ bool slot_chunk(const int32_t* cu, int N, int64_t T_total, int64_t sl
 // ============================ per chunk: what does not depend on the state ============================
 constexpr size_t kPrepFloats = 3 * kC * kD + kC * kC + kC + kD;
 
-// x = hi + lo as two bf16 tiles `tile` bytes apart; 8 values into the 16-byte chunk at `at`
-__device__ __forceinline__ void store_hi_lo(uint8_t* dst, uint32_t at, uint32_t tile, const float (&x)[8]) {
-    uint32_t hi[4], lo[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        hi[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
-        lo[j] = pack_bf16x2(x[2 * j] - bf16_lo(hi[j]), x[2 * j + 1] - bf16_hi(hi[j]));
-    }
-    *reinterpret_cast<uint4*>(dst + at) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    *reinterpret_cast<uint4*>(dst + at + tile) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-}
-
-// bb (may be null): the tensor-core reverse pass's tiles of this chunk (kda_bwd_tc.cuh)
 template <typename InT>
 __global__ void __launch_bounds__(kThreads, 2)
 bwd_prep_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const float* __restrict__ g,
                 const float* __restrict__ beta, const int32_t* __restrict__ cu, int N, int64_t T_total, int H,
-                float scale, float* __restrict__ gQg, float* __restrict__ gKg, float* __restrict__ gKr,
-                float* __restrict__ gAqk, float* __restrict__ gT, float* __restrict__ gGam, uint8_t* __restrict__ bb) {
+                float* __restrict__ gQg, float* __restrict__ gKg, float* __restrict__ gKr, float* __restrict__ gAqk,
+                float* __restrict__ gT, float* __restrict__ gGam) {
     extern __shared__ float smem[];
     float* sQ = smem;             // [C][D] q
     float* sK = sQ + kC * kD;     // [C][D] k
@@ -146,49 +133,14 @@ bwd_prep_kernel(const InT* __restrict__ q, const InT* __restrict__ k, const floa
 #pragma unroll
         for (int i = 0; i < kC; ++i) gT[base * kC * kC + i * kC + j] = x[i];
     }
-    if (!bb) {  // Qg, Kg, Kr in fp32 for the CUDA-core passes along the chains (the tensor-core ones read bb)
-        for (int idx = tid; idx < kC * kD; idx += kThreads) {
-            const int c = idx % kD;
-            const float G = sG[idx], kk = sK[idx];
-            const float gam = expf(G);
-            gQg[base * kC * kD + idx] = sQ[idx] * gam;
-            gKg[base * kC * kD + idx] = kk * gam;
-            gKr[base * kC * kD + idx] = kk * expf(sGl[c] - G);
-        }
-    }
-    if (bb) {  // the same values as bf16 hi + lo tiles, in the layouts the tensor-core reverse pass reads
-        __syncthreads();  // this CTA's global writes of A_qk and T are visible to all of it
-        uint8_t* blob = bb + base * (int64_t)kBwdBlobBytes;
-        for (int idx = tid; idx < kC * kD / 8; idx += kThreads) {  // row i, channels 8 c8 .. 8 c8 + 7
-            const int i = idx >> 4, c8 = idx & 15;
-            float kr[8], qg[8], kg[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int c = 8 * c8 + e;
-                const float G = sG[i * kD + c], kk = sK[i * kD + c];
-                const float gam = expf(G);
-                qg[e] = scale * (sQ[i * kD + c] * gam);
-                kg[e] = kk * gam;
-                kr[e] = kk * expf(sGl[c] - G);
-            }
-            const uint32_t at = (uint32_t)(c8 >> 3) * 8192u + tc::sw128((uint32_t)i, (uint32_t)(c8 & 7));
-            store_hi_lo(blob + kBB_KR, at, 16384, kr);
-            store_hi_lo(blob + kBB_QG, at, 16384, qg);
-            store_hi_lo(blob + kBB_KG, at, 16384, kg);
-        }
-        for (int idx = tid; idx < kC * kC / 8; idx += kThreads) {  // row s, columns 8 t8 .. 8 t8 + 7
-            const int s8 = idx >> 3, t8 = idx & 7;
-            const float* aq = gAqk + base * kC * kC + s8 * kC + 8 * t8;
-            const float* tt = gT + base * kC * kC + s8 * kC + 8 * t8;
-            float a[8], t[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) { a[e] = scale * aq[e]; t[e] = tt[e]; }
-            const uint32_t at = tc::sw128((uint32_t)s8, (uint32_t)t8);
-            store_hi_lo(blob + kBB_AQ, at, 8192, a);
-            store_hi_lo(blob + kBB_TT, at, 8192, t);
-        }
-        if (tid < kD) reinterpret_cast<float*>(blob + kBB_GAM)[tid] = expf(sGl[tid]);
-        if (tid < kC) reinterpret_cast<float*>(blob + kBB_BETA)[tid] = sB[tid];
+    // Qg, Kg, Kr in fp32 for the passes along the chains
+    for (int idx = tid; idx < kC * kD; idx += kThreads) {
+        const int c = idx % kD;
+        const float G = sG[idx], kk = sK[idx];
+        const float gam = expf(G);
+        gQg[base * kC * kD + idx] = sQ[idx] * gam;
+        gKg[base * kC * kD + idx] = kk * gam;
+        gKr[base * kC * kD + idx] = kk * expf(sGl[c] - G);
     }
 }
 
@@ -832,8 +784,8 @@ cudaError_t launch_bwd_typed(const void* q, const void* k, const void* v, const 
         if (tc_state) {
             e = launch_bwd_prep_tc(q, k, g, beta, cu, N, T_total, H, scale, w.tc, err, stream);
         } else {
-            bwd_prep_kernel<InT><<<grid, kThreads, smP, stream>>>(qt, kt, g, beta, cu, N, T_total, H, scale, w.Qg,
-                                                                  w.Kg, w.Kr, w.Aqk, w.T, w.gam, nullptr);
+            bwd_prep_kernel<InT><<<grid, kThreads, smP, stream>>>(qt, kt, g, beta, cu, N, T_total, H, w.Qg, w.Kg,
+                                                                  w.Kr, w.Aqk, w.T, w.gam);
             e = cudaGetLastError();
         }
         if (e != cudaSuccess) return e;
