@@ -127,7 +127,8 @@ bwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_do, const __grid_cons
                     const uint8_t* __restrict__ blobs, float* __restrict__ d_init, float* __restrict__ dS_next,
                     float* __restrict__ dZ_out, unsigned int* err) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned by pointer arithmetic on the shared array (accesses through `sm` stay shared ones)
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int chain = blockIdx.x, n = chain / H, h = chain % H;
@@ -494,7 +495,8 @@ bwd_fwd_state_tc_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_c
                         const uint8_t* __restrict__ blobs, float* __restrict__ S0s, float* __restrict__ Rb,
                         float* __restrict__ Vp, unsigned int* err) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned by pointer arithmetic on the shared array (accesses through `sm` stay shared ones)
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int chain = blockIdx.x, n = chain / H, h = chain % H;
@@ -1146,7 +1148,8 @@ bwd_prep_tc_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __r
                    const float* __restrict__ g, const float* __restrict__ beta, const int32_t* __restrict__ cu, int N,
                    int64_t T_total, int H, float scale, uint8_t* __restrict__ blobs, unsigned int* err) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned by pointer arithmetic on the shared array (accesses through `sm` stay shared ones)
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t slot = blockIdx.x;

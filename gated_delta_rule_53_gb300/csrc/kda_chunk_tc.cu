@@ -250,7 +250,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                   int N, int64_t T_total, int H, int m0, int n_items, uint8_t* __restrict__ blobs,
                   FrontendArgs fe, unsigned int* err) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned by pointer arithmetic on the shared array, so that accesses through `sm` stay shared
+    // ones (an integer round trip of the address would leave them generic)
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int offN = off[N];

@@ -33,18 +33,19 @@ __device__ __forceinline__ void t_diag_blocks(const float* A, float* T, int warp
 }
 
 // One 16 x 16 fp32 block product for 32 threads; thread t owns rows 2 (t / 4) and 2 (t / 4) + 1, columns
-// 4 (t % 4) .. +3:   out = sign * ((A0 + w1 A1) B + A3 B3), the A1 and A3 B3 terms optional.  One routine
-// with run-time operands serves every block of the solve (one copy of the code).
+// 4 (t % 4) .. +3:   out = sign * ((A0 + w1 A1) B + A3 B3), the A1 and A3 B3 terms optional.  Inlined into
+// every call site, where its operands are known shared-memory addresses (shared loads, not generic ones)
+// whenever the caller's pointers keep the shared address space.
 struct BlkJob {
     const float* a0; const float* a1; const float* b; const float* a3; const float* b3;
     float* out;
     int lda0, lda1, ldb, lda3, ldb3, ldo;
     float w1, sign;
 };
-__device__ __noinline__ void blk_job(BlkJob j, int t) {
+__device__ __forceinline__ void blk_job(BlkJob j, int t) {
     const int r0 = 2 * (t >> 2), c = 4 * (t & 3);
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll 1
+#pragma unroll
     for (int pass = 0; pass < 2; ++pass) {
         const float* a = pass ? j.a3 : j.a0;
         if (!a) break;
