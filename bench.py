@@ -94,6 +94,8 @@ def bwd_bytes_per_token_head(d: int = 128) -> int:
     return 4 * d * 2 + d * 4 + 4 + 4 * d * 4 + 4
 
 
+# The files each entry point's kernels are compiled from (a measured traffic figure stands only while they are unchanged).
+FWD_SOURCES = "kda_chunk_tc.cu+kda_tsolve.cuh+kda_frontend.cuh"
 BWD_SOURCES = "kda_chunk_bwd.cu+kda_chunk_bwd_tc.cu+kda_bwd_tc.cuh+kda_tsolve.cuh"
 
 
@@ -146,20 +148,72 @@ def smi_index(local_rank: int) -> str:
     return str(local_rank)
 
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (SM clock, its maximum, clock event reasons, power), so that the
+    clocks can be sampled every few milliseconds; None where the library or a call is unavailable."""
+
+    # clock event reason bits of nvml.h
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
+
+    def __init__(self, gpu_id: str):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        if gpu_id.startswith("GPU-") or gpu_id.startswith("MIG-"):
+            rc = self.lib.nvmlDeviceGetHandleByUUID(gpu_id.encode(), ctypes.byref(self.dev))
+        else:
+            rc = self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(int(gpu_id)), ctypes.byref(self.dev))
+        if rc != 0:
+            self.lib.nvmlShutdown()
+            raise RuntimeError("no NVML handle for GPU " + gpu_id)
+        reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = reasons or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sample(self):
+        ct, u, ull = self.ct, self.ct.c_uint(), self.ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.dev, 1, ct.byref(u)) != 0:  # NVML_CLOCK_SM
+            return None
+        sm = float(u.value)
+        smax = float(u.value) if self.lib.nvmlDeviceGetMaxClockInfo(self.dev, 1, ct.byref(u)) == 0 else sm
+        bits = ull.value if self.reasons_fn(self.dev, ct.byref(ull)) == 0 else 0
+        return sm, smax, [name for bit, name in self.REASONS.items() if bits & bit]
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 50 ms during the timed region."""
+    """SM clocks and clock event reasons sampled during the timed region: every 10 ms through NVML's read-only
+    queries, or (without NVML) every 50 ms by ``nvidia-smi``, which has to be running before the region starts."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, period_s: float = 0.01):
         self.gpu_index = gpu_index
+        self.period_s = period_s
         self.proc = None
+        self.nvml = None
         self.lines = []
+        self.samples = []
         self.thread = None
+        self.running = False
+        self.first = threading.Event()
 
     def start(self):
+        try:
+            self.nvml = _Nvml(str(self.gpu_index))
+        except Exception:
+            self.nvml = None
+        if self.nvml is not None:
+            self.running = True
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                                           "-lms", "50", "-i", str(self.gpu_index)], stdout=subprocess.PIPE,
@@ -169,12 +223,26 @@ class ClockSampler:
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+        self.first.wait(timeout=5.0)  # nvidia-smi starts in a fraction of a second: begin the region after it
+
+    def _poll(self):
+        while self.running:
+            s = self.nvml.sample()
+            if s is not None:
+                self.samples.append(s)
+            time.sleep(self.period_s)
 
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
+            self.first.set()
 
     def stop(self):
+        if self.nvml is not None:
+            self.running = False
+            self.thread.join(timeout=2)
+            self.nvml.close()
+            return self.summarise(self.samples, "nvml")
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -184,22 +252,30 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm, smax, reasons = [], [], set()
+        return self.summarise(self.parse_smi(self.lines), "nvidia-smi")
+
+    @staticmethod
+    def parse_smi(lines):
+        """(sm MHz, max sm MHz, [active reasons]) of each nvidia-smi csv line of FIELDS."""
+        out = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                sm, smax = float(parts[1]), float(parts[2])
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+            out.append((sm, smax, [n for n, val in zip(names, parts[5:9]) if val.lower().startswith("active")]))
+        return out
+
+    @staticmethod
+    def summarise(samples, source):
+        sm = [s[0] for s in samples]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(s[1] for s in samples) if samples else None,
+                "reasons": sorted({r for s in samples for r in s[2]}), "samples": len(sm), "source": source}
 
 
 # ------------------------------------------------------------------------------------------------
@@ -616,7 +692,7 @@ def run_ours(args):
         "gpu_launches": args.steps * launches_per_call,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved_gbs / hbm_peak,
-                     "traffic": measured_traffic("kda_chunk_fwd", "kda_chunk_tc.cu", w.name),
+                     "traffic": measured_traffic("kda_chunk_fwd", FWD_SOURCES, w.name),
                      "peak_source": peak_src,
                      "kernel": "kda_chunk_fwd (bf16): chunk_offsets_kernel + chunk_prep_kernel + chunk_state_kernel "
                                "per range of chunk rows, timed as one call", "algorithmic_bytes_per_launch": pbytes,
@@ -638,7 +714,7 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": fe_bytes,
                      "roofline": {"bound": "hbm", "achieved": fe_gbs, "peak": hbm_peak, "unit": "GB/s",
                                   "frac": fe_gbs / hbm_peak,
-                                  "traffic": measured_traffic("shortconv_kernel", "kda_frontend.cu", wf.name),
+                                  "traffic": measured_traffic("shortconv_kernel", "kda_frontend.cu+kda_frontend.cuh", wf.name),
                                   "peak_source": peak_src}},
     }
     if seg is not None:
@@ -664,7 +740,7 @@ def run_ours(args):
                      "traffic_GB_s": (bwd_traffic / (ms_bwd_launch * 1e-3) / 1e9) if bwd_traffic else None,
                      "peak_source": peak_src,
                      "kernel": "bwd_prep_tc_kernel + bwd_fwd_state_tc_kernel + bwd_state_tc_kernel + "
-                               "bwd_chunk_a_tc_kernel + bwd_chunk_b_tc_kernel + bwd_dbeta_kernel, timed as one call"}}
+                               "bwd_chunk_ab_tc_kernel + bwd_dbeta_kernel, timed as one call"}}
     line["fused_prefill"] = {
         "workload": "frontend_32k raw q, k, v bf16 [32768, 12288] + g = max(-5, -softplus(z)), beta -> "
                     "ShortConv(4)+SiLU+L2norm -> chunk_kda (the long workload's path at 32K tokens)",
@@ -681,7 +757,7 @@ def run_ours(args):
         "value": Tv * world / (ms_var * 1e-3), "unit": "tokens/s", "ms_per_step": ms_var, "steps": vsteps,
         "algorithmic_bytes_per_launch": var_bytes,
         "roofline": {"bound": "hbm", "achieved": var_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": var_gbs / hbm_peak,
-                     "traffic": measured_traffic("kda_chunk_fwd", "kda_chunk_tc.cu", "varlen_32"),
+                     "traffic": measured_traffic("kda_chunk_fwd", FWD_SOURCES, "varlen_32"),
                      "peak_source": peak_src}}
     line["long_256k"] = {
         "workload": f"long_256k: T={Tl}, raw q,k,v bf16 [{Tl}, {Cl}] -> ShortConv(4)+SiLU+L2norm -> chunk_kda with "
@@ -691,7 +767,7 @@ def run_ours(args):
         "two_pass_value": Tl * world / (ms_long2 * 1e-3), "two_pass_ms_per_step": ms_long2,
         "roofline": {"bound": "hbm", "achieved": long_gbs, "peak": hbm_peak, "unit": "GB/s",
                      "frac": long_gbs / hbm_peak,
-                     "traffic": measured_traffic("kda_chunk_fwd_frontend", "kda_chunk_tc.cu", "long_256k"),
+                     "traffic": measured_traffic("kda_chunk_fwd_frontend", FWD_SOURCES, "long_256k"),
                      "peak_source": peak_src}}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)

@@ -101,3 +101,57 @@ def test_source_hash_of_several_files():
     joined = b"".join(open(os.path.join(csrc, n), "rb").read() for n in names)
     assert bench.kernel_source_hash(bench.BWD_SOURCES) == hashlib.sha256(joined).hexdigest()[:16]
     assert bench.kernel_source_hash(names[0]) == hashlib.sha256(open(os.path.join(csrc, names[0]), "rb").read()).hexdigest()[:16]
+
+
+def test_clock_sampler_parses_and_summarises():
+    sys.path.insert(0, ROOT)
+    import bench
+    lines = ["0, 2070, 2070, 900.1, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+             "0, 1980, 2070, 1380.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+             "0, 2070, 2070, 1390.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+             "garbage", "0, [N/A], 2070, 0, 0, Not Active, Not Active, Not Active, Not Active"]
+    got = bench.ClockSampler.summarise(bench.ClockSampler.parse_smi(lines), "nvidia-smi")
+    assert got == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3,
+                   "source": "nvidia-smi"}
+    assert bench.ClockSampler.summarise([], "nvml")["sm_mhz"] is None
+
+
+def test_clock_sampler_polls_nvml_and_falls_back(monkeypatch):
+    """The NVML path samples on its own thread until stopped; without NVML and nvidia-smi the line
+    says the clocks are unavailable instead of failing."""
+    sys.path.insert(0, ROOT)
+    import time
+
+    import bench
+
+    class FakeNvml:
+        closed = False
+
+        def __init__(self, gpu_id):
+            assert gpu_id == "3"
+
+        def sample(self):
+            return (1965.0, 2070.0, ["sw_power_cap"])
+
+        def close(self):
+            FakeNvml.closed = True
+
+    monkeypatch.setattr(bench, "_Nvml", FakeNvml)
+    cs = bench.ClockSampler("3", period_s=0.001)
+    cs.start()
+    time.sleep(0.05)
+    got = cs.stop()
+    assert got["source"] == "nvml" and got["samples"] >= 2 and got["sm_mhz"] == 1965.0
+    assert got["reasons"] == ["sw_power_cap"] and FakeNvml.closed
+
+    def no_nvml(gpu_id):
+        raise OSError("no libnvidia-ml")
+
+    def no_smi(*a, **k):
+        raise FileNotFoundError("nvidia-smi")
+
+    monkeypatch.setattr(bench, "_Nvml", no_nvml)
+    monkeypatch.setattr(bench.subprocess, "Popen", no_smi)
+    cs = bench.ClockSampler("0")
+    cs.start()
+    assert cs.stop()["sm_mhz"] is None
