@@ -317,16 +317,19 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // takes tokens 8w .. 8w+7, lane the 4 channels from 4 lane.
     auto frontend_tile = [&](int p, int h, int64_t c0, uint8_t* dst, uint32_t region, int row0) {
         const __nv_bfloat16* x = p == 0 ? fe.xq : (p == 1 ? fe.xk : fe.xv);
-        float y[fe::kFeRun][4], ss[fe::kFeRun];
+        float y[fe::kFeRun][4], inv[fe::kFeRun];
         fe::frontend_run<__nv_bfloat16>(x, fe.x_stride, fe.conv_w, cu, N, T_total, H, p, h, lane,
-                                        c0 + fe::kFeRun * warp, fe.cs_in, y, ss);
+                                        c0 + fe::kFeRun * warp, fe.cs_in, fe.eps, y, inv);
 #pragma unroll
         for (int i = 0; i < fe::kFeRun; ++i) {
-            const float inv = p < 2 ? rsqrtf(ss[i] + fe.eps) : 1.0f;
+            float2 a = make_float2(y[i][0], y[i][1]), b = make_float2(y[i][2], y[i][3]);
+            if (p < 2) {
+                a = __fmul2_rn(a, make_float2(inv[i], inv[i]));
+                b = __fmul2_rn(b, make_float2(inv[i], inv[i]));
+            }
             const uint32_t at = (lane >> 4) * region + sw128(row0 + fe::kFeRun * warp + i, (lane & 15) >> 1) +
                                 (lane & 1) * 8;
-            *reinterpret_cast<uint2*>(dst + at) =
-                make_uint2(pack_bf16x2(y[i][0] * inv, y[i][1] * inv), pack_bf16x2(y[i][2] * inv, y[i][3] * inv));
+            *reinterpret_cast<uint2*>(dst + at) = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(b.x, b.y));
         }
     };
 

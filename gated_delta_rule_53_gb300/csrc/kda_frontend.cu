@@ -35,15 +35,14 @@ shortconv_kernel(const __nv_bfloat16* __restrict__ xq, const __nv_bfloat16* __re
     if (t0 >= T_total) return;
     const __nv_bfloat16* x = p == 0 ? xq : (p == 1 ? xk : xv);
     OutT* out = p == 0 ? q_out : (p == 1 ? k_out : v_out);
-    float y[kRun][4], ss[kRun];
-    fe::frontend_run<OutT, kRun>(x, x_stride, conv_w, cu, N, T_total, H, p, h, lane, t0, cs_in, y, ss);
+    float y[kRun][4], inv[kRun];
+    fe::frontend_run<OutT, kRun>(x, x_stride, conv_w, cu, N, T_total, H, p, h, lane, t0, cs_in, eps, y, inv);
 #pragma unroll
     for (int i = 0; i < kRun; ++i) {
         const int64_t t = t0 + i;
         if (t < T_total) {
-            const float inv = p < 2 ? rsqrtf(ss[i] + eps) : 1.0f;
-            store4<OutT>(out + (t * H + h) * kHeadDim + 4 * lane, y[i][0] * inv, y[i][1] * inv, y[i][2] * inv,
-                         y[i][3] * inv);
+            store4<OutT>(out + (t * H + h) * kHeadDim + 4 * lane, y[i][0] * inv[i], y[i][1] * inv[i],
+                         y[i][2] * inv[i], y[i][3] * inv[i]);
         }
     }
 }

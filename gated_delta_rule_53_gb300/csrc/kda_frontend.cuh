@@ -5,8 +5,8 @@
 //
 // One warp owns one (part, head) and a run of RUN tokens; each lane owns 4 adjacent channels,
 // so a token row of the head is one 256-byte coalesced load.  The warp loads its rows and their
-// 3-token history up front, computes every token's convolution and SiLU, then reduces all the
-// run's squared norms together (the shuffles of different tokens overlap).  A run that crosses a
+// 3-token history up front, computes every token's convolution and SiLU (two channels per packed
+// fp32 instruction), then reduces all the run's squared norms together.  A run that crosses a
 // sequence start takes a general path that reads the carried state.
 #pragma once
 
@@ -16,10 +16,6 @@ namespace kda {
 namespace fe {
 
 constexpr int kFeRun = 8;  // tokens per warp run of the fused prefill (8 warps x 8 = one 64-token chunk)
-
-__device__ __forceinline__ float4 bf16x4(uint2 u) {
-    return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
-}
 
 // Largest n with cu[n] <= t < cu[n + 1] (skips empty sequences).
 __device__ __forceinline__ int find_seq(const int32_t* cu, int N, int64_t t) {
@@ -46,36 +42,78 @@ __device__ __forceinline__ float silu<__nv_bfloat16>(float y) {
     return fmaf(hy, t, hy);
 }
 
+// Two adjacent channels as a float2, computed with the packed fp32 instructions of sm_100 and later: one
+// instruction for both, each half rounded exactly as the scalar multiply or fma.
+__device__ __forceinline__ float2 bf16x2f(uint32_t u) { return make_float2(bf16_lo(u), bf16_hi(u)); }
+
+// ShortConv of a channel pair over the window h0 (oldest) .. h3 (current): w0 h0 + w1 h1 + w2 h2 + w3 h3,
+// accumulated in that order.
+__device__ __forceinline__ float2 conv4(const float2 (&w)[4], float2 h0, float2 h1, float2 h2, float2 h3) {
+    float2 acc = __fmul2_rn(w[0], h0);
+    acc = __ffma2_rn(w[1], h1, acc);
+    acc = __ffma2_rn(w[2], h2, acc);
+    return __ffma2_rn(w[3], h3, acc);
+}
+
+template <typename OutT>
+__device__ __forceinline__ float2 silu2(float2 y) {
+    return make_float2(silu<OutT>(y.x), silu<OutT>(y.y));
+}
+template <>
+__device__ __forceinline__ float2 silu2<__nv_bfloat16>(float2 y) {
+    const float2 hy = __fmul2_rn(y, make_float2(0.5f, 0.5f));
+    float tx, ty;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(tx) : "f"(hy.x));
+    asm("tanh.approx.f32 %0, %1;" : "=f"(ty) : "f"(hy.y));
+    return __ffma2_rn(hy, make_float2(tx, ty), hy);
+}
+
+// Squared norm of a lane's four channels (y0, y1) and (y2, y3): (y0^2 + y2^2) + (y1^2 + y3^2).
+__device__ __forceinline__ float sq4(float2 a, float2 b) {
+    const float2 s = __ffma2_rn(b, b, __fmul2_rn(a, a));
+    return s.x + s.y;
+}
+
 // y[i][e]: part p (0 q, 1 k, 2 v) of token t0 + i, channel 4 lane + e of head h, after the convolution
-// and SiLU; for p < 2, ss[i] = the token's squared norm over the head (the caller scales by
-// 1 / sqrt(ss + eps)).  Tokens at or past T_total give zeros.  x: raw rows of part p.
+// and SiLU; inv[i]: for p < 2, 1 / sqrt(the token's squared norm over the head + eps), the factor the
+// caller scales y by (1 for p = 2).  Tokens at or past T_total give zeros.  x: raw rows of part p.
 template <typename OutT, int RUN = kFeRun>
 __device__ __forceinline__ void frontend_run(const __nv_bfloat16* __restrict__ x, int64_t x_stride,
                                              const __nv_bfloat16* __restrict__ conv_w,
                                              const int32_t* __restrict__ cu, int N, int64_t T_total, int H, int p,
                                              int h, int lane, int64_t t0, const __nv_bfloat16* __restrict__ cs_in,
-                                             float (&y)[RUN][4], float (&ss)[RUN]) {
+                                             float eps, float (&y)[RUN][4], float (&inv)[RUN]) {
     const int64_t C = (int64_t)H * kHeadDim;
     const int64_t ch = (int64_t)h * kHeadDim + 4 * lane;
     const int64_t gc = p * C + ch;
     // raw rows t0 - 3 .. t0 + RUN - 1 (zero outside the tensor), loaded before any arithmetic
     uint2 xr[RUN + 3];
+    if (t0 >= 3 && t0 + RUN <= T_total) {  // the whole window inside the tensor (the warp agrees)
+        const __nv_bfloat16* xp = x + (t0 - 3) * x_stride + ch;
 #pragma unroll
-    for (int i = 0; i < RUN + 3; ++i) {
-        const int64_t s = t0 - 3 + i;
-        xr[i] = (s >= 0 && s < T_total) ? *reinterpret_cast<const uint2*>(x + s * x_stride + ch) : make_uint2(0, 0);
+        for (int i = 0; i < RUN + 3; ++i) xr[i] = *reinterpret_cast<const uint2*>(xp + i * x_stride);
+    } else {
+#pragma unroll
+        for (int i = 0; i < RUN + 3; ++i) {
+            const int64_t s = t0 - 3 + i;
+            xr[i] = (s >= 0 && s < T_total) ? *reinterpret_cast<const uint2*>(x + s * x_stride + ch) : make_uint2(0, 0);
+        }
     }
     // taps of the lane's 4 channels: w[e][0..3], oldest .. current
     const uint4 w01 = *reinterpret_cast<const uint4*>(conv_w + gc * 4);
     const uint4 w23 = *reinterpret_cast<const uint4*>(conv_w + gc * 4 + 8);
     const uint32_t wr[8] = {w01.x, w01.y, w01.z, w01.w, w23.x, w23.y, w23.z, w23.w};
-    float w[4][4];
+    // as channel pairs: wp[c][j] = tap j of channels 2c and 2c + 1
+    float2 wp[2][4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        w[e][0] = bf16_lo(wr[2 * e]); w[e][1] = bf16_hi(wr[2 * e]);
-        w[e][2] = bf16_lo(wr[2 * e + 1]); w[e][3] = bf16_hi(wr[2 * e + 1]);
+    for (int c = 0; c < 2; ++c) {
+        wp[c][0] = make_float2(bf16_lo(wr[4 * c]), bf16_lo(wr[4 * c + 2]));
+        wp[c][1] = make_float2(bf16_hi(wr[4 * c]), bf16_hi(wr[4 * c + 2]));
+        wp[c][2] = make_float2(bf16_lo(wr[4 * c + 1]), bf16_lo(wr[4 * c + 3]));
+        wp[c][3] = make_float2(bf16_hi(wr[4 * c + 1]), bf16_hi(wr[4 * c + 3]));
     }
 
+    float ss[RUN];  // squared norms over the lane's channels, then over the head
     // Sequence bounds.  Fast path: the run and its 3-token history lie inside one sequence.
     int n = cu ? find_seq(cu, N, t0) : 0;
     int64_t bos = cu ? cu[n] : 0, eos = cu ? cu[n + 1] : T_total;
@@ -85,18 +123,12 @@ __device__ __forceinline__ void frontend_run(const __nv_bfloat16* __restrict__ x
     if (simple) {
 #pragma unroll
         for (int i = 0; i < RUN; ++i) {
-            const float4 a0 = bf16x4(xr[i]), a1 = bf16x4(xr[i + 1]), a2 = bf16x4(xr[i + 2]), a3 = bf16x4(xr[i + 3]);
-            const float h0[4] = {a0.x, a0.y, a0.z, a0.w}, h1[4] = {a1.x, a1.y, a1.z, a1.w};
-            const float h2[4] = {a2.x, a2.y, a2.z, a2.w}, h3[4] = {a3.x, a3.y, a3.z, a3.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float acc = w[e][0] * h0[e];
-                acc = fmaf(w[e][1], h1[e], acc);
-                acc = fmaf(w[e][2], h2[e], acc);
-                acc = fmaf(w[e][3], h3[e], acc);
-                y[i][e] = silu<OutT>(acc);
-            }
-            ss[i] = y[i][0] * y[i][0] + y[i][1] * y[i][1] + y[i][2] * y[i][2] + y[i][3] * y[i][3];
+            const float2 y01 = silu2<OutT>(conv4(wp[0], bf16x2f(xr[i].x), bf16x2f(xr[i + 1].x), bf16x2f(xr[i + 2].x),
+                                                 bf16x2f(xr[i + 3].x)));
+            const float2 y23 = silu2<OutT>(conv4(wp[1], bf16x2f(xr[i].y), bf16x2f(xr[i + 1].y), bf16x2f(xr[i + 2].y),
+                                                 bf16x2f(xr[i + 3].y)));
+            y[i][0] = y01.x; y[i][1] = y01.y; y[i][2] = y23.x; y[i][3] = y23.y;
+            ss[i] = p < 2 ? sq4(y01, y23) : 0.f;
         }
     } else {
         // general path: a sequence starts inside the window; earlier positions read the carried state (or zero)
@@ -107,38 +139,66 @@ __device__ __forceinline__ void frontend_run(const __nv_bfloat16* __restrict__ x
                 while ((int64_t)cu[n + 1] <= t) ++n;
                 bos = cu[n];
             }
-            float hist[4][4];
+            uint2 hist[4];  // position t - 3 + j, raw bf16
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {  // position t - 3 + j
+            for (int j = 0; j < 4; ++j) {
                 const int64_t s2 = t - 3 + j;
-                float4 a;
                 if (s2 >= bos) {
-                    a = bf16x4(xr[i + j]);
+                    hist[j] = xr[i + j];
                 } else {
                     const int64_t back = bos - s2;
-                    a = (cs_in && back <= 3)
-                            ? bf16x4(*reinterpret_cast<const uint2*>(cs_in + ((int64_t)n * 3 + (3 - back)) * 3 * C + gc))
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                    hist[j] = (cs_in && back <= 3)
+                                  ? *reinterpret_cast<const uint2*>(cs_in + ((int64_t)n * 3 + (3 - back)) * 3 * C + gc)
+                                  : make_uint2(0, 0);
                 }
-                hist[j][0] = a.x; hist[j][1] = a.y; hist[j][2] = a.z; hist[j][3] = a.w;
             }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float acc = w[e][0] * hist[0][e];
-                acc = fmaf(w[e][1], hist[1][e], acc);
-                acc = fmaf(w[e][2], hist[2][e], acc);
-                acc = fmaf(w[e][3], hist[3][e], acc);
-                y[i][e] = silu<OutT>(acc);
-            }
-            ss[i] = y[i][0] * y[i][0] + y[i][1] * y[i][1] + y[i][2] * y[i][2] + y[i][3] * y[i][3];
+            // the same arithmetic as the fast path
+            const float2 y01 = silu2<OutT>(conv4(wp[0], bf16x2f(hist[0].x), bf16x2f(hist[1].x), bf16x2f(hist[2].x),
+                                                 bf16x2f(hist[3].x)));
+            const float2 y23 = silu2<OutT>(conv4(wp[1], bf16x2f(hist[0].y), bf16x2f(hist[1].y), bf16x2f(hist[2].y),
+                                                 bf16x2f(hist[3].y)));
+            y[i][0] = y01.x; y[i][1] = y01.y; y[i][2] = y23.x; y[i][3] = y23.y;
+            ss[i] = p < 2 ? sq4(y01, y23) : 0.f;
         }
     }
-    // squared norms of q and k over the head: all the run's reductions interleaved
+    // squared norms of q and k over the head (the sum over the 32 lanes), and the scale factors
+#pragma unroll
+    for (int i = 0; i < RUN; ++i) inv[i] = 1.0f;
     if (p < 2) {
+        if constexpr (RUN == 8) {
+            // Reduce-scatter: in each of the first three steps a lane keeps half of its tokens and adds its
+            // partner's partial sums of them, so that lane L ends with token 4 b4 + 2 b3 + b2 (bits of L); two
+            // more steps finish that sum, then every lane reads each token's total from a lane holding it.  The
+            // additions pair lanes in the order of a plain xor-shuffle reduction (16, 8, 4, 2, 1), with the
+            // lane's own partial sum first, so every lane gets the bits that reduction would give; the lanes
+            // holding a token's total take its reciprocal square root, which the others then read.
+            constexpr unsigned kAll = 0xFFFFFFFFu;
+            const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+            float r4[4], r2[2];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
+            for (int j = 0; j < 4; ++j) {
+                const float keep = b4 ? ss[4 + j] : ss[j], send = b4 ? ss[j] : ss[4 + j];
+                r4[j] = keep + __shfl_xor_sync(kAll, send, 16);
+            }
 #pragma unroll
-            for (int i = 0; i < RUN; ++i) ss[i] += __shfl_xor_sync(0xFFFFFFFFu, ss[i], o);
+            for (int j = 0; j < 2; ++j) {
+                const float keep = b3 ? r4[2 + j] : r4[j], send = b3 ? r4[j] : r4[2 + j];
+                r2[j] = keep + __shfl_xor_sync(kAll, send, 8);
+            }
+            float r = (b2 ? r2[1] : r2[0]) + __shfl_xor_sync(kAll, b2 ? r2[0] : r2[1], 4);
+            r += __shfl_xor_sync(kAll, r, 2);
+            r += __shfl_xor_sync(kAll, r, 1);
+            const float ri = rsqrtf(r + eps);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) inv[i] = __shfl_sync(kAll, ri, ((i & 4) << 2) | ((i & 2) << 2) | ((i & 1) << 2));
+        } else {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                for (int i = 0; i < RUN; ++i) ss[i] += __shfl_xor_sync(0xFFFFFFFFu, ss[i], o);
+#pragma unroll
+            for (int i = 0; i < RUN; ++i) inv[i] = rsqrtf(ss[i] + eps);
+        }
     }
 }
 
