@@ -393,9 +393,9 @@ def run_ours(args):
     ws_full, _ = kda.kda_chunk_fwd_workspace_size(w.N, w.T, w.H, torch.bfloat16, w.N > 1)
     ws = torch.empty(ws_full, dtype=torch.uint8, device=device)
     # chunk offsets, then per range of chunk rows the operand kernel and the state pass; with the whole
-    # workspace the library overlaps ranges of max(128, rows / 4) chunk rows once there are >= 256 rows
+    # workspace the library overlaps ranges of max(128, rows / 8) chunk rows once there are >= 256 rows
     rows = w.T // 64 + (w.N if w.N > 1 else (1 if w.T % 64 else 0))
-    ranges = 1 if rows < 256 else -(-rows // max(128, -(-rows // 4)))
+    ranges = 1 if rows < 256 else -(-rows // max(128, -(-rows // 8)))
     launches_per_call = 1 + 2 * ranges
     step = lambda: kda.kda_chunk_fwd(q, k, v, g, b, o=o, final_state=fs, workspace=ws, stream=stream)
     clocks = ClockSampler(smi_index(local))

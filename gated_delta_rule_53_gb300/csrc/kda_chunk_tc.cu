@@ -1101,8 +1101,9 @@ bool encode_chunk_map(CUtensorMap* m, const void* base, CUtensorMapDataType type
 // operand-kernel CTA there.  Measured on one GB300 (96 heads): 8K tokens (128 rows) run fastest as one
 // range (0.842 ms against 0.863 for two overlapped ranges of 64 rows); 32K tokens (512 rows) in four
 // ranges of 128 rows with four items per CTA (3.11 ms against 3.25 for eight ranges of 64 rows and one
-// item per CTA, 3.30 for one range).
-constexpr int64_t kPipeRanges = 4, kPipeMinRows = 128, kPipeItemsPerCta = 4;
+// item per CTA, 3.30 for one range); 256K tokens (4,096 rows) in eight ranges of 512 rows (33.47 ms
+// with the output gate, against 34.12 for four ranges of 1,024 rows and 33.43 for sixteen of 256).
+constexpr int64_t kPipeRanges = 8, kPipeMinRows = 128, kPipeItemsPerCta = 4;
 
 // Two streams per device (created once): a low-priority one for the operand kernel and a
 // high-priority one for the state pass.

@@ -137,7 +137,7 @@ KDA_API kda_status kda_shortconv_l2norm(const void* xq, const void* xk, const vo
  *
  * Overlapped ranges: when the call has at least 256 chunk rows (a chunk row is 64 tokens of
  * every sequence's chunk numbering, all heads) and the workspace holds at least 256 of them,
- * consecutive ranges of max(128, rows / 4) chunk rows overlap (at most half of what the workspace
+ * consecutive ranges of max(128, rows / 8) chunk rows overlap (at most half of what the workspace
  * holds).  The call then forks two internal streams from `stream` with events (the operand kernel
  * on a low-priority one, the state pass on a high-priority one) and makes `stream` wait for both
  * before it returns; nothing else changes for the caller, and the results are the same bits as

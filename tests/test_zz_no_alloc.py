@@ -4,9 +4,9 @@ It has no counterpart in the sources; it is the workspace path with the workspac
 a scratch array in the library's device image.  CPU tests: the symbol is exported and sizes
 whose smallest range does not fit are refused before anything is enqueued.  GPU tests: the
 result is bit-identical to kda_chunk_fwd with a caller workspace, also when the static
-scratch forces several ranges of chunks (8192 tokens x 96 heads: the workspace path overlaps
-its ranges on internal streams, the scratch path runs ranges of 5 chunk rows one after the
-other on the caller's stream), and on two calls in a row.
+scratch forces several ranges of chunks (8192 tokens x 96 heads: the workspace path runs the
+128 chunk rows as one range, the scratch path in ranges of 5 chunk rows one after the other on
+the caller's stream), and on two calls in a row.
 """
 import ctypes
 
