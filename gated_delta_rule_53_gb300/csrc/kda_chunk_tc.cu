@@ -312,6 +312,17 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tma_load_3d(sm + rr + warp * 8192, (warp & 1) ? &tm_q : &tm_k, 64 * (warp >> 1), h, (int)c0, barL);
         }
     };
+    // FE: an item's raw rows (3 of history + 64; q, k, v; the head's 256 bytes each) into L2
+    auto prefetch_rows = [&](int h, int64_t c0) {
+        for (int i = tid; i < 3 * 67 * 2; i += kPrepThreads) {
+            const int p = i / 134, r = (i % 134) >> 1, half = i & 1;
+            const int64_t t = c0 - 3 + r;
+            if (t >= 0 && t < T_total) {
+                const __nv_bfloat16* x = p == 0 ? fe.xq : (p == 1 ? fe.xk : fe.xv);
+                prefetch_l2(x + t * fe.x_stride + (int64_t)h * kD + 64 * half);
+            }
+        }
+    };
     // FE: part p of the chunk's 64 tokens, through the front end, as bf16 into a 128-byte-swizzled operand
     // tile at `dst` (shared or global; two regions of `region` bytes; token i at row row0 + i).  Warp w
     // takes tokens 8w .. 8w+7, lane the 4 channels from 4 lane.
@@ -354,27 +365,20 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         load_g_tma(h, c0, 32768);
         load_beta(h, c0, L);
         load_kq(h, c0, 0);
+        if (FE) prefetch_rows(h, c0);  // the first item's rows: its q and v parts then read L2, not DRAM
         if (tid == 0) pend |= FE ? 16u : 17u;
     }
     for (uint32_t ph = 0; have; ph ^= 1u) {
         const uint32_t P_RR = ph ? 32768u : 0u, P_G = 32768u - P_RR;  // this item's two regions
         const uint32_t P_KG = P_G, P_AKK = P_RR;
         uint8_t* blob = blobs + (int64_t)item * kStride;
-        // the next item's place, early: its global reads complete while this item is worked on
+        // the next item's place, early: its global reads (and with FE its raw rows) complete while this item
+        // is worked on
         const int next_item = item + gridDim.x;
         int h1 = 0, L1 = 0;
         int64_t c01 = 0;
         const bool have_next = locate(next_item, h1, c01, L1);
-        if (FE && have_next) {  // the next item's raw rows (3 of history + 64; q, k, v; this head's 256 bytes) into L2
-            for (int i = tid; i < 3 * 67 * 2; i += kPrepThreads) {
-                const int p = i / 134, r = (i % 134) >> 1, half = i & 1;
-                const int64_t t = c01 - 3 + r;
-                if (t >= 0 && t < T_total) {
-                    const __nv_bfloat16* x = p == 0 ? fe.xq : (p == 1 ? fe.xk : fe.xv);
-                    prefetch_l2(x + t * fe.x_stride + (int64_t)h1 * kD + 64 * half);
-                }
-            }
-        }
+        if (FE && have_next) prefetch_rows(h1, c01);
         if (tid == 0) {
             solo_wait(barG, ph, sAbort, err);
             pend &= ~16u;
