@@ -969,12 +969,15 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_v, const float* init_s
             const int64_t at0 = ((c0 + t0) * H + h) * kD + row;
             __nv_bfloat16* op = o + at0;
             if (gate) {
+                // o sigma(gate) = o / (1 + e^-gate): the fast divide (2 ulp for a divisor in [1, 2^126); beyond,
+                // where sigma < 1e-38, it gives 0) keeps this epilogue inside the dS product's wait
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
                     if (t0 + e < L) {
                         const uint32_t pr = half ? g_cur[4 + (e >> 1)] : g_cur[e >> 1];  // static indices
                         const float gv = (e & 1) ? bf16_hi(pr) : bf16_lo(pr);
-                        op[e * stride] = __float2bfloat16_rn(scale * __uint_as_float(xo[e]) / (1.0f + __expf(-gv)));
+                        op[e * stride] =
+                            __float2bfloat16_rn(__fdividef(scale * __uint_as_float(xo[e]), 1.0f + __expf(-gv)));
                     }
             } else if (L == kC) {
 #pragma unroll
