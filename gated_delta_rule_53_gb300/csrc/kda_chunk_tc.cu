@@ -951,11 +951,20 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_v, const float* init_s
             const int L = (eos - c0) < kC ? (int)(eos - c0) : kC;
             const int64_t stride = (int64_t)H * kD;
             const unsigned short* gp = reinterpret_cast<const unsigned short*>(gate) + ((c0 + 16 * qq) * H + h) * kD + row;
+            if (16 * qq + 16 <= L) {  // all 16 tokens inside the sequence
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t a = (16 * qq + 2 * j < L) ? (uint32_t)__ldcs(gp + (2 * j) * stride) : 0u;
-                const uint32_t c = (16 * qq + 2 * j + 1 < L) ? (uint32_t)__ldcs(gp + (2 * j + 1) * stride) : 0u;
-                g_cur[j] = a | (c << 16);
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t a = __ldcs(gp), c = __ldcs(gp + stride);
+                    g_cur[j] = a | (c << 16);
+                    gp += 2 * stride;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t a = (16 * qq + 2 * j < L) ? (uint32_t)__ldcs(gp + (2 * j) * stride) : 0u;
+                    const uint32_t c = (16 * qq + 2 * j + 1 < L) ? (uint32_t)__ldcs(gp + (2 * j + 1) * stride) : 0u;
+                    g_cur[j] = a | (c << 16);
+                }
             }
         };
         auto emit_o = [&](int mm, int p, int half) {
@@ -969,16 +978,22 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_v, const float* init_s
             const int64_t at0 = ((c0 + t0) * H + h) * kD + row;
             __nv_bfloat16* op = o + at0;
             if (gate) {
-                // o sigma(gate) = o / (1 + e^-gate): the fast divide (2 ulp for a divisor in [1, 2^126); beyond,
-                // where sigma < 1e-38, it gives 0) keeps this epilogue inside the dS product's wait
+                // o sigma(gate) = o / (1 + 2^(-gate log2 e)), token pairs on the packed fp32 instructions, with the
+                // fast divide (2 ulp for a divisor in [1, 2^126); beyond, where sigma < 1e-38, it gives 0): the
+                // epilogue has to fit inside the dS product's wait
+                const float2 sc = make_float2(scale, scale), nl = make_float2(-kLog2e, -kLog2e);
+                const bool whole = t0 + 8 <= L;
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    if (t0 + e < L) {
-                        const uint32_t pr = half ? g_cur[4 + (e >> 1)] : g_cur[e >> 1];  // static indices
-                        const float gv = (e & 1) ? bf16_hi(pr) : bf16_lo(pr);
-                        op[e * stride] =
-                            __float2bfloat16_rn(__fdividef(scale * __uint_as_float(xo[e]), 1.0f + __expf(-gv)));
-                    }
+                for (int e2 = 0; e2 < 4; ++e2) {
+                    const uint32_t pr = half ? g_cur[4 + e2] : g_cur[e2];  // static indices
+                    const float2 t = __fmul2_rn(make_float2(bf16_lo(pr), bf16_hi(pr)), nl);
+                    const float2 d = __fadd2_rn(make_float2(ex2(t.x), ex2(t.y)), make_float2(1.f, 1.f));
+                    const float2 x =
+                        __fmul2_rn(make_float2(__uint_as_float(xo[2 * e2]), __uint_as_float(xo[2 * e2 + 1])), sc);
+                    if (whole || t0 + 2 * e2 < L) op[(2 * e2) * stride] = __float2bfloat16_rn(__fdividef(x.x, d.x));
+                    if (whole || t0 + 2 * e2 + 1 < L)
+                        op[(2 * e2 + 1) * stride] = __float2bfloat16_rn(__fdividef(x.y, d.y));
+                }
             } else if (L == kC) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) op[e * stride] = __float2bfloat16_rn(scale * __uint_as_float(xo[e]));
