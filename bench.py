@@ -749,7 +749,7 @@ def run_ours(args):
         "note": "kda_chunk_fwd_frontend vs kda_shortconv_l2norm + kda_chunk_fwd; same output bits"}
     line["noalloc_prefill"] = {
         "workload": f"{w.name} through kda_chunk_fwd_noalloc: the library's static 64 MiB scratch, chunk ranges "
-                    "of 5 rows one after the other on the caller's stream",
+                    "of 6 rows one after the other on the caller's stream",
         "value": w.T * world / (ms_na * 1e-3), "unit": "tokens/s", "ms_per_step": ms_na, "steps": nsteps}
     line["varlen_32"] = {
         "workload": f"varlen_32: {Nv} packed sequences (1K..32K tokens, sum {Tv}), H={wv.H}, bf16 q,k,v, fp32 g, beta, "

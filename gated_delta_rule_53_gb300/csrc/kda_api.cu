@@ -93,6 +93,13 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Byte ranges [a, a + na) and [b, b + nb) share an address (NULL never does).
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || !na || !nb) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
 kda_status ok() {
     kda::t_last_error[0] = '\0';
     return KDA_OK;
@@ -370,6 +377,14 @@ kda_status kda_chunk_fwd_frontend(const void* xq, const void* xk, const void* xv
     REQUIRE(std::isfinite(scale), "scale must be finite");
     REQUIRE(T_total < ((int64_t)1 << 31), "T_total must be below 2^31 (tensor-map coordinates)");
     REQUIRE(T_total / 64 + N <= 0x7FFFFFFF, "too many chunks");
+    {  // o holds v during the call: it must not share memory with an input
+        const size_t ob = (size_t)T_total * H * d * 2, tb = (size_t)T_total * H;
+        const size_t xb = T_total > 0 ? ((size_t)(T_total - 1) * x_row_stride + (size_t)H * d) * 2 : 0;
+        REQUIRE(!overlaps(o, ob, xq, xb) && !overlaps(o, ob, xk, xb) && !overlaps(o, ob, xv, xb) &&
+                    !overlaps(o, ob, out_gate, ob) && !overlaps(o, ob, g, tb * d * 4) &&
+                    !overlaps(o, ob, beta, tb * 4),
+                "o must not overlap an input (it holds v during the call)");
+    }
     size_t need = 0;
     kda::chunk_tc_workspace(N, T_total, H, cu_seqlens != nullptr, nullptr, &need);
     REQUIRE(workspace != nullptr && workspace_bytes >= need,

@@ -94,9 +94,7 @@ constexpr uint32_t BLOB_TB = 32768;    // T Diag(beta) as bf16 hi then lo, each 
 constexpr uint32_t BLOB_AQ = 49152;    // A_qk as bf16 hi then lo, each [64][64]
 constexpr uint32_t BLOB_KP = 65536;    // K e^{G_C - G} bf16, two regions of [64][64]
 constexpr uint32_t BLOB_EGL = 81920;   // e^{G_C} fp32 [128]
-constexpr uint32_t BLOB_V = 82944;     // fused front end only: v bf16, two regions of [64 tokens][64]
 constexpr uint32_t kBlobBytes = 82432;     // stride of the operands of one (chunk, head)
-constexpr uint32_t kBlobBytesFE = 99328;   // the same with v (fused front end)
 constexpr uint32_t kStateBytes = kD * kD * 4;
 
 
@@ -240,8 +238,8 @@ __device__ __forceinline__ uint32_t g_off(int i, int c) {
     return (uint32_t)(c >> 5) * 8192u + sw128((uint32_t)i, (uint32_t)((c & 31) >> 2)) + (uint32_t)(c & 3) * 4u;
 }
 
-// FE: q, k, v are computed here from the raw front-end rows (ShortConv4 + SiLU + L2 norm, the same
-// arithmetic as kda_shortconv_l2norm) instead of being read.
+// FE: q and k are computed here from the raw front-end rows (ShortConv4 + SiLU + L2 norm, the same
+// arithmetic as kda_shortconv_l2norm) instead of being read (v comes from the stand-alone front end).
 template <bool FE>
 __global__ void __launch_bounds__(kPrepThreads, 2)
 chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -256,7 +254,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t sbase = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int offN = off[N];
-    constexpr uint32_t kStride = FE ? kBlobBytesFE : kBlobBytes;
+    constexpr uint32_t kStride = kBlobBytes;
 
     float* sBeta = reinterpret_cast<float*>(sm + P_BETA);
     float* sE = reinterpret_cast<float*>(sm + P_E);
@@ -312,22 +310,22 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             tma_load_3d(sm + rr + warp * 8192, (warp & 1) ? &tm_q : &tm_k, 64 * (warp >> 1), h, (int)c0, barL);
         }
     };
-    // FE: an item's raw rows (3 of history + 64; q, k, v; the head's 256 bytes each) into L2
+    // FE: an item's raw q and k rows (3 of history + 64; the head's 256 bytes each) into L2
     auto prefetch_rows = [&](int h, int64_t c0) {
-        for (int i = tid; i < 3 * 67 * 2; i += kPrepThreads) {
+        for (int i = tid; i < 2 * 67 * 2; i += kPrepThreads) {
             const int p = i / 134, r = (i % 134) >> 1, half = i & 1;
             const int64_t t = c0 - 3 + r;
             if (t >= 0 && t < T_total) {
-                const __nv_bfloat16* x = p == 0 ? fe.xq : (p == 1 ? fe.xk : fe.xv);
+                const __nv_bfloat16* x = p == 0 ? fe.xq : fe.xk;
                 prefetch_l2(x + t * fe.x_stride + (int64_t)h * kD + 64 * half);
             }
         }
     };
-    // FE: part p of the chunk's 64 tokens, through the front end, as bf16 into a 128-byte-swizzled operand
-    // tile at `dst` (shared or global; two regions of `region` bytes; token i at row row0 + i).  Warp w
+    // FE: part p (q or k) of the chunk's 64 tokens, through the front end, as bf16 into a 128-byte-swizzled
+    // operand tile in shared memory at `dst` (two regions of `region` bytes; token i at row row0 + i).  Warp w
     // takes tokens 8w .. 8w+7, lane the 4 channels from 4 lane.
     auto frontend_tile = [&](int p, int h, int64_t c0, uint8_t* dst, uint32_t region, int row0) {
-        const __nv_bfloat16* x = p == 0 ? fe.xq : (p == 1 ? fe.xk : fe.xv);
+        const __nv_bfloat16* x = p == 0 ? fe.xq : fe.xk;
         float y[fe::kFeRun][4], inv[fe::kFeRun];
         fe::frontend_run<__nv_bfloat16>(x, fe.x_stride, fe.conv_w, cu, N, T_total, H, p, h, lane,
                                         c0 + fe::kFeRun * warp, fe.cs_in, fe.eps, y, inv);
@@ -365,7 +363,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         load_g_tma(h, c0, 32768);
         load_beta(h, c0, L);
         load_kq(h, c0, 0);
-        if (FE) prefetch_rows(h, c0);  // the first item's rows: its q and v parts then read L2, not DRAM
+        if (FE) prefetch_rows(h, c0);  // the first item's rows: its q part then reads L2, not DRAM
         if (tid == 0) pend |= FE ? 16u : 17u;
     }
     for (uint32_t ph = 0; have; ph ^= 1u) {
@@ -497,7 +495,6 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
         for (int I = 0; I < 4; ++I)
             *reinterpret_cast<uint4*>(sm + P_KG + reg * 8192 + sw128(r4 + 16 * I, ch)) = kg_hold[I];
-        if (FE) frontend_tile(2, h, c0, blob + BLOB_V, 8192, 0);  // v to the workspace, while the A products run
         fence_proxy_async();
         if (tid == 0) {
             solo_wait(barA, ph, sAbort, err);
@@ -731,8 +728,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_v, const float* init_s
                    const int32_t* __restrict__ off, int64_t T_total, int H, float scale,
                    const __nv_bfloat16* __restrict__ gate, __nv_bfloat16* __restrict__ o, float* final_state,
                    const float* carry_in, float* carry_out, int first_range, int m0, int m1,
-                   const uint8_t* __restrict__ blobs, uint32_t blob_bytes, int v_in_blob, int mode,
-                   unsigned int* err) {
+                   const uint8_t* __restrict__ blobs, uint32_t blob_bytes, int mode, unsigned int* err) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(sm);
@@ -797,19 +793,15 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_v, const float* init_s
             iss ^= 1u << j;
         };
         // T_b from the workspace; v straight from its tensor (token rows of the chunk; rows past the end of the
-        // sequence meet zero columns of T_b) or, with the fused front end, from the workspace
+        // sequence meet zero columns of T_b)
         auto load_v = [&](int mm, int j) {
             if (lane == 0) {
                 fence_proxy_async();
                 mbar_arrive_expect_tx(barV + j, 32768);
                 bulk_load(sm + S_TB + j * 16384, blob_of(mm) + BLOB_TB, 16384, barV + j);
-                if (v_in_blob) {
-                    bulk_load(sm + S_V + j * 16384, blob_of(mm) + BLOB_V, 16384, barV + j);
-                } else {
-                    const int tok = (int)(bos + (int64_t)kC * (mm - on));
-                    tma_load_3d(sm + S_V + j * 16384, &tm_v, 0, h, tok, barV + j);
-                    tma_load_3d(sm + S_V + j * 16384 + 8192, &tm_v, 64, h, tok, barV + j);
-                }
+                const int tok = (int)(bos + (int64_t)kC * (mm - on));
+                tma_load_3d(sm + S_V + j * 16384, &tm_v, 0, h, tok, barV + j);
+                tma_load_3d(sm + S_V + j * 16384 + 8192, &tm_v, 64, h, tok, barV + j);
             }
             __syncwarp();
             iss ^= 8u << j;
@@ -978,22 +970,16 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_v, const float* init_s
             const int64_t at0 = ((c0 + t0) * H + h) * kD + row;
             __nv_bfloat16* op = o + at0;
             if (gate) {
-                // o sigma(gate) = o / (1 + 2^(-gate log2 e)), token pairs on the packed fp32 instructions, with the
-                // fast divide (2 ulp for a divisor in [1, 2^126); beyond, where sigma < 1e-38, it gives 0): the
-                // epilogue has to fit inside the dS product's wait
-                const float2 sc = make_float2(scale, scale), nl = make_float2(-kLog2e, -kLog2e);
-                const bool whole = t0 + 8 <= L;
+                // o sigma(gate) = o / (1 + e^-gate): the fast divide (2 ulp for a divisor in [1, 2^126); beyond,
+                // where sigma < 1e-38, it gives 0) keeps this epilogue inside the dS product's wait
 #pragma unroll
-                for (int e2 = 0; e2 < 4; ++e2) {
-                    const uint32_t pr = half ? g_cur[4 + e2] : g_cur[e2];  // static indices
-                    const float2 t = __fmul2_rn(make_float2(bf16_lo(pr), bf16_hi(pr)), nl);
-                    const float2 d = __fadd2_rn(make_float2(ex2(t.x), ex2(t.y)), make_float2(1.f, 1.f));
-                    const float2 x =
-                        __fmul2_rn(make_float2(__uint_as_float(xo[2 * e2]), __uint_as_float(xo[2 * e2 + 1])), sc);
-                    if (whole || t0 + 2 * e2 < L) op[(2 * e2) * stride] = __float2bfloat16_rn(__fdividef(x.x, d.x));
-                    if (whole || t0 + 2 * e2 + 1 < L)
-                        op[(2 * e2 + 1) * stride] = __float2bfloat16_rn(__fdividef(x.y, d.y));
-                }
+                for (int e = 0; e < 8; ++e)
+                    if (t0 + e < L) {
+                        const uint32_t pr = half ? g_cur[4 + (e >> 1)] : g_cur[e >> 1];  // static indices
+                        const float gv = (e & 1) ? bf16_hi(pr) : bf16_lo(pr);
+                        op[e * stride] =
+                            __float2bfloat16_rn(__fdividef(scale * __uint_as_float(xo[e]), 1.0f + __expf(-gv)));
+                    }
             } else if (L == kC) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) op[e * stride] = __float2bfloat16_rn(scale * __uint_as_float(xo[e]));
@@ -1176,8 +1162,7 @@ struct EventSet {
 };
 
 // Workspace: [carried states, 2 x H x 128 x 128 fp32][chunk offsets, int32 N + 1][operands of
-// `rows` chunk rows x H heads, kBlobBytes each (kBlobBytesFE with the fused front end)].  The size
-// query counts rows of the larger blob, so one workspace serves both.
+// `rows` chunk rows x H heads, kBlobBytes each] (the same with the fused front end).
 static size_t ws_header_bytes(int N, int H) {
     return (size_t)2 * H * kStateBytes + (((size_t)(N + 1) * 4 + 1023) / 1024) * 1024;
 }
@@ -1188,7 +1173,7 @@ static int64_t max_chunk_rows(int N, int64_t T_total, bool have_cu) {
 }
 
 void chunk_tc_workspace(int N, int64_t T_total, int H, bool have_cu, size_t* full_bytes, size_t* min_bytes) {
-    const size_t row = (size_t)H * kBlobBytesFE, hdr = ws_header_bytes(N, H);
+    const size_t row = (size_t)H * kBlobBytes, hdr = ws_header_bytes(N, H);
     const int64_t rows = max_chunk_rows(N, T_total, have_cu);
     if (full_bytes) *full_bytes = hdr + row * (size_t)(rows > 0 ? rows : 1);
     if (min_bytes) *min_bytes = hdr + row;
@@ -1201,7 +1186,10 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
                             cudaStream_t stream, int state_mode, float* final_state2, int state_mode2,
                             bool overlap) {
     CUtensorMap tq = {}, tk = {}, tv = {}, tg;
-    const uint32_t blob_bytes = front ? kBlobBytesFE : kBlobBytes;
+    const uint32_t blob_bytes = kBlobBytes;
+    // With the fused front end, v is computed by the stand-alone front end into `o` (the same shape) and read
+    // back from there: each chunk's v tile is loaded before that chunk's outputs are written over it.
+    if (front && !encode_chunk_map(&tv, o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, T_total, H)) return cudaErrorInvalidValue;
     if (!front && (!encode_chunk_map(&tq, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, T_total, H) ||
                    !encode_chunk_map(&tk, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, T_total, H) ||
                    !encode_chunk_map(&tv, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 64, T_total, H)))
@@ -1257,6 +1245,11 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
         e = cudaEventRecord(ev_start, stream);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(s_prep, ev_start, 0);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(s_state, ev_start, 0);
+        // v of the whole call ahead of the first state pass, beside the first range's operands (a pass bound by
+        // memory beside one bound by its instruction stream)
+        if (e == cudaSuccess && front)
+            e = launch_frontend_v(front->xv, front->x_stride, front->conv_w, cu_seqlens, N, T_total, H,
+                                  front->conv_state_in, o, s_state);
         for (int r = 0; r < nr && e == cudaSuccess; ++r) {
             const int64_t r0 = (int64_t)r * rr, r1 = r0 + rr < rows_max ? r0 + rr : rows_max;
             uint8_t* buf = blobs + (size_t)(r & 1) * (size_t)rr * H * blob_bytes;
@@ -1275,7 +1268,7 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
             chunk_state_kernel<<<(unsigned)((int64_t)N * H), kThreads, kStateSmem, s_state>>>(
                 tv, init_state, cu_seqlens, off, T_total, H, scale, static_cast<const __nv_bfloat16*>(out_gate),
                 static_cast<__nv_bfloat16*>(o), final_state, c_in, c_out, r == 0 ? 1 : 0, (int)r0, (int)r1, buf,
-                blob_bytes, front ? 1 : 0, state_mode, err);
+                blob_bytes, state_mode, err);
             e = cudaGetLastError();
             if (e == cudaSuccess) e = cudaEventRecord(ev[nr + r], s_state);
         }
@@ -1283,6 +1276,11 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
         if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev[nr - 1], 0);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev[2 * nr - 1], 0);
         return e;
+    }
+    if (front) {
+        e = launch_frontend_v(front->xv, front->x_stride, front->conv_w, cu_seqlens, N, T_total, H,
+                              front->conv_state_in, o, stream);
+        if (e != cudaSuccess) return e;
     }
     int range = 0;
     for (int64_t r0 = 0; range == 0 || r0 < rows_max; r0 += rows, ++range) {
@@ -1298,11 +1296,11 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
         chunk_state_kernel<<<(unsigned)((int64_t)N * H), kThreads, kStateSmem, stream>>>(
             tv, init_state, cu_seqlens, off, T_total, H, scale, static_cast<const __nv_bfloat16*>(out_gate),
             static_cast<__nv_bfloat16*>(o), final_state, c_in, c_out, range == 0 ? 1 : 0, (int)r0, (int)r1, blobs,
-            blob_bytes, front ? 1 : 0, state_mode, err);
+            blob_bytes, state_mode, err);
         if (final_state2)
             chunk_state_kernel<<<(unsigned)((int64_t)N * H), kThreads, kStateSmem, stream>>>(
                 tv, nullptr, cu_seqlens, off, T_total, H, scale, nullptr, nullptr, final_state2, nullptr, nullptr, 1,
-                (int)r0, (int)r1, blobs, blob_bytes, front ? 1 : 0, state_mode2, err);
+                (int)r0, (int)r1, blobs, blob_bytes, state_mode2, err);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

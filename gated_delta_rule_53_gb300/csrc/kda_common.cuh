@@ -84,6 +84,8 @@ cudaError_t launch_shortconv_l2norm(const void* xq, const void* xk, const void* 
                                     const void* conv_w, const int32_t* cu_seqlens, int N, int64_t T_total,
                                     int H, const void* conv_state_in, void* conv_state_out, float eps,
                                     kda_dtype out_dtype, void* q, void* k, void* v, cudaStream_t stream);
+cudaError_t launch_frontend_v(const void* xv, int64_t x_stride, const void* conv_w, const int32_t* cu_seqlens, int N,
+                              int64_t T_total, int H, const void* conv_state_in, void* v, cudaStream_t stream);
 
 cudaError_t launch_chunk_simt(const void* q, const void* k, const void* v, const float* g, const float* beta,
                               const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total,

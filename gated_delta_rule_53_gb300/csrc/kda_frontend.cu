@@ -28,8 +28,8 @@ shortconv_kernel(const __nv_bfloat16* __restrict__ xq, const __nv_bfloat16* __re
                  const __nv_bfloat16* __restrict__ xv, int64_t x_stride,
                  const __nv_bfloat16* __restrict__ conv_w, const int32_t* __restrict__ cu, int N,
                  int64_t T_total, int H, const __nv_bfloat16* __restrict__ cs_in, float eps,
-                 OutT* __restrict__ q_out, OutT* __restrict__ k_out, OutT* __restrict__ v_out) {
-    const int p = blockIdx.z, h = blockIdx.y;
+                 OutT* __restrict__ q_out, OutT* __restrict__ k_out, OutT* __restrict__ v_out, int p0) {
+    const int p = p0 + (int)blockIdx.z, h = blockIdx.y;  // parts p0 .. p0 + gridDim.z - 1
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t t0 = ((int64_t)blockIdx.x * kWarps + warp) * kRun;
     if (t0 >= T_total) return;
@@ -93,11 +93,11 @@ cudaError_t launch_shortconv_l2norm(const void* xq, const void* xk, const void* 
         if (out_dtype == KDA_DTYPE_BF16)
             shortconv_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, stream>>>(
                 bq, bk, bv, x_stride, w, cu_seqlens, N, T_total, H, cs_in, eps, static_cast<__nv_bfloat16*>(q),
-                static_cast<__nv_bfloat16*>(k), static_cast<__nv_bfloat16*>(v));
+                static_cast<__nv_bfloat16*>(k), static_cast<__nv_bfloat16*>(v), 0);
         else
             shortconv_kernel<float><<<grid, kWarps * 32, 0, stream>>>(
                 bq, bk, bv, x_stride, w, cu_seqlens, N, T_total, H, cs_in, eps, static_cast<float*>(q),
-                static_cast<float*>(k), static_cast<float*>(v));
+                static_cast<float*>(k), static_cast<float*>(v), 0);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -105,6 +105,19 @@ cudaError_t launch_shortconv_l2norm(const void* xq, const void* xk, const void* 
         return launch_conv_state_out(xq, xk, xv, x_stride, cu_seqlens, N, T_total, H, conv_state_in, conv_state_out,
                                      stream);
     return cudaSuccess;
+}
+
+// v alone (bf16), for the fused prefill, which computes q and k inside its chunk pass.
+cudaError_t launch_frontend_v(const void* xv, int64_t x_stride, const void* conv_w, const int32_t* cu_seqlens, int N,
+                              int64_t T_total, int H, const void* conv_state_in, void* v, cudaStream_t stream) {
+    if (T_total <= 0) return cudaSuccess;
+    const int64_t per_cta = (int64_t)kWarps * kRun;
+    dim3 grid((unsigned)((T_total + per_cta - 1) / per_cta), (unsigned)H, 1);
+    const auto* bv = static_cast<const __nv_bfloat16*>(xv);
+    shortconv_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, stream>>>(
+        bv, bv, bv, x_stride, static_cast<const __nv_bfloat16*>(conv_w), cu_seqlens, N, T_total, H,
+        static_cast<const __nv_bfloat16*>(conv_state_in), 0.f, nullptr, nullptr, static_cast<__nv_bfloat16*>(v), 2);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_conv_state_out(const void* xq, const void* xk, const void* xv, int64_t x_stride,

@@ -155,8 +155,8 @@ KDA_API kda_status kda_shortconv_l2norm(const void* xq, const void* xk, const vo
  * (chunk, head) at once, everything that does not depend on the carried state (the
  * in-chunk decays, the A_kk / A_qk blocks, T = (I + A_kk)^-1, W = T diag(beta) K e^G and
  * T diag(beta) itself) and stores the chunk's operands in the workspace (82,432 bytes per
- * chunk and head; 99,328 with the fused front end, which also stores v); the second walks
- * each sequence's chunks in order with the state, forming U = T diag(beta) V from v itself.
+ * chunk and head); the second walks each sequence's chunks in order with the state, forming
+ * U = T diag(beta) V from v itself.
  */
 KDA_API kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                          const float* init_state, const int32_t* cu_seqlens, int N, int64_t T_total, int H,
@@ -166,7 +166,8 @@ KDA_API kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, co
 /*
  * The prefill with its front end fused in: the result of kda_shortconv_l2norm (bf16 outputs)
  * followed by kda_chunk_fwd (bf16), without writing and re-reading q, k, v (the front end runs
- * inside the chunk pass, on the same arithmetic, so the outputs are the same bits).  This is the
+ * inside the chunk pass, on the same arithmetic, so the outputs are the same bits: q and k in the
+ * kernel that builds the chunk operands, v by the stand-alone front end into o).  This is the
  * pages' normalisation "in the kernel" taken one step further ("深入 Kimi-K3: Hugging Face 仓库
  * 分析", paragraph on KDA).
  *
@@ -174,6 +175,10 @@ KDA_API kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, co
  *                  as kda_shortconv_l2norm (conv_state_out may alias conv_state_in)
  *  g, beta, init_state, cu_seqlens, N, scale, chunk_size, out_gate, o, final_state, workspace
  *                  as kda_chunk_fwd with dtype KDA_DTYPE_BF16 (o bf16 [T_total, H, d])
+ *
+ * o holds v during the call (the front end writes v there and the state pass reads each chunk's
+ * tile of it before writing that chunk's outputs over it), so o must not overlap xq, xk, xv,
+ * out_gate, g or beta: KDA_ERR_INVALID_ARG otherwise.
  */
 KDA_API kda_status kda_chunk_fwd_frontend(const void* xq, const void* xk, const void* xv, int64_t x_row_stride,
                                   const void* conv_w, const void* conv_state_in, void* conv_state_out,
@@ -189,7 +194,7 @@ KDA_API kda_status kda_chunk_fwd_frontend(const void* xq, const void* xk, const 
  * 64 MiB scratch array that is part of the library's device image (every GPU that loads the
  * library holds it until exit), so neither the caller nor the library allocates anything: no
  * cudaMalloc, no internal streams, no events.  Its chunk ranges (as many chunk rows per range
- * as fit in 64 MiB; about 5 rows at H = 96) run one after the other on `stream`.
+ * as fit in 64 MiB; 6 rows at H = 96) run one after the other on `stream`.
  * The first call on a device looks up the array's device address (with that device current)
  * and keeps it; make that first call before any stream capture.
  * Returns KDA_ERR_UNSUPPORTED, before enqueueing anything, when even one chunk row of all

@@ -60,15 +60,15 @@ def _ws(lib, N, T, H, dtype=1, cu=1):
 
 
 def test_workspace_size(lib):
-    # carried states 2 x H x 64 KiB, chunk offsets rounded to 1 KiB, 99,328 bytes per chunk and head (the
-    # operands of the fused front-end path, the larger of the two layouts)
+    # carried states 2 x H x 64 KiB, chunk offsets rounded to 1 KiB, 82,432 bytes per chunk and head (the
+    # chunk operands, the same layout with and without the fused front end)
     hdr = 2 * 96 * 65536 + 1024
-    assert _ws(lib, 1, 8192, 96, cu=0) == (0, hdr + 128 * 96 * 99328, hdr + 96 * 99328)
-    assert _ws(lib, 1, 8193, 96, cu=0) == (0, hdr + 129 * 96 * 99328, hdr + 96 * 99328)
+    assert _ws(lib, 1, 8192, 96, cu=0) == (0, hdr + 128 * 96 * 82432, hdr + 96 * 82432)
+    assert _ws(lib, 1, 8193, 96, cu=0) == (0, hdr + 129 * 96 * 82432, hdr + 96 * 82432)
     # with cu_seqlens the chunk count is bounded by T / 64 + N
-    assert _ws(lib, 32, 520949, 96)[1] == hdr + (520949 // 64 + 32) * 96 * 99328
-    assert _ws(lib, 300, 1000, 4)[2] == 2 * 4 * 65536 + 2048 + 4 * 99328
-    assert _ws(lib, 1, 0, 96, cu=0)[1] == hdr + 96 * 99328
+    assert _ws(lib, 32, 520949, 96)[1] == hdr + (520949 // 64 + 32) * 96 * 82432
+    assert _ws(lib, 300, 1000, 4)[2] == 2 * 4 * 65536 + 2048 + 4 * 82432
+    assert _ws(lib, 1, 0, 96, cu=0)[1] == hdr + 96 * 82432
     assert _ws(lib, 1, 256, 4, dtype=0) == (0, 0, 0)      # the fp32 path needs none
     assert _ws(lib, 2, 256, 4, cu=0)[0] == 1               # several sequences need cu_seqlens
     assert _ws(lib, 1, 256, 4, cu=0)[0] == 0
@@ -124,7 +124,7 @@ def test_recurrent_step_rejects_bad_arguments(lib):
 def test_chunk_fwd_frontend_rejects_bad_arguments(lib):
     def call(**over):
         a = dict(x=P(4096), stride=256, w=P(4096), cs_in=None, cs_out=None, eps=1e-6, g=P(4096), b=P(4096),
-                 init=None, cu=None, N=1, T=64, H=2, d=128, scale=1.0, chunk=64, gate=None, o=P(4096), fs=None,
+                 init=None, cu=None, N=1, T=64, H=2, d=128, scale=1.0, chunk=64, gate=None, o=P(1 << 32), fs=None,
                  ws=P(4096), wsb=1 << 30)
         a.update(over)
         return lib.kda_chunk_fwd_frontend(a["x"], a["x"], a["x"], a["stride"], a["w"], a["cs_in"], a["cs_out"],
@@ -138,8 +138,17 @@ def test_chunk_fwd_frontend_rejects_bad_arguments(lib):
     assert call(chunk=32) == 2
     assert call(eps=-1.0) == 1
     assert call(ws=None) == 1
-    assert call(wsb=1024) == 1
+    assert call(wsb=1024) == 1 and b"workspace" in lib.kda_last_error()
     assert call(N=2) == 1                 # several sequences need cu_seqlens
+    # o holds v during the call: sharing memory with an input is refused before anything is enqueued
+    assert call(o=P(4096 + 64 * 256), wsb=1024) == 1                   # inside the raw rows (T x stride x 2 bytes)
+    assert b"overlap" in lib.kda_last_error()
+    assert call(gate=P(1 << 32), wsb=1024) == 1                        # the output gate in place
+    assert b"overlap" in lib.kda_last_error()
+    assert call(g=P(1 << 33), o=P((1 << 33) + 4096), wsb=1024) == 1    # inside g (T x H x d x 4 bytes)
+    assert b"overlap" in lib.kda_last_error()
+    assert call(o=P((1 << 32) + 65536), wsb=1024) == 1                 # clear of every input: the next check
+    assert b"workspace" in lib.kda_last_error()
 
 
 def test_segment_summary_and_combine_reject_bad_arguments(lib):

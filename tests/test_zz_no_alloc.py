@@ -5,7 +5,7 @@ a scratch array in the library's device image.  CPU tests: the symbol is exporte
 whose smallest range does not fit are refused before anything is enqueued.  GPU tests: the
 result is bit-identical to kda_chunk_fwd with a caller workspace, also when the static
 scratch forces several ranges of chunks (8192 tokens x 96 heads: the workspace path runs the
-128 chunk rows as one range, the scratch path in ranges of 5 chunk rows one after the other on
+128 chunk rows as one range, the scratch path in ranges of 6 chunk rows one after the other on
 the caller's stream), and on two calls in a row.
 """
 import ctypes
@@ -47,11 +47,12 @@ def test_exported_and_declared(kda):
 def test_oversize_is_refused_on_the_host(kda):
     lib = kda.library()
     UNSUPPORTED, INVALID = 2, 1
-    least = kda.kda_chunk_fwd_workspace_size(1, 64, 300, have_cu_seqlens=False)[1]
+    # one chunk row needs 2 x 64 KiB of carried state and 82,432 bytes of operands per head (+ 1 KiB)
+    least = kda.kda_chunk_fwd_workspace_size(1, 64, 315, have_cu_seqlens=False)[1]
     assert least > SCRATCH
-    assert _call(lib, H=300) == UNSUPPORTED
+    assert _call(lib, H=315) == UNSUPPORTED
     assert b"static scratch" in lib.kda_last_error()
-    assert kda.kda_chunk_fwd_workspace_size(1, 64, 290, have_cu_seqlens=False)[1] <= SCRATCH
+    assert kda.kda_chunk_fwd_workspace_size(1, 64, 314, have_cu_seqlens=False)[1] <= SCRATCH
     assert _call(lib, N=0) == INVALID
     assert _call(lib, q=None) == INVALID
     assert _call(lib, dtype=7) == INVALID
