@@ -473,7 +473,12 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                     if (J < I) continue;
                     if (J > I) {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) kr[e] *= dn[J - 1][e];
+                        for (int e = 0; e < 8; e += 2) {
+                            const float2 x = __fmul2_rn(make_float2(kr[e], kr[e + 1]),
+                                                        make_float2(dn[J - 1][e], dn[J - 1][e + 1]));
+                            kr[e] = x.x;
+                            kr[e + 1] = x.y;
+                        }
                     }
                     const uint4 u = pack8(kr);
                     *reinterpret_cast<uint4*>(sm + P_CT + reg * kCTRegion + sw128(8 * J * (J + 1) + i, ch)) = u;
