@@ -1,11 +1,12 @@
 """Profiling harness: runs one entry point of the library on a named synthetic case a
 few times, so that a profiler can capture a handful of launches of one kernel.
 
-  python -m gated_delta_rule_53_gb300.profile {prefill_8k,prefill_2k,varlen_small,long_16k,decode_64,decode_16,
-                                               frontend_8k,gates_8k,bwd_8k,bwd_2k} [--iters N]
+  python -m gated_delta_rule_53_gb300.profile {prefill_8k,prefill_8k_gate,prefill_2k,varlen_small,long_16k,
+                                               decode_64,decode_16,frontend_8k,gates_8k,bwd_8k,bwd_2k} [--iters N]
 
 Cases (all inputs larger than the 129 MB L2, a few GB on the device at most):
   prefill_8k   kda_chunk_fwd, 1 x 8192 tokens x 96 heads, bf16
+  prefill_8k_gate  the same with a bf16 N(0, 1) sigmoid output gate (the long workload's epilogue)
   prefill_2k   kda_chunk_fwd, 1 x 2048 tokens x 96 heads, bf16
   varlen_small kda_chunk_fwd, 4 packed sequences (1500, 3000, 2100, 2600 tokens) x 96 heads, bf16, initial
                states N(0, 0.02): the packed path of the 32-sequence workload at about 1/57 of its tokens
@@ -37,14 +38,14 @@ def main():
     from kda_synth.device import fill_device
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["prefill_8k", "prefill_2k", "varlen_small", "long_16k", "decode_64", "decode_16",
-                                     "frontend_8k", "gates_8k", "bwd_8k", "bwd_2k"])
+    ap.add_argument("case", choices=["prefill_8k", "prefill_8k_gate", "prefill_2k", "varlen_small", "long_16k",
+                                     "decode_64", "decode_16", "frontend_8k", "gates_8k", "bwd_8k", "bwd_2k"])
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
     if args.case.startswith("prefill") or args.case.startswith("bwd"):
-        T = 8192 if args.case.endswith("8k") else 2048
+        T = 8192 if "8k" in args.case else 2048
         w = ks.Workload(args.case, "prefill", 53002, H=96, lengths=[T])
         q = fill_device(w.seed, ks.TID_Q, ks.UNIT_GROUPS, (T, 96, 128), "bf16", 0.0, 128.0, device=dev)
         k = fill_device(w.seed, ks.TID_K, ks.UNIT_GROUPS, (T, 96, 128), "bf16", 0.0, 128.0, device=dev)
@@ -52,6 +53,9 @@ def main():
         g = fill_device(w.seed, ks.TID_G, w.g_kind, (T, 96, 128), "f32", device=dev)
         b = fill_device(w.seed, ks.TID_BETA, ks.SIGMOID, (T, 96), "f32", device=dev)
         fn = lambda: kda.kda_chunk_fwd(q, k, v, g, b)
+        if args.case == "prefill_8k_gate":
+            gate = fill_device(w.seed, ks.TID_GATE, ks.NORMAL, (T, 96 * 128), "bf16", device=dev)
+            fn = lambda: kda.kda_chunk_fwd(q, k, v, g, b, out_gate=gate)
         if args.case.startswith("bwd"):
             do = fill_device(w.seed, ks.TID_DO, ks.NORMAL, (T, 96, 128), "bf16", device=dev)
             ws = torch.empty(kda.kda_chunk_bwd_workspace_size(1, T, 96), dtype=torch.uint8, device=dev)
