@@ -101,8 +101,9 @@ cudaError_t launch_chunk_bwd(const void* q, const void* k, const void* v, const 
                              float* dk, float* dv, float* dg, float* dbeta, float* d_init, void* workspace,
                              unsigned int* err, cudaStream_t stream);
 
-// Raw inputs of the fused prefill: q, k, v are computed from them by the front end of
-// kda_shortconv_l2norm (bf16) inside the chunk pass instead of being read.
+// Raw inputs of the fused prefill: q and k are computed from them by the front end of
+// kda_shortconv_l2norm (bf16) inside the chunk pass instead of being read, v by that front end
+// into the output buffer, from which the state pass reads it.
 struct ChunkFrontend {
     const void* xq;
     const void* xk;
