@@ -99,6 +99,24 @@ FWD_SOURCES = "kda_chunk_tc.cu+kda_tsolve.cuh+kda_frontend.cuh"
 BWD_SOURCES = "kda_chunk_bwd.cu+kda_chunk_bwd_tc.cu+kda_bwd_tc.cuh+kda_tsolve.cuh"
 
 
+def prefill_launches(rows_max: int, rows_fit: int, packed: bool, fused: bool = False) -> int:
+    """Kernel launches of one kda_chunk_fwd (fused: kda_chunk_fwd_frontend) call, as the library issues them:
+    the chunk-offset kernel (packed sequences only), the front end of v (fused only), then per range of chunk
+    rows an operand kernel and a state pass.  Ranges: about eight of at least 128 rows, at most half of what
+    the workspace holds, overlapped, once the call and the workspace both hold 256 rows; otherwise as many
+    rows as the workspace holds, one range after the other."""
+    extra = (1 if packed else 0) + (1 if fused else 0)
+    if rows_max <= 0:
+        return extra + 1  # no chunk: the state pass alone (initial states pass through)
+    rows_fit = max(min(rows_fit, rows_max), 1)
+    if rows_fit >= 256 and rows_max >= 256:
+        rr = min(max(128, -(-rows_max // 8)), rows_fit // 2)
+        nr = -(-rows_max // rr)
+    else:
+        nr = -(-rows_max // rows_fit)
+    return extra + 2 * nr
+
+
 def fp32_alu_peak_tflops(sms: int = 152, lanes: int = 128, mhz: float = 2070.0) -> float:
     """fp32 FMA rate of the part: SMs x fp32 lanes per SM x 2 flop x the maximum SM clock."""
     return sms * lanes * 2 * mhz * 1e6 / 1e12
@@ -392,11 +410,10 @@ def run_ours(args):
     # the prefill's workspace (per-chunk operands of the state-independent kernel): all chunks in one range
     ws_full, _ = kda.kda_chunk_fwd_workspace_size(w.N, w.T, w.H, torch.bfloat16, w.N > 1)
     ws = torch.empty(ws_full, dtype=torch.uint8, device=device)
-    # chunk offsets, then per range of chunk rows the operand kernel and the state pass; with the whole
-    # workspace the library overlaps ranges of max(128, rows / 8) chunk rows once there are >= 256 rows
+    # per range of chunk rows the operand kernel and the state pass (and the chunk offsets of packed sequences);
+    # with the whole workspace the library overlaps ranges of max(128, rows / 8) chunk rows from 256 rows on
     rows = w.T // 64 + (w.N if w.N > 1 else (1 if w.T % 64 else 0))
-    ranges = 1 if rows < 256 else -(-rows // max(128, -(-rows // 8)))
-    launches_per_call = 1 + 2 * ranges
+    launches_per_call = prefill_launches(rows, rows, w.N > 1)
     step = lambda: kda.kda_chunk_fwd(q, k, v, g, b, o=o, final_state=fs, workspace=ws, stream=stream)
     clocks = ClockSampler(smi_index(local))
     clocks.start()
@@ -449,7 +466,8 @@ def run_ours(args):
         seg = {"workload": f"{w.name} cut into {nseg} segments of {w.T // nseg} tokens: context-parallel ranks "
                            "played in turn on one GPU (no exchange between devices timed)",
                "value": w.T / (ms_seg * 1e-3), "unit": "tokens/s", "ms_per_step": ms_seg, "steps": ssteps,
-               "gpu_launches": ssteps * (nseg * 4 + (nseg - 1) + nseg * 3),
+               # per segment: operand kernel + two state passes (summary), operand kernel + state pass (re-run)
+               "gpu_launches": ssteps * (nseg * 3 + (nseg - 1) + nseg * 2),
                "segment_summary_ms": ms_sum, "state_combine_ms": ms_comb, "segment_rerun_ms": ms_run,
                "last_rank_ms": ms_sum + (nseg - 1) * ms_comb + ms_run,
                "note": "last_rank_ms: the measured per-call times of the work on the last of the ranks (its "
@@ -628,6 +646,8 @@ def run_ours(args):
                                                                workspace=wsv, stream=stream),
                                      vsteps, args.warmup, stream, dist)
     var_bytes = prefill_bytes(Tv, wv.H, Nv, init_state=True)
+    var_rows_fit = (wsv.numel() - (2 * wv.H * 128 * 128 * 4 + -(-(Nv + 1) * 4 // 1024) * 1024)) // (wv.H * 82432)
+    var_launches = prefill_launches(Tv // 64 + Nv, var_rows_fit, True)
     var_gbs = var_bytes / (ms_var_launch * 1e-3) / 1e9
     del qv, kv, vv, gvv, bv, s0v, cuv, ov, fsv, wsv
     torch.cuda.empty_cache()
@@ -733,7 +753,7 @@ def run_ours(args):
         "workload": f"{w.name}: kda_chunk_bwd of the prefill (bf16 q, k, v and dL/do; fp32 gradients of q, k, v, g, "
                     "beta, S0), dL/dS_final = 0",
         "value": w.T * world / (ms_bwd * 1e-3), "unit": "tokens/s", "ms_per_step": ms_bwd, "steps": bsteps,
-        "gpu_launches": 6 * bsteps, "algorithmic_bytes_per_launch": bwd_bytes,
+        "gpu_launches": 5 * bsteps, "algorithmic_bytes_per_launch": bwd_bytes,
         "algorithmic_flops_per_launch": bwd_flops, "products_tflops": bwd_tflops,
         "roofline": {"bound": "hbm", "achieved": bwd_gbs, "peak": hbm_peak, "unit": "GB/s",
                      "frac": bwd_gbs / hbm_peak, "traffic": bwd_traffic,
@@ -745,7 +765,8 @@ def run_ours(args):
         "workload": "frontend_32k raw q, k, v bf16 [32768, 12288] + g = max(-5, -softplus(z)), beta -> "
                     "ShortConv(4)+SiLU+L2norm -> chunk_kda (the long workload's path at 32K tokens)",
         "value": wf.T * world / (ms_fused * 1e-3), "unit": "tokens/s", "ms_per_step": ms_fused, "steps": lsteps,
-        "gpu_launches": lsteps * 3, "two_pass_value": wf.T * world / (ms_two * 1e-3), "two_pass_ms_per_step": ms_two,
+        "gpu_launches": lsteps * prefill_launches(-(-wf.T // 64), -(-wf.T // 64), False, fused=True),
+        "two_pass_value": wf.T * world / (ms_two * 1e-3), "two_pass_ms_per_step": ms_two,
         "note": "kda_chunk_fwd_frontend vs kda_shortconv_l2norm + kda_chunk_fwd; same output bits"}
     line["noalloc_prefill"] = {
         "workload": f"{w.name} through kda_chunk_fwd_noalloc: the library's static 64 MiB scratch, chunk ranges "
@@ -755,7 +776,7 @@ def run_ours(args):
         "workload": f"varlen_32: {Nv} packed sequences (1K..32K tokens, sum {Tv}), H={wv.H}, bf16 q,k,v, fp32 g, beta, "
                     "initial states N(0, 0.02); values drawn on the device with the workload's distributions",
         "value": Tv * world / (ms_var * 1e-3), "unit": "tokens/s", "ms_per_step": ms_var, "steps": vsteps,
-        "algorithmic_bytes_per_launch": var_bytes,
+        "gpu_launches": vsteps * var_launches, "algorithmic_bytes_per_launch": var_bytes,
         "roofline": {"bound": "hbm", "achieved": var_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": var_gbs / hbm_peak,
                      "traffic": measured_traffic("kda_chunk_fwd", FWD_SOURCES, "varlen_32"),
                      "peak_source": peak_src}}
@@ -763,6 +784,7 @@ def run_ours(args):
         "workload": f"long_256k: T={Tl}, raw q,k,v bf16 [{Tl}, {Cl}] -> ShortConv(4)+SiLU+L2norm -> chunk_kda with "
                     "g = max(-5, -softplus(z)) -> o * sigmoid(gate); kda_chunk_fwd_frontend (fused)",
         "value": Tl * world / (ms_long * 1e-3), "unit": "tokens/s", "ms_per_step": ms_long, "steps": lsteps5,
+        "gpu_launches": lsteps5 * prefill_launches(-(-Tl // 64), -(-Tl // 64), False, fused=True),
         "algorithmic_bytes_per_launch": long_bytes,
         "two_pass_value": Tl * world / (ms_long2 * 1e-3), "two_pass_ms_per_step": ms_long2,
         "roofline": {"bound": "hbm", "achieved": long_gbs, "peak": hbm_peak, "unit": "GB/s",

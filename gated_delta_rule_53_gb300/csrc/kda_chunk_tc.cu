@@ -140,6 +140,7 @@ __device__ __forceinline__ void cta_sync_tc() {
 }
 
 // Chunk offsets of the packed sequences: off[n] = sum over n' < n of ceil(L_n' / 64), off[N] = all.
+// Without cu_seqlens (one sequence) the kernels take off = NULL as {0, ceil(T_total / 64)} instead.
 __global__ void __launch_bounds__(1024) chunk_offsets_kernel(const int32_t* __restrict__ cu, int N, int64_t T_total,
                                                              int32_t* __restrict__ off) {
     __shared__ int32_t warp_tot[32];
@@ -253,7 +254,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int offN = off[N];
+    const int offN = off ? off[N] : (int)((T_total + kC - 1) / kC);
     constexpr uint32_t kStride = kBlobBytes;
 
     float* sBeta = reinterpret_cast<float*>(sm + P_BETA);
@@ -273,13 +274,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         const int m = m0 + item / H;
         if (m >= offN) return false;
         int lo = 0, hi = N;  // off[lo] <= m < off[hi]
-        while (hi - lo > 1) {
+        while (off && hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
             if (off[mid] <= m) lo = mid; else hi = mid;
         }
         int64_t bos, eos;
         seq_bounds(cu, lo, T_total, bos, eos);
-        c0 = bos + (int64_t)kC * (m - off[lo]);
+        c0 = bos + (int64_t)kC * (m - (off ? off[lo] : 0));
         L = (eos - c0) < kC ? (int)(eos - c0) : kC;
         return true;
     };
@@ -740,7 +741,7 @@ chunk_state_kernel(const __grid_constant__ CUtensorMap tm_v, const float* init_s
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool zero_u = (mode & kStateZeroU) != 0;  // U taken as zero (v = 0): the transition operator
     const int chain = blockIdx.x, n = chain / H, h = chain % H;
-    const int on = off[n], on1 = off[n + 1];
+    const int on = off ? off[n] : 0, on1 = off ? off[n + 1] : (int)((T_total + kC - 1) / kC);
     int lo = on > m0 ? on : m0, hi = on1 < m1 ? on1 : m1;
     const bool empty_seq = on == on1;
     if (empty_seq) {
@@ -1225,7 +1226,8 @@ cudaError_t launch_chunk_tc(const void* q, const void* k, const void* v, const f
     e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    chunk_offsets_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, T_total, off);
+    if (cu_seqlens) chunk_offsets_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, N, T_total, off);
+    else off = nullptr;  // one sequence: the kernels use {0, ceil(T_total / 64)}
     // A second state pass on the same operands (final_state2, state_mode2) needs them all at once.
     if (final_state2 && rows < rows_max) return cudaErrorInvalidValue;
     if (overlap && !final_state2 && rows >= 2 * kPipeMinRows && rows_max >= 2 * kPipeMinRows) {

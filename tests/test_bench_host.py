@@ -155,3 +155,18 @@ def test_clock_sampler_polls_nvml_and_falls_back(monkeypatch):
     cs = bench.ClockSampler("0")
     cs.start()
     assert cs.stop()["sm_mhz"] is None
+
+
+def test_prefill_launch_count_follows_the_range_rule():
+    """gpu_launches of the prefill lines: the chunk-offset kernel only for packed sequences, the front end of
+    v only for the fused call, and an operand kernel + a state pass per range (the library's rule: about eight
+    overlapped ranges of at least 128 rows from 256 rows on, else ranges of what the workspace holds)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.prefill_launches(128, 128, False) == 2                 # 8K tokens: one range
+    assert bench.prefill_launches(128, 6, False) == 2 * 22              # the 64 MiB scratch: 6 rows per range
+    assert bench.prefill_launches(512, 512, False, fused=True) == 9     # 32K fused: 4 ranges of 128 + v
+    assert bench.prefill_launches(4096, 4096, False, fused=True) == 17  # 256K fused: 8 ranges of 512 + v
+    assert bench.prefill_launches(8172, 3033, True) == 1 + 2 * 8        # packed, capped workspace: 8 of 1022
+    assert bench.prefill_launches(300, 200, True) == 1 + 2 * 2          # workspace below 256 rows: serial
+    assert bench.prefill_launches(0, 5, False) == 1                     # empty call: the state pass alone
