@@ -276,6 +276,36 @@ def test_chunk_frontend_fused_equals_two_passes(kda, orc, rows):
     assert orc.rel_l2(host(f2[n:n + 1, h:h + 1]), f_ref) <= BF16_S_REL
 
 
+def test_chunk_frontend_fused_packed_overlapped_equals_two_passes(kda):
+    """The fused prefill on packed sequences with enough chunk rows for the overlapped ranges (8 sequences,
+    20,523 tokens: 325 chunks in at most 328 chunk rows, three ranges whose boundaries cut through
+    sequences): the front end of v runs ahead of the state passes on their stream and the state passes
+    read v back from o, with carried conv state, initial states and the output gate; the same bits as the
+    two passes."""
+    H, d = 4, 128
+    C = H * d
+    lengths = [3000, 5, 4100, 64, 2999, 6000, 1, 4354]
+    T, N = sum(lengths), len(lengths)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    xs = [ks.fill(117, tid, ks.NORMAL, (T, C), "bf16") for tid in (1, 2, 3)]
+    cw = ks.fill(117, ks.TID_CONV_W, ks.NORMAL, (3 * C, 4), "bf16", 0.0, 0.25)
+    cs = ks.fill(117, ks.TID_CONV_STATE, ks.NORMAL, (N, 3, 3 * C), "bf16")
+    g = ks.fill(117, ks.TID_G, ks.NEG5_SIGMOID, (T, H, d), "f32")
+    b = ks.fill(117, ks.TID_BETA, ks.SIGMOID, (T, H), "f32")
+    s0 = ks.fill(117, ks.TID_STATE, ks.NORMAL, (N, H, d, d), "f32", 0.0, 0.02)
+    gate = ks.fill(117, ks.TID_GATE, ks.NORMAL, (T, C), "bf16")
+    xd = [dev(x) for x in xs]
+    cu_d, cs_d = dev(cu), dev(cs)
+    q, k, v = kda.kda_shortconv_l2norm(*xd, dev(cw), H, cu_d, cs_d)
+    o1, f1 = kda.kda_chunk_fwd(q, k, v, dev(g), dev(b), dev(s0), cu_d, out_gate=dev(gate))
+    o2, f2 = kda.kda_chunk_fwd_frontend(*xd, dev(cw), dev(g), dev(b), H, dev(s0), cu_d, conv_state_in=cs_d,
+                                        out_gate=dev(gate))
+    torch.cuda.synchronize()
+    assert T // 64 + N >= 256   # the overlapped ranges
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
+    assert kda.device_error() == 0
+
+
 # ------------------------------------------------------------------------------------------
 # kda_shortconv_l2norm
 # ------------------------------------------------------------------------------------------
