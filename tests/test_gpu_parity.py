@@ -115,6 +115,27 @@ def test_chunk_output_gate(kda, orc, dtype):
     assert orc.rel_l2(host(o), o_ref) <= tol and orc.rel_l2(host(fs), fs_ref) <= tol
 
 
+def test_chunk_output_gate_extremes(kda, orc):
+    """The bf16 path's gated epilogue, o / (1 + e^-gate) with the fast divide, at gate values whose sigmoid is
+    0 to fp32 (-100: the divisor passes 2^126 and the quotient is 0), tiny (-20), 1/2 (0), near 1 (20) and 1
+    (100), mixed with N(0, 4) values; packed sequences with whole and partial chunks (both ways the gate
+    values are loaded).  Against the oracle's o * sigmoid(gate), elementwise within the bf16 bounds."""
+    w, q, k, v, g, b, s0 = small_prefill(118, [200, 64, 37], 2, "bf16", init_std=0.02)
+    z = ks.bf16_to_f64(ks.fill(118, ks.TID_GATE, ks.NORMAL, (w.T, w.H * w.d), "bf16")) * 2.0
+    special = np.array([-100.0, -20.0, 0.0, 20.0, 100.0])
+    pick = (np.arange(z.size).reshape(z.shape) % 7)
+    z = np.where(pick < 5, special[np.minimum(pick, 4)], z)
+    gate = ks.f32_to_bf16(z.astype(np.float32))
+    o, fs = run_chunk(kda, w, q, k, v, g, b, s0, gate=gate)
+    o_ref, fs_ref = oracle_chunk(orc, w, q, k, v, g, b, s0, gate=gate)
+    assert orc.rel_l2(host(o), o_ref) <= BF16_O_REL and orc.max_abs(host(o), o_ref) <= BF16_O_ABS
+    assert orc.rel_l2(host(fs), fs_ref) <= BF16_S_REL
+    # where sigma(gate) is 0 to fp32 the output is exactly zero
+    o_h = host(o).reshape(w.T, -1)
+    assert np.all(o_h[z.reshape(w.T, -1) == -100.0] == 0.0)
+    assert kda.device_error() == 0
+
+
 def test_chunk_final_state_may_alias_initial(kda, orc):
     w, q, k, v, g, b, s0 = small_prefill(103, [70, 5], 2, "f32", init_std=0.02)
     s = dev(s0)
