@@ -165,9 +165,9 @@ KDA_API kda_status kda_chunk_fwd(const void* q, const void* k, const void* v, co
 
 /*
  * The prefill with its front end fused in: the result of kda_shortconv_l2norm (bf16 outputs)
- * followed by kda_chunk_fwd (bf16), without writing and re-reading q, k, v (the front end runs
- * inside the chunk pass, on the same arithmetic, so the outputs are the same bits: q and k in the
- * kernel that builds the chunk operands, v by the stand-alone front end into o).  This is the
+ * followed by kda_chunk_fwd (bf16), without writing and re-reading q and k (the front end runs on
+ * the same arithmetic, so the outputs are the same bits: q and k inside the kernel that builds the
+ * chunk operands, v by the stand-alone front end into o, from where the state pass reads it).  This is the
  * pages' normalisation "in the kernel" taken one step further ("深入 Kimi-K3: Hugging Face 仓库
  * 分析", paragraph on KDA).
  *
