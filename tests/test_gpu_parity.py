@@ -105,6 +105,25 @@ def test_chunk_ragged_varlen_with_state_and_scale(kda, orc, dtype):
     assert torch.equal(fs[5], dev(s0)[5])
 
 
+def test_chunk_many_short_sequences(kda, orc):
+    """1,500 packed sequences of 0 to 70 tokens (bf16, initial states): the chunk offsets' scan runs over
+    more than 1,024 sequences (its carry across passes), the state pass runs 3,000 chains in waves, and the
+    2,500 or so chunk rows go through the overlapped ranges.  Against the oracle's token loop, and the
+    empty sequences keep their initial states exactly."""
+    rng = np.random.default_rng(119)
+    lengths = [int(x) for x in rng.integers(0, 71, size=1500)]
+    lengths[0], lengths[1], lengths[2] = 0, 64, 65
+    w, q, k, v, g, b, s0 = small_prefill(119, lengths, 2, "bf16", init_std=0.02)
+    assert w.T // 64 + w.N >= 256
+    o, fs = run_chunk(kda, w, q, k, v, g, b, s0)
+    o_ref, fs_ref = oracle_chunk(orc, w, q, k, v, g, b, s0)
+    assert orc.rel_l2(host(o), o_ref) <= BF16_O_REL and orc.max_abs(host(o), o_ref) <= BF16_O_ABS
+    assert orc.rel_l2(host(fs), fs_ref) <= BF16_S_REL
+    empty = [n for n, L in enumerate(lengths) if L == 0]
+    assert len(empty) > 5 and all(torch.equal(fs[n], dev(s0)[n]) for n in empty)
+    assert kda.device_error() == 0
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_chunk_output_gate(kda, orc, dtype):
     w, q, k, v, g, b, s0 = small_prefill(102, [200], 2, dtype, g_kind=ks.NEG_SOFTPLUS5)
